@@ -1,0 +1,216 @@
+// api.cu -- the extern "C" boundary of libcsa2.so: argument checks, workspace
+// layout and kernel launches.  Every call validates on the host and returns a
+// status without launching anything when an argument is wrong.
+#include <cstdint>
+
+#include "kernels.cuh"
+
+using namespace csa2;
+
+namespace {
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+csa2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
+
+csa2_status check_dims(const csa2_dims* d, int32_t batch) {
+  if (!d || batch < 0) return CSA2_ERR_INVALID_ARG;
+  if (d->idx_k_dtype != CSA2_IDXK_E4M3 && d->idx_k_dtype != CSA2_IDXK_F32) return CSA2_ERR_INVALID_ARG;
+  if (d->idx_heads < 1 || d->idx_heads > kMaxIdxHeads) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (d->idx_k_dtype == CSA2_IDXK_E4M3 && d->idx_dim != 128) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (d->idx_k_dtype == CSA2_IDXK_F32 && d->idx_dim != 64) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (d->pool_blocks < 1 || d->pool_blocks > kMaxPool) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (d->topk < 1 || d->topk > kMaxTopk) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (d->heads < 1 || d->heads > kMaxHeads) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (d->swa < 0 || d->swa > kMaxSwa) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (d->max_ctx < 1 || d->max_ctx > kMaxCtx) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  return CSA2_OK;
+}
+
+csa2_status check_paging(const csa2_dims* d, const int32_t* page_table) {
+  if (!page_table) return CSA2_OK;
+  if (d->max_pages < 1 || d->num_pages < 1) return CSA2_ERR_INVALID_ARG;
+  if (int64_t(d->max_pages) * kPage > kMaxCtx) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(page_table, 4)) return CSA2_ERR_INVALID_ARG;
+  return CSA2_OK;
+}
+
+csa2_status check_ws(const csa2_dims* d, int32_t batch, const void* ws, size_t ws_bytes, WsLayout* L) {
+  *L = make_layout(*d, batch);
+  if (!ws || !aligned(ws, 256)) return CSA2_ERR_INVALID_ARG;
+  if (ws_bytes < size_t(L->total)) return CSA2_ERR_WORKSPACE_TOO_SMALL;
+  return CSA2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t csa2_version(void) { return 100; }
+
+const char* csa2_status_string(csa2_status st) {
+  switch (st) {
+    case CSA2_OK: return "CSA2_OK";
+    case CSA2_ERR_INVALID_ARG: return "CSA2_ERR_INVALID_ARG";
+    case CSA2_ERR_UNSUPPORTED_SHAPE: return "CSA2_ERR_UNSUPPORTED_SHAPE";
+    case CSA2_ERR_WORKSPACE_TOO_SMALL: return "CSA2_ERR_WORKSPACE_TOO_SMALL";
+    case CSA2_ERR_CUDA: return "CSA2_ERR_CUDA";
+    case CSA2_ERR_DEVICE_ASSERT: return "CSA2_ERR_DEVICE_ASSERT";
+    case CSA2_ERR_TIMEOUT: return "CSA2_ERR_TIMEOUT";
+  }
+  return "CSA2_ERR_UNKNOWN";
+}
+
+csa2_status csa2_workspace_size(const csa2_dims* d, int32_t batch, size_t* bytes) {
+  if (!bytes) return CSA2_ERR_INVALID_ARG;
+  csa2_status st = check_dims(d, batch);
+  if (st != CSA2_OK) return st;
+  *bytes = size_t(make_layout(*d, batch).total);
+  return CSA2_OK;
+}
+
+csa2_status fp4_kv_quantize(const uint16_t* x, int64_t n, uint8_t* codes, uint8_t* scales,
+                            void* stream) {
+  if (n < 0) return CSA2_ERR_INVALID_ARG;
+  if (n == 0) return CSA2_OK;
+  if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 4)) return CSA2_ERR_INVALID_ARG;
+  return from_cuda(launch_quantize(x, n, nullptr, codes, scales, as_stream(stream)));
+}
+
+csa2_status fp4_kv_quantize_scatter(const uint16_t* x, int64_t n, const int64_t* dst_rows,
+                                    uint8_t* codes, uint8_t* scales, void* stream) {
+  if (n < 0) return CSA2_ERR_INVALID_ARG;
+  if (n == 0) return CSA2_OK;
+  if (!x || !dst_rows || !codes || !scales || !aligned(x, 16) || !aligned(codes, 4) ||
+      !aligned(dst_rows, 8))
+    return CSA2_ERR_INVALID_ARG;
+  return from_cuda(launch_quantize(x, n, dst_rows, codes, scales, as_stream(stream)));
+}
+
+csa2_status fp4_kv_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t n, uint16_t* y,
+                              void* stream) {
+  if (n < 0) return CSA2_ERR_INVALID_ARG;
+  if (n == 0) return CSA2_OK;
+  if (!codes || !scales || !y || !aligned(codes, 8) || !aligned(y, 16)) return CSA2_ERR_INVALID_ARG;
+  return from_cuda(launch_dequantize(codes, scales, n, y, as_stream(stream)));
+}
+
+csa2_status indexer_full_topk(const csa2_dims* d, int32_t batch, const void* idx_k,
+                              const int32_t* page_table, const int32_t* ctx_len, const void* idx_q,
+                              const float* w, int32_t* pool_blocks_out, int32_t* pool_len_out,
+                              int32_t* topk_out, void* ws, size_t ws_bytes, void* stream) {
+  csa2_status st = check_dims(d, batch);
+  if (st != CSA2_OK) return st;
+  if ((st = check_paging(d, page_table)) != CSA2_OK) return st;
+  WsLayout L;
+  if ((st = check_ws(d, batch, ws, ws_bytes, &L)) != CSA2_OK) return st;
+  if (batch == 0) return CSA2_OK;
+  if (!idx_k || !ctx_len || !idx_q || !w || !pool_blocks_out || !pool_len_out || !topk_out)
+    return CSA2_ERR_INVALID_ARG;
+  if (!aligned(idx_k, 16) || !aligned(idx_q, 4)) return CSA2_ERR_INVALID_ARG;
+  IdxArgs a = {};
+  a.d = *d;
+  a.batch = batch;
+  a.idx_k = idx_k;
+  a.page_table = page_table;
+  a.ctx_len = ctx_len;
+  a.idx_q = idx_q;
+  a.w = w;
+  a.pool_out = pool_blocks_out;
+  a.pool_len_out = pool_len_out;
+  a.topk_out = topk_out;
+  a.ws = static_cast<uint8_t*>(ws);
+  a.L = L;
+  return from_cuda(launch_full(a, as_stream(stream)));
+}
+
+csa2_status indexer_reindex_topk(const csa2_dims* d, int32_t batch, const void* idx_k,
+                                 const int32_t* page_table, const int32_t* ctx_len,
+                                 const void* idx_q, const float* w, const int32_t* pool_blocks,
+                                 const int32_t* pool_len, int32_t* topk_out, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  csa2_status st = check_dims(d, batch);
+  if (st != CSA2_OK) return st;
+  if ((st = check_paging(d, page_table)) != CSA2_OK) return st;
+  WsLayout L;
+  if ((st = check_ws(d, batch, ws, ws_bytes, &L)) != CSA2_OK) return st;
+  if (batch == 0) return CSA2_OK;
+  if (!idx_k || !ctx_len || !idx_q || !w || !pool_blocks || !pool_len || !topk_out)
+    return CSA2_ERR_INVALID_ARG;
+  if (!aligned(idx_k, 16) || !aligned(idx_q, 4)) return CSA2_ERR_INVALID_ARG;
+  IdxArgs a = {};
+  a.d = *d;
+  a.batch = batch;
+  a.idx_k = idx_k;
+  a.page_table = page_table;
+  a.ctx_len = ctx_len;
+  a.idx_q = idx_q;
+  a.w = w;
+  a.pool_in = pool_blocks;
+  a.pool_len_in = pool_len;
+  a.topk_out = topk_out;
+  a.ws = static_cast<uint8_t*>(ws);
+  a.L = L;
+  return from_cuda(launch_reindex(a, as_stream(stream)));
+}
+
+csa2_status csa2_sparse_attn_decode(const csa2_dims* d, int32_t batch, int32_t mode,
+                                    const uint16_t* q, const uint8_t* kv_codes,
+                                    const uint8_t* kv_scales, const uint16_t* kv_rope,
+                                    const int32_t* page_table, const int32_t* ctx_len,
+                                    const int32_t* topk, const uint16_t* swa_kv,
+                                    const int32_t* swa_len, float scale, float* out, float* lse,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  csa2_status st = check_dims(d, batch);
+  if (st != CSA2_OK) return st;
+  if (mode < CSA2_MODE_FULL || mode > CSA2_MODE_REUSE) return CSA2_ERR_INVALID_ARG;
+  if ((st = check_paging(d, page_table)) != CSA2_OK) return st;
+  WsLayout L;
+  if ((st = check_ws(d, batch, ws, ws_bytes, &L)) != CSA2_OK) return st;
+  if (batch == 0) return CSA2_OK;
+  if (!q || !kv_codes || !kv_scales || !kv_rope || !ctx_len || !topk || !swa_len || !out || !lse)
+    return CSA2_ERR_INVALID_ARG;
+  if (d->swa > 0 && !swa_kv) return CSA2_ERR_INVALID_ARG;
+  if (!aligned(kv_codes, 8) || !aligned(kv_rope, 16) || !aligned(q, 4) || !aligned(out, 16) ||
+      (swa_kv && !aligned(swa_kv, 16)))
+    return CSA2_ERR_INVALID_ARG;
+  if (!(scale == scale)) return CSA2_ERR_INVALID_ARG;
+  AttnArgs a = {};
+  a.d = *d;
+  a.batch = batch;
+  a.q = q;
+  a.codes = kv_codes;
+  a.scales = kv_scales;
+  a.rope = kv_rope;
+  a.page_table = page_table;
+  a.ctx_len = ctx_len;
+  a.topk = topk;
+  a.swa = swa_kv;
+  a.swa_len = swa_len;
+  a.scale = scale;
+  a.out = out;
+  a.lse = lse;
+  a.ws = static_cast<uint8_t*>(ws);
+  a.L = L;
+  return from_cuda(launch_attention(a, as_stream(stream)));
+}
+
+csa2_status csa2_get_device_status(const void* ws, void* stream, int32_t* word) {
+  if (!ws || !word) return CSA2_ERR_INVALID_ARG;
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, as_stream(stream));
+  if (e == cudaSuccess) e = cudaStreamSynchronize(as_stream(stream));
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  *word = v;
+  if (v & CSA2_DEV_TIMEOUT) return CSA2_ERR_TIMEOUT;
+  return v ? CSA2_ERR_DEVICE_ASSERT : CSA2_OK;
+}
+
+csa2_status csa2_clear_device_status(void* ws, void* stream) {
+  if (!ws) return CSA2_ERR_INVALID_ARG;
+  return from_cuda(cudaMemsetAsync(ws, 0, 256, as_stream(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,160 @@
+// codec.cu -- FP4 main-KV codec: bf16 latent <-> packed E2M1 + E4M3 scales.
+//
+// Format (foosynaptic atlas "DeepSeek-V4.1-Flash 梗概", section 3.2, "FP4 main
+// KV": E2M1 with one E4M3 scale per 16 channels; newsaint.id "DeepSeek-V4.1-
+// Flash 2026: ...", section 8, FP4Quantizer: levels {0,.5,1,1.5,2,3,4,6},
+// scale = amax/6 limited to 448, no second-level scale).
+//
+// Rounding (the reading this library implements):
+//   s_code = E4M3 round-to-nearest-even, saturating, of amax/6;
+//   magnitude code = nearest E2M1 level to |x|/s, ties to the even code,
+//   saturating at 6; the sign bit of x is kept; s == 0 gives magnitude 0.
+// Both roundings use the hardware RNE conversions.  amax/6 is formed with a
+// correctly rounded fp32 division: amax has <= 8 significant bits, so amax/6
+// is exact or non-terminating in binary and can never sit on an E4M3
+// midpoint -- rounding it first to fp32 cannot change the E4M3 result.
+// |x|/s is formed as r0 = |x|*rcp(s) plus one FMA residual correction: away
+// from an E2M1 midpoint |x|/s is at least 2^-8 (relative) from it, far more
+// than r0's error; on an exact midpoint the correction returns it exactly,
+// so the conversion sees the exact tie and rounds it to the even code.
+//
+// Layout: one warp per 512-channel row.  Round r in {0,1} covers channels
+// [256r, 256r+256): lane l loads 8 bf16 (16 B, coalesced), lanes 2g and 2g+1
+// share group g, and each lane stores 4 packed bytes (coalesced 128 B per
+// warp) and, for even lanes, one scale byte.
+#include "common.cuh"
+
+namespace csa2 {
+
+__device__ inline uint32_t e2m1x2_rn(float hi, float lo) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r & 0xFF;
+}
+
+__device__ inline uint32_t f32_to_e4m3_rn(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+  return uint32_t(r) & 0xFF;
+}
+
+// |x| / s rounded so that RNE onto the E2M1 grid sees the exact decision.
+__device__ inline float scaled_mag(float ax, float s, float rcp) {
+  float r0 = ax * rcp;
+  float e = __fmaf_rn(-r0, s, ax);
+  return __fmaf_rn(rcp, e, r0);
+}
+
+__global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__ x, int64_t n,
+                                                       const int64_t* __restrict__ dst_rows,
+                                                       uint32_t* __restrict__ codes,
+                                                       uint8_t* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t row = warp; row < n; row += nwarps) {
+    int64_t dst = dst_rows ? dst_rows[row] : row;
+    if (dst < 0) continue;
+    uint4 v[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) v[r] = __ldcs(x + row * 64 + r * 32 + lane);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+      float ax[8];
+      uint32_t sgn[8];
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t lo = w[i] << 16, hi = w[i] & 0xFFFF0000u;
+        sgn[2 * i] = lo >> 31;
+        sgn[2 * i + 1] = hi >> 31;
+        ax[2 * i] = __uint_as_float(lo & 0x7FFFFFFFu);
+        ax[2 * i + 1] = __uint_as_float(hi & 0x7FFFFFFFu);
+        amax = fmaxf(amax, fmaxf(ax[2 * i], ax[2 * i + 1]));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      uint32_t sc = f32_to_e4m3_rn(__fdiv_rn(amax, 6.0f));
+      float s = e4m3_to_f32(sc);
+      float rcp = s > 0.0f ? __frcp_rn(s) : 0.0f;
+      uint32_t packed = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float m0 = scaled_mag(ax[2 * i], s, rcp);
+        float m1 = scaled_mag(ax[2 * i + 1], s, rcp);
+        uint32_t byte = e2m1x2_rn(m1, m0) | (sgn[2 * i] << 3) | (sgn[2 * i + 1] << 7);
+        packed |= byte << (8 * i);
+      }
+      codes[dst * 64 + r * 32 + lane] = packed;
+      if ((lane & 1) == 0) scales[dst * 32 + r * 16 + (lane >> 1)] = uint8_t(sc);
+    }
+  }
+}
+
+// Two E2M1 nibbles (low nibble = first) -> f16x2 (low half = first), exact.
+__device__ inline uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t h2;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(byte));
+  return h2;
+}
+
+__device__ inline uint32_t f16x2_to_bf16x2(uint32_t h2) {
+  float lo = __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF)));
+  float hi = __half2float(__ushort_as_half(uint16_t(h2 >> 16)));
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__global__ void __launch_bounds__(256) dequantize_kernel(const uint2* __restrict__ codes,
+                                                         const uint8_t* __restrict__ scales,
+                                                         int64_t n, uint4* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t row = warp; row < n; row += nwarps) {
+    uint2 c = __ldcs(codes + row * 32 + lane);          // 16 nibbles = group `lane`
+    uint32_t sc = scales[row * 32 + lane];
+    uint32_t s2 = e4m3x2_to_f16x2(uint16_t(sc | (sc << 8)));
+    __half2 sh = *reinterpret_cast<__half2*>(&s2);
+    uint32_t cw[2] = {c.x, c.y};
+    uint32_t out[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t byte = (cw[i >> 2] >> (8 * (i & 3))) & 0xFF;
+      uint32_t h2 = e2m1x2_to_f16x2(byte);
+      __half2 v = __hmul2(*reinterpret_cast<__half2*>(&h2), sh);   // exact
+      out[i] = f16x2_to_bf16x2(*reinterpret_cast<uint32_t*>(&v));
+    }
+    __stcs(y + row * 64 + lane * 2, make_uint4(out[0], out[1], out[2], out[3]));
+    __stcs(y + row * 64 + lane * 2 + 1, make_uint4(out[4], out[5], out[6], out[7]));
+  }
+}
+
+static int codec_grid(int64_t n) {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t want = (n + 7) / 8;                    // 8 warps per block, 1 row per warp
+  int64_t cap = int64_t(sms) * 8;                // 8 blocks of 256 per SM, grid-stride
+  return int(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+cudaError_t launch_quantize(const uint16_t* x, int64_t n, const int64_t* dst_rows, uint8_t* codes,
+                            uint8_t* scales, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  quantize_kernel<<<codec_grid(n), 256, 0, st>>>(reinterpret_cast<const uint4*>(x), n, dst_rows,
+                                                 reinterpret_cast<uint32_t*>(codes), scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t n, uint16_t* y,
+                              cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  dequantize_kernel<<<codec_grid(n), 256, 0, st>>>(reinterpret_cast<const uint2*>(codes), scales,
+                                                   n, reinterpret_cast<uint4*>(y));
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -1,0 +1,55 @@
+// kernels.cuh -- argument blocks and host launchers of the library's kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace csa2 {
+
+struct IdxArgs {
+  csa2_dims d;
+  int batch;
+  const void* idx_k;
+  const int32_t* page_table;
+  const int32_t* ctx_len;
+  const void* idx_q;
+  const float* w;
+  const int32_t* pool_in;      // Reindex: pool blocks [B][P]
+  const int32_t* pool_len_in;  // Reindex: [B]
+  int32_t* pool_out;           // Full: [B][P]
+  int32_t* pool_len_out;       // Full: [B]
+  int32_t* topk_out;           // [B][K]
+  uint8_t* ws;
+  WsLayout L;
+  float err_coef;              // delta = err_coef * sum_h|w_h|*||q_h||_1 * max|k|
+};
+
+struct AttnArgs {
+  csa2_dims d;
+  int batch;
+  const uint16_t* q;
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const uint16_t* rope;
+  const int32_t* page_table;
+  const int32_t* ctx_len;
+  const int32_t* topk;
+  const uint16_t* swa;
+  const int32_t* swa_len;
+  float scale;
+  float* out;
+  float* lse;
+  uint8_t* ws;
+  WsLayout L;
+};
+
+cudaError_t launch_quantize(const uint16_t* x, int64_t n, const int64_t* dst_rows, uint8_t* codes,
+                            uint8_t* scales, cudaStream_t st);
+cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t n, uint16_t* y,
+                              cudaStream_t st);
+cudaError_t launch_full(IdxArgs a, cudaStream_t st);
+cudaError_t launch_reindex(IdxArgs a, cudaStream_t st);
+cudaError_t launch_attention(AttnArgs a, cudaStream_t st);
+size_t select_smem_bytes();
+size_t attn_smem_bytes(int heads);
+
+}  // namespace csa2

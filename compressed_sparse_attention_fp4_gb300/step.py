@@ -1,0 +1,122 @@
+"""Decode-step runner: one query token per sequence through a CSA2 layer
+schedule of Full / Reindex / Reuse layers, every step in libcsa2 kernels.
+
+Layer modes (foosynaptic atlas "DeepSeek-V4.1-Flash 梗概", section 3.2, mode
+table): Full runs the indexer over the whole context (new pool and Top-K),
+Reindex re-scores the latest pool with its own indexer query (new Top-K),
+Reuse keeps the latest Top-K; every layer then runs core attention with its
+own query and SWA window.  Main KV and indexer K are one cache shared by all
+layers.
+
+The runner owns no method arithmetic: it orders the library calls, holds the
+buffers between them and can capture the whole step in a CUDA graph.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+from . import csa2
+
+
+@dataclass
+class StepBuffers:
+    """Device tensors of one decode step (all on the same CUDA device)."""
+    dims: csa2.Dims
+    batch: int
+    schedule: list
+    # cache (shared by all layers)
+    kv_codes: torch.Tensor          # uint8 [rows, 256]
+    kv_scales: torch.Tensor         # uint8 [rows, 32]
+    kv_rope: torch.Tensor           # bf16  [rows, 64]
+    idx_k: torch.Tensor             # uint8 [rows, 128] (E4M3) or fp32 [rows, 64]
+    page_table: torch.Tensor | None
+    ctx_len: torch.Tensor           # int32 [B]
+    # per-layer inputs
+    q: torch.Tensor                 # bf16 [L, B, H, 576]
+    swa: torch.Tensor               # bf16 [L, B, W, 576]
+    swa_len: torch.Tensor           # int32 [L, B]
+    idx_q: torch.Tensor             # bf16 / fp32 [L, B, Hi, Di]
+    idx_w: torch.Tensor             # fp32 [L, B, Hi]
+    scale: float
+    # optional decode-time append of the newest token at every Full layer
+    new_latent: torch.Tensor | None = None   # bf16 [B, 512]
+    new_rows: torch.Tensor | None = None     # int64 [B] cache rows of position N-1
+    # outputs
+    out: torch.Tensor = None        # fp32 [L, B, H, 512]
+    lse: torch.Tensor = None        # fp32 [L, B, H]
+    topk: torch.Tensor = None       # int32 [L, B, K]  (indices each layer used)
+    pool: torch.Tensor = None       # int32 [B, P]
+    pool_len: torch.Tensor = None   # int32 [B]
+    ws: torch.Tensor = None
+    launches: int = 0
+
+    def allocate_outputs(self):
+        L, B, d = len(self.schedule), self.batch, self.dims
+        dev = self.q.device
+        self.out = torch.empty((L, B, d.heads, csa2.LATENT), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((L, B, d.heads), dtype=torch.float32, device=dev)
+        self.topk = torch.full((L, B, d.topk), -1, dtype=torch.int32, device=dev)
+        self.pool = torch.full((B, d.pool_blocks), -1, dtype=torch.int32, device=dev)
+        self.pool_len = torch.zeros((B,), dtype=torch.int32, device=dev)
+        self.ws = csa2.alloc_workspace(d, B, device=dev)
+        return self
+
+
+def run_step(sb: StepBuffers, stream=None) -> int:
+    """Enqueue one decode step; returns the number of kernel launches."""
+    d, B = sb.dims, sb.batch
+    cur = None
+    launches = 0
+    for l, mode in enumerate(sb.schedule):
+        if mode == "F":
+            if sb.new_latent is not None:
+                csa2.fp4_kv_quantize_scatter(sb.new_latent, sb.new_rows, sb.kv_codes,
+                                             sb.kv_scales, stream=stream)
+                launches += 1
+            csa2.indexer_full_topk(d, B, sb.idx_k, sb.page_table, sb.ctx_len, sb.idx_q[l],
+                                   sb.idx_w[l], sb.pool, sb.pool_len, sb.topk[l], sb.ws,
+                                   stream=stream)
+            launches += 2
+            cur = l
+            m = csa2.MODE_FULL
+        elif mode == "Ri":
+            csa2.indexer_reindex_topk(d, B, sb.idx_k, sb.page_table, sb.ctx_len, sb.idx_q[l],
+                                      sb.idx_w[l], sb.pool, sb.pool_len, sb.topk[l], sb.ws,
+                                      stream=stream)
+            launches += 2
+            cur = l
+            m = csa2.MODE_REINDEX
+        elif mode == "Ru":
+            if cur is None:
+                raise ValueError("a Reuse layer needs an earlier Full / Reindex layer")
+            m = csa2.MODE_REUSE
+        else:
+            raise ValueError(f"unknown layer mode {mode!r}")
+        csa2.csa2_sparse_attn_decode(d, B, m, sb.q[l], sb.kv_codes, sb.kv_scales, sb.kv_rope,
+                                     sb.page_table, sb.ctx_len, sb.topk[cur], sb.swa[l],
+                                     sb.swa_len[l], sb.scale, sb.out[l], sb.lse[l], sb.ws,
+                                     stream=stream)
+        launches += 2
+    sb.launches = launches
+    return launches
+
+
+class GraphedStep:
+    """One decode step captured once in a CUDA graph and replayed."""
+
+    def __init__(self, sb: StepBuffers, warmup: int = 1):
+        self.sb = sb
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                run_step(sb)
+        torch.cuda.current_stream().wait_stream(s)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.launches = run_step(sb)
+
+    def replay(self):
+        self.graph.replay()

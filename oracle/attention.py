@@ -54,9 +54,10 @@ def sparse_attn_decode(q, latent, rope, topk, swa, swa_len, scale):
     q = np.asarray(q, dtype=np.float64)
     topk = np.asarray(topk, dtype=np.int64)
     idx = topk[topk >= 0]
-    k_main = np.concatenate([np.asarray(latent, dtype=np.float64)[idx],
-                             np.asarray(rope, dtype=np.float64)[idx]], axis=1)
-    v_main = np.asarray(latent, dtype=np.float64)[idx]
+    lat_sel = np.asarray(latent[idx], dtype=np.float64).reshape(idx.shape[0], LATENT)
+    rope_sel = np.asarray(rope[idx], dtype=np.float64).reshape(idx.shape[0], ROPE)
+    k_main = np.concatenate([lat_sel, rope_sel], axis=1)
+    v_main = lat_sel
     swa = np.asarray(swa, dtype=np.float64)[:swa_len]
     keys = np.concatenate([k_main, swa], axis=0)            # [E, 576]
     vals = np.concatenate([v_main, swa[:, :LATENT]], axis=0)  # [E, 512]

@@ -1,0 +1,102 @@
+"""The C-ABI library loads on a CPU host, exports every function that
+include/csa2.h declares, and rejects bad arguments on the host (before any
+CUDA call, so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def mod():
+    from compressed_sparse_attention_fp4_gb300 import build
+    build.build()
+    from compressed_sparse_attention_fp4_gb300 import csa2
+    return csa2
+
+
+def test_header_functions_exported(mod):
+    names = declared_functions()
+    assert len(names) >= 11
+    lib = ctypes.CDLL(mod.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(mod.SIGNATURES), set(names) - set(mod.SIGNATURES)
+
+
+def test_version_and_strings(mod):
+    assert mod.version() == 100
+    for code, name in mod.STATUS.items():
+        assert mod._lib.csa2_status_string(code).decode() == name
+
+
+def test_workspace_size_and_shape_checks(mod):
+    d = mod.Dims(max_ctx=131072)
+    assert mod.workspace_size(d, 8) > 8 * 131072 * 4
+    bad = [dict(idx_heads=17), dict(idx_heads=0), dict(idx_dim=64), dict(pool_blocks=4096),
+           dict(topk=1024), dict(heads=128), dict(swa=256), dict(max_ctx=(1 << 20) + 1)]
+    for kw in bad:
+        with pytest.raises(mod.Csa2Error) as e:
+            mod.workspace_size(mod.Dims(**{**d.__dict__, **kw}), 1)
+        assert e.value.code == 2, kw
+    with pytest.raises(mod.Csa2Error) as e:
+        mod.workspace_size(mod.Dims(idx_k_dtype=7), 1)
+    assert e.value.code == 1
+    with pytest.raises(mod.Csa2Error):
+        mod.workspace_size(d, -1)
+
+
+def test_host_argument_errors(mod):
+    lib = mod._lib
+    d = mod.Dims(max_ctx=1024, pool_blocks=64, topk=128)
+    dc = ctypes.byref(d.c())
+    P = ctypes.c_void_p
+    fake = P(0x10000)           # never dereferenced: validation fails first
+    assert lib.fp4_kv_quantize(None, 5, fake, fake, None) == 1
+    assert lib.fp4_kv_quantize(fake, -1, fake, fake, None) == 1
+    assert lib.fp4_kv_quantize(P(0x10001), 5, fake, fake, None) == 1      # misaligned
+    assert lib.fp4_kv_quantize(None, 0, None, None, None) == 0            # empty: no-op
+    assert lib.fp4_kv_dequantize(fake, None, 3, fake, None) == 1
+    assert lib.fp4_kv_quantize_scatter(fake, 2, None, fake, fake, None) == 1
+    ws = mod.workspace_size(d, 2)
+    # workspace too small / misaligned / missing
+    args = [fake, None] + [fake] * 6          # contiguous cache: no page table
+    assert lib.indexer_full_topk(dc, 2, *args, fake, ws - 1, None) == 3
+    assert lib.indexer_full_topk(dc, 2, *args, P(0x10010), ws, None) == 1
+    assert lib.indexer_full_topk(dc, 2, *args, None, ws, None) == 1
+    # null input with a big-enough workspace
+    assert lib.indexer_full_topk(dc, 2, None, *args[1:], fake, ws, None) == 1
+    assert lib.indexer_reindex_topk(dc, 2, fake, None, *([fake] * 4), None, fake, fake, ws, None) == 1
+    # attention: bad mode, null swa with a window, NaN scale
+    a = [fake] * 4 + [None] + [fake] * 4      # no page table
+    assert lib.csa2_sparse_attn_decode(dc, 2, 3, *a, 0.1, fake, fake, fake, ws, None) == 1
+    assert lib.csa2_sparse_attn_decode(dc, 2, 0, *a[:7], None, fake, 0.1, fake, fake, fake, ws, None) == 1
+    assert lib.csa2_sparse_attn_decode(dc, 2, 0, *a, float("nan"), fake, fake, fake, ws, None) == 1
+    # paged layout needs max_pages / num_pages
+    dp = mod.Dims(max_ctx=1024, pool_blocks=64, topk=128, max_pages=0, num_pages=0)
+    assert lib.indexer_full_topk(ctypes.byref(dp.c()), 1, fake, fake, *([fake] * 6), fake,
+                                 mod.workspace_size(dp, 1), None) == 1
+    assert lib.csa2_get_device_status(None, None, None) == 1
+    assert lib.csa2_clear_device_status(None, None) == 1
+
+
+def test_workspace_layout_mirror(mod):
+    """The test-side mirror of the workspace layout agrees with the library's size."""
+    from tests.helpers import ws_offsets
+    d = mod.Dims(max_ctx=4096, pool_blocks=64, topk=128)
+    off = ws_offsets(d, 3)
+    assert off["blk_delta"] > off["blk_scores"] > off["pos_scores"] >= 256
+    assert mod.workspace_size(d, 3) > off["ri_delta"]

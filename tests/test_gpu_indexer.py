@@ -1,0 +1,122 @@
+"""GPU parity of the hierarchical indexer against the oracle (bit-exact ids).
+
+Full mode (pool + Top-K) and Reindex mode through the C ABI, on ragged
+contexts (partial last block, contexts shorter than the pool, single
+positions), paged and contiguous caches, E4M3 and fp32 indexer keys, heavy
+exact ties, and the error bound the certified selection relies on.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import indexer as oix
+from tests.gpu_problem import make_problem, oracle_keys, run_full, run_reindex
+from tests.helpers import ws_offsets
+
+pytestmark = pytest.mark.gpu
+
+
+def check_full(p, pool, plen, topk):
+    pool, plen, topk = pool.cpu().numpy(), plen.cpu().numpy(), topk.cpu().numpy()
+    for b in range(p.B):
+        n = p.ctx_lens[b]
+        r = oix.full_topk(p.idx_q_f64[b], p.w_raw[b].astype(np.float64), oracle_keys(p, b),
+                          p.P, p.K)
+        P_sel = len(r["pool"])
+        assert plen[b] == P_sel, (b, plen[b], P_sel)
+        np.testing.assert_array_equal(pool[b, :P_sel], r["pool"], err_msg=f"pool b={b} n={n}")
+        assert np.all(pool[b, P_sel:] == -1)
+        np.testing.assert_array_equal(topk[b], r["topk"], err_msg=f"topk b={b} n={n}")
+        print(f"b={b} n={n} margin_pool={r['margin_pool']:.3g} margin_topk={r['margin_topk']:.3g}")
+
+
+def check_reindex(p, pool, topk, q64, w):
+    pool, topk = pool.cpu().numpy(), topk.cpu().numpy()
+    for b in range(p.B):
+        pl = pool[b][pool[b] >= 0]
+        r = oix.reindex_topk(q64[b], w[b].astype(np.float64), oracle_keys(p, b), pl, p.K)
+        np.testing.assert_array_equal(topk[b], r["topk"], err_msg=f"reindex b={b}")
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_full_fp8_ragged(paged):
+    p = make_problem([1, 7, 8, 9, 1000, 16383, 70001], paged=paged, seed=1, with_kv=False)
+    check_full(p, *run_full(p))
+
+
+def test_full_small_pool_deep_selection():
+    p = make_problem([50000, 33333], P=64, K=128, seed=2, with_kv=False)
+    check_full(p, *run_full(p))
+
+
+def test_full_fp32_keys():
+    p = make_problem([4096, 3001, 64], Hi=4, Di=64, dtype="fp32", P=64, K=128, H=16, seed=3,
+                     with_kv=False)
+    check_full(p, *run_full(p))
+
+
+@pytest.mark.parametrize("dtype", ["fp8", "fp32"])
+def test_reindex(dtype):
+    kw = dict(Hi=4, Di=64, P=64, K=128) if dtype == "fp32" else {}
+    p = make_problem([20000, 9000, 17], dtype=dtype, seed=4, with_kv=False, **kw)
+    pool, plen, _ = run_full(p)
+    rng = np.random.default_rng(9)
+    q2 = rng.standard_normal(p.idx_q_f64.shape).astype(np.float32)
+    from compressed_sparse_attention_fp4_gb300 import synth
+    from tests.helpers import bf16_f64
+    if dtype == "fp8":
+        raw = synth.to_bf16_bits(q2)
+        q64 = bf16_f64(raw)
+        qd = torch.from_numpy(raw.view(np.int16)).cuda().view(torch.bfloat16)
+    else:
+        q64 = q2.astype(np.float64)
+        qd = torch.from_numpy(q2).cuda()
+    w2 = rng.random(p.w_raw.shape).astype(np.float32)
+    topk = run_reindex(p, pool, plen, qd, torch.from_numpy(w2).cuda())
+    check_reindex(p, pool, topk, q64, w2)
+    # Reindex with the Full layer's own query reproduces the Full Top-K
+    pool, plen, tk_full = run_full(p)
+    tk = run_reindex(p, pool, plen)
+    np.testing.assert_array_equal(tk.cpu().numpy(), tk_full.cpu().numpy())
+
+
+def test_full_exact_ties():
+    """Keys drawn from 3 distinct rows: huge groups of exactly equal scores."""
+    p = make_problem([30000, 5000], kind="ties", P=256, K=512, seed=5, with_kv=False)
+    check_full(p, *run_full(p))
+
+
+def test_full_ties_large_band():
+    """Ties spanning more than the in-shared-memory sort capacity."""
+    p = make_problem([130000], kind="ties", P=2048, K=512, seed=6, with_kv=False)
+    check_full(p, *run_full(p))
+
+
+def test_error_bound_holds():
+    """|approximate score - exact score| <= delta for every position."""
+    p = make_problem([60000, 12345], seed=7, with_kv=False)
+    run_full(p)
+    off = ws_offsets(p.dims, p.B)
+    ws = p.ws.cpu().numpy()
+    pos = ws[off["pos_scores"]:off["pos_scores"] + p.B * p.dims.max_ctx * 4].view(np.float32)
+    dl = ws[off["blk_delta"]:off["blk_delta"] + p.B * off["nb_max"] * 4].view(np.float32)
+    worst = 0.0
+    for b in range(p.B):
+        n = p.ctx_lens[b]
+        s = oix.scores(p.idx_q_f64[b], p.w_raw[b].astype(np.float64), oracle_keys(p, b))
+        v = pos[b * p.dims.max_ctx: b * p.dims.max_ctx + n].astype(np.float64)
+        d = np.repeat(dl[b * off["nb_max"]: b * off["nb_max"] + (n + 7) // 8], 8)[:n].astype(np.float64)
+        err = np.abs(v - s)
+        assert np.all(err <= d), np.max(err / d)
+        worst = max(worst, float(np.max(err / d)))
+    print(f"max observed |v - s| / delta = {worst:.3g}")
+
+
+def test_pool_len_and_padding_short_context():
+    p = make_problem([3, 0 + 1, 40], P=2048, K=512, seed=8, with_kv=False)
+    pool, plen, topk = run_full(p)
+    assert plen.cpu().tolist() == [1, 1, 5]
+    tk = topk.cpu().numpy()
+    assert tk[0, :3].tolist() == [0, 1, 2] and np.all(tk[0, 3:] == -1)
+    assert tk[1, :1].tolist() == [0] and np.all(tk[1, 1:] == -1)
+    assert tk[2, :40].tolist() == list(range(40))
