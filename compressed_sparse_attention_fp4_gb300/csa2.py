@@ -50,6 +50,8 @@ SIGNATURES = {
                                     _P, _P, _SZ, _P]),
     "csa2_sparse_attn_decode": (_I32, [ctypes.POINTER(CDims), _I32, _I32, _P, _P, _P, _P, _P,
                                        _P, _P, _P, _P, _F, _P, _P, _P, _SZ, _P]),
+    "csa2_sparse_attn_decode_noalloc": (_I32, [ctypes.POINTER(CDims), _I32, _I32, _P, _P, _P, _P,
+                                               _P, _P, _P, _P, _P, _F, _P, _P, _P, _P]),
     "csa2_get_device_status": (_I32, [_P, _P, ctypes.POINTER(_I32)]),
     "csa2_clear_device_status": (_I32, [_P, _P]),
 }
@@ -178,6 +180,21 @@ def csa2_sparse_attn_decode(dims: Dims, batch: int, mode: int, q, kv_codes, kv_s
         ctypes.byref(dims.c()), batch, mode, _ptr(q), _ptr(kv_codes), _ptr(kv_scales),
         _ptr(kv_rope), _ptr(page_table), _ptr(ctx_len), _ptr(topk), _ptr(swa_kv), _ptr(swa_len),
         float(scale), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def csa2_sparse_attn_decode_noalloc(dims: Dims, batch: int, mode: int, q, kv_codes, kv_scales,
+                                    kv_rope, page_table, ctx_len, topk, swa_kv, swa_len,
+                                    scale: float, out, lse, err_word=None, stream=None):
+    """Decode attention without a workspace: for callers that cannot allocate.
+
+    The split-KV scratch is a fixed array inside the library (12 MiB per GPU,
+    kept until exit); calls that overlap on the GPU race on it.  err_word is
+    an optional device int32 tensor that receives the call's device error bits.
+    """
+    _check("csa2_sparse_attn_decode_noalloc", _lib.csa2_sparse_attn_decode_noalloc(
+        ctypes.byref(dims.c()), batch, mode, _ptr(q), _ptr(kv_codes), _ptr(kv_scales),
+        _ptr(kv_rope), _ptr(page_table), _ptr(ctx_len), _ptr(topk), _ptr(swa_kv), _ptr(swa_len),
+        float(scale), _ptr(out), _ptr(lse), _ptr(err_word), _stream(stream)))
 
 
 def get_device_status(ws: torch.Tensor, stream=None) -> int:

@@ -212,6 +212,36 @@ csa2_status csa2_sparse_attn_decode(const csa2_dims* d, int32_t batch, int32_t m
                                     const int32_t* swa_len, float scale, float* out,
                                     float* lse, void* ws, size_t ws_bytes, void* stream);
 
+/* Allocation-free variant of csa2_sparse_attn_decode.  The pages describe
+ * no counterpart of this call; it exists for callers that must not allocate
+ * GPU memory on their hot path -- e.g. a plugin running inside another
+ * engine's execution step, or a serving loop whose memory budget is fixed
+ * before it starts -- and so cannot provide the workspace the other calls
+ * take.  The split-KV scratch lives instead in a fixed device array of
+ * CSA2_NOALLOC_SCRATCH_BYTES inside the library, held on every GPU that
+ * loads the library until the process exits.
+ *   Limit: 256 + B*S*H*2048 + B*S*H*8 bytes (each part rounded up to 256)
+ *   with S = ceil((topk + swa) / 64) must fit the array -- e.g. batch 8 at
+ *   Top-512, SWA-128, 64 heads; larger batches return
+ *   CSA2_ERR_WORKSPACE_TOO_SMALL and launch nothing.
+ *   Arguments and results are those of csa2_sparse_attn_decode without
+ *   ws / ws_bytes; err_word (device int32, may be NULL) receives the device
+ *   error bits of this call, ORed in.
+ *   The first call on a device looks up the array's device address (once
+ *   per device, with that device current); make that first call before any
+ *   stream capture.  The call allocates nothing (no cudaMalloc / cudaFree).
+ *   All calls share the one array and it keeps the last call's contents:
+ *   calls whose GPU work can overlap (e.g. on unsynchronised streams) race
+ *   on it and must be serialised by the caller. */
+#define CSA2_NOALLOC_SCRATCH_BYTES (12u << 20)
+csa2_status csa2_sparse_attn_decode_noalloc(const csa2_dims* d, int32_t batch, int32_t mode,
+                                            const uint16_t* q, const uint8_t* kv_codes,
+                                            const uint8_t* kv_scales, const uint16_t* kv_rope,
+                                            const int32_t* page_table, const int32_t* ctx_len,
+                                            const int32_t* topk, const uint16_t* swa_kv,
+                                            const int32_t* swa_len, float scale, float* out,
+                                            float* lse, int32_t* err_word, void* stream);
+
 /* Copies the device error word of `ws` to *word (synchronising `stream`)
  * and returns CSA2_OK if it is zero, CSA2_ERR_DEVICE_ASSERT otherwise. */
 csa2_status csa2_get_device_status(const void* ws, void* stream, int32_t* word);
