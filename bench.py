@@ -191,6 +191,25 @@ def cpu_baseline(wl, budget_s=20.0, max_queries=8):
 
 
 # ---------------------------------------------------------------------------
+# multi-rank aggregation (replicas: every rank runs its own copy of the step)
+# ---------------------------------------------------------------------------
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest per-rank value (the slowest replica sets the job time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_queries_per_s(world: int, batch: int, t_step_ms: float) -> float:
+    """Queries of all ranks per second: each rank decodes `batch` sequences."""
+    return world * batch / (t_step_ms * 1e-3)
+
+
+# ---------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -267,12 +286,8 @@ def main():
         torch.cuda.synchronize()
     barrier()
     times = np.array([a.elapsed_time(b) for a, b in ev])          # ms
-    t_step = float(times.mean())
-    if world > 1:
-        t = torch.tensor([t_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step = float(t.item())
-    qps = world * wl.batch / (t_step * 1e-3)
+    t_step = max_over_ranks(float(times.mean()), world, dev)
+    qps = job_queries_per_s(world, wl.batch, t_step)
     launches = g.launches * args.steps
     status = csa2.get_device_status(sb.ws)
 
