@@ -29,6 +29,10 @@ STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED_SHAP
 _P, _I32, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
 
 
+class CKernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int32), ("total_ms", ctypes.c_double)]
+
+
 class CDims(ctypes.Structure):
     _fields_ = [("idx_heads", ctypes.c_int32), ("idx_dim", ctypes.c_int32),
                 ("idx_k_dtype", ctypes.c_int32), ("pool_blocks", ctypes.c_int32),
@@ -53,6 +57,8 @@ SIGNATURES = {
     "csa2_sparse_attn_decode_noalloc": (_I32, [ctypes.POINTER(CDims), _I32, _I32, _P, _P, _P, _P,
                                                _P, _P, _P, _P, _P, _F, _P, _P, _P, _P]),
     "csa2_get_device_status": (_I32, [_P, _P, ctypes.POINTER(_I32)]),
+    "csa2_profile_enable": (_I32, [_I32]),
+    "csa2_profile_read": (_I32, [ctypes.POINTER(CKernelTime), _I32, ctypes.POINTER(_I32)]),
     "csa2_clear_device_status": (_I32, [_P, _P]),
 }
 
@@ -204,6 +210,19 @@ def get_device_status(ws: torch.Tensor, stream=None) -> int:
     if code not in (0, 5, 6):
         raise Csa2Error("csa2_get_device_status", code)
     return word.value
+
+
+def profile_enable(on: bool = True):
+    """Bracket every library kernel launch with CUDA events (not during capture)."""
+    _check("csa2_profile_enable", _lib.csa2_profile_enable(1 if on else 0))
+
+
+def profile_read() -> dict:
+    """{kernel name: (launches, total ms)} of the launches recorded so far."""
+    arr = (CKernelTime * 64)()
+    n = ctypes.c_int32(0)
+    _check("csa2_profile_read", _lib.csa2_profile_read(arr, 64, ctypes.byref(n)))
+    return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(min(n.value, 64))}
 
 
 def clear_device_status(ws: torch.Tensor, stream=None):

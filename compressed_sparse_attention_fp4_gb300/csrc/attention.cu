@@ -1,4 +1,5 @@
-// attention.cu -- CSA2 sparse MLA-style decode attention (all layer modes).
+// attention.cu -- CSA2 sparse MLA-style decode attention (all layer modes) on
+// the tcgen05 tensor cores.
 //
 // For one decode query per sequence and every head h, one softmax over the
 // entries E = {selected main-KV positions} + {SWA rows} (foosynaptic atlas
@@ -12,17 +13,37 @@
 // "DeepSeek-V4.1-Flash 2026: ...", section 4).
 //
 // Split-KV: the entry list (K Top-K slots, then W SWA slots) is cut into
-// chunks of 64 slots; each CTA computes, for all heads, the chunk's partial
-// (max logit m, sum of exp l, unnormalised output o), and a combine kernel
-// merges the partials: o = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s.
+// chunks of 128 slots; one CTA per (sequence, chunk):
+//   1. gathers its 128 entries, dequantizes FP4 to bf16 into shared memory
+//      (128-byte swizzled, one 16 KB region per 64 channels) and loads the
+//      query [64 heads x 576] the same way;
+//   2. S^T[128 entries x 64 heads] = KV . Q^T on tcgen05 (M=128, N=64,
+//      K=576, bf16 in, fp32 in tensor memory);
+//   3. softmax over the entries (= TMEM lanes): per-head max and sum across
+//      the 4 lane quarters; P^T is written back as bf16 hi + lo parts, so
+//      its rounding stays near 2^-17;
+//   4. O^T[512 dims x 64 heads] = V^T . P^T on tcgen05 (the same KV tile read
+//      MN-major), 4 M-tiles of 128 dims, hi and lo accumulated together;
+//   5. writes the chunk's unnormalised output and (max, sum) per head.
+// A combine kernel merges the chunks: o = sum_s e^(m_s - M) o_s / sum_s
+// e^(m_s - M) l_s, lse = M + ln(sum_s e^(m_s - M) l_s).
 #include "common.cuh"
 #include "kernels.cuh"
+#include "profile.cuh"
+#include "tc.cuh"
 
 namespace csa2 {
 
+constexpr int kAttnThreads = 256;
+constexpr int kEntries = 128;                       // entries per CTA (= MMA M)
+constexpr int kQRows = 64;                          // MMA N (heads, zero padded)
+constexpr int kRegion = kEntries * 128;             // 64 channels x 128 entries, bytes
+constexpr int kQRegion = kQRows * 128;
+constexpr int kKvBytes = 9 * kRegion;               // 576 channels
+constexpr int kQBytes = 9 * kQRegion;
+constexpr uint32_t kTmemCols = 512;                 // S^T: 64 cols, O^T: 4 x 64 cols
 
-constexpr int kKvStride = kDqk + 2;          // bf16 elements per smem row (bank skew)
-constexpr int kAttnThreads = 512;
+static_assert(kEntries == kAttnChunk, "split size of the workspace layout");
 
 __device__ inline uint32_t e2m1x2_to_f16x2_a(uint32_t byte) {
   uint32_t h2;
@@ -36,25 +57,32 @@ __device__ inline uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
-__global__ void __launch_bounds__(kAttnThreads) attn_partial_cc_kernel(AttnArgs a) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  uint16_t* kv_s = reinterpret_cast<uint16_t*>(smem_raw);                  // [64][578]
-  float* q_s = reinterpret_cast<float*>(smem_raw + kAttnChunk * kKvStride * 2);  // [H][576]
-  __shared__ int64_t row_s[kAttnChunk];     // >= 0 main row, -2 - r SWA row r, -1 empty
-  __shared__ float p_s[kAttnThreads / 32][kAttnChunk];
+__device__ inline void st_shared_v4(uint8_t* base, uint32_t off, uint4 v) {
+  *reinterpret_cast<uint4*>(base + off) = v;
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_partial_tc_kernel(AttnArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 128-byte swizzled operands need 1024-byte aligned regions
+  uint8_t* kv_s = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);   // 9 x 16 KB
+  uint8_t* q_s = kv_s + kKvBytes;                   // 9 regions x 8 KB; later P^T hi / lo
+  __shared__ uint64_t bar_s, bar_o;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int64_t row_s[kEntries];               // >= 0 main row, -2 - r SWA row r, -1 empty
+  __shared__ float red_m[2][4][32], red_l[2][4][32];
 
   const int b = blockIdx.y, split = blockIdx.x;
   const int H = a.d.heads, K = a.d.topk, W = a.d.swa;
-  const bool paged = a.page_table != nullptr;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const bool paged = a.page_table != nullptr;
   const int64_t n_ctx = checked_ctx(a.ctx_len, a.d, b, paged, a.ws);
   int swl = a.swa_len[b];
   if (swl < 0 || swl > W) {
     if (tid == 0) raise_err(a.ws, CSA2_DEV_SWA_LEN);
     swl = swl < 0 ? 0 : W;
   }
-  if (tid < kAttnChunk) {
-    int slot = split * kAttnChunk + tid;
+  if (tid < kEntries) {
+    int slot = split * kEntries + tid;
     int64_t r = -1;
     if (slot < K) {
       int32_t t = a.topk[int64_t(b) * K + slot];
@@ -70,98 +98,183 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_cc_kernel(AttnArgs 
     }
     row_s[tid] = r;
   }
-  // query -> fp32 smem
-  for (int i = tid; i < H * kDqk; i += blockDim.x)
-    q_s[i] = bf16_to_f32(a.q[int64_t(b) * H * kDqk + i]);
+  if (wid == 0) tc::tmem_alloc(&tmem_slot, kTmemCols);
+  if (tid == 0) {
+    tc::mbar_init(&bar_s, 1);
+    tc::mbar_init(&bar_o, 1);
+    tc::fence_mbar_init();
+  }
+  tc::tc_fence_before_sync();
   __syncthreads();
-  // gather + dequantize the chunk's keys / values into bf16 smem rows
-  for (int task = tid; task < kAttnChunk * 36; task += blockDim.x) {
-    int e = task / 36, part = task % 36;     // parts 0..31: latent groups, 32..35: rope / tail
-    int64_t r = row_s[e];
-    uint32_t* dst = reinterpret_cast<uint32_t*>(kv_s + e * kKvStride);
-    if (r == -1) {
-      if (part < 32) for (int i = 0; i < 8; ++i) dst[part * 8 + i] = 0;
-      else for (int i = 0; i < 8; ++i) dst[256 + (part - 32) * 8 + i] = 0;
-    } else if (r >= 0) {
+  tc::tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  // ---- query -> swizzled smem (rows >= H are zero) -------------------------
+  const uint4* qg = reinterpret_cast<const uint4*>(a.q + int64_t(b) * H * kDqk);
+#pragma unroll 4
+  for (int i = tid; i < kQRows * 72; i += kAttnThreads) {
+    int h = i / 72, c = i % 72;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (h < H) v = __ldg(qg + h * 72 + c);
+    st_shared_v4(q_s, (c >> 3) * kQRegion + tc::sw128_offset(h, c & 7), v);
+  }
+  // ---- entries -> dequantized bf16, swizzled smem ------------------------------
+#pragma unroll 2
+  for (int task = tid; task < kEntries * 36; task += kAttnThreads) {
+    const int e = task / 36, part = task % 36;      // 16 channels per part
+    const int64_t r = row_s[e];
+    const uint32_t region = part >> 2, ch0 = (part & 3) * 2;
+    const uint32_t o0 = region * kRegion + tc::sw128_offset(e, ch0);
+    const uint32_t o1 = region * kRegion + tc::sw128_offset(e, ch0 + 1);
+    uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
+    if (r >= 0) {
       if (part < 32) {
-        uint2 c = *reinterpret_cast<const uint2*>(a.codes + r * kCodesPerRow + part * 8);
-        uint32_t sc = a.scales[r * kScalesPerRow + part];
-        float s = e4m3_to_f32(sc);
-        uint32_t cw[2] = {c.x, c.y};
+        uint2 cd = __ldg(reinterpret_cast<const uint2*>(a.codes + r * kCodesPerRow) + part);
+        float s = e4m3_to_f32(__ldg(a.scales + r * kScalesPerRow + part));
+        uint32_t cw[2] = {cd.x, cd.y};
+        uint32_t w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           uint32_t h2 = e2m1x2_to_f16x2_a((cw[i >> 2] >> (8 * (i & 3))) & 0xFF);
           float lo = __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF))) * s;
           float hi = __half2float(__ushort_as_half(uint16_t(h2 >> 16))) * s;
-          dst[part * 8 + i] = pack_bf16x2(lo, hi);
+          w[i] = pack_bf16x2(lo, hi);
         }
+        v0 = make_uint4(w[0], w[1], w[2], w[3]);
+        v1 = make_uint4(w[4], w[5], w[6], w[7]);
       } else {
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(a.rope + r * kRope) + (part - 32) * 8;
-        for (int i = 0; i < 8; ++i) dst[256 + (part - 32) * 8 + i] = src[i];
+        const uint4* rp = reinterpret_cast<const uint4*>(a.rope + r * kRope) + (part - 32) * 2;
+        v0 = __ldg(rp);
+        v1 = __ldg(rp + 1);
       }
-    } else {
-      int sr = int(-2 - r);
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(a.swa + (int64_t(b) * W + sr) * kDqk);
-      if (part < 32) for (int i = 0; i < 8; ++i) dst[part * 8 + i] = src[part * 8 + i];
-      else for (int i = 0; i < 8; ++i) dst[256 + (part - 32) * 8 + i] = src[256 + (part - 32) * 8 + i];
+    } else if (r <= -2) {
+      const uint4* sp = reinterpret_cast<const uint4*>(a.swa + (int64_t(b) * W + (-2 - r)) * kDqk) + part * 2;
+      v0 = __ldg(sp);
+      v1 = __ldg(sp + 1);
     }
+    st_shared_v4(kv_s, o0, v0);
+    st_shared_v4(kv_s, o1, v1);
   }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before_sync();
   __syncthreads();
-  const int nwarps = blockDim.x / 32;
-  float* o_base = reinterpret_cast<float*>(a.ws + a.L.attn_o);
-  float* ml_base = reinterpret_cast<float*>(a.ws + a.L.attn_ml);
-  for (int h = wid; h < H; h += nwarps) {
-    const float* qh = q_s + h * kDqk;
-    // logits of entries lane and lane + 32
-    float l2[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      int e = lane + 32 * k;
-      const uint32_t* kr = reinterpret_cast<const uint32_t*>(kv_s + e * kKvStride);
-      float acc = 0.0f;
-#pragma unroll 8
-      for (int c2 = 0; c2 < kDqk / 2; ++c2) {
-        uint32_t kk = kr[c2];
-        acc = __fmaf_rn(qh[2 * c2], __uint_as_float(kk << 16), acc);
-        acc = __fmaf_rn(qh[2 * c2 + 1], __uint_as_float(kk & 0xFFFF0000u), acc);
-      }
-      l2[k] = row_s[e] == -1 ? -INFINITY : acc * a.scale;
+
+  // ---- S^T = KV . Q^T ------------------------------------------------------------
+  const uint32_t kv_addr = tc::smem_u32(kv_s), q_addr = tc::smem_u32(q_s);
+  if (tid == 0) {
+    tc::tc_fence_after_sync();
+    constexpr uint32_t idS = tc::idesc_bf16(kEntries, kQRows, 0, 0);
+#pragma unroll 1
+    for (int ks = 0; ks < 36; ++ks) {
+      uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+      uint64_t ad = tc::smem_desc(kv_addr + kb * kRegion + off, 16, 1024, 2);
+      uint64_t bd = tc::smem_desc(q_addr + kb * kQRegion + off, 16, 1024, 2);
+      tc::mma_bf16(tmem, ad, bd, idS, ks > 0);
     }
-    float m = fmaxf(l2[0], l2[1]);
+    tc::mma_commit(&bar_s);
+  }
+  bool ok = tc::mbar_wait_bounded(&bar_s, 0);
+  tc::tc_fence_after_sync();
+
+  // ---- softmax over the 128 entries (TMEM lanes) ------------------------------
+  const int quarter = wid & 3, half = wid >> 2;     // lanes 32*quarter.., heads 32*half..
+  const int e = quarter * 32 + lane;
+  const bool valid = row_s[e] != -1;
+  float x[32];
+  tc::tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(half * 32), x);
+  const float c2 = a.scale * 1.4426950408889634f;   // logits in base 2
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    x[j] = valid ? x[j] * c2 : -INFINITY;
+    float m = x[j];
 #pragma unroll
     for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    float p0 = l2[0] == -INFINITY ? 0.0f : expf(l2[0] - m);
-    float p1 = l2[1] == -INFINITY ? 0.0f : expf(l2[1] - m);
-    float l = p0 + p1;
+    if (lane == 0) red_m[half][quarter][j] = m;
+  }
+  __syncthreads();
+  float p[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float M = fmaxf(fmaxf(red_m[half][0][j], red_m[half][1][j]), fmaxf(red_m[half][2][j], red_m[half][3][j]));
+    p[j] = (M == -INFINITY || x[j] == -INFINITY) ? 0.0f : exp2f(x[j] - M);
+    float l = p[j];
 #pragma unroll
     for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
-    p_s[wid][lane] = p0;
-    p_s[wid][lane + 32] = p1;
-    __syncwarp();
-    // output dims [16*lane, 16*lane + 16)
-    float acc[16];
+    if (lane == 0) red_l[half][quarter][j] = l;
+  }
+  // P^T rows (entry e): heads 32*half.. as 4 chunks, hi and lo bf16 parts.
+  // The query buffer is free: the S^T MMAs completed (bar_s) before this.
+  uint8_t* p_hi = q_s;
+  uint8_t* p_lo = q_s + kRegion;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-    for (int e = 0; e < kAttnChunk; ++e) {
-      float p = p_s[wid][e];
-      const uint32_t* vr = reinterpret_cast<const uint32_t*>(kv_s + e * kKvStride) + lane * 8;
+  for (int t = 0; t < 4; ++t) {
+    uint32_t wh[4], wl[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint32_t vv = vr[i];
-        acc[2 * i] = __fmaf_rn(p, __uint_as_float(vv << 16), acc[2 * i]);
-        acc[2 * i + 1] = __fmaf_rn(p, __uint_as_float(vv & 0xFFFF0000u), acc[2 * i + 1]);
-      }
+    for (int i = 0; i < 4; ++i) {
+      float v0 = p[8 * t + 2 * i], v1 = p[8 * t + 2 * i + 1];
+      uint32_t hb = pack_bf16x2(v0, v1);
+      float h0 = __uint_as_float(hb << 16), h1 = __uint_as_float(hb & 0xFFFF0000u);
+      wh[i] = hb;
+      wl[i] = pack_bf16x2(v0 - h0, v1 - h1);
     }
-    __syncwarp();
-    int64_t pidx = (int64_t(b) * a.L.splits + split) * H + h;
-    float4* op = reinterpret_cast<float4*>(o_base + pidx * kLatent + lane * 16);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) op[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-    if (lane == 0) {
-      ml_base[pidx * 2] = m;
-      ml_base[pidx * 2 + 1] = l;
+    uint32_t off = tc::sw128_offset(e, half * 4 + t);
+    st_shared_v4(p_hi, off, make_uint4(wh[0], wh[1], wh[2], wh[3]));
+    st_shared_v4(p_lo, off, make_uint4(wl[0], wl[1], wl[2], wl[3]));
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before_sync();
+  __syncthreads();
+  float* ml_base = reinterpret_cast<float*>(a.ws + a.L.attn_ml);
+  const int64_t prow = (int64_t(b) * a.L.splits + split) * H;
+  if (quarter == 0) {
+    int h = half * 32 + lane;
+    if (h < H) {
+      float M = fmaxf(fmaxf(red_m[half][0][lane], red_m[half][1][lane]), fmaxf(red_m[half][2][lane], red_m[half][3][lane]));
+      float L = red_l[half][0][lane] + red_l[half][1][lane] + red_l[half][2][lane] + red_l[half][3][lane];
+      ml_base[(prow + h) * 2] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
+      ml_base[(prow + h) * 2 + 1] = L;
     }
   }
+
+  // ---- O^T = V^T . P^T  (4 M-tiles of 128 channels; hi and lo parts) -------------
+  if (tid == 0) {
+    tc::tc_fence_after_sync();
+    constexpr uint32_t idO = tc::idesc_bf16(kEntries, kQRows, 1, 1);
+    const uint32_t ph = tc::smem_u32(p_hi), pl = tc::smem_u32(p_lo);
+#pragma unroll 1
+    for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll 1
+      for (int part = 0; part < 2; ++part) {
+#pragma unroll 1
+        for (int ks = 0; ks < 8; ++ks) {
+          uint64_t ad = tc::smem_desc(kv_addr + (2 * mt) * kRegion + ks * 2048, kRegion, 1024, 2);
+          uint64_t bd = tc::smem_desc((part ? pl : ph) + ks * 2048, kRegion, 1024, 2);
+          tc::mma_bf16(tmem + 64 + 64 * mt, ad, bd, idO, part > 0 || ks > 0);
+        }
+      }
+    }
+    tc::mma_commit(&bar_o);
+  }
+  ok = tc::mbar_wait_bounded(&bar_o, 0) && ok;
+  tc::tc_fence_after_sync();
+  if (!ok && tid == 0) raise_err(a.ws, CSA2_DEV_TIMEOUT);
+
+  // ---- unnormalised partial output -------------------------------------------------
+  float* o_base = reinterpret_cast<float*>(a.ws + a.L.attn_o);
+#pragma unroll 1
+  for (int mt = 0; mt < 4; ++mt) {
+    float o[32];
+    tc::tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(64 + 64 * mt + half * 32), o);
+    const int dim = mt * 128 + quarter * 32 + lane;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      int h = half * 32 + j;
+      if (h < H) o_base[(prow + h) * kLatent + dim] = o[j];
+    }
+  }
+  tc::tc_fence_before_sync();
+  __syncthreads();
+  if (wid == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
@@ -189,19 +302,18 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
   if (threadIdx.x == 0) a.lse[int64_t(b) * H + h] = (Lsum > 0.0f) ? M + logf(Lsum) : -INFINITY;
 }
 
-size_t attn_smem_bytes(int heads) {
-  return size_t(kAttnChunk) * kKvStride * 2 + size_t(heads) * kDqk * 4;
-}
+size_t attn_smem_bytes(int) { return size_t(kKvBytes) + size_t(kQBytes) + 1024; }
 
 cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
   size_t smem = attn_smem_bytes(a.d.heads);
-  cudaError_t e = cudaFuncSetAttribute(attn_partial_cc_kernel,
+  cudaError_t e = cudaFuncSetAttribute(attn_partial_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  attn_partial_cc_kernel<<<dim3(unsigned(a.L.splits), unsigned(a.batch)), kAttnThreads, smem, st>>>(a);
+  CSA2_PROFILED(st, "attn_partial_tc",
+                (attn_partial_tc_kernel<<<dim3(unsigned(a.L.splits), unsigned(a.batch)), kAttnThreads, smem, st>>>(a)));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_combine_kernel<<<dim3(unsigned(a.d.heads), unsigned(a.batch)), 128, 0, st>>>(a);
+  CSA2_PROFILED(st, "attn_combine", (attn_combine_kernel<<<dim3(unsigned(a.d.heads), unsigned(a.batch)), 128, 0, st>>>(a)));
   return cudaGetLastError();
 }
 

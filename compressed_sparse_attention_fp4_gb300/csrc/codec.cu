@@ -23,6 +23,7 @@
 // share group g, and each lane stores 4 packed bytes (coalesced 128 B per
 // warp) and, for even lanes, one scale byte.
 #include "common.cuh"
+#include "profile.cuh"
 
 namespace csa2 {
 
@@ -144,16 +145,18 @@ static int codec_grid(int64_t n) {
 cudaError_t launch_quantize(const uint16_t* x, int64_t n, const int64_t* dst_rows, uint8_t* codes,
                             uint8_t* scales, cudaStream_t st) {
   if (n == 0) return cudaSuccess;
-  quantize_kernel<<<codec_grid(n), 256, 0, st>>>(reinterpret_cast<const uint4*>(x), n, dst_rows,
-                                                 reinterpret_cast<uint32_t*>(codes), scales);
+  CSA2_PROFILED(st, "fp4_quantize",
+                (quantize_kernel<<<codec_grid(n), 256, 0, st>>>(reinterpret_cast<const uint4*>(x), n, dst_rows,
+                                                                reinterpret_cast<uint32_t*>(codes), scales)));
   return cudaGetLastError();
 }
 
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t n, uint16_t* y,
                               cudaStream_t st) {
   if (n == 0) return cudaSuccess;
-  dequantize_kernel<<<codec_grid(n), 256, 0, st>>>(reinterpret_cast<const uint2*>(codes), scales,
-                                                   n, reinterpret_cast<uint4*>(y));
+  CSA2_PROFILED(st, "fp4_dequantize",
+                (dequantize_kernel<<<codec_grid(n), 256, 0, st>>>(reinterpret_cast<const uint2*>(codes), scales,
+                                                                  n, reinterpret_cast<uint4*>(y))));
   return cudaGetLastError();
 }
 

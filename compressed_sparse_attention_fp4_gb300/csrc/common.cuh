@@ -23,7 +23,7 @@ constexpr int kMaxSwa = 128;
 constexpr int kMaxIdxHeads = 16;
 constexpr int64_t kMaxCtx = int64_t(1) << 20;   // 8 selection CTAs x 16384 blocks
 constexpr int kSelCapPerCta = 16384;           // items a selection CTA holds
-constexpr int kAttnChunk = 64;                 // entries per split-KV partial
+constexpr int kAttnChunk = 128;                // entries per split-KV partial
 
 // ---------------------------------------------------------------------------
 // Workspace layout.  Computed identically on the host (sizing, validation)

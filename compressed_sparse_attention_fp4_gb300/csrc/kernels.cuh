@@ -48,6 +48,8 @@ cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64
                               cudaStream_t st);
 cudaError_t launch_full(IdxArgs a, cudaStream_t st);
 cudaError_t launch_reindex(IdxArgs a, cudaStream_t st);
+cudaError_t launch_select(IdxArgs a, bool reindex, cudaStream_t st);
+cudaError_t launch_scan_tc(const IdxArgs& a, bool reindex, cudaStream_t st);
 cudaError_t launch_attention(AttnArgs a, cudaStream_t st);
 size_t select_smem_bytes();
 size_t attn_smem_bytes(int heads);

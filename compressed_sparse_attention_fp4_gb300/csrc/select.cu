@@ -1,0 +1,779 @@
+// select.cu -- certified Top-P / Top-K selection of the CSA2 indexer.
+//
+// Picks the P best items (blocks for the candidate pool, positions for the
+// Top-K) under the order (exact score desc, index asc), given approximate
+// scores v with a rigorous bound |v - s| <= delta (foosynaptic atlas
+// "DeepSeek-V4.1-Flash 梗概", section 3.2: the Full layer keeps the Top-2048
+// blocks of 8 as the pool, Reindex layers take Top-512 inside it).
+//
+//   U = v + delta (rounded up), L = v - delta (rounded down)
+//   mu'     >= P-th largest U     (upper edge of its 22-bit radix bucket)
+//   lambda' <= P-th largest L     (lower edge of its bucket)
+//   L > mu'              -> selected (its exact score beats the P-th best)
+//   U < lambda'          -> not selected
+//   otherwise ("band")   -> exact score (fixed point, exact.cuh), then the
+//                           best (P - #selected) band items by exact score.
+// The result is the selection on exact scores.
+//
+// One CTA holds up to 16,384 items in shared memory; a sequence with more
+// items (the block scores of a context above 131,072 positions) is split over
+// a thread-block cluster of up to 8 CTAs that merge their radix histograms
+// through distributed shared memory.  Cluster barriers are hardware barriers
+// (no software spin).
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "exact.cuh"
+#include "kernels.cuh"
+#include "profile.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace csa2 {
+
+enum ItemKind { kBlocks = 0, kPoolPos = 1, kReindexPos = 2 };
+
+constexpr int kSelThreads = 1024;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSortCap = 4096;
+constexpr int kBins = 2048;                 // 11-bit radix digits
+constexpr int kExItems = 128;               // band items re-scored per chunk (<= 8 positions each)
+
+struct SelSmem {
+  uint32_t keyU[kSelCapPerCta];             // reused: sort keys (rank 0)
+  uint32_t keyL[kSelCapPerCta];             // reused: band list, sort ids
+  uint32_t band_bits[kSelCapPerCta / 32];
+  uint32_t sel_bits[kSelCapPerCta / 32];
+  uint32_t word_off[kSelCapPerCta / 32];
+  uint32_t hist[2][kBins];                  // this CTA's histograms (U, L)
+  uint32_t ghist[2][kBins];                 // cluster-wide sums
+  Factor qf[kMaxIdxHeads * 128];            // query factors, [channel][head]
+  int32_t qi[128 * kMaxIdxHeads];           // query as integers, [channel][head]
+  int32_t q_elo[kMaxIdxHeads];              // q = qi * 2^q_elo (exact)
+  int32_t q_fast[kMaxIdxHeads];             // 1: the int32 x int32 -> int64 path is exact
+  unsigned long long q_l1[kMaxIdxHeads];    // sum_c |qi|
+  float w[kMaxIdxHeads];
+  int32_t pool_ids[kMaxPool];
+  uint32_t red[2][kSelWarps];
+  uint32_t bucket[2], rem[2];
+  uint32_t kmin, kmax, base_key;
+  int shift0;
+  uint32_t cnt_in, cnt_band, cnt_sel;
+  uint32_t n_cand;
+};
+
+// Scratch of the exact re-scoring, overlaid on keyU (free between the
+// classification and the final pick).
+struct ExScratch {
+  double dd[64 * kMaxIdxHeads];             // exact head dots of a round
+  double cand_score[kSelThreads];
+  int64_t cand_pos[kSelThreads];            // candidate positions of a chunk
+  unsigned long long item_best[128];
+  int32_t cand_item[kSelThreads];
+  int32_t krows[64 * 129];                  // staged keys: E4M3 as k*2^9 integers, or fp32 bits
+};
+static_assert(sizeof(ExScratch) <= sizeof(uint32_t) * kSelCapPerCta, "exact scratch must fit keyU");
+
+__device__ inline ExScratch& ex_scratch(SelSmem& sm) { return *reinterpret_cast<ExScratch*>(sm.keyU); }
+
+struct SelCtx {
+  int rank, cs;
+  int64_t n_ctx;
+  int b;
+};
+
+__device__ inline void cl_sync(const SelCtx& c) {
+  if (c.cs > 1) cg::this_cluster().sync(); else __syncthreads();
+}
+
+template <class T>
+__device__ inline const T* remote(const SelCtx& c, const T* p, int r) {
+  return c.cs > 1 ? cg::this_cluster().map_shared_rank(p, r) : p;
+}
+
+// Block-wide exclusive scan of word popcounts of `bits` (nwords <= 512) into
+// sm.word_off; returns the total.
+__device__ uint32_t scan_words(SelSmem& sm, const uint32_t* bits, int nwords) {
+  __syncthreads();
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  uint32_t v = tid < nwords ? __popc(bits[tid]) : 0;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm.red[0][wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t s = sm.red[0][lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t y = __shfl_up_sync(0xFFFFFFFFu, s, o);
+      if (lane >= o) s += y;
+    }
+    sm.red[0][lane] = s;
+  }
+  __syncthreads();
+  uint32_t base = wid ? sm.red[0][wid - 1] : 0;
+  if (tid < nwords) sm.word_off[tid] = base + x - v;
+  uint32_t total = sm.red[0][kSelWarps - 1];
+  __syncthreads();
+  return total;
+}
+
+// For both key kinds j in {0: U, 1: L}: the bin (scanning from the top) that
+// holds the sm.rem[j]-th largest key of sm.ghist[j]; updates bucket / rem.
+// Thread t owns bins 2047-2t and 2046-2t.
+__device__ void find_buckets(SelSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  uint32_t c0[2], c1[2], tot[2], incl[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    c0[j] = sm.ghist[j][kBins - 1 - 2 * tid];
+    c1[j] = sm.ghist[j][kBins - 2 - 2 * tid];
+    tot[j] = c0[j] + c1[j];
+    uint32_t x = tot[j];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
+    }
+    incl[j] = x;
+    if (lane == 31) sm.red[j][wid] = x;
+  }
+  __syncthreads();
+  if (wid < 2) {
+    uint32_t s = sm.red[wid][lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t y = __shfl_up_sync(0xFFFFFFFFu, s, o);
+      if (lane >= o) s += y;
+    }
+    sm.red[wid][lane] = s;
+  }
+  __syncthreads();
+  uint32_t rem[2] = {sm.rem[0], sm.rem[1]};
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    uint32_t before = (wid ? sm.red[j][wid - 1] : 0) + incl[j] - tot[j];
+    if (before < rem[j] && rem[j] <= before + tot[j]) {
+      if (before + c0[j] >= rem[j]) {
+        sm.bucket[j] = kBins - 1 - 2 * tid;
+        sm.rem[j] = rem[j] - before;
+      } else {
+        sm.bucket[j] = kBins - 2 - 2 * tid;
+        sm.rem[j] = rem[j] - before - c0[j];
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Cluster-wide radix localisation of the k-th largest key of keyU and of
+// keyL.  The keys are first mapped to [kmin, kmax] (cluster min / max over
+// the valid items), so that the 2048 bins of the first pass spread over the
+// occupied range; the second pass splits the chosen bin into 2048 more, which
+// leaves a final bucket of at most 2^10 keys.  Returns muEdge (>= k-th largest
+// U key) and lamEdge (<= k-th largest L key).
+__device__ void radix_edges(SelSmem& sm, const SelCtx& c, int n_local, uint32_t k,
+                            uint32_t& muEdge, uint32_t& lamEdge) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  // ---- key range ----------------------------------------------------------
+  uint32_t mn = 0xFFFFFFFFu, mx = 0;
+  for (int i = tid; i < n_local; i += blockDim.x) {
+    uint32_t u = sm.keyU[i], l = sm.keyL[i];
+    if (u) { mn = min(mn, l); mx = max(mx, u); }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  }
+  if (lane == 0) { sm.red[0][wid] = mn; sm.red[1][wid] = mx; }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t a0 = 0xFFFFFFFFu, a1 = 0;
+    for (int i = 0; i < kSelWarps; ++i) { a0 = min(a0, sm.red[0][i]); a1 = max(a1, sm.red[1][i]); }
+    sm.kmin = a0;
+    sm.kmax = a1;
+  }
+  cl_sync(c);
+  if (tid == 0) {
+    uint32_t a0 = 0xFFFFFFFFu, a1 = 0;
+    for (int r = 0; r < c.cs; ++r) { a0 = min(a0, *remote(c, &sm.kmin, r)); a1 = max(a1, *remote(c, &sm.kmax, r)); }
+    sm.rem[0] = k;
+    sm.rem[1] = k;
+    sm.base_key = a0;
+    uint32_t range = a1 - a0;
+    int bits = range ? 32 - __clz(range) : 0;
+    sm.shift0 = bits > 11 ? bits - 11 : 0;
+  }
+  cl_sync(c);       // the range is read before any rank overwrites kmin / kmax
+  const uint32_t kb = sm.base_key;
+  const int sh0 = sm.shift0, sh1 = sh0 > 11 ? sh0 - 11 : 0;
+  uint32_t b0U = 0, b0L = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int i = tid; i < 2 * kBins; i += blockDim.x) (&sm.hist[0][0])[i] = 0;
+    __syncthreads();
+    const int sh = pass ? sh1 : sh0;
+    for (int i = tid; i < n_local; i += blockDim.x) {
+      uint32_t u = sm.keyU[i];
+      if (!u) continue;
+      uint32_t du = u - kb, dl = sm.keyL[i] - kb;
+      if (pass == 0) {
+        atomicAdd(&sm.hist[0][du >> sh], 1u);
+        atomicAdd(&sm.hist[1][dl >> sh], 1u);
+      } else {
+        // offset inside the first-pass bin, in units of 2^sh1 keys
+        if ((du >> sh0) == b0U) atomicAdd(&sm.hist[0][(du - (b0U << sh0)) >> sh], 1u);
+        if ((dl >> sh0) == b0L) atomicAdd(&sm.hist[1][(dl - (b0L << sh0)) >> sh], 1u);
+      }
+    }
+    cl_sync(c);
+    for (int i = tid; i < 2 * kBins; i += blockDim.x) {
+      uint32_t s = 0;
+      for (int r = 0; r < c.cs; ++r) s += remote(c, &sm.hist[0][0], r)[i];
+      (&sm.ghist[0][0])[i] = s;
+    }
+    cl_sync(c);     // every rank has read every histogram before they are reset
+    find_buckets(sm);
+    if (pass == 0) { b0U = sm.bucket[0]; b0L = sm.bucket[1]; }
+  }
+  uint32_t lo_u = (b0U << sh0) + (sm.bucket[0] << sh1);
+  uint32_t lo_l = (b0L << sh0) + (sm.bucket[1] << sh1);
+  muEdge = kb + lo_u + ((1u << sh1) - 1);
+  lamEdge = kb + lo_l;
+  __syncthreads();
+}
+
+// RN64(v * 2^e) for an int64 v, built with integer operations only (the
+// fp64 conversion instructions are slow on this GPU).  Requires the result to
+// be a normal fp64 number, which holds for every indexer product sum.
+__device__ inline double int_to_f64_rn(long long v, int e) {
+  if (v == 0) return 0.0;
+  unsigned long long sign = v < 0 ? (1ull << 63) : 0ull;
+  unsigned long long mag = v < 0 ? 0ull - (unsigned long long)v : (unsigned long long)v;
+  int p = 63 - __clzll((long long)mag);          // leading bit index
+  unsigned long long m;
+  int ex = p + e;
+  if (p <= 52) {
+    m = mag << (52 - p);
+  } else {
+    int sh = p - 52;
+    m = mag >> sh;
+    unsigned long long rem = mag & ((1ull << sh) - 1), half = 1ull << (sh - 1);
+    if (rem > half || (rem == half && (m & 1ull))) {
+      ++m;
+      if (m == (1ull << 53)) { m >>= 1; ++ex; }
+    }
+  }
+  unsigned long long bits = sign | ((unsigned long long)(ex + 1023) << 52) | (m & ((1ull << 52) - 1));
+  return __longlong_as_double((long long)bits);
+}
+
+// Exact fp64 value of an fp32 number, built with integer operations only.
+__device__ inline double f32_to_f64_exact(float x) {
+  uint32_t u = __float_as_uint(x);
+  unsigned long long sign = (unsigned long long)(u >> 31) << 63;
+  int E = (u >> 23) & 0xFF;
+  uint32_t m = u & 0x7FFFFF;
+  if (E == 0) {
+    if (m == 0) return __longlong_as_double((long long)sign);
+    int p = 31 - __clz(m);                       // subnormal: normalise
+    unsigned long long mm = (unsigned long long)(m << (23 - p)) & 0x7FFFFF;
+    int ex = p - 149;
+    return __longlong_as_double((long long)(sign | ((unsigned long long)(ex + 1023) << 52) | (mm << 29)));
+  }
+  return __longlong_as_double((long long)(sign | ((unsigned long long)(E - 127 + 1023) << 52) |
+                                          ((unsigned long long)m << 29)));
+}
+
+struct ItemVal {
+  float v, delta;
+  bool valid;
+};
+
+__device__ inline ItemVal load_item(const IdxArgs& a, ItemKind kind, const SelCtx& c,
+                                    const int32_t* pool_ids, int64_t item) {
+  const float* __restrict__ ws_f = reinterpret_cast<const float*>(a.ws);
+  ItemVal r = {0.0f, 0.0f, false};
+  if (kind == kBlocks) {
+    int64_t nb = (c.n_ctx + kBlock - 1) / kBlock;
+    if (item < nb) {
+      r.valid = true;
+      r.v = ws_f[(a.L.blk_scores >> 2) + int64_t(c.b) * a.L.nb_max + item];
+      r.delta = ws_f[(a.L.blk_delta >> 2) + int64_t(c.b) * a.L.nb_max + item];
+    }
+  } else {
+    int32_t blk = pool_ids[item >> 3];
+    int64_t t = int64_t(blk) * kBlock + (item & 7);
+    if (blk >= 0 && t < c.n_ctx) {
+      r.valid = true;
+      if (kind == kPoolPos) {
+        r.v = ws_f[(a.L.pos_scores >> 2) + int64_t(c.b) * a.d.max_ctx + t];
+        r.delta = ws_f[(a.L.blk_delta >> 2) + int64_t(c.b) * a.L.nb_max + blk];
+      } else {
+        int64_t P8 = int64_t(a.d.pool_blocks) * kBlock;
+        r.v = ws_f[(a.L.ri_scores >> 2) + int64_t(c.b) * P8 + item];
+        r.delta = ws_f[(a.L.ri_delta >> 2) + int64_t(c.b) * a.d.pool_blocks + (item >> 3)];
+      }
+    }
+  }
+  return r;
+}
+
+// Exact scores of a list of positions (fp64, -inf for invalid ones), using
+// the whole CTA.  Round of up to kExRows positions: their indexer-K rows are
+// staged in shared memory; one thread per (position, head) sums the Di exact
+// products serially in int64 (or, for a span too wide, in the multi-limb
+// accumulator) and rounds once; then one thread per position forms the fp64
+// head sum in head order.  All positions of a round proceed in parallel.
+constexpr int kExRows = 64;
+constexpr int kExRowWords = 129;          // 128 words + 1 word of bank skew
+
+__device__ void exact_scores(const IdxArgs& a, SelSmem& sm, const SelCtx& c, const int64_t* pos,
+                             int np, double* out) {
+  ExScratch& ex = ex_scratch(sm);
+  const int tid = threadIdx.x;
+  const int hi = a.d.idx_heads, di = a.d.idx_dim;
+  const bool fp8 = a.d.idx_k_dtype == CSA2_IDXK_E4M3;
+  for (int r0 = 0; r0 < np; r0 += kExRows) {
+    const int nr = min(kExRows, np - r0);
+    __syncthreads();
+    // stage the rows: E4M3 keys as exact integers k * 2^9, fp32 keys as bits
+    for (int i = tid; i < nr * di; i += blockDim.x) {
+      int rr = i / di, ch = i % di;
+      int64_t t = pos[r0 + rr];
+      int32_t v = 0;
+      if (t >= 0 && t < c.n_ctx) {
+        int64_t row = kv_row(a.page_table, a.d, c.b, t, a.ws);
+        if (row >= 0) {
+          if (fp8) {
+            Factor f = factor_e4m3(reinterpret_cast<const uint8_t*>(a.idx_k)[row * di + ch]);
+            v = f.sig * (1 << (f.exp + 9));
+          } else {
+            v = reinterpret_cast<const int32_t*>(a.idx_k)[row * di + ch];
+          }
+        }
+      }
+      ex.krows[rr * kExRowWords + ch] = v;
+    }
+    __syncthreads();
+    for (int task = tid; task < nr * hi; task += blockDim.x) {
+      const int rr = task / hi, h = task % hi;
+      const int32_t* kr = ex.krows + rr * kExRowWords;
+      double d;
+      if (fp8 && sm.q_fast[h]) {
+        // |sum| <= sum|qi| * 448*2^9 < 2^62: the int64 sum is exact
+        long long acc = 0;
+#pragma unroll 8
+        for (int ch = 0; ch < 128; ++ch) acc += (long long)sm.qi[ch * kMaxIdxHeads + h] * (long long)kr[ch];
+        d = int_to_f64_rn(acc, sm.q_elo[h] - 9);
+      } else {
+        auto kf = [&](int ch) {
+          return fp8 ? Factor{kr[ch], -9} : factor_f32(__int_as_float(kr[ch]));
+        };
+        Factor qrow[128];
+        for (int ch = 0; ch < di; ++ch) qrow[ch] = sm.qf[ch * kMaxIdxHeads + h];
+        d = exact_head_dot(qrow, di, kf);
+      }
+      ex.dd[rr * kMaxIdxHeads + h] = d;
+    }
+    __syncthreads();
+    // w_h * ReLU(d_h): independent products, one thread per (position, head)
+    for (int task = tid; task < nr * hi; task += blockDim.x) {
+      const int rr = task / hi, h = task % hi;
+      double d = ex.dd[rr * kMaxIdxHeads + h];
+      unsigned long long db = (unsigned long long)__double_as_longlong(d);
+      bool positive = (db >> 63) == 0 && db != 0;
+      ex.dd[rr * kMaxIdxHeads + h] = __dmul_rn(f32_to_f64_exact(sm.w[h]), positive ? d : 0.0);
+    }
+    __syncthreads();
+    // the ordered fp64 sum over heads, one thread per position
+    if (tid < nr) {
+      int64_t t = pos[r0 + tid];
+      double s = -INFINITY;
+      if (t >= 0 && t < c.n_ctx) {
+        s = 0.0;
+        for (int h = 0; h < hi; ++h) s = __dadd_rn(s, ex.dd[tid * kMaxIdxHeads + h]);
+      }
+      out[r0 + tid] = s;
+    }
+  }
+  __syncthreads();
+}
+
+// Monotone 64-bit key of a double (larger value -> larger key).
+__device__ inline uint64_t f64_key(double x) {
+  uint64_t u = uint64_t(__double_as_longlong(x + 0.0));
+  return (u >> 63) ? ~u : (u | (uint64_t(1) << 63));
+}
+
+// Selects the k best of n items of `kind`; writes their ids ascending to
+// out[0 .. k).  All CTAs of the cluster take part (items split by rank).
+__device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c, ItemKind kind,
+                                 int64_t n_items, int64_t k, int32_t* out, double* g_exact,
+                                 int32_t* g_list, uint8_t* g_pick) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int64_t base = int64_t(c.rank) * kSelCapPerCta;
+  const int n_local = int(max64(0, min64(kSelCapPerCta, n_items - base)));
+  const int nwords = (n_local + 31) / 32;
+  for (int i = tid; i < kSelCapPerCta / 32; i += blockDim.x) { sm.band_bits[i] = 0; sm.sel_bits[i] = 0; }
+  if (tid == 0) { sm.cnt_in = 0; sm.cnt_band = 0; }
+  __syncthreads();
+#pragma unroll 4
+  for (int i = tid; i < n_local; i += blockDim.x) {
+    ItemVal it = load_item(a, kind, c, sm.pool_ids, base + i);
+    uint32_t ku = 0, kl = 0;
+    if (it.valid) {
+      ku = f32_key(__fadd_ru(it.v, it.delta));
+      kl = f32_key(__fadd_rd(it.v, -it.delta));
+    }
+    sm.keyU[i] = ku;
+    sm.keyL[i] = kl;
+  }
+  __syncthreads();
+  if (k >= n_items) {
+    for (int i = tid; i < n_local; i += blockDim.x)
+      if (sm.keyU[i]) atomicOr(&sm.sel_bits[i >> 5], 1u << (i & 31));
+  } else {
+    uint32_t muE, lamE;
+    radix_edges(sm, c, n_local, uint32_t(k), muE, lamE);
+    uint32_t my_in = 0, my_band = 0;
+    for (int i = tid; i < n_local; i += blockDim.x) {
+      uint32_t u = sm.keyU[i], l = sm.keyL[i];
+      if (u == 0) continue;
+      if (l > muE) { atomicOr(&sm.sel_bits[i >> 5], 1u << (i & 31)); ++my_in; }
+      else if (u >= lamE) { atomicOr(&sm.band_bits[i >> 5], 1u << (i & 31)); ++my_band; }
+    }
+    atomicAdd(&sm.cnt_in, my_in);
+    atomicAdd(&sm.cnt_band, my_band);
+    // ordered list of this CTA's band items (keyL area is free now)
+    uint32_t nband = scan_words(sm, sm.band_bits, nwords);
+    int32_t* blist = reinterpret_cast<int32_t*>(sm.keyL);
+    for (int wv = tid; wv < nwords; wv += blockDim.x) {
+      uint32_t bits = sm.band_bits[wv], o = sm.word_off[wv];
+      while (bits) {
+        int bp = __ffs(bits) - 1;
+        bits &= bits - 1;
+        blist[o++] = wv * 32 + bp;
+      }
+    }
+    __syncthreads();
+    // exact scores of the band, a chunk of items at a time.  For a block,
+    // only the positions whose upper bound reaches the block's best lower
+    // bound can hold its exact maximum; the others are not re-scored.
+    const float* ws_f = reinterpret_cast<const float*>(a.ws);
+    ExScratch& ex = ex_scratch(sm);
+    for (uint32_t j0 = 0; j0 < nband; j0 += kExItems) {
+      const int nit = int(min64(kExItems, int64_t(nband) - j0));
+      if (tid == 0) sm.n_cand = 0;
+      __syncthreads();
+      for (int j = wid; j < nit; j += kSelWarps) {
+        int64_t gi = base + blist[j0 + j];
+        if (kind == kBlocks) {
+          int64_t t = gi * kBlock + (lane & 7);
+          bool ok = lane < kBlock && t < c.n_ctx;
+          float dl = ws_f[(a.L.blk_delta >> 2) + int64_t(c.b) * a.L.nb_max + gi];
+          float v = ok ? ws_f[(a.L.pos_scores >> 2) + int64_t(c.b) * a.d.max_ctx + t] : -INFINITY;
+          float lo = ok ? __fadd_rd(v, -dl) : -INFINITY;
+          float hv = ok ? __fadd_ru(v, dl) : -INFINITY;
+          float lmax = lo;
+#pragma unroll
+          for (int o = 16; o; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+          bool cand = ok && hv >= lmax;
+          uint32_t m = __ballot_sync(0xFFFFFFFFu, cand);
+          uint32_t slot0 = 0;
+          if (lane == 0) slot0 = atomicAdd(&sm.n_cand, uint32_t(__popc(m)));
+          slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
+          if (cand) {
+            uint32_t sl = slot0 + __popc(m & ((1u << lane) - 1));
+            ex.cand_pos[sl] = t;
+            ex.cand_item[sl] = j;
+          }
+        } else if (lane == 0) {
+          int32_t blk = sm.pool_ids[gi >> 3];
+          uint32_t sl = atomicAdd(&sm.n_cand, 1u);
+          ex.cand_pos[sl] = blk < 0 ? -1 : int64_t(blk) * kBlock + (gi & 7);
+          ex.cand_item[sl] = j;
+        }
+        if (lane == 0) ex.item_best[j] = 0;       // key of -inf is above 0
+      }
+      __syncthreads();
+      const int ncand = int(sm.n_cand);
+      exact_scores(a, sm, c, ex.cand_pos, ncand, ex.cand_score);
+      for (int i = tid; i < ncand; i += blockDim.x)
+        atomicMax(&ex.item_best[ex.cand_item[i]], f64_key(ex.cand_score[i]));
+      __syncthreads();
+      for (int j = tid; j < nit; j += blockDim.x) {
+        int64_t gi = base + blist[j0 + j];
+        uint64_t kk = ex.item_best[j];
+        uint64_t u = (kk >> 63) ? (kk & ~(uint64_t(1) << 63)) : ~kk;   // inverse of f64_key
+        g_exact[gi] = kk ? __longlong_as_double((long long)u) : -INFINITY;
+        g_pick[gi] = 0;
+      }
+      __syncthreads();
+    }
+    cl_sync(c);
+    uint32_t tot_in = 0, tot_band = 0, band_off = 0;
+    for (int r = 0; r < c.cs; ++r) {
+      uint32_t ci = *remote(c, &sm.cnt_in, r), cb = *remote(c, &sm.cnt_band, r);
+      tot_in += ci;
+      tot_band += cb;
+      if (r < c.rank) band_off += cb;
+    }
+    for (uint32_t j = tid; j < nband; j += blockDim.x) g_list[band_off + j] = int32_t(base + blist[j]);
+    cl_sync(c);
+    // ---- rank 0 picks the best (k - tot_in) band items by exact score -----
+    int64_t need = k - int64_t(tot_in);
+    if (c.rank == 0 && need > 0) {
+      if (need >= int64_t(tot_band)) {
+        for (uint32_t i = tid; i < tot_band; i += blockDim.x) g_pick[g_list[i]] = 1;
+      } else if (tot_band <= kSortCap) {
+        uint64_t* skey = reinterpret_cast<uint64_t*>(sm.keyU);
+        int32_t* sidx = reinterpret_cast<int32_t*>(sm.keyL);
+        int nsort = 1;
+        while (nsort < int(tot_band)) nsort <<= 1;
+        for (int i = tid; i < nsort; i += blockDim.x) {
+          if (i < int(tot_band)) { int32_t it = g_list[i]; skey[i] = f64_key(g_exact[it]); sidx[i] = it; }
+          else { skey[i] = 0; sidx[i] = INT_MAX; }
+        }
+        __syncthreads();
+        for (int size = 2; size <= nsort; size <<= 1) {
+          for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = tid; i < nsort; i += blockDim.x) {
+              int j = i ^ stride;
+              if (j > i) {
+                bool desc = (i & size) == 0;
+                bool i_first = skey[i] > skey[j] || (skey[i] == skey[j] && sidx[i] < sidx[j]);
+                if (desc != i_first) {
+                  uint64_t tk = skey[i]; skey[i] = skey[j]; skey[j] = tk;
+                  int32_t ti = sidx[i]; sidx[i] = sidx[j]; sidx[j] = ti;
+                }
+              }
+            }
+            __syncthreads();
+          }
+        }
+        for (int i = tid; i < need; i += blockDim.x) g_pick[sidx[i]] = 1;
+      } else {
+        // large band (massive exact ties): 64-bit radix select streamed over
+        // the global band list by this CTA alone
+        uint32_t* h64 = &sm.hist[0][0];
+        __shared__ unsigned long long pref64;
+        __shared__ uint32_t rem64;
+        if (tid == 0) { pref64 = 0; rem64 = uint32_t(need); }
+        __syncthreads();
+        for (int pass = 0; pass < 8; ++pass) {
+          int shift = 56 - 8 * pass;
+          uint64_t maskHi = pass ? (~uint64_t(0) << (64 - 8 * pass)) : 0;
+          if (tid < 256) h64[tid] = 0;
+          __syncthreads();
+          for (uint32_t i = tid; i < tot_band; i += blockDim.x) {
+            uint64_t key = f64_key(g_exact[g_list[i]]);
+            if ((key & maskHi) == pref64) atomicAdd(&h64[(key >> shift) & 0xFF], 1u);
+          }
+          __syncthreads();
+          if (tid == 0) {
+            uint32_t acc = 0;
+            for (int bkt = 255; bkt >= 0; --bkt) {
+              if (acc + h64[bkt] >= rem64) { pref64 |= uint64_t(bkt) << shift; rem64 -= acc; break; }
+              acc += h64[bkt];
+            }
+          }
+          __syncthreads();
+        }
+        if (tid == 0) {
+          uint64_t kappa = pref64;
+          uint32_t taken = 0;
+          for (uint32_t i = 0; i < tot_band; ++i) {
+            uint64_t key = f64_key(g_exact[g_list[i]]);
+            if (key > kappa) g_pick[g_list[i]] = 1;
+            else if (key == kappa && taken < rem64) { g_pick[g_list[i]] = 1; ++taken; }
+          }
+        }
+      }
+    }
+    cl_sync(c);
+    for (int wv = tid; wv < nwords; wv += blockDim.x) {
+      uint32_t bits = sm.band_bits[wv];
+      while (bits) {
+        int bp = __ffs(bits) - 1;
+        bits &= bits - 1;
+        if (g_pick[base + wv * 32 + bp]) atomicOr(&sm.sel_bits[wv], 1u << bp);
+      }
+    }
+  }
+  // ---- ordered output ------------------------------------------------------
+  uint32_t nsel = scan_words(sm, sm.sel_bits, nwords);
+  if (tid == 0) sm.cnt_sel = nsel;
+  cl_sync(c);
+  uint32_t off = 0;
+  for (int r = 0; r < c.rank; ++r) off += *remote(c, &sm.cnt_sel, r);
+  for (int wv = tid; wv < nwords; wv += blockDim.x) {
+    uint32_t bits = sm.sel_bits[wv], o = sm.word_off[wv];
+    while (bits) {
+      int bp = __ffs(bits) - 1;
+      bits &= bits - 1;
+      int64_t gi = base + wv * 32 + bp;
+      int64_t id = (kind == kBlocks) ? gi : int64_t(sm.pool_ids[gi >> 3]) * kBlock + (gi & 7);
+      if (off + o < k) out[off + o] = int32_t(id);
+      ++o;
+    }
+  }
+  cl_sync(c);     // no rank leaves while another still reads its counters
+}
+
+// Sum of one int per thread over the CTA (uses sm.red[1]).
+__device__ int64_t block_sum(SelSmem& sm, int v) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  __syncthreads();
+  if (lane == 0) sm.red[1][wid] = uint32_t(v);
+  __syncthreads();
+  int64_t t = 0;
+  for (int i = 0; i < kSelWarps; ++i) t += sm.red[1][i];
+  __syncthreads();
+  return t;
+}
+
+__device__ void load_query_factors(const IdxArgs& a, SelSmem& sm, int b) {
+  const int hi = a.d.idx_heads, di = a.d.idx_dim;
+  const bool fp8 = a.d.idx_k_dtype == CSA2_IDXK_E4M3;
+  if (threadIdx.x < kMaxIdxHeads) {
+    sm.q_elo[threadIdx.x] = INT_MAX;
+    sm.q_fast[threadIdx.x] = 1;
+    sm.q_l1[threadIdx.x] = 0;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < hi * di; i += blockDim.x) {
+    int h = i / di, ch = i % di;
+    int64_t qidx = int64_t(b) * hi * di + i;
+    float v = fp8 ? bf16_to_f32(reinterpret_cast<const uint16_t*>(a.idx_q)[qidx])
+                  : reinterpret_cast<const float*>(a.idx_q)[qidx];
+    Factor f = factor_f32(v);
+    sm.qf[ch * kMaxIdxHeads + h] = f;
+    if (f.sig) atomicMin(&sm.q_elo[h], f.exp + __ffs(abs(f.sig)) - 1);   // lowest set bit
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < hi * di; i += blockDim.x) {
+    int h = i / di, ch = i % di;
+    Factor f = sm.qf[ch * kMaxIdxHeads + h];
+    int32_t qv = 0;
+    if (f.sig) {
+      // q = sig * 2^exp = qv * 2^q_elo; sh < 0 only drops trailing zero bits
+      int sh = f.exp - sm.q_elo[h];
+      int mag = abs(f.sig);
+      int bits = 32 - __clz(mag) + sh;
+      if (bits > 30) {
+        atomicAnd(&sm.q_fast[h], 0);
+      } else {
+        mag = sh >= 0 ? (mag << sh) : (mag >> -sh);
+        qv = f.sig < 0 ? -mag : mag;
+        atomicAdd(&sm.q_l1[h], (unsigned long long)mag);
+      }
+    }
+    sm.qi[ch * kMaxIdxHeads + h] = qv;
+  }
+  if (threadIdx.x < hi) sm.w[threadIdx.x] = a.w[int64_t(b) * hi + threadIdx.x];
+  __syncthreads();
+  if (threadIdx.x < kMaxIdxHeads) {
+    // int64 room: sum_c |qi| * max|k*2^9| (448 * 512) must stay below 2^62
+    if (threadIdx.x >= hi || !fp8 || di != 128 || sm.q_l1[threadIdx.x] >= (1ull << 62) / 229376ull)
+      sm.q_fast[threadIdx.x] = 0;
+  }
+}
+
+// Full mode: pool over the cluster, then Top-K of the pool positions on rank
+// 0.  Reindex mode (cluster of 1): Top-K of the pool positions.
+__global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int cs, bool reindex) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
+  const int b = blockIdx.y;
+  SelCtx c;
+  c.b = b;
+  c.cs = cs;
+  c.rank = cs > 1 ? int(cg::this_cluster().block_rank()) : 0;
+  c.n_ctx = checked_ctx(a.ctx_len, a.d, b, a.page_table != nullptr, a.ws);
+  load_query_factors(a, sm, b);
+  const int64_t scap = a.L.sel_cap;
+  double* g_exact = reinterpret_cast<double*>(a.ws + a.L.sel_exact) + int64_t(b) * scap;
+  int32_t* g_list = reinterpret_cast<int32_t*>(a.ws + a.L.sel_list) + int64_t(b) * scap;
+  uint8_t* g_pick = a.ws + a.L.sel_pick + int64_t(b) * scap;
+  const int P = a.d.pool_blocks, K = a.d.topk;
+  __syncthreads();
+  int64_t nb = (c.n_ctx + kBlock - 1) / kBlock;
+  if (!reindex) {
+    int64_t p_sel = min64(P, nb);
+    int32_t* pool = a.pool_out + int64_t(b) * P;
+    certified_select(a, sm, c, kBlocks, nb, p_sel, pool, g_exact, g_list, g_pick);
+    if (c.rank != 0) return;
+    for (int i = threadIdx.x; i < P; i += blockDim.x)
+      if (i >= p_sel) pool[i] = -1;
+    if (threadIdx.x == 0) a.pool_len_out[b] = int32_t(p_sel);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kMaxPool; i += blockDim.x) sm.pool_ids[i] = i < p_sel ? pool[i] : -1;
+    __syncthreads();
+    SelCtx c1 = c;
+    c1.cs = 1;
+    c1.rank = 0;
+    // valid pool positions (the context's last block may be partial)
+    int has_last = __syncthreads_or(threadIdx.x < kMaxPool && threadIdx.x < p_sel &&
+                                    (sm.pool_ids[threadIdx.x] == nb - 1 ||
+                                     (threadIdx.x + 1024 < p_sel && sm.pool_ids[threadIdx.x + 1024] == nb - 1)));
+    int64_t npos = p_sel * kBlock - (has_last ? (nb * kBlock - c.n_ctx) : 0);
+    int64_t k_sel = min64(K, npos);
+    int32_t* tk = a.topk_out + int64_t(b) * K;
+    certified_select(a, sm, c1, kPoolPos, p_sel * kBlock, k_sel, tk, g_exact, g_list, g_pick);
+    for (int i = threadIdx.x; i < K; i += blockDim.x)
+      if (i >= k_sel) tk[i] = -1;
+  } else {
+    int32_t plen = a.pool_len_in[b];
+    if (plen < 0 || plen > P) { if (threadIdx.x == 0) raise_err(a.ws, CSA2_DEV_POOL); plen = 0; }
+    for (int i = threadIdx.x; i < kMaxPool; i += blockDim.x) {
+      int32_t blk = i < plen ? a.pool_in[int64_t(b) * P + i] : -1;
+      if (blk >= nb) { raise_err(a.ws, CSA2_DEV_POOL); blk = -1; }
+      sm.pool_ids[i] = blk;
+    }
+    __syncthreads();
+    int my = 0;
+    for (int i = threadIdx.x; i < plen; i += blockDim.x) {
+      int32_t blk = sm.pool_ids[i];
+      if (blk >= 0) my += int(min64(kBlock, c.n_ctx - int64_t(blk) * kBlock));
+    }
+    int64_t npos = block_sum(sm, my);
+    int64_t k_sel = min64(K, npos);
+    int32_t* tk = a.topk_out + int64_t(b) * K;
+    certified_select(a, sm, c, kReindexPos, int64_t(plen) * kBlock, k_sel, tk, g_exact, g_list, g_pick);
+    for (int i = threadIdx.x; i < K; i += blockDim.x)
+      if (i >= k_sel) tk[i] = -1;
+  }
+}
+
+cudaError_t launch_select(IdxArgs a, bool reindex, cudaStream_t st) {
+  int cs = reindex ? 1 : int((a.L.nb_max + kSelCapPerCta - 1) / kSelCapPerCta);
+  size_t smem = sizeof(SelSmem);
+  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(cs), unsigned(a.batch), 1);
+  cfg.blockDim = dim3(kSelThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  CSA2_PROFILED(st, reindex ? "select_reindex" : "select_full", (e = cudaLaunchKernelEx(&cfg, select_kernel, a, cs, reindex)));
+  return e;
+}
+
+size_t select_smem_bytes() { return sizeof(SelSmem); }
+
+}  // namespace csa2

@@ -197,7 +197,7 @@ csa2_status indexer_reindex_topk(const csa2_dims* d, int32_t batch,
  *   logit = scale * q[b][h] . key(e);  out = softmax-weighted sum of values;
  *   lse = max logit + ln(sum exp(logit - max)); empty E: out 0, lse -inf.
  *   mode: csa2_mode, informational (indices are always supplied).
- *   q:        device bf16 [B][H][576]
+ *   q:        device bf16 [B][H][576], 16-byte aligned
  *   kv_codes, kv_scales, kv_rope: device, layout above
  *   topk:     device int32 [B][K], -1 = padding
  *   swa_kv:   device bf16 [B][W][576];  swa_len: device int32 [B]
@@ -241,6 +241,20 @@ csa2_status csa2_sparse_attn_decode_noalloc(const csa2_dims* d, int32_t batch, i
                                             const int32_t* topk, const uint16_t* swa_kv,
                                             const int32_t* swa_len, float scale, float* out,
                                             float* lse, int32_t* err_word, void* stream);
+
+/* Kernel timing, a tracing aid.  While enabled, the library brackets every
+ * kernel it launches with a pair of CUDA events on the launching stream
+ * (not for use during stream capture).  Enabling (or disabling) clears the
+ * records.  csa2_profile_read waits for the recorded events and returns per
+ * kernel name the number of launches and their summed milliseconds in
+ * out[0 .. min(*n_entries, max_entries)), *n_entries = number of kernels. */
+typedef struct {
+  char name[32];
+  int32_t launches;
+  double total_ms;
+} csa2_kernel_time;
+csa2_status csa2_profile_enable(int32_t on);
+csa2_status csa2_profile_read(csa2_kernel_time* out, int32_t max_entries, int32_t* n_entries);
 
 /* Copies the device error word of `ws` to *word (synchronising `stream`)
  * and returns CSA2_OK if it is zero, CSA2_ERR_DEVICE_ASSERT otherwise. */
