@@ -173,7 +173,7 @@ csa2_status csa2_sparse_attn_decode(const csa2_dims* d, int32_t batch, int32_t m
   if (!q || !kv_codes || !kv_scales || !kv_rope || !ctx_len || !topk || !swa_len || !out || !lse)
     return CSA2_ERR_INVALID_ARG;
   if (d->swa > 0 && !swa_kv) return CSA2_ERR_INVALID_ARG;
-  if (!aligned(kv_codes, 8) || !aligned(kv_rope, 16) || !aligned(q, 16) || !aligned(out, 16) ||
+  if (!aligned(kv_codes, 16) || !aligned(kv_scales, 2) || !aligned(kv_rope, 16) || !aligned(q, 16) || !aligned(out, 16) ||
       (swa_kv && !aligned(swa_kv, 16)))
     return CSA2_ERR_INVALID_ARG;
   if (!(scale == scale)) return CSA2_ERR_INVALID_ARG;

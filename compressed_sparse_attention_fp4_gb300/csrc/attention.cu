@@ -27,6 +27,11 @@
 //   5. writes the chunk's unnormalised output and (max, sum) per head.
 // A combine kernel merges the chunks: o = sum_s e^(m_s - M) o_s / sum_s
 // e^(m_s - M) l_s, lse = M + ln(sum_s e^(m_s - M) l_s).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "profile.cuh"
@@ -34,7 +39,7 @@
 
 namespace csa2 {
 
-constexpr int kAttnThreads = 256;
+constexpr int kAttnThreads = 512;
 constexpr int kEntries = 128;                       // entries per CTA (= MMA M)
 constexpr int kQRows = 64;                          // MMA N (heads, zero padded)
 constexpr int kRegion = kEntries * 128;             // 64 channels x 128 entries, bytes
@@ -61,20 +66,23 @@ __device__ inline void st_shared_v4(uint8_t* base, uint32_t off, uint4 v) {
   *reinterpret_cast<uint4*>(base + off) = v;
 }
 
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_partial_tc_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_partial_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
+                           const __grid_constant__ CUtensorMap swamap, int swa_tma_split) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 128-byte swizzled operands need 1024-byte aligned regions
   uint8_t* kv_s = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);   // 9 x 16 KB
   uint8_t* q_s = kv_s + kKvBytes;                   // 9 regions x 8 KB; later P^T hi / lo
-  __shared__ uint64_t bar_s, bar_o;
+  __shared__ uint64_t bar_ld, bar_s, bar_o;
   __shared__ uint32_t tmem_slot;
   __shared__ int64_t row_s[kEntries];               // >= 0 main row, -2 - r SWA row r, -1 empty
-  __shared__ float red_m[2][4][32], red_l[2][4][32];
+  __shared__ float red_m[4][4][16], red_l[4][4][16];
 
   const int b = blockIdx.y, split = blockIdx.x;
   const int H = a.d.heads, K = a.d.topk, W = a.d.swa;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const bool paged = a.page_table != nullptr;
+  const bool swa_tma = split == swa_tma_split;      // this CTA's rows are the SWA window
   const int64_t n_ctx = checked_ctx(a.ctx_len, a.d, b, paged, a.ws);
   int swl = a.swa_len[b];
   if (swl < 0 || swl > W) {
@@ -100,6 +108,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_partial_tc_kernel(AttnAr
   }
   if (wid == 0) tc::tmem_alloc(&tmem_slot, kTmemCols);
   if (tid == 0) {
+    tc::mbar_init(&bar_ld, 1);
     tc::mbar_init(&bar_s, 1);
     tc::mbar_init(&bar_o, 1);
     tc::fence_mbar_init();
@@ -109,51 +118,87 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_partial_tc_kernel(AttnAr
   tc::tc_fence_after_sync();
   const uint32_t tmem = tmem_slot;
 
-  // ---- query -> swizzled smem (rows >= H are zero) -------------------------
-  const uint4* qg = reinterpret_cast<const uint4*>(a.q + int64_t(b) * H * kDqk);
-#pragma unroll 4
-  for (int i = tid; i < kQRows * 72; i += kAttnThreads) {
-    int h = i / 72, c = i % 72;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (h < H) v = __ldg(qg + h * 72 + c);
-    st_shared_v4(q_s, (c >> 3) * kQRegion + tc::sw128_offset(h, c & 7), v);
+  // ---- TMA: the query (9 boxes of 64 channels x 64 heads) and, for the
+  //      window's CTA, the SWA rows (9 boxes of 64 channels x 128 rows) ----------
+  if (tid == 0) {
+    tc::mbar_expect_tx(&bar_ld, uint32_t(kQBytes) + (swa_tma ? uint32_t(kKvBytes) : 0u));
+    for (int kb = 0; kb < 9; ++kb) tc::tma_load_2d(&qmap, q_s + kb * kQRegion, 64 * kb, b * H, &bar_ld);
+    if (swa_tma)
+      for (int kb = 0; kb < 9; ++kb) tc::tma_load_2d(&swamap, kv_s + kb * kRegion, 64 * kb, b * W, &bar_ld);
   }
-  // ---- entries -> dequantized bf16, swizzled smem ------------------------------
-#pragma unroll 2
-  for (int task = tid; task < kEntries * 36; task += kAttnThreads) {
-    const int e = task / 36, part = task % 36;      // 16 channels per part
-    const int64_t r = row_s[e];
-    const uint32_t region = part >> 2, ch0 = (part & 3) * 2;
-    const uint32_t o0 = region * kRegion + tc::sw128_offset(e, ch0);
-    const uint32_t o1 = region * kRegion + tc::sw128_offset(e, ch0 + 1);
-    uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
-    if (r >= 0) {
-      if (part < 32) {
-        uint2 cd = __ldg(reinterpret_cast<const uint2*>(a.codes + r * kCodesPerRow) + part);
-        float s = e4m3_to_f32(__ldg(a.scales + r * kScalesPerRow + part));
-        uint32_t cw[2] = {cd.x, cd.y};
+  // ---- FP4 entries: gather (all loads first), dequantize to bf16 -------------------
+  if (!swa_tma) {
+    // latent: task = (entry, pair of 16-channel groups); 4 tasks per thread
+    uint4 cd[4];
+    uint32_t sc[4];
+    int64_t rr[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int task = tid + k * kAttnThreads, e = task >> 4, gp = task & 15;
+      rr[k] = row_s[e];
+      cd[k] = make_uint4(0, 0, 0, 0);
+      sc[k] = 0;
+      if (rr[k] >= 0) {
+        cd[k] = __ldg(reinterpret_cast<const uint4*>(a.codes + rr[k] * kCodesPerRow) + gp);
+        sc[k] = __ldg(reinterpret_cast<const uint16_t*>(a.scales + rr[k] * kScalesPerRow) + gp);
+      }
+    }
+    // rope: task = (entry, 16-byte chunk); 2 tasks per thread
+    uint4 rp[2];
+    int64_t rr2[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int task = tid + k * kAttnThreads, e = task >> 3, rc = task & 7;
+      rr2[k] = row_s[e];
+      rp[k] = make_uint4(0, 0, 0, 0);
+      if (rr2[k] >= 0) rp[k] = __ldg(reinterpret_cast<const uint4*>(a.rope + rr2[k] * kRope) + rc);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int task = tid + k * kAttnThreads, e = task >> 4, gp = task & 15;
+      if (rr[k] <= -2) continue;                     // SWA row: copied below
+      uint32_t cw[4] = {cd[k].x, cd[k].y, cd[k].z, cd[k].w};
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {                  // two 16-channel groups
+        float s = e4m3_to_f32((sc[k] >> (8 * g)) & 0xFF);
         uint32_t w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          uint32_t h2 = e2m1x2_to_f16x2_a((cw[i >> 2] >> (8 * (i & 3))) & 0xFF);
+          uint32_t h2 = e2m1x2_to_f16x2_a((cw[2 * g + (i >> 2)] >> (8 * (i & 3))) & 0xFF);
           float lo = __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF))) * s;
           float hi = __half2float(__ushort_as_half(uint16_t(h2 >> 16))) * s;
           w[i] = pack_bf16x2(lo, hi);
         }
-        v0 = make_uint4(w[0], w[1], w[2], w[3]);
-        v1 = make_uint4(w[4], w[5], w[6], w[7]);
-      } else {
-        const uint4* rp = reinterpret_cast<const uint4*>(a.rope + r * kRope) + (part - 32) * 2;
-        v0 = __ldg(rp);
-        v1 = __ldg(rp + 1);
+        const int part = 2 * gp + g;                 // 16-channel group index 0..31
+        const uint32_t region = part >> 2, ch0 = (part & 3) * 2;
+        st_shared_v4(kv_s, region * kRegion + tc::sw128_offset(e, ch0), make_uint4(w[0], w[1], w[2], w[3]));
+        st_shared_v4(kv_s, region * kRegion + tc::sw128_offset(e, ch0 + 1), make_uint4(w[4], w[5], w[6], w[7]));
       }
-    } else if (r <= -2) {
-      const uint4* sp = reinterpret_cast<const uint4*>(a.swa + (int64_t(b) * W + (-2 - r)) * kDqk) + part * 2;
-      v0 = __ldg(sp);
-      v1 = __ldg(sp + 1);
     }
-    st_shared_v4(kv_s, o0, v0);
-    st_shared_v4(kv_s, o1, v1);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int task = tid + k * kAttnThreads, e = task >> 3, rc = task & 7;
+      if (rr2[k] <= -2) continue;
+      st_shared_v4(kv_s, 8 * kRegion + tc::sw128_offset(e, rc), rp[k]);
+    }
+    // SWA rows of a CTA the window does not start on a 128-row boundary for
+#pragma unroll 4
+    for (int task = tid; task < kEntries * 72; task += kAttnThreads) {
+      const int e = task / 72, c = task % 72;
+      const int64_t r = row_s[e];
+      if (r > -2) continue;
+      uint4 v = __ldg(reinterpret_cast<const uint4*>(a.swa + (int64_t(b) * W + (-2 - r)) * kDqk) + c);
+      st_shared_v4(kv_s, (c >> 3) * kRegion + tc::sw128_offset(e, c & 7), v);
+    }
+  }
+  bool ok = tc::mbar_wait_bounded(&bar_ld, 0);
+  if (swa_tma) {
+    // window rows past swa_len (or past W) are not entries: zero them so that
+    // P = 0 never meets a non-finite value
+    for (int task = tid; task < kEntries * 72; task += kAttnThreads) {
+      const int e = task / 72, c = task % 72;
+      if (row_s[e] == -1) st_shared_v4(kv_s, (c >> 3) * kRegion + tc::sw128_offset(e, c & 7), make_uint4(0, 0, 0, 0));
+    }
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before_sync();
@@ -173,41 +218,41 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_partial_tc_kernel(AttnAr
     }
     tc::mma_commit(&bar_s);
   }
-  bool ok = tc::mbar_wait_bounded(&bar_s, 0);
+  ok = tc::mbar_wait_bounded(&bar_s, 0) && ok;
   tc::tc_fence_after_sync();
 
   // ---- softmax over the 128 entries (TMEM lanes) ------------------------------
-  const int quarter = wid & 3, half = wid >> 2;     // lanes 32*quarter.., heads 32*half..
+  const int quarter = wid & 3, hg = wid >> 2;       // lanes 32*quarter.., heads 16*hg..
   const int e = quarter * 32 + lane;
   const bool valid = row_s[e] != -1;
-  float x[32];
-  tc::tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(half * 32), x);
+  float x[16];
+  tc::tmem_ld16(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(hg * 16), x);
   const float c2 = a.scale * 1.4426950408889634f;   // logits in base 2
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
+  for (int j = 0; j < 16; ++j) {
     x[j] = valid ? x[j] * c2 : -INFINITY;
     float m = x[j];
 #pragma unroll
     for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if (lane == 0) red_m[half][quarter][j] = m;
+    if (lane == 0) red_m[hg][quarter][j] = m;
   }
   __syncthreads();
-  float p[32];
+  float p[16];
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    float M = fmaxf(fmaxf(red_m[half][0][j], red_m[half][1][j]), fmaxf(red_m[half][2][j], red_m[half][3][j]));
+  for (int j = 0; j < 16; ++j) {
+    float M = fmaxf(fmaxf(red_m[hg][0][j], red_m[hg][1][j]), fmaxf(red_m[hg][2][j], red_m[hg][3][j]));
     p[j] = (M == -INFINITY || x[j] == -INFINITY) ? 0.0f : exp2f(x[j] - M);
     float l = p[j];
 #pragma unroll
     for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
-    if (lane == 0) red_l[half][quarter][j] = l;
+    if (lane == 0) red_l[hg][quarter][j] = l;
   }
-  // P^T rows (entry e): heads 32*half.. as 4 chunks, hi and lo bf16 parts.
+  // P^T rows (entry e): heads 16*hg.. as 2 chunks, hi and lo bf16 parts.
   // The query buffer is free: the S^T MMAs completed (bar_s) before this.
   uint8_t* p_hi = q_s;
   uint8_t* p_lo = q_s + kRegion;
 #pragma unroll
-  for (int t = 0; t < 4; ++t) {
+  for (int t = 0; t < 2; ++t) {
     uint32_t wh[4], wl[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -217,7 +262,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_partial_tc_kernel(AttnAr
       wh[i] = hb;
       wl[i] = pack_bf16x2(v0 - h0, v1 - h1);
     }
-    uint32_t off = tc::sw128_offset(e, half * 4 + t);
+    uint32_t off = tc::sw128_offset(e, hg * 2 + t);
     st_shared_v4(p_hi, off, make_uint4(wh[0], wh[1], wh[2], wh[3]));
     st_shared_v4(p_lo, off, make_uint4(wl[0], wl[1], wl[2], wl[3]));
   }
@@ -226,11 +271,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_partial_tc_kernel(AttnAr
   __syncthreads();
   float* ml_base = reinterpret_cast<float*>(a.ws + a.L.attn_ml);
   const int64_t prow = (int64_t(b) * a.L.splits + split) * H;
-  if (quarter == 0) {
-    int h = half * 32 + lane;
+  if (quarter == 0 && lane < 16) {
+    int h = hg * 16 + lane;
     if (h < H) {
-      float M = fmaxf(fmaxf(red_m[half][0][lane], red_m[half][1][lane]), fmaxf(red_m[half][2][lane], red_m[half][3][lane]));
-      float L = red_l[half][0][lane] + red_l[half][1][lane] + red_l[half][2][lane] + red_l[half][3][lane];
+      float M = fmaxf(fmaxf(red_m[hg][0][lane], red_m[hg][1][lane]), fmaxf(red_m[hg][2][lane], red_m[hg][3][lane]));
+      float L = red_l[hg][0][lane] + red_l[hg][1][lane] + red_l[hg][2][lane] + red_l[hg][3][lane];
       ml_base[(prow + h) * 2] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
       ml_base[(prow + h) * 2 + 1] = L;
     }
@@ -263,12 +308,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_partial_tc_kernel(AttnAr
   float* o_base = reinterpret_cast<float*>(a.ws + a.L.attn_o);
 #pragma unroll 1
   for (int mt = 0; mt < 4; ++mt) {
-    float o[32];
-    tc::tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(64 + 64 * mt + half * 32), o);
+    float o[16];
+    tc::tmem_ld16(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(64 + 64 * mt + hg * 16), o);
     const int dim = mt * 128 + quarter * 32 + lane;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      int h = half * 32 + j;
+    for (int j = 0; j < 16; ++j) {
+      int h = hg * 16 + j;
       if (h < H) o_base[(prow + h) * kLatent + dim] = o[j];
     }
   }
@@ -304,13 +349,50 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
 
 size_t attn_smem_bytes(int) { return size_t(kKvBytes) + size_t(kQBytes) + 1024; }
 
+static PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [rows][576] bf16 rows of 1152 bytes, boxes of 64 channels x box_rows.
+static bool encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto fn = attn_encode_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[2] = {uint64_t(kDqk), rows};
+  cuuint64_t gstride[1] = {uint64_t(kDqk) * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
+  CUtensorMap qmap, swamap;
+  if (!encode_rows_map(&qmap, a.q, uint64_t(a.batch) * a.d.heads, kQRows)) return cudaErrorInvalidValue;
+  // the window is loaded by TMA when it starts a 128-entry split
+  int swa_split = -1;
+  if (a.d.swa > 0 && a.d.swa <= kEntries && a.d.topk % kEntries == 0) swa_split = a.d.topk / kEntries;
+  swamap = qmap;
+  if (swa_split >= 0 &&
+      !encode_rows_map(&swamap, a.swa, uint64_t(a.batch) * a.d.swa, kEntries))
+    return cudaErrorInvalidValue;
   size_t smem = attn_smem_bytes(a.d.heads);
   cudaError_t e = cudaFuncSetAttribute(attn_partial_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   CSA2_PROFILED(st, "attn_partial_tc",
-                (attn_partial_tc_kernel<<<dim3(unsigned(a.L.splits), unsigned(a.batch)), kAttnThreads, smem, st>>>(a)));
+                (attn_partial_tc_kernel<<<dim3(unsigned(a.L.splits), unsigned(a.batch)), kAttnThreads, smem, st>>>(
+                    a, qmap, swamap, swa_split)));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CSA2_PROFILED(st, "attn_combine", (attn_combine_kernel<<<dim3(unsigned(a.d.heads), unsigned(a.batch)), 128, 0, st>>>(a)));

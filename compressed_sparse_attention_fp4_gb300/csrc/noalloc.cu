@@ -85,7 +85,7 @@ extern "C" csa2_status csa2_sparse_attn_decode_noalloc(
   if (!q || !kv_codes || !kv_scales || !kv_rope || !ctx_len || !topk || !swa_len || !out || !lse)
     return CSA2_ERR_INVALID_ARG;
   if (d->swa > 0 && !swa_kv) return CSA2_ERR_INVALID_ARG;
-  if (!is_aligned(kv_codes, 8) || !is_aligned(kv_rope, 16) || !is_aligned(q, 16) ||
+  if (!is_aligned(kv_codes, 16) || !is_aligned(kv_scales, 2) || !is_aligned(kv_rope, 16) || !is_aligned(q, 16) ||
       !is_aligned(out, 16) || (swa_kv && !is_aligned(swa_kv, 16)) ||
       (err_word && !is_aligned(err_word, 4)))
     return CSA2_ERR_INVALID_ARG;

@@ -63,17 +63,10 @@ struct ScanSmem {
 };
 
 __device__ inline void tma_load_box(const CUtensorMap* map, uint8_t* dst, int32_t row, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(tc::smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row),
-        "r"(tc::smem_u32(bar))
-      : "memory");
+  tc::tma_load_2d(map, dst, 0, row, bar);
 }
 
-__device__ inline void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
+__device__ inline void mbar_expect_tx(uint64_t* bar, uint32_t bytes) { tc::mbar_expect_tx(bar, bytes); }
 
 __device__ inline void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(

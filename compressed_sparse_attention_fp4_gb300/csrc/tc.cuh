@@ -50,6 +50,22 @@ __device__ inline bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
   }
 }
 
+// ---- TMA ------------------------------------------------------------------------
+// Arrive on `bar` and add `bytes` to the transaction count it waits for.
+__device__ inline void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// 2D tiled tensor load (coordinates: x = innermost element index, y = row),
+// completing on `bar`.  `map` is a kernel parameter (generic address).
+__device__ inline void tma_load_2d(const void* map, void* dst, int32_t x, int32_t y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---- proxies ------------------------------------------------------------------
 // Generic-proxy shared-memory writes become visible to the tensor cores.
 __device__ inline void fence_proxy_async_smem() {

@@ -198,7 +198,8 @@ csa2_status indexer_reindex_topk(const csa2_dims* d, int32_t batch,
  *   lse = max logit + ln(sum exp(logit - max)); empty E: out 0, lse -inf.
  *   mode: csa2_mode, informational (indices are always supplied).
  *   q:        device bf16 [B][H][576], 16-byte aligned
- *   kv_codes, kv_scales, kv_rope: device, layout above
+ *   kv_codes, kv_scales, kv_rope: device, layout above (16-, 2- and
+ *             16-byte aligned)
  *   topk:     device int32 [B][K], -1 = padding
  *   swa_kv:   device bf16 [B][W][576];  swa_len: device int32 [B]
  *   out:      device fp32 [B][H][512];  lse: device fp32 [B][H]
