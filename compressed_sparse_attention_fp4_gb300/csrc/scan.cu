@@ -5,23 +5,34 @@
 //   d_{t,h} = q_h . k_t,  s_t = sum_h w_h ReLU(d_{t,h}),  bs_j = max over block j,
 // and a rigorous bound delta_j >= |s_t - v_t| for the approximate v_t.
 //
-// Work: persistent CTAs walk contiguous ranges of 128-position tiles.
-//   * TMA (tensor map, 128-byte swizzle) streams each tile's 128 x 128 B of
-//     E4M3 keys into a 4-stage shared-memory ring.
-//   * 8 warps convert the keys to f16 (exact: E4M3 is a subset of f16) and
-//     store them into tensor memory as the MMA's A operand, together with
-//     their absolute values |A|.
-//   * One thread issues D = A . Qf^T and D2 = |A| . |Qf|^T (M=128 positions,
-//     N=16 heads, K=128, f16 in, fp32 accumulation).  Qf = q_h * 2^e_h in f16,
-//     with a per-head power of two e_h so that every bf16 query element lands
-//     in f16's exact range (the rare element that does not is counted in the
-//     bound).
-//   * The epilogue reads D and D2 from tensor memory: v_t = sum_h w'_h
-//     ReLU(D_h) with w'_h = w_h 2^-e_h, and delta_t = C * sum_h |w'_h| D2_h
-//     + (query rounding term), C covering the tensor-core accumulation error
-//     (modelled as at most 2^-14 of sum|products| per head dot), the fp32
-//     head sum and the fp64 rounding of the exact score.  Block max of v and
-//     delta over 8 positions are written with the position scores.
+// The MMAs take the E4M3 keys exactly as they sit in the cache
+// (kind::f8f6f4, E4M3 x E4M3, fp32 accumulation in tensor memory); nothing
+// converts them.  The bf16 query is split exactly into two E4M3 pieces per
+// head, Qs = q_h 2^e_h = q1 + r1 (e_h puts max |q_h| 2^e_h in [2^7, 2^8); q1 is
+// the E4M3 rounding of Qs and r1 the remainder, which has at most 4
+// significant bits and is exact in E4M3 unless it falls below 2^-9 -- that
+// rare loss is counted in the bound).
+//
+// Work: one persistent CTA per SM walks a contiguous range of 128-position
+// tiles; its warps specialise and hand tiles on through mbarriers, so the
+// key stream, the MMAs and the epilogue of consecutive tiles overlap:
+//   * warp 0 (one thread): TMA (tensor map, 128-byte swizzle = the MMA's
+//     K-major operand layout) streams each tile's 128 x 128 B of keys into a
+//     6-stage shared-memory ring.
+//   * warps 2-5 write |k| (sign bits cleared) of each tile into one of two
+//     buffers, and rebuild the query operands when a new sequence starts.
+//   * warp 1 (one thread) issues D = K . [q1; r1]^T (M=128 positions, N=32)
+//     and D2 = |K| . ceil(|Qs|)^T (N=16; ceil = the E4M3 value at or above),
+//     K=128 in 4 steps each, into one of two tensor-memory buffers; its
+//     commits free the ring stage, the |k| buffer and hand D to
+//   * warps 6-9, the epilogue: v_t = sum_h w'_h ReLU(D_h + D_{16+h}) with
+//     w'_h = w_h 2^-e_h, and delta_t = C sum_h |w'_h| D2_h + (query rounding
+//     term).  C covers the tensor-core accumulation: modelled as at most
+//     2^-16 of sum|products| per head dot (each product truncated to 2^-23 of
+//     the largest in its step, 128 products), taken with a factor-4 margin
+//     (2^-14; the worst observed on adversarial operands is 2^-18.8), plus the
+//     fp32 head sum and the fp64 rounding of the exact score.  Block max of v
+//     and delta over 8 positions are written with the position scores.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -35,76 +46,61 @@
 
 namespace csa2 {
 
-constexpr int kScanThreads = 256;
+constexpr int kScanThreads = 320;          // warp 0 TMA, 1 MMA, 2-5 |k| + query, 6-9 epilogue
+constexpr int kGroupThreads = 128;         // threads of the |k| group and of the epilogue group
 constexpr int kTile = 128;                 // positions per tile (= MMA M)
-constexpr int kStages = 4;                 // TMA ring depth
+constexpr int kStages = 6;                 // TMA ring depth
 constexpr int kStageBytes = kTile * 128;   // 16 KB of E4M3 keys
-constexpr uint32_t kScanTmemCols = 256;
-// tensor-memory columns
-constexpr uint32_t kColA = 0, kColAbs = 64, kColD = 128;   // D[buf] at 128 + 32 buf, D2 at +16
-
-// Error-model constant of the tensor-core scores (see file comment).
+constexpr uint32_t kScanTmemCols = 128;    // D buffer j: cols 64j .. 64j+31, D2: 64j+32 .. 64j+47
 constexpr float kTcErr = 6.3e-5f;          // 2^-14 + 2^-19 + fp64 rounding, rounded up
 
 struct ScanSmem {
-  uint8_t stage[kStages][kStageBytes];     // 1024-aligned (swizzle atoms)
-  uint8_t qf[2][16 * 128];                 // f16 query [16 heads][128], 2 regions of 64 ch
-  uint8_t qa[2][16 * 128];                 // |query|, same layout
-  uint64_t full[kStages];
-  uint64_t dbar[2];
+  uint8_t stage[kStages][kStageBytes];     // keys, 1024-aligned (swizzle atoms)
+  uint8_t kabs[2][kStageBytes];            // |keys|, same layout
+  uint8_t qp[32 * 128];                    // B of D: rows 0-15 q1 (head h), 16-31 r1
+  uint8_t qa[16 * 128];                    // B of D2: ceil(|Qs|)
+  uint64_t full[kStages], empty[kStages];
+  uint64_t a_full[2], a_empty[2], d_full[2], d_empty[2];
   uint32_t tmem_slot;
-  int32_t cur_b;
-  float wq[kMaxIdxHeads];                  // w_h * 2^-e_h
+  float qmax[2][kMaxIdxHeads];             // [group]: per-head max |q|
+  float qerr[2][kMaxIdxHeads];             // [group]: per-head sum of split errors
+  float wq[kMaxIdxHeads];                  // epilogue: w_h 2^-e_h
   float wq_abs[kMaxIdxHeads];
-  float qmax_bits[kMaxIdxHeads];
-  float qerr[kMaxIdxHeads];
   float q_extra;
-  int32_t abort_flag;
+  volatile int32_t abort_flag;
 };
 
-__device__ inline void tma_load_box(const CUtensorMap* map, uint8_t* dst, int32_t row, uint64_t* bar) {
-  tc::tma_load_2d(map, dst, 0, row, bar);
-}
-
-__device__ inline void mbar_expect_tx(uint64_t* bar, uint32_t bytes) { tc::mbar_expect_tx(bar, bytes); }
-
-__device__ inline void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
-      ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
-        "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-        "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
-        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
-        "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
-
-// D (+)= A[tmem] . B[smem]^T
-__device__ inline void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                  bool accumulate) {
+__device__ inline void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, bool accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(uint32_t(accumulate))
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(uint32_t(accumulate))
       : "memory");
 }
 
-// f16 A and B, fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+// kind::f8f6f4 with E4M3 A and B (format code 0), fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
   return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+__device__ inline uint32_t e4m3_rn(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+  return uint32_t(r) & 0xFF;
+}
+
+__device__ inline float e4m3_val(uint32_t code) {
+  uint32_t h2 = e4m3x2_to_f16x2(uint16_t(code));
+  return __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF)));
 }
 
 struct TileRef {
   int b;
-  int64_t t0;        // first position
-  int nvalid;        // valid positions in the tile
+  int64_t t0;        // first item
+  int nvalid;        // valid items in the tile
 };
 
-// Global tile g -> (sequence, first position); tiles of sequence b are
-// ceil(N_b / 128).  Linear walk from a hint (tiles are visited in order).
 // Items of sequence b: its positions (Full) or its pool positions, 8 per pool
 // block (Reindex).
 __device__ inline int64_t scan_items(const IdxArgs& a, int b, bool reindex) {
@@ -118,6 +114,8 @@ __device__ inline int64_t scan_items(const IdxArgs& a, int b, bool reindex) {
   return n;
 }
 
+// Global tile g -> (sequence, first item); tiles of sequence b are
+// ceil(items_b / 128).  Linear walk from a hint (tiles are visited in order).
 __device__ inline TileRef tile_of(const IdxArgs& a, bool reindex, int64_t g, int& hint_b,
                                   int64_t& hint_base) {
   while (true) {
@@ -151,9 +149,9 @@ __device__ inline void issue_tile_load(const IdxArgs& a, bool reindex, const CUt
       rows[j] = int32_t(row);
       if (row >= 0) bytes += kBlock * 128;
     }
-    mbar_expect_tx(&sm.full[stage], bytes);
+    tc::mbar_expect_tx(&sm.full[stage], bytes);
     for (int j = 0; j < nblk; ++j)
-      if (rows[j] >= 0) tma_load_box(map, sm.stage[stage] + j * kBlock * 128, rows[j], &sm.full[stage]);
+      if (rows[j] >= 0) tc::tma_load_2d(map, sm.stage[stage] + j * kBlock * 128, 0, rows[j], &sm.full[stage]);
     return;
   }
   uint32_t bytes = 0;
@@ -165,74 +163,109 @@ __device__ inline void issue_tile_load(const IdxArgs& a, bool reindex, const CUt
     rows[h] = int32_t(row);
     if (row >= 0) bytes += 64 * 128;
   }
-  mbar_expect_tx(&sm.full[stage], bytes);
+  tc::mbar_expect_tx(&sm.full[stage], bytes);
   for (int h = 0; h < nbox; ++h)
-    if (rows[h] >= 0) tma_load_box(map, sm.stage[stage] + h * 64 * 128, rows[h], &sm.full[stage]);
+    if (rows[h] >= 0) tc::tma_load_2d(map, sm.stage[stage] + h * 64 * 128, 0, rows[h], &sm.full[stage]);
 }
 
-// Per-sequence query operands: Qf = q * 2^e_h (f16) and |Qf|, 128-byte
-// swizzled K-major (16 rows, 2 regions of 64 channels); the weights
-// w'_h = w_h 2^-e_h; and the query-rounding term of the bound.
-__device__ void build_query(const IdxArgs& a, ScanSmem& sm, int b) {
-  const int tid = threadIdx.x, hi = a.d.idx_heads;
-  if (tid < kMaxIdxHeads) { sm.qmax_bits[tid] = 0.0f; sm.qerr[tid] = 0.0f; }
-  __syncthreads();
-  const int h = tid >> 4, c0 = (tid & 15) * 8;            // 16 heads x 16 chunks of 8 channels
-  float qv[8];
+__device__ inline void group_sync(int id) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kGroupThreads) : "memory");
+}
+
+__device__ inline int head_shift(float qm) { return qm > 0.0f ? max(-60, min(60, 7 - ilogbf(qm))) : 0; }
+
+// Per-sequence query split, run by one 128-thread group (gt = 0..127; thread
+// gt owns head gt/8, channels 16*(gt%8) .. +15; named barrier `bar_id`):
+//   e_h: max |q_h| 2^e_h in [2^7, 2^8);  Qs = q 2^e_h = q1 + r1 (E4M3 pieces);
+//   err_h = sum_c |Qs - q1 - r1| (nonzero only where r1 underflows E4M3).
+// The |k| group (operands = true) writes q1, r1 and ceil(|Qs|) as the
+// 128-byte swizzled K-major B operands; the epilogue group derives
+// w'_h = w_h 2^-e_h and the query rounding term 448 sum_h |w'_h| err_h.
+__device__ void query_split(const IdxArgs& a, ScanSmem& sm, int b, int gt, bool operands, int bar_id) {
+  const int hi = a.d.idx_heads;
+  const int grp = operands ? 0 : 1;
+  if (gt < kMaxIdxHeads) { sm.qmax[grp][gt] = 0.0f; sm.qerr[grp][gt] = 0.0f; }
+  group_sync(bar_id);
+  const int h = gt >> 3, c0 = (gt & 7) * 16;
+  float qv[16];
   float mx = 0.0f;
+  const uint16_t* qrow = reinterpret_cast<const uint16_t*>(a.idx_q) + (int64_t(b) * hi + h) * 128 + c0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    qv[i] = h < hi ? bf16_to_f32(reinterpret_cast<const uint16_t*>(a.idx_q)[(int64_t(b) * hi + h) * 128 + c0 + i]) : 0.0f;
+  for (int i = 0; i < 16; ++i) {
+    qv[i] = h < hi ? bf16_to_f32(qrow[i]) : 0.0f;
     mx = fmaxf(mx, fabsf(qv[i]));
   }
-  atomicMax(reinterpret_cast<int*>(&sm.qmax_bits[h]), __float_as_int(mx));
-  __syncthreads();
-  float qm = sm.qmax_bits[h];
-  int e = 0;
-  if (qm > 0.0f) e = 14 - ilogbf(qm);                      // max |q| * 2^e in [2^14, 2^15)
-  uint32_t wf[4], wa[4];
+  atomicMax(reinterpret_cast<int*>(&sm.qmax[grp][h]), __float_as_int(mx));
+  group_sync(bar_id);
+  const int e = head_shift(sm.qmax[grp][h]);
+  uint32_t w1[4] = {0, 0, 0, 0}, w2[4] = {0, 0, 0, 0}, wa[4] = {0, 0, 0, 0};
   float err = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float x0 = ldexpf(qv[2 * i], e), x1 = ldexpf(qv[2 * i + 1], e);
-    __half2 hv = __floats2half2_rn(x0, x1);
-    err = __fadd_ru(err, fabsf(__low2float(hv) - x0));
-    err = __fadd_ru(err, fabsf(__high2float(hv) - x1));
-    wf[i] = *reinterpret_cast<uint32_t*>(&hv);
-    wa[i] = wf[i] & 0x7FFF7FFFu;
+  for (int i = 0; i < 16; ++i) {
+    const float x = ldexpf(qv[i], e);                     // exact: a power-of-two scaling
+    const uint32_t c1 = e4m3_rn(x);
+    const float d1 = e4m3_val(c1);
+    const float r = x - d1;                                // exact
+    const uint32_t c2 = e4m3_rn(r);
+    const float d2 = e4m3_val(c2);
+    err = __fadd_ru(err, fabsf(r - d2));                   // r - d2 exact
+    uint32_t ca = e4m3_rn(fabsf(x));
+    if (e4m3_val(ca) < fabsf(x) && ca < 0x7Eu) ++ca;       // next larger E4M3 magnitude
+    w1[i >> 2] |= c1 << (8 * (i & 3));
+    w2[i >> 2] |= c2 << (8 * (i & 3));
+    wa[i >> 2] |= ca << (8 * (i & 3));
   }
-  const uint32_t region = c0 >> 6, chunk = (c0 & 63) >> 3;
-  const uint32_t off = tc::sw128_offset(h, chunk);
-  *reinterpret_cast<uint4*>(sm.qf[region] + off) = make_uint4(wf[0], wf[1], wf[2], wf[3]);
-  *reinterpret_cast<uint4*>(sm.qa[region] + off) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-  if (err > 0.0f) atomicAdd(&sm.qerr[h], err);
-  __syncthreads();
-  if (tid < kMaxIdxHeads) {
-    float w = tid < hi ? a.w[int64_t(b) * hi + tid] : 0.0f;
-    float qm2 = sm.qmax_bits[tid];
-    int e2 = qm2 > 0.0f ? 14 - ilogbf(qm2) : 0;
-    sm.wq[tid] = ldexpf(w, -e2);
-    sm.wq_abs[tid] = fabsf(sm.wq[tid]);
+  if (operands) {
+    const uint32_t chunk = uint32_t(c0 >> 4);
+    *reinterpret_cast<uint4*>(sm.qp + tc::sw128_offset(h, chunk)) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+    *reinterpret_cast<uint4*>(sm.qp + tc::sw128_offset(16 + h, chunk)) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+    *reinterpret_cast<uint4*>(sm.qa + tc::sw128_offset(h, chunk)) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+    tc::fence_proxy_async_smem();
+  } else if (err > 0.0f) {
+    atomicAdd(&sm.qerr[grp][h], err);
   }
-  __syncthreads();
-  if (tid == 0) {
-    // |Qf - q 2^e| summed per head, times the largest E4M3 magnitude
-    float x = 0.0f;
-    for (int i = 0; i < hi; ++i) x = __fmaf_ru(sm.wq_abs[i], __fmul_ru(sm.qerr[i], 1.001f), x);
-    sm.q_extra = __fmul_ru(x, 448.0f);
-    sm.cur_b = b;
+  group_sync(bar_id);
+  if (!operands) {
+    if (gt < kMaxIdxHeads) {
+      const float w = gt < hi ? a.w[int64_t(b) * hi + gt] : 0.0f;
+      sm.wq[gt] = ldexpf(w, -head_shift(sm.qmax[grp][gt]));
+      sm.wq_abs[gt] = fabsf(sm.wq[gt]);
+    }
+    group_sync(bar_id);
+    if (gt == 0) {
+      float x = 0.0f;
+      for (int i = 0; i < hi; ++i) x = __fmaf_ru(sm.wq_abs[i], __fmul_ru(sm.qerr[grp][i], 1.001f), x);
+      sm.q_extra = __fmul_ru(x, 448.0f);
+    }
+    group_sync(bar_id);
   }
-  tc::fence_proxy_async_smem();
-  __syncthreads();
 }
 
-// Epilogue of one tile for the thread owning row r (warps of half 0): scores,
-// bounds, block maxima, writes.
+// Bounded wait that also gives up once another role has aborted.
+__device__ inline bool wait_or_abort(ScanSmem& sm, uint64_t* bar, uint32_t parity) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = tc::globaltimer_ns();
+  while (true) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if (sm.abort_flag) return false;
+    if (tc::globaltimer_ns() - t0 > 200ull * 1000 * 1000) {
+      sm.abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ inline void arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+
+// Epilogue of one tile for the thread owning row r: scores, bounds, block
+// maxima, writes.
 __device__ inline void scan_epilogue(const IdxArgs& a, bool reindex, const ScanSmem& sm,
                                      const TileRef& pt, uint32_t tmem_d, int r, int lane) {
-  float dv[16], d2[16];
-  tc::tmem_ld16(tmem_d, dv);
-  tc::tmem_ld16(tmem_d + 16, d2);
+  float dv[32], d2[16];
+  tc::tmem_ld32(tmem_d, dv);
+  tc::tmem_ld16(tmem_d + 32, d2);
   bool valid = r < pt.nvalid;
   if (reindex && valid) {
     const bool paged = a.page_table != nullptr;
@@ -245,7 +278,7 @@ __device__ inline void scan_epilogue(const IdxArgs& a, bool reindex, const ScanS
   float v = 0.0f, bnd = 0.0f;
 #pragma unroll
   for (int h = 0; h < 16; ++h) {
-    v = __fmaf_rn(sm.wq[h], fmaxf(dv[h], 0.0f), v);
+    v = __fmaf_rn(sm.wq[h], fmaxf(dv[h] + dv[16 + h], 0.0f), v);
     bnd = __fmaf_ru(sm.wq_abs[h], d2[h], bnd);
   }
   float delta = __fadd_ru(__fmul_ru(__fmul_ru(bnd, 1.0003f), kTcErr), sm.q_extra);
@@ -273,14 +306,15 @@ __device__ inline void scan_epilogue(const IdxArgs& a, bool reindex, const ScanS
   }
 }
 
-__global__ void __launch_bounds__(kScanThreads, 2)
+__device__ inline uint32_t parity_of(int64_t k, int n) { return uint32_t((k / n) & 1); }
+
+__global__ void __launch_bounds__(kScanThreads, 1)
     scan_tc_kernel(IdxArgs a, const __grid_constant__ CUtensorMap kmap, bool reindex) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   ScanSmem& sm = *reinterpret_cast<ScanSmem*>(
       smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u));
   __shared__ int64_t total_tiles_s;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int quarter = wid & 3, half = wid >> 2;
   // ---- tiles of all sequences, this CTA's contiguous share ----------------------
   if (wid == 0) {
     int64_t tsum = 0;
@@ -297,109 +331,123 @@ __global__ void __launch_bounds__(kScanThreads, 2)
 
   if (wid == 0) tc::tmem_alloc(&sm.tmem_slot, kScanTmemCols);
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) tc::mbar_init(&sm.full[s], 1);
-    tc::mbar_init(&sm.dbar[0], 1);
-    tc::mbar_init(&sm.dbar[1], 1);
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&sm.full[s], 1);
+      tc::mbar_init(&sm.empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&sm.a_full[i], 4);
+      tc::mbar_init(&sm.a_empty[i], 1);
+      tc::mbar_init(&sm.d_full[i], 1);
+      tc::mbar_init(&sm.d_empty[i], 4);
+    }
     tc::fence_mbar_init();
-    sm.cur_b = -1;
     sm.abort_flag = 0;
   }
   tc::tc_fence_before_sync();
   __syncthreads();
   tc::tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_slot;
-  constexpr uint32_t idesc = idesc_f16(kTile, 16);
-  const int r = quarter * 32 + lane;                 // this thread's row of the tile
-  const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+  const int64_t ntiles = g1 - g0;
 
-  // producer (thread 0): the first kStages tiles
-  int pb = 0;
-  int64_t pbase = 0, next_load = g0;
-  if (tid == 0) {
-    for (int s = 0; s < kStages && next_load < g1; ++s, ++next_load)
-      issue_tile_load(a, reindex, &kmap, sm, tile_of(a, reindex, next_load, pb, pbase), s);
-  }
-  int cb = 0;
-  int64_t cbase = 0;
-  TileRef prev = {0, 0, 0};
-  bool pending = false;
-  int64_t k = 0;
-  for (int64_t g = g0; g < g1; ++g, ++k) {
-    const TileRef tr = tile_of(a, reindex, g, cb, cbase);
-    const int stage = int(k % kStages);
-    const uint32_t buf = uint32_t(k & 1);
-    // ---- this thread's 64 channels of its row, E4M3 -> f16 (exact) ----------
-    if (!tc::mbar_wait_bounded(&sm.full[stage], uint32_t((k / kStages) & 1))) sm.abort_flag = 1;
-    uint32_t af[32], aa[32];
-    const uint8_t* srow = sm.stage[stage] + r * 128;
+  if (wid == 0) {
+    // ================= producer: TMA ring =================
+    if (lane == 0) {
+      int pb = 0;
+      int64_t pbase = 0;
+      int64_t k = 0;
+      for (; k < ntiles; ++k) {
+        const int stage = int(k % kStages);
+        if (k >= kStages && !wait_or_abort(sm, &sm.empty[stage], parity_of(k - kStages, kStages))) break;
+        issue_tile_load(a, reindex, &kmap, sm, tile_of(a, reindex, g0 + k, pb, pbase), stage);
+      }
+      // after an abort, let the copies still in flight land before the CTA exits
+      if (sm.abort_flag)
+        for (int64_t j = max64(0, k - kStages); j < k; ++j)
+          tc::mbar_wait_bounded(&sm.full[j % kStages], parity_of(j, kStages), 20ull * 1000 * 1000);
+    }
+  } else if (wid == 1) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      constexpr uint32_t id_d = idesc_e4m3(kTile, 32), id_d2 = idesc_e4m3(kTile, 16);
+      const uint32_t qp0 = tc::smem_u32(sm.qp), qa0 = tc::smem_u32(sm.qa);
+      int64_t issued = 0;
+      for (int64_t k = 0; k < ntiles; ++k) {
+        const int stage = int(k % kStages);
+        const uint32_t buf = uint32_t(k & 1);
+        if (!wait_or_abort(sm, &sm.a_full[buf], parity_of(k, 2))) break;
+        if (!wait_or_abort(sm, &sm.full[stage], parity_of(k, kStages))) break;
+        if (k >= 2 && !wait_or_abort(sm, &sm.d_empty[buf], parity_of(k - 2, 2))) break;
+        tc::tc_fence_after_sync();
+        const uint32_t k0 = tc::smem_u32(sm.stage[stage]), ka0 = tc::smem_u32(sm.kabs[buf]);
+        const uint32_t dcol = tmem + 64 * buf;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t c = half * 4 + j;
-      uint4 v = *reinterpret_cast<const uint4*>(srow + ((c ^ (uint32_t(r) & 7u)) << 4));
-      uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-          uint32_t f = e4m3x2_to_f16x2(uint16_t(w4[i] >> (16 * p)));
-          af[j * 8 + i * 2 + p] = f;
-          aa[j * 8 + i * 2 + p] = f & 0x7FFF7FFFu;
+        for (int ks = 0; ks < 4; ++ks) {                 // K = 32 E4M3 (32 bytes) per step
+          mma_f8(dcol, tc::smem_desc(k0 + 32 * ks, 16, 1024, 2), tc::smem_desc(qp0 + 32 * ks, 16, 1024, 2),
+                 id_d, ks > 0);
+          mma_f8(dcol + 32, tc::smem_desc(ka0 + 32 * ks, 16, 1024, 2),
+                 tc::smem_desc(qa0 + 32 * ks, 16, 1024, 2), id_d2, ks > 0);
         }
+        tc::mma_commit(&sm.empty[stage]);
+        tc::mma_commit(&sm.a_empty[buf]);
+        tc::mma_commit(&sm.d_full[buf]);
+        issued = k + 1;
       }
+      // after an abort, let the issued MMAs finish before the tensor memory is freed
+      if (sm.abort_flag && issued > 0)
+        tc::mbar_wait_bounded(&sm.d_full[(issued - 1) & 1], parity_of(issued - 1, 2), 20ull * 1000 * 1000);
     }
-    // ---- the previous tile's MMAs read A: wait for them ---------------------
-    if (pending) {
-      if (!tc::mbar_wait_bounded(&sm.dbar[buf ^ 1u], uint32_t(((k - 1) >> 1) & 1))) sm.abort_flag = 1;
+  } else if (wid < 6) {
+    // ================= |k| and query operands (warps 2-5) =================
+    const int gt = tid - 64;
+    int cb = 0, cur_b = -1;
+    int64_t cbase = 0;
+    for (int64_t k = 0; k < ntiles; ++k) {
+      const TileRef tr = tile_of(a, reindex, g0 + k, cb, cbase);
+      if (tr.b != cur_b) {
+        // every MMA of the previous tiles must have read the old operands
+        if (k > 0 && !wait_or_abort(sm, &sm.d_full[(k - 1) & 1], parity_of(k - 1, 2))) break;
+        query_split(a, sm, tr.b, gt, true, 1);
+        cur_b = tr.b;
+      }
+      const int stage = int(k % kStages);
+      const uint32_t buf = uint32_t(k & 1);
+      if (!wait_or_abort(sm, &sm.full[stage], parity_of(k, kStages))) break;
+      if (k >= 2 && !wait_or_abort(sm, &sm.a_empty[buf], parity_of(k - 2, 2))) break;
+      const uint4* src = reinterpret_cast<const uint4*>(sm.stage[stage]);
+      uint4* dst = reinterpret_cast<uint4*>(sm.kabs[buf]);
+#pragma unroll
+      for (int i = 0; i < kStageBytes / 16 / kGroupThreads; ++i) {
+        uint4 v = src[gt + i * kGroupThreads];
+        v.x &= 0x7F7F7F7Fu; v.y &= 0x7F7F7F7Fu; v.z &= 0x7F7F7F7Fu; v.w &= 0x7F7F7F7Fu;
+        dst[gt + i * kGroupThreads] = v;
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) arrive(&sm.a_full[buf]);
+    }
+  } else {
+    // ================= epilogue (warps 6-9) =================
+    const int gt = tid - 192;
+    const int quarter = wid & 3;                      // TMEM lanes 32*quarter ..
+    const int r = quarter * 32 + lane;                // row of the tile
+    const uint32_t lane_base = uint32_t(quarter * 32) << 16;
+    int cb = 0, cur_b = -1;
+    int64_t cbase = 0;
+    for (int64_t k = 0; k < ntiles; ++k) {
+      const TileRef tr = tile_of(a, reindex, g0 + k, cb, cbase);
+      if (tr.b != cur_b) {
+        query_split(a, sm, tr.b, gt, false, 2);
+        cur_b = tr.b;
+      }
+      const uint32_t buf = uint32_t(k & 1);
+      if (!wait_or_abort(sm, &sm.d_full[buf], parity_of(k, 2))) break;
       tc::tc_fence_after_sync();
-    }
-    if (tr.b != sm.cur_b) {
-      // new sequence: finish the previous tile with its own weights, then
-      // build this sequence's query operands
-      if (pending && half == 0) scan_epilogue(a, reindex, sm, prev, tmem + lane_base + kColD + 32 * (buf ^ 1u), r, lane);
-      pending = false;
+      scan_epilogue(a, reindex, sm, tr, tmem + lane_base + 64 * buf, r, lane);
       tc::tc_fence_before_sync();
-      __syncthreads();
-      build_query(a, sm, tr.b);
+      __syncwarp();
+      if (lane == 0) arrive(&sm.d_empty[buf]);
     }
-    tmem_st32(tmem + lane_base + kColA + half * 32, af);
-    tmem_st32(tmem + lane_base + kColAbs + half * 32, aa);
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-    tc::tc_fence_before_sync();
-    __syncthreads();
-    const bool abort_now = sm.abort_flag != 0;
-    // ---- this tile's MMAs (one thread); refill the consumed stage ----------------
-    if (tid == 0 && !abort_now) {
-      tc::tc_fence_after_sync();
-      const uint32_t qf0 = tc::smem_u32(sm.qf[0]), qa0 = tc::smem_u32(sm.qa[0]);
-      const uint32_t dcol = tmem + kColD + 32 * buf;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t boff = (ks >> 2) * (16 * 128) + (ks & 3) * 32;
-        mma_f16_ts(dcol, tmem + kColA + 8 * ks, tc::smem_desc(qf0 + boff, 16, 1024, 2), idesc, ks > 0);
-      }
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t boff = (ks >> 2) * (16 * 128) + (ks & 3) * 32;
-        mma_f16_ts(dcol + 16, tmem + kColAbs + 8 * ks, tc::smem_desc(qa0 + boff, 16, 1024, 2), idesc, ks > 0);
-      }
-      tc::mma_commit(&sm.dbar[buf]);
-      if (next_load < g1) {
-        issue_tile_load(a, reindex, &kmap, sm, tile_of(a, reindex, next_load, pb, pbase), stage);
-        ++next_load;
-      }
-    }
-    if (abort_now) break;
-    if (pending && half == 0) scan_epilogue(a, reindex, sm, prev, tmem + lane_base + kColD + 32 * (buf ^ 1u), r, lane);
-    prev = tr;
-    pending = true;
-  }
-  // ---- the last tile ------------------------------------------------------------------
-  if (pending && !sm.abort_flag) {
-    const uint32_t buf = uint32_t((k - 1) & 1);
-    bool ok = tc::mbar_wait_bounded(&sm.dbar[buf], uint32_t(((k - 1) >> 1) & 1));
-    tc::tc_fence_after_sync();
-    if (ok && half == 0) scan_epilogue(a, reindex, sm, prev, tmem + lane_base + kColD + 32 * buf, r, lane);
-    if (!ok) sm.abort_flag = 1;
   }
   tc::tc_fence_before_sync();
   __syncthreads();
@@ -448,7 +496,7 @@ cudaError_t launch_scan_tc(const IdxArgs& a, bool reindex, cudaStream_t st) {
   size_t smem = sizeof(ScanSmem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  int64_t grid = min64(int64_t(2) * sms, tiles_ub);
+  int64_t grid = min64(int64_t(sms), tiles_ub);
   if (grid < 1) grid = 1;
   CSA2_PROFILED(st, reindex ? "reindex_score_tc" : "indexer_scan_tc",
                 (scan_tc_kernel<<<unsigned(grid), kScanThreads, smem, st>>>(a, map, reindex)));
