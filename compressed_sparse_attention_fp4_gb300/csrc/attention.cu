@@ -209,12 +209,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (tid == 0) {
     tc::tc_fence_after_sync();
     constexpr uint32_t idS = tc::idesc_bf16(kEntries, kQRows, 0, 0);
-#pragma unroll 1
+    // descriptors are formed once; an offset of x bytes adds x/16 to the
+    // start-address field (the operands lie below 256 KB, so it never carries)
+    const uint64_t ad0 = tc::smem_desc(kv_addr, 16, 1024, 2), bd0 = tc::smem_desc(q_addr, 16, 1024, 2);
+#pragma unroll
     for (int ks = 0; ks < 36; ++ks) {
-      uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-      uint64_t ad = tc::smem_desc(kv_addr + kb * kRegion + off, 16, 1024, 2);
-      uint64_t bd = tc::smem_desc(q_addr + kb * kQRegion + off, 16, 1024, 2);
-      tc::mma_bf16(tmem, ad, bd, idS, ks > 0);
+      const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+      tc::mma_bf16(tmem, ad0 + ((kb * kRegion + off) >> 4), bd0 + ((kb * kQRegion + off) >> 4), idS, ks > 0);
     }
     tc::mma_commit(&bar_s);
   }
@@ -285,17 +286,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (tid == 0) {
     tc::tc_fence_after_sync();
     constexpr uint32_t idO = tc::idesc_bf16(kEntries, kQRows, 1, 1);
-    const uint32_t ph = tc::smem_u32(p_hi), pl = tc::smem_u32(p_lo);
-#pragma unroll 1
+    const uint64_t av0 = tc::smem_desc(kv_addr, kRegion, 1024, 2);
+    const uint64_t bp0[2] = {tc::smem_desc(tc::smem_u32(p_hi), kRegion, 1024, 2),
+                             tc::smem_desc(tc::smem_u32(p_lo), kRegion, 1024, 2)};
+#pragma unroll
     for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll 1
+#pragma unroll
       for (int part = 0; part < 2; ++part) {
-#pragma unroll 1
-        for (int ks = 0; ks < 8; ++ks) {
-          uint64_t ad = tc::smem_desc(kv_addr + (2 * mt) * kRegion + ks * 2048, kRegion, 1024, 2);
-          uint64_t bd = tc::smem_desc((part ? pl : ph) + ks * 2048, kRegion, 1024, 2);
-          tc::mma_bf16(tmem + 64 + 64 * mt, ad, bd, idO, part > 0 || ks > 0);
-        }
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_bf16(tmem + 64 + 64 * mt, av0 + (((2 * mt) * kRegion + ks * 2048) >> 4),
+                       bp0[part] + ((ks * 2048) >> 4), idO, part > 0 || ks > 0);
       }
     }
     tc::mma_commit(&bar_o);

@@ -370,7 +370,12 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     // ================= MMA issuer =================
     if (lane == 0) {
       constexpr uint32_t id_d = idesc_e4m3(kTile, 32), id_d2 = idesc_e4m3(kTile, 16);
-      const uint32_t qp0 = tc::smem_u32(sm.qp), qa0 = tc::smem_u32(sm.qa);
+      // descriptors are formed once; an offset of x bytes adds x/16 to the
+      // start-address field (every operand lies below 256 KB, so it never carries)
+      const uint64_t dq = tc::smem_desc(tc::smem_u32(sm.qp), 16, 1024, 2);
+      const uint64_t dqa = tc::smem_desc(tc::smem_u32(sm.qa), 16, 1024, 2);
+      const uint64_t dk0 = tc::smem_desc(tc::smem_u32(sm.stage[0]), 16, 1024, 2);
+      const uint64_t dka0 = tc::smem_desc(tc::smem_u32(sm.kabs[0]), 16, 1024, 2);
       int64_t issued = 0;
       for (int64_t k = 0; k < ntiles; ++k) {
         const int stage = int(k % kStages);
@@ -379,14 +384,13 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         if (!wait_or_abort(sm, &sm.full[stage], parity_of(k, kStages))) break;
         if (k >= 2 && !wait_or_abort(sm, &sm.d_empty[buf], parity_of(k - 2, 2))) break;
         tc::tc_fence_after_sync();
-        const uint32_t k0 = tc::smem_u32(sm.stage[stage]), ka0 = tc::smem_u32(sm.kabs[buf]);
+        const uint64_t dk = dk0 + uint64_t(stage) * (kStageBytes >> 4);
+        const uint64_t dka = dka0 + uint64_t(buf) * (kStageBytes >> 4);
         const uint32_t dcol = tmem + 64 * buf;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {                 // K = 32 E4M3 (32 bytes) per step
-          mma_f8(dcol, tc::smem_desc(k0 + 32 * ks, 16, 1024, 2), tc::smem_desc(qp0 + 32 * ks, 16, 1024, 2),
-                 id_d, ks > 0);
-          mma_f8(dcol + 32, tc::smem_desc(ka0 + 32 * ks, 16, 1024, 2),
-                 tc::smem_desc(qa0 + 32 * ks, 16, 1024, 2), id_d2, ks > 0);
+          mma_f8(dcol, dk + 2 * ks, dq + 2 * ks, id_d, ks > 0);
+          mma_f8(dcol + 32, dka + 2 * ks, dqa + 2 * ks, id_d2, ks > 0);
         }
         tc::mma_commit(&sm.empty[stage]);
         tc::mma_commit(&sm.a_empty[buf]);
