@@ -16,9 +16,10 @@
 // Work: one persistent CTA per SM walks a contiguous range of 128-position
 // tiles; its warps specialise and hand tiles on through mbarriers, so the
 // key stream, the MMAs and the epilogue of consecutive tiles overlap:
-//   * warp 0 (one thread): TMA (tensor map, 128-byte swizzle = the MMA's
-//     K-major operand layout) streams each tile's 128 x 128 B of keys into a
-//     6-stage shared-memory ring.
+//   * warp 0: one thread streams each tile's 128 x 128 B of keys by TMA
+//     (tensor map, 128-byte swizzle = the MMA's K-major operand layout) into
+//     a 6-stage shared-memory ring; for Reindex tiles (16 scattered pool
+//     blocks) the whole warp gathers them with cp.async instead.
 //   * warps 2-5 write |k| (sign bits cleared) of each tile into one of two
 //     buffers, and rebuild the query operands when a new sequence starts.
 //   * warp 1 (one thread) issues D = K . [q1; r1]^T (M=128 positions, N=32)
@@ -133,27 +134,8 @@ __device__ inline TileRef tile_of(const IdxArgs& a, bool reindex, int64_t g, int
   }
 }
 
-__device__ inline void issue_tile_load(const IdxArgs& a, bool reindex, const CUtensorMap* map,
-                                       ScanSmem& sm, const TileRef& tr, int stage) {
-  if (reindex) {
-    // one 8-row box per pool block (a block never crosses a 64-position page)
-    const bool paged = a.page_table != nullptr;
-    const int64_t n_ctx = checked_ctx(a.ctx_len, a.d, tr.b, paged, a.ws);
-    const int nblk = (tr.nvalid + kBlock - 1) / kBlock;
-    int32_t rows[kTile / kBlock];
-    uint32_t bytes = 0;
-    for (int j = 0; j < nblk; ++j) {
-      int32_t blk = __ldg(a.pool_in + int64_t(tr.b) * a.d.pool_blocks + (tr.t0 >> 3) + j);
-      int64_t row = -1;
-      if (blk >= 0 && int64_t(blk) * kBlock < n_ctx) row = kv_row(a.page_table, a.d, tr.b, int64_t(blk) * kBlock, a.ws);
-      rows[j] = int32_t(row);
-      if (row >= 0) bytes += kBlock * 128;
-    }
-    tc::mbar_expect_tx(&sm.full[stage], bytes);
-    for (int j = 0; j < nblk; ++j)
-      if (rows[j] >= 0) tc::tma_load_2d(map, sm.stage[stage] + j * kBlock * 128, 0, rows[j], &sm.full[stage]);
-    return;
-  }
+__device__ inline void issue_tile_load(const IdxArgs& a, const CUtensorMap* map, ScanSmem& sm,
+                                       const TileRef& tr, int stage) {
   uint32_t bytes = 0;
   int32_t rows[2];
   int nbox = (tr.nvalid > 64) ? 2 : 1;
@@ -166,6 +148,39 @@ __device__ inline void issue_tile_load(const IdxArgs& a, bool reindex, const CUt
   tc::mbar_expect_tx(&sm.full[stage], bytes);
   for (int h = 0; h < nbox; ++h)
     if (rows[h] >= 0) tc::tma_load_2d(map, sm.stage[stage] + h * 64 * 128, 0, rows[h], &sm.full[stage]);
+}
+
+// Reindex tiles: the pool blocks are scattered 1 KB runs (8 rows, never
+// across a page), so the whole producer warp gathers them with 16-byte
+// cp.async copies straight into the 128-byte swizzled layout; each lane's
+// copies arrive on the stage's mbarrier when they land (32 arrivals).
+__device__ inline void gather_pool_tile(const IdxArgs& a, ScanSmem& sm, const TileRef& tr, int stage, int lane) {
+  int64_t rowj = -1;
+  int nrow = 0;                                          // rows of the block inside the context
+  if (lane < kTile / kBlock && lane * kBlock < tr.nvalid) {
+    const bool paged = a.page_table != nullptr;
+    const int64_t n_ctx = checked_ctx(a.ctx_len, a.d, tr.b, paged, a.ws);
+    const int32_t blk = __ldg(a.pool_in + int64_t(tr.b) * a.d.pool_blocks + (tr.t0 >> 3) + lane);
+    if (blk >= 0 && int64_t(blk) * kBlock < n_ctx) {
+      rowj = kv_row(a.page_table, a.d, tr.b, int64_t(blk) * kBlock, a.ws);
+      nrow = int(min64(kBlock, n_ctx - int64_t(blk) * kBlock));
+    }
+  }
+  const uint8_t* keys = reinterpret_cast<const uint8_t*>(a.idx_k);
+  const uint32_t dst0 = tc::smem_u32(sm.stage[stage]);
+#pragma unroll 4
+  for (int m = 0; m < 32; ++m) {                         // copy i = lane + 32m: block m/2
+    const int64_t rj = __shfl_sync(0xFFFFFFFFu, rowj, m >> 1);
+    const int nr = __shfl_sync(0xFFFFFFFFu, nrow, m >> 1);
+    const int rin = 4 * (m & 1) + (lane >> 3), c = lane & 7;
+    if (rj < 0 || rin >= nr) continue;
+    const int r = (m >> 1) * kBlock + rin;
+    const uint8_t* src = keys + (rj + rin) * 128 + c * 16;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst0 + tc::sw128_offset(r, c)), "l"(src)
+                 : "memory");
+  }
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(&sm.full[stage]))
+               : "memory");
 }
 
 __device__ inline void group_sync(int id) {
@@ -332,7 +347,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   if (wid == 0) tc::tmem_alloc(&sm.tmem_slot, kScanTmemCols);
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&sm.full[s], 1);
+      tc::mbar_init(&sm.full[s], reindex ? 32 : 1);     // 32 cp.async lanes or one TMA arrive
       tc::mbar_init(&sm.empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -350,7 +365,17 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   const uint32_t tmem = sm.tmem_slot;
   const int64_t ntiles = g1 - g0;
 
-  if (wid == 0) {
+  if (wid == 0 && reindex) {
+    // ================= producer: cp.async gather of pool blocks =================
+    int pb = 0;
+    int64_t pbase = 0;
+    for (int64_t k = 0; k < ntiles; ++k) {
+      const int stage = int(k % kStages);
+      if (k >= kStages && !wait_or_abort(sm, &sm.empty[stage], parity_of(k - kStages, kStages))) break;
+      gather_pool_tile(a, sm, tile_of(a, reindex, g0 + k, pb, pbase), stage, lane);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");     // nothing in flight when the CTA exits
+  } else if (wid == 0) {
     // ================= producer: TMA ring =================
     if (lane == 0) {
       int pb = 0;
@@ -359,7 +384,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       for (; k < ntiles; ++k) {
         const int stage = int(k % kStages);
         if (k >= kStages && !wait_or_abort(sm, &sm.empty[stage], parity_of(k - kStages, kStages))) break;
-        issue_tile_load(a, reindex, &kmap, sm, tile_of(a, reindex, g0 + k, pb, pbase), stage);
+        issue_tile_load(a, &kmap, sm, tile_of(a, reindex, g0 + k, pb, pbase), stage);
       }
       // after an abort, let the copies still in flight land before the CTA exits
       if (sm.abort_flag)
@@ -384,6 +409,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         if (!wait_or_abort(sm, &sm.full[stage], parity_of(k, kStages))) break;
         if (k >= 2 && !wait_or_abort(sm, &sm.d_empty[buf], parity_of(k - 2, 2))) break;
         tc::tc_fence_after_sync();
+        if (reindex) tc::fence_proxy_async_smem();       // the gathered keys are generic-proxy writes
         const uint64_t dk = dk0 + uint64_t(stage) * (kStageBytes >> 4);
         const uint64_t dka = dka0 + uint64_t(buf) * (kStageBytes >> 4);
         const uint32_t dcol = tmem + 64 * buf;

@@ -423,16 +423,27 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
   for (int i = tid; i < kSelCapPerCta / 32; i += blockDim.x) { sm.band_bits[i] = 0; sm.sel_bits[i] = 0; }
   if (tid == 0) { sm.cnt_in = 0; sm.cnt_band = 0; }
   __syncthreads();
-#pragma unroll 4
-  for (int i = tid; i < n_local; i += blockDim.x) {
-    ItemVal it = load_item(a, kind, c, sm.pool_ids, base + i);
-    uint32_t ku = 0, kl = 0;
-    if (it.valid) {
-      ku = f32_key(__fadd_ru(it.v, it.delta));
-      kl = f32_key(__fadd_rd(it.v, -it.delta));
+  {
+    // every item load of this thread is issued before any key is formed
+    constexpr int kPer = kSelCapPerCta / kSelThreads;
+    ItemVal it[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = tid + j * kSelThreads;
+      it[j] = i < n_local ? load_item(a, kind, c, sm.pool_ids, base + i) : ItemVal{0.0f, 0.0f, false};
     }
-    sm.keyU[i] = ku;
-    sm.keyL[i] = kl;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = tid + j * kSelThreads;
+      if (i >= n_local) break;
+      uint32_t ku = 0, kl = 0;
+      if (it[j].valid) {
+        ku = f32_key(__fadd_ru(it[j].v, it[j].delta));
+        kl = f32_key(__fadd_rd(it[j].v, -it[j].delta));
+      }
+      sm.keyU[i] = ku;
+      sm.keyL[i] = kl;
+    }
   }
   __syncthreads();
   if (k >= n_items) {
@@ -531,6 +542,26 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
     if (c.rank == 0 && need > 0) {
       if (need >= int64_t(tot_band)) {
         for (uint32_t i = tid; i < tot_band; i += blockDim.x) g_pick[g_list[i]] = 1;
+      } else if (tot_band <= kSelThreads) {
+        // small band: each item's rank = the number of band items ahead of it
+        uint64_t* skey = reinterpret_cast<uint64_t*>(sm.keyU);
+        int32_t* sidx = reinterpret_cast<int32_t*>(sm.keyL);
+        for (uint32_t i = tid; i < tot_band; i += blockDim.x) {
+          int32_t it = g_list[i];
+          skey[i] = f64_key(g_exact[it]);
+          sidx[i] = it;
+        }
+        __syncthreads();
+        if (tid < tot_band) {
+          const uint64_t mk = skey[tid];
+          const int32_t mi = sidx[tid];
+          uint32_t rank = 0;
+          for (uint32_t j = 0; j < tot_band; ++j) {
+            const uint64_t kj = skey[j];
+            rank += (kj > mk || (kj == mk && sidx[j] < mi)) ? 1u : 0u;
+          }
+          if (rank < uint32_t(need)) g_pick[mi] = 1;
+        }
       } else if (tot_band <= kSortCap) {
         uint64_t* skey = reinterpret_cast<uint64_t*>(sm.keyU);
         int32_t* sidx = reinterpret_cast<int32_t*>(sm.keyL);
@@ -640,8 +671,13 @@ __device__ int64_t block_sum(SelSmem& sm, int v) {
   return t;
 }
 
+// Query factors of sequence b.  Elements h*di + ch are spread over the
+// threads so that a warp's 32 elements share one head (di is 64 or 128):
+// per-head minima, sums and flags are reduced in the warp first and reach
+// shared memory with one atomic per warp.
 __device__ void load_query_factors(const IdxArgs& a, SelSmem& sm, int b) {
   const int hi = a.d.idx_heads, di = a.d.idx_dim;
+  const int lane = threadIdx.x & 31;
   const bool fp8 = a.d.idx_k_dtype == CSA2_IDXK_E4M3;
   if (threadIdx.x < kMaxIdxHeads) {
     sm.q_elo[threadIdx.x] = INT_MAX;
@@ -650,33 +686,45 @@ __device__ void load_query_factors(const IdxArgs& a, SelSmem& sm, int b) {
   }
   __syncthreads();
   for (int i = threadIdx.x; i < hi * di; i += blockDim.x) {
-    int h = i / di, ch = i % di;
-    int64_t qidx = int64_t(b) * hi * di + i;
-    float v = fp8 ? bf16_to_f32(reinterpret_cast<const uint16_t*>(a.idx_q)[qidx])
-                  : reinterpret_cast<const float*>(a.idx_q)[qidx];
-    Factor f = factor_f32(v);
+    const int h = i / di, ch = i % di;
+    const int64_t qidx = int64_t(b) * hi * di + i;
+    const float v = fp8 ? bf16_to_f32(reinterpret_cast<const uint16_t*>(a.idx_q)[qidx])
+                        : reinterpret_cast<const float*>(a.idx_q)[qidx];
+    const Factor f = factor_f32(v);
     sm.qf[ch * kMaxIdxHeads + h] = f;
-    if (f.sig) atomicMin(&sm.q_elo[h], f.exp + __ffs(abs(f.sig)) - 1);   // lowest set bit
+    int lsb = f.sig ? f.exp + __ffs(abs(f.sig)) - 1 : INT_MAX;      // lowest set bit
+#pragma unroll
+    for (int o = 16; o; o >>= 1) lsb = min(lsb, __shfl_xor_sync(0xFFFFFFFFu, lsb, o));
+    if (lane == 0 && lsb != INT_MAX) atomicMin(&sm.q_elo[h], lsb);
   }
   __syncthreads();
   for (int i = threadIdx.x; i < hi * di; i += blockDim.x) {
-    int h = i / di, ch = i % di;
-    Factor f = sm.qf[ch * kMaxIdxHeads + h];
+    const int h = i / di, ch = i % di;
+    const Factor f = sm.qf[ch * kMaxIdxHeads + h];
     int32_t qv = 0;
+    bool wide = false;
+    unsigned long long mag64 = 0;
     if (f.sig) {
       // q = sig * 2^exp = qv * 2^q_elo; sh < 0 only drops trailing zero bits
-      int sh = f.exp - sm.q_elo[h];
+      const int sh = f.exp - sm.q_elo[h];
       int mag = abs(f.sig);
-      int bits = 32 - __clz(mag) + sh;
+      const int bits = 32 - __clz(mag) + sh;
       if (bits > 30) {
-        atomicAnd(&sm.q_fast[h], 0);
+        wide = true;
       } else {
         mag = sh >= 0 ? (mag << sh) : (mag >> -sh);
         qv = f.sig < 0 ? -mag : mag;
-        atomicAdd(&sm.q_l1[h], (unsigned long long)mag);
+        mag64 = (unsigned long long)mag;
       }
     }
     sm.qi[ch * kMaxIdxHeads + h] = qv;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mag64 += __shfl_xor_sync(0xFFFFFFFFu, mag64, o);
+    const bool any_wide = __any_sync(0xFFFFFFFFu, wide);
+    if (lane == 0) {
+      if (any_wide) atomicAnd(&sm.q_fast[h], 0);
+      atomicAdd(&sm.q_l1[h], mag64);
+    }
   }
   if (threadIdx.x < hi) sm.w[threadIdx.x] = a.w[int64_t(b) * hi + threadIdx.x];
   __syncthreads();
