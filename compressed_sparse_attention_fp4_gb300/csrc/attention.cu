@@ -24,9 +24,18 @@
 //      its rounding stays near 2^-17;
 //   4. O^T[512 dims x 64 heads] = V^T . P^T on tcgen05 (the same KV tile read
 //      MN-major), 4 M-tiles of 128 dims, hi and lo accumulated together;
-//   5. writes the chunk's unnormalised output and (max, sum) per head.
-// A combine kernel merges the chunks: o = sum_s e^(m_s - M) o_s / sum_s
-// e^(m_s - M) l_s, lse = M + ln(sum_s e^(m_s - M) l_s).
+//   5. merges the chunks of the sequence: o = sum_s 2^(m_s - M) o_s / L,
+//      L = sum_s 2^(m_s - M) l_s, lse = M ln 2 + ln L (m in base-2 logits).
+//      With at most 8 chunks the sequence's CTAs form a thread-block
+//      cluster: each publishes its per-head (m_s, l_s) in shared memory;
+//      after a cluster barrier each reads them all, forms M and L, scales
+//      its O_s into shared memory and adds it into the output with bulk
+//      reduce-add copies (cp.reduce.async.bulk .add.f32; the SWA chunk, which
+//      finishes first, zeroes the output rows before the barrier).  The order of the additions is not fixed, so the
+//      last bits of the output may differ between runs.  With more chunks,
+//      each CTA writes its unnormalised O_s and (m_s, l_s) and a combine
+//      kernel merges them (natural-log m there).
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -36,6 +45,8 @@
 #include "kernels.cuh"
 #include "profile.cuh"
 #include "tc.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace csa2 {
 
@@ -62,10 +73,45 @@ __device__ inline uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Reduces 16 values per lane over the warp's 32 lanes by a butterfly
+// reduce-scatter (8 + 4 + 2 + 1 + 1 shuffles instead of 16 x 5): returns the
+// reduction of value index butterfly_index(lane), held by lanes 2i and 2i+1.
+__device__ inline int butterfly_index(int lane) {
+  return (((lane >> 4) & 1) << 3) | (((lane >> 3) & 1) << 2) | (((lane >> 2) & 1) << 1) | ((lane >> 1) & 1);
+}
+
+template <bool kMax>
+__device__ inline float butterfly16(const float (&v)[16], int lane) {
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+  float y[8], z[4], w[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float keep = b4 ? v[8 + i] : v[i], give = b4 ? v[i] : v[8 + i];
+    y[i] = op(keep, __shfl_xor_sync(0xFFFFFFFFu, give, 16));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b3 ? y[4 + i] : y[i], give = b3 ? y[i] : y[4 + i];
+    z[i] = op(keep, __shfl_xor_sync(0xFFFFFFFFu, give, 8));
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b2 ? z[2 + i] : z[i], give = b2 ? z[i] : z[2 + i];
+    w[i] = op(keep, __shfl_xor_sync(0xFFFFFFFFu, give, 4));
+  }
+  const float keep = b1 ? w[1] : w[0], give = b1 ? w[0] : w[1];
+  float u = op(keep, __shfl_xor_sync(0xFFFFFFFFu, give, 2));
+  return op(u, __shfl_xor_sync(0xFFFFFFFFu, u, 1));
+}
+
 __device__ inline void st_shared_v4(uint8_t* base, uint32_t off, uint4 v) {
   *reinterpret_cast<uint4*>(base + off) = v;
 }
 
+constexpr int kMaxClusterSplits = 8;                // portable cluster size
+
+template <bool kFused>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_partial_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
                            const __grid_constant__ CUtensorMap swamap, int swa_tma_split) {
@@ -76,7 +122,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __shared__ uint64_t bar_ld, bar_s, bar_o;
   __shared__ uint32_t tmem_slot;
   __shared__ int64_t row_s[kEntries];               // >= 0 main row, -2 - r SWA row r, -1 empty
-  __shared__ float red_m[4][4][16], red_l[4][4][16];
+  __shared__ __align__(16) float red_m[4][4][16];
+  __shared__ __align__(16) float red_l[4][4][16];
+  __shared__ float fac_s[kQRows];                    // fused: 2^(m_s - M) / L per head
+  __shared__ float ml_s[2][kQRows];                  // fused: this chunk's (m, l), base-2 m
 
   const int b = blockIdx.y, split = blockIdx.x;
   const int H = a.d.heads, K = a.d.topk, W = a.d.swa;
@@ -117,6 +166,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc::tc_fence_after_sync();
   const uint32_t tmem = tmem_slot;
+  if constexpr (kFused) {
+    // the chunk that finishes first (the TMA-loaded SWA window, else chunk 0)
+    if (split == (swa_tma_split >= 0 ? swa_tma_split : 0)) {
+      // the output rows of this sequence start at zero; the other chunks add
+      // into them only after the cluster barrier below
+      float4* ob = reinterpret_cast<float4*>(a.out + int64_t(b) * H * kLatent);
+      for (int i = tid; i < H * (kLatent / 4); i += kAttnThreads) ob[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+  }
 
   // ---- TMA: the query (9 boxes of 64 channels x 64 heads) and, for the
   //      window's CTA, the SWA rows (9 boxes of 64 channels x 128 rows) ----------
@@ -230,23 +289,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc::tmem_ld16(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(hg * 16), x);
   const float c2 = a.scale * 1.4426950408889634f;   // logits in base 2
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    x[j] = valid ? x[j] * c2 : -INFINITY;
-    float m = x[j];
-#pragma unroll
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    if (lane == 0) red_m[hg][quarter][j] = m;
+  for (int j = 0; j < 16; ++j) x[j] = valid ? x[j] * c2 : -INFINITY;
+  {
+    const float m = butterfly16<true>(x, lane);
+    if ((lane & 1) == 0) red_m[hg][quarter][butterfly_index(lane)] = m;
   }
   __syncthreads();
   float p[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    float M = fmaxf(fmaxf(red_m[hg][0][j], red_m[hg][1][j]), fmaxf(red_m[hg][2][j], red_m[hg][3][j]));
-    p[j] = (M == -INFINITY || x[j] == -INFINITY) ? 0.0f : exp2f(x[j] - M);
-    float l = p[j];
+  for (int j4 = 0; j4 < 4; ++j4) {
+    float4 m4[4];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
-    if (lane == 0) red_l[hg][quarter][j] = l;
+    for (int q = 0; q < 4; ++q) m4[q] = reinterpret_cast<const float4*>(&red_m[hg][q][0])[j4];
+    const float Mj[4] = {fmaxf(fmaxf(m4[0].x, m4[1].x), fmaxf(m4[2].x, m4[3].x)),
+                         fmaxf(fmaxf(m4[0].y, m4[1].y), fmaxf(m4[2].y, m4[3].y)),
+                         fmaxf(fmaxf(m4[0].z, m4[1].z), fmaxf(m4[2].z, m4[3].z)),
+                         fmaxf(fmaxf(m4[0].w, m4[1].w), fmaxf(m4[2].w, m4[3].w))};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = 4 * j4 + i;
+      p[j] = (Mj[i] == -INFINITY || x[j] == -INFINITY) ? 0.0f : exp2f(x[j] - Mj[i]);
+    }
+  }
+  {
+    const float l = butterfly16<false>(p, lane);
+    if ((lane & 1) == 0) red_l[hg][quarter][butterfly_index(lane)] = l;
   }
   // P^T rows (entry e): heads 16*hg.. as 2 chunks, hi and lo bf16 parts.
   // The query buffer is free: the S^T MMAs completed (bar_s) before this.
@@ -277,8 +344,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (h < H) {
       float M = fmaxf(fmaxf(red_m[hg][0][lane], red_m[hg][1][lane]), fmaxf(red_m[hg][2][lane], red_m[hg][3][lane]));
       float L = red_l[hg][0][lane] + red_l[hg][1][lane] + red_l[hg][2][lane] + red_l[hg][3][lane];
-      ml_base[(prow + h) * 2] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
-      ml_base[(prow + h) * 2 + 1] = L;
+      if constexpr (kFused) {
+        ml_s[0][h] = M;
+        ml_s[1][h] = L;
+      } else {
+        ml_base[(prow + h) * 2] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
+        ml_base[(prow + h) * 2 + 1] = L;
+      }
     }
   }
 
@@ -305,22 +377,69 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc::tc_fence_after_sync();
   if (!ok && tid == 0) raise_err(a.ws, CSA2_DEV_TIMEOUT);
 
-  // ---- unnormalised partial output -------------------------------------------------
-  float* o_base = reinterpret_cast<float*>(a.ws + a.L.attn_o);
+  if constexpr (kFused) {
+    // every chunk's (m, l) is in its shared memory; the zeroed output rows
+    // are visible too
+    cg::cluster_group cl = cg::this_cluster();
+    cl.sync();
+    if (tid < kQRows) {
+      const int S = a.L.splits;
+      float mr[kMaxClusterSplits], lr[kMaxClusterSplits];
+      float M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kMaxClusterSplits; ++r) {
+        mr[r] = (r < S && tid < H) ? cl.map_shared_rank(&ml_s[0][0], r)[tid] : -INFINITY;
+        lr[r] = (r < S && tid < H) ? cl.map_shared_rank(&ml_s[1][0], r)[tid] : 0.0f;
+        M = fmaxf(M, mr[r]);
+      }
+      float L = 0.0f;
+#pragma unroll
+      for (int r = 0; r < kMaxClusterSplits; ++r)
+        if (mr[r] != -INFINITY) L += lr[r] * exp2f(mr[r] - M);
+      const float ms = mr[split < kMaxClusterSplits ? split : 0];
+      fac_s[tid] = (ms == -INFINITY || !(L > 0.0f)) ? 0.0f : exp2f(ms - M) / L;
+      if (split == 0 && tid < H)
+        a.lse[int64_t(b) * H + tid] = L > 0.0f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
+    }
+    // done with the other chunks' shared memory; they may leave once every
+    // chunk has arrived (the matching wait is at the end)
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    __syncthreads();
+  }
+  // ---- O^T through shared memory as [head][dim] (the KV tile is no longer
+  //      read: the PV MMAs completed), then one bulk copy of 2 KB per head:
+  //      a reduce-add into the output (fused) or the partial (combine) -------
+  float* obuf = reinterpret_cast<float*>(kv_s);
 #pragma unroll 1
   for (int mt = 0; mt < 4; ++mt) {
     float o[16];
     tc::tmem_ld16(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(64 + 64 * mt + hg * 16), o);
     const int dim = mt * 128 + quarter * 32 + lane;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      int h = hg * 16 + j;
-      if (h < H) o_base[(prow + h) * kLatent + dim] = o[j];
-    }
+    for (int j = 0; j < 16; ++j) obuf[(hg * 16 + j) * kLatent + dim] = kFused ? o[j] * fac_s[hg * 16 + j] : o[j];
   }
+  tc::fence_proxy_async_smem();
   tc::tc_fence_before_sync();
   __syncthreads();
   if (wid == 0) tc::tmem_dealloc(tmem, kTmemCols);
+  if (tid < H) {
+    const uint32_t src = tc::smem_u32(obuf + tid * kLatent);
+    if constexpr (kFused) {
+      float* dst = a.out + (int64_t(b) * H + tid) * kLatent;
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
+                   ::"l"(dst), "r"(src), "r"(uint32_t(kLatent * 4))
+                   : "memory");
+    } else {
+      float* dst = reinterpret_cast<float*>(a.ws + a.L.attn_o) + (prow + tid) * kLatent;
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                   ::"l"(dst), "r"(src), "r"(uint32_t(kLatent * 4))
+                   : "memory");
+    }
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // shared source read out
+  }
+  if constexpr (kFused) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
@@ -388,11 +507,32 @@ cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
       !encode_rows_map(&swamap, a.swa, uint64_t(a.batch) * a.d.swa, kEntries))
     return cudaErrorInvalidValue;
   size_t smem = attn_smem_bytes(a.d.heads);
-  cudaError_t e = cudaFuncSetAttribute(attn_partial_tc_kernel,
+  if (a.L.splits <= kMaxClusterSplits) {
+    // one cluster per sequence; the merge happens inside the cluster
+    cudaError_t e = cudaFuncSetAttribute(attn_partial_tc_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(a.L.splits), unsigned(a.batch), 1);
+    cfg.blockDim = dim3(kAttnThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(a.L.splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    CSA2_PROFILED(st, "attn_fused_tc",
+                  (e = cudaLaunchKernelEx(&cfg, attn_partial_tc_kernel<true>, a, qmap, swamap, swa_split)));
+    return e;
+  }
+  cudaError_t e = cudaFuncSetAttribute(attn_partial_tc_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   CSA2_PROFILED(st, "attn_partial_tc",
-                (attn_partial_tc_kernel<<<dim3(unsigned(a.L.splits), unsigned(a.batch)), kAttnThreads, smem, st>>>(
+                (attn_partial_tc_kernel<false><<<dim3(unsigned(a.L.splits), unsigned(a.batch)), kAttnThreads, smem, st>>>(
                     a, qmap, swamap, swa_split)));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
