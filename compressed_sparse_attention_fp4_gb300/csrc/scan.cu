@@ -15,25 +15,34 @@
 //
 // Work: one persistent CTA per SM walks a contiguous range of 128-position
 // tiles; its warps specialise and hand tiles on through mbarriers, so the
-// key stream, the MMAs and the epilogue of consecutive tiles overlap:
-//   * warp 0: one thread streams each tile's 128 x 128 B of keys by TMA
-//     (tensor map, 128-byte swizzle = the MMA's K-major operand layout) into
-//     a 6-stage shared-memory ring; for Reindex tiles (16 scattered pool
-//     blocks) the whole warp gathers them with cp.async instead.
-//   * warps 2-5 write |k| (sign bits cleared) of each tile into one of two
-//     buffers, and rebuild the query operands when a new sequence starts.
-//   * warp 1 (one thread) issues D = K . [q1; r1]^T (M=128 positions, N=32)
-//     and D2 = |K| . ceil(|Qs|)^T (N=16; ceil = the E4M3 value at or above),
-//     K=128 in 4 steps each, into one of two tensor-memory buffers; its
-//     commits free the ring stage, the |k| buffer and hand D to
-//   * warps 6-9, the epilogue: v_t = sum_h w'_h ReLU(D_h + D_{16+h}) with
-//     w'_h = w_h 2^-e_h, and delta_t = C sum_h |w'_h| D2_h + (query rounding
-//     term).  C covers the tensor-core accumulation: modelled as at most
-//     2^-16 of sum|products| per head dot (each product truncated to 2^-23 of
-//     the largest in its step, 128 products), taken with a factor-4 margin
-//     (2^-14; the worst observed on adversarial operands is 2^-18.8), plus the
-//     fp32 head sum and the fp64 rounding of the exact score.  Block max of v
-//     and delta over 8 positions are written with the position scores.
+// key stream, the MMAs and the epilogue of consecutive tiles overlap.  Each
+// stage of the 6-stage shared-memory ring holds a tile's keys (128 rows x
+// 128 B, 128-byte swizzled K-major) followed by the query pieces (32 rows:
+// q1 of the 16 heads, then r1), so that one MMA per K-step with A = the keys
+// and B = the whole stage (N = 160) yields, per position t,
+//   columns 0..127:   the Gram row k_t . k_s  (its diagonal is ||k_t||^2),
+//   columns 128..159: k_t . q1_h and k_t . r1_h.
+//   * warp 0: one thread streams the keys of each tile by TMA (tensor map
+//     with the same swizzle); for Reindex tiles (16 scattered pool blocks)
+//     the whole warp gathers them with cp.async instead, resolving the rows
+//     of a window of 6 tiles at a time.
+//   * warps 2-5 (the query group) split the query when a new sequence starts
+//     and copy the pieces into each stage behind its keys.
+//   * warp 1 (one thread) issues the 4 MMAs of a tile (kind::f8f6f4, M=128,
+//     N=160, K=32 each) into the next of three tensor-memory accumulators.
+//   * warps 6-9 and 10-13, two epilogue groups taking alternate tiles from
+//     three tensor-memory accumulators: v_t = sum_h w'_h ReLU(D_h + D_{16+h}) with
+//     w'_h = w_h 2^-e_h, block max over 8 positions, and the bound
+//       delta_t = C ||u||_2 ||k_t||_2 + (query rounding term),
+//     u_c = sum_h |w'_h| (|q1_hc| + |r1_hc|): by Cauchy-Schwarz it is at least
+//     C sum_c u_c |k_tc|, which covers the error of the weighted head sum.
+// C covers the tensor-core accumulation: modelled as at most 2^-16 of
+// sum|products| per dot product (each product truncated to 2^-23 of the
+// largest in its step, 128 products), taken with a factor-4 margin (2^-14;
+// the worst observed on adversarial operands is 2^-18.8), plus the fp32 head
+// sum and the fp64 rounding of the exact score.  ||k_t||^2 comes from the
+// same MMA (all its products are positive, so it is low by at most 2^-14 of
+// itself) and is raised accordingly before the square root.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -47,27 +56,33 @@
 
 namespace csa2 {
 
-constexpr int kScanThreads = 320;          // warp 0 TMA, 1 MMA, 2-5 |k| + query, 6-9 epilogue
-constexpr int kGroupThreads = 128;         // threads of the |k| group and of the epilogue group
+constexpr int kScanThreads = 448;          // warp 0 TMA, 1 MMA, 2-5 query, 6-9 / 10-13 epilogue
+constexpr int kGroupThreads = 128;         // threads of the query group and of each epilogue group
 constexpr int kTile = 128;                 // positions per tile (= MMA M)
-constexpr int kStages = 6;                 // TMA ring depth
-constexpr int kStageBytes = kTile * 128;   // 16 KB of E4M3 keys
-constexpr uint32_t kScanTmemCols = 128;    // D buffer j: cols 64j .. 64j+31, D2: 64j+32 .. 64j+47
+constexpr int kStages = 6;                 // ring depth
+constexpr int kKeyBytes = kTile * 128;     // 16 KB of E4M3 keys
+constexpr int kQpBytes = 32 * 128;         // q1 (16 rows) + r1 (16 rows)
+constexpr int kStageStride = kKeyBytes + kQpBytes;
+constexpr int kMmaN = kTile + 32;          // Gram row + the two query pieces
+constexpr int kDBufs = 3;                  // tensor-memory accumulators in flight
+constexpr uint32_t kScanTmemCols = 512;    // D buffer j: cols 160j .. 160j+159
 constexpr float kTcErr = 6.3e-5f;          // 2^-14 + 2^-19 + fp64 rounding, rounded up
 
 struct ScanSmem {
-  uint8_t stage[kStages][kStageBytes];     // keys, 1024-aligned (swizzle atoms)
-  uint8_t kabs[2][kStageBytes];            // |keys|, same layout
-  uint8_t qp[32 * 128];                    // B of D: rows 0-15 q1 (head h), 16-31 r1
-  uint8_t qa[16 * 128];                    // B of D2: ceil(|Qs|)
-  uint64_t full[kStages], empty[kStages];
-  uint64_t a_full[2], a_empty[2], d_full[2], d_empty[2];
+  uint8_t stage[kStages][kStageStride];    // keys, then query pieces; 1024-aligned
+  uint8_t qp[kQpBytes];                    // the current sequence's pieces (query group)
+  float uq[2][kMaxIdxHeads][128];          // [epilogue group]: |w'_h| (|q1_hc| + |r1_hc|)
+  int64_t win_row[kStages * 16];           // Reindex producer: rows of a window's pool blocks
+  int32_t win_n[kStages * 16];             //   and their rows inside the context
+  float red[2][4];
+  uint64_t full[kStages], empty[kStages], hdr[kStages];
+  uint64_t d_full[kDBufs], d_empty[kDBufs];
   uint32_t tmem_slot;
-  float qmax[2][kMaxIdxHeads];             // [group]: per-head max |q|
-  float qerr[2][kMaxIdxHeads];             // [group]: per-head sum of split errors
-  float wq[kMaxIdxHeads];                  // epilogue: w_h 2^-e_h
-  float wq_abs[kMaxIdxHeads];
-  float q_extra;
+  float qmax[3][kMaxIdxHeads];             // [group: query, epilogue 0, epilogue 1]: max |q_h|
+  float qerr[2][kMaxIdxHeads];             // [epilogue group]: per-head sum of split errors
+  float wq[2][kMaxIdxHeads];               // [epilogue group]: w_h 2^-e_h
+  float unorm[2];                          // [epilogue group]: ||u||_2, rounded up
+  float q_extra[2];
   volatile int32_t abort_flag;
 };
 
@@ -151,27 +166,31 @@ __device__ inline void issue_tile_load(const IdxArgs& a, const CUtensorMap* map,
 }
 
 // Reindex tiles: the pool blocks are scattered 1 KB runs (8 rows, never
-// across a page), so the whole producer warp gathers them with 16-byte
+// across a page).  The producer warp first resolves the rows of the blocks
+// of a window of up to kStages tiles (pool id, then page table: the loads of
+// all blocks are in flight together), then gathers each tile with 16-byte
 // cp.async copies straight into the 128-byte swizzled layout; each lane's
 // copies arrive on the stage's mbarrier when they land (32 arrivals).
-__device__ inline void gather_pool_tile(const IdxArgs& a, ScanSmem& sm, const TileRef& tr, int stage, int lane) {
-  int64_t rowj = -1;
-  int nrow = 0;                                          // rows of the block inside the context
-  if (lane < kTile / kBlock && lane * kBlock < tr.nvalid) {
-    const bool paged = a.page_table != nullptr;
-    const int64_t n_ctx = checked_ctx(a.ctx_len, a.d, tr.b, paged, a.ws);
-    const int32_t blk = __ldg(a.pool_in + int64_t(tr.b) * a.d.pool_blocks + (tr.t0 >> 3) + lane);
-    if (blk >= 0 && int64_t(blk) * kBlock < n_ctx) {
-      rowj = kv_row(a.page_table, a.d, tr.b, int64_t(blk) * kBlock, a.ws);
-      nrow = int(min64(kBlock, n_ctx - int64_t(blk) * kBlock));
-    }
+__device__ inline void resolve_block(const IdxArgs& a, const TileRef& tr, int j, int64_t& row, int& nrow) {
+  row = -1;
+  nrow = 0;
+  if (j * kBlock >= tr.nvalid) return;
+  const bool paged = a.page_table != nullptr;
+  const int64_t n_ctx = checked_ctx(a.ctx_len, a.d, tr.b, paged, a.ws);
+  const int32_t blk = __ldg(a.pool_in + int64_t(tr.b) * a.d.pool_blocks + (tr.t0 >> 3) + j);
+  if (blk >= 0 && int64_t(blk) * kBlock < n_ctx) {
+    row = kv_row(a.page_table, a.d, tr.b, int64_t(blk) * kBlock, a.ws);
+    nrow = row >= 0 ? int(min64(kBlock, n_ctx - int64_t(blk) * kBlock)) : 0;
   }
+}
+
+__device__ inline void gather_pool_tile(const IdxArgs& a, ScanSmem& sm, int w, int stage, int lane) {
   const uint8_t* keys = reinterpret_cast<const uint8_t*>(a.idx_k);
   const uint32_t dst0 = tc::smem_u32(sm.stage[stage]);
 #pragma unroll 4
   for (int m = 0; m < 32; ++m) {                         // copy i = lane + 32m: block m/2
-    const int64_t rj = __shfl_sync(0xFFFFFFFFu, rowj, m >> 1);
-    const int nr = __shfl_sync(0xFFFFFFFFu, nrow, m >> 1);
+    const int64_t rj = sm.win_row[w * 16 + (m >> 1)];
+    const int nr = sm.win_n[w * 16 + (m >> 1)];
     const int rin = 4 * (m & 1) + (lane >> 3), c = lane & 7;
     if (rj < 0 || rin >= nr) continue;
     const int r = (m >> 1) * kBlock + rin;
@@ -193,13 +212,19 @@ __device__ inline int head_shift(float qm) { return qm > 0.0f ? max(-60, min(60,
 // gt owns head gt/8, channels 16*(gt%8) .. +15; named barrier `bar_id`):
 //   e_h: max |q_h| 2^e_h in [2^7, 2^8);  Qs = q 2^e_h = q1 + r1 (E4M3 pieces);
 //   err_h = sum_c |Qs - q1 - r1| (nonzero only where r1 underflows E4M3).
-// The |k| group (operands = true) writes q1, r1 and ceil(|Qs|) as the
-// 128-byte swizzled K-major B operands; the epilogue group derives
-// w'_h = w_h 2^-e_h and the query rounding term 448 sum_h |w'_h| err_h.
-__device__ void query_split(const IdxArgs& a, ScanSmem& sm, int b, int gt, bool operands, int bar_id) {
+// The query group (operands = true) writes q1 and r1 as 32 rows of the
+// 128-byte swizzled K-major layout into sm.qp; the epilogue group (operands
+// = false) derives w'_h = w_h 2^-e_h, ||u||_2 with u_c = sum_h |w'_h|
+// (|q1_hc| + |r1_hc|), and the query rounding term 448 sum_h |w'_h| err_h,
+// all rounded up where they bound an error.
+__device__ void query_split(const IdxArgs& a, ScanSmem& sm, int b, int gt, int grp, int bar_id) {
   const int hi = a.d.idx_heads;
-  const int grp = operands ? 0 : 1;
-  if (gt < kMaxIdxHeads) { sm.qmax[grp][gt] = 0.0f; sm.qerr[grp][gt] = 0.0f; }
+  const bool operands = grp == 0;
+  const int eg = grp - 1;                                  // epilogue group
+  if (gt < kMaxIdxHeads) {
+    sm.qmax[grp][gt] = 0.0f;
+    if (!operands) sm.qerr[eg][gt] = 0.0f;
+  }
   group_sync(bar_id);
   const int h = gt >> 3, c0 = (gt & 7) * 16;
   float qv[16];
@@ -213,7 +238,8 @@ __device__ void query_split(const IdxArgs& a, ScanSmem& sm, int b, int gt, bool 
   atomicMax(reinterpret_cast<int*>(&sm.qmax[grp][h]), __float_as_int(mx));
   group_sync(bar_id);
   const int e = head_shift(sm.qmax[grp][h]);
-  uint32_t w1[4] = {0, 0, 0, 0}, w2[4] = {0, 0, 0, 0}, wa[4] = {0, 0, 0, 0};
+  const float wabs = fabsf(ldexpf(h < hi ? a.w[int64_t(b) * hi + h] : 0.0f, -e));
+  uint32_t w1[4] = {0, 0, 0, 0}, w2[4] = {0, 0, 0, 0};
   float err = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
@@ -224,36 +250,40 @@ __device__ void query_split(const IdxArgs& a, ScanSmem& sm, int b, int gt, bool 
     const uint32_t c2 = e4m3_rn(r);
     const float d2 = e4m3_val(c2);
     err = __fadd_ru(err, fabsf(r - d2));                   // r - d2 exact
-    uint32_t ca = e4m3_rn(fabsf(x));
-    if (e4m3_val(ca) < fabsf(x) && ca < 0x7Eu) ++ca;       // next larger E4M3 magnitude
+    if (!operands) sm.uq[eg][h][c0 + i] = __fmul_ru(wabs, fabsf(d1) + fabsf(d2));   // the sum is exact
     w1[i >> 2] |= c1 << (8 * (i & 3));
     w2[i >> 2] |= c2 << (8 * (i & 3));
-    wa[i >> 2] |= ca << (8 * (i & 3));
   }
   if (operands) {
     const uint32_t chunk = uint32_t(c0 >> 4);
     *reinterpret_cast<uint4*>(sm.qp + tc::sw128_offset(h, chunk)) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
     *reinterpret_cast<uint4*>(sm.qp + tc::sw128_offset(16 + h, chunk)) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-    *reinterpret_cast<uint4*>(sm.qa + tc::sw128_offset(h, chunk)) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
-    tc::fence_proxy_async_smem();
-  } else if (err > 0.0f) {
-    atomicAdd(&sm.qerr[grp][h], err);
+    group_sync(bar_id);
+    return;
+  }
+  if (err > 0.0f) atomicAdd(&sm.qerr[eg][h], err);
+  if (gt < kMaxIdxHeads) {
+    const float w = gt < hi ? a.w[int64_t(b) * hi + gt] : 0.0f;
+    sm.wq[eg][gt] = ldexpf(w, -head_shift(sm.qmax[grp][gt]));
   }
   group_sync(bar_id);
-  if (!operands) {
-    if (gt < kMaxIdxHeads) {
-      const float w = gt < hi ? a.w[int64_t(b) * hi + gt] : 0.0f;
-      sm.wq[gt] = ldexpf(w, -head_shift(sm.qmax[grp][gt]));
-      sm.wq_abs[gt] = fabsf(sm.wq[gt]);
-    }
-    group_sync(bar_id);
-    if (gt == 0) {
-      float x = 0.0f;
-      for (int i = 0; i < hi; ++i) x = __fmaf_ru(sm.wq_abs[i], __fmul_ru(sm.qerr[grp][i], 1.001f), x);
-      sm.q_extra = __fmul_ru(x, 448.0f);
-    }
-    group_sync(bar_id);
+  // ||u||^2: channel gt's u_c, squared and summed over the group, rounded up
+  float uc = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kMaxIdxHeads; ++i) uc = __fadd_ru(uc, sm.uq[eg][i][gt]);
+  float sq = __fmul_ru(uc, uc);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) sq = __fadd_ru(sq, __shfl_xor_sync(0xFFFFFFFFu, sq, o));
+  if ((gt & 31) == 0) sm.red[eg][gt >> 5] = sq;
+  group_sync(bar_id);
+  if (gt == 0) {
+    const float* rd = sm.red[eg];
+    sm.unorm[eg] = __fsqrt_ru(__fadd_ru(__fadd_ru(rd[0], rd[1]), __fadd_ru(rd[2], rd[3])));
+    float x = 0.0f;
+    for (int i = 0; i < hi; ++i) x = __fmaf_ru(fabsf(sm.wq[eg][i]), __fmul_ru(sm.qerr[eg][i], 1.001f), x);
+    sm.q_extra[eg] = __fmul_ru(x, 448.0f);
   }
+  group_sync(bar_id);
 }
 
 // Bounded wait that also gives up once another role has aborted.
@@ -261,7 +291,7 @@ __device__ inline bool wait_or_abort(ScanSmem& sm, uint64_t* bar, uint32_t parit
   if (tc::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = tc::globaltimer_ns();
   while (true) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
+    if (tc::mbar_try_wait_sleep(bar, parity, 100000u)) return true;   // sleeps until the phase (<= 0.1 ms)
     if (sm.abort_flag) return false;
     if (tc::globaltimer_ns() - t0 > 200ull * 1000 * 1000) {
       sm.abort_flag = 1;
@@ -274,29 +304,56 @@ __device__ inline void arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
 }
 
-// Epilogue of one tile for the thread owning row r: scores, bounds, block
-// maxima, writes.
-__device__ inline void scan_epilogue(const IdxArgs& a, bool reindex, const ScanSmem& sm,
-                                     const TileRef& pt, uint32_t tmem_d, int r, int lane) {
-  float dv[32], d2[16];
-  tc::tmem_ld32(tmem_d, dv);
-  tc::tmem_ld16(tmem_d + 32, d2);
-  bool valid = r < pt.nvalid;
-  if (reindex && valid) {
-    const bool paged = a.page_table != nullptr;
-    const int64_t n_ctx = checked_ctx(a.ctx_len, a.d, pt.b, paged, a.ws);
-    const int64_t item = pt.t0 + r;
-    int32_t blk = __ldg(a.pool_in + int64_t(pt.b) * a.d.pool_blocks + (item >> 3));
-    int64_t t = int64_t(blk) * kBlock + (item & 7);
-    valid = blk >= 0 && t < n_ctx && kv_row(a.page_table, a.d, pt.b, int64_t(blk) * kBlock, a.ws) >= 0;
-  }
-  float v = 0.0f, bnd = 0.0f;
+// Whether row r of the tile is a position to score (issued before the
+// epilogue waits for the MMA, so that its loads overlap the wait).
+__device__ inline bool row_valid(const IdxArgs& a, bool reindex, const TileRef& pt, int r) {
+  if (r >= pt.nvalid) return false;
+  if (!reindex) return true;
+  const bool paged = a.page_table != nullptr;
+  const int64_t n_ctx = checked_ctx(a.ctx_len, a.d, pt.b, paged, a.ws);
+  const int64_t item = pt.t0 + r;
+  const int32_t blk = __ldg(a.pool_in + int64_t(pt.b) * a.d.pool_blocks + (item >> 3));
+  const int64_t t = int64_t(blk) * kBlock + (item & 7);
+  return blk >= 0 && t < n_ctx && kv_row(a.page_table, a.d, pt.b, int64_t(blk) * kBlock, a.ws) >= 0;
+}
+
+// Both 32-column loads of a row, then one wait.
+__device__ inline void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&va)[32], float (&vb)[32]) {
+  uint32_t ra[32], rb[32];
+#define CSA2_LD32(R, T)                                                                                 \
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "                                               \
+               "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "                \
+               "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];" \
+               : "=r"(R[0]), "=r"(R[1]), "=r"(R[2]), "=r"(R[3]), "=r"(R[4]), "=r"(R[5]), "=r"(R[6]),      \
+                 "=r"(R[7]), "=r"(R[8]), "=r"(R[9]), "=r"(R[10]), "=r"(R[11]), "=r"(R[12]), "=r"(R[13]),  \
+                 "=r"(R[14]), "=r"(R[15]), "=r"(R[16]), "=r"(R[17]), "=r"(R[18]), "=r"(R[19]),            \
+                 "=r"(R[20]), "=r"(R[21]), "=r"(R[22]), "=r"(R[23]), "=r"(R[24]), "=r"(R[25]),            \
+                 "=r"(R[26]), "=r"(R[27]), "=r"(R[28]), "=r"(R[29]), "=r"(R[30]), "=r"(R[31])             \
+               : "r"(T))
+  CSA2_LD32(ra, ta);
+  CSA2_LD32(rb, tb);
+#undef CSA2_LD32
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int h = 0; h < 16; ++h) {
-    v = __fmaf_rn(sm.wq[h], fmaxf(dv[h] + dv[16 + h], 0.0f), v);
-    bnd = __fmaf_ru(sm.wq_abs[h], d2[h], bnd);
-  }
-  float delta = __fadd_ru(__fmul_ru(__fmul_ru(bnd, 1.0003f), kTcErr), sm.q_extra);
+  for (int i = 0; i < 32; ++i) { va[i] = __uint_as_float(ra[i]); vb[i] = __uint_as_float(rb[i]); }
+}
+
+// Epilogue of one tile for the thread owning row r (TMEM lanes of warp
+// quarter q = r / 32) of epilogue group eg: scores, bounds, block maxima,
+// writes.
+__device__ inline void scan_epilogue(const IdxArgs& a, bool reindex, const ScanSmem& sm, int eg,
+                                     const TileRef& pt, uint32_t tmem_d, bool valid, int r, int lane) {
+  float dv[32], gv[32];
+  tmem_ld32x2(tmem_d + kTile, tmem_d + (r & ~31), dv, gv);   // k . q1_h, k . r1_h; Gram columns
+  float g = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) g = i == lane ? gv[i] : g;   // the diagonal element
+  float v = 0.0f;
+#pragma unroll
+  for (int h = 0; h < 16; ++h) v = __fmaf_rn(sm.wq[eg][h], fmaxf(dv[h] + dv[16 + h], 0.0f), v);
+  // ||k||^2 from the MMA is low by at most 2^-14 of itself: raise it by 2^-13
+  const float knorm = __fsqrt_ru(__fmul_ru(fmaxf(g, 0.0f), 1.0f + 0x1p-13f));
+  float delta = __fadd_ru(__fmul_ru(__fmul_ru(__fmul_ru(knorm, sm.unorm[eg]), 1.0003f), kTcErr), sm.q_extra[eg]);
   if (!valid) { v = -INFINITY; delta = 0.0f; }
   float bmax = v, bd = delta;
 #pragma unroll
@@ -321,7 +378,15 @@ __device__ inline void scan_epilogue(const IdxArgs& a, bool reindex, const ScanS
   }
 }
 
-__device__ inline uint32_t parity_of(int64_t k, int n) { return uint32_t((k / n) & 1); }
+// Ring position of a role: stage and the parity of its current use, advanced
+// once per tile (no 64-bit division on the single-thread paths).
+struct Ring {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ void next() {
+    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+  }
+};
 
 __global__ void __launch_bounds__(kScanThreads, 1)
     scan_tc_kernel(IdxArgs a, const __grid_constant__ CUtensorMap kmap, bool reindex) {
@@ -349,10 +414,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&sm.full[s], reindex ? 32 : 1);     // 32 cp.async lanes or one TMA arrive
       tc::mbar_init(&sm.empty[s], 1);
+      tc::mbar_init(&sm.hdr[s], 4);
     }
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&sm.a_full[i], 4);
-      tc::mbar_init(&sm.a_empty[i], 1);
+    for (int i = 0; i < kDBufs; ++i) {
       tc::mbar_init(&sm.d_full[i], 1);
       tc::mbar_init(&sm.d_empty[i], 4);
     }
@@ -363,16 +427,34 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   __syncthreads();
   tc::tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_slot;
-  const int64_t ntiles = g1 - g0;
+  const int ntiles = int(g1 - g0);
 
   if (wid == 0 && reindex) {
     // ================= producer: cp.async gather of pool blocks =================
-    int pb = 0;
-    int64_t pbase = 0;
-    for (int64_t k = 0; k < ntiles; ++k) {
-      const int stage = int(k % kStages);
-      if (k >= kStages && !wait_or_abort(sm, &sm.empty[stage], parity_of(k - kStages, kStages))) break;
-      gather_pool_tile(a, sm, tile_of(a, reindex, g0 + k, pb, pbase), stage, lane);
+    int hb = 0;
+    int64_t hbase = 0;
+    bool stop = false;
+    Ring ring;
+    for (int k0 = 0; k0 < ntiles && !stop; k0 += kStages) {
+      const int nwin = min(kStages, ntiles - k0);
+      for (int idx = lane; idx < nwin * 16; idx += 32) {  // tiles visited in order per lane
+        const TileRef tr = tile_of(a, reindex, g0 + k0 + idx / 16, hb, hbase);
+        int64_t row;
+        int nrow;
+        resolve_block(a, tr, idx % 16, row, nrow);
+        sm.win_row[idx] = row;
+        sm.win_n[idx] = nrow;
+      }
+      __syncwarp();
+      for (int w = 0; w < nwin; ++w, ring.next()) {
+        const int k = k0 + w;
+        if (k >= kStages && !wait_or_abort(sm, &sm.empty[ring.stage], ring.phase ^ 1u)) {
+          stop = true;
+          break;
+        }
+        gather_pool_tile(a, sm, w, ring.stage, lane);
+      }
+      __syncwarp();
     }
     asm volatile("cp.async.wait_all;" ::: "memory");     // nothing in flight when the CTA exits
   } else if (wid == 0) {
@@ -380,100 +462,90 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     if (lane == 0) {
       int pb = 0;
       int64_t pbase = 0;
-      int64_t k = 0;
-      for (; k < ntiles; ++k) {
-        const int stage = int(k % kStages);
-        if (k >= kStages && !wait_or_abort(sm, &sm.empty[stage], parity_of(k - kStages, kStages))) break;
-        issue_tile_load(a, &kmap, sm, tile_of(a, reindex, g0 + k, pb, pbase), stage);
+      int k = 0;
+      Ring ring;
+      for (; k < ntiles; ++k, ring.next()) {
+        if (k >= kStages && !wait_or_abort(sm, &sm.empty[ring.stage], ring.phase ^ 1u)) break;
+        issue_tile_load(a, &kmap, sm, tile_of(a, reindex, g0 + k, pb, pbase), ring.stage);
       }
       // after an abort, let the copies still in flight land before the CTA exits
       if (sm.abort_flag)
-        for (int64_t j = max64(0, k - kStages); j < k; ++j)
-          tc::mbar_wait_bounded(&sm.full[j % kStages], parity_of(j, kStages), 20ull * 1000 * 1000);
+        for (int j = max(0, k - kStages); j < k; ++j)
+          tc::mbar_wait_bounded(&sm.full[j % kStages], uint32_t((j / kStages) & 1), 20ull * 1000 * 1000);
     }
   } else if (wid == 1) {
     // ================= MMA issuer =================
     if (lane == 0) {
-      constexpr uint32_t id_d = idesc_e4m3(kTile, 32), id_d2 = idesc_e4m3(kTile, 16);
+      constexpr uint32_t idesc = idesc_e4m3(kTile, kMmaN);
       // descriptors are formed once; an offset of x bytes adds x/16 to the
       // start-address field (every operand lies below 256 KB, so it never carries)
-      const uint64_t dq = tc::smem_desc(tc::smem_u32(sm.qp), 16, 1024, 2);
-      const uint64_t dqa = tc::smem_desc(tc::smem_u32(sm.qa), 16, 1024, 2);
-      const uint64_t dk0 = tc::smem_desc(tc::smem_u32(sm.stage[0]), 16, 1024, 2);
-      const uint64_t dka0 = tc::smem_desc(tc::smem_u32(sm.kabs[0]), 16, 1024, 2);
-      int64_t issued = 0;
-      for (int64_t k = 0; k < ntiles; ++k) {
-        const int stage = int(k % kStages);
-        const uint32_t buf = uint32_t(k & 1);
-        if (!wait_or_abort(sm, &sm.a_full[buf], parity_of(k, 2))) break;
-        if (!wait_or_abort(sm, &sm.full[stage], parity_of(k, kStages))) break;
-        if (k >= 2 && !wait_or_abort(sm, &sm.d_empty[buf], parity_of(k - 2, 2))) break;
+      const uint64_t d0 = tc::smem_desc(tc::smem_u32(sm.stage[0]), 16, 1024, 2);
+      int issued = 0;
+      Ring ring;
+      for (int k = 0; k < ntiles; ++k, ring.next()) {
+        const int stage = ring.stage;
+        const int buf = k % kDBufs;
+        if (!wait_or_abort(sm, &sm.full[stage], ring.phase)) break;   // keys
+        if (!wait_or_abort(sm, &sm.hdr[stage], ring.phase)) break;    // query pieces
+        if (k >= kDBufs && !wait_or_abort(sm, &sm.d_empty[buf], uint32_t((k / kDBufs - 1) & 1))) break;
         tc::tc_fence_after_sync();
         if (reindex) tc::fence_proxy_async_smem();       // the gathered keys are generic-proxy writes
-        const uint64_t dk = dk0 + uint64_t(stage) * (kStageBytes >> 4);
-        const uint64_t dka = dka0 + uint64_t(buf) * (kStageBytes >> 4);
-        const uint32_t dcol = tmem + 64 * buf;
+        const uint64_t ds = d0 + uint64_t(stage) * (kStageStride >> 4);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {                 // K = 32 E4M3 (32 bytes) per step
-          mma_f8(dcol, dk + 2 * ks, dq + 2 * ks, id_d, ks > 0);
-          mma_f8(dcol + 32, dka + 2 * ks, dqa + 2 * ks, id_d2, ks > 0);
-        }
+        for (int ks = 0; ks < 4; ++ks)                   // K = 32 E4M3 (32 bytes) per step
+          mma_f8(tmem + kMmaN * buf, ds + 2 * ks, ds + 2 * ks, idesc, ks > 0);
         tc::mma_commit(&sm.empty[stage]);
-        tc::mma_commit(&sm.a_empty[buf]);
         tc::mma_commit(&sm.d_full[buf]);
         issued = k + 1;
       }
       // after an abort, let the issued MMAs finish before the tensor memory is freed
       if (sm.abort_flag && issued > 0)
-        tc::mbar_wait_bounded(&sm.d_full[(issued - 1) & 1], parity_of(issued - 1, 2), 20ull * 1000 * 1000);
+        tc::mbar_wait_bounded(&sm.d_full[(issued - 1) % kDBufs], uint32_t(((issued - 1) / kDBufs) & 1),
+                              20ull * 1000 * 1000);
     }
   } else if (wid < 6) {
-    // ================= |k| and query operands (warps 2-5) =================
+    // ================= query group (warps 2-5): pieces behind each tile's keys =====
     const int gt = tid - 64;
     int cb = 0, cur_b = -1;
     int64_t cbase = 0;
-    for (int64_t k = 0; k < ntiles; ++k) {
+    Ring ring;
+    for (int k = 0; k < ntiles; ++k, ring.next()) {
       const TileRef tr = tile_of(a, reindex, g0 + k, cb, cbase);
+      const int stage = ring.stage;
       if (tr.b != cur_b) {
-        // every MMA of the previous tiles must have read the old operands
-        if (k > 0 && !wait_or_abort(sm, &sm.d_full[(k - 1) & 1], parity_of(k - 1, 2))) break;
-        query_split(a, sm, tr.b, gt, true, 1);
+        query_split(a, sm, tr.b, gt, 0, 1);
         cur_b = tr.b;
       }
-      const int stage = int(k % kStages);
-      const uint32_t buf = uint32_t(k & 1);
-      if (!wait_or_abort(sm, &sm.full[stage], parity_of(k, kStages))) break;
-      if (k >= 2 && !wait_or_abort(sm, &sm.a_empty[buf], parity_of(k - 2, 2))) break;
-      const uint4* src = reinterpret_cast<const uint4*>(sm.stage[stage]);
-      uint4* dst = reinterpret_cast<uint4*>(sm.kabs[buf]);
+      // the stage is free once the MMAs of its previous tile completed
+      if (k >= kStages && !wait_or_abort(sm, &sm.empty[stage], ring.phase ^ 1u)) break;
+      const uint4* src = reinterpret_cast<const uint4*>(sm.qp);
+      uint4* dst = reinterpret_cast<uint4*>(sm.stage[stage] + kKeyBytes);
 #pragma unroll
-      for (int i = 0; i < kStageBytes / 16 / kGroupThreads; ++i) {
-        uint4 v = src[gt + i * kGroupThreads];
-        v.x &= 0x7F7F7F7Fu; v.y &= 0x7F7F7F7Fu; v.z &= 0x7F7F7F7Fu; v.w &= 0x7F7F7F7Fu;
-        dst[gt + i * kGroupThreads] = v;
-      }
+      for (int i = 0; i < kQpBytes / 16 / kGroupThreads; ++i) dst[gt + i * kGroupThreads] = src[gt + i * kGroupThreads];
       tc::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) arrive(&sm.a_full[buf]);
+      if (lane == 0) arrive(&sm.hdr[stage]);
     }
   } else {
-    // ================= epilogue (warps 6-9) =================
-    const int gt = tid - 192;
+    // ================= epilogue groups (warps 6-9: even tiles, 10-13: odd) ==========
+    const int eg = (wid - 6) >> 2;
+    const int gt = tid - 192 - eg * kGroupThreads;
     const int quarter = wid & 3;                      // TMEM lanes 32*quarter ..
     const int r = quarter * 32 + lane;                // row of the tile
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
     int cb = 0, cur_b = -1;
     int64_t cbase = 0;
-    for (int64_t k = 0; k < ntiles; ++k) {
+    for (int k = eg; k < ntiles; k += 2) {
       const TileRef tr = tile_of(a, reindex, g0 + k, cb, cbase);
       if (tr.b != cur_b) {
-        query_split(a, sm, tr.b, gt, false, 2);
+        query_split(a, sm, tr.b, gt, 1 + eg, 2 + eg);
         cur_b = tr.b;
       }
-      const uint32_t buf = uint32_t(k & 1);
-      if (!wait_or_abort(sm, &sm.d_full[buf], parity_of(k, 2))) break;
+      const bool valid = row_valid(a, reindex, tr, r);
+      const int buf = k % kDBufs;
+      if (!wait_or_abort(sm, &sm.d_full[buf], uint32_t((k / kDBufs) & 1))) break;
       tc::tc_fence_after_sync();
-      scan_epilogue(a, reindex, sm, tr, tmem + lane_base + 64 * buf, r, lane);
+      scan_epilogue(a, reindex, sm, eg, tr, tmem + lane_base + kMmaN * buf, valid, r, lane);
       tc::tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) arrive(&sm.d_empty[buf]);
