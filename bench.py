@@ -299,9 +299,13 @@ def main():
     csa2.profile_enable(True)
     n_prof_steps = 3
     for _ in range(n_prof_steps):
-        flush.fill_(3)
+        # the flush and the whole step are enqueued before any wait, so the
+        # GPU runs them back to back and each event pair times GPU work only
+        # (not the host's enqueue of the next call)
         torch.cuda.synchronize()
+        flush.fill_(3)
         cur = None
+        marks = []
         for l, m in enumerate(sb.schedule):
             e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             e0.record(st)
@@ -318,7 +322,9 @@ def main():
                                          sb.kv_rope, sb.page_table, sb.ctx_len, sb.topk[cur], sb.swa[l],
                                          sb.swa_len[l], sb.scale, sb.out[l], sb.lse[l], sb.ws)
             e2.record(st)
-            torch.cuda.synchronize()
+            marks.append((m, e0, e1, e2))
+        torch.cuda.synchronize()
+        for m, e0, e1, e2 in marks:
             if m == "F":
                 per["F_index"].append(e0.elapsed_time(e1))
             elif m == "Ri":

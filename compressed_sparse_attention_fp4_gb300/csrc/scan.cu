@@ -59,7 +59,7 @@ namespace csa2 {
 constexpr int kScanThreads = 448;          // warp 0 TMA, 1 MMA, 2-5 query, 6-9 / 10-13 epilogue
 constexpr int kGroupThreads = 128;         // threads of the query group and of each epilogue group
 constexpr int kTile = 128;                 // positions per tile (= MMA M)
-constexpr int kStages = 6;                 // ring depth
+constexpr int kStages = 10;                // ring depth
 constexpr int kKeyBytes = kTile * 128;     // 16 KB of E4M3 keys
 constexpr int kQpBytes = 32 * 128;         // q1 (16 rows) + r1 (16 rows)
 constexpr int kStageStride = kKeyBytes + kQpBytes;
@@ -151,6 +151,13 @@ __device__ inline TileRef tile_of(const IdxArgs& a, bool reindex, int64_t g, int
 
 __device__ inline void issue_tile_load(const IdxArgs& a, const CUtensorMap* map, ScanSmem& sm,
                                        const TileRef& tr, int stage) {
+  if (a.page_table == nullptr) {
+    // contiguous cache: the tile is one run of 128 rows (rows past the
+    // sequence are the next one's or, past the tensor, zero-filled)
+    tc::mbar_expect_tx(&sm.full[stage], kKeyBytes);
+    tc::tma_load_2d(map, sm.stage[stage], 0, int32_t(int64_t(tr.b) * a.d.max_ctx + tr.t0), &sm.full[stage]);
+    return;
+  }
   uint32_t bytes = 0;
   int32_t rows[2];
   int nbox = (tr.nvalid > 64) ? 2 : 1;
@@ -582,7 +589,7 @@ cudaError_t launch_scan_tc(const IdxArgs& a, bool reindex, cudaStream_t st) {
   CUtensorMap map;
   cuuint64_t gdim[2] = {128, rows};
   cuuint64_t gstride[1] = {128};
-  cuuint32_t box[2] = {128, reindex ? uint32_t(kBlock) : 64u};   // one pool block / half a tile
+  cuuint32_t box[2] = {128, paged ? 64u : 128u};   // a page (64 positions) or a whole tile
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.idx_k), gdim, gstride, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
