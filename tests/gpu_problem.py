@@ -60,6 +60,18 @@ def make_problem(ctx_lens, Hi=16, Di=128, dtype="fp8", P=2048, K=512, H=64, W=12
     else:
         dev_k = np.zeros((rows, Di), dtype=np.float32)
     for b, n in enumerate(ctx_lens):
+        if kind in ("trunc", "cancel"):
+            # E4M3 codes built directly: channel 0 (and 1) at 448, the rest small
+            # positive values just below a power of two (worst case for products
+            # truncated against the largest one of an MMA step)
+            raw = ((rng.integers(1, 6, (n, Di)) << 3) | 7).astype(np.uint8)
+            raw[:, 0] = 0x7E
+            if kind == "cancel":
+                raw[:, 1] = 0x7E
+            raw[:, 32::32] = 0x7E                      # one large product in every K step
+            p.idx_k_raw.append(raw)
+            dev_k[p.rows_of[b]] = raw
+            continue
         if kind == "ties":
             base = rng.standard_normal((3, Di)).astype(np.float32) * scale_ch
             k = base[rng.integers(0, 3, n)]
@@ -70,6 +82,12 @@ def make_problem(ctx_lens, Hi=16, Di=128, dtype="fp8", P=2048, K=512, H=64, W=12
         dev_k[p.rows_of[b]] = raw
     p.idx_k = torch.from_numpy(dev_k).cuda()
     q = rng.standard_normal((B, Hi, Di)).astype(np.float32)
+    if kind in ("trunc", "cancel"):
+        q = np.abs(q) * np.float32(2.0 ** -7)
+        q[:, :, 0] = 1.0
+        q[:, :, 32::32] = 1.0
+        if kind == "cancel":
+            q[:, :, 1] = -1.0                          # k0 q0 + k1 q1 = 0 exactly
     p.idx_q_raw = synth.to_bf16_bits(q) if dtype == "fp8" else q
     p.idx_q_f64 = bf16_f64(p.idx_q_raw) if dtype == "fp8" else q.astype(np.float64)
     p.idx_q = (torch.from_numpy(p.idx_q_raw.view(np.int16)).view(torch.bfloat16)

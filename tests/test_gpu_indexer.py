@@ -112,6 +112,29 @@ def test_error_bound_holds():
     print(f"max observed |v - s| / delta = {worst:.3g}")
 
 
+@pytest.mark.parametrize("kind", ["trunc", "cancel"])
+def test_error_bound_adversarial(kind):
+    """|v - s| <= delta when one product dominates every MMA step and the others
+    are small same-sign values just below a power of two (the case that loses
+    the most to truncation), and when the large products cancel exactly."""
+    p = make_problem([4096, 1000], seed=11, kind=kind, with_kv=False)
+    run_full(p)
+    off = ws_offsets(p.dims, p.B)
+    ws = p.ws.cpu().numpy()
+    pos = ws[off["pos_scores"]:off["pos_scores"] + p.B * p.dims.max_ctx * 4].view(np.float32)
+    dl = ws[off["blk_delta"]:off["blk_delta"] + p.B * off["nb_max"] * 4].view(np.float32)
+    worst = 0.0
+    for b in range(p.B):
+        n = p.ctx_lens[b]
+        s = oix.scores(p.idx_q_f64[b], p.w_raw[b].astype(np.float64), oracle_keys(p, b))
+        v = pos[b * p.dims.max_ctx: b * p.dims.max_ctx + n].astype(np.float64)
+        d = np.repeat(dl[b * off["nb_max"]: b * off["nb_max"] + (n + 7) // 8], 8)[:n].astype(np.float64)
+        err = np.abs(v - s)
+        assert np.all(err <= d), np.max(err / d)
+        worst = max(worst, float(np.max(err / d)))
+    print(f"{kind}: max observed |v - s| / delta = {worst:.3g}")
+
+
 def test_pool_len_and_padding_short_context():
     p = make_problem([3, 0 + 1, 40], P=2048, K=512, seed=8, with_kv=False)
     pool, plen, topk = run_full(p)
