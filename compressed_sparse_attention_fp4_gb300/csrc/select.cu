@@ -7,8 +7,11 @@
 // blocks of 8 as the pool, Reindex layers take Top-512 inside it).
 //
 //   U = v + delta (rounded up), L = v - delta (rounded down)
-//   mu'     >= P-th largest U     (upper edge of its 22-bit radix bucket)
-//   lambda' <= P-th largest L     (lower edge of its bucket)
+//   A radix select on v alone finds a bucket [v_lo, v_hi] holding the P-th
+//   largest v; with D = max delta over the items, the P-th largest U is at
+//   most v_hi + D and the P-th largest L at least v_lo - D, so
+//   mu'     = v_hi + D (rounded up)   >= P-th largest U
+//   lambda' = v_lo - D (rounded down) <= P-th largest L
 //   L > mu'              -> selected (its exact score beats the P-th best)
 //   U < lambda'          -> not selected
 //   otherwise ("band")   -> exact score (fixed point, exact.cuh), then the
@@ -57,6 +60,8 @@ struct SelSmem {
   uint32_t red[2][kSelWarps];
   uint32_t bucket[2], rem[2];
   uint32_t kmin, kmax, base_key;
+  float dmax, dmax_all, dred[kSelWarps];
+  uint32_t kmax_all;
   int shift0;
   uint32_t cnt_in, cnt_band, cnt_sel;
   uint32_t n_cand;
@@ -171,41 +176,59 @@ __device__ void find_buckets(SelSmem& sm) {
   __syncthreads();
 }
 
-// Cluster-wide radix localisation of the k-th largest key of keyU and of
-// keyL.  The keys are first mapped to [kmin, kmax] (cluster min / max over
-// the valid items), so that the 2048 bins of the first pass spread over the
-// occupied range; the second pass splits the chosen bin into 2048 more, which
-// leaves a final bucket of at most 2^10 keys.  Returns muEdge (>= k-th largest
-// U key) and lamEdge (<= k-th largest L key).
-__device__ void radix_edges(SelSmem& sm, const SelCtx& c, int n_local, uint32_t k,
-                            uint32_t& muEdge, uint32_t& lamEdge) {
+// Lower edge (offset from the base key) of the final bucket: the first-pass
+// bin b0 alone, or its refined sub-bin b1.
+__device__ inline uint32_t pass_lo(uint32_t b0, int sh0, uint32_t b1, int width_shift, int sh1) {
+  return width_shift == sh0 ? (b0 << sh0) : (b0 << sh0) + (b1 << sh1);
+}
+
+// Inverse of f32_key.
+__device__ inline float key_f32(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Cluster-wide radix localisation of the k-th largest v key (keyU; 0 marks
+// an invalid item).  kmin_l / kmax_l / dmax_l are this thread's minimum and
+// maximum valid key and maximum delta.  The first pass spreads 2048 bins over
+// the occupied key range; a second pass splits the chosen bin into 2048 more
+// only when it holds more than kRefine items.  Returns muEdge >= the k-th
+// largest U key and lamEdge <= the k-th largest L key (see the file comment).
+constexpr uint32_t kRefine = 64;
+
+__device__ void radix_edges(SelSmem& sm, const SelCtx& c, int n_local, uint32_t k, uint32_t kmin_l,
+                            uint32_t kmax_l, float dmax_l, uint32_t& muEdge, uint32_t& lamEdge) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  // ---- key range ----------------------------------------------------------
-  uint32_t mn = 0xFFFFFFFFu, mx = 0;
-  for (int i = tid; i < n_local; i += blockDim.x) {
-    uint32_t u = sm.keyU[i], l = sm.keyL[i];
-    if (u) { mn = min(mn, l); mx = max(mx, u); }
-  }
+  // ---- key range and the largest delta -------------------------------------------
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
-    mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
-    mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    kmin_l = min(kmin_l, __shfl_xor_sync(0xFFFFFFFFu, kmin_l, o));
+    kmax_l = max(kmax_l, __shfl_xor_sync(0xFFFFFFFFu, kmax_l, o));
+    dmax_l = fmaxf(dmax_l, __shfl_xor_sync(0xFFFFFFFFu, dmax_l, o));
   }
-  if (lane == 0) { sm.red[0][wid] = mn; sm.red[1][wid] = mx; }
+  if (lane == 0) { sm.red[0][wid] = kmin_l; sm.red[1][wid] = kmax_l; sm.dred[wid] = dmax_l; }
   __syncthreads();
   if (tid == 0) {
     uint32_t a0 = 0xFFFFFFFFu, a1 = 0;
-    for (int i = 0; i < kSelWarps; ++i) { a0 = min(a0, sm.red[0][i]); a1 = max(a1, sm.red[1][i]); }
+    float dm = 0.0f;
+    for (int i = 0; i < kSelWarps; ++i) { a0 = min(a0, sm.red[0][i]); a1 = max(a1, sm.red[1][i]); dm = fmaxf(dm, sm.dred[i]); }
     sm.kmin = a0;
     sm.kmax = a1;
+    sm.dmax = dm;
   }
   cl_sync(c);
   if (tid == 0) {
     uint32_t a0 = 0xFFFFFFFFu, a1 = 0;
-    for (int r = 0; r < c.cs; ++r) { a0 = min(a0, *remote(c, &sm.kmin, r)); a1 = max(a1, *remote(c, &sm.kmax, r)); }
+    float dm = 0.0f;
+    for (int r = 0; r < c.cs; ++r) {
+      a0 = min(a0, *remote(c, &sm.kmin, r));
+      a1 = max(a1, *remote(c, &sm.kmax, r));
+      dm = fmaxf(dm, *remote(c, &sm.dmax, r));
+    }
     sm.rem[0] = k;
     sm.rem[1] = k;
     sm.base_key = a0;
+    sm.kmax_all = a1;
+    sm.dmax_all = dm;
     uint32_t range = a1 - a0;
     int bits = range ? 32 - __clz(range) : 0;
     sm.shift0 = bits > 11 ? bits - 11 : 0;
@@ -213,38 +236,43 @@ __device__ void radix_edges(SelSmem& sm, const SelCtx& c, int n_local, uint32_t 
   cl_sync(c);       // the range is read before any rank overwrites kmin / kmax
   const uint32_t kb = sm.base_key;
   const int sh0 = sm.shift0, sh1 = sh0 > 11 ? sh0 - 11 : 0;
-  uint32_t b0U = 0, b0L = 0;
+  uint32_t b0 = 0;
+  int width_shift = sh0;
   for (int pass = 0; pass < 2; ++pass) {
     for (int i = tid; i < 2 * kBins; i += blockDim.x) (&sm.hist[0][0])[i] = 0;
     __syncthreads();
     const int sh = pass ? sh1 : sh0;
     for (int i = tid; i < n_local; i += blockDim.x) {
-      uint32_t u = sm.keyU[i];
+      const uint32_t u = sm.keyU[i];
       if (!u) continue;
-      uint32_t du = u - kb, dl = sm.keyL[i] - kb;
-      if (pass == 0) {
-        atomicAdd(&sm.hist[0][du >> sh], 1u);
-        atomicAdd(&sm.hist[1][dl >> sh], 1u);
-      } else {
-        // offset inside the first-pass bin, in units of 2^sh1 keys
-        if ((du >> sh0) == b0U) atomicAdd(&sm.hist[0][(du - (b0U << sh0)) >> sh], 1u);
-        if ((dl >> sh0) == b0L) atomicAdd(&sm.hist[1][(dl - (b0L << sh0)) >> sh], 1u);
-      }
+      const uint32_t du = u - kb;
+      if (pass == 0) atomicAdd(&sm.hist[0][du >> sh], 1u);
+      else if ((du >> sh0) == b0) atomicAdd(&sm.hist[0][(du - (b0 << sh0)) >> sh], 1u);
     }
     cl_sync(c);
-    for (int i = tid; i < 2 * kBins; i += blockDim.x) {
-      uint32_t s = 0;
-      for (int r = 0; r < c.cs; ++r) s += remote(c, &sm.hist[0][0], r)[i];
-      (&sm.ghist[0][0])[i] = s;
+    for (int i = tid; i < kBins; i += blockDim.x) {
+      uint32_t t = 0;
+      for (int r = 0; r < c.cs; ++r) t += remote(c, &sm.hist[0][0], r)[i];
+      sm.ghist[0][i] = t;
+      sm.ghist[1][i] = 0;
     }
     cl_sync(c);     // every rank has read every histogram before they are reset
     find_buckets(sm);
-    if (pass == 0) { b0U = sm.bucket[0]; b0L = sm.bucket[1]; }
+    if (pass == 0) {
+      b0 = sm.bucket[0];
+      if (sh0 == 0 || sm.ghist[0][b0] <= kRefine) break;    // narrow enough
+    } else {
+      width_shift = sh1;
+    }
   }
-  uint32_t lo_u = (b0U << sh0) + (sm.bucket[0] << sh1);
-  uint32_t lo_l = (b0L << sh0) + (sm.bucket[1] << sh1);
-  muEdge = kb + lo_u + ((1u << sh1) - 1);
-  lamEdge = kb + lo_l;
+  const uint32_t lo = pass_lo(b0, sh0, sm.bucket[0], width_shift, sh1);
+  // the bucket's top, clamped to the largest key (the k-th largest is below it)
+  const uint64_t hi64 = uint64_t(kb) + lo + ((uint64_t(1) << width_shift) - 1);
+  const uint32_t hi_key = hi64 > sm.kmax_all ? sm.kmax_all : uint32_t(hi64);
+  const float D = sm.dmax_all;
+  const float vlo = key_f32(kb + lo), vhi = key_f32(hi_key);
+  muEdge = f32_key(__fadd_ru(vhi, D));
+  lamEdge = f32_key(__fadd_rd(vlo, -D));
   __syncthreads();
 }
 
@@ -423,26 +451,33 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
   for (int i = tid; i < kSelCapPerCta / 32; i += blockDim.x) { sm.band_bits[i] = 0; sm.sel_bits[i] = 0; }
   if (tid == 0) { sm.cnt_in = 0; sm.cnt_band = 0; }
   __syncthreads();
+  uint32_t kmin_l = 0xFFFFFFFFu, kmax_l = 0;
+  float dmax_l = 0.0f;
   {
     // every item load of this thread is issued before any key is formed
     constexpr int kPer = kSelCapPerCta / kSelThreads;
-    ItemVal it[kPer];
+    float vv[kPer], dd[kPer];                        // dd < 0: not an item
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
       const int i = tid + j * kSelThreads;
-      it[j] = i < n_local ? load_item(a, kind, c, sm.pool_ids, base + i) : ItemVal{0.0f, 0.0f, false};
+      const ItemVal it = i < n_local ? load_item(a, kind, c, sm.pool_ids, base + i) : ItemVal{0.0f, 0.0f, false};
+      vv[j] = it.v;
+      dd[j] = it.valid ? it.delta : -1.0f;
     }
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
       const int i = tid + j * kSelThreads;
       if (i >= n_local) break;
-      uint32_t ku = 0, kl = 0;
-      if (it[j].valid) {
-        ku = f32_key(__fadd_ru(it[j].v, it[j].delta));
-        kl = f32_key(__fadd_rd(it[j].v, -it[j].delta));
+      uint32_t kv = 0, kd = 0;
+      if (dd[j] >= 0.0f) {
+        kv = f32_key(vv[j]);
+        kd = __float_as_uint(dd[j]);
+        kmin_l = min(kmin_l, kv);
+        kmax_l = max(kmax_l, kv);
+        dmax_l = fmaxf(dmax_l, dd[j]);
       }
-      sm.keyU[i] = ku;
-      sm.keyL[i] = kl;
+      sm.keyU[i] = kv;                               // v key (0: not an item)
+      sm.keyL[i] = kd;                               // delta bits
     }
   }
   __syncthreads();
@@ -451,11 +486,13 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
       if (sm.keyU[i]) atomicOr(&sm.sel_bits[i >> 5], 1u << (i & 31));
   } else {
     uint32_t muE, lamE;
-    radix_edges(sm, c, n_local, uint32_t(k), muE, lamE);
+    radix_edges(sm, c, n_local, uint32_t(k), kmin_l, kmax_l, dmax_l, muE, lamE);
     uint32_t my_in = 0, my_band = 0;
     for (int i = tid; i < n_local; i += blockDim.x) {
-      uint32_t u = sm.keyU[i], l = sm.keyL[i];
-      if (u == 0) continue;
+      const uint32_t kv = sm.keyU[i];
+      if (kv == 0) continue;
+      const float v = key_f32(kv), dl = __uint_as_float(sm.keyL[i]);
+      const uint32_t u = f32_key(__fadd_ru(v, dl)), l = f32_key(__fadd_rd(v, -dl));
       if (l > muE) { atomicOr(&sm.sel_bits[i >> 5], 1u << (i & 31)); ++my_in; }
       else if (u >= lamE) { atomicOr(&sm.band_bits[i >> 5], 1u << (i & 31)); ++my_band; }
     }
