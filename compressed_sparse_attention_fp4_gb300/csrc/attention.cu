@@ -130,6 +130,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int b = blockIdx.y, split = blockIdx.x;
   const int H = a.d.heads, K = a.d.topk, W = a.d.swa;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  // set-up that touches no global memory, then wait for the previous kernel
+  if (wid == 0) tc::tmem_alloc(&tmem_slot, kTmemCols);
+  if (tid == 0) {
+    tc::mbar_init(&bar_ld, 1);
+    tc::mbar_init(&bar_s, 1);
+    tc::mbar_init(&bar_o, 1);
+    tc::fence_mbar_init();
+  }
+  pdl_wait();
+  pdl_launch_dependents();
   const bool paged = a.page_table != nullptr;
   const bool swa_tma = split == swa_tma_split;      // this CTA's rows are the SWA window
   const int64_t n_ctx = checked_ctx(a.ctx_len, a.d, b, paged, a.ws);
@@ -154,13 +164,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       r = -2 - (slot - K);
     }
     row_s[tid] = r;
-  }
-  if (wid == 0) tc::tmem_alloc(&tmem_slot, kTmemCols);
-  if (tid == 0) {
-    tc::mbar_init(&bar_ld, 1);
-    tc::mbar_init(&bar_s, 1);
-    tc::mbar_init(&bar_o, 1);
-    tc::fence_mbar_init();
   }
   tc::tc_fence_before_sync();
   __syncthreads();
@@ -444,6 +447,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
   const int h = blockIdx.x, b = blockIdx.y, H = a.d.heads, S = a.L.splits;
+  pdl_wait();
+  pdl_launch_dependents();
   const float* o_base = reinterpret_cast<const float*>(a.ws + a.L.attn_o);
   const float* ml = reinterpret_cast<const float*>(a.ws + a.L.attn_ml);
   float M = -INFINITY;
@@ -512,32 +517,21 @@ cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(attn_partial_tc_kernel<true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(a.L.splits), unsigned(a.batch), 1);
-    cfg.blockDim = dim3(kAttnThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(a.L.splits);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     CSA2_PROFILED(st, "attn_fused_tc",
-                  (e = cudaLaunchKernelEx(&cfg, attn_partial_tc_kernel<true>, a, qmap, swamap, swa_split)));
+                  (e = launch_pdl(attn_partial_tc_kernel<true>, dim3(unsigned(a.L.splits), unsigned(a.batch), 1),
+                                  dim3(kAttnThreads), smem, st, unsigned(a.L.splits), a, qmap, swamap, swa_split)));
     return e;
   }
   cudaError_t e = cudaFuncSetAttribute(attn_partial_tc_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   CSA2_PROFILED(st, "attn_partial_tc",
-                (attn_partial_tc_kernel<false><<<dim3(unsigned(a.L.splits), unsigned(a.batch)), kAttnThreads, smem, st>>>(
-                    a, qmap, swamap, swa_split)));
-  e = cudaGetLastError();
+                (e = launch_pdl(attn_partial_tc_kernel<false>, dim3(unsigned(a.L.splits), unsigned(a.batch)),
+                                dim3(kAttnThreads), smem, st, 1, a, qmap, swamap, swa_split)));
   if (e != cudaSuccess) return e;
-  CSA2_PROFILED(st, "attn_combine", (attn_combine_kernel<<<dim3(unsigned(a.d.heads), unsigned(a.batch)), 128, 0, st>>>(a)));
-  return cudaGetLastError();
+  CSA2_PROFILED(st, "attn_combine", (e = launch_pdl(attn_combine_kernel, dim3(unsigned(a.d.heads), unsigned(a.batch)),
+                                                    dim3(128), 0, st, 1, a)));
+  return e;
 }
 
 }  // namespace csa2

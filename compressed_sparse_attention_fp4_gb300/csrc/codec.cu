@@ -23,6 +23,7 @@
 // share group g, and each lane stores 4 packed bytes (coalesced 128 B per
 // warp) and, for even lanes, one scale byte.
 #include "common.cuh"
+#include "kernels.cuh"
 #include "profile.cuh"
 
 namespace csa2 {
@@ -54,6 +55,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
   for (int64_t row = warp; row < n; row += nwarps) {
     int64_t dst = dst_rows ? dst_rows[row] : row;
     if (dst < 0) continue;
@@ -114,6 +117,8 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const uint2* __restrict
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
   for (int64_t row = warp; row < n; row += nwarps) {
     uint2 c = __ldcs(codes + row * 32 + lane);          // 16 nibbles = group `lane`
     uint32_t sc = scales[row * 32 + lane];
@@ -145,19 +150,22 @@ static int codec_grid(int64_t n) {
 cudaError_t launch_quantize(const uint16_t* x, int64_t n, const int64_t* dst_rows, uint8_t* codes,
                             uint8_t* scales, cudaStream_t st) {
   if (n == 0) return cudaSuccess;
+  cudaError_t e;
   CSA2_PROFILED(st, "fp4_quantize",
-                (quantize_kernel<<<codec_grid(n), 256, 0, st>>>(reinterpret_cast<const uint4*>(x), n, dst_rows,
-                                                                reinterpret_cast<uint32_t*>(codes), scales)));
-  return cudaGetLastError();
+                (e = launch_pdl(quantize_kernel, dim3(codec_grid(n)), dim3(256), 0, st, 1,
+                                reinterpret_cast<const uint4*>(x), n, dst_rows,
+                                reinterpret_cast<uint32_t*>(codes), scales)));
+  return e;
 }
 
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t n, uint16_t* y,
                               cudaStream_t st) {
   if (n == 0) return cudaSuccess;
+  cudaError_t e;
   CSA2_PROFILED(st, "fp4_dequantize",
-                (dequantize_kernel<<<codec_grid(n), 256, 0, st>>>(reinterpret_cast<const uint2*>(codes), scales,
-                                                                  n, reinterpret_cast<uint4*>(y))));
-  return cudaGetLastError();
+                (e = launch_pdl(dequantize_kernel, dim3(codec_grid(n)), dim3(256), 0, st, 1,
+                                reinterpret_cast<const uint2*>(codes), scales, n, reinterpret_cast<uint4*>(y))));
+  return e;
 }
 
 }  // namespace csa2

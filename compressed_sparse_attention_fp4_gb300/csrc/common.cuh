@@ -129,6 +129,15 @@ __device__ inline uint32_t e4m3x2_to_f16x2(uint16_t pair) {
 }
 
 // Order-preserving map of a float onto uint32 (-0 is first made +0).
+// Programmatic dependent launch.  The library launches its kernels with
+// programmatic stream serialisation: a kernel may begin while the kernel
+// before it on the stream still runs.  pdl_wait() returns once that kernel
+// has completed and its writes are visible; nothing before it may read or
+// write memory that other work on the stream touches.  pdl_launch_dependents()
+// lets the next kernel begin its own set-up early.
+__device__ inline void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ inline void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ inline uint32_t f32_key(float x) {
   uint32_t u = __float_as_uint(x + 0.0f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);

@@ -38,6 +38,8 @@ namespace csa2 {
 // ===========================================================================
 template <bool kFp8, int kDi>
 __global__ void __launch_bounds__(256) scan_cc_kernel(IdxArgs a, bool reindex) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float q_s[kDi][kMaxIdxHeads];     // [c][h]
   __shared__ float w_s[kMaxIdxHeads];
   __shared__ float wq_s;
@@ -191,8 +193,8 @@ cudaError_t launch_full(IdxArgs a, cudaStream_t st) {
     e = launch_scan_tc(a, false, st);
   } else {
     dim3 grid(unsigned((a.d.max_ctx + 255) / 256), unsigned(a.batch));
-    CSA2_PROFILED(st, "indexer_scan_cuda_core", (scan_cc_kernel<false, 64><<<grid, 256, 0, st>>>(a, false)));
-    e = cudaGetLastError();
+    CSA2_PROFILED(st, "indexer_scan_cuda_core",
+                  (e = launch_pdl(scan_cc_kernel<false, 64>, grid, dim3(256), 0, st, 1, a, false)));
   }
   if (e != cudaSuccess) return e;
   return launch_select(a, false, st);
@@ -207,8 +209,8 @@ cudaError_t launch_reindex(IdxArgs a, cudaStream_t st) {
   if (fp8) {
     e = launch_scan_tc(a, true, st);
   } else {
-    CSA2_PROFILED(st, "reindex_score_cuda_core", (scan_cc_kernel<false, 64><<<grid, 256, 0, st>>>(a, true)));
-    e = cudaGetLastError();
+    CSA2_PROFILED(st, "reindex_score_cuda_core",
+                  (e = launch_pdl(scan_cc_kernel<false, 64>, grid, dim3(256), 0, st, 1, a, true)));
   }
   if (e != cudaSuccess) return e;
   return launch_select(a, true, st);

@@ -407,6 +407,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u));
   __shared__ int64_t total_tiles_s;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
   // ---- tiles of all sequences, this CTA's contiguous share ----------------------
   if (wid == 0) {
     int64_t tsum = 0;
@@ -613,8 +615,9 @@ cudaError_t launch_scan_tc(const IdxArgs& a, bool reindex, cudaStream_t st) {
   int64_t grid = min64(int64_t(sms), tiles_ub);
   if (grid < 1) grid = 1;
   CSA2_PROFILED(st, reindex ? "reindex_score_tc" : "indexer_scan_tc",
-                (scan_tc_kernel<<<unsigned(grid), kScanThreads, smem, st>>>(a, map, reindex)));
-  return cudaGetLastError();
+                (e = launch_pdl(scan_tc_kernel, dim3(unsigned(grid)), dim3(kScanThreads), smem, st, 1, a, map,
+                                reindex)));
+  return e;
 }
 
 }  // namespace csa2

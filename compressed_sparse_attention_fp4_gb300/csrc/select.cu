@@ -778,6 +778,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
   const int b = blockIdx.y;
+  pdl_wait();
+  pdl_launch_dependents();
   SelCtx c;
   c.b = b;
   c.cs = cs;
@@ -843,19 +845,9 @@ cudaError_t launch_select(IdxArgs a, bool reindex, cudaStream_t st) {
   size_t smem = sizeof(SelSmem);
   cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(cs), unsigned(a.batch), 1);
-  cfg.blockDim = dim3(kSelThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(cs);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  CSA2_PROFILED(st, reindex ? "select_reindex" : "select_full", (e = cudaLaunchKernelEx(&cfg, select_kernel, a, cs, reindex)));
+  CSA2_PROFILED(st, reindex ? "select_reindex" : "select_full",
+                (e = launch_pdl(select_kernel, dim3(unsigned(cs), unsigned(a.batch), 1), dim3(kSelThreads), smem, st,
+                                unsigned(cs), a, cs, reindex)));
   return e;
 }
 
