@@ -27,11 +27,11 @@
 //   5. merges the chunks of the sequence: o = sum_s 2^(m_s - M) o_s / L,
 //      L = sum_s 2^(m_s - M) l_s, lse = M ln 2 + ln L (m in base-2 logits).
 //      With at most 8 chunks the sequence's CTAs form a thread-block
-//      cluster: each publishes its per-head (m_s, l_s) in shared memory;
-//      after a cluster barrier each reads them all, forms M and L, scales
-//      its O_s into shared memory and adds it into the output with bulk
-//      reduce-add copies (cp.reduce.async.bulk .add.f32; the SWA chunk, which
-//      finishes first, zeroes the output rows before the barrier).  The order of the additions is not fixed, so the
+//      cluster: each writes its per-head (m_s, l_s) into every chunk's shared
+//      memory; after a cluster barrier each forms M and L from its own copy,
+//      scales its O_s into shared memory and adds it into the output with
+//      coalesced vector reduce-adds (red.global.add.v4.f32; the SWA chunk,
+//      which finishes first, zeroes the output rows before the barrier).  The order of the additions is not fixed, so the
 //      last bits of the output may differ between runs.  With more chunks,
 //      each CTA writes its unnormalised O_s and (m_s, l_s) and a combine
 //      kernel merges them (natural-log m there).
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __shared__ __align__(16) float red_m[4][4][16];
   __shared__ __align__(16) float red_l[4][4][16];
   __shared__ float fac_s[kQRows];                    // fused: 2^(m_s - M) / L per head
-  __shared__ float ml_s[2][kQRows];                  // fused: this chunk's (m, l), base-2 m
+  __shared__ float ml_all[kMaxClusterSplits][2][kQRows];   // fused: every chunk's (m, l), base-2 m
 
   const int b = blockIdx.y, split = blockIdx.x;
   const int H = a.d.heads, K = a.d.topk, W = a.d.swa;
@@ -138,6 +138,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc::mbar_init(&bar_o, 1);
     tc::fence_mbar_init();
   }
+  // every chunk of the cluster must have started before another writes into
+  // its shared memory: arrive now, wait before the first such write
+  if constexpr (kFused) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   pdl_wait();
   pdl_launch_dependents();
   const bool paged = a.page_table != nullptr;
@@ -176,7 +179,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // into them only after the cluster barrier below
       float4* ob = reinterpret_cast<float4*>(a.out + int64_t(b) * H * kLatent);
       for (int i = tid; i < H * (kLatent / 4); i += kAttnThreads) ob[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      asm volatile("fence.proxy.async.global;" ::: "memory");
     }
   }
 
@@ -340,6 +342,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc::fence_proxy_async_smem();
   tc::tc_fence_before_sync();
   __syncthreads();
+  if constexpr (kFused) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   float* ml_base = reinterpret_cast<float*>(a.ws + a.L.attn_ml);
   const int64_t prow = (int64_t(b) * a.L.splits + split) * H;
   if (quarter == 0 && lane < 16) {
@@ -348,8 +351,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float M = fmaxf(fmaxf(red_m[hg][0][lane], red_m[hg][1][lane]), fmaxf(red_m[hg][2][lane], red_m[hg][3][lane]));
       float L = red_l[hg][0][lane] + red_l[hg][1][lane] + red_l[hg][2][lane] + red_l[hg][3][lane];
       if constexpr (kFused) {
-        ml_s[0][h] = M;
-        ml_s[1][h] = L;
+        // pushed into every chunk's shared memory (read after the cluster barrier)
+        cg::cluster_group cl = cg::this_cluster();
+        for (int r = 0; r < int(cl.num_blocks()); ++r) {
+          cl.map_shared_rank(&ml_all[0][0][0], r)[(split * 2 + 0) * kQRows + h] = M;
+          cl.map_shared_rank(&ml_all[0][0][0], r)[(split * 2 + 1) * kQRows + h] = L;
+        }
       } else {
         ml_base[(prow + h) * 2] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
         ml_base[(prow + h) * 2 + 1] = L;
@@ -383,16 +390,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if constexpr (kFused) {
     // every chunk's (m, l) is in its shared memory; the zeroed output rows
     // are visible too
-    cg::cluster_group cl = cg::this_cluster();
-    cl.sync();
+    cg::this_cluster().sync();
     if (tid < kQRows) {
       const int S = a.L.splits;
       float mr[kMaxClusterSplits], lr[kMaxClusterSplits];
       float M = -INFINITY;
 #pragma unroll
       for (int r = 0; r < kMaxClusterSplits; ++r) {
-        mr[r] = (r < S && tid < H) ? cl.map_shared_rank(&ml_s[0][0], r)[tid] : -INFINITY;
-        lr[r] = (r < S && tid < H) ? cl.map_shared_rank(&ml_s[1][0], r)[tid] : 0.0f;
+        mr[r] = (r < S && tid < H) ? ml_all[r][0][tid] : -INFINITY;
+        lr[r] = (r < S && tid < H) ? ml_all[r][1][tid] : 0.0f;
         M = fmaxf(M, mr[r]);
       }
       float L = 0.0f;
@@ -404,9 +410,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (split == 0 && tid < H)
         a.lse[int64_t(b) * H + tid] = L > 0.0f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
     }
-    // done with the other chunks' shared memory; they may leave once every
-    // chunk has arrived (the matching wait is at the end)
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     __syncthreads();
   }
   // ---- O^T through shared memory as [head][dim] (the KV tile is no longer
@@ -425,24 +428,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc::tc_fence_before_sync();
   __syncthreads();
   if (wid == 0) tc::tmem_dealloc(tmem, kTmemCols);
-  if (tid < H) {
-    const uint32_t src = tc::smem_u32(obuf + tid * kLatent);
-    if constexpr (kFused) {
-      float* dst = a.out + (int64_t(b) * H + tid) * kLatent;
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;"
-                   ::"l"(dst), "r"(src), "r"(uint32_t(kLatent * 4))
-                   : "memory");
-    } else {
-      float* dst = reinterpret_cast<float*>(a.ws + a.L.attn_o) + (prow + tid) * kLatent;
-      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                   ::"l"(dst), "r"(src), "r"(uint32_t(kLatent * 4))
+  if constexpr (kFused) {
+    // coalesced vector reduce-adds into the output rows, 16 bytes per thread
+    const float4* ob = reinterpret_cast<const float4*>(obuf);
+    float* out_b = a.out + int64_t(b) * H * kLatent;
+    for (int i = tid; i < H * (kLatent / 4); i += kAttnThreads) {
+      const float4 v = ob[i];
+      asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                   ::"l"(out_b + int64_t(i) * 4), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
                    : "memory");
     }
+  } else if (tid < H) {
+    const uint32_t src = tc::smem_u32(obuf + tid * kLatent);
+    float* dst = reinterpret_cast<float*>(a.ws + a.L.attn_o) + (prow + tid) * kLatent;
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(dst), "r"(src), "r"(uint32_t(kLatent * 4))
+                 : "memory");
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // shared source read out
   }
-  if constexpr (kFused) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
