@@ -449,6 +449,397 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Channel-split pairs.  Every 128-entry chunk is served by two CTAs: half 0
+// takes latent channels 0..255, half 1 latent channels 256..511 and the rope
+// (64).  Each gathers, dequantizes and multiplies only its channels
+// (S^T partial, M=128, N=64, K=256 or 320), the pair exchanges the partial
+// S^T through shared memory (one mbarrier arrival across the pair), both
+// form the same softmax, and each computes O^T for its own 256 latent
+// dimensions (the value channels it holds).  The 2 x chunks CTAs of a
+// sequence form one cluster (up to 16) that merges the chunks as above.
+// ---------------------------------------------------------------------------
+constexpr int kPairRegions = 5;                       // regions of 64 channels, at most
+constexpr int kPairKvBytes = kPairRegions * kRegion;  // 80 KB
+constexpr int kPairQBytes = kPairRegions * kQRegion;  // 40 KB
+constexpr int kSxBytes = kEntries * kQRows * 4;       // 32 KB: the partner's S^T partial
+constexpr uint32_t kPairTmemCols = 256;               // S^T: 64 cols, O^T: 2 x 64 cols
+
+// Arrives on the mbarrier at the same shared-memory offset in CTA `rank` of
+// the cluster, releasing this thread's (and, cumulatively, its CTA's) prior
+// writes at cluster scope.
+__device__ inline void remote_arrive(uint64_t* bar, uint32_t rank) {
+  uint32_t raddr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(tc::smem_u32(bar)), "r"(rank));
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr) : "memory");
+}
+
+__device__ inline bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = tc::globaltimer_ns();
+  while (true) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(tc::smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (tc::globaltimer_ns() - t0 > 200ull * 1000 * 1000) return false;
+  }
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_pair_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
+                     const __grid_constant__ CUtensorMap swamap, int swa_tma_split) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* kv_s = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);   // nreg x 16 KB
+  uint8_t* q_s = kv_s + kPairKvBytes;               // nreg x 8 KB; later P^T hi / lo
+  float* sx = reinterpret_cast<float*>(q_s + kPairQBytes);   // [entry][head], written by the partner
+  __shared__ uint64_t bar_ld, bar_s, bar_o, bar_x;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int64_t row_s[kEntries];               // >= 0 main row, -2 - r SWA row r, -1 empty
+  __shared__ __align__(16) float red_m[4][4][16];
+  __shared__ __align__(16) float red_l[4][4][16];
+  __shared__ float fac_s[kQRows];                   // 2^(m_chunk - M) / L per head
+  __shared__ float ml_all[kMaxClusterSplits][2][kQRows];   // every chunk's (m, l), base-2 m
+
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = int(cl.block_rank()), csize = int(cl.num_blocks());
+  const int chunk = rank >> 1, half = rank & 1;
+  const int b = blockIdx.y;
+  const int H = a.d.heads, K = a.d.topk, W = a.d.swa;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int nreg = half ? 5 : 4, reg0 = 4 * half;   // this CTA's regions of 64 channels (of 9)
+  // set-up that touches no global memory, then wait for the previous kernel
+  if (wid == 0) tc::tmem_alloc(&tmem_slot, kPairTmemCols);
+  if (tid == 0) {
+    tc::mbar_init(&bar_ld, 1);
+    tc::mbar_init(&bar_s, 1);
+    tc::mbar_init(&bar_o, 1);
+    tc::mbar_init(&bar_x, 1);                        // the partner's arrival
+    tc::fence_mbar_init();
+  }
+  // every CTA of the cluster must have started before another writes into
+  // its shared memory: arrive now, wait before the first such write
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  pdl_wait();
+  pdl_launch_dependents();
+  const bool paged = a.page_table != nullptr;
+  const bool swa_tma = chunk == swa_tma_split;      // this chunk's rows are the SWA window
+  const int64_t n_ctx = checked_ctx(a.ctx_len, a.d, b, paged, a.ws);
+  int swl = a.swa_len[b];
+  if (swl < 0 || swl > W) {
+    if (tid == 0 && half == 0) raise_err(a.ws, CSA2_DEV_SWA_LEN);
+    swl = swl < 0 ? 0 : W;
+  }
+  if (tid < kEntries) {
+    int slot = chunk * kEntries + tid;
+    int64_t r = -1;
+    if (slot < K) {
+      int32_t t = a.topk[int64_t(b) * K + slot];
+      if (t >= 0) {
+        if (t >= n_ctx) raise_err(a.ws, CSA2_DEV_TOPK_IDX);
+        else r = kv_row(a.page_table, a.d, b, t, a.ws);
+        if (r < 0) r = -1;
+      } else if (t < -1) {
+        raise_err(a.ws, CSA2_DEV_TOPK_IDX);
+      }
+    } else if (slot < K + W && slot - K < swl) {
+      r = -2 - (slot - K);
+    }
+    row_s[tid] = r;
+  }
+  tc::tc_fence_before_sync();
+  __syncthreads();
+  tc::tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+  // the chunk that finishes first (the TMA-loaded SWA window, else chunk 0)
+  // zeroes this half's output dimensions; the adds come after the cluster
+  // barrier of the merge
+  if (chunk == (swa_tma_split >= 0 ? swa_tma_split : 0)) {
+    for (int i = tid; i < H * 64; i += kAttnThreads) {
+      const int h = i >> 6, q = i & 63;
+      reinterpret_cast<float4*>(a.out + (int64_t(b) * H + h) * kLatent + half * 256)[q] =
+          make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  // ---- TMA: this half's query channels and, for the window's chunk, SWA rows ----
+  if (tid == 0) {
+    tc::mbar_expect_tx(&bar_ld, uint32_t(nreg) * (uint32_t(kQRegion) + (swa_tma ? uint32_t(kRegion) : 0u)));
+    for (int kb = 0; kb < nreg; ++kb)
+      tc::tma_load_2d(&qmap, q_s + kb * kQRegion, 64 * (reg0 + kb), b * H, &bar_ld);
+    if (swa_tma)
+      for (int kb = 0; kb < nreg; ++kb)
+        tc::tma_load_2d(&swamap, kv_s + kb * kRegion, 64 * (reg0 + kb), b * W, &bar_ld);
+  }
+  // ---- FP4 entries: gather (all loads first), dequantize to bf16 -------------------
+  if (!swa_tma) {
+    // latent: task = (entry, pair of 16-channel groups of this half); 2 per thread
+    uint4 cd[2];
+    uint32_t sc[2];
+    int64_t rr[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int task = tid + k * kAttnThreads, e = task >> 3, gp = 8 * half + (task & 7);
+      rr[k] = row_s[e];
+      cd[k] = make_uint4(0, 0, 0, 0);
+      sc[k] = 0;
+      if (rr[k] >= 0) {
+        cd[k] = __ldg(reinterpret_cast<const uint4*>(a.codes + rr[k] * kCodesPerRow) + gp);
+        sc[k] = __ldg(reinterpret_cast<const uint16_t*>(a.scales + rr[k] * kScalesPerRow) + gp);
+      }
+    }
+    // rope (half 1): task = (entry, 16-byte chunk); 2 per thread
+    uint4 rp[2];
+    int64_t rr2[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int task = tid + k * kAttnThreads, e = task >> 3, rc = task & 7;
+      rr2[k] = half ? row_s[e] : -1;
+      rp[k] = make_uint4(0, 0, 0, 0);
+      if (rr2[k] >= 0) rp[k] = __ldg(reinterpret_cast<const uint4*>(a.rope + rr2[k] * kRope) + rc);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int task = tid + k * kAttnThreads, e = task >> 3, gp = 8 * half + (task & 7);
+      if (rr[k] <= -2) continue;                     // SWA row: copied below
+      uint32_t cw[4] = {cd[k].x, cd[k].y, cd[k].z, cd[k].w};
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {                  // two 16-channel groups
+        float s = e4m3_to_f32((sc[k] >> (8 * g)) & 0xFF);
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint32_t h2 = e2m1x2_to_f16x2_a((cw[2 * g + (i >> 2)] >> (8 * (i & 3))) & 0xFF);
+          float lo = __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF))) * s;
+          float hi = __half2float(__ushort_as_half(uint16_t(h2 >> 16))) * s;
+          w[i] = pack_bf16x2(lo, hi);
+        }
+        const int part = 2 * gp + g;                 // 16-channel group index 0..31
+        const uint32_t region = (part >> 2) - reg0, ch0 = (part & 3) * 2;
+        st_shared_v4(kv_s, region * kRegion + tc::sw128_offset(e, ch0), make_uint4(w[0], w[1], w[2], w[3]));
+        st_shared_v4(kv_s, region * kRegion + tc::sw128_offset(e, ch0 + 1), make_uint4(w[4], w[5], w[6], w[7]));
+      }
+    }
+    if (half) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int task = tid + k * kAttnThreads, e = task >> 3, rc = task & 7;
+        if (rr2[k] <= -2) continue;
+        st_shared_v4(kv_s, 4 * kRegion + tc::sw128_offset(e, rc), rp[k]);
+      }
+    }
+    // SWA rows of a chunk the window does not start on a 128-row boundary for
+    const int nch = nreg * 8, c0 = reg0 * 8;          // this half's 16-byte chunks of a row
+#pragma unroll 4
+    for (int task = tid; task < kEntries * nch; task += kAttnThreads) {
+      const int e = task / nch, c = task % nch;
+      const int64_t r = row_s[e];
+      if (r > -2) continue;
+      uint4 v = __ldg(reinterpret_cast<const uint4*>(a.swa + (int64_t(b) * W + (-2 - r)) * kDqk) + c0 + c);
+      st_shared_v4(kv_s, (c >> 3) * kRegion + tc::sw128_offset(e, c & 7), v);
+    }
+  }
+  bool ok = tc::mbar_wait_bounded(&bar_ld, 0);
+  if (swa_tma) {
+    // window rows past swa_len (or past W) are not entries: zero them so that
+    // P = 0 never meets a non-finite value
+    const int nch = nreg * 8;
+    for (int task = tid; task < kEntries * nch; task += kAttnThreads) {
+      const int e = task / nch, c = task % nch;
+      if (row_s[e] == -1) st_shared_v4(kv_s, (c >> 3) * kRegion + tc::sw128_offset(e, c & 7), make_uint4(0, 0, 0, 0));
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before_sync();
+  __syncthreads();
+
+  // ---- S^T partial = KV_half . Q_half^T ------------------------------------------
+  const uint32_t kv_addr = tc::smem_u32(kv_s), q_addr = tc::smem_u32(q_s);
+  if (tid == 0) {
+    tc::tc_fence_after_sync();
+    constexpr uint32_t idS = tc::idesc_bf16(kEntries, kQRows, 0, 0);
+    // descriptors are formed once; an offset of x bytes adds x/16 to the
+    // start-address field (the operands lie below 256 KB, so it never carries)
+    const uint64_t ad0 = tc::smem_desc(kv_addr, 16, 1024, 2), bd0 = tc::smem_desc(q_addr, 16, 1024, 2);
+#pragma unroll
+    for (int ks = 0; ks < 16; ++ks) {
+      const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+      tc::mma_bf16(tmem, ad0 + ((kb * kRegion + off) >> 4), bd0 + ((kb * kQRegion + off) >> 4), idS, ks > 0);
+    }
+    if (half) {
+#pragma unroll
+      for (int ks = 16; ks < 20; ++ks) {
+        const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
+        tc::mma_bf16(tmem, ad0 + ((kb * kRegion + off) >> 4), bd0 + ((kb * kQRegion + off) >> 4), idS, true);
+      }
+    }
+    tc::mma_commit(&bar_s);
+  }
+  ok = tc::mbar_wait_bounded(&bar_s, 0) && ok;
+  tc::tc_fence_after_sync();
+
+  // ---- exchange the S^T partials within the pair ----------------------------------
+  const int quarter = wid & 3, hg = wid >> 2;       // lanes 32*quarter.., heads 16*hg..
+  const int e = quarter * 32 + lane;
+  const bool valid = row_s[e] != -1;
+  float x[16];
+  tc::tmem_ld16(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(hg * 16), x);
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA has started
+  {
+    float4* dst = reinterpret_cast<float4*>(cl.map_shared_rank(sx, rank ^ 1) + e * kQRows + hg * 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+  }
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+  __syncthreads();
+  if (tid == 0) remote_arrive(&bar_x, uint32_t(rank ^ 1));
+  ok = mbar_wait_cluster(&bar_x, 0) && ok;
+  {
+    const float4* src = reinterpret_cast<const float4*>(sx + e * kQRows + hg * 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 v = src[i];
+      // own + partner: the same sum in both CTAs (fp32 addition commutes)
+      x[4 * i] += v.x; x[4 * i + 1] += v.y; x[4 * i + 2] += v.z; x[4 * i + 3] += v.w;
+    }
+  }
+
+  // ---- softmax over the 128 entries (TMEM lanes), identical in both halves ---------
+  const float c2 = a.scale * 1.4426950408889634f;   // logits in base 2
+#pragma unroll
+  for (int j = 0; j < 16; ++j) x[j] = valid ? x[j] * c2 : -INFINITY;
+  {
+    const float m = butterfly16<true>(x, lane);
+    if ((lane & 1) == 0) red_m[hg][quarter][butterfly_index(lane)] = m;
+  }
+  __syncthreads();
+  float p[16];
+#pragma unroll
+  for (int j4 = 0; j4 < 4; ++j4) {
+    float4 m4[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) m4[q] = reinterpret_cast<const float4*>(&red_m[hg][q][0])[j4];
+    const float Mj[4] = {fmaxf(fmaxf(m4[0].x, m4[1].x), fmaxf(m4[2].x, m4[3].x)),
+                         fmaxf(fmaxf(m4[0].y, m4[1].y), fmaxf(m4[2].y, m4[3].y)),
+                         fmaxf(fmaxf(m4[0].z, m4[1].z), fmaxf(m4[2].z, m4[3].z)),
+                         fmaxf(fmaxf(m4[0].w, m4[1].w), fmaxf(m4[2].w, m4[3].w))};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = 4 * j4 + i;
+      p[j] = (Mj[i] == -INFINITY || x[j] == -INFINITY) ? 0.0f : exp2f(x[j] - Mj[i]);
+    }
+  }
+  {
+    const float l = butterfly16<false>(p, lane);
+    if ((lane & 1) == 0) red_l[hg][quarter][butterfly_index(lane)] = l;
+  }
+  // P^T rows (entry e) as bf16 hi and lo parts; the query buffer is free (the
+  // S^T MMAs completed before this)
+  uint8_t* p_hi = q_s;
+  uint8_t* p_lo = q_s + kRegion;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    uint32_t wh[4], wl[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float v0 = p[8 * t + 2 * i], v1 = p[8 * t + 2 * i + 1];
+      uint32_t hb = pack_bf16x2(v0, v1);
+      float h0 = __uint_as_float(hb << 16), h1 = __uint_as_float(hb & 0xFFFF0000u);
+      wh[i] = hb;
+      wl[i] = pack_bf16x2(v0 - h0, v1 - h1);
+    }
+    uint32_t off = tc::sw128_offset(e, hg * 2 + t);
+    st_shared_v4(p_hi, off, make_uint4(wh[0], wh[1], wh[2], wh[3]));
+    st_shared_v4(p_lo, off, make_uint4(wl[0], wl[1], wl[2], wl[3]));
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before_sync();
+  __syncthreads();
+  // this chunk's (m, l) per head, written by half 0 into every CTA of the cluster
+  if (half == 0 && quarter == 0 && lane < 16) {
+    const int h = hg * 16 + lane;
+    const float M = fmaxf(fmaxf(red_m[hg][0][lane], red_m[hg][1][lane]), fmaxf(red_m[hg][2][lane], red_m[hg][3][lane]));
+    const float L = red_l[hg][0][lane] + red_l[hg][1][lane] + red_l[hg][2][lane] + red_l[hg][3][lane];
+    for (int r = 0; r < csize; ++r) {
+      cl.map_shared_rank(&ml_all[0][0][0], r)[(chunk * 2 + 0) * kQRows + h] = M;
+      cl.map_shared_rank(&ml_all[0][0][0], r)[(chunk * 2 + 1) * kQRows + h] = L;
+    }
+  }
+
+  // ---- O^T = V_half^T . P^T  (this half's 2 M-tiles of 128 dims; hi and lo) --------
+  if (tid == 0) {
+    tc::tc_fence_after_sync();
+    constexpr uint32_t idO = tc::idesc_bf16(kEntries, kQRows, 1, 1);
+    const uint64_t av0 = tc::smem_desc(kv_addr, kRegion, 1024, 2);
+    const uint64_t bp0[2] = {tc::smem_desc(tc::smem_u32(p_hi), kRegion, 1024, 2),
+                             tc::smem_desc(tc::smem_u32(p_lo), kRegion, 1024, 2)};
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_bf16(tmem + 64 + 64 * mt, av0 + (((2 * mt) * kRegion + ks * 2048) >> 4),
+                       bp0[part] + ((ks * 2048) >> 4), idO, part > 0 || ks > 0);
+      }
+    }
+    tc::mma_commit(&bar_o);
+  }
+  ok = tc::mbar_wait_bounded(&bar_o, 0) && ok;
+  tc::tc_fence_after_sync();
+  if (!ok && tid == 0) raise_err(a.ws, CSA2_DEV_TIMEOUT);
+
+  // ---- merge over the cluster -------------------------------------------------------
+  cl.sync();                                        // every chunk's (m, l); the zeroed output
+  if (tid < kQRows) {
+    const int S = csize >> 1;
+    float mr[kMaxClusterSplits], lr[kMaxClusterSplits];
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kMaxClusterSplits; ++r) {
+      mr[r] = (r < S && tid < H) ? ml_all[r][0][tid] : -INFINITY;
+      lr[r] = (r < S && tid < H) ? ml_all[r][1][tid] : 0.0f;
+      M = fmaxf(M, mr[r]);
+    }
+    float L = 0.0f;
+#pragma unroll
+    for (int r = 0; r < kMaxClusterSplits; ++r)
+      if (mr[r] != -INFINITY) L += lr[r] * exp2f(mr[r] - M);
+    float ms = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kMaxClusterSplits; ++r) ms = r == chunk ? mr[r] : ms;
+    fac_s[tid] = (ms == -INFINITY || !(L > 0.0f)) ? 0.0f : exp2f(ms - M) / L;
+    if (rank == 0 && tid < H)
+      a.lse[int64_t(b) * H + tid] = L > 0.0f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
+  }
+  __syncthreads();
+  // scaled O^T into shared memory as [head][256 dims] (the KV tile is no longer read)
+  float* obuf = reinterpret_cast<float*>(kv_s);
+#pragma unroll 1
+  for (int mt = 0; mt < 2; ++mt) {
+    float o[16];
+    tc::tmem_ld16(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(64 + 64 * mt + hg * 16), o);
+    const int dim = mt * 128 + quarter * 32 + lane;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) obuf[(hg * 16 + j) * 256 + dim] = o[j] * fac_s[hg * 16 + j];
+  }
+  tc::tc_fence_before_sync();
+  __syncthreads();
+  if (wid == 0) tc::tmem_dealloc(tmem, kPairTmemCols);
+  // coalesced vector reduce-adds into this half's output dimensions
+  const float4* ob = reinterpret_cast<const float4*>(obuf);
+  for (int i = tid; i < H * 64; i += kAttnThreads) {
+    const float4 v = ob[i];
+    float* dst = a.out + (int64_t(b) * H + (i >> 6)) * kLatent + half * 256 + (i & 63) * 4;
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                 ::"l"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+  }
+}
+
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
   const int h = blockIdx.x, b = blockIdx.y, H = a.d.heads, S = a.L.splits;
   pdl_wait();
@@ -517,13 +908,16 @@ cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
     return cudaErrorInvalidValue;
   size_t smem = attn_smem_bytes(a.d.heads);
   if (a.L.splits <= kMaxClusterSplits) {
-    // one cluster per sequence; the merge happens inside the cluster
-    cudaError_t e = cudaFuncSetAttribute(attn_partial_tc_kernel<true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    // one cluster of 2 x chunks CTAs per sequence; the merge happens inside it
+    const size_t psmem = size_t(kPairKvBytes) + size_t(kPairQBytes) + size_t(kSxBytes) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(attn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(psmem));
     if (e != cudaSuccess) return e;
-    CSA2_PROFILED(st, "attn_fused_tc",
-                  (e = launch_pdl(attn_partial_tc_kernel<true>, dim3(unsigned(a.L.splits), unsigned(a.batch), 1),
-                                  dim3(kAttnThreads), smem, st, unsigned(a.L.splits), a, qmap, swamap, swa_split)));
+    e = cudaFuncSetAttribute(attn_pair_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    CSA2_PROFILED(st, "attn_pair_tc",
+                  (e = launch_pdl(attn_pair_kernel, dim3(unsigned(2 * a.L.splits), unsigned(a.batch), 1),
+                                  dim3(kAttnThreads), psmem, st, unsigned(2 * a.L.splits), a, qmap, swamap,
+                                  swa_split)));
     return e;
   }
   cudaError_t e = cudaFuncSetAttribute(attn_partial_tc_kernel<false>,
