@@ -13,28 +13,34 @@
 // "DeepSeek-V4.1-Flash 2026: ...", section 4).
 //
 // Split-KV: the entry list (K Top-K slots, then W SWA slots) is cut into
-// chunks of 128 slots; one CTA per (sequence, chunk):
-//   1. gathers its 128 entries, dequantizes FP4 to bf16 into shared memory
-//      (128-byte swizzled, one 16 KB region per 64 channels) and loads the
-//      query [64 heads x 576] the same way;
-//   2. S^T[128 entries x 64 heads] = KV . Q^T on tcgen05 (M=128, N=64,
-//      K=576, bf16 in, fp32 in tensor memory);
-//   3. softmax over the entries (= TMEM lanes): per-head max and sum across
-//      the 4 lane quarters; P^T is written back as bf16 hi + lo parts, so
-//      its rounding stays near 2^-17;
-//   4. O^T[512 dims x 64 heads] = V^T . P^T on tcgen05 (the same KV tile read
-//      MN-major), 4 M-tiles of 128 dims, hi and lo accumulated together;
-//   5. merges the chunks of the sequence: o = sum_s 2^(m_s - M) o_s / L,
+// chunks of 128 slots.  For each chunk:
+//   1. its 128 entries are gathered and dequantized from FP4 to bf16 into
+//      shared memory (128-byte swizzled, one 16 KB region per 64 channels);
+//      the query [64 heads x 576] and a window that starts a chunk come by TMA;
+//   2. S^T[128 entries x 64 heads] = KV . Q^T on tcgen05 (M=128, N=64, bf16 in,
+//      fp32 in tensor memory);
+//   3. softmax over the entries (= TMEM lanes): per-head max and sum by
+//      butterfly reduce-scatter and across the 4 lane quarters; P^T is written
+//      back as bf16 hi + lo parts, so its rounding stays near 2^-17;
+//   4. O^T = V^T . P^T on tcgen05 (the same KV tile read MN-major), M-tiles of
+//      128 dims, hi and lo accumulated together;
+//   5. the chunks of the sequence are merged: o = sum_s 2^(m_s - M) o_s / L,
 //      L = sum_s 2^(m_s - M) l_s, lse = M ln 2 + ln L (m in base-2 logits).
-//      With at most 8 chunks the sequence's CTAs form a thread-block
-//      cluster: each writes its per-head (m_s, l_s) into every chunk's shared
-//      memory; after a cluster barrier each forms M and L from its own copy,
-//      scales its O_s into shared memory and adds it into the output with
-//      coalesced vector reduce-adds (red.global.add.v4.f32; the SWA chunk,
-//      which finishes first, zeroes the output rows before the barrier).  The order of the additions is not fixed, so the
-//      last bits of the output may differ between runs.  With more chunks,
-//      each CTA writes its unnormalised O_s and (m_s, l_s) and a combine
-//      kernel merges them (natural-log m there).
+//
+// attn_pair_kernel (at most 8 chunks, the usual case): two CTAs per chunk
+// split the 576 channels (latent 0..255 | latent 256..511 + rope), exchange
+// their S^T partials through shared memory and each computes O^T for its 256
+// value dimensions.  The 2 x chunks CTAs of a sequence form one thread-block
+// cluster: every chunk writes its per-head (m_s, l_s) into every CTA's shared
+// memory; after a cluster barrier each forms M and L, scales its O^T part and
+// adds it into the output with coalesced vector reduce-adds
+// (red.global.add.v4.f32; the SWA chunk, which finishes first, zeroes the
+// output before the barrier).  The order of the additions is not fixed, so
+// the last bits of the output may differ between runs.
+//
+// attn_partial_tc_kernel + attn_combine_kernel (more chunks): one CTA per
+// chunk writes its unnormalised O_s and (m_s, l_s) (natural-log m) to the
+// workspace and the combine kernel merges them.
 #include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -111,7 +117,6 @@ __device__ inline void st_shared_v4(uint8_t* base, uint32_t off, uint4 v) {
 
 constexpr int kMaxClusterSplits = 8;                // portable cluster size
 
-template <bool kFused>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_partial_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
                            const __grid_constant__ CUtensorMap swamap, int swa_tma_split) {
@@ -124,8 +129,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __shared__ int64_t row_s[kEntries];               // >= 0 main row, -2 - r SWA row r, -1 empty
   __shared__ __align__(16) float red_m[4][4][16];
   __shared__ __align__(16) float red_l[4][4][16];
-  __shared__ float fac_s[kQRows];                    // fused: 2^(m_s - M) / L per head
-  __shared__ float ml_all[kMaxClusterSplits][2][kQRows];   // fused: every chunk's (m, l), base-2 m
 
   const int b = blockIdx.y, split = blockIdx.x;
   const int H = a.d.heads, K = a.d.topk, W = a.d.swa;
@@ -138,9 +141,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc::mbar_init(&bar_o, 1);
     tc::fence_mbar_init();
   }
-  // every chunk of the cluster must have started before another writes into
-  // its shared memory: arrive now, wait before the first such write
-  if constexpr (kFused) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   pdl_wait();
   pdl_launch_dependents();
   const bool paged = a.page_table != nullptr;
@@ -172,15 +172,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc::tc_fence_after_sync();
   const uint32_t tmem = tmem_slot;
-  if constexpr (kFused) {
-    // the chunk that finishes first (the TMA-loaded SWA window, else chunk 0)
-    if (split == (swa_tma_split >= 0 ? swa_tma_split : 0)) {
-      // the output rows of this sequence start at zero; the other chunks add
-      // into them only after the cluster barrier below
-      float4* ob = reinterpret_cast<float4*>(a.out + int64_t(b) * H * kLatent);
-      for (int i = tid; i < H * (kLatent / 4); i += kAttnThreads) ob[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
 
   // ---- TMA: the query (9 boxes of 64 channels x 64 heads) and, for the
   //      window's CTA, the SWA rows (9 boxes of 64 channels x 128 rows) ----------
@@ -342,7 +333,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc::fence_proxy_async_smem();
   tc::tc_fence_before_sync();
   __syncthreads();
-  if constexpr (kFused) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   float* ml_base = reinterpret_cast<float*>(a.ws + a.L.attn_ml);
   const int64_t prow = (int64_t(b) * a.L.splits + split) * H;
   if (quarter == 0 && lane < 16) {
@@ -350,17 +340,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (h < H) {
       float M = fmaxf(fmaxf(red_m[hg][0][lane], red_m[hg][1][lane]), fmaxf(red_m[hg][2][lane], red_m[hg][3][lane]));
       float L = red_l[hg][0][lane] + red_l[hg][1][lane] + red_l[hg][2][lane] + red_l[hg][3][lane];
-      if constexpr (kFused) {
-        // pushed into every chunk's shared memory (read after the cluster barrier)
-        cg::cluster_group cl = cg::this_cluster();
-        for (int r = 0; r < int(cl.num_blocks()); ++r) {
-          cl.map_shared_rank(&ml_all[0][0][0], r)[(split * 2 + 0) * kQRows + h] = M;
-          cl.map_shared_rank(&ml_all[0][0][0], r)[(split * 2 + 1) * kQRows + h] = L;
-        }
-      } else {
         ml_base[(prow + h) * 2] = M == -INFINITY ? -INFINITY : M * 0.6931471805599453f;
         ml_base[(prow + h) * 2 + 1] = L;
-      }
     }
   }
 
@@ -387,34 +368,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc::tc_fence_after_sync();
   if (!ok && tid == 0) raise_err(a.ws, CSA2_DEV_TIMEOUT);
 
-  if constexpr (kFused) {
-    // every chunk's (m, l) is in its shared memory; the zeroed output rows
-    // are visible too
-    cg::this_cluster().sync();
-    if (tid < kQRows) {
-      const int S = a.L.splits;
-      float mr[kMaxClusterSplits], lr[kMaxClusterSplits];
-      float M = -INFINITY;
-#pragma unroll
-      for (int r = 0; r < kMaxClusterSplits; ++r) {
-        mr[r] = (r < S && tid < H) ? ml_all[r][0][tid] : -INFINITY;
-        lr[r] = (r < S && tid < H) ? ml_all[r][1][tid] : 0.0f;
-        M = fmaxf(M, mr[r]);
-      }
-      float L = 0.0f;
-#pragma unroll
-      for (int r = 0; r < kMaxClusterSplits; ++r)
-        if (mr[r] != -INFINITY) L += lr[r] * exp2f(mr[r] - M);
-      const float ms = mr[split < kMaxClusterSplits ? split : 0];
-      fac_s[tid] = (ms == -INFINITY || !(L > 0.0f)) ? 0.0f : exp2f(ms - M) / L;
-      if (split == 0 && tid < H)
-        a.lse[int64_t(b) * H + tid] = L > 0.0f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
-    }
-    __syncthreads();
-  }
   // ---- O^T through shared memory as [head][dim] (the KV tile is no longer
-  //      read: the PV MMAs completed), then one bulk copy of 2 KB per head:
-  //      a reduce-add into the output (fused) or the partial (combine) -------
+  //      read: the PV MMAs completed), then one bulk copy of 2 KB per head
+  //      into the workspace partials that the combine kernel merges --------
   float* obuf = reinterpret_cast<float*>(kv_s);
 #pragma unroll 1
   for (int mt = 0; mt < 4; ++mt) {
@@ -422,23 +378,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc::tmem_ld16(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(64 + 64 * mt + hg * 16), o);
     const int dim = mt * 128 + quarter * 32 + lane;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) obuf[(hg * 16 + j) * kLatent + dim] = kFused ? o[j] * fac_s[hg * 16 + j] : o[j];
+    for (int j = 0; j < 16; ++j) obuf[(hg * 16 + j) * kLatent + dim] = o[j];
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before_sync();
   __syncthreads();
   if (wid == 0) tc::tmem_dealloc(tmem, kTmemCols);
-  if constexpr (kFused) {
-    // coalesced vector reduce-adds into the output rows, 16 bytes per thread
-    const float4* ob = reinterpret_cast<const float4*>(obuf);
-    float* out_b = a.out + int64_t(b) * H * kLatent;
-    for (int i = tid; i < H * (kLatent / 4); i += kAttnThreads) {
-      const float4 v = ob[i];
-      asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
-                   ::"l"(out_b + int64_t(i) * 4), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
-                   : "memory");
-    }
-  } else if (tid < H) {
+  if (tid < H) {
     const uint32_t src = tc::smem_u32(obuf + tid * kLatent);
     float* dst = reinterpret_cast<float*>(a.ws + a.L.attn_o) + (prow + tid) * kLatent;
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
@@ -920,11 +866,11 @@ cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
                                   swa_split)));
     return e;
   }
-  cudaError_t e = cudaFuncSetAttribute(attn_partial_tc_kernel<false>,
+  cudaError_t e = cudaFuncSetAttribute(attn_partial_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   CSA2_PROFILED(st, "attn_partial_tc",
-                (e = launch_pdl(attn_partial_tc_kernel<false>, dim3(unsigned(a.L.splits), unsigned(a.batch)),
+                (e = launch_pdl(attn_partial_tc_kernel, dim3(unsigned(a.L.splits), unsigned(a.batch)),
                                 dim3(kAttnThreads), smem, st, 1, a, qmap, swamap, swa_split)));
   if (e != cudaSuccess) return e;
   CSA2_PROFILED(st, "attn_combine", (e = launch_pdl(attn_combine_kernel, dim3(unsigned(a.d.heads), unsigned(a.batch)),

@@ -17,7 +17,7 @@ constexpr int kBlock = CSA2_BLOCK;
 constexpr int kCodesPerRow = kLatent / 2;      // 256 bytes of E2M1 nibbles
 constexpr int kScalesPerRow = kLatent / 16;    // 32 E4M3 scales
 constexpr int kMaxPool = 2048;
-constexpr int kMaxTopk = 512;
+constexpr int kMaxTopk = 2048;
 constexpr int kMaxHeads = 64;
 constexpr int kMaxSwa = 128;
 constexpr int kMaxIdxHeads = 16;

@@ -94,7 +94,7 @@ typedef struct {
   int32_t idx_dim;      /* indexer dim Di: 128 (E4M3) or 64 (fp32)            */
   int32_t idx_k_dtype;  /* csa2_idxk_dtype                                    */
   int32_t pool_blocks;  /* candidate-pool blocks P, 1..2048 (pages: 2048)     */
-  int32_t topk;         /* Top-K, 1..512                                      */
+  int32_t topk;         /* Top-K, 1..2048 (the pages use 512)                 */
   int32_t heads;        /* attention heads H, 1..64                           */
   int32_t swa;          /* SWA window rows W, 0..128                          */
   int32_t max_pages;    /* row stride of page_table (paged layout)            */
@@ -222,7 +222,7 @@ csa2_status csa2_sparse_attn_decode(const csa2_dims* d, int32_t batch, int32_t m
  * CSA2_NOALLOC_SCRATCH_BYTES inside the library, held on every GPU that
  * loads the library until the process exits.
  *   Limit: 256 + B*S*H*2048 + B*S*H*8 bytes (each part rounded up to 256)
- *   with S = ceil((topk + swa) / 64) must fit the array -- e.g. batch 8 at
+ *   with S = ceil((topk + swa) / 128) must fit the array -- e.g. batch 8 at
  *   Top-512, SWA-128, 64 heads; larger batches return
  *   CSA2_ERR_WORKSPACE_TOO_SMALL and launch nothing.
  *   Arguments and results are those of csa2_sparse_attn_decode without

@@ -47,7 +47,7 @@ def test_workspace_size_and_shape_checks(mod):
     d = mod.Dims(max_ctx=131072)
     assert mod.workspace_size(d, 8) > 8 * 131072 * 4
     bad = [dict(idx_heads=17), dict(idx_heads=0), dict(idx_dim=64), dict(pool_blocks=4096),
-           dict(topk=1024), dict(heads=128), dict(swa=256), dict(max_ctx=(1 << 20) + 1)]
+           dict(topk=4096), dict(heads=128), dict(swa=256), dict(max_ctx=(1 << 20) + 1)]
     for kw in bad:
         with pytest.raises(mod.Csa2Error) as e:
             mod.workspace_size(mod.Dims(**{**d.__dict__, **kw}), 1)

@@ -93,3 +93,22 @@ def test_attention_no_swa_window():
     tk = random_topk(p, np.random.default_rng(3))
     out, lse = run_attn(p, tk, [0, 0])
     check(p, tk, out, lse, [0, 0])
+
+
+def test_attention_more_than_eight_chunks():
+    """Top-1024 + SWA-128 = 9 chunks of 128: the one-CTA-per-chunk kernel and the
+    combine kernel (above the cluster limit)."""
+    p = make_problem([6000, 1500], K=1024, seed=16)
+    tk = random_topk(p, np.random.default_rng(4))
+    out, lse = run_attn(p, tk)
+    check(p, tk, out, lse)
+
+
+def test_attention_window_not_on_chunk_boundary():
+    """Top-448: the SWA window starts inside a chunk, so its rows are copied with
+    the FP4 entries of that chunk (both channel halves), not loaded by TMA."""
+    p = make_problem([5000, 300], K=448, seed=17)
+    tk = random_topk(p, np.random.default_rng(5))
+    sl = [128, 77]
+    out, lse = run_attn(p, tk, sl)
+    check(p, tk, out, lse, sl)

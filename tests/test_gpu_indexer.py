@@ -143,3 +143,12 @@ def test_pool_len_and_padding_short_context():
     assert tk[0, :3].tolist() == [0, 1, 2] and np.all(tk[0, 3:] == -1)
     assert tk[1, :1].tolist() == [0] and np.all(tk[1, 1:] == -1)
     assert tk[2, :40].tolist() == list(range(40))
+
+
+def test_full_and_reindex_top1024():
+    """Top-K above the pages' 512 (the attention then spans 9 chunks)."""
+    p = make_problem([40000, 3000], K=1024, seed=18, with_kv=False)
+    pool, plen, topk = run_full(p)
+    check_full(p, pool, plen, topk)
+    tk = run_reindex(p, pool, plen)
+    np.testing.assert_array_equal(tk.cpu().numpy(), topk.cpu().numpy())
