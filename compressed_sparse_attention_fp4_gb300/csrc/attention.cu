@@ -411,13 +411,19 @@ constexpr int kPairQBytes = kPairRegions * kQRegion;  // 40 KB
 constexpr int kSxBytes = kEntries * kQRows * 4;       // 32 KB: the partner's S^T partial
 constexpr uint32_t kPairTmemCols = 256;               // S^T: 64 cols, O^T: 2 x 64 cols
 
-// Arrives on the mbarrier at the same shared-memory offset in CTA `rank` of
-// the cluster, releasing this thread's (and, cumulatively, its CTA's) prior
-// writes at cluster scope.
-__device__ inline void remote_arrive(uint64_t* bar, uint32_t rank) {
+// Shared-memory address of the same object in CTA `rank` of the cluster.
+__device__ inline uint32_t cluster_addr(const void* p, uint32_t rank) {
   uint32_t raddr;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(tc::smem_u32(bar)), "r"(rank));
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr) : "memory");
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(tc::smem_u32(p)), "r"(rank));
+  return raddr;
+}
+
+// 16 bytes into another CTA's shared memory; the bytes complete a transaction
+// on that CTA's mbarrier (which expects them).
+__device__ inline void st_async_v4(uint32_t raddr, float4 v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+               ::"r"(raddr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rbar)
+               : "memory");
 }
 
 __device__ inline bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
@@ -450,6 +456,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __shared__ __align__(16) float red_l[4][4][16];
   __shared__ float fac_s[kQRows];                   // 2^(m_chunk - M) / L per head
   __shared__ float ml_all[kMaxClusterSplits][2][kQRows];   // every chunk's (m, l), base-2 m
+  __shared__ bool x_ok;
 
   cg::cluster_group cl = cg::this_cluster();
   const int rank = int(cl.block_rank()), csize = int(cl.num_blocks());
@@ -464,8 +471,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc::mbar_init(&bar_ld, 1);
     tc::mbar_init(&bar_s, 1);
     tc::mbar_init(&bar_o, 1);
-    tc::mbar_init(&bar_x, 1);                        // the partner's arrival
+    tc::mbar_init(&bar_x, 1);                        // the partner's S^T partial (32 KB)
     tc::fence_mbar_init();
+    tc::mbar_expect_tx(&bar_x, uint32_t(kSxBytes));  // this CTA's arrival; the bytes come by st.async
   }
   // every CTA of the cluster must have started before another writes into
   // its shared memory: arrive now, wait before the first such write
@@ -635,14 +643,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc::tmem_ld16(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(hg * 16), x);
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA has started
   {
-    float4* dst = reinterpret_cast<float4*>(cl.map_shared_rank(sx, rank ^ 1) + e * kQRows + hg * 16);
+    const uint32_t dst = cluster_addr(sx + e * kQRows + hg * 16, uint32_t(rank ^ 1));
+    const uint32_t rbar = cluster_addr(&bar_x, uint32_t(rank ^ 1));
 #pragma unroll
-    for (int i = 0; i < 4; ++i) dst[i] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+    for (int i = 0; i < 4; ++i)
+      st_async_v4(dst + 16 * i, make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]), rbar);
   }
-  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+  // one thread waits for the partner's bytes; the CTA barrier passes them on
+  if (tid == 0) x_ok = mbar_wait_cluster(&bar_x, 0);
   __syncthreads();
-  if (tid == 0) remote_arrive(&bar_x, uint32_t(rank ^ 1));
-  ok = mbar_wait_cluster(&bar_x, 0) && ok;
+  ok = x_ok && ok;
   {
     const float4* src = reinterpret_cast<const float4*>(sx + e * kQRows + hg * 16);
 #pragma unroll
