@@ -260,7 +260,11 @@ __device__ void radix_edges(SelSmem& sm, const SelCtx& c, int n_local, uint32_t 
     find_buckets(sm);
     if (pass == 0) {
       b0 = sm.bucket[0];
-      if (sh0 == 0 || sm.ghist[0][b0] <= kRefine) break;    // narrow enough
+      // narrow enough: few items, or a value width below the largest bound
+      // (refining could not shrink the band by more than that)
+      const uint64_t top = min64(int64_t(kb) + (int64_t(b0) << sh0) + ((int64_t(1) << sh0) - 1), int64_t(sm.kmax_all));
+      const float wv = key_f32(uint32_t(top)) - key_f32(kb + (b0 << sh0));
+      if (sh0 == 0 || sm.ghist[0][b0] <= kRefine || wv <= sm.dmax_all) break;
     } else {
       width_shift = sh1;
     }
@@ -453,7 +457,59 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
   __syncthreads();
   uint32_t kmin_l = 0xFFFFFFFFu, kmax_l = 0;
   float dmax_l = 0.0f;
-  {
+  if (kind != kBlocks) {
+    // positions: the 8 items of a pool block are contiguous scores with one
+    // bound; a thread takes whole blocks (2 per thread at most)
+    const float* ws_f = reinterpret_cast<const float*>(a.ws);
+    const bool vec = kind == kReindexPos || (a.d.max_ctx & 7) == 0;   // 32-byte aligned blocks in the row
+#pragma unroll
+    for (int k = 0; k < kSelCapPerCta / kBlock / kSelThreads; ++k) {
+      const int jb = tid + k * kSelThreads;
+      if (jb * kBlock >= n_local) break;
+      const int64_t gi0 = base + int64_t(jb) * kBlock;
+      const int32_t blk = sm.pool_ids[gi0 >> 3];
+      float v[kBlock];
+      float dl = -1.0f;
+      int nv = 0;                                    // valid positions of the block
+      if (blk >= 0 && int64_t(blk) * kBlock < c.n_ctx) {
+        nv = int(min64(kBlock, c.n_ctx - int64_t(blk) * kBlock));
+        const float* src;
+        if (kind == kPoolPos) {
+          src = ws_f + (a.L.pos_scores >> 2) + int64_t(c.b) * a.d.max_ctx + int64_t(blk) * kBlock;
+          dl = ws_f[(a.L.blk_delta >> 2) + int64_t(c.b) * a.L.nb_max + blk];
+        } else {
+          src = ws_f + (a.L.ri_scores >> 2) + int64_t(c.b) * a.d.pool_blocks * kBlock + gi0;
+          dl = ws_f[(a.L.ri_delta >> 2) + int64_t(c.b) * a.d.pool_blocks + (gi0 >> 3)];
+        }
+        if (vec) {
+          const float4 lo = reinterpret_cast<const float4*>(src)[0], hi = reinterpret_cast<const float4*>(src)[1];
+          v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w; v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
+        } else {
+#pragma unroll
+          for (int i = 0; i < kBlock; ++i) v[i] = i < nv ? src[i] : 0.0f;
+        }
+      }
+      uint32_t kv[kBlock], kd[kBlock];
+#pragma unroll
+      for (int i = 0; i < kBlock; ++i) {
+        kv[i] = 0;
+        kd[i] = 0;
+        if (i < nv) {
+          kv[i] = f32_key(v[i]);
+          kd[i] = __float_as_uint(dl);
+          kmin_l = min(kmin_l, kv[i]);
+          kmax_l = max(kmax_l, kv[i]);
+          dmax_l = fmaxf(dmax_l, dl);
+        }
+      }
+      uint4* ku = reinterpret_cast<uint4*>(sm.keyU + jb * kBlock);
+      uint4* kl = reinterpret_cast<uint4*>(sm.keyL + jb * kBlock);
+      ku[0] = make_uint4(kv[0], kv[1], kv[2], kv[3]);
+      ku[1] = make_uint4(kv[4], kv[5], kv[6], kv[7]);
+      kl[0] = make_uint4(kd[0], kd[1], kd[2], kd[3]);
+      kl[1] = make_uint4(kd[4], kd[5], kd[6], kd[7]);
+    }
+  } else {
     // every item load of this thread is issued before any key is formed
     constexpr int kPer = kSelCapPerCta / kSelThreads;
     float vv[kPer], dd[kPer];                        // dd < 0: not an item
