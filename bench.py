@@ -77,9 +77,11 @@ def full_call_bytes(wl):
     return sum(idx_row * n + q_w + wl.pool_blocks * 4 + wl.topk * 4 for n in wl.ctx_lens)
 
 
-# ncu dram traffic per launch of the scan kernel, keyed by the hash of the
-# indexer source it was captured on (null once the kernel changes).
-TRAFFIC = {}
+# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
+# of the scan kernel per indexed position, keyed by the hash of the scan source
+# it was captured on (null once the kernel changes).  Captured on decode-128k
+# (1,048,576 positions); the traffic grows in proportion to the positions.
+TRAFFIC = {"965592bbeb77": 139013632 / 1048576}
 
 
 def src_hash(name):
@@ -370,7 +372,8 @@ def main():
     scan_bytes = sum(wl.idx_dim * (1 if wl.idx_k_dtype == "fp8" else 4) * n for n in wl.ctx_lens)
     achieved = scan_bytes / (kern_us[scan_name] * 1e-6) / 1e9
     th = src_hash("scan.cu")
-    traffic = TRAFFIC.get(th)
+    per_pos = TRAFFIC.get(th) if wl.idx_k_dtype == "fp8" else None
+    traffic = per_pos * sum(wl.ctx_lens) if per_pos is not None else None
     fb = full_call_bytes(wl)
     sbytes = step_bytes(wl)
     line = {
