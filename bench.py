@@ -172,7 +172,16 @@ def oracle_query(wl, b, kv, layers):
                                  wl.topk, wl.scale)
 
 
-def cpu_baseline(wl, budget_s=20.0, max_queries=8):
+def arm_config(wl, world):
+    """The workload description both arms print."""
+    return {"workload": f"decode-{wl.name}", "batch": wl.batch,
+            "ctx": wl.ctx_lens[0] if len(set(wl.ctx_lens)) == 1 else "mixed",
+            "schedule": "".join(m[0] if m != "Ri" else "I" for m in wl.schedule),
+            "l2": "flushed before every timed step (2x L2 write)",
+            "parallelism": f"replicas x{world}"}
+
+
+def cpu_baseline(wl, budget_s=20.0, max_queries=16):
     from compressed_sparse_attention_fp4_gb300 import synth
     cores = len(os.sched_getaffinity(0))
     done, t_cpu = 0, 0.0
@@ -240,12 +249,13 @@ def main():
         ms = 1000.0 * float(np.mean(steps_t))
         val = 1.0 / float(np.mean(steps_t))
         cb["value"] = val
+        cfg = arm_config(wl, world)
+        cfg["sample"] = "1 query per step (the CPU oracle on the host cores)"
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "queries/s",
-                "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": {"workload": f"decode-{wl.name}",
-                                                "batch": wl.batch, "ctx": wl.ctx_lens[0],
-                                                "sample": "1 query per step"},
+                "data": "synthetic (seeded; shapes and value recipes of the workload)",
+                "config": cfg,
                 "cpu_baseline": cb,
                 "e2e": {"value": val, "unit": "queries/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
@@ -381,11 +391,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; shapes and value recipes of the workload)",
-        "config": {"workload": f"decode-{wl.name}", "batch": wl.batch,
-                   "ctx": wl.ctx_lens[0] if len(set(wl.ctx_lens)) == 1 else "mixed",
-                   "schedule": "".join(m[0] if m != "Ri" else "I" for m in wl.schedule),
-                   "l2": "flushed before every timed step (2x L2 write)",
-                   "parallelism": f"replicas x{world}"},
+        "config": arm_config(wl, world),
         "step_gbs": sbytes / (t_step * 1e-3) / 1e9,
         "step_frac_of_peak": sbytes / (t_step * 1e-3) / 1e9 / peak,
         "algorithmic_bytes_per_step": sbytes,
