@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* kv_s = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);   // nreg x 16 KB
   uint8_t* q_s = kv_s + kPairKvBytes;               // nreg x 8 KB; later P^T hi / lo
-  float* sx = reinterpret_cast<float*>(q_s + kPairQBytes);   // [entry][head], written by the partner
+  float* sx = reinterpret_cast<float*>(q_s + kPairQBytes);   // [entry][head chunk], written by the partner
   __shared__ uint64_t bar_ld, bar_s, bar_o, bar_x;
   __shared__ uint32_t tmem_slot;
   __shared__ int64_t row_s[kEntries];               // >= 0 main row, -2 - r SWA row r, -1 empty
@@ -642,22 +642,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   float x[16];
   tc::tmem_ld16(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(hg * 16), x);
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA has started
+  // row e of sx holds 16 chunks of 4 heads; chunk c sits at c ^ (e % 16) so
+  // that the 32 rows of a warp spread over the banks
   {
-    const uint32_t dst = cluster_addr(sx + e * kQRows + hg * 16, uint32_t(rank ^ 1));
+    const uint32_t dst = cluster_addr(sx + e * kQRows, uint32_t(rank ^ 1));
     const uint32_t rbar = cluster_addr(&bar_x, uint32_t(rank ^ 1));
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      st_async_v4(dst + 16 * i, make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]), rbar);
+      st_async_v4(dst + 16 * ((hg * 4 + i) ^ (e & 15)),
+                  make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]), rbar);
   }
   // one thread waits for the partner's bytes; the CTA barrier passes them on
   if (tid == 0) x_ok = mbar_wait_cluster(&bar_x, 0);
   __syncthreads();
   ok = x_ok && ok;
   {
-    const float4* src = reinterpret_cast<const float4*>(sx + e * kQRows + hg * 16);
+    const float4* src = reinterpret_cast<const float4*>(sx + e * kQRows);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float4 v = src[i];
+      const float4 v = src[(hg * 4 + i) ^ (e & 15)];
       // own + partner: the same sum in both CTAs (fp32 addition commutes)
       x[4 * i] += v.x; x[4 * i + 1] += v.y; x[4 * i + 2] += v.z; x[4 * i + 3] += v.w;
     }
