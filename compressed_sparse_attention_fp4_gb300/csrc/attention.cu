@@ -418,11 +418,11 @@ __device__ inline uint32_t cluster_addr(const void* p, uint32_t rank) {
   return raddr;
 }
 
-// 16 bytes into another CTA's shared memory; the bytes complete a transaction
-// on that CTA's mbarrier (which expects them).
-__device__ inline void st_async_v4(uint32_t raddr, float4 v, uint32_t rbar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
-               ::"r"(raddr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rbar)
+// Bulk copy of `bytes` from this CTA's shared memory into another CTA's; the
+// bytes complete a transaction on that CTA's mbarrier (which expects them).
+__device__ inline void bulk_to_peer(uint32_t raddr, const void* src, uint32_t bytes, uint32_t rbar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(raddr), "r"(tc::smem_u32(src)), "r"(bytes), "r"(rbar)
                : "memory");
 }
 
@@ -449,6 +449,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* kv_s = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);   // nreg x 16 KB
   uint8_t* q_s = kv_s + kPairKvBytes;               // nreg x 8 KB; later P^T hi / lo
   float* sx = reinterpret_cast<float*>(q_s + kPairQBytes);   // [entry][head chunk], written by the partner
+  float* sx_out = sx + kEntries * kQRows;           // this CTA's partial, copied to the partner
   __shared__ uint64_t bar_ld, bar_s, bar_o, bar_x;
   __shared__ uint32_t tmem_slot;
   __shared__ int64_t row_s[kEntries];               // >= 0 main row, -2 - r SWA row r, -1 empty
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc::mbar_init(&bar_o, 1);
     tc::mbar_init(&bar_x, 1);                        // the partner's S^T partial (32 KB)
     tc::fence_mbar_init();
-    tc::mbar_expect_tx(&bar_x, uint32_t(kSxBytes));  // this CTA's arrival; the bytes come by st.async
+    tc::mbar_expect_tx(&bar_x, uint32_t(kSxBytes));  // this CTA's arrival; the partner's bulk copy brings the bytes
   }
   // every CTA of the cluster must have started before another writes into
   // its shared memory: arrive now, wait before the first such write
@@ -642,15 +643,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   float x[16];
   tc::tmem_ld16(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(hg * 16), x);
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA has started
-  // row e of sx holds 16 chunks of 4 heads; chunk c sits at c ^ (e % 16) so
-  // that the 32 rows of a warp spread over the banks
+  // row e holds 16 chunks of 4 heads; chunk c sits at c ^ (e % 16) so that
+  // the 32 rows of a warp spread over the banks.  The partial goes to this
+  // CTA's sx_out, then one bulk copy into the partner's sx.
   {
-    const uint32_t dst = cluster_addr(sx + e * kQRows, uint32_t(rank ^ 1));
-    const uint32_t rbar = cluster_addr(&bar_x, uint32_t(rank ^ 1));
+    float4* dst = reinterpret_cast<float4*>(sx_out + e * kQRows);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      st_async_v4(dst + 16 * ((hg * 4 + i) ^ (e & 15)),
-                  make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]), rbar);
+      dst[(hg * 4 + i) ^ (e & 15)] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+  }
+  tc::fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    bulk_to_peer(cluster_addr(sx, uint32_t(rank ^ 1)), sx_out, uint32_t(kSxBytes),
+                 cluster_addr(&bar_x, uint32_t(rank ^ 1)));
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
   }
   // one thread waits for the partner's bytes; the CTA barrier passes them on
   if (tid == 0) x_ok = mbar_wait_cluster(&bar_x, 0);
@@ -788,6 +795,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc::tc_fence_before_sync();
   __syncthreads();
   if (wid == 0) tc::tmem_dealloc(tmem, kPairTmemCols);
+  if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // sx_out read out
   // coalesced vector reduce-adds into this half's output dimensions
   const float4* ob = reinterpret_cast<const float4*>(obuf);
   for (int i = tid; i < H * 64; i += kAttnThreads) {
@@ -868,7 +876,7 @@ cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
   size_t smem = attn_smem_bytes(a.d.heads);
   if (a.L.splits <= kMaxClusterSplits) {
     // one cluster of 2 x chunks CTAs per sequence; the merge happens inside it
-    const size_t psmem = size_t(kPairKvBytes) + size_t(kPairQBytes) + size_t(kSxBytes) + 1024;
+    const size_t psmem = size_t(kPairKvBytes) + size_t(kPairQBytes) + 2 * size_t(kSxBytes) + 1024;
     cudaError_t e = cudaFuncSetAttribute(attn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(psmem));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(attn_pair_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
