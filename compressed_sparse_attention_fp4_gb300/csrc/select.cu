@@ -69,13 +69,17 @@ struct SelSmem {
 
 // Scratch of the exact re-scoring, overlaid on keyU (free between the
 // classification and the final pick).
+constexpr int kExRows = 48;                // positions per round of the exact re-scoring
+constexpr int kExRowWords = 129;          // 128 words + 1 word of bank skew
+constexpr int kExSumThreads = 64;         // threads that form the ordered head sums
+
 struct ExScratch {
-  double dd[64 * kMaxIdxHeads];             // exact head dots of a round
+  double dd[2][kExRows * kMaxIdxHeads];     // w_h * ReLU(d_h) of a round, double-buffered
   double cand_score[kSelThreads];
   int64_t cand_pos[kSelThreads];            // candidate positions of a chunk
   unsigned long long item_best[128];
   int32_t cand_item[kSelThreads];
-  int32_t krows[64 * 129];                  // staged keys: E4M3 as k*2^9 integers, or fp32 bits
+  int32_t krows[kExRows * kExRowWords];     // staged keys: E4M3 as k*2^9 integers, or fp32 bits
 };
 static_assert(sizeof(ExScratch) <= sizeof(uint32_t) * kSelCapPerCta, "exact scratch must fit keyU");
 
@@ -357,84 +361,86 @@ __device__ inline ItemVal load_item(const IdxArgs& a, ItemKind kind, const SelCt
 }
 
 // Exact scores of a list of positions (fp64, -inf for invalid ones), using
-// the whole CTA.  Round of up to kExRows positions: their indexer-K rows are
-// staged in shared memory; one thread per (position, head) sums the Di exact
-// products serially in int64 (or, for a span too wide, in the multi-limb
-// accumulator) and rounds once; then one thread per position forms the fp64
-// head sum in head order.  All positions of a round proceed in parallel.
-constexpr int kExRows = 64;
-constexpr int kExRowWords = 129;          // 128 words + 1 word of bank skew
-
+// the whole CTA, in rounds of up to kExRows positions.  In round r the first
+// kExSumThreads threads form the ordered fp64 head sums of round r - 1 (a
+// chain of dependent fp64 additions, one thread per position) while the
+// other threads stage round r's indexer-K rows in shared memory and compute
+// its products w_h * ReLU(d_h): one thread per (position, head) sums the Di
+// exact products serially in int64 (or, for a span too wide, in the
+// multi-limb accumulator) and rounds once.
 __device__ void exact_scores(const IdxArgs& a, SelSmem& sm, const SelCtx& c, const int64_t* pos,
                              int np, double* out) {
   ExScratch& ex = ex_scratch(sm);
   const int tid = threadIdx.x;
   const int hi = a.d.idx_heads, di = a.d.idx_dim;
   const bool fp8 = a.d.idx_k_dtype == CSA2_IDXK_E4M3;
-  for (int r0 = 0; r0 < np; r0 += kExRows) {
-    const int nr = min(kExRows, np - r0);
-    __syncthreads();
-    // stage the rows: E4M3 keys as exact integers k * 2^9, fp32 keys as bits
-    for (int i = tid; i < nr * di; i += blockDim.x) {
-      int rr = i / di, ch = i % di;
-      int64_t t = pos[r0 + rr];
-      int32_t v = 0;
-      if (t >= 0 && t < c.n_ctx) {
-        int64_t row = kv_row(a.page_table, a.d, c.b, t, a.ws);
-        if (row >= 0) {
-          if (fp8) {
-            Factor f = factor_e4m3(reinterpret_cast<const uint8_t*>(a.idx_k)[row * di + ch]);
-            v = f.sig * (1 << (f.exp + 9));
-          } else {
-            v = reinterpret_cast<const int32_t*>(a.idx_k)[row * di + ch];
+  const int rounds = (np + kExRows - 1) / kExRows;
+  constexpr int kWork = kSelThreads - kExSumThreads;
+  for (int r = 0; r <= rounds; ++r) {
+    if (tid < kExSumThreads) {
+      // ---- ordered head sums of the previous round --------------------------------
+      if (r > 0) {
+        const int r0 = (r - 1) * kExRows, nr = min(kExRows, np - r0);
+        if (tid < nr) {
+          const int64_t t = pos[r0 + tid];
+          double sum = -INFINITY;
+          if (t >= 0 && t < c.n_ctx) {
+            sum = 0.0;
+            const double* row = ex.dd[(r - 1) & 1] + tid * kMaxIdxHeads;
+            for (int h = 0; h < hi; ++h) sum = __dadd_rn(sum, row[h]);
           }
+          out[r0 + tid] = sum;
         }
       }
-      ex.krows[rr * kExRowWords + ch] = v;
-    }
-    __syncthreads();
-    for (int task = tid; task < nr * hi; task += blockDim.x) {
-      const int rr = task / hi, h = task % hi;
-      const int32_t* kr = ex.krows + rr * kExRowWords;
-      double d;
-      if (fp8 && sm.q_fast[h]) {
-        // |sum| <= sum|qi| * 448*2^9 < 2^62: the int64 sum is exact
-        long long acc = 0;
+    } else if (r < rounds) {
+      const int wt = tid - kExSumThreads;
+      const int r0 = r * kExRows, nr = min(kExRows, np - r0);
+      // ---- stage the rows: E4M3 keys as exact integers k * 2^9, fp32 keys as bits
+      for (int i = wt; i < nr * di; i += kWork) {
+        int rr = i / di, ch = i % di;
+        int64_t t = pos[r0 + rr];
+        int32_t v = 0;
+        if (t >= 0 && t < c.n_ctx) {
+          int64_t row = kv_row(a.page_table, a.d, c.b, t, a.ws);
+          if (row >= 0) {
+            if (fp8) {
+              Factor f = factor_e4m3(reinterpret_cast<const uint8_t*>(a.idx_k)[row * di + ch]);
+              v = f.sig * (1 << (f.exp + 9));
+            } else {
+              v = reinterpret_cast<const int32_t*>(a.idx_k)[row * di + ch];
+            }
+          }
+        }
+        ex.krows[rr * kExRowWords + ch] = v;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kWork) : "memory");
+      // ---- products of this round --------------------------------------------------
+      for (int task = wt; task < nr * hi; task += kWork) {
+        const int rr = task / hi, h = task % hi;
+        const int32_t* kr = ex.krows + rr * kExRowWords;
+        double d;
+        if (fp8 && sm.q_fast[h]) {
+          // |sum| <= sum|qi| * 448*2^9 < 2^62: the int64 sum is exact
+          long long acc = 0;
 #pragma unroll 8
-        for (int ch = 0; ch < 128; ++ch) acc += (long long)sm.qi[ch * kMaxIdxHeads + h] * (long long)kr[ch];
-        d = int_to_f64_rn(acc, sm.q_elo[h] - 9);
-      } else {
-        auto kf = [&](int ch) {
-          return fp8 ? Factor{kr[ch], -9} : factor_f32(__int_as_float(kr[ch]));
-        };
-        Factor qrow[128];
-        for (int ch = 0; ch < di; ++ch) qrow[ch] = sm.qf[ch * kMaxIdxHeads + h];
-        d = exact_head_dot(qrow, di, kf);
+          for (int ch = 0; ch < 128; ++ch) acc += (long long)sm.qi[ch * kMaxIdxHeads + h] * (long long)kr[ch];
+          d = int_to_f64_rn(acc, sm.q_elo[h] - 9);
+        } else {
+          auto kf = [&](int ch) {
+            return fp8 ? Factor{kr[ch], -9} : factor_f32(__int_as_float(kr[ch]));
+          };
+          Factor qrow[128];
+          for (int ch = 0; ch < di; ++ch) qrow[ch] = sm.qf[ch * kMaxIdxHeads + h];
+          d = exact_head_dot(qrow, di, kf);
+        }
+        // w_h * ReLU(d_h)
+        const unsigned long long db = (unsigned long long)__double_as_longlong(d);
+        const bool positive = (db >> 63) == 0 && db != 0;
+        ex.dd[r & 1][rr * kMaxIdxHeads + h] = __dmul_rn(f32_to_f64_exact(sm.w[h]), positive ? d : 0.0);
       }
-      ex.dd[rr * kMaxIdxHeads + h] = d;
     }
     __syncthreads();
-    // w_h * ReLU(d_h): independent products, one thread per (position, head)
-    for (int task = tid; task < nr * hi; task += blockDim.x) {
-      const int rr = task / hi, h = task % hi;
-      double d = ex.dd[rr * kMaxIdxHeads + h];
-      unsigned long long db = (unsigned long long)__double_as_longlong(d);
-      bool positive = (db >> 63) == 0 && db != 0;
-      ex.dd[rr * kMaxIdxHeads + h] = __dmul_rn(f32_to_f64_exact(sm.w[h]), positive ? d : 0.0);
-    }
-    __syncthreads();
-    // the ordered fp64 sum over heads, one thread per position
-    if (tid < nr) {
-      int64_t t = pos[r0 + tid];
-      double s = -INFINITY;
-      if (t >= 0 && t < c.n_ctx) {
-        s = 0.0;
-        for (int h = 0; h < hi; ++h) s = __dadd_rn(s, ex.dd[tid * kMaxIdxHeads + h]);
-      }
-      out[r0 + tid] = s;
-    }
   }
-  __syncthreads();
 }
 
 // Monotone 64-bit key of a double (larger value -> larger key).
