@@ -300,8 +300,15 @@ def main():
     times = np.array([a.elapsed_time(b) for a, b in ev])          # ms
     t_step = max_over_ranks(float(times.mean()), world, dev)
     qps = job_queries_per_s(world, wl.batch, t_step)
-    launches = g.launches * args.steps
     status = csa2.get_device_status(sb.ws)
+    # kernel launches of one step, as the library's launch records count them
+    # (one eager step; the graph replays the same launches)
+    csa2.profile_enable(True)
+    torch.cuda.synchronize()
+    run_step(sb)
+    torch.cuda.synchronize()
+    launches = sum(n for n, _ in csa2.profile_read().values()) * args.steps
+    csa2.profile_enable(False)
 
     # ---- per-call breakdown (eager, events on the launching stream) ---------
     # The library's kernel timing brackets each of its launches with events

@@ -442,6 +442,28 @@ __device__ inline bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Remote arrival (release at cluster scope) on an mbarrier of another CTA.
+__device__ inline void mbar_arrive_remote(uint32_t rbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
+}
+
+// Cache row of entry slot `slot` of sequence b: a main-KV row (>= 0), SWA
+// row r as -2 - r, or -1 for an empty slot.  t is the slot's Top-K index
+// (slots < K); a bad index is reported when `report` is set.
+__device__ inline int64_t entry_row(const AttnArgs& a, int b, int slot, int32_t t, int64_t n_ctx, int swl,
+                                    bool report) {
+  const int K = a.d.topk, W = a.d.swa;
+  if (slot < K) {
+    if (t >= 0 && t < n_ctx) {
+      const int64_t r = kv_row(a.page_table, a.d, b, t, a.ws);
+      return r < 0 ? -1 : r;
+    }
+    if (report && (t >= n_ctx || t < -1)) raise_err(a.ws, CSA2_DEV_TOPK_IDX);
+    return -1;
+  }
+  return (slot < K + W && slot - K < swl) ? -2 - int64_t(slot - K) : -1;
+}
+
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_pair_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap swamap, int swa_tma_split) {
@@ -450,22 +472,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* q_s = kv_s + kPairKvBytes;               // nreg x 8 KB; later P^T hi / lo
   float* sx = reinterpret_cast<float*>(q_s + kPairQBytes);   // [entry][head chunk], written by the partner
   float* sx_out = sx + kEntries * kQRows;           // this CTA's partial, copied to the partner
-  __shared__ uint64_t bar_ld, bar_s, bar_o, bar_x;
+  __shared__ uint64_t bar_ld, bar_s, bar_o, bar_x, bar_ml, bar_zero;
   __shared__ uint32_t tmem_slot;
   __shared__ int64_t row_s[kEntries];               // >= 0 main row, -2 - r SWA row r, -1 empty
   __shared__ __align__(16) float red_m[4][4][16];
   __shared__ __align__(16) float red_l[4][4][16];
   __shared__ float fac_s[kQRows];                   // 2^(m_chunk - M) / L per head
-  __shared__ float ml_all[kMaxClusterSplits][2][kQRows];   // every chunk's (m, l), base-2 m
-  __shared__ bool x_ok;
+  __shared__ __align__(16) float ml_all[kMaxClusterSplits][2][kQRows];   // every chunk's (m, l), base-2 m
+  __shared__ __align__(16) float ml_mine[2][kQRows];                      // this chunk's, copied to all
+  __shared__ bool x_ok, ml_ok, z_ok;
 
   cg::cluster_group cl = cg::this_cluster();
   const int rank = int(cl.block_rank()), csize = int(cl.num_blocks());
-  const int chunk = rank >> 1, half = rank & 1;
+  const int chunk = rank >> 1, half = rank & 1, S = csize >> 1;
   const int b = blockIdx.y;
   const int H = a.d.heads, K = a.d.topk, W = a.d.swa;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nreg = half ? 5 : 4, reg0 = 4 * half;   // this CTA's regions of 64 channels (of 9)
+  const bool paged = a.page_table != nullptr;
+  const bool swa_tma = chunk == swa_tma_split;      // this chunk's rows are the SWA window
+  // the chunk that finishes first (the TMA-loaded SWA window, else chunk 0)
+  // zeroes the output and tells the other chunks of its half when it has
+  const bool zero_cta = chunk == (swa_tma_split >= 0 ? swa_tma_split : 0);
   // set-up that touches no global memory, then wait for the previous kernel
   if (wid == 0) tc::tmem_alloc(&tmem_slot, kPairTmemCols);
   if (tid == 0) {
@@ -473,54 +501,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc::mbar_init(&bar_s, 1);
     tc::mbar_init(&bar_o, 1);
     tc::mbar_init(&bar_x, 1);                        // the partner's S^T partial (32 KB)
+    tc::mbar_init(&bar_ml, 1);                       // every chunk's (m, l) (S x 512 bytes)
+    tc::mbar_init(&bar_zero, 1);                     // the zeroing chunk of this half is done
     tc::fence_mbar_init();
-    tc::mbar_expect_tx(&bar_x, uint32_t(kSxBytes));  // this CTA's arrival; the partner's bulk copy brings the bytes
+    // this CTA's own arrivals; the copies of the other CTAs bring the bytes
+    tc::mbar_expect_tx(&bar_x, uint32_t(kSxBytes));
+    tc::mbar_expect_tx(&bar_ml, uint32_t(S) * uint32_t(sizeof(ml_mine)));
   }
   // every CTA of the cluster must have started before another writes into
   // its shared memory: arrive now, wait before the first such write
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   pdl_wait();
   pdl_launch_dependents();
-  const bool paged = a.page_table != nullptr;
-  const bool swa_tma = chunk == swa_tma_split;      // this chunk's rows are the SWA window
-  const int64_t n_ctx = checked_ctx(a.ctx_len, a.d, b, paged, a.ws);
-  int swl = a.swa_len[b];
-  if (swl < 0 || swl > W) {
-    if (tid == 0 && half == 0) raise_err(a.ws, CSA2_DEV_SWA_LEN);
-    swl = swl < 0 ? 0 : W;
-  }
-  if (tid < kEntries) {
-    int slot = chunk * kEntries + tid;
-    int64_t r = -1;
-    if (slot < K) {
-      int32_t t = a.topk[int64_t(b) * K + slot];
-      if (t >= 0) {
-        if (t >= n_ctx) raise_err(a.ws, CSA2_DEV_TOPK_IDX);
-        else r = kv_row(a.page_table, a.d, b, t, a.ws);
-        if (r < 0) r = -1;
-      } else if (t < -1) {
-        raise_err(a.ws, CSA2_DEV_TOPK_IDX);
-      }
-    } else if (slot < K + W && slot - K < swl) {
-      r = -2 - (slot - K);
-    }
-    row_s[tid] = r;
-  }
-  tc::tc_fence_before_sync();
-  __syncthreads();
-  tc::tc_fence_after_sync();
-  const uint32_t tmem = tmem_slot;
-  // the chunk that finishes first (the TMA-loaded SWA window, else chunk 0)
-  // zeroes this half's output dimensions; the adds come after the cluster
-  // barrier of the merge
-  if (chunk == (swa_tma_split >= 0 ? swa_tma_split : 0)) {
-    for (int i = tid; i < H * 64; i += kAttnThreads) {
-      const int h = i >> 6, q = i & 63;
-      reinterpret_cast<float4*>(a.out + (int64_t(b) * H + h) * kLatent + half * 256)[q] =
-          make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
-  // ---- TMA: this half's query channels and, for the window's chunk, SWA rows ----
+  // ---- loads that depend on nothing earlier in this kernel go out first:
+  //      this half's query channels (and the window's rows) by TMA, the
+  //      chunk's Top-K indices and the lengths ---------------------------------------
   if (tid == 0) {
     tc::mbar_expect_tx(&bar_ld, uint32_t(nreg) * (uint32_t(kQRegion) + (swa_tma ? uint32_t(kRegion) : 0u)));
     for (int kb = 0; kb < nreg; ++kb)
@@ -529,36 +524,47 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int kb = 0; kb < nreg; ++kb)
         tc::tma_load_2d(&swamap, kv_s + kb * kRegion, 64 * (reg0 + kb), b * W, &bar_ld);
   }
+  auto topk_at = [&](int e) -> int32_t {
+    const int slot = chunk * kEntries + e;
+    return slot < K ? __ldg(a.topk + int64_t(b) * K + slot) : -1;
+  };
+  const int eg = tid >> 3;                          // this thread's gather entries: eg, eg + 64
+  int32_t tg0 = -1, tg1 = -1;
+  if (!swa_tma) {
+    tg0 = topk_at(eg);
+    tg1 = topk_at(eg + 64);
+  }
+  const int32_t trow = tid < kEntries ? topk_at(tid) : -1;
+  int swl = __ldg(a.swa_len + b);
+  const int64_t n_ctx = checked_ctx(a.ctx_len, a.d, b, paged, a.ws);
+  if (swl < 0 || swl > W) {
+    if (tid == 0 && half == 0) raise_err(a.ws, CSA2_DEV_SWA_LEN);
+    swl = swl < 0 ? 0 : W;
+  }
+  if (tid < kEntries) row_s[tid] = entry_row(a, b, chunk * kEntries + tid, trow, n_ctx, swl, true);
   // ---- FP4 entries: gather (all loads first), dequantize to bf16 -------------------
   if (!swa_tma) {
-    // latent: task = (entry, pair of 16-channel groups of this half); 2 per thread
-    uint4 cd[2];
+    // latent: task = (entry, pair of 16-channel groups of this half); rope
+    // (half 1): task = (entry, 16-byte chunk); entries eg and eg + 64
+    const int64_t rr[2] = {entry_row(a, b, chunk * kEntries + eg, tg0, n_ctx, swl, false),
+                           entry_row(a, b, chunk * kEntries + eg + 64, tg1, n_ctx, swl, false)};
+    const int gp = 8 * half + (tid & 7), rc = tid & 7;
+    uint4 cd[2], rp[2];
     uint32_t sc[2];
-    int64_t rr[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const int task = tid + k * kAttnThreads, e = task >> 3, gp = 8 * half + (task & 7);
-      rr[k] = row_s[e];
       cd[k] = make_uint4(0, 0, 0, 0);
+      rp[k] = make_uint4(0, 0, 0, 0);
       sc[k] = 0;
       if (rr[k] >= 0) {
         cd[k] = __ldg(reinterpret_cast<const uint4*>(a.codes + rr[k] * kCodesPerRow) + gp);
         sc[k] = __ldg(reinterpret_cast<const uint16_t*>(a.scales + rr[k] * kScalesPerRow) + gp);
+        if (half) rp[k] = __ldg(reinterpret_cast<const uint4*>(a.rope + rr[k] * kRope) + rc);
       }
     }
-    // rope (half 1): task = (entry, 16-byte chunk); 2 per thread
-    uint4 rp[2];
-    int64_t rr2[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const int task = tid + k * kAttnThreads, e = task >> 3, rc = task & 7;
-      rr2[k] = half ? row_s[e] : -1;
-      rp[k] = make_uint4(0, 0, 0, 0);
-      if (rr2[k] >= 0) rp[k] = __ldg(reinterpret_cast<const uint4*>(a.rope + rr2[k] * kRope) + rc);
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int task = tid + k * kAttnThreads, e = task >> 3, gp = 8 * half + (task & 7);
+      const int e = eg + 64 * k;
       if (rr[k] <= -2) continue;                     // SWA row: copied below
       uint32_t cw[4] = {cd[k].x, cd[k].y, cd[k].z, cd[k].w};
 #pragma unroll
@@ -577,15 +583,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         st_shared_v4(kv_s, region * kRegion + tc::sw128_offset(e, ch0), make_uint4(w[0], w[1], w[2], w[3]));
         st_shared_v4(kv_s, region * kRegion + tc::sw128_offset(e, ch0 + 1), make_uint4(w[4], w[5], w[6], w[7]));
       }
+      if (half) st_shared_v4(kv_s, 4 * kRegion + tc::sw128_offset(e, rc), rp[k]);
     }
-    if (half) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int task = tid + k * kAttnThreads, e = task >> 3, rc = task & 7;
-        if (rr2[k] <= -2) continue;
-        st_shared_v4(kv_s, 4 * kRegion + tc::sw128_offset(e, rc), rp[k]);
-      }
-    }
+  }
+  tc::tc_fence_before_sync();
+  __syncthreads();
+  tc::tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+  if (!swa_tma) {
     // SWA rows of a chunk the window does not start on a 128-row boundary for
     const int nch = nreg * 8, c0 = reg0 * 8;          // this half's 16-byte chunks of a row
 #pragma unroll 4
@@ -596,6 +601,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       uint4 v = __ldg(reinterpret_cast<const uint4*>(a.swa + (int64_t(b) * W + (-2 - r)) * kDqk) + c0 + c);
       st_shared_v4(kv_s, (c >> 3) * kRegion + tc::sw128_offset(e, c & 7), v);
     }
+  }
+  if (zero_cta) {
+    for (int i = tid; i < H * 64; i += kAttnThreads) {
+      const int h = i >> 6, q = i & 63;
+      reinterpret_cast<float4*>(a.out + (int64_t(b) * H + h) * kLatent + half * 256)[q] =
+          make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA has started
+    // the zeros happen before every later reduce-add of this half
+    if (tid < csize && (tid & 1) == half && (tid >> 1) != chunk)
+      mbar_arrive_remote(cluster_addr(&bar_zero, uint32_t(tid)));
   }
   bool ok = tc::mbar_wait_bounded(&bar_ld, 0);
   if (swa_tma) {
@@ -642,7 +659,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const bool valid = row_s[e] != -1;
   float x[16];
   tc::tmem_ld16(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(hg * 16), x);
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA has started
+  if (!zero_cta) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA has started
   // row e holds 16 chunks of 4 heads; chunk c sits at c ^ (e % 16) so that
   // the 32 rows of a warp spread over the banks.  The partial goes to this
   // CTA's sx_out, then one bulk copy into the partner's sx.
@@ -724,16 +741,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc::fence_proxy_async_smem();
   tc::tc_fence_before_sync();
   __syncthreads();
-  // this chunk's (m, l) per head, written by half 0 into every CTA of the cluster
-  if (half == 0 && quarter == 0 && lane < 16) {
-    const int h = hg * 16 + lane;
-    const float M = fmaxf(fmaxf(red_m[hg][0][lane], red_m[hg][1][lane]), fmaxf(red_m[hg][2][lane], red_m[hg][3][lane]));
-    const float L = red_l[hg][0][lane] + red_l[hg][1][lane] + red_l[hg][2][lane] + red_l[hg][3][lane];
-    for (int r = 0; r < csize; ++r) {
-      cl.map_shared_rank(&ml_all[0][0][0], r)[(chunk * 2 + 0) * kQRows + h] = M;
-      cl.map_shared_rank(&ml_all[0][0][0], r)[(chunk * 2 + 1) * kQRows + h] = L;
-    }
-  }
 
   // ---- O^T = V_half^T . P^T  (this half's 2 M-tiles of 128 dims; hi and lo) --------
   if (tid == 0) {
@@ -754,14 +761,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     tc::mma_commit(&bar_o);
   }
-  ok = tc::mbar_wait_bounded(&bar_o, 0) && ok;
-  tc::tc_fence_after_sync();
-  if (!ok && tid == 0) raise_err(a.ws, CSA2_DEV_TIMEOUT);
+  // this chunk's (m, l) per head: half 0 copies it into every CTA of the cluster
+  if (half == 0 && quarter == 0) {
+    if (lane < 16) {
+      const int h = hg * 16 + lane;
+      ml_mine[0][h] = fmaxf(fmaxf(red_m[hg][0][lane], red_m[hg][1][lane]), fmaxf(red_m[hg][2][lane], red_m[hg][3][lane]));
+      ml_mine[1][h] = red_l[hg][0][lane] + red_l[hg][1][lane] + red_l[hg][2][lane] + red_l[hg][3][lane];
+    }
+    tc::fence_proxy_async_smem();
+    asm volatile("bar.sync 2, 128;" ::: "memory");   // the 4 warps of quarter 0
+    if (wid == 0 && lane < csize) {
+      bulk_to_peer(cluster_addr(&ml_all[chunk][0][0], uint32_t(lane)), &ml_mine[0][0], uint32_t(sizeof(ml_mine)),
+                   cluster_addr(&bar_ml, uint32_t(lane)));
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+  }
 
   // ---- merge over the cluster -------------------------------------------------------
-  cl.sync();                                        // every chunk's (m, l); the zeroed output
+  if (tid == 32) ml_ok = mbar_wait_cluster(&bar_ml, 0);     // every chunk's (m, l)
+  if (tid == 64) z_ok = zero_cta || mbar_wait_cluster(&bar_zero, 0);
+  __syncthreads();
+  ok = ml_ok && z_ok && ok;
   if (tid < kQRows) {
-    const int S = csize >> 1;
     float mr[kMaxClusterSplits], lr[kMaxClusterSplits];
     float M = -INFINITY;
 #pragma unroll
@@ -781,29 +802,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (rank == 0 && tid < H)
       a.lse[int64_t(b) * H + tid] = L > 0.0f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
   }
+  ok = tc::mbar_wait_bounded(&bar_o, 0) && ok;
+  tc::tc_fence_after_sync();
   __syncthreads();
-  // scaled O^T into shared memory as [head][256 dims] (the KV tile is no longer read)
-  float* obuf = reinterpret_cast<float*>(kv_s);
+  if (!ok && tid == 0) raise_err(a.ws, CSA2_DEV_TIMEOUT);
+  // scaled O^T added into this half's output dimensions straight from tensor
+  // memory: for one head the 32 lanes of a warp hold 32 consecutive dims
 #pragma unroll 1
   for (int mt = 0; mt < 2; ++mt) {
     float o[16];
     tc::tmem_ld16(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(64 + 64 * mt + hg * 16), o);
-    const int dim = mt * 128 + quarter * 32 + lane;
+    float* dst = a.out + int64_t(b) * H * kLatent + half * 256 + mt * 128 + quarter * 32 + lane;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) obuf[(hg * 16 + j) * 256 + dim] = o[j] * fac_s[hg * 16 + j];
+    for (int j = 0; j < 16; ++j) {
+      const int h = hg * 16 + j;
+      if (h < H)
+        asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst + int64_t(h) * kLatent), "f"(o[j] * fac_s[h])
+                     : "memory");
+    }
   }
   tc::tc_fence_before_sync();
   __syncthreads();
-  if (wid == 0) tc::tmem_dealloc(tmem, kPairTmemCols);
-  if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // sx_out read out
-  // coalesced vector reduce-adds into this half's output dimensions
-  const float4* ob = reinterpret_cast<const float4*>(obuf);
-  for (int i = tid; i < H * 64; i += kAttnThreads) {
-    const float4 v = ob[i];
-    float* dst = a.out + (int64_t(b) * H + (i >> 6)) * kLatent + half * 256 + (i & 63) * 4;
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
-                 ::"l"(dst), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
-                 : "memory");
+  if (wid == 0) {
+    tc::tmem_dealloc(tmem, kPairTmemCols);
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // sx_out, ml_mine read out
   }
 }
 

@@ -50,7 +50,7 @@ class StepBuffers:
     pool: torch.Tensor = None       # int32 [B, P]
     pool_len: torch.Tensor = None   # int32 [B]
     ws: torch.Tensor = None
-    launches: int = 0
+    calls: int = 0                  # library calls of the last run_step
 
     def allocate_outputs(self):
         L, B, d = len(self.schedule), self.batch, self.dims
@@ -65,27 +65,27 @@ class StepBuffers:
 
 
 def run_step(sb: StepBuffers, stream=None) -> int:
-    """Enqueue one decode step; returns the number of kernel launches."""
+    """Enqueue one decode step; returns the number of library calls made."""
     d, B = sb.dims, sb.batch
     cur = None
-    launches = 0
+    calls = 0
     for l, mode in enumerate(sb.schedule):
         if mode == "F":
             if sb.new_latent is not None:
                 csa2.fp4_kv_quantize_scatter(sb.new_latent, sb.new_rows, sb.kv_codes,
                                              sb.kv_scales, stream=stream)
-                launches += 1
+                calls += 1
             csa2.indexer_full_topk(d, B, sb.idx_k, sb.page_table, sb.ctx_len, sb.idx_q[l],
                                    sb.idx_w[l], sb.pool, sb.pool_len, sb.topk[l], sb.ws,
                                    stream=stream)
-            launches += 2
+            calls += 1
             cur = l
             m = csa2.MODE_FULL
         elif mode == "Ri":
             csa2.indexer_reindex_topk(d, B, sb.idx_k, sb.page_table, sb.ctx_len, sb.idx_q[l],
                                       sb.idx_w[l], sb.pool, sb.pool_len, sb.topk[l], sb.ws,
                                       stream=stream)
-            launches += 2
+            calls += 1
             cur = l
             m = csa2.MODE_REINDEX
         elif mode == "Ru":
@@ -98,9 +98,9 @@ def run_step(sb: StepBuffers, stream=None) -> int:
                                      sb.page_table, sb.ctx_len, sb.topk[cur], sb.swa[l],
                                      sb.swa_len[l], sb.scale, sb.out[l], sb.lse[l], sb.ws,
                                      stream=stream)
-        launches += 2
-    sb.launches = launches
-    return launches
+        calls += 1
+    sb.calls = calls
+    return calls
 
 
 class GraphedStep:
@@ -116,7 +116,7 @@ class GraphedStep:
         torch.cuda.current_stream().wait_stream(s)
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
-            self.launches = run_step(sb)
+            self.calls = run_step(sb)
 
     def replay(self):
         self.graph.replay()
