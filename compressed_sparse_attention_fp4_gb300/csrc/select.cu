@@ -72,6 +72,7 @@ struct SelSmem {
 constexpr int kExRows = 48;                // positions per round of the exact re-scoring
 constexpr int kExRowWords = 129;          // 128 words + 1 word of bank skew
 constexpr int kExSumThreads = 64;         // threads that form the ordered head sums
+constexpr int kStageWords = 2;            // row words a staging thread loads per batch
 
 struct ExScratch {
   double dd[2][kExRows * kMaxIdxHeads];     // w_h * ReLU(d_h) of a round, double-buffered
@@ -395,23 +396,41 @@ __device__ void exact_scores(const IdxArgs& a, SelSmem& sm, const SelCtx& c, con
     } else if (r < rounds) {
       const int wt = tid - kExSumThreads;
       const int r0 = r * kExRows, nr = min(kExRows, np - r0);
-      // ---- stage the rows: E4M3 keys as exact integers k * 2^9, fp32 keys as bits
-      for (int i = wt; i < nr * di; i += kWork) {
-        int rr = i / di, ch = i % di;
-        int64_t t = pos[r0 + rr];
-        int32_t v = 0;
-        if (t >= 0 && t < c.n_ctx) {
-          int64_t row = kv_row(a.page_table, a.d, c.b, t, a.ws);
-          if (row >= 0) {
-            if (fp8) {
-              Factor f = factor_e4m3(reinterpret_cast<const uint8_t*>(a.idx_k)[row * di + ch]);
-              v = f.sig * (1 << (f.exp + 9));
-            } else {
-              v = reinterpret_cast<const int32_t*>(a.idx_k)[row * di + ch];
-            }
+      // ---- stage the rows: E4M3 keys as exact integers k * 2^9, fp32 keys as
+      //      bits; 4-byte words of the rows, every load of a batch issued first
+      const int wpr = fp8 ? di >> 2 : di;            // words of a row
+      for (int w0 = 0; w0 < nr * wpr; w0 += kStageWords * kWork) {
+        int64_t srow[kStageWords];
+        uint32_t sw[kStageWords];
+#pragma unroll
+        for (int j = 0; j < kStageWords; ++j) {
+          const int i = w0 + wt + j * kWork;
+          srow[j] = -1;
+          if (i < nr * wpr) {
+            const int64_t t = pos[r0 + i / wpr];
+            if (t >= 0 && t < c.n_ctx) srow[j] = kv_row(a.page_table, a.d, c.b, t, a.ws);
           }
         }
-        ex.krows[rr * kExRowWords + ch] = v;
+#pragma unroll
+        for (int j = 0; j < kStageWords; ++j) {
+          const int i = w0 + wt + j * kWork;
+          sw[j] = srow[j] >= 0 ? reinterpret_cast<const uint32_t*>(a.idx_k)[srow[j] * wpr + i % wpr] : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < kStageWords; ++j) {
+          const int i = w0 + wt + j * kWork;
+          if (i >= nr * wpr) break;
+          int32_t* dst = ex.krows + (i / wpr) * kExRowWords;
+          if (fp8) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const Factor f = factor_e4m3((sw[j] >> (8 * q)) & 0xFFu);
+              dst[4 * (i % wpr) + q] = f.sig * (1 << (f.exp + 9));
+            }
+          } else {
+            dst[i % wpr] = int32_t(sw[j]);
+          }
+        }
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kWork) : "memory");
       // ---- products of this round --------------------------------------------------
@@ -468,44 +487,55 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
     // bound; a thread takes whole blocks (2 per thread at most)
     const float* ws_f = reinterpret_cast<const float*>(a.ws);
     const bool vec = kind == kReindexPos || (a.d.max_ctx & 7) == 0;   // 32-byte aligned blocks in the row
+    constexpr int kPB = kSelCapPerCta / kBlock / kSelThreads;   // blocks per thread
+    // every load of this thread is issued before any key is formed
+    float v[kPB][kBlock], dl[kPB];
+    int nv[kPB];                                     // valid positions of the block
 #pragma unroll
-    for (int k = 0; k < kSelCapPerCta / kBlock / kSelThreads; ++k) {
+    for (int k = 0; k < kPB; ++k) {
       const int jb = tid + k * kSelThreads;
-      if (jb * kBlock >= n_local) break;
       const int64_t gi0 = base + int64_t(jb) * kBlock;
+      dl[k] = -1.0f;
+      nv[k] = 0;
+#pragma unroll
+      for (int i = 0; i < kBlock; ++i) v[k][i] = 0.0f;
+      if (jb * kBlock >= n_local) continue;
       const int32_t blk = sm.pool_ids[gi0 >> 3];
-      float v[kBlock];
-      float dl = -1.0f;
-      int nv = 0;                                    // valid positions of the block
       if (blk >= 0 && int64_t(blk) * kBlock < c.n_ctx) {
-        nv = int(min64(kBlock, c.n_ctx - int64_t(blk) * kBlock));
+        nv[k] = int(min64(kBlock, c.n_ctx - int64_t(blk) * kBlock));
         const float* src;
         if (kind == kPoolPos) {
           src = ws_f + (a.L.pos_scores >> 2) + int64_t(c.b) * a.d.max_ctx + int64_t(blk) * kBlock;
-          dl = ws_f[(a.L.blk_delta >> 2) + int64_t(c.b) * a.L.nb_max + blk];
+          dl[k] = ws_f[(a.L.blk_delta >> 2) + int64_t(c.b) * a.L.nb_max + blk];
         } else {
           src = ws_f + (a.L.ri_scores >> 2) + int64_t(c.b) * a.d.pool_blocks * kBlock + gi0;
-          dl = ws_f[(a.L.ri_delta >> 2) + int64_t(c.b) * a.d.pool_blocks + (gi0 >> 3)];
+          dl[k] = ws_f[(a.L.ri_delta >> 2) + int64_t(c.b) * a.d.pool_blocks + (gi0 >> 3)];
         }
         if (vec) {
           const float4 lo = reinterpret_cast<const float4*>(src)[0], hi = reinterpret_cast<const float4*>(src)[1];
-          v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w; v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
+          v[k][0] = lo.x; v[k][1] = lo.y; v[k][2] = lo.z; v[k][3] = lo.w;
+          v[k][4] = hi.x; v[k][5] = hi.y; v[k][6] = hi.z; v[k][7] = hi.w;
         } else {
 #pragma unroll
-          for (int i = 0; i < kBlock; ++i) v[i] = i < nv ? src[i] : 0.0f;
+          for (int i = 0; i < kBlock; ++i) v[k][i] = i < nv[k] ? src[i] : 0.0f;
         }
       }
+    }
+#pragma unroll
+    for (int k = 0; k < kPB; ++k) {
+      const int jb = tid + k * kSelThreads;
+      if (jb * kBlock >= n_local) break;
       uint32_t kv[kBlock], kd[kBlock];
 #pragma unroll
       for (int i = 0; i < kBlock; ++i) {
         kv[i] = 0;
         kd[i] = 0;
-        if (i < nv) {
-          kv[i] = f32_key(v[i]);
-          kd[i] = __float_as_uint(dl);
+        if (i < nv[k]) {
+          kv[i] = f32_key(v[k][i]);
+          kd[i] = __float_as_uint(dl[k]);
           kmin_l = min(kmin_l, kv[i]);
           kmax_l = max(kmax_l, kv[i]);
-          dmax_l = fmaxf(dmax_l, dl);
+          dmax_l = fmaxf(dmax_l, dl[k]);
         }
       }
       uint4* ku = reinterpret_cast<uint4*>(sm.keyU + jb * kBlock);
@@ -775,29 +805,42 @@ __device__ int64_t block_sum(SelSmem& sm, int v) {
 // per-head minima, sums and flags are reduced in the warp first and reach
 // shared memory with one atomic per warp.
 __device__ void load_query_factors(const IdxArgs& a, SelSmem& sm, int b) {
-  const int hi = a.d.idx_heads, di = a.d.idx_dim;
+  const int hi = a.d.idx_heads, di = a.d.idx_dim, n = hi * di;
   const int lane = threadIdx.x & 31;
   const bool fp8 = a.d.idx_k_dtype == CSA2_IDXK_E4M3;
+  // every global load of this thread is issued before the first use
+  constexpr int kPer = kMaxIdxHeads * 128 / kSelThreads;
+  static_assert(kPer * kSelThreads == kMaxIdxHeads * 128, "query elements per thread");
+  float qv[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int i = threadIdx.x + j * kSelThreads;
+    const int64_t qidx = int64_t(b) * n + i;
+    qv[j] = i >= n ? 0.0f
+                   : fp8 ? bf16_to_f32(reinterpret_cast<const uint16_t*>(a.idx_q)[qidx])
+                         : reinterpret_cast<const float*>(a.idx_q)[qidx];
+  }
+  const float wv = threadIdx.x < hi ? a.w[int64_t(b) * hi + threadIdx.x] : 0.0f;
   if (threadIdx.x < kMaxIdxHeads) {
     sm.q_elo[threadIdx.x] = INT_MAX;
     sm.q_fast[threadIdx.x] = 1;
     sm.q_l1[threadIdx.x] = 0;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < hi * di; i += blockDim.x) {
+  // a warp's 32 elements lie in one head (n is a multiple of 32)
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int i = threadIdx.x + j * kSelThreads;
+    if (i >= n) break;
     const int h = i / di, ch = i % di;
-    const int64_t qidx = int64_t(b) * hi * di + i;
-    const float v = fp8 ? bf16_to_f32(reinterpret_cast<const uint16_t*>(a.idx_q)[qidx])
-                        : reinterpret_cast<const float*>(a.idx_q)[qidx];
-    const Factor f = factor_f32(v);
+    const Factor f = factor_f32(qv[j]);
     sm.qf[ch * kMaxIdxHeads + h] = f;
     int lsb = f.sig ? f.exp + __ffs(abs(f.sig)) - 1 : INT_MAX;      // lowest set bit
-#pragma unroll
-    for (int o = 16; o; o >>= 1) lsb = min(lsb, __shfl_xor_sync(0xFFFFFFFFu, lsb, o));
+    lsb = __reduce_min_sync(0xFFFFFFFFu, lsb);
     if (lane == 0 && lsb != INT_MAX) atomicMin(&sm.q_elo[h], lsb);
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < hi * di; i += blockDim.x) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const int h = i / di, ch = i % di;
     const Factor f = sm.qf[ch * kMaxIdxHeads + h];
     int32_t qv = 0;
@@ -817,15 +860,16 @@ __device__ void load_query_factors(const IdxArgs& a, SelSmem& sm, int b) {
       }
     }
     sm.qi[ch * kMaxIdxHeads + h] = qv;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) mag64 += __shfl_xor_sync(0xFFFFFFFFu, mag64, o);
+    // mag < 2^30: the warp sums of its 16-bit halves fit 32 bits
+    const uint32_t s_lo = __reduce_add_sync(0xFFFFFFFFu, uint32_t(mag64 & 0xFFFF));
+    const uint32_t s_hi = __reduce_add_sync(0xFFFFFFFFu, uint32_t(mag64 >> 16));
     const bool any_wide = __any_sync(0xFFFFFFFFu, wide);
     if (lane == 0) {
       if (any_wide) atomicAnd(&sm.q_fast[h], 0);
-      atomicAdd(&sm.q_l1[h], mag64);
+      atomicAdd(&sm.q_l1[h], (unsigned long long)s_hi * 65536ull + s_lo);
     }
   }
-  if (threadIdx.x < hi) sm.w[threadIdx.x] = a.w[int64_t(b) * hi + threadIdx.x];
+  if (threadIdx.x < hi) sm.w[threadIdx.x] = wv;
   __syncthreads();
   if (threadIdx.x < kMaxIdxHeads) {
     // int64 room: sum_c |qi| * max|k*2^9| (448 * 512) must stay below 2^62
