@@ -355,10 +355,15 @@ def main():
     kern_us = {k: 1000.0 * ms / n for k, (n, ms) in kern.items()}
 
     # ---- end to end through the public API with host buffers --------------
+    # Per-step inputs: every layer's query and indexer query / weights, the
+    # new token's latent (the FP4 append) and the newest SWA row of every
+    # layer (the window is a device-resident cache, like the main KV: one
+    # row per layer and sequence arrives per step, into its last slot).
     L = len(wl.schedule)
     pin = lambda t: t.cpu().pin_memory()
-    h_in = {"q": pin(sb.q), "swa": pin(sb.swa), "idx_q": pin(sb.idx_q), "idx_w": pin(sb.idx_w),
-            "new_latent": pin(sb.new_latent)}
+    swa_new = sb.swa[:, :, -1, :]                                 # [L, B, 576] strided view
+    h_in = {"q": pin(sb.q), "swa_row": pin(swa_new.contiguous()), "idx_q": pin(sb.idx_q),
+            "idx_w": pin(sb.idx_w), "new_latent": pin(sb.new_latent)}
     h_out = {"out": torch.empty_like(sb.out, device="cpu").pin_memory(),
              "lse": torch.empty_like(sb.lse, device="cpu").pin_memory(),
              "topk": torch.empty_like(sb.topk, device="cpu").pin_memory()}
@@ -370,7 +375,7 @@ def main():
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         sb.q.copy_(h_in["q"], non_blocking=True)
-        sb.swa.copy_(h_in["swa"], non_blocking=True)
+        swa_new.copy_(h_in["swa_row"], non_blocking=True)
         sb.idx_q.copy_(h_in["idx_q"], non_blocking=True)
         sb.idx_w.copy_(h_in["idx_w"], non_blocking=True)
         sb.new_latent.copy_(h_in["new_latent"], non_blocking=True)

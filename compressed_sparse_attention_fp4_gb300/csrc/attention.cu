@@ -899,9 +899,8 @@ cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
   if (a.L.splits <= kMaxClusterSplits) {
     // one cluster of 2 x chunks CTAs per sequence; the merge happens inside it
     const size_t psmem = size_t(kPairKvBytes) + size_t(kPairQBytes) + 2 * size_t(kSxBytes) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(attn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(psmem));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_pair_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    static KernelAttrs done;
+    cudaError_t e = prepare_kernel(attn_pair_kernel, psmem, true, done);
     if (e != cudaSuccess) return e;
     CSA2_PROFILED(st, "attn_pair_tc",
                   (e = launch_pdl(attn_pair_kernel, dim3(unsigned(2 * a.L.splits), unsigned(a.batch), 1),
@@ -909,8 +908,8 @@ cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
                                   swa_split)));
     return e;
   }
-  cudaError_t e = cudaFuncSetAttribute(attn_partial_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  static KernelAttrs done_partial;
+  cudaError_t e = prepare_kernel(attn_partial_tc_kernel, smem, false, done_partial);
   if (e != cudaSuccess) return e;
   CSA2_PROFILED(st, "attn_partial_tc",
                 (e = launch_pdl(attn_partial_tc_kernel, dim3(unsigned(a.L.splits), unsigned(a.batch)),

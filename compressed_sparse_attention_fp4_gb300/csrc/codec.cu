@@ -139,9 +139,7 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const uint2* __restrict
 }
 
 static int codec_grid(int64_t n) {
-  int dev = 0, sms = 152;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sms();
   int64_t want = (n + 7) / 8;                    // 8 warps per block, 1 row per warp
   int64_t cap = int64_t(sms) * 8;                // 8 blocks of 256 per SM, grid-stride
   return int(want < cap ? (want > 0 ? want : 1) : cap);

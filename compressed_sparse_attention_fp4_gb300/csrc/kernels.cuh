@@ -1,9 +1,57 @@
 // kernels.cuh -- argument blocks and host launchers of the library's kernels.
 #pragma once
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace csa2 {
+
+// The function attributes a launcher has set, per device, so that each is
+// set once per device and not on every call (the launch path of a decode
+// step runs thousands of times a second).
+constexpr int kMaxDevices = 64;
+struct KernelAttrs {
+  std::atomic<int> smem[kMaxDevices];        // dynamic shared memory limit set (0: none)
+  std::atomic<bool> cluster[kMaxDevices];    // non-portable cluster sizes allowed
+};
+
+// Raises `kernel`'s dynamic shared memory limit to `smem` and, when asked,
+// allows non-portable cluster sizes, on the current device.
+template <typename... KArgs>
+inline cudaError_t prepare_kernel(void (*kernel)(KArgs...), size_t smem, bool nonportable_cluster,
+                                  KernelAttrs& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool slot = dev >= 0 && dev < kMaxDevices;
+  if (!slot || done.smem[dev].load(std::memory_order_acquire) < int(smem)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    if (slot) done.smem[dev].store(int(smem), std::memory_order_release);
+  }
+  if (nonportable_cluster && (!slot || !done.cluster[dev].load(std::memory_order_acquire))) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    if (slot) done.cluster[dev].store(true, std::memory_order_release);
+  }
+  return cudaSuccess;
+}
+
+// Number of SMs of the current device (read once per device).
+inline int device_sms() {
+  static std::atomic<int> sms[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int n = sms[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+  }
+  int n = 152;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 152;
+  if (dev >= 0 && dev < kMaxDevices) sms[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
 
 // Launches `kernel` with programmatic stream serialisation (see pdl_wait) and,
 // for cluster_x > 1, thread-block clusters of cluster_x CTAs along x.

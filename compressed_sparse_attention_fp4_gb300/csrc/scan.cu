@@ -606,11 +606,10 @@ cudaError_t launch_scan_tc(const IdxArgs& a, bool reindex, cudaStream_t st) {
   // upper bound and the CTAs split the actual tiles evenly
   int64_t items_ub = reindex ? int64_t(a.d.pool_blocks) * kBlock : a.d.max_ctx;
   int64_t tiles_ub = int64_t(a.batch) * ((items_ub + kTile - 1) / kTile);
-  int dev = 0, sms = 152;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  size_t smem = sizeof(ScanSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  const int sms = device_sms();
+  const size_t smem = sizeof(ScanSmem) + 1024;
+  static KernelAttrs done;
+  cudaError_t e = prepare_kernel(scan_tc_kernel, smem, false, done);
   if (e != cudaSuccess) return e;
   int64_t grid = min64(int64_t(sms), tiles_ub);
   if (grid < 1) grid = 1;

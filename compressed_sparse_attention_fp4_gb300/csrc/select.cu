@@ -949,7 +949,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
 cudaError_t launch_select(IdxArgs a, bool reindex, cudaStream_t st) {
   int cs = reindex ? 1 : int((a.L.nb_max + kSelCapPerCta - 1) / kSelCapPerCta);
   size_t smem = sizeof(SelSmem);
-  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  static KernelAttrs done;
+  cudaError_t e = prepare_kernel(select_kernel, smem, false, done);
   if (e != cudaSuccess) return e;
   CSA2_PROFILED(st, reindex ? "select_reindex" : "select_full",
                 (e = launch_pdl(select_kernel, dim3(unsigned(cs), unsigned(a.batch), 1), dim3(kSelThreads), smem, st,

@@ -67,6 +67,8 @@ class StepBuffers:
 def run_step(sb: StepBuffers, stream=None) -> int:
     """Enqueue one decode step; returns the number of library calls made."""
     d, B = sb.dims, sb.batch
+    if stream is None:
+        stream = torch.cuda.current_stream()         # resolved once for the whole step
     cur = None
     calls = 0
     for l, mode in enumerate(sb.schedule):
