@@ -97,14 +97,17 @@ __device__ inline int64_t kv_row(const int32_t* __restrict__ page_table, const c
 
 // Context length of sequence b, checked against the capacity (max_ctx, and
 // max_pages * 64 for a paged cache).  A bad length is reported and treated as 0.
-__device__ inline int64_t checked_ctx(const int32_t* __restrict__ ctx_len, const csa2_dims& d,
-                                      int b, bool paged, uint8_t* ws) {
-  int64_t n = __ldg(ctx_len + b);
+__device__ inline int64_t check_ctx(int64_t n, const csa2_dims& d, bool paged, uint8_t* ws) {
   if (n < 0 || n > d.max_ctx || (paged && n > int64_t(d.max_pages) * kPage)) {
     raise_err(ws, CSA2_DEV_CTX_LEN);
     return 0;
   }
   return n;
+}
+
+__device__ inline int64_t checked_ctx(const int32_t* __restrict__ ctx_len, const csa2_dims& d,
+                                      int b, bool paged, uint8_t* ws) {
+  return check_ctx(__ldg(ctx_len + b), d, paged, ws);
 }
 
 // ---------------------------------------------------------------------------

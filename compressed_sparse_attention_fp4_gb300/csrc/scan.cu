@@ -72,13 +72,14 @@ constexpr int kMmaN = kTile + 32;          // Gram row + the two query pieces
 constexpr int kDBufs = 3;                  // tensor-memory accumulators in flight
 constexpr uint32_t kScanTmemCols = 512;    // D buffer j: cols 160j .. 160j+159
 constexpr float kTcErr = 1.6e-5f;          // 2^-16 + 2^-19 + fp64 rounding, rounded up
+constexpr int kSeqCache = 64;              // sequences whose item counts sit in shared memory
 
 struct ScanSmem {
   uint8_t stage[kStages][kStageStride];    // keys, then query pieces; 1024-aligned
   uint8_t qp[kQpBytes];                    // the current sequence's pieces (query group)
   float uq[2][kMaxIdxHeads][128];          // [epilogue group]: |w'_h| (|q1_hc| + |r1_hc|)
-  int64_t win_row[kStages * 16];           // Reindex producer: rows of a window's pool blocks
-  int32_t win_n[kStages * 16];             //   and their rows inside the context
+  int64_t seq_items[kSeqCache];            // items of the first sequences (read once)
+  int32_t n_seq_cached;
   float red[2][4];
   uint64_t full[kStages], empty[kStages], hdr[kStages];
   uint64_t d_full[kDBufs], d_empty[kDBufs];
@@ -137,10 +138,10 @@ __device__ inline int64_t scan_items(const IdxArgs& a, int b, bool reindex) {
 
 // Global tile g -> (sequence, first item); tiles of sequence b are
 // ceil(items_b / 128).  Linear walk from a hint (tiles are visited in order).
-__device__ inline TileRef tile_of(const IdxArgs& a, bool reindex, int64_t g, int& hint_b,
+__device__ inline TileRef tile_of(const IdxArgs& a, const ScanSmem& sm, bool reindex, int64_t g, int& hint_b,
                                   int64_t& hint_base) {
   while (true) {
-    int64_t n = scan_items(a, hint_b, reindex);
+    const int64_t n = hint_b < sm.n_seq_cached ? sm.seq_items[hint_b] : scan_items(a, hint_b, reindex);
     int64_t nt = (n + kTile - 1) / kTile;
     if (g < hint_base + nt) {
       TileRef r;
@@ -178,40 +179,18 @@ __device__ inline void issue_tile_load(const IdxArgs& a, const CUtensorMap* map,
 }
 
 // Reindex tiles: the pool blocks are scattered 1 KB runs (8 rows, never
-// across a page).  The producer warp first resolves the rows of the blocks
-// of a window of up to kStages tiles (pool id, then page table: the loads of
-// all blocks are in flight together), then gathers each tile with 16-byte
-// cp.async copies straight into the 128-byte swizzled layout; each lane's
-// copies arrive on the stage's mbarrier when they land (32 arrivals).
-__device__ inline void resolve_block(const IdxArgs& a, const TileRef& tr, int j, int64_t& row, int& nrow) {
-  row = -1;
-  nrow = 0;
-  if (j * kBlock >= tr.nvalid) return;
-  const bool paged = a.page_table != nullptr;
-  const int64_t n_ctx = checked_ctx(a.ctx_len, a.d, tr.b, paged, a.ws);
-  const int32_t blk = __ldg(a.pool_in + int64_t(tr.b) * a.d.pool_blocks + (tr.t0 >> 3) + j);
-  if (blk >= 0 && int64_t(blk) * kBlock < n_ctx) {
-    row = kv_row(a.page_table, a.d, tr.b, int64_t(blk) * kBlock, a.ws);
-    nrow = row >= 0 ? int(min64(kBlock, n_ctx - int64_t(blk) * kBlock)) : 0;
-  }
-}
+// across a page).  The producer warp resolves the cache rows of the blocks of
+// a window of up to kStages tiles (pool ids and lengths, then page table: the
+// loads of all its blocks in flight together), then gathers each tile with one
+// 8-row TMA box per block: block j lands 1 KB-aligned at rows 8j..8j+7, where
+// the 128-byte swizzle of an 8-row box is that of the whole tile.
+constexpr int kResolvePer = kStages * 16 / 32;   // blocks a producer lane resolves per window
 
-__device__ inline void gather_pool_tile(const IdxArgs& a, ScanSmem& sm, int w, int stage, int lane) {
-  const uint8_t* keys = reinterpret_cast<const uint8_t*>(a.idx_k);
-  const uint32_t dst0 = tc::smem_u32(sm.stage[stage]);
-#pragma unroll 4
-  for (int m = 0; m < 32; ++m) {                         // copy i = lane + 32m: block m/2
-    const int64_t rj = sm.win_row[w * 16 + (m >> 1)];
-    const int nr = sm.win_n[w * 16 + (m >> 1)];
-    const int rin = 4 * (m & 1) + (lane >> 3), c = lane & 7;
-    if (rj < 0 || rin >= nr) continue;
-    const int r = (m >> 1) * kBlock + rin;
-    const uint8_t* src = keys + (rj + rin) * 128 + c * 16;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst0 + tc::sw128_offset(r, c)), "l"(src)
-                 : "memory");
-  }
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(&sm.full[stage]))
-               : "memory");
+__device__ inline void gather_pool_tile(const CUtensorMap* map, ScanSmem& sm, int64_t row, int stage, int lane) {
+  const uint32_t nblk = __popc(__ballot_sync(0xFFFFFFFFu, row >= 0));
+  if (lane == 0) tc::mbar_expect_tx(&sm.full[stage], nblk * uint32_t(kBlock * 128));
+  __syncwarp();
+  if (row >= 0) tc::tma_load_2d(map, sm.stage[stage] + lane * (kBlock * 128), 0, int32_t(row), &sm.full[stage]);
 }
 
 __device__ inline void group_sync(int id) {
@@ -233,24 +212,33 @@ __device__ void query_split(const IdxArgs& a, ScanSmem& sm, int b, int gt, int g
   const int hi = a.d.idx_heads;
   const bool operands = grp == 0;
   const int eg = grp - 1;                                  // epilogue group
+  const int h = gt >> 3, c0 = (gt & 7) * 16;
+  // the query row piece and the weights are loaded before anything waits
+  uint32_t wds[8] = {0, 0, 0, 0, 0, 0, 0, 0};          // bf16 pairs (the query is 4-byte aligned)
+  if (h < hi) {
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint16_t*>(a.idx_q) +
+                                                             (int64_t(b) * hi + h) * 128 + c0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wds[i] = __ldg(qrow + i);
+  }
+  const float w_h = (!operands && h < hi) ? __ldg(a.w + int64_t(b) * hi + h) : 0.0f;
+  const float w_g = (!operands && gt < hi) ? __ldg(a.w + int64_t(b) * hi + gt) : 0.0f;
   if (gt < kMaxIdxHeads) {
     sm.qmax[grp][gt] = 0.0f;
     if (!operands) sm.qerr[eg][gt] = 0.0f;
   }
   group_sync(bar_id);
-  const int h = gt >> 3, c0 = (gt & 7) * 16;
   float qv[16];
   float mx = 0.0f;
-  const uint16_t* qrow = reinterpret_cast<const uint16_t*>(a.idx_q) + (int64_t(b) * hi + h) * 128 + c0;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    qv[i] = h < hi ? bf16_to_f32(qrow[i]) : 0.0f;
+    qv[i] = bf16_to_f32(uint16_t(wds[i >> 1] >> (16 * (i & 1))));
     mx = fmaxf(mx, fabsf(qv[i]));
   }
   atomicMax(reinterpret_cast<int*>(&sm.qmax[grp][h]), __float_as_int(mx));
   group_sync(bar_id);
   const int e = head_shift(sm.qmax[grp][h]);
-  const float wabs = fabsf(ldexpf(h < hi ? a.w[int64_t(b) * hi + h] : 0.0f, -e));
+  const float wabs = fabsf(ldexpf(w_h, -e));
   uint32_t w1[4] = {0, 0, 0, 0}, w2[4] = {0, 0, 0, 0};
   float err = 0.0f;
 #pragma unroll
@@ -274,10 +262,7 @@ __device__ void query_split(const IdxArgs& a, ScanSmem& sm, int b, int gt, int g
     return;
   }
   if (err > 0.0f) atomicAdd(&sm.qerr[eg][h], err);
-  if (gt < kMaxIdxHeads) {
-    const float w = gt < hi ? a.w[int64_t(b) * hi + gt] : 0.0f;
-    sm.wq[eg][gt] = ldexpf(w, -head_shift(sm.qmax[grp][gt]));
-  }
+  if (gt < kMaxIdxHeads) sm.wq[eg][gt] = ldexpf(w_g, -head_shift(sm.qmax[grp][gt]));
   group_sync(bar_id);
   // ||u||^2: channel gt's u_c, squared and summed over the group, rounded up
   float uc = 0.0f;
@@ -411,11 +396,21 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   pdl_launch_dependents();
   // ---- tiles of all sequences, this CTA's contiguous share ----------------------
   if (wid == 0) {
+    // every sequence's items are read once (the first kSeqCache are kept for
+    // the tile walks of all roles)
+    const int ncache = min(a.batch, kSeqCache);
     int64_t tsum = 0;
-    for (int b = lane; b < a.batch; b += 32) tsum += (scan_items(a, b, reindex) + kTile - 1) / kTile;
+    for (int b = lane; b < a.batch; b += 32) {
+      const int64_t n = scan_items(a, b, reindex);
+      if (b < ncache) sm.seq_items[b] = n;
+      tsum += (n + kTile - 1) / kTile;
+    }
 #pragma unroll
     for (int o = 16; o; o >>= 1) tsum += __shfl_xor_sync(0xFFFFFFFFu, tsum, o);
-    if (lane == 0) total_tiles_s = tsum;
+    if (lane == 0) {
+      total_tiles_s = tsum;
+      sm.n_seq_cached = ncache;
+    }
   }
   __syncthreads();
   const int64_t T = total_tiles_s;
@@ -426,7 +421,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   if (wid == 0) tc::tmem_alloc(&sm.tmem_slot, kScanTmemCols);
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&sm.full[s], reindex ? 32 : 1);     // 32 cp.async lanes or one TMA arrive
+      tc::mbar_init(&sm.full[s], 1);                    // the producer's arrival (with its TMA bytes)
       tc::mbar_init(&sm.empty[s], 1);
       tc::mbar_init(&sm.hdr[s], 4);
     }
@@ -444,33 +439,76 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   const int ntiles = int(g1 - g0);
 
   if (wid == 0 && reindex) {
-    // ================= producer: cp.async gather of pool blocks =================
+    // ================= producer: TMA gather of pool blocks =================
     int hb = 0;
     int64_t hbase = 0;
     bool stop = false;
+    const bool paged = a.page_table != nullptr;
     Ring ring;
+    int k = 0;
     for (int k0 = 0; k0 < ntiles && !stop; k0 += kStages) {
       const int nwin = min(kStages, ntiles - k0);
-      for (int idx = lane; idx < nwin * 16; idx += 32) {  // tiles visited in order per lane
-        const TileRef tr = tile_of(a, reindex, g0 + k0 + idx / 16, hb, hbase);
-        int64_t row;
-        int nrow;
-        resolve_block(a, tr, idx % 16, row, nrow);
-        sm.win_row[idx] = row;
-        sm.win_n[idx] = nrow;
+      // block idx = lane + 32 j of the window: tile idx / 16, block idx % 16
+      int32_t blk[kResolvePer], pg[kResolvePer];
+      int32_t nraw[kResolvePer], bq[kResolvePer];
+#pragma unroll
+      for (int j = 0; j < kResolvePer; ++j) {
+        const int idx = lane + 32 * j;
+        blk[j] = -1;
+        nraw[j] = 0;
+        bq[j] = 0;
+        if (idx < nwin * 16) {
+          const TileRef tr = tile_of(a, sm, reindex, g0 + k0 + idx / 16, hb, hbase);
+          if ((idx % 16) * kBlock < tr.nvalid) {
+            bq[j] = tr.b;
+            blk[j] = __ldg(a.pool_in + int64_t(tr.b) * a.d.pool_blocks + (tr.t0 >> 3) + idx % 16);
+            nraw[j] = __ldg(a.ctx_len + tr.b);
+          }
+        }
       }
-      __syncwarp();
-      for (int w = 0; w < nwin; ++w, ring.next()) {
-        const int k = k0 + w;
-        if (k >= kStages && !wait_or_abort(sm, &sm.empty[ring.stage], ring.phase ^ 1u)) {
+#pragma unroll
+      for (int j = 0; j < kResolvePer; ++j) {
+        pg[j] = -1;
+        if (blk[j] >= 0) {
+          const int64_t n = check_ctx(nraw[j], a.d, paged, a.ws);
+          if (int64_t(blk[j]) * kBlock >= n) blk[j] = -1;
+          else if (paged) pg[j] = __ldg(a.page_table + int64_t(bq[j]) * a.d.max_pages + ((int64_t(blk[j]) * kBlock) >> 6));
+        }
+      }
+      int64_t row[kResolvePer];
+#pragma unroll
+      for (int j = 0; j < kResolvePer; ++j) {
+        row[j] = -1;
+        if (blk[j] >= 0) {
+          const int64_t t = int64_t(blk[j]) * kBlock;
+          if (!paged) {
+            row[j] = int64_t(bq[j]) * a.d.max_ctx + t;
+          } else if (pg[j] < 0 || pg[j] >= a.d.num_pages) {
+            raise_err(a.ws, CSA2_DEV_PAGE_ID);
+          } else {
+            row[j] = int64_t(pg[j]) * kPage + (t & (kPage - 1));
+          }
+        }
+      }
+      for (int w = 0; w < nwin; ++w, ++k, ring.next()) {
+        // the lanes agree on the outcome (they issue the tile together)
+        const bool free_ = k < kStages || wait_or_abort(sm, &sm.empty[ring.stage], ring.phase ^ 1u);
+        if (!__all_sync(0xFFFFFFFFu, free_)) {
           stop = true;
           break;
         }
-        gather_pool_tile(a, sm, w, ring.stage, lane);
+        // tile w's 16 blocks are held by lanes 16 (w % 2) .. + 15 in register j = w / 2
+        int64_t my = -1;
+#pragma unroll
+        for (int j = 0; j < kResolvePer; ++j) my = (j == (w >> 1)) ? row[j] : my;
+        const int64_t rb = __shfl_sync(0xFFFFFFFFu, my, (lane & 15) + 16 * (w & 1));
+        gather_pool_tile(&kmap, sm, lane < 16 ? rb : -1, ring.stage, lane);
       }
-      __syncwarp();
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");     // nothing in flight when the CTA exits
+    // after an abort, let the copies still in flight land before the CTA exits
+    if (sm.abort_flag && lane == 0)
+      for (int j = max(0, k - kStages); j < k; ++j)
+        tc::mbar_wait_bounded(&sm.full[j % kStages], uint32_t((j / kStages) & 1), 20ull * 1000 * 1000);
   } else if (wid == 0) {
     // ================= producer: TMA ring =================
     if (lane == 0) {
@@ -480,7 +518,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       Ring ring;
       for (; k < ntiles; ++k, ring.next()) {
         if (k >= kStages && !wait_or_abort(sm, &sm.empty[ring.stage], ring.phase ^ 1u)) break;
-        issue_tile_load(a, &kmap, sm, tile_of(a, reindex, g0 + k, pb, pbase), ring.stage);
+        issue_tile_load(a, &kmap, sm, tile_of(a, sm, reindex, g0 + k, pb, pbase), ring.stage);
       }
       // after an abort, let the copies still in flight land before the CTA exits
       if (sm.abort_flag)
@@ -503,7 +541,6 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         if (!wait_or_abort(sm, &sm.hdr[stage], ring.phase)) break;    // query pieces
         if (k >= kDBufs && !wait_or_abort(sm, &sm.d_empty[buf], uint32_t((k / kDBufs - 1) & 1))) break;
         tc::tc_fence_after_sync();
-        if (reindex) tc::fence_proxy_async_smem();       // the gathered keys are generic-proxy writes
         const uint64_t ds = d0 + uint64_t(stage) * (kStageStride >> 4);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)                   // K = 32 E4M3 (32 bytes) per step
@@ -524,7 +561,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     int64_t cbase = 0;
     Ring ring;
     for (int k = 0; k < ntiles; ++k, ring.next()) {
-      const TileRef tr = tile_of(a, reindex, g0 + k, cb, cbase);
+      const TileRef tr = tile_of(a, sm, reindex, g0 + k, cb, cbase);
       const int stage = ring.stage;
       if (tr.b != cur_b) {
         query_split(a, sm, tr.b, gt, 0, 1);
@@ -550,7 +587,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     int cb = 0, cur_b = -1;
     int64_t cbase = 0;
     for (int k = eg; k < ntiles; k += 2) {
-      const TileRef tr = tile_of(a, reindex, g0 + k, cb, cbase);
+      const TileRef tr = tile_of(a, sm, reindex, g0 + k, cb, cbase);
       if (tr.b != cur_b) {
         query_split(a, sm, tr.b, gt, 1 + eg, 2 + eg);
         cur_b = tr.b;
@@ -596,7 +633,8 @@ cudaError_t launch_scan_tc(const IdxArgs& a, bool reindex, cudaStream_t st) {
   CUtensorMap map;
   cuuint64_t gdim[2] = {128, rows};
   cuuint64_t gstride[1] = {128};
-  cuuint32_t box[2] = {128, paged ? 64u : 128u};   // a page (64 positions) or a whole tile
+  // Full: a page (64 positions) or a whole tile; Reindex: one pool block
+  cuuint32_t box[2] = {128, reindex ? uint32_t(kBlock) : (paged ? 64u : 128u)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.idx_k), gdim, gstride, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
