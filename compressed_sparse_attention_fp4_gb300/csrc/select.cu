@@ -602,6 +602,13 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
       }
     }
     __syncthreads();
+    // A selection held by one CTA with a band of at most kSelThreads items
+    // keeps the band's exact-score keys in shared memory (in the histogram
+    // space, free after the radix step) and marks its picks directly; the
+    // workspace lists serve the cluster case and larger bands.
+    const bool local_pick = c.cs == 1 && nband <= uint32_t(kSelThreads);
+    uint64_t* band_key = reinterpret_cast<uint64_t*>(&sm.hist[0][0]);
+    static_assert(sizeof(sm.hist) >= kSelThreads * sizeof(uint64_t), "band keys fit the histograms");
     // exact scores of the band, a chunk of items at a time.  For a block,
     // only the positions whose upper bound reaches the block's best lower
     // bound can hold its exact maximum; the others are not re-scored.
@@ -650,6 +657,10 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
       for (int j = tid; j < nit; j += blockDim.x) {
         int64_t gi = base + blist[j0 + j];
         uint64_t kk = ex.item_best[j];
+        if (local_pick) {
+          band_key[j0 + j] = kk ? kk : f64_key(-INFINITY);   // the key of the decoded score
+          continue;
+        }
         uint64_t u = (kk >> 63) ? (kk & ~(uint64_t(1) << 63)) : ~kk;   // inverse of f64_key
         g_exact[gi] = kk ? __longlong_as_double((long long)u) : -INFINITY;
         g_pick[gi] = 0;
@@ -664,21 +675,29 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
       tot_band += cb;
       if (r < c.rank) band_off += cb;
     }
-    for (uint32_t j = tid; j < nband; j += blockDim.x) g_list[band_off + j] = int32_t(base + blist[j]);
+    if (!local_pick)
+      for (uint32_t j = tid; j < nband; j += blockDim.x) g_list[band_off + j] = int32_t(base + blist[j]);
     cl_sync(c);
     // ---- rank 0 picks the best (k - tot_in) band items by exact score -----
     int64_t need = k - int64_t(tot_in);
     if (c.rank == 0 && need > 0) {
       if (need >= int64_t(tot_band)) {
-        for (uint32_t i = tid; i < tot_band; i += blockDim.x) g_pick[g_list[i]] = 1;
+        for (uint32_t i = tid; i < tot_band; i += blockDim.x) {
+          if (local_pick) atomicOr(&sm.sel_bits[blist[i] >> 5], 1u << (blist[i] & 31));
+          else g_pick[g_list[i]] = 1;
+        }
       } else if (tot_band <= kSelThreads) {
         // small band: each item's rank = the number of band items ahead of it
         uint64_t* skey = reinterpret_cast<uint64_t*>(sm.keyU);
         int32_t* sidx = reinterpret_cast<int32_t*>(sm.keyL);
         for (uint32_t i = tid; i < tot_band; i += blockDim.x) {
-          int32_t it = g_list[i];
-          skey[i] = f64_key(g_exact[it]);
-          sidx[i] = it;
+          if (local_pick) {                    // sidx is the band list itself (base 0)
+            skey[i] = band_key[i];
+          } else {
+            int32_t it = g_list[i];
+            skey[i] = f64_key(g_exact[it]);
+            sidx[i] = it;
+          }
         }
         __syncthreads();
         if (tid < tot_band) {
@@ -689,7 +708,10 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
             const uint64_t kj = skey[j];
             rank += (kj > mk || (kj == mk && sidx[j] < mi)) ? 1u : 0u;
           }
-          if (rank < uint32_t(need)) g_pick[mi] = 1;
+          if (rank < uint32_t(need)) {
+            if (local_pick) atomicOr(&sm.sel_bits[mi >> 5], 1u << (mi & 31));
+            else g_pick[mi] = 1;
+          }
         }
       } else if (tot_band <= kSortCap) {
         uint64_t* skey = reinterpret_cast<uint64_t*>(sm.keyU);
@@ -757,14 +779,15 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
       }
     }
     cl_sync(c);
-    for (int wv = tid; wv < nwords; wv += blockDim.x) {
-      uint32_t bits = sm.band_bits[wv];
-      while (bits) {
-        int bp = __ffs(bits) - 1;
-        bits &= bits - 1;
-        if (g_pick[base + wv * 32 + bp]) atomicOr(&sm.sel_bits[wv], 1u << bp);
+    if (!local_pick)
+      for (int wv = tid; wv < nwords; wv += blockDim.x) {
+        uint32_t bits = sm.band_bits[wv];
+        while (bits) {
+          int bp = __ffs(bits) - 1;
+          bits &= bits - 1;
+          if (g_pick[base + wv * 32 + bp]) atomicOr(&sm.sel_bits[wv], 1u << bp);
+        }
       }
-    }
   }
   // ---- ordered output ------------------------------------------------------
   uint32_t nsel = scan_words(sm, sm.sel_bits, nwords);
