@@ -41,6 +41,8 @@ constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSortCap = 4096;
 constexpr int kBins = 2048;                 // 11-bit radix digits
 constexpr int kExItems = 128;               // band items re-scored per chunk (<= 8 positions each)
+constexpr int kQiStride = 132;              // words per head row of the integer query (16-byte
+                                            // loads of 16 heads spread over all banks)
 
 struct SelSmem {
   uint32_t keyU[kSelCapPerCta];             // reused: sort keys (rank 0)
@@ -51,7 +53,7 @@ struct SelSmem {
   uint32_t hist[2][kBins];                  // this CTA's histograms (U, L)
   uint32_t ghist[2][kBins];                 // cluster-wide sums
   Factor qf[kMaxIdxHeads * 128];            // query factors, [channel][head]
-  int32_t qi[128 * kMaxIdxHeads];           // query as integers, [channel][head]
+  __align__(16) int32_t qi[kMaxIdxHeads * kQiStride];   // query as integers, [head][channel]
   int32_t q_elo[kMaxIdxHeads];              // q = qi * 2^q_elo (exact)
   int32_t q_fast[kMaxIdxHeads];             // 1: the int32 x int32 -> int64 path is exact
   unsigned long long q_l1[kMaxIdxHeads];    // sum_c |qi|
@@ -70,7 +72,7 @@ struct SelSmem {
 // Scratch of the exact re-scoring, overlaid on keyU (free between the
 // classification and the final pick).
 constexpr int kExRows = 48;                // positions per round of the exact re-scoring
-constexpr int kExRowWords = 129;          // 128 words + 1 word of bank skew
+constexpr int kExRowWords = 132;          // 128 words + 4: 16-byte aligned rows
 constexpr int kExSumThreads = 64;         // threads that form the ordered head sums
 constexpr int kStageWords = 2;            // row words a staging thread loads per batch
 
@@ -80,7 +82,7 @@ struct ExScratch {
   int64_t cand_pos[kSelThreads];            // candidate positions of a chunk
   unsigned long long item_best[128];
   int32_t cand_item[kSelThreads];
-  int32_t krows[kExRows * kExRowWords];     // staged keys: E4M3 as k*2^9 integers, or fp32 bits
+  __align__(16) int32_t krows[kExRows * kExRowWords];   // staged keys: E4M3 as k*2^9 integers, or fp32 bits
 };
 static_assert(sizeof(ExScratch) <= sizeof(uint32_t) * kSelCapPerCta, "exact scratch must fit keyU");
 
@@ -422,11 +424,13 @@ __device__ void exact_scores(const IdxArgs& a, SelSmem& sm, const SelCtx& c, con
           if (i >= nr * wpr) break;
           int32_t* dst = ex.krows + (i / wpr) * kExRowWords;
           if (fp8) {
+            int32_t kq[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const Factor f = factor_e4m3((sw[j] >> (8 * q)) & 0xFFu);
-              dst[4 * (i % wpr) + q] = f.sig * (1 << (f.exp + 9));
+              kq[q] = f.sig * (1 << (f.exp + 9));
             }
+            reinterpret_cast<int4*>(dst)[i % wpr] = make_int4(kq[0], kq[1], kq[2], kq[3]);
           } else {
             dst[i % wpr] = int32_t(sw[j]);
           }
@@ -440,9 +444,18 @@ __device__ void exact_scores(const IdxArgs& a, SelSmem& sm, const SelCtx& c, con
         double d;
         if (fp8 && sm.q_fast[h]) {
           // |sum| <= sum|qi| * 448*2^9 < 2^62: the int64 sum is exact
+          // 16-byte loads of 4 channels of the query row and of the key row
+          const int4* q4 = reinterpret_cast<const int4*>(sm.qi + h * kQiStride);
+          const int4* k4 = reinterpret_cast<const int4*>(kr);
           long long acc = 0;
 #pragma unroll 8
-          for (int ch = 0; ch < 128; ++ch) acc += (long long)sm.qi[ch * kMaxIdxHeads + h] * (long long)kr[ch];
+          for (int c4 = 0; c4 < 32; ++c4) {
+            const int4 qv = q4[c4], kv = k4[c4];
+            acc += (long long)qv.x * kv.x;
+            acc += (long long)qv.y * kv.y;
+            acc += (long long)qv.z * kv.z;
+            acc += (long long)qv.w * kv.w;
+          }
           d = int_to_f64_rn(acc, sm.q_elo[h] - 9);
         } else {
           auto kf = [&](int ch) {
@@ -882,7 +895,7 @@ __device__ void load_query_factors(const IdxArgs& a, SelSmem& sm, int b) {
         mag64 = (unsigned long long)mag;
       }
     }
-    sm.qi[ch * kMaxIdxHeads + h] = qv;
+    sm.qi[h * kQiStride + ch] = qv;
     // mag < 2^30: the warp sums of its 16-bit halves fit 32 bits
     const uint32_t s_lo = __reduce_add_sync(0xFFFFFFFFu, uint32_t(mag64 & 0xFFFF));
     const uint32_t s_hi = __reduce_add_sync(0xFFFFFFFFu, uint32_t(mag64 >> 16));
