@@ -16,7 +16,7 @@
 // Work: one persistent CTA per SM walks a contiguous range of 128-position
 // tiles; its warps specialise and hand tiles on through mbarriers, so the
 // key stream, the MMAs and the epilogue of consecutive tiles overlap.  Each
-// stage of the 6-stage shared-memory ring holds a tile's keys (128 rows x
+// stage of the 10-stage shared-memory ring holds a tile's keys (128 rows x
 // 128 B, 128-byte swizzled K-major) followed by the query pieces (32 rows:
 // q1 of the 16 heads, then r1), so that one MMA per K-step with A = the keys
 // and B = the whole stage (N = 160) yields, per position t,
@@ -24,8 +24,8 @@
 //   columns 128..159: k_t . q1_h and k_t . r1_h.
 //   * warp 0: one thread streams the keys of each tile by TMA (tensor map
 //     with the same swizzle); for Reindex tiles (16 scattered pool blocks)
-//     the whole warp gathers them with cp.async instead, resolving the rows
-//     of a window of 6 tiles at a time.
+//     the warp resolves the rows of a window of up to 10 tiles at a time and
+//     16 lanes load a tile's blocks with one 8-row TMA box each.
 //   * warps 2-5 (the query group) split the query when a new sequence starts
 //     and copy the pieces into each stage behind its keys.
 //   * warp 1 (one thread) issues the 4 MMAs of a tile (kind::f8f6f4, M=128,
