@@ -31,11 +31,12 @@
 // split the 576 channels (latent 0..255 | latent 256..511 + rope), exchange
 // their S^T partials through shared memory and each computes O^T for its 256
 // value dimensions.  The 2 x chunks CTAs of a sequence form one thread-block
-// cluster: every chunk writes its per-head (m_s, l_s) into every CTA's shared
-// memory; after a cluster barrier each forms M and L, scales its O^T part and
-// adds it into the output with coalesced vector reduce-adds
-// (red.global.add.v4.f32; the SWA chunk, which finishes first, zeroes the
-// output before the barrier).  The order of the additions is not fixed, so
+// cluster: every chunk copies its per-head (m_s, l_s) into every CTA's shared
+// memory, on an mbarrier that counts the bytes; the chunk that finishes first
+// (the TMA-loaded SWA window) zeroes the output early and signals the other
+// chunks of its half; each CTA then forms M and L, scales its O^T part and
+// adds it into the output with coalesced reduce-adds (red.global.add.f32)
+// straight from tensor memory.  The order of the additions is not fixed, so
 // the last bits of the output may differ between runs.
 //
 // attn_partial_tc_kernel + attn_combine_kernel (more chunks): one CTA per
@@ -400,7 +401,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // takes latent channels 0..255, half 1 latent channels 256..511 and the rope
 // (64).  Each gathers, dequantizes and multiplies only its channels
 // (S^T partial, M=128, N=64, K=256 or 320), the pair exchanges the partial
-// S^T through shared memory (one mbarrier arrival across the pair), both
+// S^T through shared memory (one bulk copy into the partner, completing on
+// its mbarrier), both
 // form the same softmax, and each computes O^T for its own 256 latent
 // dimensions (the value channels it holds).  The 2 x chunks CTAs of a
 // sequence form one cluster (up to 16) that merges the chunks as above.
