@@ -432,10 +432,12 @@ def main():
     def e2e_rate(graphed):
         run_pipelined(args.warmup, graphed)
         torch.cuda.synchronize()
+        barrier()
         t0 = time.perf_counter()
         run_pipelined(args.steps, graphed)
         torch.cuda.synchronize()
-        return world * wl.batch * args.steps / (time.perf_counter() - t0)
+        elapsed = max_over_ranks(time.perf_counter() - t0, world, dev)   # the slowest rank
+        return world * wl.batch * args.steps / elapsed
 
     e2e_qps = e2e_rate(True)
     e2e_eager_qps = e2e_rate(False)
