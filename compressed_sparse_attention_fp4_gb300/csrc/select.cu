@@ -38,6 +38,7 @@ enum ItemKind { kBlocks = 0, kPoolPos = 1, kReindexPos = 2 };
 
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
+static_assert(kMaxPool % kSelThreads == 0, "pool ids per selection thread");
 constexpr int kSortCap = 4096;
 constexpr int kBins = 2048;                 // 11-bit radix digits
 constexpr int kExItems = 128;               // band items re-scored per chunk (<= 8 positions each)
@@ -926,8 +927,23 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
   c.b = b;
   c.cs = cs;
   c.rank = cs > 1 ? int(cg::this_cluster().block_rank()) : 0;
-  c.n_ctx = checked_ctx(a.ctx_len, a.d, b, a.page_table != nullptr, a.ws);
+  // the length (and, for Reindex, the pool) loads go out with the query's
+  // loads; their checks come after the query factors
+  const int32_t n_raw = __ldg(a.ctx_len + b);
+  constexpr int kPoolPer = kMaxPool / kSelThreads;
+  int32_t plen_raw = 0, pin_raw[kPoolPer];
+#pragma unroll
+  for (int j = 0; j < kPoolPer; ++j) pin_raw[j] = -1;
+  if (reindex) {
+    plen_raw = __ldg(a.pool_len_in + b);
+#pragma unroll
+    for (int j = 0; j < kPoolPer; ++j) {
+      const int i = threadIdx.x + j * kSelThreads;
+      if (i < a.d.pool_blocks) pin_raw[j] = __ldg(a.pool_in + int64_t(b) * a.d.pool_blocks + i);
+    }
+  }
   load_query_factors(a, sm, b);
+  c.n_ctx = check_ctx(n_raw, a.d, a.page_table != nullptr, a.ws);
   const int64_t scap = a.L.sel_cap;
   double* g_exact = reinterpret_cast<double*>(a.ws + a.L.sel_exact) + int64_t(b) * scap;
   int32_t* g_list = reinterpret_cast<int32_t*>(a.ws + a.L.sel_list) + int64_t(b) * scap;
@@ -960,10 +976,12 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
     for (int i = threadIdx.x; i < K; i += blockDim.x)
       if (i >= k_sel) tk[i] = -1;
   } else {
-    int32_t plen = a.pool_len_in[b];
+    int32_t plen = plen_raw;
     if (plen < 0 || plen > P) { if (threadIdx.x == 0) raise_err(a.ws, CSA2_DEV_POOL); plen = 0; }
-    for (int i = threadIdx.x; i < kMaxPool; i += blockDim.x) {
-      int32_t blk = i < plen ? a.pool_in[int64_t(b) * P + i] : -1;
+#pragma unroll
+    for (int j = 0; j < kPoolPer; ++j) {
+      const int i = threadIdx.x + j * kSelThreads;
+      int32_t blk = i < plen ? pin_raw[j] : -1;
       if (blk >= nb) { raise_err(a.ws, CSA2_DEV_POOL); blk = -1; }
       sm.pool_ids[i] = blk;
     }
