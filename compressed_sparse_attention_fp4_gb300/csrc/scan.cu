@@ -155,13 +155,17 @@ __device__ inline TileRef tile_of(const IdxArgs& a, const ScanSmem& sm, bool rei
   }
 }
 
+// The keys are read once: they go through L2 as evict-first lines, so that
+// the 128 MB stream does not push out the scores this kernel writes (which
+// the selection reads next).
 __device__ inline void issue_tile_load(const IdxArgs& a, const CUtensorMap* map, ScanSmem& sm,
-                                       const TileRef& tr, int stage) {
+                                       const TileRef& tr, int stage, uint64_t policy) {
   if (a.page_table == nullptr) {
     // contiguous cache: the tile is one run of 128 rows (rows past the
     // sequence are the next one's or, past the tensor, zero-filled)
     tc::mbar_expect_tx(&sm.full[stage], kKeyBytes);
-    tc::tma_load_2d(map, sm.stage[stage], 0, int32_t(int64_t(tr.b) * a.d.max_ctx + tr.t0), &sm.full[stage]);
+    tc::tma_load_2d_hint(map, sm.stage[stage], 0, int32_t(int64_t(tr.b) * a.d.max_ctx + tr.t0), &sm.full[stage],
+                         policy);
     return;
   }
   uint32_t bytes = 0;
@@ -175,7 +179,7 @@ __device__ inline void issue_tile_load(const IdxArgs& a, const CUtensorMap* map,
   }
   tc::mbar_expect_tx(&sm.full[stage], bytes);
   for (int h = 0; h < nbox; ++h)
-    if (rows[h] >= 0) tc::tma_load_2d(map, sm.stage[stage] + h * 64 * 128, 0, rows[h], &sm.full[stage]);
+    if (rows[h] >= 0) tc::tma_load_2d_hint(map, sm.stage[stage] + h * 64 * 128, 0, rows[h], &sm.full[stage], policy);
 }
 
 // Reindex tiles: the pool blocks are scattered 1 KB runs (8 rows, never
@@ -186,11 +190,13 @@ __device__ inline void issue_tile_load(const IdxArgs& a, const CUtensorMap* map,
 // the 128-byte swizzle of an 8-row box is that of the whole tile.
 constexpr int kResolvePer = kStages * 16 / 32;   // blocks a producer lane resolves per window
 
-__device__ inline void gather_pool_tile(const CUtensorMap* map, ScanSmem& sm, int64_t row, int stage, int lane) {
+__device__ inline void gather_pool_tile(const CUtensorMap* map, ScanSmem& sm, int64_t row, int stage, int lane,
+                                        uint64_t policy) {
   const uint32_t nblk = __popc(__ballot_sync(0xFFFFFFFFu, row >= 0));
   if (lane == 0) tc::mbar_expect_tx(&sm.full[stage], nblk * uint32_t(kBlock * 128));
   __syncwarp();
-  if (row >= 0) tc::tma_load_2d(map, sm.stage[stage] + lane * (kBlock * 128), 0, int32_t(row), &sm.full[stage]);
+  if (row >= 0)
+    tc::tma_load_2d_hint(map, sm.stage[stage] + lane * (kBlock * 128), 0, int32_t(row), &sm.full[stage], policy);
 }
 
 __device__ inline void group_sync(int id) {
@@ -440,6 +446,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 
   if (wid == 0 && reindex) {
     // ================= producer: TMA gather of pool blocks =================
+    const uint64_t policy = tc::l2_policy_evict_first();
     int hb = 0;
     int64_t hbase = 0;
     bool stop = false;
@@ -502,7 +509,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 #pragma unroll
         for (int j = 0; j < kResolvePer; ++j) my = (j == (w >> 1)) ? row[j] : my;
         const int64_t rb = __shfl_sync(0xFFFFFFFFu, my, (lane & 15) + 16 * (w & 1));
-        gather_pool_tile(&kmap, sm, lane < 16 ? rb : -1, ring.stage, lane);
+        gather_pool_tile(&kmap, sm, lane < 16 ? rb : -1, ring.stage, lane, policy);
       }
     }
     // after an abort, let the copies still in flight land before the CTA exits
@@ -512,13 +519,14 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   } else if (wid == 0) {
     // ================= producer: TMA ring =================
     if (lane == 0) {
+      const uint64_t policy = tc::l2_policy_evict_first();
       int pb = 0;
       int64_t pbase = 0;
       int k = 0;
       Ring ring;
       for (; k < ntiles; ++k, ring.next()) {
         if (k >= kStages && !wait_or_abort(sm, &sm.empty[ring.stage], ring.phase ^ 1u)) break;
-        issue_tile_load(a, &kmap, sm, tile_of(a, sm, reindex, g0 + k, pb, pbase), ring.stage);
+        issue_tile_load(a, &kmap, sm, tile_of(a, sm, reindex, g0 + k, pb, pbase), ring.stage, policy);
       }
       // after an abort, let the copies still in flight land before the CTA exits
       if (sm.abort_flag)

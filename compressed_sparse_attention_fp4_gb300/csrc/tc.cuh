@@ -81,6 +81,23 @@ __device__ inline void tma_load_2d(const void* map, void* dst, int32_t x, int32_
       : "memory");
 }
 
+// L2 policy for data read once: its lines are the first evicted.
+__device__ inline uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_2d with an L2 cache policy (e.g. l2_policy_evict_first()).
+__device__ inline void tma_load_2d_hint(const void* map, void* dst, int32_t x, int32_t y, uint64_t* bar,
+                                        uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // ---- proxies ------------------------------------------------------------------
 // Generic-proxy shared-memory writes become visible to the tensor cores.
 __device__ inline void fence_proxy_async_smem() {
