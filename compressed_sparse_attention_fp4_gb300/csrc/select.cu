@@ -714,15 +714,17 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
           }
         }
         __syncthreads();
-        if (tid < tot_band) {
-          const uint64_t mk = skey[tid];
-          const int32_t mi = sidx[tid];
+        // one warp per item: the lanes count the band items ahead of it
+        for (uint32_t i = wid; i < tot_band; i += kSelWarps) {
+          const uint64_t mk = skey[i];
+          const int32_t mi = sidx[i];
           uint32_t rank = 0;
-          for (uint32_t j = 0; j < tot_band; ++j) {
+          for (uint32_t j = lane; j < tot_band; j += 32) {
             const uint64_t kj = skey[j];
             rank += (kj > mk || (kj == mk && sidx[j] < mi)) ? 1u : 0u;
           }
-          if (rank < uint32_t(need)) {
+          rank = __reduce_add_sync(0xFFFFFFFFu, rank);
+          if (lane == 0 && rank < uint32_t(need)) {
             if (local_pick) atomicOr(&sm.sel_bits[mi >> 5], 1u << (mi & 31));
             else g_pick[mi] = 1;
           }
