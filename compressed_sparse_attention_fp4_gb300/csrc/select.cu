@@ -67,6 +67,7 @@ struct SelSmem {
   uint32_t kmax_all;
   int shift0;
   uint32_t cnt_in, cnt_band, cnt_sel;
+  uint32_t tot3[3];                         // cluster sums read once by warp 0
   uint32_t n_cand;
 };
 
@@ -215,31 +216,47 @@ __device__ void radix_edges(SelSmem& sm, const SelCtx& c, int n_local, uint32_t 
   }
   if (lane == 0) { sm.red[0][wid] = kmin_l; sm.red[1][wid] = kmax_l; sm.dred[wid] = dmax_l; }
   __syncthreads();
-  if (tid == 0) {
-    uint32_t a0 = 0xFFFFFFFFu, a1 = 0;
-    float dm = 0.0f;
-    for (int i = 0; i < kSelWarps; ++i) { a0 = min(a0, sm.red[0][i]); a1 = max(a1, sm.red[1][i]); dm = fmaxf(dm, sm.dred[i]); }
-    sm.kmin = a0;
-    sm.kmax = a1;
-    sm.dmax = dm;
+  static_assert(kSelWarps == 32, "one lane per warp partial");
+  if (wid == 0) {                      // the warps' partials, one per lane
+    uint32_t a0 = sm.red[0][lane], a1 = sm.red[1][lane];
+    float dm = sm.dred[lane];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      a0 = min(a0, __shfl_xor_sync(0xFFFFFFFFu, a0, o));
+      a1 = max(a1, __shfl_xor_sync(0xFFFFFFFFu, a1, o));
+      dm = fmaxf(dm, __shfl_xor_sync(0xFFFFFFFFu, dm, o));
+    }
+    if (lane == 0) {
+      sm.kmin = a0;
+      sm.kmax = a1;
+      sm.dmax = dm;
+    }
   }
   cl_sync(c);
-  if (tid == 0) {
+  if (wid == 0) {                      // the ranks' values, one rank per lane
     uint32_t a0 = 0xFFFFFFFFu, a1 = 0;
     float dm = 0.0f;
-    for (int r = 0; r < c.cs; ++r) {
-      a0 = min(a0, *remote(c, &sm.kmin, r));
-      a1 = max(a1, *remote(c, &sm.kmax, r));
-      dm = fmaxf(dm, *remote(c, &sm.dmax, r));
+    if (lane < c.cs) {
+      a0 = *remote(c, &sm.kmin, lane);
+      a1 = *remote(c, &sm.kmax, lane);
+      dm = *remote(c, &sm.dmax, lane);
     }
-    sm.rem[0] = k;
-    sm.rem[1] = k;
-    sm.base_key = a0;
-    sm.kmax_all = a1;
-    sm.dmax_all = dm;
-    uint32_t range = a1 - a0;
-    int bits = range ? 32 - __clz(range) : 0;
-    sm.shift0 = bits > 11 ? bits - 11 : 0;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      a0 = min(a0, __shfl_xor_sync(0xFFFFFFFFu, a0, o));
+      a1 = max(a1, __shfl_xor_sync(0xFFFFFFFFu, a1, o));
+      dm = fmaxf(dm, __shfl_xor_sync(0xFFFFFFFFu, dm, o));
+    }
+    if (lane == 0) {
+      sm.rem[0] = k;
+      sm.rem[1] = k;
+      sm.base_key = a0;
+      sm.kmax_all = a1;
+      sm.dmax_all = dm;
+      uint32_t range = a1 - a0;
+      int bits = range ? 32 - __clz(range) : 0;
+      sm.shift0 = bits > 11 ? bits - 11 : 0;
+    }
   }
   cl_sync(c);       // the range is read before any rank overwrites kmin / kmax
   const uint32_t kb = sm.base_key;
@@ -682,12 +699,24 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
       __syncthreads();
     }
     cl_sync(c);
-    uint32_t tot_in = 0, tot_band = 0, band_off = 0;
-    for (int r = 0; r < c.cs; ++r) {
-      uint32_t ci = *remote(c, &sm.cnt_in, r), cb = *remote(c, &sm.cnt_band, r);
-      tot_in += ci;
-      tot_band += cb;
-      if (r < c.rank) band_off += cb;
+    uint32_t tot_in = sm.cnt_in, tot_band = sm.cnt_band, band_off = 0;
+    if (c.cs > 1) {
+      // the ranks' counters, one rank per lane of warp 0 (not one remote read
+      // per rank by every thread)
+      if (wid == 0) {
+        uint32_t ci = 0, cb = 0;
+        if (lane < c.cs) {
+          ci = *remote(c, &sm.cnt_in, lane);
+          cb = *remote(c, &sm.cnt_band, lane);
+        }
+        const uint32_t ti = __reduce_add_sync(0xFFFFFFFFu, ci), tb = __reduce_add_sync(0xFFFFFFFFu, cb);
+        const uint32_t bo = __reduce_add_sync(0xFFFFFFFFu, lane < c.rank ? cb : 0u);
+        if (lane == 0) { sm.tot3[0] = ti; sm.tot3[1] = tb; sm.tot3[2] = bo; }
+      }
+      __syncthreads();
+      tot_in = sm.tot3[0];
+      tot_band = sm.tot3[1];
+      band_off = sm.tot3[2];
     }
     if (!local_pick)
       for (uint32_t j = tid; j < nband; j += blockDim.x) g_list[band_off + j] = int32_t(base + blist[j]);
@@ -810,7 +839,14 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
   if (tid == 0) sm.cnt_sel = nsel;
   cl_sync(c);
   uint32_t off = 0;
-  for (int r = 0; r < c.rank; ++r) off += *remote(c, &sm.cnt_sel, r);
+  if (c.cs > 1) {
+    if (wid == 0) {
+      const uint32_t v = __reduce_add_sync(0xFFFFFFFFu, lane < c.rank ? *remote(c, &sm.cnt_sel, lane) : 0u);
+      if (lane == 0) sm.tot3[0] = v;
+    }
+    __syncthreads();
+    off = sm.tot3[0];
+  }
   for (int wv = tid; wv < nwords; wv += blockDim.x) {
     uint32_t bits = sm.sel_bits[wv], o = sm.word_off[wv];
     while (bits) {
