@@ -604,23 +604,40 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
     }
   }
   __syncthreads();
+  // The 32 items of a word are one warp's in each pass over the items: the
+  // warp forms the word by ballot and lane 0 stores it (no shared atomics).
   if (k >= n_items) {
-    for (int i = tid; i < n_local; i += blockDim.x)
-      if (sm.keyU[i]) atomicOr(&sm.sel_bits[i >> 5], 1u << (i & 31));
+    for (int i0 = tid - lane; i0 < n_local; i0 += blockDim.x) {
+      const int i = i0 + lane;
+      const uint32_t m = __ballot_sync(0xFFFFFFFFu, i < n_local && sm.keyU[i] != 0);
+      if (lane == 0) sm.sel_bits[i0 >> 5] = m;
+    }
   } else {
     uint32_t muE, lamE;
     radix_edges(sm, c, n_local, uint32_t(k), kmin_l, kmax_l, dmax_l, muE, lamE);
-    uint32_t my_in = 0, my_band = 0;
-    for (int i = tid; i < n_local; i += blockDim.x) {
-      const uint32_t kv = sm.keyU[i];
-      if (kv == 0) continue;
-      const float v = key_f32(kv), dl = __uint_as_float(sm.keyL[i]);
-      const uint32_t u = f32_key(__fadd_ru(v, dl)), l = f32_key(__fadd_rd(v, -dl));
-      if (l > muE) { atomicOr(&sm.sel_bits[i >> 5], 1u << (i & 31)); ++my_in; }
-      else if (u >= lamE) { atomicOr(&sm.band_bits[i >> 5], 1u << (i & 31)); ++my_band; }
+    uint32_t my_in = 0, my_band = 0;                  // lane 0's warp totals
+    for (int i0 = tid - lane; i0 < n_local; i0 += blockDim.x) {
+      const int i = i0 + lane;
+      const uint32_t kv = i < n_local ? sm.keyU[i] : 0u;
+      bool in = false, band = false;
+      if (kv != 0) {
+        const float v = key_f32(kv), dl = __uint_as_float(sm.keyL[i]);
+        const uint32_t u = f32_key(__fadd_ru(v, dl)), l = f32_key(__fadd_rd(v, -dl));
+        in = l > muE;
+        band = !in && u >= lamE;
+      }
+      const uint32_t mi = __ballot_sync(0xFFFFFFFFu, in), mb = __ballot_sync(0xFFFFFFFFu, band);
+      if (lane == 0) {
+        sm.sel_bits[i0 >> 5] = mi;
+        sm.band_bits[i0 >> 5] = mb;
+        my_in += __popc(mi);
+        my_band += __popc(mb);
+      }
     }
-    atomicAdd(&sm.cnt_in, my_in);
-    atomicAdd(&sm.cnt_band, my_band);
+    if (lane == 0) {
+      atomicAdd(&sm.cnt_in, my_in);
+      atomicAdd(&sm.cnt_band, my_band);
+    }
     // ordered list of this CTA's band items (keyL area is free now)
     uint32_t nband = scan_words(sm, sm.band_bits, nwords);
     int32_t* blist = reinterpret_cast<int32_t*>(sm.keyL);
