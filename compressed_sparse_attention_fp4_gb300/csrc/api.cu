@@ -37,6 +37,12 @@ csa2_status check_paging(const csa2_dims* d, const int32_t* page_table) {
   return CSA2_OK;
 }
 
+// The indexer scan addresses cache rows with 32-bit tensor coordinates.
+csa2_status check_idx_rows(const csa2_dims* d, int32_t batch, const int32_t* page_table) {
+  const int64_t rows = page_table ? d->num_pages * int64_t(kPage) : int64_t(batch) * d->max_ctx;
+  return rows > int64_t(INT32_MAX) ? CSA2_ERR_UNSUPPORTED_SHAPE : CSA2_OK;
+}
+
 csa2_status check_ws(const csa2_dims* d, int32_t batch, const void* ws, size_t ws_bytes, WsLayout* L) {
   *L = make_layout(*d, batch);
   if (!ws || !aligned(ws, 256)) return CSA2_ERR_INVALID_ARG;
@@ -104,6 +110,7 @@ csa2_status indexer_full_topk(const csa2_dims* d, int32_t batch, const void* idx
   csa2_status st = check_dims(d, batch);
   if (st != CSA2_OK) return st;
   if ((st = check_paging(d, page_table)) != CSA2_OK) return st;
+  if ((st = check_idx_rows(d, batch, page_table)) != CSA2_OK) return st;
   WsLayout L;
   if ((st = check_ws(d, batch, ws, ws_bytes, &L)) != CSA2_OK) return st;
   if (batch == 0) return CSA2_OK;
@@ -134,6 +141,7 @@ csa2_status indexer_reindex_topk(const csa2_dims* d, int32_t batch, const void* 
   csa2_status st = check_dims(d, batch);
   if (st != CSA2_OK) return st;
   if ((st = check_paging(d, page_table)) != CSA2_OK) return st;
+  if ((st = check_idx_rows(d, batch, page_table)) != CSA2_OK) return st;
   WsLayout L;
   if ((st = check_ws(d, batch, ws, ws_bytes, &L)) != CSA2_OK) return st;
   if (batch == 0) return CSA2_OK;

@@ -163,6 +163,9 @@ csa2_status fp4_kv_dequantize(const uint8_t* codes, const uint8_t* scales,
  *   pool_blocks_out: device int32 [B][P], ascending, -1 padded
  *   pool_len_out:    device int32 [B]
  *   topk_out:        device int32 [B][K]
+ * The indexer-K cache may hold at most 2^31 - 1 rows (B * max_ctx
+ * contiguous, num_pages * 64 paged): its tiles are addressed by 32-bit row
+ * coordinates.  A larger cache is CSA2_ERR_UNSUPPORTED_SHAPE.
  * Errors: CSA2_ERR_INVALID_ARG, CSA2_ERR_UNSUPPORTED_SHAPE,
  *         CSA2_ERR_WORKSPACE_TOO_SMALL, CSA2_ERR_CUDA. */
 csa2_status indexer_full_topk(const csa2_dims* d, int32_t batch,

@@ -89,6 +89,18 @@ def test_host_argument_errors(mod):
     dp = mod.Dims(max_ctx=1024, pool_blocks=64, topk=128, max_pages=0, num_pages=0)
     assert lib.indexer_full_topk(ctypes.byref(dp.c()), 1, fake, fake, *([fake] * 6), fake,
                                  mod.workspace_size(dp, 1), None) == 1
+    # an indexer-K cache beyond 32-bit row coordinates (4096 x 2^20 rows; paged:
+    # 2^26 pages of 64) is an unsupported shape, reported before the workspace is read
+    dbig = mod.Dims(max_ctx=1 << 20)
+    assert lib.indexer_full_topk(ctypes.byref(dbig.c()), 4096, *args, fake, 1 << 40, None) == 2
+    assert lib.indexer_reindex_topk(ctypes.byref(dbig.c()), 4096, fake, None, *([fake] * 5), fake, fake,
+                                    1 << 40, None) == 2
+    dpb = mod.Dims(max_ctx=1 << 20, max_pages=1 << 14, num_pages=1 << 26)
+    assert lib.indexer_full_topk(ctypes.byref(dpb.c()), 1, fake, fake, *([fake] * 6), fake, 1 << 40,
+                                 None) == 2
+    # 2047 x 2^20 rows fit: the call gets past the row check and stops at the
+    # misaligned workspace (before anything is launched)
+    assert lib.indexer_full_topk(ctypes.byref(dbig.c()), 2047, *args, P(0x10010), 1 << 40, None) == 1
     assert lib.csa2_get_device_status(None, None, None) == 1
     assert lib.csa2_clear_device_status(None, None) == 1
 
