@@ -482,7 +482,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __shared__ float fac_s[kQRows];                   // 2^(m_chunk - M) / L per head
   __shared__ __align__(16) float ml_all[kMaxClusterSplits][2][kQRows];   // every chunk's (m, l), base-2 m
   __shared__ __align__(16) float ml_mine[2][kQRows];                      // this chunk's, copied to all
-  __shared__ bool x_ok, ml_ok, z_ok;
+  __shared__ bool ml_ok, z_ok;
 
   cg::cluster_group cl = cg::this_cluster();
   const int rank = int(cl.block_rank()), csize = int(cl.num_blocks());
@@ -662,31 +662,32 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   float x[16];
   tc::tmem_ld16(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(hg * 16), x);
   if (!zero_cta) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA has started
-  // row e holds 16 chunks of 4 heads; chunk c sits at c ^ (e % 16) so that
-  // the 32 rows of a warp spread over the banks.  The partial goes to this
-  // CTA's sx_out, then one bulk copy into the partner's sx.
+  // Each warp's part (its 32 rows x 16 heads) is one contiguous 2 KB block
+  // of sx_out (block wid; the 16-byte slot i of lane l at 4l + (i ^ s_l),
+  // s_l = (l >> 1) & 3, so that 8 consecutive lanes cover all banks), sent by
+  // the warp itself as one bulk copy into the same block of the partner's sx
+  // (the partner's warp wid holds the same rows and heads).
+  const int sw = (lane >> 1) & 3;
   {
-    float4* dst = reinterpret_cast<float4*>(sx_out + e * kQRows);
+    float4* blk = reinterpret_cast<float4*>(sx_out) + wid * 128;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      dst[(hg * 4 + i) ^ (e & 15)] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+      blk[lane * 4 + (i ^ sw)] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+    tc::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      const float4* peer_blk = reinterpret_cast<const float4*>(sx) + wid * 128;   // the partner's sx, same block
+      bulk_to_peer(cluster_addr(peer_blk, uint32_t(rank ^ 1)), blk, 2048u, cluster_addr(&bar_x, uint32_t(rank ^ 1)));
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
   }
-  tc::fence_proxy_async_smem();
-  __syncthreads();
-  if (tid == 0) {
-    bulk_to_peer(cluster_addr(sx, uint32_t(rank ^ 1)), sx_out, uint32_t(kSxBytes),
-                 cluster_addr(&bar_x, uint32_t(rank ^ 1)));
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  }
-  // one thread waits for the partner's bytes; the CTA barrier passes them on
-  if (tid == 0) x_ok = mbar_wait_cluster(&bar_x, 0);
-  __syncthreads();
-  ok = x_ok && ok;
+  // every thread waits for the partner's 16 blocks itself
+  ok = mbar_wait_cluster(&bar_x, 0) && ok;
   {
-    const float4* src = reinterpret_cast<const float4*>(sx + e * kQRows);
+    const float4* src = reinterpret_cast<const float4*>(sx) + wid * 128;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float4 v = src[(hg * 4 + i) ^ (e & 15)];
+      const float4 v = src[lane * 4 + (i ^ sw)];
       // own + partner: the same sum in both CTAs (fp32 addition commutes)
       x[4 * i] += v.x; x[4 * i + 1] += v.y; x[4 * i + 2] += v.z; x[4 * i + 3] += v.w;
     }
@@ -825,10 +826,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   }
   tc::tc_fence_before_sync();
   __syncthreads();
-  if (wid == 0) {
-    tc::tmem_dealloc(tmem, kPairTmemCols);
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");   // sx_out, ml_mine read out
-  }
+  if (wid == 0) tc::tmem_dealloc(tmem, kPairTmemCols);
+  // the bulk copies this thread committed (a warp's sx_out block, warp 0's
+  // ml_mine copies) have read their source before the CTA exits
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
