@@ -28,6 +28,8 @@ Modules:
 
 * ``codec``     -- E2M1 / E4M3 formats, FP4 KV quantize / dequantize.
 * ``indexer``   -- indexer scores, block scores, pool and Top-K selection.
+* ``indexer_fp4`` -- the indexer with FP4 query and key (a next row: pinned,
+  no kernel yet).
 * ``attention`` -- joint softmax over the selected main KV and the SWA window.
 * ``schedule``  -- Full / Reindex / Reuse layer schedules.
 

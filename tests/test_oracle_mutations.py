@@ -4,14 +4,16 @@ Each test plants one mistake in a copy of an oracle function (on the CPU) and
 checks that an independent pin from the other oracle tests rejects it: a
 wrong tie rule, a dropped sign, a wrong E4M3 bias, an off-by-one block, a
 transposed head/channel contraction, ties to the higher index, a missing
-SWA branch, a dropped attention scale.
+SWA branch, a dropped attention scale; for the FP4 indexer, an unquantized
+query and dropped scales.
 """
 import numpy as np
 import pytest
 
-from oracle import attention, codec, indexer
+from oracle import attention, codec, indexer, indexer_fp4
 from tests import test_oracle_codec as tc
 from tests import test_oracle_indexer as ti
+from tests import test_oracle_indexer_fp4 as tf
 
 
 def test_tie_rule_mutation_is_caught(monkeypatch):
@@ -90,3 +92,21 @@ def test_dropped_scale_is_caught(monkeypatch):
     monkeypatch.setattr(attention, "sparse_attn_decode", no_scale)
     with pytest.raises(AssertionError):
         ta.test_all_positions_equals_dense_sdpa()
+
+
+def test_fp4_indexer_unquantized_query_is_caught(monkeypatch):
+    def raw_query_full(q, w, k, pool_blocks, topk):
+        kc, ks = indexer_fp4.quantize(k)
+        return indexer.full_topk(q, w, indexer_fp4.dequantize(kc, ks), pool_blocks, topk)
+    monkeypatch.setattr(indexer_fp4, "full_topk", raw_query_full)
+    with pytest.raises(AssertionError):
+        tf.test_depends_only_on_quantized_inputs()
+
+
+def test_fp4_indexer_dropped_scales_are_caught(monkeypatch):
+    monkeypatch.setattr(indexer_fp4, "dequantize",
+                        lambda codes, scales: codec.dequantize_rows(codes, np.full_like(scales, 0x38)))  # 1.0
+    with pytest.raises(AssertionError):
+        tf.test_grid_values_round_trip_and_score_unchanged()
+    with pytest.raises(AssertionError):
+        tf.test_quantization_error_bound()
