@@ -52,6 +52,7 @@
 #include "kernels.cuh"
 #include "profile.cuh"
 #include "tc.cuh"
+#include "tmap.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -877,15 +878,9 @@ static PFN_cuTensorMapEncodeTiled_v12000 attn_encode_fn() {
 
 // [rows][576] bf16 rows of 1152 bytes, boxes of 64 channels x box_rows.
 static bool encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
-  auto fn = attn_encode_fn();
-  if (!fn) return false;
-  cuuint64_t gdim[2] = {uint64_t(kDqk), rows};
-  cuuint64_t gstride[1] = {uint64_t(kDqk) * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_2d_cached(attn_encode_fn(), map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, uint64_t(kDqk), rows,
+                          uint64_t(kDqk) * 2, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
