@@ -60,6 +60,7 @@ SIGNATURES = {
     "csa2_profile_enable": (_I32, [_I32]),
     "csa2_profile_read": (_I32, [ctypes.POINTER(CKernelTime), _I32, ctypes.POINTER(_I32)]),
     "csa2_clear_device_status": (_I32, [_P, _P]),
+    "csa2_selftest_wait_timeout": (_I32, [_P, _SZ, ctypes.c_uint32, _P]),
 }
 
 
@@ -227,3 +228,11 @@ def profile_read() -> dict:
 
 def clear_device_status(ws: torch.Tensor, stream=None):
     _check("csa2_clear_device_status", _lib.csa2_clear_device_status(_ptr(ws), _stream(stream)))
+
+
+def selftest_wait_timeout(ws: torch.Tensor, limit_us: int = 2000, stream=None):
+    """Runs the device timeout path on purpose: a bounded wait on an mbarrier
+    nothing arrives at gives up after limit_us and sets CSA2_DEV_TIMEOUT in
+    the error word of ws (read it with get_device_status)."""
+    _check("csa2_selftest_wait_timeout",
+           _lib.csa2_selftest_wait_timeout(_ptr(ws), ws.numel(), int(limit_us), _stream(stream)))

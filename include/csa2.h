@@ -267,6 +267,15 @@ csa2_status csa2_get_device_status(const void* ws, void* stream, int32_t* word);
 /* Zeroes the device error word of `ws` (enqueued on `stream`). */
 csa2_status csa2_clear_device_status(void* ws, void* stream);
 
+/* Self-test of the device timeout path.  Enqueues one small kernel whose
+ * thread waits, with the bounded mbarrier wait every library kernel uses, on
+ * an mbarrier that nothing arrives at; after limit_us microseconds
+ * (1 .. 1,000,000) the wait gives up, CSA2_DEV_TIMEOUT is set in the error
+ * word of ws (device, 256-byte aligned, ws_bytes >= 256) and the kernel
+ * returns: no fault, no trap, the context stays usable.
+ * Errors: CSA2_ERR_INVALID_ARG, CSA2_ERR_CUDA. */
+csa2_status csa2_selftest_wait_timeout(void* ws, size_t ws_bytes, uint32_t limit_us, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

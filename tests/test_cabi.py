@@ -103,6 +103,12 @@ def test_host_argument_errors(mod):
     assert lib.indexer_full_topk(ctypes.byref(dbig.c()), 2047, *args, P(0x10010), 1 << 40, None) == 1
     assert lib.csa2_get_device_status(None, None, None) == 1
     assert lib.csa2_clear_device_status(None, None) == 1
+    # the timeout self-test validates its arguments before launching
+    assert lib.csa2_selftest_wait_timeout(None, 256, 1000, None) == 1
+    assert lib.csa2_selftest_wait_timeout(P(0x10010), 256, 1000, None) == 1     # misaligned
+    assert lib.csa2_selftest_wait_timeout(fake, 255, 1000, None) == 1
+    assert lib.csa2_selftest_wait_timeout(fake, 256, 0, None) == 1
+    assert lib.csa2_selftest_wait_timeout(fake, 256, 2000000, None) == 1
 
 
 def test_workspace_layout_mirror(mod):

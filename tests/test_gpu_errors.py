@@ -13,7 +13,7 @@ from tests.gpu_problem import make_problem, run_full
 
 pytestmark = pytest.mark.gpu
 
-CTX, PAGE, TOPK, SWA = 0x01, 0x02, 0x04, 0x08
+CTX, PAGE, TOPK, SWA, TIMEOUT = 0x01, 0x02, 0x04, 0x08, 0x20
 
 
 def attn(p, tk, sl):
@@ -70,3 +70,19 @@ def test_ctx_len_above_capacity():
     assert csa2.get_device_status(p.ws) & CTX
     assert plen.cpu().tolist()[1] == 0
     assert np.all(topk.cpu().numpy()[1] == -1)
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    """A bounded wait on an mbarrier that nothing arrives at gives up after its
+    limit, reports CSA2_DEV_TIMEOUT through the error word, and the context
+    still runs the library's kernels afterwards."""
+    p = make_problem([3000, 1500], seed=21, with_kv=False)
+    csa2.clear_device_status(p.ws)
+    csa2.selftest_wait_timeout(p.ws, limit_us=2000)
+    assert csa2.get_device_status(p.ws) & TIMEOUT
+    csa2.clear_device_status(p.ws)
+    assert csa2.get_device_status(p.ws) == 0
+    pool, pool_len, tk = run_full(p)                  # a normal call on the same context
+    torch.cuda.synchronize()
+    assert csa2.get_device_status(p.ws) == 0
+    assert int(pool_len.min()) > 0 and int((tk >= 0).sum()) > 0
