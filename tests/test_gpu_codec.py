@@ -130,3 +130,23 @@ def test_codec_workload_full_size(lib):
     print("round-trip max|err|/amax per group: median %.4g p99 %.4g max %.4g" % tuple(q.tolist()))
     # |x - dq| <= s and s <= amax/6 * (1 + 2^-4): at most ~0.177 of the group amax
     assert float(q[2]) <= 0.18
+
+
+def test_fp4_slab_save_reload_byte_stable(lib, tmp_path):
+    """The packed FP4 slab is a byte-stable storage format: written by the GPU,
+    saved to a file and loaded back, it is byte-identical, dequantizes to the
+    same bf16 values, and quantizing those values again gives the same bytes."""
+    rng = np.random.default_rng(9)
+    x = torch.from_numpy(rng.standard_normal((4096, 512)).astype(np.float32)).cuda().to(torch.bfloat16)
+    codes, scales = lib.fp4_kv_quantize(x)
+    path = tmp_path / "slab.bin"
+    np.concatenate([codes.cpu().numpy().ravel(), scales.cpu().numpy().ravel()]).tofile(path)
+    raw = np.fromfile(path, dtype=np.uint8)
+    c2 = torch.from_numpy(raw[:codes.numel()].reshape(tuple(codes.shape)).copy()).cuda()
+    s2 = torch.from_numpy(raw[codes.numel():].reshape(tuple(scales.shape)).copy()).cuda()
+    assert torch.equal(c2, codes) and torch.equal(s2, scales)
+    y1 = lib.fp4_kv_dequantize(codes, scales)
+    y2 = lib.fp4_kv_dequantize(c2, s2)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    c3, s3 = lib.fp4_kv_quantize(y2)
+    assert torch.equal(c3, codes) and torch.equal(s3, scales)
