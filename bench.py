@@ -25,6 +25,7 @@ import math
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -105,7 +106,8 @@ class ClockSampler:
     def __init__(self, gpu_index=0):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # raw samples go to a temporary file; the summary goes into the JSON line
+        self.path = os.path.join(tempfile.gettempdir(), f"csa2_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
