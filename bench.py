@@ -78,13 +78,6 @@ def full_call_bytes(wl):
     return sum(idx_row * n + q_w + wl.pool_blocks * 4 + wl.topk * 4 for n in wl.ctx_lens)
 
 
-# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
-# of the scan kernel per indexed position, keyed by the hash of the scan source
-# it was captured on (null once the kernel changes).  Captured on decode-128k
-# (1,048,576 positions); the traffic grows in proportion to the positions.
-TRAFFIC = {"035146e3c735": (134321664 + 3892224) / 1048576}
-
-
 def src_hash(name):
     """Hash of a kernel source's code: comments, blank lines and trailing blanks are
     left out, so that only a change of the code itself drops the stored traffic."""
@@ -99,22 +92,28 @@ def src_hash(name):
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while it is
+    open.  The GPU is selected by its UUID (a CUDA ordinal can name another
+    physical GPU when CUDA_VISIBLE_DEVICES remaps them)."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index=0):
-        self.idx = gpu_index
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
         self.proc = None
-        # raw samples go to a temporary file; the summary goes into the JSON line
+        self.rows = []
+        # raw samples go to a temporary file (removed on exit); the summary
+        # goes into the JSON line
         self.path = os.path.join(tempfile.gettempdir(), f"csa2_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
+        if not self.uuid:
+            return self
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.uuid}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except Exception:
@@ -122,32 +121,47 @@ class ClockSampler:
         return self
 
     def __exit__(self, *a):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
-            self.f.close()
-
-    def summary(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                self.rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
             except ValueError:
                 continue
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+
+    def summary(self):
+        if not self.uuid or self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = self.rows
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "gpu": self.uuid}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
         return {"sm_mhz": float(np.median([r[0] for r in rows])), "sm_max_mhz": rows[0][1],
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "gpu": self.uuid}
+
+
+def gpu_uuid(dev) -> str | None:
+    """nvidia-smi id ("GPU-<uuid>") of a torch CUDA device, if torch reports it."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return None
+    return u if u.startswith("GPU-") else "GPU-" + u
 
 
 # ---------------------------------------------------------------------------
@@ -227,65 +241,122 @@ def job_queries_per_s(world: int, batch: int, t_step_ms: float) -> float:
 
 
 # ---------------------------------------------------------------------------
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="128k")
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    args = ap.parse_args()
+# per-kernel algorithmic bytes (one launch, whole batch) and in-graph timing
+# ---------------------------------------------------------------------------
+def kernel_bytes(wl, name):
+    """Algorithmic HBM bytes of one launch of a library kernel on workload wl
+    (None for the latency-bound selection kernels)."""
+    idx_row = wl.idx_dim * (1 if wl.idx_k_dtype == "fp8" else 4)
+    if name in ("indexer_scan_tc", "indexer_scan_cuda_core"):
+        return sum(idx_row * n for n in wl.ctx_lens)
+    if name == "reindex_score_tc":
+        return sum(idx_row * min(wl.pool_blocks * 8, n) + wl.pool_blocks * 4 for n in wl.ctx_lens)
+    if name in ("attn_pair_tc", "attn_partial_tc"):
+        return wl.batch * attn_layer_bytes(wl)
+    if name == "quantize":
+        return wl.batch * (1024 + 288)
+    return None
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    from compressed_sparse_attention_fp4_gb300 import synth
-    wl = synth.workload(args.workload)
 
-    if args.impl == "reference":
-        if rank != 0:
-            return
-        steps_t = []
-        cb = None
-        for s in range(args.warmup + args.steps):
-            r = cpu_baseline(wl, budget_s=8.0, max_queries=1)
-            if s >= args.warmup:
-                steps_t.append(1.0 / r["value"])
-                cb = r
-        ms = 1000.0 * float(np.mean(steps_t))
-        val = 1.0 / float(np.mean(steps_t))
-        cb["value"] = val
-        cfg = arm_config(wl, world)
-        cfg["sample"] = "1 query per step (the CPU oracle on the host cores)"
-        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "queries/s",
-                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic (seeded; shapes and value recipes of the workload)",
-                "config": cfg,
-                "cpu_baseline": cb,
-                "e2e": {"value": val, "unit": "queries/s", "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
-        return
-
+def time_graph(g, flush, reps, stream):
+    """Mean device time (ms) of `reps` replays of graph g, the L2 flushed
+    before each (events on the launching stream, around the replay only)."""
     import torch
-    import torch.distributed as dist
-    if world > 1:
-        dist.init_process_group("nccl")
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-    dev = torch.device("cuda", torch.cuda.current_device())
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        g.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in ev]))
 
+
+def graph_attribution(sb, flush, reps=60):
+    """Where the graph-replayed step's time goes: the step's first j library
+    calls are captured as their own graph (j = 1 .. all) and timed like the
+    step; call j's share is t_j - t_{j-1}.  The shares add up to the whole
+    step's time and keep the overlap of consecutive kernels inside a graph."""
+    import torch
+    from compressed_sparse_attention_fp4_gb300.step import GraphedStep, step_calls
+    labels = [lab for lab, _ in step_calls(sb)]
+    st = torch.cuda.current_stream()
+    t_prev, rows = 0.0, []
+    for j in range(1, len(labels) + 1):
+        g = GraphedStep(sb, warmup=1, ncalls=j)
+        t = time_graph(g, flush, reps, st)
+        rows.append({"call": labels[j - 1], "us": 1000.0 * (t - t_prev)})
+        t_prev = t
+        del g
+    by_kind = {}
+    for r in rows:
+        k = r["call"].split("@")[0]
+        by_kind.setdefault(k, []).append(r["us"])
+    return {"calls": rows, "step_us": 1000.0 * t_prev,
+            "per_kind_us": {k: {"calls": len(v), "total": float(np.sum(v)), "mean": float(np.mean(v))}
+                            for k, v in by_kind.items()}}
+
+
+def roofline_table(wl, kern, steps_launches, peak, peak_kind):
+    """One entry per library kernel: launches per step, mean event-timed
+    duration, algorithmic bytes per launch, achieved GB/s and fraction of peak."""
+    tab = {}
+    for name, (n, ms) in kern.items():
+        avg_us = 1000.0 * ms / n
+        byt = kernel_bytes(wl, name)
+        e = {"launches_per_step": steps_launches.get(name, 0), "avg_us": avg_us,
+             "us_per_step": avg_us * steps_launches.get(name, 0)}
+        if byt is None:
+            e["bound"] = "latency"
+        else:
+            gbs = byt / (avg_us * 1e-6) / 1e9
+            e.update(bound="hbm", bytes_per_launch=byt, achieved_gbs=gbs, frac=gbs / peak,
+                     peak=peak, peak_source=peak_kind)
+        tab[name] = e
+    return tab
+
+
+# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch
+# per unit of work, keyed by (kernel, hash of its source file when captured);
+# null once the kernel's source changes.  Units: indexed positions for the
+# scans, sequence-layers for the attention.
+TRAFFIC_UNITS = {
+    # decode-128k capture (1,048,576 positions): 134,321,664 B read + 3,892,224 B written
+    ("indexer_scan_tc", "035146e3c735"): (134321664 + 3892224) / 1048576,
+}
+
+
+def traffic_of(wl, name):
+    files = {"indexer_scan_tc": "scan.cu", "reindex_score_tc": "scan.cu", "attn_pair_tc": "attention.cu",
+             "attn_partial_tc": "attention.cu"}
+    if name not in files:
+        return None
+    per_unit = TRAFFIC_UNITS.get((name, src_hash(files[name])))
+    if per_unit is None:
+        return None
+    if name == "indexer_scan_tc":
+        return per_unit * sum(wl.ctx_lens) if wl.idx_k_dtype == "fp8" else None
+    if name == "reindex_score_tc":
+        return per_unit * sum(min(wl.pool_blocks * 8, n) for n in wl.ctx_lens)
+    return per_unit * wl.batch
+
+
+def measure_workload(wl, args, dev, world, flush, with_e2e):
+    """Times one decode workload: graph-replayed step (the headline), per-kernel
+    event timing (eager), in-graph attribution and, optionally, the end-to-end
+    serving loop through the public API with host buffers."""
+    import torch
     from compressed_sparse_attention_fp4_gb300 import csa2, workload
     from compressed_sparse_attention_fp4_gb300.step import GraphedStep, run_step
 
-    sb = workload.build(wl, device=dev)
-    g = GraphedStep(sb, warmup=2)
-    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
-
     def barrier():
         if world > 1:
+            import torch.distributed as dist
             dist.barrier()
 
+    sb = workload.build(wl, device=dev)
+    g = GraphedStep(sb, warmup=2)
+    st = torch.cuda.current_stream()
     # ---- device-resident timing: graph replay, L2 flushed before each step --
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -295,91 +366,79 @@ def main():
           for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(gpu_uuid(dev)) as clk:
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
-            ev[i][0].record()
+            ev[i][0].record(st)
             g.replay()
-            ev[i][1].record()
+            ev[i][1].record(st)
         torch.cuda.synchronize()
     barrier()
     times = np.array([a.elapsed_time(b) for a, b in ev])          # ms
     t_step = max_over_ranks(float(times.mean()), world, dev)
     qps = job_queries_per_s(world, wl.batch, t_step)
     status = csa2.get_device_status(sb.ws)
-    # kernel launches of one step, as the library's launch records count them
-    # (one eager step; the graph replays the same launches)
+
+    # ---- kernels of one step and their durations (eager, the library's own
+    #      event records on the launching stream; the flush and the whole step
+    #      are enqueued before any wait, so each pair times GPU work only) -----
     csa2.profile_enable(True)
     torch.cuda.synchronize()
     run_step(sb)
     torch.cuda.synchronize()
-    launches = sum(n for n, _ in csa2.profile_read().values()) * args.steps
+    per_step = {k: n for k, (n, _) in csa2.profile_read().items()}
     csa2.profile_enable(False)
-
-    # ---- per-call breakdown (eager, events on the launching stream) ---------
-    # The library's kernel timing brackets each of its launches with events
-    # on the same stream, giving per-kernel durations for the roofline.
-    st = torch.cuda.current_stream()
-    per = {"F_index": [], "Ri_index": [], "attn": []}
     csa2.profile_enable(True)
-    n_prof_steps = 3
-    for _ in range(n_prof_steps):
-        # the flush and the whole step are enqueued before any wait, so the
-        # GPU runs them back to back and each event pair times GPU work only
-        # (not the host's enqueue of the next call)
-        torch.cuda.synchronize()
+    n_prof = 5
+    for _ in range(n_prof):
         flush.fill_(3)
-        cur = None
-        marks = []
-        for l, m in enumerate(sb.schedule):
-            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-            e0.record(st)
-            if m == "F":
-                csa2.indexer_full_topk(sb.dims, sb.batch, sb.idx_k, sb.page_table, sb.ctx_len,
-                                       sb.idx_q[l], sb.idx_w[l], sb.pool, sb.pool_len, sb.topk[l], sb.ws)
-                cur = l
-            elif m == "Ri":
-                csa2.indexer_reindex_topk(sb.dims, sb.batch, sb.idx_k, sb.page_table, sb.ctx_len,
-                                          sb.idx_q[l], sb.idx_w[l], sb.pool, sb.pool_len, sb.topk[l], sb.ws)
-                cur = l
-            e1.record(st)
-            csa2.csa2_sparse_attn_decode(sb.dims, sb.batch, 2, sb.q[l], sb.kv_codes, sb.kv_scales,
-                                         sb.kv_rope, sb.page_table, sb.ctx_len, sb.topk[cur], sb.swa[l],
-                                         sb.swa_len[l], sb.scale, sb.out[l], sb.lse[l], sb.ws)
-            e2.record(st)
-            marks.append((m, e0, e1, e2))
-        torch.cuda.synchronize()
-        for m, e0, e1, e2 in marks:
-            if m == "F":
-                per["F_index"].append(e0.elapsed_time(e1))
-            elif m == "Ri":
-                per["Ri_index"].append(e0.elapsed_time(e1))
-            per["attn"].append(e1.elapsed_time(e2))
-    per_ms = {k: float(np.median(v)) for k, v in per.items() if v}
+        run_step(sb)
+    torch.cuda.synchronize()
     kern = csa2.profile_read()
     csa2.profile_enable(False)
     kern_us = {k: 1000.0 * ms / n for k, (n, ms) in kern.items()}
+    attribution = graph_attribution(sb, flush, args.attribution_reps) if args.attribution_reps > 0 else None
 
-    # ---- end to end through the public API with host buffers --------------
-    # Per-step inputs: every layer's query and indexer query / weights, the
-    # new token's latent (the FP4 append) and the newest SWA row of every
-    # layer (the window is a device-resident cache, like the main KV: one
-    # row per layer and sequence arrives per step, into its last slot).  The
-    # step's result: every layer's output, lse and Top-K indices.  As in a
-    # serving loop, two device sets of inputs and results alternate: step i
-    # (set i % 2) computes while a copy stream uploads step i + 1's inputs and
-    # reads back step i - 1's results.  Every copy is inside the timed region;
-    # the L2 is flushed on the compute stream before every step.  The step
-    # itself is the library's captured step graph of its set (`GraphedStep`,
-    # the way a serving loop replays a decode step); `e2e_eager` makes the
-    # same run with one eager library call per layer step instead.
+    res = {"wl": wl, "sb": sb, "graph": g, "t_step": t_step, "qps": qps, "status": status,
+           "clocks": clk.summary(), "per_step": per_step, "kern": kern, "kern_us": kern_us,
+           "attribution": attribution, "launches": sum(per_step.values()) * args.steps,
+           "step_ms_spread": [float(np.percentile(times, 5)), float(np.median(times)),
+                              float(np.percentile(times, 95))]}
+    if with_e2e:
+        res.update(e2e_legs(sb, args, dev, world, flush, wl))
+    return res
+
+
+def e2e_legs(sb, args, dev, world, flush, wl):
+    """End to end through the public API with host buffers.
+
+    Per-step inputs: every layer's query and indexer query / weights, the new
+    token's latent (the FP4 append) and the newest SWA row of every layer (the
+    window is a device-resident cache, like the main KV: one row per layer and
+    sequence arrives per step, into its last slot).  The step's result: every
+    layer's output, lse and Top-K indices.  As in a serving loop, two device
+    sets of inputs and results alternate: step i (set i % 2) computes while a
+    copy stream uploads step i + 1's inputs and reads back step i - 1's
+    results.  Every copy is inside the timed region; the L2 is flushed on the
+    compute stream before every step.  The step itself is the library's
+    captured step graph of its set (`GraphedStep`, the way a serving loop
+    replays a decode step); `e2e_eager` makes the same run with one eager
+    library call per layer step instead."""
+    import torch
+    from compressed_sparse_attention_fp4_gb300.step import GraphedStep, run_step
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
     pin = lambda t: t.cpu().pin_memory()
     names_in = ("q", "idx_q", "idx_w", "new_latent")
     names_out = ("out", "lse", "topk")
     h_in = {k: pin(getattr(sb, k)) for k in names_in}
     h_in["swa_row"] = pin(sb.swa[:, :, -1, :].contiguous())       # [L, B, 576]
-    dev = [{k: getattr(sb, k) for k in names_in + ("swa",) + names_out}]
-    dev.append({k: v.clone() for k, v in dev[0].items()})
+    devs = [{k: getattr(sb, k) for k in names_in + ("swa",) + names_out}]
+    devs.append({k: v.clone() for k, v in devs[0].items()})
     h_out = [{k: torch.empty_like(getattr(sb, k), device="cpu").pin_memory() for k in names_out}
              for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
@@ -394,13 +453,13 @@ def main():
         with torch.cuda.stream(copy_s):
             copy_s.wait_event(ev_done[s_])                 # the set's last step read its inputs
             for k in names_in:
-                dev[s_][k].copy_(h_in[k], non_blocking=True)
-            dev[s_]["swa"][:, :, -1, :].copy_(h_in["swa_row"], non_blocking=True)
+                devs[s_][k].copy_(h_in[k], non_blocking=True)
+            devs[s_]["swa"][:, :, -1, :].copy_(h_in["swa_row"], non_blocking=True)
             ev_in[s_].record(copy_s)
 
     graphs = []
     for s_ in range(2):
-        for k, v in dev[s_].items():
+        for k, v in devs[s_].items():
             setattr(sb, k, v)
         graphs.append(GraphedStep(sb, warmup=1))
 
@@ -411,7 +470,7 @@ def main():
         if graphed:
             graphs[s_].replay()
         else:
-            for k, v in dev[s_].items():
+            for k, v in devs[s_].items():
                 setattr(sb, k, v)
             run_step(sb, stream=comp)
         ev_done[s_].record(comp)
@@ -420,7 +479,7 @@ def main():
         with torch.cuda.stream(copy_s):
             copy_s.wait_event(ev_done[s_])
             for k in names_out:
-                h_out[s_][k].copy_(dev[s_][k], non_blocking=True)
+                h_out[s_][k].copy_(devs[s_][k], non_blocking=True)
             ev_out[s_].record(copy_s)
 
     def run_pipelined(n, graphed):
@@ -443,42 +502,164 @@ def main():
 
     e2e_qps = e2e_rate(True)
     e2e_eager_qps = e2e_rate(False)
-    for k, v in dev[0].items():
+    for k, v in devs[0].items():
         setattr(sb, k, v)
+    return {"e2e": {"value": e2e_qps, "unit": "queries/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "e2e_eager": {"value": e2e_eager_qps, "unit": "queries/s"}}
 
-    # ---- roofline of the dominant kernel: the Full-layer indexer scan ---------
-    peak, peak_kind = peaks()
-    scan_name = "indexer_scan_tc" if "indexer_scan_tc" in kern_us else "indexer_scan_cuda_core"
-    scan_bytes = sum(wl.idx_dim * (1 if wl.idx_k_dtype == "fp8" else 4) * n for n in wl.ctx_lens)
-    achieved = scan_bytes / (kern_us[scan_name] * 1e-6) / 1e9
-    th = src_hash("scan.cu")
-    per_pos = TRAFFIC.get(th) if wl.idx_k_dtype == "fp8" else None
-    traffic = per_pos * sum(wl.ctx_lens) if per_pos is not None else None
-    fb = full_call_bytes(wl)
+
+def summarise(res, peak, peak_kind):
+    """The measured figures of one workload as JSON-ready values."""
+    wl = res["wl"]
     sbytes = step_bytes(wl)
+    t = res["t_step"]
+    tab = roofline_table(wl, res["kern"], res["per_step"], peak, peak_kind)
+    for name, e in tab.items():
+        if "bytes_per_launch" in e:
+            e["traffic"] = traffic_of(wl, name)
+    # the roofline line names the kernel with the largest share of the step's
+    # kernel time (event-timed launches x launches per step)
+    dom = max((n for n in tab if "bytes_per_launch" in tab[n]), key=lambda n: tab[n]["us_per_step"])
+    d = tab[dom]
+    roof = {"bound": "hbm", "kernel": dom, "achieved": d["achieved_gbs"], "peak": peak, "unit": "GB/s",
+            "frac": d["frac"], "peak_source": peak_kind, "bytes_per_launch": d["bytes_per_launch"],
+            "avg_launch_us": d["avg_us"], "traffic": d.get("traffic")}
+    return {
+        "value": res["qps"], "ms_per_step": t,
+        "ms_per_step_p5_p50_p95": res["step_ms_spread"],
+        "algorithmic_bytes_per_step": sbytes,
+        "step_gbs": sbytes / (t * 1e-3) / 1e9,
+        "step_frac_of_peak": sbytes / (t * 1e-3) / 1e9 / peak,
+        "kernel_us": res["kern_us"],
+        "roofline": roof,
+        "roofline_kernels": tab,
+        "graph_attribution": res["attribution"],
+        "device_status": res["status"],
+    }
+
+
+def codec_rates(dev, reps=20):
+    """FP4 write and read of the 1,048,576 x 512 codec slab: GB/s of the
+    algorithmic bytes (1 KiB of bf16 in, 288 B of codes and scales out per row
+    for the write; the reverse for the read), CUDA events around each launch,
+    inputs larger than L2."""
+    import torch
+    from compressed_sparse_attention_fp4_gb300 import csa2, synth
+    n = 1 << 20
+    x = torch.from_numpy(synth.codec_slab(n=n).view(np.int16)).to(dev).view(torch.bfloat16)
+    codes = torch.empty((n, 256), dtype=torch.uint8, device=dev)
+    scales = torch.empty((n, 32), dtype=torch.uint8, device=dev)
+    y = torch.empty((n, 512), dtype=torch.bfloat16, device=dev)
+    st = torch.cuda.current_stream()
+    out = {}
+    for name, fn in (("quantize", lambda: csa2.fp4_kv_quantize(x, codes, scales)),
+                     ("dequantize", lambda: csa2.fp4_kv_dequantize(codes, scales, y))):
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for i in range(reps):
+            ev[i][0].record(st)
+            fn()
+            ev[i][1].record(st)
+        torch.cuda.synchronize()
+        us = 1000.0 * float(np.mean([a.elapsed_time(b) for a, b in ev]))
+        byt = n * (1024 + 288)
+        out[name] = {"avg_us": us, "bytes_per_launch": byt, "achieved_gbs": byt / (us * 1e-6) / 1e9}
+    return out
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="128k")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--attribution-reps", type=int, default=60,
+                    help="replays per prefix graph of the in-graph time attribution (0: none)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the 1M-context and codec workloads measured beside the headline")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    from compressed_sparse_attention_fp4_gb300 import synth
+    wl = synth.workload(args.workload)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # a bounded run: at most 2 untimed and 8 timed queries (or 60 s of
+        # timed CPU work), whatever --steps / --warmup ask for
+        n_warm, n_steps = min(args.warmup, 2), min(args.steps, 8)
+        steps_t = []
+        cb = None
+        for s in range(n_warm + n_steps):
+            r = cpu_baseline(wl, budget_s=8.0, max_queries=1)
+            if s >= n_warm:
+                steps_t.append(1.0 / r["value"])
+                cb = r
+                if sum(steps_t) > 60.0:
+                    break
+        ms = 1000.0 * float(np.mean(steps_t))
+        val = 1.0 / float(np.mean(steps_t))
+        cb["value"] = val
+        cfg = arm_config(wl, world)
+        cfg["sample"] = (f"1 query per step (the CPU oracle on the host cores), "
+                         f"{len(steps_t)} timed steps")
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "queries/s",
+                "n_gpus": world, "steps": len(steps_t), "warmup": n_warm, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded; shapes and value recipes of the workload)",
+                "config": cfg,
+                "cpu_baseline": cb,
+                "e2e": {"value": val, "unit": "queries/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl")
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    peak, peak_kind = peaks()
+
+    res = measure_workload(wl, args, dev, world, flush, with_e2e=True)
+    summ = summarise(res, peak, peak_kind)
     line = {
-        "metric": METRIC, "value": qps, "unit": "queries/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step,
+        "metric": METRIC, "value": res["qps"], "unit": "queries/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["t_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; shapes and value recipes of the workload)",
         "config": arm_config(wl, world),
-        "step_gbs": sbytes / (t_step * 1e-3) / 1e9,
-        "step_frac_of_peak": sbytes / (t_step * 1e-3) / 1e9 / peak,
-        "algorithmic_bytes_per_step": sbytes,
-        "per_call_ms": per_ms,
-        "kernel_us": kern_us,
-        "full_indexer_call_gbs": fb / (per_ms["F_index"] * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": scan_name,
-                     "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": peak_kind,
-                     "bytes_per_launch": scan_bytes, "traffic": traffic},
-        "clocks": clk.summary(),
-        "gpu_launches": launches,
-        "device_status": status,
-        "e2e_eager": {"value": e2e_eager_qps, "unit": "queries/s"},
-        "e2e": {"value": e2e_qps, "unit": "queries/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "roofline": summ["roofline"],
+        "clocks": res["clocks"],
+        "gpu_launches": res["launches"],
+        "e2e": res["e2e"],
+        "e2e_eager": res["e2e_eager"],
     }
+    for k in ("ms_per_step_p5_p50_p95", "algorithmic_bytes_per_step", "step_gbs", "step_frac_of_peak",
+              "kernel_us", "roofline_kernels", "graph_attribution", "device_status"):
+        line[k] = summ[k]
+    if not args.no_extra and world == 1 and wl.name == "128k":
+        # the other context the metric names, and the FP4 codec slab, in the
+        # same run (each its own graph-timed workload)
+        del res
+        torch.cuda.empty_cache()
+        wl1 = synth.workload("1m")
+        r1 = measure_workload(wl1, args, dev, world, flush, with_e2e=False)
+        s1 = summarise(r1, peak, peak_kind)
+        s1["config"] = arm_config(wl1, world)
+        s1["clocks"] = r1["clocks"]
+        del r1
+        torch.cuda.empty_cache()
+        line["workloads"] = {"decode-1m": s1, "codec-1m-rows": codec_rates(dev)}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
     if world > 1:

@@ -3,39 +3,18 @@
 // status without launching anything when an argument is wrong.
 #include <cstdint>
 
+#include "checks.cuh"
 #include "kernels.cuh"
 
 using namespace csa2;
 
 namespace {
 
-inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline bool aligned(const void* p, uintptr_t a) { return is_aligned(p, a); }
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 csa2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
-
-csa2_status check_dims(const csa2_dims* d, int32_t batch) {
-  if (!d || batch < 0) return CSA2_ERR_INVALID_ARG;
-  if (d->idx_k_dtype != CSA2_IDXK_E4M3 && d->idx_k_dtype != CSA2_IDXK_F32) return CSA2_ERR_INVALID_ARG;
-  if (d->idx_heads < 1 || d->idx_heads > kMaxIdxHeads) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  if (d->idx_k_dtype == CSA2_IDXK_E4M3 && d->idx_dim != 128) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  if (d->idx_k_dtype == CSA2_IDXK_F32 && d->idx_dim != 64) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  if (d->pool_blocks < 1 || d->pool_blocks > kMaxPool) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  if (d->topk < 1 || d->topk > kMaxTopk) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  if (d->heads < 1 || d->heads > kMaxHeads) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  if (d->swa < 0 || d->swa > kMaxSwa) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  if (d->max_ctx < 1 || d->max_ctx > kMaxCtx) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  return CSA2_OK;
-}
-
-csa2_status check_paging(const csa2_dims* d, const int32_t* page_table) {
-  if (!page_table) return CSA2_OK;
-  if (d->max_pages < 1 || d->num_pages < 1) return CSA2_ERR_INVALID_ARG;
-  if (int64_t(d->max_pages) * kPage > kMaxCtx) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned(page_table, 4)) return CSA2_ERR_INVALID_ARG;
-  return CSA2_OK;
-}
 
 // The indexer scan addresses cache rows with 32-bit tensor coordinates.
 csa2_status check_idx_rows(const csa2_dims* d, int32_t batch, const int32_t* page_table) {
@@ -178,13 +157,9 @@ csa2_status csa2_sparse_attn_decode(const csa2_dims* d, int32_t batch, int32_t m
   WsLayout L;
   if ((st = check_ws(d, batch, ws, ws_bytes, &L)) != CSA2_OK) return st;
   if (batch == 0) return CSA2_OK;
-  if (!q || !kv_codes || !kv_scales || !kv_rope || !ctx_len || !topk || !swa_len || !out || !lse)
-    return CSA2_ERR_INVALID_ARG;
-  if (d->swa > 0 && !swa_kv) return CSA2_ERR_INVALID_ARG;
-  if (!aligned(kv_codes, 16) || !aligned(kv_scales, 2) || !aligned(kv_rope, 16) || !aligned(q, 16) || !aligned(out, 16) ||
-      (swa_kv && !aligned(swa_kv, 16)))
-    return CSA2_ERR_INVALID_ARG;
-  if (!(scale == scale)) return CSA2_ERR_INVALID_ARG;
+  if ((st = check_attn_ptrs(d, mode, q, kv_codes, kv_scales, kv_rope, ctx_len, topk, swa_kv, swa_len, scale, out,
+                            lse)) != CSA2_OK)
+    return st;
   AttnArgs a = {};
   a.d = *d;
   a.batch = batch;

@@ -117,8 +117,6 @@ __device__ inline void st_shared_v4(uint8_t* base, uint32_t off, uint4 v) {
   *reinterpret_cast<uint4*>(base + off) = v;
 }
 
-constexpr int kMaxClusterSplits = 8;                // portable cluster size
-
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_partial_tc_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
                            const __grid_constant__ CUtensorMap swamap, int swa_tma_split) {
@@ -894,7 +892,7 @@ cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
       !encode_rows_map(&swamap, a.swa, uint64_t(a.batch) * a.d.swa, kEntries))
     return cudaErrorInvalidValue;
   size_t smem = attn_smem_bytes(a.d.heads);
-  if (a.L.splits <= kMaxClusterSplits) {
+  if (!attn_uses_partials(a.d)) {
     // one cluster of 2 x chunks CTAs per sequence; the merge happens inside it
     const size_t psmem = size_t(kPairKvBytes) + size_t(kPairQBytes) + 2 * size_t(kSxBytes) + 1024;
     static KernelAttrs done;

@@ -24,6 +24,7 @@ constexpr int kMaxIdxHeads = 16;
 constexpr int64_t kMaxCtx = int64_t(1) << 20;   // 8 selection CTAs x 16384 blocks
 constexpr int kSelCapPerCta = 16384;           // items a selection CTA holds
 constexpr int kAttnChunk = 128;                // entries per split-KV partial
+constexpr int kMaxClusterSplits = 8;           // chunks merged inside one cluster (portable size)
 
 // ---------------------------------------------------------------------------
 // Workspace layout.  Computed identically on the host (sizing, validation)
@@ -52,6 +53,16 @@ __host__ __device__ inline int64_t max64(int64_t a, int64_t b) { return a > b ? 
 
 __host__ __device__ inline int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
+// Split-KV chunks of an attention call: ceil((K + W) / 128), at least 1.
+// Up to kMaxClusterSplits chunks are merged inside one thread-block cluster
+// (no scratch but the error word); more write partials that a combine kernel
+// merges (attn_o / attn_ml of the workspace).
+__host__ __device__ inline int attn_splits(const csa2_dims& d) {
+  const int s = (d.topk + d.swa + kAttnChunk - 1) / kAttnChunk;
+  return s < 1 ? 1 : s;
+}
+__host__ __device__ inline bool attn_uses_partials(const csa2_dims& d) { return attn_splits(d) > kMaxClusterSplits; }
+
 __host__ __device__ inline WsLayout make_layout(const csa2_dims& d, int batch) {
   WsLayout L;
   int64_t off = 0;
@@ -63,8 +74,7 @@ __host__ __device__ inline WsLayout make_layout(const csa2_dims& d, int batch) {
   int64_t pool = d.pool_blocks;
   L.ri_scores = off;  off = align256(off + int64_t(batch) * pool * kBlock * 4);
   L.ri_delta = off;   off = align256(off + int64_t(batch) * pool * 4);
-  L.splits = (d.topk + d.swa + kAttnChunk - 1) / kAttnChunk;
-  if (L.splits < 1) L.splits = 1;
+  L.splits = attn_splits(d);
   L.attn_o = off;  off = align256(off + int64_t(batch) * L.splits * d.heads * kLatent * 4);
   L.attn_ml = off; off = align256(off + int64_t(batch) * L.splits * d.heads * 2 * 4);
   L.sel_cap = L.nb_max > pool * kBlock ? L.nb_max : pool * kBlock;

@@ -11,11 +11,13 @@
 // exits.  The caller still passes every input and output buffer.
 //
 // The array is shared by every call on a device and keeps the previous call's
-// contents; the error word at its start is cleared by each call, the rest is
-// fully rewritten before it is read.  Two calls whose work overlaps on the GPU
+// contents; the error word at its start is cleared by each call, the partial
+// outputs (used only when the entries span more than kMaxClusterSplits chunks
+// of 128) are fully rewritten before they are read.  Two calls whose work overlaps on the GPU
 // (different streams, no ordering between them) race on the array.
 #include <mutex>
 
+#include "checks.cuh"
 #include "kernels.cuh"
 
 using namespace csa2;
@@ -56,8 +58,6 @@ __global__ void publish_error_word(int32_t* err_word) {
   if (v) atomicOr(err_word, v);
 }
 
-inline bool is_aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
 }  // namespace
 
 extern "C" csa2_status csa2_sparse_attn_decode_noalloc(
@@ -65,36 +65,34 @@ extern "C" csa2_status csa2_sparse_attn_decode_noalloc(
     const uint8_t* kv_scales, const uint16_t* kv_rope, const int32_t* page_table,
     const int32_t* ctx_len, const int32_t* topk, const uint16_t* swa_kv, const int32_t* swa_len,
     float scale, float* out, float* lse, int32_t* err_word, void* stream) {
-  if (!d || batch < 0) return CSA2_ERR_INVALID_ARG;
+  csa2_status st = check_attn_dims(d, batch);
+  if (st != CSA2_OK) return st;
   if (mode < CSA2_MODE_FULL || mode > CSA2_MODE_REUSE) return CSA2_ERR_INVALID_ARG;
-  if (d->heads < 1 || d->heads > kMaxHeads || d->topk < 1 || d->topk > kMaxTopk || d->swa < 0 ||
-      d->swa > kMaxSwa || d->max_ctx < 1 || d->max_ctx > kMaxCtx)
-    return CSA2_ERR_UNSUPPORTED_SHAPE;
-  if (page_table && (d->max_pages < 1 || d->num_pages < 1 || !is_aligned(page_table, 4)))
-    return CSA2_ERR_INVALID_ARG;
-  // scratch needed: error word, partial outputs and (max, sum) per split
+  if ((st = check_paging(d, page_table)) != CSA2_OK) return st;
+  // scratch needed: the error word; the partial outputs and (max, sum) per
+  // chunk only when the chunks are merged by the combine kernel
   WsLayout L = {};
-  L.splits = (d->topk + d->swa + kAttnChunk - 1) / kAttnChunk;
-  int64_t rows = int64_t(batch) * L.splits * d->heads;
+  L.splits = attn_splits(*d);
   L.err = 0;
   L.attn_o = 256;
-  L.attn_ml = align256(L.attn_o + rows * kLatent * 4);
-  L.total = align256(L.attn_ml + rows * 2 * 4);
+  L.attn_ml = 256;
+  L.total = 256;
+  if (attn_uses_partials(*d)) {
+    const int64_t rows = int64_t(batch) * L.splits * d->heads;
+    L.attn_ml = align256(L.attn_o + rows * kLatent * 4);
+    L.total = align256(L.attn_ml + rows * 2 * 4);
+  }
   if (L.total > int64_t(kScratchBytes)) return CSA2_ERR_WORKSPACE_TOO_SMALL;
   if (batch == 0) return CSA2_OK;
-  if (!q || !kv_codes || !kv_scales || !kv_rope || !ctx_len || !topk || !swa_len || !out || !lse)
-    return CSA2_ERR_INVALID_ARG;
-  if (d->swa > 0 && !swa_kv) return CSA2_ERR_INVALID_ARG;
-  if (!is_aligned(kv_codes, 16) || !is_aligned(kv_scales, 2) || !is_aligned(kv_rope, 16) || !is_aligned(q, 16) ||
-      !is_aligned(out, 16) || (swa_kv && !is_aligned(swa_kv, 16)) ||
-      (err_word && !is_aligned(err_word, 4)))
-    return CSA2_ERR_INVALID_ARG;
-  if (!(scale == scale)) return CSA2_ERR_INVALID_ARG;
+  if ((st = check_attn_ptrs(d, mode, q, kv_codes, kv_scales, kv_rope, ctx_len, topk, swa_kv, swa_len, scale, out,
+                            lse)) != CSA2_OK)
+    return st;
+  if (err_word && !is_aligned(err_word, 4)) return CSA2_ERR_INVALID_ARG;
 
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return CSA2_ERR_CUDA;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(scratch, 0, 256, st) != cudaSuccess) return CSA2_ERR_CUDA;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(scratch, 0, 256, cs) != cudaSuccess) return CSA2_ERR_CUDA;
 
   AttnArgs a = {};
   a.d = *d;
@@ -113,9 +111,9 @@ extern "C" csa2_status csa2_sparse_attn_decode_noalloc(
   a.lse = lse;
   a.ws = static_cast<uint8_t*>(scratch);
   a.L = L;
-  if (launch_attention(a, st) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (launch_attention(a, cs) != cudaSuccess) return CSA2_ERR_CUDA;
   if (err_word) {
-    publish_error_word<<<1, 1, 0, st>>>(err_word);
+    publish_error_word<<<1, 1, 0, cs>>>(err_word);
     if (cudaGetLastError() != cudaSuccess) return CSA2_ERR_CUDA;
   }
   return CSA2_OK;

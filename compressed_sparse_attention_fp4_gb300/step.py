@@ -64,30 +64,31 @@ class StepBuffers:
         return self
 
 
-def run_step(sb: StepBuffers, stream=None) -> int:
-    """Enqueue one decode step; returns the number of library calls made."""
+def step_calls(sb: StepBuffers, stream=None) -> list:
+    """The library calls of one decode step, in order, as (label, thunk) pairs.
+
+    Labels: ``append`` (FP4 write of the newest token), ``F`` / ``Ri`` (the
+    indexer of a Full / Reindex layer) and ``attn:<mode>`` (a layer's core
+    attention), each with its layer number."""
     d, B = sb.dims, sb.batch
     if stream is None:
         stream = torch.cuda.current_stream()         # resolved once for the whole step
+    calls = []
     cur = None
-    calls = 0
     for l, mode in enumerate(sb.schedule):
         if mode == "F":
             if sb.new_latent is not None:
-                csa2.fp4_kv_quantize_scatter(sb.new_latent, sb.new_rows, sb.kv_codes,
-                                             sb.kv_scales, stream=stream)
-                calls += 1
-            csa2.indexer_full_topk(d, B, sb.idx_k, sb.page_table, sb.ctx_len, sb.idx_q[l],
-                                   sb.idx_w[l], sb.pool, sb.pool_len, sb.topk[l], sb.ws,
-                                   stream=stream)
-            calls += 1
+                calls.append((f"append@{l}", lambda: csa2.fp4_kv_quantize_scatter(
+                    sb.new_latent, sb.new_rows, sb.kv_codes, sb.kv_scales, stream=stream)))
+            calls.append((f"F@{l}", lambda l=l: csa2.indexer_full_topk(
+                d, B, sb.idx_k, sb.page_table, sb.ctx_len, sb.idx_q[l], sb.idx_w[l], sb.pool,
+                sb.pool_len, sb.topk[l], sb.ws, stream=stream)))
             cur = l
             m = csa2.MODE_FULL
         elif mode == "Ri":
-            csa2.indexer_reindex_topk(d, B, sb.idx_k, sb.page_table, sb.ctx_len, sb.idx_q[l],
-                                      sb.idx_w[l], sb.pool, sb.pool_len, sb.topk[l], sb.ws,
-                                      stream=stream)
-            calls += 1
+            calls.append((f"Ri@{l}", lambda l=l: csa2.indexer_reindex_topk(
+                d, B, sb.idx_k, sb.page_table, sb.ctx_len, sb.idx_q[l], sb.idx_w[l], sb.pool,
+                sb.pool_len, sb.topk[l], sb.ws, stream=stream)))
             cur = l
             m = csa2.MODE_REINDEX
         elif mode == "Ru":
@@ -96,29 +97,40 @@ def run_step(sb: StepBuffers, stream=None) -> int:
             m = csa2.MODE_REUSE
         else:
             raise ValueError(f"unknown layer mode {mode!r}")
-        csa2.csa2_sparse_attn_decode(d, B, m, sb.q[l], sb.kv_codes, sb.kv_scales, sb.kv_rope,
-                                     sb.page_table, sb.ctx_len, sb.topk[cur], sb.swa[l],
-                                     sb.swa_len[l], sb.scale, sb.out[l], sb.lse[l], sb.ws,
-                                     stream=stream)
-        calls += 1
-    sb.calls = calls
+        calls.append((f"attn:{mode}@{l}", lambda l=l, m=m, cur=cur: csa2.csa2_sparse_attn_decode(
+            d, B, m, sb.q[l], sb.kv_codes, sb.kv_scales, sb.kv_rope, sb.page_table, sb.ctx_len,
+            sb.topk[cur], sb.swa[l], sb.swa_len[l], sb.scale, sb.out[l], sb.lse[l], sb.ws,
+            stream=stream)))
     return calls
 
 
-class GraphedStep:
-    """One decode step captured once in a CUDA graph and replayed."""
+def run_step(sb: StepBuffers, stream=None, ncalls: int | None = None) -> int:
+    """Enqueue one decode step (or its first `ncalls` library calls); returns
+    the number of library calls made."""
+    calls = step_calls(sb, stream)
+    if ncalls is not None:
+        calls = calls[:ncalls]
+    for _, fn in calls:
+        fn()
+    sb.calls = len(calls)
+    return len(calls)
 
-    def __init__(self, sb: StepBuffers, warmup: int = 1):
+
+class GraphedStep:
+    """One decode step (or its first `ncalls` library calls) captured once in
+    a CUDA graph and replayed."""
+
+    def __init__(self, sb: StepBuffers, warmup: int = 1, ncalls: int | None = None):
         self.sb = sb
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
             for _ in range(warmup):
-                run_step(sb)
+                run_step(sb, ncalls=ncalls)
         torch.cuda.current_stream().wait_stream(s)
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
-            self.calls = run_step(sb)
+            self.calls = run_step(sb, ncalls=ncalls)
 
     def replay(self):
         self.graph.replay()

@@ -224,10 +224,13 @@ csa2_status csa2_sparse_attn_decode(const csa2_dims* d, int32_t batch, int32_t m
  * take.  The split-KV scratch lives instead in a fixed device array of
  * CSA2_NOALLOC_SCRATCH_BYTES inside the library, held on every GPU that
  * loads the library until the process exits.
- *   Limit: 256 + B*S*H*2048 + B*S*H*8 bytes (each part rounded up to 256)
- *   with S = ceil((topk + swa) / 128) must fit the array -- e.g. batch 8 at
- *   Top-512, SWA-128, 64 heads; larger batches return
- *   CSA2_ERR_WORKSPACE_TOO_SMALL and launch nothing.
+ *   Limit: with S = ceil((topk + swa) / 128) chunks of entries, up to 8
+ *   chunks are merged inside one thread-block cluster and need only the
+ *   256-byte error word (any batch).  Above 8 chunks the per-chunk partial
+ *   outputs live in the array: 256 + B*S*H*2048 + B*S*H*8 bytes (each part
+ *   rounded up to 256) must fit it -- up to batch 5 at Top-2048, SWA-128,
+ *   64 heads; larger shapes return CSA2_ERR_WORKSPACE_TOO_SMALL and launch
+ *   nothing.
  *   Arguments and results are those of csa2_sparse_attn_decode without
  *   ws / ws_bytes; err_word (device int32, may be NULL) receives the device
  *   error bits of this call, ORed in.

@@ -22,12 +22,21 @@ def rand_inputs(rng, n=300, H=8, W=20):
 
 
 def sdpa(q, keys, vals, scale):
+    """Dense attention two ways: PyTorch's float64 scaled_dot_product_attention
+    (its backend picks the kernel) and the textbook softmax written out in
+    NumPy; both must agree before either is used as the reference."""
     qt = torch.tensor(q)[None, :, None, :]                       # [1,H,1,576]
     kt = torch.tensor(keys)[None, None].expand(1, q.shape[0], -1, -1)
     vt = torch.tensor(vals)[None, None].expand(1, q.shape[0], -1, -1)
-    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)
-    logits = scale * torch.tensor(q) @ torch.tensor(keys).T
-    return o[0, :, 0].numpy(), torch.logsumexp(logits, dim=1).numpy()
+    o_t = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)[0, :, 0].numpy()
+    logits = scale * (np.asarray(q) @ np.asarray(keys).T)
+    m = logits.max(axis=1, keepdims=True)
+    e = np.exp(logits - m)
+    z = e.sum(axis=1, keepdims=True)
+    o_np = (e @ np.asarray(vals)) / z
+    lse = (m + np.log(z))[:, 0]
+    assert np.allclose(o_t, o_np, rtol=1e-9, atol=1e-9)
+    return o_np, lse
 
 
 def test_all_positions_equals_dense_sdpa():
