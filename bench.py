@@ -251,7 +251,7 @@ def kernel_bytes(wl, name):
         return sum(idx_row * n for n in wl.ctx_lens)
     if name == "reindex_score_tc":
         return sum(idx_row * min(wl.pool_blocks * 8, n) + wl.pool_blocks * 4 for n in wl.ctx_lens)
-    if name in ("attn_pair_tc", "attn_partial_tc"):
+    if name in ("attn_cluster_tc", "attn_partial_tc"):
         return wl.batch * attn_layer_bytes(wl)
     if name == "quantize":
         return wl.batch * (1024 + 288)
@@ -327,7 +327,7 @@ TRAFFIC_UNITS = {
 
 
 def traffic_of(wl, name):
-    files = {"indexer_scan_tc": "scan.cu", "reindex_score_tc": "scan.cu", "attn_pair_tc": "attention.cu",
+    files = {"indexer_scan_tc": "scan.cu", "reindex_score_tc": "scan.cu", "attn_cluster_tc": "attention.cu",
              "attn_partial_tc": "attention.cu"}
     if name not in files:
         return None

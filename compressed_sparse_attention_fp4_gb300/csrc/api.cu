@@ -177,6 +177,7 @@ csa2_status csa2_sparse_attn_decode(const csa2_dims* d, int32_t batch, int32_t m
   a.lse = lse;
   a.ws = static_cast<uint8_t*>(ws);
   a.L = L;
+  a.early = mode == CSA2_MODE_REUSE;
   return from_cuda(launch_attention(a, as_stream(stream)));
 }
 

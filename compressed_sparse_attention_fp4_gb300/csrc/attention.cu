@@ -27,17 +27,17 @@
 //   5. the chunks of the sequence are merged: o = sum_s 2^(m_s - M) o_s / L,
 //      L = sum_s 2^(m_s - M) l_s, lse = M ln 2 + ln L (m in base-2 logits).
 //
-// attn_pair_kernel (at most 8 chunks, the usual case): two CTAs per chunk
-// split the 576 channels (latent 0..255 | latent 256..511 + rope), exchange
-// their S^T partials through shared memory and each computes O^T for its 256
-// value dimensions.  The 2 x chunks CTAs of a sequence form one thread-block
+// attn_cluster_kernel (K + W <= 1024, the usual case): one CTA per (sequence,
+// group of 32 heads, chunk of 128 entries) with all 576 channels of its
+// entries; the chunks of a (sequence, head group) form one thread-block
 // cluster: every chunk copies its per-head (m_s, l_s) into every CTA's shared
-// memory, on an mbarrier that counts the bytes; the chunk that finishes first
-// (the TMA-loaded SWA window) zeroes the output early and signals the other
-// chunks of its half; each CTA then forms M and L, scales its O^T part and
-// adds it into the output with coalesced reduce-adds (red.global.add.f32)
-// straight from tensor memory.  The order of the additions is not fixed, so
-// the last bits of the output may differ between runs.
+// memory, on an mbarrier that counts the bytes; chunk 0 zeroes the head
+// group's output rows early and signals the other chunks; each CTA then forms
+// M and L, scales its O^T part and adds it into the output with coalesced
+// reduce-adds (red.global.add.f32) straight from tensor memory.  The order of
+// the additions is not fixed, so the last bits of the output may differ
+// between runs.  In Reuse mode the entries are gathered before the kernel
+// waits for the one before it (see the kernel's comment).
 //
 // attn_partial_tc_kernel + attn_combine_kernel (more chunks): one CTA per
 // chunk writes its unnormalised O_s and (m_s, l_s) (natural-log m) to the
@@ -396,21 +396,58 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Channel-split pairs.  Every 128-entry chunk is served by two CTAs: half 0
-// takes latent channels 0..255, half 1 latent channels 256..511 and the rope
-// (64).  Each gathers, dequantizes and multiplies only its channels
-// (S^T partial, M=128, N=64, K=256 or 320), the pair exchanges the partial
-// S^T through shared memory (one bulk copy into the partner, completing on
-// its mbarrier), both
-// form the same softmax, and each computes O^T for its own 256 latent
-// dimensions (the value channels it holds).  The 2 x chunks CTAs of a
-// sequence form one cluster (up to 16) that merges the chunks as above.
+// Cluster kernel (K + W <= 1024, the usual case).  One CTA per (sequence,
+// group of 32 heads, chunk of 128 entry slots); the chunks of one (sequence,
+// head group) form a thread-block cluster (up to 8 CTAs) that merges them.
+// A CTA holds all 576 key channels of its 128 entries (144 KB of bf16) and
+// the query of its 32 heads (36 KB), so no partial scores are exchanged:
+//   * S^T[128 entries x 32 heads] = KV . Q^T (M = 128, N = 32, K = 576),
+//     issued box by box as the query's 64-channel boxes land, the K steps
+//     spread round-robin over 4 tensor-memory accumulators so that
+//     consecutive MMAs do not wait for each other's accumulation (the
+//     softmax adds the 4 partial sums);
+//   * softmax over the 128 entries (TMEM lanes; 16 warps, 8 heads each);
+//   * P^T stored K-major as bf16 hi and lo parts side by side: rows 0..31
+//     hold the hi parts of the 32 heads, rows 32..63 the lo parts;
+//   * O^T[512 dims x (hi | lo) 64] = V^T . [P_hi | P_lo]^T: 4 M-tiles, N = 64,
+//     K = 128 (one instruction covers both parts), the tiles' MMAs issued
+//     interleaved;
+//   * merge: every chunk copies its (m, l) into every CTA of the cluster
+//     (warp 1, while thread 0 issues the O MMAs); every chunk zeroes its share
+//     of the head group's output rows and signals the others; each CTA adds
+//     its scaled O (hi + lo) into the output with coalesced reduce-adds
+//     (red.global.add.f32) straight from tensor memory.
+// One CTA per SM (its shared memory), as every tensor-memory kernel of the
+// library.  In Reuse mode (the indices and the main-KV cache come from
+// earlier work on the stream) the Top-K indices are read and the entries
+// gathered and dequantized before griddepcontrol.wait; the query, the SWA
+// window and the outputs wait for the previous kernel.
 // ---------------------------------------------------------------------------
-constexpr int kPairRegions = 5;                       // regions of 64 channels, at most
-constexpr int kPairKvBytes = kPairRegions * kRegion;  // 80 KB
-constexpr int kPairQBytes = kPairRegions * kQRegion;  // 40 KB
-constexpr int kSxBytes = kEntries * kQRows * 4;       // 32 KB: the partner's S^T partial
-constexpr uint32_t kPairTmemCols = 256;               // S^T: 64 cols, O^T: 2 x 64 cols
+constexpr int kCEntries = kEntries;                  // entry slots per CTA (= MMA M)
+constexpr int kCHeads = 32;                          // heads per CTA (MMA N)
+constexpr int kCQRegion = kCHeads * 128;             // 64 channels x 32 heads: 4 KB
+constexpr int kCQBytes = 9 * kCQRegion;              // 36 KB (later P^T hi / lo)
+constexpr int kCPRegion = 2 * kCHeads * 128;         // P^T hi | lo: 64 rows x 64 entries: 8 KB
+constexpr int kSAcc = 4;                            // S^T partial accumulators
+constexpr uint32_t kCTmemCols = 512;                 // S^T: 4 x 32 cols, O^T: 4 x 64 cols (hi | lo)
+constexpr uint32_t kCOCol = kSAcc * kCHeads;         // first O^T column
+static_assert(2 * kCPRegion <= kCQBytes, "P^T (two regions of 64 entries) fits the query buffer");
+static_assert(kCOCol + 4 * 2 * kCHeads <= kCTmemCols, "tensor-memory columns");
+
+struct ClusterSmall {
+  uint64_t bar_q[9];                                 // query box kb (and window box kb) landed
+  uint64_t bar_s, bar_o, bar_ml, bar_zero;
+  uint32_t valid[kCEntries / 32];                    // bit e: entry slot e holds an entry
+  uint32_t tmem_slot;
+  int32_t ok_ml, ok_z;
+  __align__(16) float red_m[4][4][8];                // [head octet][lane quarter][head]
+  float red_l[4][4][8];
+  float fac[kCHeads];                                // 2^(m_chunk - M) / L per head
+  __align__(16) float ml_mine[2][kCHeads];           // this chunk's (m, l), base-2 m
+  __align__(16) float ml_all[kMaxClusterSplits][2][kCHeads];   // every chunk's (m, l)
+};
+
+size_t cluster_smem_bytes() { return 1024 + size_t(kKvBytes) + size_t(kCQBytes) + sizeof(ClusterSmall); }
 
 // Shared-memory address of the same object in CTA `rank` of the cluster.
 __device__ inline uint32_t cluster_addr(const void* p, uint32_t rank) {
@@ -448,386 +485,359 @@ __device__ inline void mbar_arrive_remote(uint32_t rbar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
 }
 
-// Cache row of entry slot `slot` of sequence b: a main-KV row (>= 0), SWA
-// row r as -2 - r, or -1 for an empty slot.  t is the slot's Top-K index
-// (slots < K); a bad index is reported when `report` is set.
-__device__ inline int64_t entry_row(const AttnArgs& a, int b, int slot, int32_t t, int64_t n_ctx, int swl,
-                                    bool report) {
-  const int K = a.d.topk, W = a.d.swa;
-  if (slot < K) {
-    if (t >= 0 && t < n_ctx) {
-      const int64_t r = kv_row(a.page_table, a.d, b, t, a.ws);
-      return r < 0 ? -1 : r;
-    }
-    if (report && (t >= n_ctx || t < -1)) raise_err(a.ws, CSA2_DEV_TOPK_IDX);
-    return -1;
+// Reduces 8 values per lane over the warp (reduce-scatter): returns the
+// reduction of value index octet_index(lane), held by lanes 4i .. 4i+3.
+__device__ inline int octet_index(int lane) {
+  return (((lane >> 4) & 1) << 2) | (((lane >> 3) & 1) << 1) | ((lane >> 2) & 1);
+}
+
+template <bool kMax>
+__device__ inline float butterfly8(const float (&v)[8], int lane) {
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+  float y[4], z[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b4 ? v[4 + i] : v[i], give = b4 ? v[i] : v[4 + i];
+    y[i] = op(keep, __shfl_xor_sync(0xFFFFFFFFu, give, 16));
   }
-  return (slot < K + W && slot - K < swl) ? -2 - int64_t(slot - K) : -1;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b3 ? y[2 + i] : y[i], give = b3 ? y[i] : y[2 + i];
+    z[i] = op(keep, __shfl_xor_sync(0xFFFFFFFFu, give, 8));
+  }
+  const float keep = b2 ? z[1] : z[0], give = b2 ? z[0] : z[1];
+  float u = op(keep, __shfl_xor_sync(0xFFFFFFFFu, give, 4));
+  u = op(u, __shfl_xor_sync(0xFFFFFFFFu, u, 2));
+  return op(u, __shfl_xor_sync(0xFFFFFFFFu, u, 1));
+}
+
+// Gathers this thread's share of the chunk's FP4 main-KV entries and writes
+// them, dequantized exactly to bf16, into the 128-byte swizzled KV tile:
+// entry e = tid % 128, channel regions 2 sub and 2 sub + 1 (sub = tid / 128:
+// latent channels 128 sub .. 128 sub + 127) and rope chunks 2 sub, 2 sub + 1.
+// Returns the entry's cache row (-1: no main entry; -2 - r: SWA row r, filled
+// later).
+__device__ inline int64_t cluster_gather(const AttnArgs& a, uint8_t* kv_s, int b, int chunk, int64_t n_ctx,
+                                         int tid, bool swa_tma) {
+  const int e = tid & (kCEntries - 1), sub = tid >> 7;
+  const int K = a.d.topk, W = a.d.swa;
+  const int slot = chunk * kCEntries + e;
+  if (swa_tma) return slot < K + W ? -2 - int64_t(slot - K) : -1;   // the window's rows come by TMA
+  int64_t row = -1;
+  if (slot < K) {
+    const int32_t t = __ldg(a.topk + int64_t(b) * K + slot);
+    if (t >= 0 && t < n_ctx) {
+      row = kv_row(a.page_table, a.d, b, t, a.ws);
+      if (row < 0) row = -1;
+    } else if (sub == 0 && (t >= n_ctx || t < -1)) {
+      raise_err(a.ws, CSA2_DEV_TOPK_IDX);
+    }
+  } else if (slot < K + W) {
+    row = -2 - int64_t(slot - K);                    // SWA slot (length checked later)
+  }
+  uint4 cd[4], rp[2];
+  uint32_t sc[2] = {0, 0};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) cd[i] = make_uint4(0, 0, 0, 0);
+  rp[0] = rp[1] = make_uint4(0, 0, 0, 0);
+  if (row >= 0) {
+    // codes: 64 bytes (channels 128 sub ..); scales: 8 bytes; rope: 32 bytes
+    const uint4* cp = reinterpret_cast<const uint4*>(a.codes + row * kCodesPerRow) + 4 * sub;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cd[i] = __ldg(cp + i);
+    const uint16_t* sp = reinterpret_cast<const uint16_t*>(a.scales + row * kScalesPerRow) + 4 * sub;
+    sc[0] = uint32_t(__ldg(sp)) | (uint32_t(__ldg(sp + 1)) << 16);
+    sc[1] = uint32_t(__ldg(sp + 2)) | (uint32_t(__ldg(sp + 3)) << 16);
+    const uint4* rq = reinterpret_cast<const uint4*>(a.rope + row * kRope) + 2 * sub;
+    rp[0] = __ldg(rq);
+    rp[1] = __ldg(rq + 1);
+  }
+  if (row <= -2) return row;                         // the SWA rows are written later
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {                      // region 2 sub + r: channels 64 (2 sub + r) ..
+    const uint32_t cw[8] = {cd[2 * r].x, cd[2 * r].y, cd[2 * r].z, cd[2 * r].w,
+                            cd[2 * r + 1].x, cd[2 * r + 1].y, cd[2 * r + 1].z, cd[2 * r + 1].w};
+    uint8_t* region = kv_s + (2 * sub + r) * kRegion;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {                    // 16-byte chunk c: channels 8c .. 8c + 7
+      const float s = e4m3_to_f32((sc[r] >> (8 * (c >> 1))) & 0xFF);
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t h2 = e2m1x2_to_f16x2_a((cw[c] >> (8 * i)) & 0xFF);
+        w[i] = pack_bf16x2(__half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF))) * s,
+                           __half2float(__ushort_as_half(uint16_t(h2 >> 16))) * s);
+      }
+      st_shared_v4(region, tc::sw128_offset(e, c), make_uint4(w[0], w[1], w[2], w[3]));
+    }
+  }
+  st_shared_v4(kv_s + 8 * kRegion, tc::sw128_offset(e, 2 * sub), rp[0]);
+  st_shared_v4(kv_s + 8 * kRegion, tc::sw128_offset(e, 2 * sub + 1), rp[1]);
+  return row;
+}
+
+// Writes the 576 channels of SWA row `r` (or zeros) as entry e of the KV tile:
+// thread sub of the entry takes 16-byte chunks 18 sub .. 18 sub + 17.
+__device__ inline void swa_row_to_tile(const AttnArgs& a, uint8_t* kv_s, int b, int e, int sub, int64_t r) {
+  uint4 v[18];
+  const uint4* src = r >= 0 ? reinterpret_cast<const uint4*>(a.swa + (int64_t(b) * a.d.swa + r) * kDqk) : nullptr;
+#pragma unroll
+  for (int i = 0; i < 18; ++i) v[i] = src ? __ldg(src + sub * 18 + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int i = 0; i < 18; ++i) {
+    const int c = sub * 18 + i;                      // 16-byte chunk of the 576-channel row
+    st_shared_v4(kv_s, (c >> 3) * kRegion + tc::sw128_offset(e, c & 7), v[i]);
+  }
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    attn_pair_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
-                     const __grid_constant__ CUtensorMap swamap, int swa_tma_split) {
+    attn_cluster_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
+                        const __grid_constant__ CUtensorMap swamap, int swa_tma_chunk, int early) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* kv_s = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);   // nreg x 16 KB
-  uint8_t* q_s = kv_s + kPairKvBytes;               // nreg x 8 KB; later P^T hi / lo
-  float* sx = reinterpret_cast<float*>(q_s + kPairQBytes);   // [entry][head chunk], written by the partner
-  float* sx_out = sx + kEntries * kQRows;           // this CTA's partial, copied to the partner
-  __shared__ uint64_t bar_ld, bar_s, bar_o, bar_x, bar_ml, bar_zero;
-  __shared__ uint32_t tmem_slot;
-  __shared__ int64_t row_s[kEntries];               // >= 0 main row, -2 - r SWA row r, -1 empty
-  __shared__ __align__(16) float red_m[4][4][16];
-  __shared__ __align__(16) float red_l[4][4][16];
-  __shared__ float fac_s[kQRows];                   // 2^(m_chunk - M) / L per head
-  __shared__ __align__(16) float ml_all[kMaxClusterSplits][2][kQRows];   // every chunk's (m, l), base-2 m
-  __shared__ __align__(16) float ml_mine[2][kQRows];                      // this chunk's, copied to all
-  __shared__ bool ml_ok, z_ok;
+  uint8_t* kv_s = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);   // 9 x 16 KB
+  uint8_t* q_s = kv_s + kKvBytes;                    // 9 x 4 KB; later P^T hi / lo
+  ClusterSmall& sm = *reinterpret_cast<ClusterSmall*>(q_s + kCQBytes);
 
   cg::cluster_group cl = cg::this_cluster();
-  const int rank = int(cl.block_rank()), csize = int(cl.num_blocks());
-  const int chunk = rank >> 1, half = rank & 1, S = csize >> 1;
-  const int b = blockIdx.y;
+  const int chunk = int(cl.block_rank()), S = int(cl.num_blocks());
+  const int nhg = (a.d.heads + kCHeads - 1) / kCHeads;
+  const int b = blockIdx.y / nhg, hg = blockIdx.y % nhg;
   const int H = a.d.heads, K = a.d.topk, W = a.d.swa;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int nreg = half ? 5 : 4, reg0 = 4 * half;   // this CTA's regions of 64 channels (of 9)
   const bool paged = a.page_table != nullptr;
-  const bool swa_tma = chunk == swa_tma_split;      // this chunk's rows are the SWA window
-  // the chunk that finishes first (the TMA-loaded SWA window, else chunk 0)
-  // zeroes the output and tells the other chunks of its half when it has
-  const bool zero_cta = chunk == (swa_tma_split >= 0 ? swa_tma_split : 0);
-  // set-up that touches no global memory, then wait for the previous kernel
-  if (wid == 0) tc::tmem_alloc(&tmem_slot, kPairTmemCols);
+  const bool swa_tma = chunk == swa_tma_chunk;      // this chunk's rows are the SWA window
+  const bool lse_cta = chunk == 0;                   // writes the head group's lse
+  const int h0 = hg * kCHeads, nh = min(kCHeads, H - h0);
+  // ---- set-up that touches no global memory -----------------------------------------
+  if (wid == 0) tc::tmem_alloc(&sm.tmem_slot, kCTmemCols);
   if (tid == 0) {
-    tc::mbar_init(&bar_ld, 1);
-    tc::mbar_init(&bar_s, 1);
-    tc::mbar_init(&bar_o, 1);
-    tc::mbar_init(&bar_x, 1);                        // the partner's S^T partial (32 KB)
-    tc::mbar_init(&bar_ml, 1);                       // every chunk's (m, l) (S x 512 bytes)
-    tc::mbar_init(&bar_zero, 1);                     // the zeroing chunk of this half is done
+    for (int kb = 0; kb < 9; ++kb) tc::mbar_init(&sm.bar_q[kb], 1);
+    tc::mbar_init(&sm.bar_s, 1);
+    tc::mbar_init(&sm.bar_o, 1);
+    tc::mbar_init(&sm.bar_ml, 1);                    // every chunk's (m, l): S x 256 bytes
+    tc::mbar_init(&sm.bar_zero, S > 1 ? S - 1 : 1);  // the other chunks have zeroed their rows
     tc::fence_mbar_init();
-    // this CTA's own arrivals; the copies of the other CTAs bring the bytes
-    tc::mbar_expect_tx(&bar_x, uint32_t(kSxBytes));
-    tc::mbar_expect_tx(&bar_ml, uint32_t(S) * uint32_t(sizeof(ml_mine)));
+    tc::mbar_expect_tx(&sm.bar_ml, uint32_t(S) * uint32_t(sizeof(sm.ml_mine)));
   }
+  __syncwarp();
   // every CTA of the cluster must have started before another writes into
   // its shared memory: arrive now, wait before the first such write
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  // ---- the chunk's main-KV entries: before the wait in Reuse mode -----------------
+  int64_t row = -1;
+  if (early) row = cluster_gather(a, kv_s, b, chunk, checked_ctx(a.ctx_len, a.d, b, paged, a.ws), tid, swa_tma);
   pdl_wait();
   pdl_launch_dependents();
-  // ---- loads that depend on nothing earlier in this kernel go out first:
-  //      this half's query channels (and the window's rows) by TMA, the
-  //      chunk's Top-K indices and the lengths ---------------------------------------
   if (tid == 0) {
-    tc::mbar_expect_tx(&bar_ld, uint32_t(nreg) * (uint32_t(kQRegion) + (swa_tma ? uint32_t(kRegion) : 0u)));
-    for (int kb = 0; kb < nreg; ++kb)
-      tc::tma_load_2d(&qmap, q_s + kb * kQRegion, 64 * (reg0 + kb), b * H, &bar_ld);
-    if (swa_tma)
-      for (int kb = 0; kb < nreg; ++kb)
-        tc::tma_load_2d(&swamap, kv_s + kb * kRegion, 64 * (reg0 + kb), b * W, &bar_ld);
+    // the query of this head group (9 boxes of 64 channels x 32 heads) and,
+    // for the window's chunk, its rows (9 boxes of 64 channels x 128 rows):
+    // box kb completes on bar_q[kb], so the S MMAs start with the first box
+    for (int kb = 0; kb < 9; ++kb) {
+      tc::mbar_expect_tx(&sm.bar_q[kb], uint32_t(kCQRegion) + (swa_tma ? uint32_t(kRegion) : 0u));
+      tc::tma_load_2d(&qmap, q_s + kb * kCQRegion, 64 * kb, b * H + h0, &sm.bar_q[kb]);
+      if (swa_tma) tc::tma_load_2d(&swamap, kv_s + kb * kRegion, 64 * kb, b * W, &sm.bar_q[kb]);
+    }
   }
-  auto topk_at = [&](int e) -> int32_t {
-    const int slot = chunk * kEntries + e;
-    return slot < K ? __ldg(a.topk + int64_t(b) * K + slot) : -1;
-  };
-  const int eg = tid >> 3;                          // this thread's gather entries: eg, eg + 64
-  int32_t tg0 = -1, tg1 = -1;
-  if (!swa_tma) {
-    tg0 = topk_at(eg);
-    tg1 = topk_at(eg + 64);
-  }
-  const int32_t trow = tid < kEntries ? topk_at(tid) : -1;
+  if (!early) row = cluster_gather(a, kv_s, b, chunk, checked_ctx(a.ctx_len, a.d, b, paged, a.ws), tid, swa_tma);
   int swl = __ldg(a.swa_len + b);
-  const int64_t n_ctx = checked_ctx(a.ctx_len, a.d, b, paged, a.ws);
   if (swl < 0 || swl > W) {
-    if (tid == 0 && half == 0) raise_err(a.ws, CSA2_DEV_SWA_LEN);
+    if (tid == 0 && chunk == 0 && hg == 0) raise_err(a.ws, CSA2_DEV_SWA_LEN);
     swl = swl < 0 ? 0 : W;
   }
-  if (tid < kEntries) row_s[tid] = entry_row(a, b, chunk * kEntries + tid, trow, n_ctx, swl, true);
-  // ---- FP4 entries: gather (all loads first), dequantize to bf16 -------------------
-  if (!swa_tma) {
-    // latent: task = (entry, pair of 16-channel groups of this half); rope
-    // (half 1): task = (entry, 16-byte chunk); entries eg and eg + 64
-    const int64_t rr[2] = {entry_row(a, b, chunk * kEntries + eg, tg0, n_ctx, swl, false),
-                           entry_row(a, b, chunk * kEntries + eg + 64, tg1, n_ctx, swl, false)};
-    const int gp = 8 * half + (tid & 7), rc = tid & 7;
-    uint4 cd[2], rp[2];
-    uint32_t sc[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      cd[k] = make_uint4(0, 0, 0, 0);
-      rp[k] = make_uint4(0, 0, 0, 0);
-      sc[k] = 0;
-      if (rr[k] >= 0) {
-        cd[k] = __ldg(reinterpret_cast<const uint4*>(a.codes + rr[k] * kCodesPerRow) + gp);
-        sc[k] = __ldg(reinterpret_cast<const uint16_t*>(a.scales + rr[k] * kScalesPerRow) + gp);
-        if (half) rp[k] = __ldg(reinterpret_cast<const uint4*>(a.rope + rr[k] * kRope) + rc);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int e = eg + 64 * k;
-      if (rr[k] <= -2) continue;                     // SWA row: copied below
-      uint32_t cw[4] = {cd[k].x, cd[k].y, cd[k].z, cd[k].w};
-#pragma unroll
-      for (int g = 0; g < 2; ++g) {                  // two 16-channel groups
-        float s = e4m3_to_f32((sc[k] >> (8 * g)) & 0xFF);
-        uint32_t w[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint32_t h2 = e2m1x2_to_f16x2_a((cw[2 * g + (i >> 2)] >> (8 * (i & 3))) & 0xFF);
-          float lo = __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF))) * s;
-          float hi = __half2float(__ushort_as_half(uint16_t(h2 >> 16))) * s;
-          w[i] = pack_bf16x2(lo, hi);
-        }
-        const int part = 2 * gp + g;                 // 16-channel group index 0..31
-        const uint32_t region = (part >> 2) - reg0, ch0 = (part & 3) * 2;
-        st_shared_v4(kv_s, region * kRegion + tc::sw128_offset(e, ch0), make_uint4(w[0], w[1], w[2], w[3]));
-        st_shared_v4(kv_s, region * kRegion + tc::sw128_offset(e, ch0 + 1), make_uint4(w[4], w[5], w[6], w[7]));
-      }
-      if (half) st_shared_v4(kv_s, 4 * kRegion + tc::sw128_offset(e, rc), rp[k]);
-    }
+  // entry slot e holds an entry: a main row, or an SWA row below swa_len
+  const bool has = row >= 0 || (row <= -2 && -2 - row < swl);
+  {
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, has);
+    if (tid < kCEntries && lane == 0) sm.valid[tid >> 5] = m;
   }
+  {
+    // this chunk's share of the head group's output rows: zeros
+    const int z0 = nh * chunk / S, z1 = nh * (chunk + 1) / S;
+    float4* orow = reinterpret_cast<float4*>(a.out + (int64_t(b) * H + h0 + z0) * kLatent);
+    for (int i = tid; i < (z1 - z0) * 128; i += kAttnThreads) orow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // SWA rows of a chunk the window does not start on a 128-row boundary for
+  if (!swa_tma && row <= -2) swa_row_to_tile(a, kv_s, b, tid & (kCEntries - 1), tid >> 7, has ? -2 - row : -1);
+  __syncthreads();
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA has started
+  // the zeros happen before every later reduce-add of this head group
+  if (S > 1 && tid < S && tid != chunk) mbar_arrive_remote(cluster_addr(&sm.bar_zero, uint32_t(tid)));
+  __syncwarp();
+  tc::fence_proxy_async_smem();
   tc::tc_fence_before_sync();
   __syncthreads();
   tc::tc_fence_after_sync();
-  const uint32_t tmem = tmem_slot;
-  if (!swa_tma) {
-    // SWA rows of a chunk the window does not start on a 128-row boundary for
-    const int nch = nreg * 8, c0 = reg0 * 8;          // this half's 16-byte chunks of a row
-#pragma unroll 4
-    for (int task = tid; task < kEntries * nch; task += kAttnThreads) {
-      const int e = task / nch, c = task % nch;
-      const int64_t r = row_s[e];
-      if (r > -2) continue;
-      uint4 v = __ldg(reinterpret_cast<const uint4*>(a.swa + (int64_t(b) * W + (-2 - r)) * kDqk) + c0 + c);
-      st_shared_v4(kv_s, (c >> 3) * kRegion + tc::sw128_offset(e, c & 7), v);
+  const uint32_t tmem = sm.tmem_slot;
+
+  // ---- S^T = KV . Q^T, box by box as the query lands --------------------------------------
+  const uint32_t kv_addr = tc::smem_u32(kv_s), q_addr = tc::smem_u32(q_s);
+  bool ok = true;
+  if (tid == 0) {
+    constexpr uint32_t idS = tc::idesc_bf16(kCEntries, kCHeads, 0, 0);
+    const uint64_t ad0 = tc::smem_desc(kv_addr, 16, 1024, 2), bd0 = tc::smem_desc(q_addr, 16, 1024, 2);
+    for (int kb = 0; kb < 9; ++kb) {
+      ok = tc::mbar_wait_bounded(&sm.bar_q[kb], 0) && ok;
+      tc::tc_fence_after_sync();
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {                 // K step 4 kb + k4 into accumulator k4
+        const uint32_t off = uint32_t(kb * kRegion + k4 * 32), qoff = uint32_t(kb * kCQRegion + k4 * 32);
+        tc::mma_bf16(tmem + uint32_t(k4 * kCHeads), ad0 + (off >> 4), bd0 + (qoff >> 4), idS, kb > 0);
+      }
+    }
+    tc::mma_commit(&sm.bar_s);
+  }
+  __syncwarp();
+  ok = tc::mbar_wait_bounded(&sm.bar_s, 0) && ok;
+  tc::tc_fence_after_sync();
+  if (swa_tma && !has) {
+    // window rows past swa_len (or past W) are not entries: their scores are
+    // masked; zero their values so that P = 0 never meets a non-finite value
+    const int e = tid & (kCEntries - 1), sub = tid >> 7;
+#pragma unroll
+    for (int i = 0; i < 18; ++i) {
+      const int c = sub * 18 + i;
+      st_shared_v4(kv_s, (c >> 3) * kRegion + tc::sw128_offset(e, c & 7), make_uint4(0, 0, 0, 0));
     }
   }
-  if (zero_cta) {
-    for (int i = tid; i < H * 64; i += kAttnThreads) {
-      const int h = i >> 6, q = i & 63;
-      reinterpret_cast<float4*>(a.out + (int64_t(b) * H + h) * kLatent + half * 256)[q] =
-          make_float4(0.f, 0.f, 0.f, 0.f);
+
+  // ---- softmax over the 128 entries (TMEM lanes): 16 warps, 8 heads each ---------------
+  const int quarter = wid & 3, oct = wid >> 2;       // lanes 32 quarter.., heads 8 oct..
+  const int e = quarter * 32 + lane;
+  uint8_t* p_s = q_s;                                // the query is no longer read (S^T done)
+  {
+    float x[8];
+    {
+      const uint32_t ta = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(oct * 8);
+      float x1[8], x2[8], x3[8];
+      tc::tmem_ld8(ta, x);
+      tc::tmem_ld8(ta + kCHeads, x1);
+      tc::tmem_ld8(ta + 2 * kCHeads, x2);
+      tc::tmem_ld8(ta + 3 * kCHeads, x3);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = (x[j] + x1[j]) + (x2[j] + x3[j]);
+    }
+    const bool v_e = (sm.valid[e >> 5] >> (e & 31)) & 1;
+    const float c2 = a.scale * 1.4426950408889634f;   // logits in base 2
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = v_e ? x[j] * c2 : -INFINITY;
+    {
+      float mx[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mx[j]) : "f"(x[j]));
+      if (lane == 0) {
+        float4* dst = reinterpret_cast<float4*>(&sm.red_m[oct][quarter][0]);
+        dst[0] = make_float4(mx[0], mx[1], mx[2], mx[3]);
+        dst[1] = make_float4(mx[4], mx[5], mx[6], mx[7]);
+      }
     }
     __syncthreads();
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA has started
-    // the zeros happen before every later reduce-add of this half
-    if (tid < csize && (tid & 1) == half && (tid >> 1) != chunk)
-      mbar_arrive_remote(cluster_addr(&bar_zero, uint32_t(tid)));
-  }
-  bool ok = tc::mbar_wait_bounded(&bar_ld, 0);
-  if (swa_tma) {
-    // window rows past swa_len (or past W) are not entries: zero them so that
-    // P = 0 never meets a non-finite value
-    const int nch = nreg * 8;
-    for (int task = tid; task < kEntries * nch; task += kAttnThreads) {
-      const int e = task / nch, c = task % nch;
-      if (row_s[e] == -1) st_shared_v4(kv_s, (c >> 3) * kRegion + tc::sw128_offset(e, c & 7), make_uint4(0, 0, 0, 0));
+    float p[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float Mj = fmaxf(fmaxf(sm.red_m[oct][0][j], sm.red_m[oct][1][j]),
+                             fmaxf(sm.red_m[oct][2][j], sm.red_m[oct][3][j]));
+      p[j] = (Mj == -INFINITY || x[j] == -INFINITY) ? 0.0f : exp2f(x[j] - Mj);
+    }
+    const float l = butterfly8<false>(p, lane);
+    if ((lane & 3) == 0) sm.red_l[oct][quarter][octet_index(lane)] = l;
+    // P^T[row][entry], K-major in two regions of 64 entries: row h the hi
+    // bf16 part of head h, row 32 + h its lo part (2-byte stores: the 32
+    // lanes write 64 consecutive bytes of a row)
+    uint8_t* reg = p_s + (e >> 6) * kCPRegion;
+    const uint32_t ch = uint32_t((e >> 3) & 7), el = uint32_t(e & 7) * 2;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int h = oct * 8 + j;
+      const uint32_t hb = pack_bf16x2(p[j], 0.0f);
+      const float hv = __uint_as_float(hb << 16);
+      *reinterpret_cast<uint16_t*>(reg + tc::sw128_offset(uint32_t(h), ch) + el) = uint16_t(hb & 0xFFFF);
+      *reinterpret_cast<uint16_t*>(reg + tc::sw128_offset(uint32_t(kCHeads + h), ch) + el) =
+          uint16_t(pack_bf16x2(p[j] - hv, 0.0f) & 0xFFFF);
     }
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before_sync();
   __syncthreads();
-
-  // ---- S^T partial = KV_half . Q_half^T ------------------------------------------
-  const uint32_t kv_addr = tc::smem_u32(kv_s), q_addr = tc::smem_u32(q_s);
-  if (tid == 0) {
-    tc::tc_fence_after_sync();
-    constexpr uint32_t idS = tc::idesc_bf16(kEntries, kQRows, 0, 0);
-    // descriptors are formed once; an offset of x bytes adds x/16 to the
-    // start-address field (the operands lie below 256 KB, so it never carries)
-    const uint64_t ad0 = tc::smem_desc(kv_addr, 16, 1024, 2), bd0 = tc::smem_desc(q_addr, 16, 1024, 2);
-#pragma unroll
-    for (int ks = 0; ks < 16; ++ks) {
-      const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-      tc::mma_bf16(tmem, ad0 + ((kb * kRegion + off) >> 4), bd0 + ((kb * kQRegion + off) >> 4), idS, ks > 0);
-    }
-    if (half) {
-#pragma unroll
-      for (int ks = 16; ks < 20; ++ks) {
-        const uint32_t kb = ks >> 2, off = (ks & 3) * 32;
-        tc::mma_bf16(tmem, ad0 + ((kb * kRegion + off) >> 4), bd0 + ((kb * kQRegion + off) >> 4), idS, true);
-      }
-    }
-    tc::mma_commit(&bar_s);
-  }
-  ok = tc::mbar_wait_bounded(&bar_s, 0) && ok;
   tc::tc_fence_after_sync();
 
-  // ---- exchange the S^T partials within the pair ----------------------------------
-  const int quarter = wid & 3, hg = wid >> 2;       // lanes 32*quarter.., heads 16*hg..
-  const int e = quarter * 32 + lane;
-  const bool valid = row_s[e] != -1;
-  float x[16];
-  tc::tmem_ld16(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(hg * 16), x);
-  if (!zero_cta) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA has started
-  // Each warp's part (its 32 rows x 16 heads) is one contiguous 2 KB block
-  // of sx_out (block wid; the 16-byte slot i of lane l at 4l + (i ^ s_l),
-  // s_l = (l >> 1) & 3, so that 8 consecutive lanes cover all banks), sent by
-  // the warp itself as one bulk copy into the same block of the partner's sx
-  // (the partner's warp wid holds the same rows and heads).
-  const int sw = (lane >> 1) & 3;
-  {
-    float4* blk = reinterpret_cast<float4*>(sx_out) + wid * 128;
+  // ---- O^T = V^T . [P_hi | P_lo]^T  (4 M-tiles of 128 dims, N = 64, K = 128) -------------
+  if (tid == 0) {
+    constexpr uint32_t idO = tc::idesc_bf16(kCEntries, 2 * kCHeads, 1, 0);
+    const uint64_t bp0 = tc::smem_desc(tc::smem_u32(p_s), 16, 1024, 2);
+    const uint64_t av0 = tc::smem_desc(kv_addr, kRegion, 1024, 2);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      blk[lane * 4 + (i ^ sw)] = make_float4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+    for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)                 // consecutive MMAs: different accumulators
+        tc::mma_bf16(tmem + kCOCol + 64 * mt, av0 + (((2 * mt) * kRegion + ks * 2048) >> 4),
+                     bp0 + (((ks >> 2) * kCPRegion + (ks & 3) * 32) >> 4), idO, ks > 0);
+    }
+    tc::mma_commit(&sm.bar_o);
+  }
+  __syncwarp();
+  // this chunk's (m, l) per head, copied into every CTA of the cluster by
+  // warp 1 while thread 0 issues the O MMAs
+  if (wid == 1) {
+    const int o8 = lane >> 3, j = lane & 7;
+    sm.ml_mine[0][lane] = fmaxf(fmaxf(sm.red_m[o8][0][j], sm.red_m[o8][1][j]),
+                                fmaxf(sm.red_m[o8][2][j], sm.red_m[o8][3][j]));
+    sm.ml_mine[1][lane] = (sm.red_l[o8][0][j] + sm.red_l[o8][1][j]) + (sm.red_l[o8][2][j] + sm.red_l[o8][3][j]);
     tc::fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) {
-      const float4* peer_blk = reinterpret_cast<const float4*>(sx) + wid * 128;   // the partner's sx, same block
-      bulk_to_peer(cluster_addr(peer_blk, uint32_t(rank ^ 1)), blk, 2048u, cluster_addr(&bar_x, uint32_t(rank ^ 1)));
+    if (lane < S) {
+      bulk_to_peer(cluster_addr(&sm.ml_all[chunk][0][0], uint32_t(lane)), &sm.ml_mine[0][0],
+                   uint32_t(sizeof(sm.ml_mine)), cluster_addr(&sm.bar_ml, uint32_t(lane)));
       asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     }
-  }
-  // every thread waits for the partner's 16 blocks itself
-  ok = mbar_wait_cluster(&bar_x, 0) && ok;
-  {
-    const float4* src = reinterpret_cast<const float4*>(sx) + wid * 128;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 v = src[lane * 4 + (i ^ sw)];
-      // own + partner: the same sum in both CTAs (fp32 addition commutes)
-      x[4 * i] += v.x; x[4 * i + 1] += v.y; x[4 * i + 2] += v.z; x[4 * i + 3] += v.w;
-    }
+    __syncwarp();
   }
 
-  // ---- softmax over the 128 entries (TMEM lanes), identical in both halves ---------
-  const float c2 = a.scale * 1.4426950408889634f;   // logits in base 2
-#pragma unroll
-  for (int j = 0; j < 16; ++j) x[j] = valid ? x[j] * c2 : -INFINITY;
-  {
-    const float m = butterfly16<true>(x, lane);
-    if ((lane & 1) == 0) red_m[hg][quarter][butterfly_index(lane)] = m;
-  }
+  // ---- merge over the cluster ------------------------------------------------------------
+  if (tid == 32) sm.ok_ml = mbar_wait_cluster(&sm.bar_ml, 0);
+  if (tid == 64) sm.ok_z = S == 1 || mbar_wait_cluster(&sm.bar_zero, 0);
   __syncthreads();
-  float p[16];
-#pragma unroll
-  for (int j4 = 0; j4 < 4; ++j4) {
-    float4 m4[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) m4[q] = reinterpret_cast<const float4*>(&red_m[hg][q][0])[j4];
-    const float Mj[4] = {fmaxf(fmaxf(m4[0].x, m4[1].x), fmaxf(m4[2].x, m4[3].x)),
-                         fmaxf(fmaxf(m4[0].y, m4[1].y), fmaxf(m4[2].y, m4[3].y)),
-                         fmaxf(fmaxf(m4[0].z, m4[1].z), fmaxf(m4[2].z, m4[3].z)),
-                         fmaxf(fmaxf(m4[0].w, m4[1].w), fmaxf(m4[2].w, m4[3].w))};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int j = 4 * j4 + i;
-      p[j] = (Mj[i] == -INFINITY || x[j] == -INFINITY) ? 0.0f : exp2f(x[j] - Mj[i]);
-    }
-  }
-  {
-    const float l = butterfly16<false>(p, lane);
-    if ((lane & 1) == 0) red_l[hg][quarter][butterfly_index(lane)] = l;
-  }
-  // P^T rows (entry e) as bf16 hi and lo parts; the query buffer is free (the
-  // S^T MMAs completed before this)
-  uint8_t* p_hi = q_s;
-  uint8_t* p_lo = q_s + kRegion;
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    uint32_t wh[4], wl[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float v0 = p[8 * t + 2 * i], v1 = p[8 * t + 2 * i + 1];
-      uint32_t hb = pack_bf16x2(v0, v1);
-      float h0 = __uint_as_float(hb << 16), h1 = __uint_as_float(hb & 0xFFFF0000u);
-      wh[i] = hb;
-      wl[i] = pack_bf16x2(v0 - h0, v1 - h1);
-    }
-    uint32_t off = tc::sw128_offset(e, hg * 2 + t);
-    st_shared_v4(p_hi, off, make_uint4(wh[0], wh[1], wh[2], wh[3]));
-    st_shared_v4(p_lo, off, make_uint4(wl[0], wl[1], wl[2], wl[3]));
-  }
-  tc::fence_proxy_async_smem();
-  tc::tc_fence_before_sync();
-  __syncthreads();
-
-  // ---- O^T = V_half^T . P^T  (this half's 2 M-tiles of 128 dims; hi and lo) --------
-  if (tid == 0) {
-    tc::tc_fence_after_sync();
-    constexpr uint32_t idO = tc::idesc_bf16(kEntries, kQRows, 1, 1);
-    const uint64_t av0 = tc::smem_desc(kv_addr, kRegion, 1024, 2);
-    const uint64_t bp0[2] = {tc::smem_desc(tc::smem_u32(p_hi), kRegion, 1024, 2),
-                             tc::smem_desc(tc::smem_u32(p_lo), kRegion, 1024, 2)};
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          tc::mma_bf16(tmem + 64 + 64 * mt, av0 + (((2 * mt) * kRegion + ks * 2048) >> 4),
-                       bp0[part] + ((ks * 2048) >> 4), idO, part > 0 || ks > 0);
-      }
-    }
-    tc::mma_commit(&bar_o);
-  }
-  // this chunk's (m, l) per head: half 0 copies it into every CTA of the cluster
-  if (half == 0 && quarter == 0) {
-    if (lane < 16) {
-      const int h = hg * 16 + lane;
-      ml_mine[0][h] = fmaxf(fmaxf(red_m[hg][0][lane], red_m[hg][1][lane]), fmaxf(red_m[hg][2][lane], red_m[hg][3][lane]));
-      ml_mine[1][h] = red_l[hg][0][lane] + red_l[hg][1][lane] + red_l[hg][2][lane] + red_l[hg][3][lane];
-    }
-    tc::fence_proxy_async_smem();
-    asm volatile("bar.sync 2, 128;" ::: "memory");   // the 4 warps of quarter 0
-    if (wid == 0 && lane < csize) {
-      bulk_to_peer(cluster_addr(&ml_all[chunk][0][0], uint32_t(lane)), &ml_mine[0][0], uint32_t(sizeof(ml_mine)),
-                   cluster_addr(&bar_ml, uint32_t(lane)));
-      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    }
-  }
-
-  // ---- merge over the cluster -------------------------------------------------------
-  if (tid == 32) ml_ok = mbar_wait_cluster(&bar_ml, 0);     // every chunk's (m, l)
-  if (tid == 64) z_ok = zero_cta || mbar_wait_cluster(&bar_zero, 0);
-  __syncthreads();
-  ok = ml_ok && z_ok && ok;
-  if (tid < kQRows) {
-    float mr[kMaxClusterSplits], lr[kMaxClusterSplits];
+  ok = sm.ok_ml && sm.ok_z && ok;
+  if (tid < kCHeads) {
     float M = -INFINITY;
-#pragma unroll
-    for (int r = 0; r < kMaxClusterSplits; ++r) {
-      mr[r] = (r < S && tid < H) ? ml_all[r][0][tid] : -INFINITY;
-      lr[r] = (r < S && tid < H) ? ml_all[r][1][tid] : 0.0f;
-      M = fmaxf(M, mr[r]);
-    }
+    for (int r = 0; r < S; ++r) M = fmaxf(M, sm.ml_all[r][0][tid]);
     float L = 0.0f;
-#pragma unroll
-    for (int r = 0; r < kMaxClusterSplits; ++r)
-      if (mr[r] != -INFINITY) L += lr[r] * exp2f(mr[r] - M);
-    float ms = -INFINITY;
-#pragma unroll
-    for (int r = 0; r < kMaxClusterSplits; ++r) ms = r == chunk ? mr[r] : ms;
-    fac_s[tid] = (ms == -INFINITY || !(L > 0.0f)) ? 0.0f : exp2f(ms - M) / L;
-    if (rank == 0 && tid < H)
-      a.lse[int64_t(b) * H + tid] = L > 0.0f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
+    for (int r = 0; r < S; ++r) {
+      const float mr = sm.ml_all[r][0][tid];
+      if (mr != -INFINITY) L += sm.ml_all[r][1][tid] * exp2f(mr - M);
+    }
+    const float ms = sm.ml_all[chunk][0][tid];
+    sm.fac[tid] = (ms == -INFINITY || !(L > 0.0f)) ? 0.0f : exp2f(ms - M) / L;
+    if (lse_cta && tid < nh)
+      a.lse[int64_t(b) * H + h0 + tid] = L > 0.0f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
   }
-  ok = tc::mbar_wait_bounded(&bar_o, 0) && ok;
+  ok = tc::mbar_wait_bounded(&sm.bar_o, 0) && ok;
   tc::tc_fence_after_sync();
   __syncthreads();
   if (!ok && tid == 0) raise_err(a.ws, CSA2_DEV_TIMEOUT);
-  // scaled O^T added into this half's output dimensions straight from tensor
-  // memory: for one head the 32 lanes of a warp hold 32 consecutive dims
+  // scaled O (hi + lo parts) added into the output straight from tensor
+  // memory: for one head a warp's 32 lanes hold 32 consecutive dims
+  float* dst0 = a.out + (int64_t(b) * H + h0) * kLatent + quarter * 32 + lane;
 #pragma unroll 1
-  for (int mt = 0; mt < 2; ++mt) {
-    float o[16];
-    tc::tmem_ld16(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(64 + 64 * mt + hg * 16), o);
-    float* dst = a.out + int64_t(b) * H * kLatent + half * 256 + mt * 128 + quarter * 32 + lane;
+  for (int mt = 0; mt < 4; ++mt) {
+    float hi[8], lo[8];
+    const uint32_t ta = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(kCOCol + 64 * mt + oct * 8);
+    tc::tmem_ld8(ta, hi);
+    tc::tmem_ld8(ta + kCHeads, lo);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int h = hg * 16 + j;
-      if (h < H)
-        asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst + int64_t(h) * kLatent), "f"(o[j] * fac_s[h])
+    for (int j = 0; j < 8; ++j) {
+      const int hh = oct * 8 + j;
+      if (hh < nh)
+        asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst0 + int64_t(hh) * kLatent + mt * 128),
+                     "f"((hi[j] + lo[j]) * sm.fac[hh])
                      : "memory");
     }
   }
   tc::tc_fence_before_sync();
   __syncthreads();
-  if (wid == 0) tc::tmem_dealloc(tmem, kPairTmemCols);
-  // the bulk copies this thread committed (a warp's sx_out block, warp 0's
-  // ml_mine copies) have read their source before the CTA exits
+  tc::tc_fence_after_sync();
+  if (wid == 0) tc::tmem_dealloc(tmem, kCTmemCols);
+  // warp 1's (m, l) copies have read their shared source before the CTA exits
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
@@ -882,28 +892,39 @@ static bool encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, u
 }
 
 cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
-  CUtensorMap qmap, swamap;
-  if (!encode_rows_map(&qmap, a.q, uint64_t(a.batch) * a.d.heads, kQRows)) return cudaErrorInvalidValue;
-  // the window is loaded by TMA when it starts a 128-entry split
-  int swa_split = -1;
-  if (a.d.swa > 0 && a.d.swa <= kEntries && a.d.topk % kEntries == 0) swa_split = a.d.topk / kEntries;
-  swamap = qmap;
-  if (swa_split >= 0 &&
-      !encode_rows_map(&swamap, a.swa, uint64_t(a.batch) * a.d.swa, kEntries))
-    return cudaErrorInvalidValue;
-  size_t smem = attn_smem_bytes(a.d.heads);
+  const int H = a.d.heads, K = a.d.topk, W = a.d.swa;
   if (!attn_uses_partials(a.d)) {
-    // one cluster of 2 x chunks CTAs per sequence; the merge happens inside it
-    const size_t psmem = size_t(kPairKvBytes) + size_t(kPairQBytes) + 2 * size_t(kSxBytes) + 1024;
+    // one cluster of 128-entry chunks per (sequence, group of 32 heads)
+    const int chunks = a.L.splits;
+    const int nhg = (H + kCHeads - 1) / kCHeads;
+    CUtensorMap qmap, swamap;
+    if (!encode_rows_map(&qmap, a.q, uint64_t(a.batch) * H, kCHeads)) return cudaErrorInvalidValue;
+    // the window is loaded by TMA when it starts a 128-entry chunk
+    const int swa_chunk = (W > 0 && K % kCEntries == 0) ? K / kCEntries : -1;
+    swamap = qmap;
+    if (swa_chunk >= 0 && !encode_rows_map(&swamap, a.swa, uint64_t(a.batch) * W, kCEntries))
+      return cudaErrorInvalidValue;
+    const size_t smem = cluster_smem_bytes();
     static KernelAttrs done;
-    cudaError_t e = prepare_kernel(attn_pair_kernel, psmem, true, done);
+    cudaError_t e = prepare_kernel(attn_cluster_kernel, smem, false, done);
     if (e != cudaSuccess) return e;
-    CSA2_PROFILED(st, "attn_pair_tc",
-                  (e = launch_pdl(attn_pair_kernel, dim3(unsigned(2 * a.L.splits), unsigned(a.batch), 1),
-                                  dim3(kAttnThreads), psmem, st, unsigned(2 * a.L.splits), a, qmap, swamap,
-                                  swa_split)));
+    CSA2_PROFILED(st, "attn_cluster_tc",
+                  (e = launch_pdl(attn_cluster_kernel, dim3(unsigned(chunks), unsigned(nhg * a.batch), 1),
+                                  dim3(kAttnThreads), smem, st, unsigned(chunks), a, qmap, swamap, swa_chunk,
+                                  a.early)));
     return e;
   }
+  // more than 8 chunks: one CTA per 128-entry chunk writes partials,
+  // the combine kernel merges them
+  CUtensorMap qmap, swamap;
+  if (!encode_rows_map(&qmap, a.q, uint64_t(a.batch) * H, kQRows)) return cudaErrorInvalidValue;
+  // the window is loaded by TMA when it starts a 128-entry split
+  int swa_split = -1;
+  if (W > 0 && W <= kEntries && K % kEntries == 0) swa_split = K / kEntries;
+  swamap = qmap;
+  if (swa_split >= 0 && !encode_rows_map(&swamap, a.swa, uint64_t(a.batch) * W, kEntries))
+    return cudaErrorInvalidValue;
+  const size_t smem = attn_smem_bytes(H);
   static KernelAttrs done_partial;
   cudaError_t e = prepare_kernel(attn_partial_tc_kernel, smem, false, done_partial);
   if (e != cudaSuccess) return e;
@@ -911,7 +932,7 @@ cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
                 (e = launch_pdl(attn_partial_tc_kernel, dim3(unsigned(a.L.splits), unsigned(a.batch)),
                                 dim3(kAttnThreads), smem, st, 1, a, qmap, swamap, swa_split)));
   if (e != cudaSuccess) return e;
-  CSA2_PROFILED(st, "attn_combine", (e = launch_pdl(attn_combine_kernel, dim3(unsigned(a.d.heads), unsigned(a.batch)),
+  CSA2_PROFILED(st, "attn_combine", (e = launch_pdl(attn_combine_kernel, dim3(unsigned(H), unsigned(a.batch)),
                                                     dim3(128), 0, st, 1, a)));
   return e;
 }

@@ -53,10 +53,11 @@ __host__ __device__ inline int64_t max64(int64_t a, int64_t b) { return a > b ? 
 
 __host__ __device__ inline int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
-// Split-KV chunks of an attention call: ceil((K + W) / 128), at least 1.
-// Up to kMaxClusterSplits chunks are merged inside one thread-block cluster
-// (no scratch but the error word); more write partials that a combine kernel
-// merges (attn_o / attn_ml of the workspace).
+// Split-KV chunks of 128 entries of an attention call: ceil((K + W) / 128),
+// at least 1.  Calls with K + W <= 1024 (kMaxClusterSplits chunks of 128)
+// merge inside thread-block clusters and use no scratch but the error word;
+// larger ones write per-chunk partials that a combine kernel merges (attn_o /
+// attn_ml of the workspace).
 __host__ __device__ inline int attn_splits(const csa2_dims& d) {
   const int s = (d.topk + d.swa + kAttnChunk - 1) / kAttnChunk;
   return s < 1 ? 1 : s;

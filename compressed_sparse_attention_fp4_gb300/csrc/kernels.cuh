@@ -115,6 +115,7 @@ struct AttnArgs {
   float* lse;
   uint8_t* ws;
   WsLayout L;
+  int early;                   // Reuse mode: indices and main KV may be read before the wait
 };
 
 cudaError_t launch_quantize(const uint16_t* x, int64_t n, const int64_t* dst_rows, uint8_t* codes,

@@ -12,8 +12,8 @@
 //
 // The array is shared by every call on a device and keeps the previous call's
 // contents; the error word at its start is cleared by each call, the partial
-// outputs (used only when the entries span more than kMaxClusterSplits chunks
-// of 128) are fully rewritten before they are read.  Two calls whose work overlaps on the GPU
+// outputs (used only when Top-K + SWA exceeds 1024 entries) are fully
+// rewritten before they are read.  Two calls whose work overlaps on the GPU
 // (different streams, no ordering between them) race on the array.
 #include <mutex>
 
@@ -111,6 +111,7 @@ extern "C" csa2_status csa2_sparse_attn_decode_noalloc(
   a.lse = lse;
   a.ws = static_cast<uint8_t*>(scratch);
   a.L = L;
+  a.early = mode == CSA2_MODE_REUSE;
   if (launch_attention(a, cs) != cudaSuccess) return CSA2_ERR_CUDA;
   if (err_word) {
     publish_error_word<<<1, 1, 0, cs>>>(err_word);

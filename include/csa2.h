@@ -199,7 +199,15 @@ csa2_status indexer_reindex_topk(const csa2_dims* d, int32_t batch,
  *   entries, the SWA row (576) / its first 512 channels for SWA entries;
  *   logit = scale * q[b][h] . key(e);  out = softmax-weighted sum of values;
  *   lse = max logit + ln(sum exp(logit - max)); empty E: out 0, lse -inf.
- *   mode: csa2_mode, informational (indices are always supplied).
+ *   mode: csa2_mode.  Indices are always supplied.  CSA2_MODE_REUSE (the
+ *     layer keeps the KV and indices an earlier layer used) lets the call
+ *     start reading topk, ctx_len, page_table and the main-KV planes
+ *     (kv_codes, kv_scales, kv_rope) while the operation enqueued just before
+ *     it on the stream is still running: in this mode those buffers must not
+ *     be written by that operation (they were written by earlier work on the
+ *     stream, before it began).  q, swa_kv, swa_len, out and lse are always
+ *     accessed only after it has finished.  CSA2_MODE_FULL and
+ *     CSA2_MODE_REINDEX read nothing before it has finished.
  *   q:        device bf16 [B][H][576], 16-byte aligned
  *   kv_codes, kv_scales, kv_rope: device, layout above (16-, 2- and
  *             16-byte aligned)

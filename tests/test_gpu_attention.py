@@ -55,12 +55,15 @@ def check(p, topk_np, out, lse, swa_len=None):
 
 
 @pytest.mark.parametrize("paged", [False, True])
-def test_attention_random(paged):
+@pytest.mark.parametrize("mode", [csa2.MODE_REUSE, csa2.MODE_FULL])
+def test_attention_random(paged, mode):
+    """Reuse mode gathers the entries before waiting for the previous kernel;
+    Full (and Reindex) mode after it: both must give the oracle's result."""
     p = make_problem([100, 5000, 3000], paged=paged, seed=11)
     rng = np.random.default_rng(0)
     tk = random_topk(p, rng)
     sl = [0, 7, 128]
-    out, lse = run_attn(p, tk, sl)
+    out, lse = run_attn(p, tk, sl, mode=mode)
     check(p, tk, out, lse, sl)
 
 
@@ -104,11 +107,31 @@ def test_attention_more_than_eight_chunks():
     check(p, tk, out, lse)
 
 
-def test_attention_window_not_on_chunk_boundary():
-    """Top-448: the SWA window starts inside a chunk, so its rows are copied with
-    the FP4 entries of that chunk (both channel halves), not loaded by TMA."""
-    p = make_problem([5000, 300], K=448, seed=17)
+@pytest.mark.parametrize("mode", [csa2.MODE_REUSE, csa2.MODE_REINDEX])
+def test_attention_window_not_on_chunk_boundary(mode):
+    """Top-500: the SWA window starts inside a 128-entry chunk, so its rows are
+    copied with the FP4 entries of that chunk, not loaded by TMA."""
+    p = make_problem([5000, 300], K=500, seed=17)
     tk = random_topk(p, np.random.default_rng(5))
     sl = [128, 77]
+    out, lse = run_attn(p, tk, sl, mode=mode)
+    check(p, tk, out, lse, sl)
+
+
+def test_attention_window_tma_short_window():
+    """Top-384 (a multiple of 128) with a 100-row window: the window's chunk
+    comes by TMA, only partly inside the window."""
+    p = make_problem([5000, 60], K=384, W=100, seed=19)
+    tk = random_topk(p, np.random.default_rng(6))
+    sl = [100, 60]
     out, lse = run_attn(p, tk, sl)
     check(p, tk, out, lse, sl)
+
+
+def test_attention_48_heads_eight_chunks():
+    """48 heads (the second head group half full) and Top-896 + SWA-128 =
+    8 chunks of 128: the largest cluster."""
+    p = make_problem([9000, 1200], H=48, K=896, seed=20)
+    tk = random_topk(p, np.random.default_rng(7))
+    out, lse = run_attn(p, tk)
+    check(p, tk, out, lse)
