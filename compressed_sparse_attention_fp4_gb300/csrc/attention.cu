@@ -401,27 +401,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // head group) form a thread-block cluster (up to 8 CTAs) that merges them.
 // A CTA holds all 576 key channels of its 128 entries (144 KB of bf16) and
 // the query of its 32 heads (36 KB), so no partial scores are exchanged:
-//   * S^T[128 entries x 32 heads] = KV . Q^T (M = 128, N = 32, K = 576),
-//     issued box by box as the query's 64-channel boxes land, the K steps
-//     spread round-robin over 4 tensor-memory accumulators so that
-//     consecutive MMAs do not wait for each other's accumulation (the
-//     softmax adds the 4 partial sums);
+//   * S^T[128 entries x 32 heads] = KV . Q^T (M = 128, N = 32, K = 576), the
+//     K steps spread round-robin over 4 tensor-memory accumulators, each
+//     issued by its own thread (the softmax adds the 4 partial sums);
 //   * softmax over the 128 entries (TMEM lanes; 16 warps, 8 heads each);
 //   * P^T stored K-major as bf16 hi and lo parts side by side: rows 0..31
 //     hold the hi parts of the 32 heads, rows 32..63 the lo parts;
 //   * O^T[512 dims x (hi | lo) 64] = V^T . [P_hi | P_lo]^T: 4 M-tiles, N = 64,
-//     K = 128 (one instruction covers both parts), the tiles' MMAs issued
-//     interleaved;
+//     K = 128 (one instruction covers both parts), each tile's MMAs issued
+//     by its own thread;
 //   * merge: every chunk copies its (m, l) into every CTA of the cluster
-//     (warp 1, while thread 0 issues the O MMAs); every chunk zeroes its share
+//     (warp 1, while the O MMAs are issued); every chunk zeroes its share
 //     of the head group's output rows and signals the others; each CTA adds
 //     its scaled O (hi + lo) into the output with coalesced reduce-adds
 //     (red.global.add.f32) straight from tensor memory.
-// One CTA per SM (its shared memory), as every tensor-memory kernel of the
-// library.  In Reuse mode (the indices and the main-KV cache come from
-// earlier work on the stream) the Top-K indices are read and the entries
-// gathered and dequantized before griddepcontrol.wait; the query, the SWA
-// window and the outputs wait for the previous kernel.
+// Chunk c holds the Top-K slots [K c / S, K (c + 1) / S) and then window
+// rows up to 128 entries (the window filled into the chunks in order), so
+// that every CTA loads a share of the window.  One CTA per SM (its shared
+// memory), as every tensor-memory kernel of the library.  In Reuse mode (the
+// indices and the main-KV cache come from earlier work on the stream) the
+// Top-K indices are read and the entries gathered and dequantized before
+// griddepcontrol.wait; the query, the window and the outputs are read or
+// written only after it (an L2 prefetch of the query and window rows is
+// issued before it), with coalesced 16-byte loads by all threads.
 // ---------------------------------------------------------------------------
 constexpr int kCEntries = kEntries;                  // entry slots per CTA (= MMA M)
 constexpr int kCHeads = 32;                          // heads per CTA (MMA N)
@@ -435,7 +437,6 @@ static_assert(2 * kCPRegion <= kCQBytes, "P^T (two regions of 64 entries) fits t
 static_assert(kCOCol + 4 * 2 * kCHeads <= kCTmemCols, "tensor-memory columns");
 
 struct ClusterSmall {
-  uint64_t bar_q[9];                                 // query box kb (and window box kb) landed
   uint64_t bar_s, bar_o, bar_ml, bar_zero;
   uint32_t valid[kCEntries / 32];                    // bit e: entry slot e holds an entry
   uint32_t tmem_slot;
@@ -516,25 +517,24 @@ __device__ inline float butterfly8(const float (&v)[8], int lane) {
 // them, dequantized exactly to bf16, into the 128-byte swizzled KV tile:
 // entry e = tid % 128, channel regions 2 sub and 2 sub + 1 (sub = tid / 128:
 // latent channels 128 sub .. 128 sub + 127) and rope chunks 2 sub, 2 sub + 1.
-// Returns the entry's cache row (-1: no main entry; -2 - r: SWA row r, filled
-// later).
-__device__ inline int64_t cluster_gather(const AttnArgs& a, uint8_t* kv_s, int b, int chunk, int64_t n_ctx,
-                                         int tid, bool swa_tma) {
+// Entry e of chunk c is Top-K slot m0 + e for e < nm, window row w0 + e - nm
+// for nm <= e < nm + nw, else empty.  Returns the entry's cache row (-1: no
+// main entry, its tile row zeroed; -2 - r: window row r, written later).
+__device__ inline int64_t cluster_gather(const AttnArgs& a, uint8_t* kv_s, int b, int m0, int nm, int w0, int nw,
+                                         int64_t n_ctx, int tid) {
   const int e = tid & (kCEntries - 1), sub = tid >> 7;
-  const int K = a.d.topk, W = a.d.swa;
-  const int slot = chunk * kCEntries + e;
-  if (swa_tma) return slot < K + W ? -2 - int64_t(slot - K) : -1;   // the window's rows come by TMA
+  const int K = a.d.topk;
   int64_t row = -1;
-  if (slot < K) {
-    const int32_t t = __ldg(a.topk + int64_t(b) * K + slot);
+  if (e < nm) {
+    const int32_t t = __ldg(a.topk + int64_t(b) * K + m0 + e);
     if (t >= 0 && t < n_ctx) {
       row = kv_row(a.page_table, a.d, b, t, a.ws);
       if (row < 0) row = -1;
     } else if (sub == 0 && (t >= n_ctx || t < -1)) {
       raise_err(a.ws, CSA2_DEV_TOPK_IDX);
     }
-  } else if (slot < K + W) {
-    row = -2 - int64_t(slot - K);                    // SWA slot (length checked later)
+  } else if (e < nm + nw) {
+    return -2 - int64_t(w0 + e - nm);                // window row: written after the wait
   }
   uint4 cd[4], rp[2];
   uint32_t sc[2] = {0, 0};
@@ -553,7 +553,6 @@ __device__ inline int64_t cluster_gather(const AttnArgs& a, uint8_t* kv_s, int b
     rp[0] = __ldg(rq);
     rp[1] = __ldg(rq + 1);
   }
-  if (row <= -2) return row;                         // the SWA rows are written later
 #pragma unroll
   for (int r = 0; r < 2; ++r) {                      // region 2 sub + r: channels 64 (2 sub + r) ..
     const uint32_t cw[8] = {cd[2 * r].x, cd[2 * r].y, cd[2 * r].z, cd[2 * r].w,
@@ -577,23 +576,7 @@ __device__ inline int64_t cluster_gather(const AttnArgs& a, uint8_t* kv_s, int b
   return row;
 }
 
-// Writes the 576 channels of SWA row `r` (or zeros) as entry e of the KV tile:
-// thread sub of the entry takes 16-byte chunks 18 sub .. 18 sub + 17.
-__device__ inline void swa_row_to_tile(const AttnArgs& a, uint8_t* kv_s, int b, int e, int sub, int64_t r) {
-  uint4 v[18];
-  const uint4* src = r >= 0 ? reinterpret_cast<const uint4*>(a.swa + (int64_t(b) * a.d.swa + r) * kDqk) : nullptr;
-#pragma unroll
-  for (int i = 0; i < 18; ++i) v[i] = src ? __ldg(src + sub * 18 + i) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-  for (int i = 0; i < 18; ++i) {
-    const int c = sub * 18 + i;                      // 16-byte chunk of the 576-channel row
-    st_shared_v4(kv_s, (c >> 3) * kRegion + tc::sw128_offset(e, c & 7), v[i]);
-  }
-}
-
-__global__ void __launch_bounds__(kAttnThreads, 1)
-    attn_cluster_kernel(AttnArgs a, const __grid_constant__ CUtensorMap qmap,
-                        const __grid_constant__ CUtensorMap swamap, int swa_tma_chunk, int early) {
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_cluster_kernel(AttnArgs a, int early) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* kv_s = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);   // 9 x 16 KB
   uint8_t* q_s = kv_s + kKvBytes;                    // 9 x 4 KB; later P^T hi / lo
@@ -606,15 +589,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int H = a.d.heads, K = a.d.topk, W = a.d.swa;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const bool paged = a.page_table != nullptr;
-  const bool swa_tma = chunk == swa_tma_chunk;      // this chunk's rows are the SWA window
   const bool lse_cta = chunk == 0;                   // writes the head group's lse
   const int h0 = hg * kCHeads, nh = min(kCHeads, H - h0);
+  const int m0 = attn_chunk_main_lo(K, chunk, S), nm = attn_chunk_main_lo(K, chunk + 1, S) - m0;
+  int w0, nw;
+  attn_chunk_window(K, W, chunk, S, w0, nw);
   // ---- set-up that touches no global memory -----------------------------------------
   if (wid == 0) tc::tmem_alloc(&sm.tmem_slot, kCTmemCols);
   if (tid == 0) {
-    for (int kb = 0; kb < 9; ++kb) tc::mbar_init(&sm.bar_q[kb], 1);
-    tc::mbar_init(&sm.bar_s, 1);
-    tc::mbar_init(&sm.bar_o, 1);
+    tc::mbar_init(&sm.bar_s, kSAcc);                 // one commit per MMA-issuing thread
+    tc::mbar_init(&sm.bar_o, 4);
     tc::mbar_init(&sm.bar_ml, 1);                    // every chunk's (m, l): S x 256 bytes
     tc::mbar_init(&sm.bar_zero, S > 1 ? S - 1 : 1);  // the other chunks have zeroed their rows
     tc::fence_mbar_init();
@@ -626,80 +610,118 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   // ---- the chunk's main-KV entries: before the wait in Reuse mode -----------------
   int64_t row = -1;
-  if (early) row = cluster_gather(a, kv_s, b, chunk, checked_ctx(a.ctx_len, a.d, b, paged, a.ws), tid, swa_tma);
+  {
+    // L2 prefetch (a hint: nothing is read into the SM) of what is read right
+    // after the wait: the window length, this head group's query rows (36 KB)
+    // and this chunk's window rows; the reads themselves follow the wait
+    const char* qb = reinterpret_cast<const char*>(a.q + (int64_t(b) * H + h0) * kDqk);
+    const char* wb = reinterpret_cast<const char*>(a.swa + (int64_t(b) * W + w0) * kDqk);
+    const int qlines = (nh * kDqk * 2 + 127) / 128, wlines = (nw * kDqk * 2 + 127) / 128;
+    for (int i = tid; i < qlines + wlines; i += kAttnThreads) {
+      const char* pf = i < qlines ? qb + 128 * i : wb + 128 * (i - qlines);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(pf));
+    }
+    if (tid == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.swa_len + b));
+  }
+  if (early) row = cluster_gather(a, kv_s, b, m0, nm, w0, nw, checked_ctx(a.ctx_len, a.d, b, paged, a.ws), tid);
   pdl_wait();
   pdl_launch_dependents();
-  if (tid == 0) {
-    // the query of this head group (9 boxes of 64 channels x 32 heads) and,
-    // for the window's chunk, its rows (9 boxes of 64 channels x 128 rows):
-    // box kb completes on bar_q[kb], so the S MMAs start with the first box
-    for (int kb = 0; kb < 9; ++kb) {
-      tc::mbar_expect_tx(&sm.bar_q[kb], uint32_t(kCQRegion) + (swa_tma ? uint32_t(kRegion) : 0u));
-      tc::tma_load_2d(&qmap, q_s + kb * kCQRegion, 64 * kb, b * H + h0, &sm.bar_q[kb]);
-      if (swa_tma) tc::tma_load_2d(&swamap, kv_s + kb * kRegion, 64 * kb, b * W, &sm.bar_q[kb]);
-    }
-  }
-  if (!early) row = cluster_gather(a, kv_s, b, chunk, checked_ctx(a.ctx_len, a.d, b, paged, a.ws), tid, swa_tma);
+  // ---- after the wait: the window length, this head group's query (32 rows
+  //      x 576 channels, one contiguous 36 KB run) and this chunk's window rows
+  //      (nw contiguous rows), every load issued before any is used ---------------
   int swl = __ldg(a.swa_len + b);
-  if (swl < 0 || swl > W) {
-    if (tid == 0 && chunk == 0 && hg == 0) raise_err(a.ws, CSA2_DEV_SWA_LEN);
-    swl = swl < 0 ? 0 : W;
+  constexpr int kQVec = kCHeads * (kDqk / 8);        // 16-byte pieces of the query rows
+  constexpr int kQPer = (kQVec + kAttnThreads - 1) / kAttnThreads;
+  const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + (int64_t(b) * H + h0) * kDqk);
+  uint4 qv[kQPer];
+#pragma unroll
+  for (int k = 0; k < kQPer; ++k) {
+    const int i = tid + k * kAttnThreads;
+    qv[k] = (i < kQVec && i / (kDqk / 8) < nh) ? __ldg(qsrc + i) : make_uint4(0, 0, 0, 0);
   }
-  // entry slot e holds an entry: a main row, or an SWA row below swa_len
-  const bool has = row >= 0 || (row <= -2 && -2 - row < swl);
-  {
-    const uint32_t m = __ballot_sync(0xFFFFFFFFu, has);
-    if (tid < kCEntries && lane == 0) sm.valid[tid >> 5] = m;
+  constexpr int kWPer = 8;                           // window pieces per thread per batch
+  const int nwv = nw * (kDqk / 8);
+  const uint4* wsrc = reinterpret_cast<const uint4*>(a.swa + (int64_t(b) * W + w0) * kDqk);
+  uint4 wv[kWPer];
+#pragma unroll
+  for (int k = 0; k < kWPer; ++k) {
+    const int i = tid + k * kAttnThreads;
+    wv[k] = i < nwv ? __ldg(wsrc + i) : make_uint4(0, 0, 0, 0);
   }
+  if (!early) row = cluster_gather(a, kv_s, b, m0, nm, w0, nw, checked_ctx(a.ctx_len, a.d, b, paged, a.ws), tid);
   {
     // this chunk's share of the head group's output rows: zeros
     const int z0 = nh * chunk / S, z1 = nh * (chunk + 1) / S;
     float4* orow = reinterpret_cast<float4*>(a.out + (int64_t(b) * H + h0 + z0) * kLatent);
     for (int i = tid; i < (z1 - z0) * 128; i += kAttnThreads) orow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  // SWA rows of a chunk the window does not start on a 128-row boundary for
-  if (!swa_tma && row <= -2) swa_row_to_tile(a, kv_s, b, tid & (kCEntries - 1), tid >> 7, has ? -2 - row : -1);
-  __syncthreads();
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every CTA has started
-  // the zeros happen before every later reduce-add of this head group
-  if (S > 1 && tid < S && tid != chunk) mbar_arrive_remote(cluster_addr(&sm.bar_zero, uint32_t(tid)));
-  __syncwarp();
+  if (swl < 0 || swl > W) {
+    if (tid == 0 && chunk == 0 && hg == 0) raise_err(a.ws, CSA2_DEV_SWA_LEN);
+    swl = swl < 0 ? 0 : W;
+  }
+  // query pieces into the swizzled K-major tile [region][head row]
+#pragma unroll
+  for (int k = 0; k < kQPer; ++k) {
+    const int i = tid + k * kAttnThreads;
+    if (i < kQVec) {
+      const int h = i / (kDqk / 8), j = i % (kDqk / 8);
+      st_shared_v4(q_s, (j >> 3) * kCQRegion + tc::sw128_offset(h, j & 7), qv[k]);
+    }
+  }
+  // window rows as entries nm .. nm + nw - 1 (rows at or past swa_len:
+  // zeros); more than one batch only when a chunk holds over 56 window rows
+  for (int base = 0; base < nwv; base += kWPer * kAttnThreads) {
+    if (base > 0) {
+#pragma unroll
+      for (int k = 0; k < kWPer; ++k) {
+        const int i = base + tid + k * kAttnThreads;
+        wv[k] = i < nwv ? __ldg(wsrc + i) : make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kWPer; ++k) {
+      const int i = base + tid + k * kAttnThreads;
+      if (i < nwv) {
+        const int r = i / (kDqk / 8), j = i % (kDqk / 8);
+        st_shared_v4(kv_s, (j >> 3) * kRegion + tc::sw128_offset(nm + r, j & 7),
+                     w0 + r < swl ? wv[k] : make_uint4(0, 0, 0, 0));
+      }
+    }
+  }
+  // entry slot e holds an entry: a main row, or a window row below swa_len
+  const bool has = row >= 0 || (row <= -2 && -2 - row < swl);
+  {
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, has);
+    if (tid < kCEntries && lane == 0) sm.valid[tid >> 5] = m;
+  }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before_sync();
   __syncthreads();
   tc::tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_slot;
 
-  // ---- S^T = KV . Q^T, box by box as the query lands --------------------------------------
+  // ---- S^T = KV . Q^T: lane 0 of warps 0..3 each issues the 9 K steps of one
+  //      of 4 accumulators (K step 4 kb + k4 into accumulator k4) ----------------------
   const uint32_t kv_addr = tc::smem_u32(kv_s), q_addr = tc::smem_u32(q_s);
-  bool ok = true;
-  if (tid == 0) {
+  if (wid < kSAcc && lane == 0) {
     constexpr uint32_t idS = tc::idesc_bf16(kCEntries, kCHeads, 0, 0);
     const uint64_t ad0 = tc::smem_desc(kv_addr, 16, 1024, 2), bd0 = tc::smem_desc(q_addr, 16, 1024, 2);
-    for (int kb = 0; kb < 9; ++kb) {
-      ok = tc::mbar_wait_bounded(&sm.bar_q[kb], 0) && ok;
-      tc::tc_fence_after_sync();
+    const int k4 = wid;
 #pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {                 // K step 4 kb + k4 into accumulator k4
-        const uint32_t off = uint32_t(kb * kRegion + k4 * 32), qoff = uint32_t(kb * kCQRegion + k4 * 32);
-        tc::mma_bf16(tmem + uint32_t(k4 * kCHeads), ad0 + (off >> 4), bd0 + (qoff >> 4), idS, kb > 0);
-      }
+    for (int kb = 0; kb < 9; ++kb) {
+      const uint32_t off = uint32_t(kb * kRegion + k4 * 32), qoff = uint32_t(kb * kCQRegion + k4 * 32);
+      tc::mma_bf16(tmem + uint32_t(k4 * kCHeads), ad0 + (off >> 4), bd0 + (qoff >> 4), idS, kb > 0);
     }
     tc::mma_commit(&sm.bar_s);
   }
   __syncwarp();
-  ok = tc::mbar_wait_bounded(&sm.bar_s, 0) && ok;
+  // the cluster has started (warps 1 and 2, which write into other CTAs);
+  // this chunk's zeros precede the others' reduce-adds (warp 2 signals)
+  if (wid == 1 || wid == 2) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (wid == 2 && S > 1 && lane < S && lane != chunk) mbar_arrive_remote(cluster_addr(&sm.bar_zero, uint32_t(lane)));
+  __syncwarp();
+  bool ok = tc::mbar_wait_bounded(&sm.bar_s, 0);
   tc::tc_fence_after_sync();
-  if (swa_tma && !has) {
-    // window rows past swa_len (or past W) are not entries: their scores are
-    // masked; zero their values so that P = 0 never meets a non-finite value
-    const int e = tid & (kCEntries - 1), sub = tid >> 7;
-#pragma unroll
-    for (int i = 0; i < 18; ++i) {
-      const int c = sub * 18 + i;
-      st_shared_v4(kv_s, (c >> 3) * kRegion + tc::sw128_offset(e, c & 7), make_uint4(0, 0, 0, 0));
-    }
-  }
 
   // ---- softmax over the 128 entries (TMEM lanes): 16 warps, 8 heads each ---------------
   const int quarter = wid & 3, oct = wid >> 2;       // lanes 32 quarter.., heads 8 oct..
@@ -761,23 +783,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc::tc_fence_after_sync();
 
-  // ---- O^T = V^T . [P_hi | P_lo]^T  (4 M-tiles of 128 dims, N = 64, K = 128) -------------
-  if (tid == 0) {
+  // ---- O^T = V^T . [P_hi | P_lo]^T  (4 M-tiles of 128 dims, N = 64, K = 128):
+  //      lane 0 of warps 0, 2, 3, 4 each issues one tile's 8 K steps -------------------
+  if ((wid == 0 || (wid >= 2 && wid <= 4)) && lane == 0) {
     constexpr uint32_t idO = tc::idesc_bf16(kCEntries, 2 * kCHeads, 1, 0);
     const uint64_t bp0 = tc::smem_desc(tc::smem_u32(p_s), 16, 1024, 2);
     const uint64_t av0 = tc::smem_desc(kv_addr, kRegion, 1024, 2);
+    const int mt = wid == 0 ? 0 : wid - 1;
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt)                 // consecutive MMAs: different accumulators
-        tc::mma_bf16(tmem + kCOCol + 64 * mt, av0 + (((2 * mt) * kRegion + ks * 2048) >> 4),
-                     bp0 + (((ks >> 2) * kCPRegion + (ks & 3) * 32) >> 4), idO, ks > 0);
-    }
+    for (int ks = 0; ks < 8; ++ks)
+      tc::mma_bf16(tmem + kCOCol + 64 * mt, av0 + (((2 * mt) * kRegion + ks * 2048) >> 4),
+                   bp0 + (((ks >> 2) * kCPRegion + (ks & 3) * 32) >> 4), idO, ks > 0);
     tc::mma_commit(&sm.bar_o);
   }
   __syncwarp();
   // this chunk's (m, l) per head, copied into every CTA of the cluster by
-  // warp 1 while thread 0 issues the O MMAs
+  // warp 1 while the O MMAs are issued
   if (wid == 1) {
     const int o8 = lane >> 3, j = lane & 7;
     sm.ml_mine[0][lane] = fmaxf(fmaxf(sm.red_m[o8][0][j], sm.red_m[o8][1][j]),
@@ -897,21 +918,13 @@ cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
     // one cluster of 128-entry chunks per (sequence, group of 32 heads)
     const int chunks = a.L.splits;
     const int nhg = (H + kCHeads - 1) / kCHeads;
-    CUtensorMap qmap, swamap;
-    if (!encode_rows_map(&qmap, a.q, uint64_t(a.batch) * H, kCHeads)) return cudaErrorInvalidValue;
-    // the window is loaded by TMA when it starts a 128-entry chunk
-    const int swa_chunk = (W > 0 && K % kCEntries == 0) ? K / kCEntries : -1;
-    swamap = qmap;
-    if (swa_chunk >= 0 && !encode_rows_map(&swamap, a.swa, uint64_t(a.batch) * W, kCEntries))
-      return cudaErrorInvalidValue;
     const size_t smem = cluster_smem_bytes();
     static KernelAttrs done;
     cudaError_t e = prepare_kernel(attn_cluster_kernel, smem, false, done);
     if (e != cudaSuccess) return e;
     CSA2_PROFILED(st, "attn_cluster_tc",
                   (e = launch_pdl(attn_cluster_kernel, dim3(unsigned(chunks), unsigned(nhg * a.batch), 1),
-                                  dim3(kAttnThreads), smem, st, unsigned(chunks), a, qmap, swamap, swa_chunk,
-                                  a.early)));
+                                  dim3(kAttnThreads), smem, st, unsigned(chunks), a, a.early)));
     return e;
   }
   // more than 8 chunks: one CTA per 128-entry chunk writes partials,

@@ -54,14 +54,30 @@ __host__ __device__ inline int64_t max64(int64_t a, int64_t b) { return a > b ? 
 __host__ __device__ inline int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
 // Split-KV chunks of 128 entries of an attention call: ceil((K + W) / 128),
-// at least 1.  Calls with K + W <= 1024 (kMaxClusterSplits chunks of 128)
-// merge inside thread-block clusters and use no scratch but the error word;
-// larger ones write per-chunk partials that a combine kernel merges (attn_o /
-// attn_ml of the workspace).
+// at least 1 (the partial path: one CTA per chunk, partials in the
+// workspace's attn_o / attn_ml, merged by a combine kernel).
 __host__ __device__ inline int attn_splits(const csa2_dims& d) {
   const int s = (d.topk + d.swa + kAttnChunk - 1) / kAttnChunk;
   return s < 1 ? 1 : s;
 }
+
+// Chunk c of S (cluster path) holds Top-K slots [K c / S, K (c + 1) / S) and
+// then window rows up to its 128 entries, the window filled into the chunks
+// in order: chunk c takes min(128 - (its Top-K slots), rows left).  With
+// S = ceil((K + W) / 128) every window row finds a place.
+__host__ __device__ inline int attn_chunk_main_lo(int K, int c, int S) { return int(int64_t(K) * c / S); }
+__host__ __device__ inline void attn_chunk_window(int K, int W, int c, int S, int& w0, int& nw) {
+  w0 = 0;
+  nw = 0;
+  for (int i = 0; i <= c; ++i) {
+    const int room = kAttnChunk - (attn_chunk_main_lo(K, i + 1, S) - attn_chunk_main_lo(K, i, S));
+    w0 += nw;
+    nw = W - w0 < room ? W - w0 : room;
+  }
+}
+
+// Calls with K + W <= 1024 (at most kMaxClusterSplits chunks of 128) merge
+// inside thread-block clusters and use no scratch but the error word.
 __host__ __device__ inline bool attn_uses_partials(const csa2_dims& d) { return attn_splits(d) > kMaxClusterSplits; }
 
 __host__ __device__ inline WsLayout make_layout(const csa2_dims& d, int batch) {
