@@ -55,6 +55,7 @@ struct SelSmem {
   uint32_t ghist[2][kBins];                 // cluster-wide sums
   Factor qf[kMaxIdxHeads * 128];            // query factors, [channel][head]
   __align__(16) int32_t qi[kMaxIdxHeads * kQiStride];   // query as integers, [head][channel]
+  int32_t k_lut[256];                       // E4M3 byte -> its value * 2^9 (an exact integer)
   int32_t q_elo[kMaxIdxHeads];              // q = qi * 2^q_elo (exact)
   int32_t q_fast[kMaxIdxHeads];             // 1: the int32 x int32 -> int64 path is exact
   unsigned long long q_l1[kMaxIdxHeads];    // sum_c |qi|
@@ -69,6 +70,7 @@ struct SelSmem {
   uint32_t cnt_in, cnt_band, cnt_sel;
   uint32_t tot3[3];                         // cluster sums read once by warp 0
   uint32_t n_cand;
+  int32_t fast_exact;                       // E4M3 keys, every head on the int64 path
 };
 
 // Scratch of the exact re-scoring, overlaid on keyU (free between the
@@ -493,6 +495,75 @@ __device__ void exact_scores(const IdxArgs& a, SelSmem& sm, const SelCtx& c, con
   }
 }
 
+// Exact scores of up to kFastRows positions in one pass (E4M3 keys, every
+// head's query on the int64 path): the positions' key rows are staged once
+// (all loads in flight together), two threads per (position, head) each sum
+// 64 exact products k*2^9 x qi in int64 and combine their halves, the head
+// dot is rounded once to fp64 and w_h * ReLU(d_h) formed; then one thread
+// per position adds the heads in order in fp64.  -inf for invalid positions.
+constexpr int kFastRows = 64;
+static_assert(kFastRows * 128 <= int(sizeof(int32_t)) * kExRows * kExRowWords, "staged rows fit");
+static_assert(kFastRows * kMaxIdxHeads <= 2 * kExRows * kMaxIdxHeads, "head products fit");
+
+__device__ void exact_scores_fast(const IdxArgs& a, SelSmem& sm, const SelCtx& c, const int64_t* pos, int np,
+                                  double* out) {
+  ExScratch& ex = ex_scratch(sm);
+  const int tid = threadIdx.x, hi = a.d.idx_heads;
+  uint4* rows = reinterpret_cast<uint4*>(ex.krows);           // [kFastRows][8] x 16 bytes
+  double* dd = &ex.dd[0][0];                                   // [kFastRows][kMaxIdxHeads]
+  // ---- stage the rows: 8 threads per position, one 16-byte piece each ----------
+  if (tid < np * 8) {
+    const int p = tid >> 3, part = tid & 7;
+    const int64_t t = pos[p];
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (t >= 0 && t < c.n_ctx) {
+      const int64_t r = kv_row(a.page_table, a.d, c.b, t, a.ws);
+      if (r >= 0) v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(a.idx_k) + r * 128) + part);
+    }
+    rows[p * 8 + part] = v;
+  }
+  __syncthreads();
+  // ---- products: task = (position, head, half of the 128 channels) ------------
+  for (int task = tid; task < np * hi * 2; task += kSelThreads) {
+    const int half = task & 1, ph = task >> 1, p = ph / hi, h = ph % hi;
+    const uint4* kr = rows + p * 8 + half * 4;                 // 64 key bytes
+    const int4* q4 = reinterpret_cast<const int4*>(sm.qi + h * kQiStride + half * 64);
+    long long acc = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint4 kw = kr[w];
+      const uint32_t kb[4] = {kw.x, kw.y, kw.z, kw.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int4 qv = q4[w * 4 + u];
+        acc += (long long)qv.x * sm.k_lut[kb[u] & 0xFF];
+        acc += (long long)qv.y * sm.k_lut[(kb[u] >> 8) & 0xFF];
+        acc += (long long)qv.z * sm.k_lut[(kb[u] >> 16) & 0xFF];
+        acc += (long long)qv.w * sm.k_lut[kb[u] >> 24];
+      }
+    }
+    acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);               // the other half (exact)
+    if (half == 0) {
+      const double d = int_to_f64_rn(acc, sm.q_elo[h] - 9);
+      const unsigned long long db = (unsigned long long)__double_as_longlong(d);
+      const bool positive = (db >> 63) == 0 && db != 0;
+      dd[p * kMaxIdxHeads + h] = __dmul_rn(f32_to_f64_exact(sm.w[h]), positive ? d : 0.0);
+    }
+  }
+  __syncthreads();
+  // ---- ordered head sums ----------------------------------------------------------
+  if (tid < np) {
+    const int64_t t = pos[tid];
+    double sum = -INFINITY;
+    if (t >= 0 && t < c.n_ctx) {
+      sum = 0.0;
+      for (int h = 0; h < hi; ++h) sum = __dadd_rn(sum, dd[tid * kMaxIdxHeads + h]);
+    }
+    out[tid] = sum;
+  }
+  __syncthreads();
+}
+
 // Monotone 64-bit key of a double (larger value -> larger key).
 __device__ inline uint64_t f64_key(double x) {
   uint64_t u = uint64_t(__double_as_longlong(x + 0.0));
@@ -505,8 +576,10 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
                                  int64_t n_items, int64_t k, int32_t* out, double* g_exact,
                                  int32_t* g_list, uint8_t* g_pick) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int64_t base = int64_t(c.rank) * kSelCapPerCta;
-  const int n_local = int(max64(0, min64(kSelCapPerCta, n_items - base)));
+  // the items are split evenly over the cluster's CTAs (whole 32-item words)
+  const int64_t per = min64(kSelCapPerCta, ((n_items + c.cs - 1) / c.cs + 31) & ~int64_t(31));
+  const int64_t base = int64_t(c.rank) * per;
+  const int n_local = int(max64(0, min64(per, n_items - base)));
   const int nwords = (n_local + 31) / 32;
   for (int i = tid; i < kSelCapPerCta / 32; i += blockDim.x) { sm.band_bits[i] = 0; sm.sel_bits[i] = 0; }
   if (tid == 0) { sm.cnt_in = 0; sm.cnt_band = 0; }
@@ -666,7 +739,20 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
       const int nit = int(min64(kExItems, int64_t(nband) - j0));
       if (tid == 0) sm.n_cand = 0;
       __syncthreads();
-      for (int j = wid; j < nit; j += kSelWarps) {
+      // a few band blocks: every valid position of each is a candidate (no
+      // filter by the position scores, one round trip less)
+      const bool all_pos = sm.fast_exact && kind == kBlocks && nit * kBlock <= kFastRows;
+      if (all_pos) {
+        if (tid < nit * kBlock) {
+          const int j = tid >> 3;
+          const int64_t t = (base + blist[j0 + j]) * kBlock + (tid & 7);
+          ex.cand_pos[tid] = t < c.n_ctx ? t : -1;
+          ex.cand_item[tid] = j;
+          if ((tid & 7) == 0) ex.item_best[j] = 0;
+        }
+        if (tid == 0) sm.n_cand = uint32_t(nit * kBlock);
+      }
+      for (int j = all_pos ? nit : wid; j < nit; j += kSelWarps) {
         int64_t gi = base + blist[j0 + j];
         if (kind == kBlocks) {
           int64_t t = gi * kBlock + (lane & 7);
@@ -698,7 +784,11 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
       }
       __syncthreads();
       const int ncand = int(sm.n_cand);
-      exact_scores(a, sm, c, ex.cand_pos, ncand, ex.cand_score);
+      if (sm.fast_exact)
+        for (int c0 = 0; c0 < ncand; c0 += kFastRows)
+          exact_scores_fast(a, sm, c, ex.cand_pos + c0, min(kFastRows, ncand - c0), ex.cand_score + c0);
+      else
+        exact_scores(a, sm, c, ex.cand_pos, ncand, ex.cand_score);
       for (int i = tid; i < ncand; i += blockDim.x)
         atomicMax(&ex.item_best[ex.cand_item[i]], f64_key(ex.cand_score[i]));
       __syncthreads();
@@ -968,6 +1058,16 @@ __device__ void load_query_factors(const IdxArgs& a, SelSmem& sm, int b) {
     if (threadIdx.x >= hi || !fp8 || di != 128 || sm.q_l1[threadIdx.x] >= (1ull << 62) / 229376ull)
       sm.q_fast[threadIdx.x] = 0;
   }
+  if (threadIdx.x < 256) {
+    const Factor f = factor_e4m3(threadIdx.x);
+    sm.k_lut[threadIdx.x] = f.sig * (1 << (f.exp + 9));
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int fast = fp8 && di == 128;
+    for (int h = 0; h < hi; ++h) fast = fast && sm.q_fast[h];
+    sm.fast_exact = fast;
+  }
 }
 
 // Full mode: pool over the cluster, then Top-K of the pool positions on rank
@@ -1010,16 +1110,14 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
     int64_t p_sel = min64(P, nb);
     int32_t* pool = a.pool_out + int64_t(b) * P;
     certified_select(a, sm, c, kBlocks, nb, p_sel, pool, g_exact, g_list, g_pick);
-    if (c.rank != 0) return;
-    for (int i = threadIdx.x; i < P; i += blockDim.x)
-      if (i >= p_sel) pool[i] = -1;
-    if (threadIdx.x == 0) a.pool_len_out[b] = int32_t(p_sel);
+    if (c.rank == 0) {
+      for (int i = threadIdx.x; i < P; i += blockDim.x)
+        if (i >= p_sel) pool[i] = -1;
+      if (threadIdx.x == 0) a.pool_len_out[b] = int32_t(p_sel);
+    }
+    cl_sync(c);                    // every rank's pool ids are written (read through L2)
+    for (int i = threadIdx.x; i < kMaxPool; i += blockDim.x) sm.pool_ids[i] = i < p_sel ? __ldcg(pool + i) : -1;
     __syncthreads();
-    for (int i = threadIdx.x; i < kMaxPool; i += blockDim.x) sm.pool_ids[i] = i < p_sel ? pool[i] : -1;
-    __syncthreads();
-    SelCtx c1 = c;
-    c1.cs = 1;
-    c1.rank = 0;
     // valid pool positions (the context's last block may be partial)
     int has_last = __syncthreads_or(threadIdx.x < kMaxPool && threadIdx.x < p_sel &&
                                     (sm.pool_ids[threadIdx.x] == nb - 1 ||
@@ -1027,9 +1125,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
     int64_t npos = p_sel * kBlock - (has_last ? (nb * kBlock - c.n_ctx) : 0);
     int64_t k_sel = min64(K, npos);
     int32_t* tk = a.topk_out + int64_t(b) * K;
-    certified_select(a, sm, c1, kPoolPos, p_sel * kBlock, k_sel, tk, g_exact, g_list, g_pick);
-    for (int i = threadIdx.x; i < K; i += blockDim.x)
-      if (i >= k_sel) tk[i] = -1;
+    certified_select(a, sm, c, kPoolPos, p_sel * kBlock, k_sel, tk, g_exact, g_list, g_pick);
+    if (c.rank == 0)
+      for (int i = threadIdx.x; i < K; i += blockDim.x)
+        if (i >= k_sel) tk[i] = -1;
   } else {
     int32_t plen = plen_raw;
     if (plen < 0 || plen > P) { if (threadIdx.x == 0) raise_err(a.ws, CSA2_DEV_POOL); plen = 0; }
@@ -1056,7 +1155,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
 }
 
 cudaError_t launch_select(IdxArgs a, bool reindex, cudaStream_t st) {
-  int cs = reindex ? 1 : int((a.L.nb_max + kSelCapPerCta - 1) / kSelCapPerCta);
+  // one CTA per sequence while its items fit (16,384); the block selection of a
+  // longer context spreads over a cluster (up to 8 x 16,384 blocks), which
+  // then also takes the positions of the pool
+  const int cs = reindex ? 1 : int((a.L.nb_max + kSelCapPerCta - 1) / kSelCapPerCta);
   size_t smem = sizeof(SelSmem);
   static KernelAttrs done;
   cudaError_t e = prepare_kernel(select_kernel, smem, false, done);
