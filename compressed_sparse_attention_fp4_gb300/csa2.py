@@ -18,7 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))  # package directory
 LIB_PATH = os.path.join(_PKG, "_build", "libcsa2.so")
 
 LATENT, ROPE, DQK, PAGE, BLOCK = 512, 64, 576, 64, 8
-IDXK_E4M3, IDXK_F32 = 0, 1
+IDXK_E4M3, IDXK_F32, IDXK_FP4 = 0, 1, 2
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
 
 STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED_SHAPE",
@@ -47,6 +47,7 @@ SIGNATURES = {
     "csa2_workspace_size": (_I32, [ctypes.POINTER(CDims), _I32, ctypes.POINTER(_SZ)]),
     "fp4_kv_quantize": (_I32, [_P, _I64, _P, _P, _P]),
     "fp4_kv_quantize_scatter": (_I32, [_P, _I64, _P, _P, _P, _P]),
+    "fp4_idx_k_quantize_scatter": (_I32, [_P, _I64, _P, _P, _I64, _P]),
     "fp4_kv_dequantize": (_I32, [_P, _P, _I64, _P, _P]),
     "indexer_full_topk": (_I32, [ctypes.POINTER(CDims), _I32, _P, _P, _P, _P, _P, _P, _P, _P,
                                  _P, _SZ, _P]),
@@ -152,6 +153,23 @@ def fp4_kv_quantize_scatter(x: torch.Tensor, dst_rows: torch.Tensor, codes: torc
     _check("fp4_kv_quantize_scatter",
            _lib.fp4_kv_quantize_scatter(_ptr(x), x.shape[0], _ptr(dst_rows), _ptr(codes),
                                         _ptr(scales), _stream(stream)))
+
+
+def fp4_idx_k_quantize_scatter(x: torch.Tensor, idx_k: torch.Tensor, cache_rows: int,
+                               dst_rows: torch.Tensor | None = None, stream=None):
+    """bf16 [n, 128] indexer keys into the two-plane FP4 indexer-K buffer
+    ``idx_k`` (uint8, cache_rows * 72 bytes: codes [rows][64], then scales
+    [rows][8]); row i goes to dst_rows[i] (int64) or to row i."""
+    _check("fp4_idx_k_quantize_scatter",
+           _lib.fp4_idx_k_quantize_scatter(_ptr(x), x.shape[0], _ptr(dst_rows), _ptr(idx_k), int(cache_rows),
+                                           _stream(stream)))
+
+
+def fp4_idx_k_planes(idx_k: torch.Tensor, cache_rows: int):
+    """Views (codes [rows, 64], scales [rows, 8]) of a two-plane FP4 indexer-K buffer."""
+    flat = idx_k.reshape(-1)
+    return (flat[:cache_rows * 64].view(cache_rows, 64),
+            flat[cache_rows * 64:cache_rows * 72].view(cache_rows, 8))
 
 
 def fp4_kv_dequantize(codes: torch.Tensor, scales: torch.Tensor, y: torch.Tensor | None = None,

@@ -16,10 +16,25 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 
 csa2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
 
+// Rows of the indexer-K cache: B * max_ctx contiguous, num_pages * 64 paged.
+int64_t idx_cache_rows(const csa2_dims* d, int32_t batch, const int32_t* page_table) {
+  return page_table ? d->num_pages * int64_t(kPage) : int64_t(batch) * d->max_ctx;
+}
+
 // The indexer scan addresses cache rows with 32-bit tensor coordinates.
 csa2_status check_idx_rows(const csa2_dims* d, int32_t batch, const int32_t* page_table) {
-  const int64_t rows = page_table ? d->num_pages * int64_t(kPage) : int64_t(batch) * d->max_ctx;
-  return rows > int64_t(INT32_MAX) ? CSA2_ERR_UNSUPPORTED_SHAPE : CSA2_OK;
+  return idx_cache_rows(d, batch, page_table) > int64_t(INT32_MAX) ? CSA2_ERR_UNSUPPORTED_SHAPE : CSA2_OK;
+}
+
+// Pointer checks of an indexer call; the FP4 query is read in 16-byte pieces.
+csa2_status check_idx_ptrs(const csa2_dims* d, const void* idx_k, const void* idx_q) {
+  if (!aligned(idx_k, 16) || !aligned(idx_q, d->idx_k_dtype == CSA2_IDXK_FP4 ? 16 : 4)) return CSA2_ERR_INVALID_ARG;
+  return CSA2_OK;
+}
+
+const uint8_t* fp4_scales_plane(const csa2_dims* d, int32_t batch, const int32_t* page_table, const void* idx_k) {
+  if (d->idx_k_dtype != CSA2_IDXK_FP4) return nullptr;
+  return static_cast<const uint8_t*>(idx_k) + idx_cache_rows(d, batch, page_table) * 64;
 }
 
 csa2_status check_ws(const csa2_dims* d, int32_t batch, const void* ws, size_t ws_bytes, WsLayout* L) {
@@ -74,6 +89,16 @@ csa2_status fp4_kv_quantize_scatter(const uint16_t* x, int64_t n, const int64_t*
   return from_cuda(launch_quantize(x, n, dst_rows, codes, scales, as_stream(stream)));
 }
 
+csa2_status fp4_idx_k_quantize_scatter(const uint16_t* x, int64_t n, const int64_t* dst_rows,
+                                       uint8_t* idx_k, int64_t cache_rows, void* stream) {
+  if (n < 0 || cache_rows < 0) return CSA2_ERR_INVALID_ARG;
+  if (n == 0) return CSA2_OK;
+  if (!x || !idx_k || !aligned(x, 16) || !aligned(idx_k, 16) || (dst_rows && !aligned(dst_rows, 8)))
+    return CSA2_ERR_INVALID_ARG;
+  if (!dst_rows && n > cache_rows) return CSA2_ERR_INVALID_ARG;
+  return from_cuda(launch_quantize_idx(x, n, dst_rows, idx_k, cache_rows, as_stream(stream)));
+}
+
 csa2_status fp4_kv_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t n, uint16_t* y,
                               void* stream) {
   if (n < 0) return CSA2_ERR_INVALID_ARG;
@@ -95,11 +120,12 @@ csa2_status indexer_full_topk(const csa2_dims* d, int32_t batch, const void* idx
   if (batch == 0) return CSA2_OK;
   if (!idx_k || !ctx_len || !idx_q || !w || !pool_blocks_out || !pool_len_out || !topk_out)
     return CSA2_ERR_INVALID_ARG;
-  if (!aligned(idx_k, 16) || !aligned(idx_q, 4)) return CSA2_ERR_INVALID_ARG;
+  if ((st = check_idx_ptrs(d, idx_k, idx_q)) != CSA2_OK) return st;
   IdxArgs a = {};
   a.d = *d;
   a.batch = batch;
   a.idx_k = idx_k;
+  a.idx_scales = fp4_scales_plane(d, batch, page_table, idx_k);
   a.page_table = page_table;
   a.ctx_len = ctx_len;
   a.idx_q = idx_q;
@@ -126,11 +152,12 @@ csa2_status indexer_reindex_topk(const csa2_dims* d, int32_t batch, const void* 
   if (batch == 0) return CSA2_OK;
   if (!idx_k || !ctx_len || !idx_q || !w || !pool_blocks || !pool_len || !topk_out)
     return CSA2_ERR_INVALID_ARG;
-  if (!aligned(idx_k, 16) || !aligned(idx_q, 4)) return CSA2_ERR_INVALID_ARG;
+  if ((st = check_idx_ptrs(d, idx_k, idx_q)) != CSA2_OK) return st;
   IdxArgs a = {};
   a.d = *d;
   a.batch = batch;
   a.idx_k = idx_k;
+  a.idx_scales = fp4_scales_plane(d, batch, page_table, idx_k);
   a.page_table = page_table;
   a.ctx_len = ctx_len;
   a.idx_q = idx_q;

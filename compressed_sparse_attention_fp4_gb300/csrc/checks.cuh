@@ -25,9 +25,10 @@ inline csa2_status check_attn_dims(const csa2_dims* d, int32_t batch) {
 inline csa2_status check_dims(const csa2_dims* d, int32_t batch) {
   csa2_status st = check_attn_dims(d, batch);
   if (st != CSA2_OK) return st;
-  if (d->idx_k_dtype != CSA2_IDXK_E4M3 && d->idx_k_dtype != CSA2_IDXK_F32) return CSA2_ERR_INVALID_ARG;
+  if (d->idx_k_dtype != CSA2_IDXK_E4M3 && d->idx_k_dtype != CSA2_IDXK_F32 && d->idx_k_dtype != CSA2_IDXK_FP4)
+    return CSA2_ERR_INVALID_ARG;
   if (d->idx_heads < 1 || d->idx_heads > kMaxIdxHeads) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  if (d->idx_k_dtype == CSA2_IDXK_E4M3 && d->idx_dim != 128) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (d->idx_k_dtype != CSA2_IDXK_F32 && d->idx_dim != 128) return CSA2_ERR_UNSUPPORTED_SHAPE;
   if (d->idx_k_dtype == CSA2_IDXK_F32 && d->idx_dim != 64) return CSA2_ERR_UNSUPPORTED_SHAPE;
   if (d->pool_blocks < 1 || d->pool_blocks > kMaxPool) return CSA2_ERR_UNSUPPORTED_SHAPE;
   return CSA2_OK;

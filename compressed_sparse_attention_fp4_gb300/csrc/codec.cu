@@ -5,48 +5,19 @@
 // Flash 2026: ...", section 8, FP4Quantizer: levels {0,.5,1,1.5,2,3,4,6},
 // scale = amax/6 limited to 448, no second-level scale).
 //
-// Rounding (the reading this library implements):
-//   s_code = E4M3 round-to-nearest-even, saturating, of amax/6;
-//   magnitude code = nearest E2M1 level to |x|/s, ties to the even code,
-//   saturating at 6; the sign bit of x is kept; s == 0 gives magnitude 0.
-// Both roundings use the hardware RNE conversions.  amax/6 is formed with a
-// correctly rounded fp32 division: amax has <= 8 significant bits, so amax/6
-// is exact or non-terminating in binary and can never sit on an E4M3
-// midpoint -- rounding it first to fp32 cannot change the E4M3 result.
-// |x|/s is formed as r0 = |x|*rcp(s) plus one FMA residual correction: away
-// from an E2M1 midpoint |x|/s is at least 2^-8 (relative) from it, far more
-// than r0's error; on an exact midpoint the correction returns it exactly,
-// so the conversion sees the exact tie and rounds it to the even code.
+// Rounding: the reading fp4.cuh states and implements (shared with the
+// FP4 indexer keys and query).
 //
 // Layout: one warp per 512-channel row.  Round r in {0,1} covers channels
 // [256r, 256r+256): lane l loads 8 bf16 (16 B, coalesced), lanes 2g and 2g+1
 // share group g, and each lane stores 4 packed bytes (coalesced 128 B per
 // warp) and, for even lanes, one scale byte.
 #include "common.cuh"
+#include "fp4.cuh"
 #include "kernels.cuh"
 #include "profile.cuh"
 
 namespace csa2 {
-
-__device__ inline uint32_t e2m1x2_rn(float hi, float lo) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
-      : "=r"(r) : "f"(hi), "f"(lo));
-  return r & 0xFF;
-}
-
-__device__ inline uint32_t f32_to_e4m3_rn(float x) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
-  return uint32_t(r) & 0xFF;
-}
-
-// |x| / s rounded so that RNE onto the E2M1 grid sees the exact decision.
-__device__ inline float scaled_mag(float ax, float s, float rcp) {
-  float r0 = ax * rcp;
-  float e = __fmaf_rn(-r0, s, ax);
-  return __fmaf_rn(rcp, e, r0);
-}
 
 __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__ x, int64_t n,
                                                        const int64_t* __restrict__ dst_rows,
@@ -65,31 +36,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__
     for (int r = 0; r < 2; ++r) v[r] = __ldcs(x + row * 64 + r * 32 + lane);
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
-      float ax[8];
-      uint32_t sgn[8];
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t lo = w[i] << 16, hi = w[i] & 0xFFFF0000u;
-        sgn[2 * i] = lo >> 31;
-        sgn[2 * i + 1] = hi >> 31;
-        ax[2 * i] = __uint_as_float(lo & 0x7FFFFFFFu);
-        ax[2 * i + 1] = __uint_as_float(hi & 0x7FFFFFFFu);
-        amax = fmaxf(amax, fmaxf(ax[2 * i], ax[2 * i + 1]));
-      }
-      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-      uint32_t sc = f32_to_e4m3_rn(__fdiv_rn(amax, 6.0f));
-      float s = e4m3_to_f32(sc);
-      float rcp = s > 0.0f ? __frcp_rn(s) : 0.0f;
-      uint32_t packed = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float m0 = scaled_mag(ax[2 * i], s, rcp);
-        float m1 = scaled_mag(ax[2 * i + 1], s, rcp);
-        uint32_t byte = e2m1x2_rn(m1, m0) | (sgn[2 * i] << 3) | (sgn[2 * i + 1] << 7);
-        packed |= byte << (8 * i);
-      }
+      uint32_t sc;
+      const uint32_t packed = fp4_quantize_half_group(v[r], &sc);
       codes[dst * 64 + r * 32 + lane] = packed;
       if ((lane & 1) == 0) scales[dst * 32 + r * 16 + (lane >> 1)] = uint8_t(sc);
     }
@@ -138,6 +86,35 @@ __global__ void __launch_bounds__(256) dequantize_kernel(const uint2* __restrict
   }
 }
 
+// FP4 indexer keys: rows of 128 bf16 channels into the two-plane indexer-K
+// cache (codes [rows][64], then scales [rows][8]).  A warp takes two rows:
+// lane l covers row 2w + l/16, channels 8 (l % 16) .. + 7 (16 B of input, 4
+// bytes of codes); lanes 2g and 2g+1 of a half-warp share group g.  Rows whose
+// destination is negative or not below cache_rows are skipped.
+__global__ void __launch_bounds__(256) quantize_idx_kernel(const uint4* __restrict__ x, int64_t n,
+                                                           const int64_t* __restrict__ dst_rows,
+                                                           uint32_t* __restrict__ codes,
+                                                           uint8_t* __restrict__ scales, int64_t cache_rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int half = lane >> 4, part = lane & 15;
+  for (int64_t pair = warp; 2 * pair < n; pair += nwarps) {
+    const int64_t row = 2 * pair + half;
+    const bool have = row < n;
+    const int64_t dst = have ? (dst_rows ? dst_rows[row] : row) : -1;
+    const uint4 v = have ? __ldcs(x + row * 16 + part) : make_uint4(0, 0, 0, 0);
+    uint32_t sc;
+    const uint32_t packed = fp4_quantize_half_group(v, &sc);   // all 32 lanes take part
+    if (dst >= 0 && dst < cache_rows) {
+      codes[dst * 16 + part] = packed;
+      if ((part & 1) == 0) scales[dst * 8 + (part >> 1)] = uint8_t(sc);
+    }
+  }
+}
+
 static int codec_grid(int64_t n) {
   const int sms = device_sms();
   int64_t want = (n + 7) / 8;                    // 8 warps per block, 1 row per warp
@@ -153,6 +130,17 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t n, const int64_t* dst_row
                 (e = launch_pdl(quantize_kernel, dim3(codec_grid(n)), dim3(256), 0, st, 1,
                                 reinterpret_cast<const uint4*>(x), n, dst_rows,
                                 reinterpret_cast<uint32_t*>(codes), scales)));
+  return e;
+}
+
+cudaError_t launch_quantize_idx(const uint16_t* x, int64_t n, const int64_t* dst_rows, uint8_t* idx_k,
+                                int64_t cache_rows, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  cudaError_t e;
+  CSA2_PROFILED(st, "fp4_idx_quantize",
+                (e = launch_pdl(quantize_idx_kernel, dim3(codec_grid((n + 1) / 2)), dim3(256), 0, st, 1,
+                                reinterpret_cast<const uint4*>(x), n, dst_rows,
+                                reinterpret_cast<uint32_t*>(idx_k), idx_k + cache_rows * 64, cache_rows)));
   return e;
 }
 

@@ -191,6 +191,9 @@ cudaError_t launch_full(IdxArgs a, cudaStream_t st) {
   if (fp8) {
     // E4M3 keys: tensor-core scan (tcgen05), bound from the |A| . |q| product
     e = launch_scan_tc(a, false, st);
+  } else if (a.d.idx_k_dtype == CSA2_IDXK_FP4) {
+    // FP4 keys: exact group dots on the tensor cores, scales in fp32
+    e = launch_scan_fp4(a, false, st);
   } else {
     dim3 grid(unsigned((a.d.max_ctx + 255) / 256), unsigned(a.batch));
     CSA2_PROFILED(st, "indexer_scan_cuda_core",
@@ -208,6 +211,8 @@ cudaError_t launch_reindex(IdxArgs a, cudaStream_t st) {
   cudaError_t e;
   if (fp8) {
     e = launch_scan_tc(a, true, st);
+  } else if (a.d.idx_k_dtype == CSA2_IDXK_FP4) {
+    e = launch_scan_fp4(a, true, st);
   } else {
     CSA2_PROFILED(st, "reindex_score_cuda_core",
                   (e = launch_pdl(scan_cc_kernel<false, 64>, grid, dim3(256), 0, st, 1, a, true)));

@@ -84,6 +84,7 @@ struct IdxArgs {
   csa2_dims d;
   int batch;
   const void* idx_k;
+  const uint8_t* idx_scales;   // FP4 keys: the scales plane (idx_k + cache rows * 64)
   const int32_t* page_table;
   const int32_t* ctx_len;
   const void* idx_q;
@@ -120,12 +121,15 @@ struct AttnArgs {
 
 cudaError_t launch_quantize(const uint16_t* x, int64_t n, const int64_t* dst_rows, uint8_t* codes,
                             uint8_t* scales, cudaStream_t st);
+cudaError_t launch_quantize_idx(const uint16_t* x, int64_t n, const int64_t* dst_rows, uint8_t* idx_k,
+                                int64_t cache_rows, cudaStream_t st);
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t n, uint16_t* y,
                               cudaStream_t st);
 cudaError_t launch_full(IdxArgs a, cudaStream_t st);
 cudaError_t launch_reindex(IdxArgs a, cudaStream_t st);
 cudaError_t launch_select(IdxArgs a, bool reindex, cudaStream_t st);
 cudaError_t launch_scan_tc(const IdxArgs& a, bool reindex, cudaStream_t st);
+cudaError_t launch_scan_fp4(const IdxArgs& a, bool reindex, cudaStream_t st);
 cudaError_t launch_attention(AttnArgs a, cudaStream_t st);
 size_t select_smem_bytes();
 size_t attn_smem_bytes(int heads);

@@ -48,22 +48,17 @@
 // head sum and the fp64 rounding of the exact score.  ||k_t||^2 comes from the
 // same MMA (all its products are positive, so it is low by at most 2^-14 of
 // itself) and is raised accordingly before the square root.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include <cmath>
-#include <mutex>
 
 #include "common.cuh"
 #include "kernels.cuh"
 #include "profile.cuh"
+#include "scan_common.cuh"
 #include "tc.cuh"
 
 namespace csa2 {
 
 constexpr int kScanThreads = 448;          // warp 0 TMA, 1 MMA, 2-5 query, 6-9 / 10-13 epilogue
-constexpr int kGroupThreads = 128;         // threads of the query group and of each epilogue group
-constexpr int kTile = 128;                 // positions per tile (= MMA M)
 constexpr int kStages = 10;                // ring depth
 constexpr int kKeyBytes = kTile * 128;     // 16 KB of E4M3 keys
 constexpr int kQpBytes = 32 * 128;         // q1 (16 rows) + r1 (16 rows)
@@ -72,7 +67,6 @@ constexpr int kMmaN = kTile + 32;          // Gram row + the two query pieces
 constexpr int kDBufs = 3;                  // tensor-memory accumulators in flight
 constexpr uint32_t kScanTmemCols = 512;    // D buffer j: cols 160j .. 160j+159
 constexpr float kTcErr = 1.6e-5f;          // 2^-16 + 2^-19 + fp64 rounding, rounded up
-constexpr int kSeqCache = 64;              // sequences whose item counts sit in shared memory
 
 struct ScanSmem {
   uint8_t stage[kStages][kStageStride];    // keys, then query pieces; 1024-aligned
@@ -92,20 +86,6 @@ struct ScanSmem {
   volatile int32_t abort_flag;
 };
 
-__device__ inline void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(uint32_t(accumulate))
-      : "memory");
-}
-
-// kind::f8f6f4 with E4M3 A and B (format code 0), fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
-  return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
-}
-
 __device__ inline uint32_t e4m3_rn(float x) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
@@ -115,92 +95,6 @@ __device__ inline uint32_t e4m3_rn(float x) {
 __device__ inline float e4m3_val(uint32_t code) {
   uint32_t h2 = e4m3x2_to_f16x2(uint16_t(code));
   return __half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF)));
-}
-
-struct TileRef {
-  int b;
-  int64_t t0;        // first item
-  int nvalid;        // valid items in the tile
-};
-
-// Items of sequence b: its positions (Full) or its pool positions, 8 per pool
-// block (Reindex).
-__device__ inline int64_t scan_items(const IdxArgs& a, int b, bool reindex) {
-  if (reindex) {
-    int64_t plen = __ldg(a.pool_len_in + b);
-    return (plen < 0 || plen > a.d.pool_blocks) ? 0 : plen * kBlock;
-  }
-  int64_t n = __ldg(a.ctx_len + b);
-  const bool paged = a.page_table != nullptr;
-  if (n < 0 || n > a.d.max_ctx || (paged && n > int64_t(a.d.max_pages) * kPage)) n = 0;
-  return n;
-}
-
-// Global tile g -> (sequence, first item); tiles of sequence b are
-// ceil(items_b / 128).  Linear walk from a hint (tiles are visited in order).
-__device__ inline TileRef tile_of(const IdxArgs& a, const ScanSmem& sm, bool reindex, int64_t g, int& hint_b,
-                                  int64_t& hint_base) {
-  while (true) {
-    const int64_t n = hint_b < sm.n_seq_cached ? sm.seq_items[hint_b] : scan_items(a, hint_b, reindex);
-    int64_t nt = (n + kTile - 1) / kTile;
-    if (g < hint_base + nt) {
-      TileRef r;
-      r.b = hint_b;
-      r.t0 = (g - hint_base) * kTile;
-      r.nvalid = int(min64(kTile, n - r.t0));
-      return r;
-    }
-    hint_base += nt;
-    ++hint_b;
-  }
-}
-
-// The keys are read once: they go through L2 as evict-first lines, so that
-// the 128 MB stream does not push out the scores this kernel writes (which
-// the selection reads next).
-__device__ inline void issue_tile_load(const IdxArgs& a, const CUtensorMap* map, ScanSmem& sm,
-                                       const TileRef& tr, int stage, uint64_t policy) {
-  if (a.page_table == nullptr) {
-    // contiguous cache: the tile is one run of 128 rows (rows past the
-    // sequence are the next one's or, past the tensor, zero-filled)
-    tc::mbar_expect_tx(&sm.full[stage], kKeyBytes);
-    tc::tma_load_2d_hint(map, sm.stage[stage], 0, int32_t(int64_t(tr.b) * a.d.max_ctx + tr.t0), &sm.full[stage],
-                         policy);
-    return;
-  }
-  uint32_t bytes = 0;
-  int32_t rows[2];
-  int nbox = (tr.nvalid > 64) ? 2 : 1;
-  for (int h = 0; h < nbox; ++h) {
-    int64_t t = tr.t0 + 64 * h;
-    int64_t row = kv_row(a.page_table, a.d, tr.b, t, a.ws);
-    rows[h] = int32_t(row);
-    if (row >= 0) bytes += 64 * 128;
-  }
-  tc::mbar_expect_tx(&sm.full[stage], bytes);
-  for (int h = 0; h < nbox; ++h)
-    if (rows[h] >= 0) tc::tma_load_2d_hint(map, sm.stage[stage] + h * 64 * 128, 0, rows[h], &sm.full[stage], policy);
-}
-
-// Reindex tiles: the pool blocks are scattered 1 KB runs (8 rows, never
-// across a page).  The producer warp resolves the cache rows of the blocks of
-// a window of up to kStages tiles (pool ids and lengths, then page table: the
-// loads of all its blocks in flight together), then gathers each tile with one
-// 8-row TMA box per block: block j lands 1 KB-aligned at rows 8j..8j+7, where
-// the 128-byte swizzle of an 8-row box is that of the whole tile.
-constexpr int kResolvePer = kStages * 16 / 32;   // blocks a producer lane resolves per window
-
-__device__ inline void gather_pool_tile(const CUtensorMap* map, ScanSmem& sm, int64_t row, int stage, int lane,
-                                        uint64_t policy) {
-  const uint32_t nblk = __popc(__ballot_sync(0xFFFFFFFFu, row >= 0));
-  if (lane == 0) tc::mbar_expect_tx(&sm.full[stage], nblk * uint32_t(kBlock * 128));
-  __syncwarp();
-  if (row >= 0)
-    tc::tma_load_2d_hint(map, sm.stage[stage] + lane * (kBlock * 128), 0, int32_t(row), &sm.full[stage], policy);
-}
-
-__device__ inline void group_sync(int id) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kGroupThreads) : "memory");
 }
 
 __device__ inline int head_shift(float qm) { return qm > 0.0f ? max(-60, min(60, 7 - ilogbf(qm))) : 0; }
@@ -289,24 +183,6 @@ __device__ void query_split(const IdxArgs& a, ScanSmem& sm, int b, int gt, int g
   group_sync(bar_id);
 }
 
-// Bounded wait that also gives up once another role has aborted.
-__device__ inline bool wait_or_abort(ScanSmem& sm, uint64_t* bar, uint32_t parity) {
-  if (tc::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = tc::globaltimer_ns();
-  while (true) {
-    if (tc::mbar_try_wait_sleep(bar, parity, 100000u)) return true;   // sleeps until the phase (<= 0.1 ms)
-    if (sm.abort_flag) return false;
-    if (tc::globaltimer_ns() - t0 > 200ull * 1000 * 1000) {
-      sm.abort_flag = 1;
-      return false;
-    }
-  }
-}
-
-__device__ inline void arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
-}
-
 // Whether row r of the tile is a position to score (issued before the
 // epilogue waits for the MMA, so that its loads overlap the wait).
 __device__ inline bool row_valid(const IdxArgs& a, bool reindex, const TileRef& pt, int r) {
@@ -381,16 +257,6 @@ __device__ inline void scan_epilogue(const IdxArgs& a, bool reindex, const ScanS
   }
 }
 
-// Ring position of a role: stage and the parity of its current use, advanced
-// once per tile (no 64-bit division on the single-thread paths).
-struct Ring {
-  int stage = 0;
-  uint32_t phase = 0;
-  __device__ void next() {
-    if (++stage == kStages) { stage = 0; phase ^= 1u; }
-  }
-};
-
 __global__ void __launch_bounds__(kScanThreads, 1)
     scan_tc_kernel(IdxArgs a, const __grid_constant__ CUtensorMap kmap, bool reindex) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -402,21 +268,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   pdl_launch_dependents();
   // ---- tiles of all sequences, this CTA's contiguous share ----------------------
   if (wid == 0) {
-    // every sequence's items are read once (the first kSeqCache are kept for
-    // the tile walks of all roles)
-    const int ncache = min(a.batch, kSeqCache);
-    int64_t tsum = 0;
-    for (int b = lane; b < a.batch; b += 32) {
-      const int64_t n = scan_items(a, b, reindex);
-      if (b < ncache) sm.seq_items[b] = n;
-      tsum += (n + kTile - 1) / kTile;
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) tsum += __shfl_xor_sync(0xFFFFFFFFu, tsum, o);
-    if (lane == 0) {
-      total_tiles_s = tsum;
-      sm.n_seq_cached = ncache;
-    }
+    const int64_t tsum = count_tiles(a, sm, reindex, lane);
+    if (lane == 0) total_tiles_s = tsum;
   }
   __syncthreads();
   const int64_t T = total_tiles_s;
@@ -446,93 +299,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 
   if (wid == 0 && reindex) {
     // ================= producer: TMA gather of pool blocks =================
-    const uint64_t policy = tc::l2_policy_evict_first();
-    int hb = 0;
-    int64_t hbase = 0;
-    bool stop = false;
-    const bool paged = a.page_table != nullptr;
-    Ring ring;
-    int k = 0;
-    for (int k0 = 0; k0 < ntiles && !stop; k0 += kStages) {
-      const int nwin = min(kStages, ntiles - k0);
-      // block idx = lane + 32 j of the window: tile idx / 16, block idx % 16
-      int32_t blk[kResolvePer], pg[kResolvePer];
-      int32_t nraw[kResolvePer], bq[kResolvePer];
-#pragma unroll
-      for (int j = 0; j < kResolvePer; ++j) {
-        const int idx = lane + 32 * j;
-        blk[j] = -1;
-        nraw[j] = 0;
-        bq[j] = 0;
-        if (idx < nwin * 16) {
-          const TileRef tr = tile_of(a, sm, reindex, g0 + k0 + idx / 16, hb, hbase);
-          if ((idx % 16) * kBlock < tr.nvalid) {
-            bq[j] = tr.b;
-            blk[j] = __ldg(a.pool_in + int64_t(tr.b) * a.d.pool_blocks + (tr.t0 >> 3) + idx % 16);
-            nraw[j] = __ldg(a.ctx_len + tr.b);
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kResolvePer; ++j) {
-        pg[j] = -1;
-        if (blk[j] >= 0) {
-          const int64_t n = check_ctx(nraw[j], a.d, paged, a.ws);
-          if (int64_t(blk[j]) * kBlock >= n) blk[j] = -1;
-          else if (paged) pg[j] = __ldg(a.page_table + int64_t(bq[j]) * a.d.max_pages + ((int64_t(blk[j]) * kBlock) >> 6));
-        }
-      }
-      int64_t row[kResolvePer];
-#pragma unroll
-      for (int j = 0; j < kResolvePer; ++j) {
-        row[j] = -1;
-        if (blk[j] >= 0) {
-          const int64_t t = int64_t(blk[j]) * kBlock;
-          if (!paged) {
-            row[j] = int64_t(bq[j]) * a.d.max_ctx + t;
-          } else if (pg[j] < 0 || pg[j] >= a.d.num_pages) {
-            raise_err(a.ws, CSA2_DEV_PAGE_ID);
-          } else {
-            row[j] = int64_t(pg[j]) * kPage + (t & (kPage - 1));
-          }
-        }
-      }
-      for (int w = 0; w < nwin; ++w, ++k, ring.next()) {
-        // the lanes agree on the outcome (they issue the tile together)
-        const bool free_ = k < kStages || wait_or_abort(sm, &sm.empty[ring.stage], ring.phase ^ 1u);
-        if (!__all_sync(0xFFFFFFFFu, free_)) {
-          stop = true;
-          break;
-        }
-        // tile w's 16 blocks are held by lanes 16 (w % 2) .. + 15 in register j = w / 2
-        int64_t my = -1;
-#pragma unroll
-        for (int j = 0; j < kResolvePer; ++j) my = (j == (w >> 1)) ? row[j] : my;
-        const int64_t rb = __shfl_sync(0xFFFFFFFFu, my, (lane & 15) + 16 * (w & 1));
-        gather_pool_tile(&kmap, sm, lane < 16 ? rb : -1, ring.stage, lane, policy);
-      }
-    }
-    // after an abort, let the copies still in flight land before the CTA exits
-    if (sm.abort_flag && lane == 0)
-      for (int j = max(0, k - kStages); j < k; ++j)
-        tc::mbar_wait_bounded(&sm.full[j % kStages], uint32_t((j / kStages) & 1), 20ull * 1000 * 1000);
+    produce_reindex<128, kStages>(a, &kmap, sm, sm.stage[0], kStageStride, sm.full, sm.empty, g0, ntiles, lane);
   } else if (wid == 0) {
     // ================= producer: TMA ring =================
-    if (lane == 0) {
-      const uint64_t policy = tc::l2_policy_evict_first();
-      int pb = 0;
-      int64_t pbase = 0;
-      int k = 0;
-      Ring ring;
-      for (; k < ntiles; ++k, ring.next()) {
-        if (k >= kStages && !wait_or_abort(sm, &sm.empty[ring.stage], ring.phase ^ 1u)) break;
-        issue_tile_load(a, &kmap, sm, tile_of(a, sm, reindex, g0 + k, pb, pbase), ring.stage, policy);
-      }
-      // after an abort, let the copies still in flight land before the CTA exits
-      if (sm.abort_flag)
-        for (int j = max(0, k - kStages); j < k; ++j)
-          tc::mbar_wait_bounded(&sm.full[j % kStages], uint32_t((j / kStages) & 1), 20ull * 1000 * 1000);
-    }
+    if (lane == 0) produce_full<128, kStages>(a, &kmap, sm, sm.stage[0], kStageStride, sm.full, sm.empty, g0, ntiles);
   } else if (wid == 1) {
     // ================= MMA issuer =================
     if (lane == 0) {
@@ -541,7 +311,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       // start-address field (every operand lies below 256 KB, so it never carries)
       const uint64_t d0 = tc::smem_desc(tc::smem_u32(sm.stage[0]), 16, 1024, 2);
       int issued = 0;
-      Ring ring;
+      RingPos<kStages> ring;
       for (int k = 0; k < ntiles; ++k, ring.next()) {
         const int stage = ring.stage;
         const int buf = k % kDBufs;
@@ -567,7 +337,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     const int gt = tid - 64;
     int cb = 0, cur_b = -1;
     int64_t cbase = 0;
-    Ring ring;
+    RingPos<kStages> ring;
     for (int k = 0; k < ntiles; ++k, ring.next()) {
       const TileRef tr = tile_of(a, sm, reindex, g0 + k, cb, cbase);
       const int stage = ring.stage;
@@ -619,46 +389,15 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 // ---------------------------------------------------------------------------
 // Host side: tensor map over the indexer-K cache and the launch
 // ---------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static std::once_flag once;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 cudaError_t launch_scan_tc(const IdxArgs& a, bool reindex, cudaStream_t st) {
-  auto fn = encode_fn();
-  if (!fn) return cudaErrorNotSupported;
-  const bool paged = a.page_table != nullptr;
-  const uint64_t rows = paged ? uint64_t(a.d.num_pages) * kPage : uint64_t(a.batch) * uint64_t(a.d.max_ctx);
   CUtensorMap map;
-  cuuint64_t gdim[2] = {128, rows};
-  cuuint64_t gstride[1] = {128};
-  // Full: a page (64 positions) or a whole tile; Reindex: one pool block
-  cuuint32_t box[2] = {128, reindex ? uint32_t(kBlock) : (paged ? 64u : 128u)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.idx_k), gdim, gstride, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  // the tile count is known only on the device; the grid is sized for an
-  // upper bound and the CTAs split the actual tiles evenly
-  int64_t items_ub = reindex ? int64_t(a.d.pool_blocks) * kBlock : a.d.max_ctx;
-  int64_t tiles_ub = int64_t(a.batch) * ((items_ub + kTile - 1) / kTile);
-  const int sms = device_sms();
+  cudaError_t e = idx_key_map(&map, a, reindex, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = scan_grid(a, reindex);
   const size_t smem = sizeof(ScanSmem) + 1024;
   static KernelAttrs done;
-  cudaError_t e = prepare_kernel(scan_tc_kernel, smem, false, done);
+  e = prepare_kernel(scan_tc_kernel, smem, false, done);
   if (e != cudaSuccess) return e;
-  int64_t grid = min64(int64_t(sms), tiles_ub);
-  if (grid < 1) grid = 1;
   CSA2_PROFILED(st, reindex ? "reindex_score_tc" : "indexer_scan_tc",
                 (e = launch_pdl(scan_tc_kernel, dim3(unsigned(grid)), dim3(kScanThreads), smem, st, 1, a, map,
                                 reindex)));

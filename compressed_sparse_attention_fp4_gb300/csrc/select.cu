@@ -27,6 +27,7 @@
 
 #include "common.cuh"
 #include "exact.cuh"
+#include "fp4.cuh"
 #include "kernels.cuh"
 #include "profile.cuh"
 
@@ -505,6 +506,81 @@ constexpr int kFastRows = 64;
 static_assert(kFastRows * 128 <= int(sizeof(int32_t)) * kExRows * kExRowWords, "staged rows fit");
 static_assert(kFastRows * kMaxIdxHeads <= 2 * kExRows * kMaxIdxHeads, "head products fit");
 
+// FP4 query and keys: d_h = sum_g sk_g sq_hg I_hg / 4 with I_hg = sum over the
+// group of (2 qhat)(2 khat), small integers.  Writing each E4M3 scale as
+// M 2^E (M <= 15, E in [-9, 5]), the group term times 2^20 is the integer
+// M_k M_q I << (E_k + E_q + 18) (shift 0..28, below 2^47); the 8 terms sum
+// exactly in int64 (below 2^50) and d_h = sum * 2^-20 is exact in fp64.
+// Staging: 8 threads per position, one group each (8 code bytes widened to
+// 16 signed bytes, and the scale's M, E); products: two threads per
+// (position, head), 4 groups each (dp4a), halves combined.
+__device__ void exact_scores_fp4(const IdxArgs& a, SelSmem& sm, const SelCtx& c, const int64_t* pos, int np,
+                                 double* out) {
+  ExScratch& ex = ex_scratch(sm);
+  const int tid = threadIdx.x, hi = a.d.idx_heads;
+  uint4* rows = reinterpret_cast<uint4*>(ex.krows);           // [kFastRows][8] x 16 signed bytes
+  int2* ksc = reinterpret_cast<int2*>(ex.krows + kFastRows * 32);   // [kFastRows][8] (M, E)
+  double* dd = &ex.dd[0][0];                                   // [kFastRows][kMaxIdxHeads]
+  if (tid < np * 8) {
+    const int p = tid >> 3, g = tid & 7;
+    const int64_t t = pos[p];
+    uint2 cw = make_uint2(0, 0);
+    uint32_t sc = 0;
+    if (t >= 0 && t < c.n_ctx) {
+      const int64_t r = kv_row(a.page_table, a.d, c.b, t, a.ws);
+      if (r >= 0) {
+        cw = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(a.idx_k) + r * 64) + g);
+        sc = __ldg(a.idx_scales + r * 8 + g);
+      }
+    }
+    rows[p * 8 + g] = make_uint4(e2m1x4_to_i8x4_twice(cw.x), e2m1x4_to_i8x4_twice(cw.x >> 16),
+                                 e2m1x4_to_i8x4_twice(cw.y), e2m1x4_to_i8x4_twice(cw.y >> 16));
+    const Factor f = factor_e4m3(sc);
+    ksc[p * 8 + g] = make_int2(f.sig, f.exp);
+  }
+  __syncthreads();
+  // warp-uniform trip count: both halves of a task sit in one warp and every
+  // lane takes part in the combining shuffle
+  const int lane = tid & 31, ntask = np * hi * 2;
+  for (int base = tid - lane; base < ntask; base += kSelThreads) {
+    const int task = base + lane;
+    const bool act = task < ntask;
+    const int half = task & 1, ph = task >> 1, p = act ? ph / hi : 0, h = act ? ph % hi : 0;
+    const uint4* q4 = reinterpret_cast<const uint4*>(sm.qi + h * kQiStride);
+    long long acc = 0;
+#pragma unroll 1
+    for (int gg = 0; gg < (act ? 4 : 0); ++gg) {
+      const int g = 4 * half + gg;
+      const uint4 kv = rows[p * 8 + g], qv = q4[g];
+      int dot = __dp4a(int(kv.x), int(qv.x), 0);
+      dot = __dp4a(int(kv.y), int(qv.y), dot);
+      dot = __dp4a(int(kv.z), int(qv.z), dot);
+      dot = __dp4a(int(kv.w), int(qv.w), dot);
+      const int2 kf = ksc[p * 8 + g];
+      const Factor qf = sm.qf[h * 8 + g];
+      acc += (long long)(kf.x * qf.sig * dot) * (1ll << (kf.y + qf.exp + 18));   // shift 0..28
+    }
+    acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);               // the other half (exact)
+    if (act && half == 0) {
+      const double d = int_to_f64_rn(acc, -20);
+      const unsigned long long db = (unsigned long long)__double_as_longlong(d);
+      const bool positive = (db >> 63) == 0 && db != 0;
+      dd[p * kMaxIdxHeads + h] = __dmul_rn(f32_to_f64_exact(sm.w[h]), positive ? d : 0.0);
+    }
+  }
+  __syncthreads();
+  if (tid < np) {
+    const int64_t t = pos[tid];
+    double sum = -INFINITY;
+    if (t >= 0 && t < c.n_ctx) {
+      sum = 0.0;
+      for (int h = 0; h < hi; ++h) sum = __dadd_rn(sum, dd[tid * kMaxIdxHeads + h]);
+    }
+    out[tid] = sum;
+  }
+  __syncthreads();
+}
+
 __device__ void exact_scores_fast(const IdxArgs& a, SelSmem& sm, const SelCtx& c, const int64_t* pos, int np,
                                   double* out) {
   ExScratch& ex = ex_scratch(sm);
@@ -524,13 +600,18 @@ __device__ void exact_scores_fast(const IdxArgs& a, SelSmem& sm, const SelCtx& c
   }
   __syncthreads();
   // ---- products: task = (position, head, half of the 128 channels) ------------
-  for (int task = tid; task < np * hi * 2; task += kSelThreads) {
-    const int half = task & 1, ph = task >> 1, p = ph / hi, h = ph % hi;
+  // warp-uniform trip count: both halves of a task sit in one warp and every
+  // lane takes part in the combining shuffle
+  const int lane = tid & 31, ntask = np * hi * 2;
+  for (int base = tid - lane; base < ntask; base += kSelThreads) {
+    const int task = base + lane;
+    const bool act = task < ntask;
+    const int half = task & 1, ph = task >> 1, p = act ? ph / hi : 0, h = act ? ph % hi : 0;
     const uint4* kr = rows + p * 8 + half * 4;                 // 64 key bytes
     const int4* q4 = reinterpret_cast<const int4*>(sm.qi + h * kQiStride + half * 64);
     long long acc = 0;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < (act ? 4 : 0); ++w) {
       const uint4 kw = kr[w];
       const uint32_t kb[4] = {kw.x, kw.y, kw.z, kw.w};
 #pragma unroll
@@ -543,7 +624,7 @@ __device__ void exact_scores_fast(const IdxArgs& a, SelSmem& sm, const SelCtx& c
       }
     }
     acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);               // the other half (exact)
-    if (half == 0) {
+    if (act && half == 0) {
       const double d = int_to_f64_rn(acc, sm.q_elo[h] - 9);
       const unsigned long long db = (unsigned long long)__double_as_longlong(d);
       const bool positive = (db >> 63) == 0 && db != 0;
@@ -572,6 +653,7 @@ __device__ inline uint64_t f64_key(double x) {
 
 // Selects the k best of n items of `kind`; writes their ids ascending to
 // out[0 .. k).  All CTAs of the cluster take part (items split by rank).
+template <bool kFp4>
 __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c, ItemKind kind,
                                  int64_t n_items, int64_t k, int32_t* out, double* g_exact,
                                  int32_t* g_list, uint8_t* g_pick) {
@@ -784,11 +866,15 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
       }
       __syncthreads();
       const int ncand = int(sm.n_cand);
-      if (sm.fast_exact)
+      if constexpr (kFp4) {
+        for (int c0 = 0; c0 < ncand; c0 += kFastRows)
+          exact_scores_fp4(a, sm, c, ex.cand_pos + c0, min(kFastRows, ncand - c0), ex.cand_score + c0);
+      } else if (sm.fast_exact) {
         for (int c0 = 0; c0 < ncand; c0 += kFastRows)
           exact_scores_fast(a, sm, c, ex.cand_pos + c0, min(kFastRows, ncand - c0), ex.cand_score + c0);
-      else
+      } else {
         exact_scores(a, sm, c, ex.cand_pos, ncand, ex.cand_score);
+      }
       for (int i = tid; i < ncand; i += blockDim.x)
         atomicMax(&ex.item_best[ex.cand_item[i]], f64_key(ex.cand_score[i]));
       __syncthreads();
@@ -982,6 +1068,31 @@ __device__ int64_t block_sum(SelSmem& sm, int v) {
   return t;
 }
 
+// FP4 query: quantized exactly as the scan does; per (head, group) the
+// widened codes 2 qhat (signed bytes) and the scale's (M, E).
+__device__ void load_query_fp4(const IdxArgs& a, SelSmem& sm, int b) {
+  const int hi = a.d.idx_heads;
+  if (threadIdx.x < kMaxIdxHeads * 8) {
+    const int h = threadIdx.x >> 3, g = threadIdx.x & 7;
+    uint4 lo = make_uint4(0, 0, 0, 0), hi4 = make_uint4(0, 0, 0, 0);
+    if (h < hi) {
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(a.idx_q) +
+                                                        (int64_t(b) * hi + h) * 128 + 16 * g);
+      lo = __ldg(src);
+      hi4 = __ldg(src + 1);
+    }
+    uint32_t sc;
+    const uint2 cw = fp4_quantize_group(lo, hi4, &sc);
+    reinterpret_cast<uint4*>(sm.qi + h * kQiStride)[g] =
+        make_uint4(e2m1x4_to_i8x4_twice(cw.x), e2m1x4_to_i8x4_twice(cw.x >> 16), e2m1x4_to_i8x4_twice(cw.y),
+                   e2m1x4_to_i8x4_twice(cw.y >> 16));
+    sm.qf[h * 8 + g] = factor_e4m3(sc);
+  }
+  if (threadIdx.x < hi) sm.w[threadIdx.x] = a.w[int64_t(b) * hi + threadIdx.x];
+  if (threadIdx.x == 0) sm.fast_exact = 1;
+  __syncthreads();
+}
+
 // Query factors of sequence b.  Elements h*di + ch are spread over the
 // threads so that a warp's 32 elements share one head (di is 64 or 128):
 // per-head minima, sums and flags are reduced in the warp first and reach
@@ -989,6 +1100,7 @@ __device__ int64_t block_sum(SelSmem& sm, int v) {
 __device__ void load_query_factors(const IdxArgs& a, SelSmem& sm, int b) {
   const int hi = a.d.idx_heads, di = a.d.idx_dim, n = hi * di;
   const int lane = threadIdx.x & 31;
+
   const bool fp8 = a.d.idx_k_dtype == CSA2_IDXK_E4M3;
   // every global load of this thread is issued before the first use
   constexpr int kPer = kMaxIdxHeads * 128 / kSelThreads;
@@ -1072,6 +1184,7 @@ __device__ void load_query_factors(const IdxArgs& a, SelSmem& sm, int b) {
 
 // Full mode: pool over the cluster, then Top-K of the pool positions on rank
 // 0.  Reindex mode (cluster of 1): Top-K of the pool positions.
+template <bool kFp4>
 __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int cs, bool reindex) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
@@ -1097,7 +1210,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
       if (i < a.d.pool_blocks) pin_raw[j] = __ldg(a.pool_in + int64_t(b) * a.d.pool_blocks + i);
     }
   }
-  load_query_factors(a, sm, b);
+  if constexpr (kFp4)
+    load_query_fp4(a, sm, b);
+  else
+    load_query_factors(a, sm, b);
   c.n_ctx = check_ctx(n_raw, a.d, a.page_table != nullptr, a.ws);
   const int64_t scap = a.L.sel_cap;
   double* g_exact = reinterpret_cast<double*>(a.ws + a.L.sel_exact) + int64_t(b) * scap;
@@ -1109,7 +1225,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
   if (!reindex) {
     int64_t p_sel = min64(P, nb);
     int32_t* pool = a.pool_out + int64_t(b) * P;
-    certified_select(a, sm, c, kBlocks, nb, p_sel, pool, g_exact, g_list, g_pick);
+    certified_select<kFp4>(a, sm, c, kBlocks, nb, p_sel, pool, g_exact, g_list, g_pick);
     if (c.rank == 0) {
       for (int i = threadIdx.x; i < P; i += blockDim.x)
         if (i >= p_sel) pool[i] = -1;
@@ -1125,7 +1241,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
     int64_t npos = p_sel * kBlock - (has_last ? (nb * kBlock - c.n_ctx) : 0);
     int64_t k_sel = min64(K, npos);
     int32_t* tk = a.topk_out + int64_t(b) * K;
-    certified_select(a, sm, c, kPoolPos, p_sel * kBlock, k_sel, tk, g_exact, g_list, g_pick);
+    certified_select<kFp4>(a, sm, c, kPoolPos, p_sel * kBlock, k_sel, tk, g_exact, g_list, g_pick);
     if (c.rank == 0)
       for (int i = threadIdx.x; i < K; i += blockDim.x)
         if (i >= k_sel) tk[i] = -1;
@@ -1148,7 +1264,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
     int64_t npos = block_sum(sm, my);
     int64_t k_sel = min64(K, npos);
     int32_t* tk = a.topk_out + int64_t(b) * K;
-    certified_select(a, sm, c, kReindexPos, int64_t(plen) * kBlock, k_sel, tk, g_exact, g_list, g_pick);
+    certified_select<kFp4>(a, sm, c, kReindexPos, int64_t(plen) * kBlock, k_sel, tk, g_exact, g_list, g_pick);
     for (int i = threadIdx.x; i < K; i += blockDim.x)
       if (i >= k_sel) tk[i] = -1;
   }
@@ -1159,12 +1275,14 @@ cudaError_t launch_select(IdxArgs a, bool reindex, cudaStream_t st) {
   // longer context spreads over a cluster (up to 8 x 16,384 blocks), which
   // then also takes the positions of the pool
   const int cs = reindex ? 1 : int((a.L.nb_max + kSelCapPerCta - 1) / kSelCapPerCta);
-  size_t smem = sizeof(SelSmem);
-  static KernelAttrs done;
-  cudaError_t e = prepare_kernel(select_kernel, smem, false, done);
+  const size_t smem = sizeof(SelSmem);
+  const bool fp4 = a.d.idx_k_dtype == CSA2_IDXK_FP4;
+  auto kern = fp4 ? select_kernel<true> : select_kernel<false>;
+  static KernelAttrs done[2];
+  cudaError_t e = prepare_kernel(kern, smem, false, done[fp4 ? 1 : 0]);
   if (e != cudaSuccess) return e;
   CSA2_PROFILED(st, reindex ? "select_reindex" : "select_full",
-                (e = launch_pdl(select_kernel, dim3(unsigned(cs), unsigned(a.batch), 1), dim3(kSelThreads), smem, st,
+                (e = launch_pdl(kern, dim3(unsigned(cs), unsigned(a.batch), 1), dim3(kSelThreads), smem, st,
                                 unsigned(cs), a, cs, reindex)));
   return e;
 }

@@ -41,7 +41,11 @@
  *   codes   uint8  [rows][256]   packed E2M1, channel 2j low nibble of byte j
  *   scales  uint8  [rows][32]    E4M3 scale of channels 16g..16g+15
  *   rope    bf16   [rows][64]    high-precision key part
- *   idx_k   E4M3   [rows][128]   or fp32 [rows][64] (indexer keys)
+ *   idx_k   E4M3   [rows][128], or fp32 [rows][64], or FP4 in two planes:
+ *           codes uint8 [rows][64] (E2M1, channel 2j low nibble of byte j)
+ *           followed by scales uint8 [rows][8] (E4M3, channels 16g..16g+15),
+ *           the scales plane starting at idx_k + rows * 64, where rows =
+ *           batch * max_ctx (contiguous) or num_pages * 64 (paged)
  * Logical position t of sequence b lives in row
  *   page_table == NULL : b * dims.max_ctx + t
  *   page_table != NULL : page_table[b * dims.max_pages + t / 64] * 64 + t % 64
@@ -83,7 +87,10 @@ typedef enum {
 
 typedef enum {
   CSA2_IDXK_E4M3 = 0,   /* indexer K E4M3 [rows][idx_dim], query bf16 */
-  CSA2_IDXK_F32 = 1     /* indexer K fp32 [rows][idx_dim], query fp32 */
+  CSA2_IDXK_F32 = 1,    /* indexer K fp32 [rows][idx_dim], query fp32 */
+  CSA2_IDXK_FP4 = 2     /* indexer K FP4 (two planes, idx_dim 128), query bf16,
+                           quantized by the call to the same FP4 format; the
+                           score is that of the dequantized query and keys */
 } csa2_idxk_dtype;
 
 typedef enum { CSA2_MODE_FULL = 0, CSA2_MODE_REINDEX = 1, CSA2_MODE_REUSE = 2 } csa2_mode;
@@ -91,7 +98,7 @@ typedef enum { CSA2_MODE_FULL = 0, CSA2_MODE_REINDEX = 1, CSA2_MODE_REUSE = 2 } 
 /* Problem dimensions, shared by every call of a decode step. */
 typedef struct {
   int32_t idx_heads;    /* indexer heads Hi, 1..16                            */
-  int32_t idx_dim;      /* indexer dim Di: 128 (E4M3) or 64 (fp32)            */
+  int32_t idx_dim;      /* indexer dim Di: 128 (E4M3, FP4) or 64 (fp32)       */
   int32_t idx_k_dtype;  /* csa2_idxk_dtype                                    */
   int32_t pool_blocks;  /* candidate-pool blocks P, 1..2048 (pages: 2048)     */
   int32_t topk;         /* Top-K, 1..2048 (the pages use 512)                 */
@@ -138,6 +145,21 @@ csa2_status fp4_kv_quantize_scatter(const uint16_t* x, int64_t n,
                                     const int64_t* dst_rows, uint8_t* codes,
                                     uint8_t* scales, void* stream);
 
+/* FP4 indexer-key write (the main-KV format of fp4_kv_quantize applied to
+ * the indexer keys: foosynaptic atlas 3.2 "FP4 main KV" and the FP4-trained
+ * indexer of newsaint.id section 4).  Row i of x (bf16 [n][128], device,
+ * 16-byte aligned) is quantized per 16 channels exactly as fp4_kv_quantize
+ * does and written to row dst_rows[i] (int64 [n], device; NULL: row i) of
+ * the two-plane FP4 indexer-K buffer idx_k (device, 16-byte aligned) of
+ * cache_rows rows: codes at idx_k + row * 64, scales at
+ * idx_k + cache_rows * 64 + row * 8.  Rows whose destination is negative or
+ * not below cache_rows are skipped.
+ * Errors: CSA2_ERR_INVALID_ARG (null pointer with n > 0, n < 0,
+ *         cache_rows < 0, misalignment, n > cache_rows without dst_rows),
+ *         CSA2_ERR_CUDA. */
+csa2_status fp4_idx_k_quantize_scatter(const uint16_t* x, int64_t n, const int64_t* dst_rows,
+                                       uint8_t* idx_k, int64_t cache_rows, void* stream);
+
 /* Inverse of fp4_kv_quantize: y (bf16 [n][512], device) = sign * E2M1 level
  * * E4M3 scale, which bf16 holds exactly (newsaint.id section 4: FP4 values
  * are dequantized just before attention).
@@ -158,7 +180,8 @@ csa2_status fp4_kv_dequantize(const uint8_t* codes, const uint8_t* scales,
  * use fp32 / tensor-core scores with a rigorous error bound and re-score in
  * exact arithmetic every candidate the bound cannot decide.
  *   idx_k:   device, layout above (dtype per d->idx_k_dtype)
- *   idx_q:   device, bf16 (E4M3 keys) or fp32 [B][Hi][Di]
+ *   idx_q:   device, bf16 (E4M3 and FP4 keys; 16-byte aligned for FP4) or
+ *            fp32 [B][Hi][Di]
  *   w:       device, fp32 [B][Hi]
  *   pool_blocks_out: device int32 [B][P], ascending, -1 padded
  *   pool_len_out:    device int32 [B]

@@ -147,3 +147,75 @@ def run_reindex(p, pool, plen, q=None, w=None):
                               pool, plen, topk, p.ws)
     torch.cuda.synchronize()
     return topk
+
+
+def make_fp4_problem(ctx_lens, Hi=16, P=2048, K=512, paged=False, seed=0, kind="random"):
+    """Indexer-only problem with FP4 keys: bf16 keys are drawn, written into the
+    two-plane FP4 indexer-K buffer by the library's quantize call, and kept as
+    float64 for the oracle (which quantizes them itself)."""
+    rng = np.random.default_rng(seed)
+    p = Problem()
+    p.ctx_lens = list(ctx_lens)
+    B = len(ctx_lens)
+    p.B, p.Hi, p.Di, p.P, p.K = B, Hi, 128, P, K
+    max_ctx = max(max(ctx_lens), 1)
+    if paged:
+        pages = [-(-n // 64) for n in ctx_lens]
+        total = sum(pages) + 3
+        perm = rng.permutation(total).astype(np.int32)
+        table = np.full((B, max(max(pages), 1)), -1, dtype=np.int32)
+        off = 0
+        for b, pg in enumerate(pages):
+            table[b, :pg] = perm[off:off + pg]
+            off += pg
+        p.table = table
+        rows = total * 64
+        dims = csa2.Dims(idx_heads=Hi, idx_dim=128, idx_k_dtype=csa2.IDXK_FP4, pool_blocks=P, topk=K,
+                         heads=64, swa=128, max_pages=table.shape[1], num_pages=total,
+                         max_ctx=table.shape[1] * 64)
+    else:
+        p.table = None
+        rows = B * max_ctx
+        dims = csa2.Dims(idx_heads=Hi, idx_dim=128, idx_k_dtype=csa2.IDXK_FP4, pool_blocks=P, topk=K,
+                         heads=64, swa=128, max_ctx=max_ctx)
+    p.dims, p.rows = dims, rows
+    p.rows_of = []
+    for b, n in enumerate(ctx_lens):
+        t = np.arange(n, dtype=np.int64)
+        p.rows_of.append(table[b, t // 64].astype(np.int64) * 64 + t % 64 if paged else b * max_ctx + t)
+    scale_ch = rng.lognormal(0, 0.5, 128).astype(np.float32)
+    p.k_bits = []
+    p.idx_k = torch.zeros(rows * 72, dtype=torch.uint8, device="cuda")
+    for b, n in enumerate(ctx_lens):
+        if kind == "ties":
+            base = rng.standard_normal((3, 128)).astype(np.float32) * scale_ch
+            k = base[rng.integers(0, 3, n)]
+        elif kind == "wide":
+            # every group of 16 at its own power-of-two scale across the E4M3
+            # range: group terms of very different size, with cancellation
+            k = rng.standard_normal((n, 128)).astype(np.float32)
+            k *= np.repeat(np.exp2(rng.integers(-8, 8, (n, 8))), 16, axis=1).astype(np.float32)
+        else:
+            k = rng.standard_normal((n, 128)).astype(np.float32) * scale_ch
+        bits = synth.to_bf16_bits(k)
+        p.k_bits.append(bits)
+        if n:
+            x = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+            csa2.fp4_idx_k_quantize_scatter(x, p.idx_k, rows, torch.from_numpy(p.rows_of[b]).cuda())
+    q = rng.standard_normal((B, Hi, 128)).astype(np.float32)
+    if kind == "wide":
+        q *= np.repeat(np.exp2(rng.integers(-6, 6, (B, Hi, 8))), 16, axis=2).astype(np.float32)
+    p.idx_q_raw = synth.to_bf16_bits(q)
+    p.idx_q_f64 = bf16_f64(p.idx_q_raw)
+    p.idx_q = torch.from_numpy(p.idx_q_raw.view(np.int16)).view(torch.bfloat16).cuda()
+    p.w_raw = rng.random((B, Hi)).astype(np.float32)
+    p.w = torch.from_numpy(p.w_raw).cuda()
+    p.ctx = torch.tensor(ctx_lens, dtype=torch.int32, device="cuda")
+    p.page_table = None if p.table is None else torch.from_numpy(p.table).cuda()
+    p.ws = csa2.alloc_workspace(dims, B)
+    return p
+
+
+def fp4_keys_f64(p, b):
+    """The bf16 keys of sequence b as float64 (before quantization)."""
+    return bf16_f64(p.k_bits[b])

@@ -152,3 +152,19 @@ def test_full_and_reindex_top1024():
     check_full(p, pool, plen, topk)
     tk = run_reindex(p, pool, plen)
     np.testing.assert_array_equal(tk.cpu().numpy(), topk.cpu().numpy())
+
+
+def test_eight_heads_odd_band():
+    """8 indexer heads: a warp of the exact re-scoring holds (position, head)
+    halves of an odd number of positions; Full and Reindex still match."""
+    p = make_problem([20000, 9000, 17, 4099], Hi=8, P=512, K=512, seed=19, with_kv=False)
+    pool, plen, topk = run_full(p)
+    check_full(p, pool, plen, topk)
+    rng = np.random.default_rng(29)
+    from compressed_sparse_attention_fp4_gb300 import synth
+    from tests.helpers import bf16_f64
+    raw = synth.to_bf16_bits(rng.standard_normal(p.idx_q_f64.shape).astype(np.float32))
+    qd = torch.from_numpy(raw.view(np.int16)).cuda().view(torch.bfloat16)
+    w2 = rng.random(p.w_raw.shape).astype(np.float32)
+    tk = run_reindex(p, pool, plen, qd, torch.from_numpy(w2).cuda())
+    check_reindex(p, pool, tk, bf16_f64(raw), w2)
