@@ -7,7 +7,7 @@ captured once as a CUDA graph and replayed.  Metric: decode queries/s
 (sequences x steps / time); achieved HBM GB/s of the algorithmic bytes
 against the measured peak.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 128k|1m|mix|tiny]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 128k|1m|1m-fp4|128k-fp4|mix|tiny]
                   [--impl ours|reference]
 
 N > 1 (torchrun): every rank runs its own replica of the workload (no data-
@@ -56,25 +56,35 @@ def attn_layer_bytes(wl):
     return (K * ENTRY_B + W * 576 * 2 + H * 576 * 2 + H * 513 * 4 + K * 4)
 
 
+def idx_row_bytes(wl):
+    """Bytes of one indexer-K row: E4M3 128, fp32 4 x Di, FP4 64 + 8."""
+    return {"fp8": wl.idx_dim, "fp32": 4 * wl.idx_dim, "fp4": 72}[wl.idx_k_dtype]
+
+
+def idx_qw_bytes(wl):
+    """Indexer query (bf16 for E4M3 / FP4 keys, fp32 otherwise) and weights."""
+    return wl.idx_heads * wl.idx_dim * (4 if wl.idx_k_dtype == "fp32" else 2) + wl.idx_heads * 4
+
+
 def step_bytes(wl):
     """Algorithmic HBM bytes of one decode step over the whole batch."""
     tot = 0
-    idx_row = wl.idx_dim * (1 if wl.idx_k_dtype == "fp8" else 4)
-    q_w = wl.idx_heads * wl.idx_dim * (2 if wl.idx_k_dtype == "fp8" else 4) + wl.idx_heads * 4
+    idx_row, q_w = idx_row_bytes(wl), idx_qw_bytes(wl)
     for n in wl.ctx_lens:
         pool_pos = min(wl.pool_blocks * 8, n)
         for m in wl.schedule:
             tot += attn_layer_bytes(wl)
             if m == "F":
                 tot += idx_row * n + q_w + wl.pool_blocks * 4 + wl.topk * 4 + 1024 + ENTRY_B
+                if wl.idx_k_dtype == "fp4":
+                    tot += 2 * wl.idx_dim + 72                 # the new token's indexer-key write
             elif m == "Ri":
                 tot += idx_row * pool_pos + wl.pool_blocks * 4 + q_w + wl.topk * 4
     return tot
 
 
 def full_call_bytes(wl):
-    idx_row = wl.idx_dim * (1 if wl.idx_k_dtype == "fp8" else 4)
-    q_w = wl.idx_heads * wl.idx_dim * 2 + wl.idx_heads * 4
+    idx_row, q_w = idx_row_bytes(wl), idx_qw_bytes(wl)
     return sum(idx_row * n + q_w + wl.pool_blocks * 4 + wl.topk * 4 for n in wl.ctx_lens)
 
 
@@ -172,14 +182,22 @@ def oracle_query(wl, b, kv, layers):
     from oracle import schedule
     from oracle import codec as oc
     f64 = lambda x: (np.asarray(x, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    keys = oc.e4m3_decode(kv["idx_k"]) if wl.idx_k_dtype == "fp8" else kv["idx_k"].astype(np.float64)
+    from oracle import indexer_fp4 as ofp4
+    fp4q = lambda x: ofp4.dequantize(*ofp4.quantize(x))                # FP4 keys: the oracle's own write
+    if wl.idx_k_dtype == "fp8":
+        keys = oc.e4m3_decode(kv["idx_k"])
+    elif wl.idx_k_dtype == "fp4":
+        keys = fp4q(f64(kv["idx_k"]))
+    else:
+        keys = kv["idx_k"].astype(np.float64)
     codes, scales = oc.quantize_rows(f64(kv["latent"][-1:]))          # FP4 write of the new token
     lat = np.zeros((kv["latent"].shape[0], 512))
     rope = f64(kv["rope"])
     L = []
     for li in layers:
         L.append({"q": f64(li["q"]), "swa": f64(li["swa"]), "swa_len": li["swa_len"],
-                  "idx_q": f64(li["idx_q"]) if wl.idx_k_dtype == "fp8" else li["idx_q"].astype(np.float64),
+                  "idx_q": (f64(li["idx_q"]) if wl.idx_k_dtype == "fp8" else fp4q(f64(li["idx_q"]))
+                            if wl.idx_k_dtype == "fp4" else li["idx_q"].astype(np.float64)),
                   "idx_w": li["idx_w"].astype(np.float64)})
 
     class LazyLatent:
@@ -246,15 +264,17 @@ def job_queries_per_s(world: int, batch: int, t_step_ms: float) -> float:
 def kernel_bytes(wl, name):
     """Algorithmic HBM bytes of one launch of a library kernel on workload wl
     (None for the latency-bound selection kernels)."""
-    idx_row = wl.idx_dim * (1 if wl.idx_k_dtype == "fp8" else 4)
-    if name in ("indexer_scan_tc", "indexer_scan_cuda_core"):
+    idx_row = idx_row_bytes(wl)
+    if name in ("indexer_scan_tc", "indexer_scan_fp4", "indexer_scan_cuda_core"):
         return sum(idx_row * n for n in wl.ctx_lens)
-    if name == "reindex_score_tc":
+    if name in ("reindex_score_tc", "reindex_score_fp4", "reindex_score_cuda_core"):
         return sum(idx_row * min(wl.pool_blocks * 8, n) + wl.pool_blocks * 4 for n in wl.ctx_lens)
     if name in ("attn_cluster_tc", "attn_partial_tc"):
         return wl.batch * attn_layer_bytes(wl)
-    if name == "quantize":
+    if name == "fp4_quantize":
         return wl.batch * (1024 + 288)
+    if name == "fp4_idx_quantize":
+        return wl.batch * (2 * wl.idx_dim + 72)
     return None
 
 
@@ -327,16 +347,16 @@ TRAFFIC_UNITS = {
 
 
 def traffic_of(wl, name):
-    files = {"indexer_scan_tc": "scan.cu", "reindex_score_tc": "scan.cu", "attn_cluster_tc": "attention.cu",
-             "attn_partial_tc": "attention.cu"}
+    files = {"indexer_scan_tc": "scan.cu", "reindex_score_tc": "scan.cu", "indexer_scan_fp4": "scan_fp4.cu",
+             "reindex_score_fp4": "scan_fp4.cu", "attn_cluster_tc": "attention.cu", "attn_partial_tc": "attention.cu"}
     if name not in files:
         return None
     per_unit = TRAFFIC_UNITS.get((name, src_hash(files[name])))
     if per_unit is None:
         return None
-    if name == "indexer_scan_tc":
-        return per_unit * sum(wl.ctx_lens) if wl.idx_k_dtype == "fp8" else None
-    if name == "reindex_score_tc":
+    if name in ("indexer_scan_tc", "indexer_scan_fp4"):
+        return per_unit * sum(wl.ctx_lens)
+    if name in ("reindex_score_tc", "reindex_score_fp4"):
         return per_unit * sum(min(wl.pool_blocks * 8, n) for n in wl.ctx_lens)
     return per_unit * wl.batch
 
@@ -659,7 +679,14 @@ def main():
         s1["clocks"] = r1["clocks"]
         del r1
         torch.cuda.empty_cache()
-        line["workloads"] = {"decode-1m": s1, "codec-1m-rows": codec_rates(dev)}
+        wl4 = synth.workload("1m-fp4")
+        r4 = measure_workload(wl4, args, dev, world, flush, with_e2e=False)
+        s4 = summarise(r4, peak, peak_kind)
+        s4["config"] = arm_config(wl4, world)
+        s4["clocks"] = r4["clocks"]
+        del r4
+        torch.cuda.empty_cache()
+        line["workloads"] = {"decode-1m": s1, "decode-1m-fp4": s4, "codec-1m-rows": codec_rates(dev)}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
     if world > 1:

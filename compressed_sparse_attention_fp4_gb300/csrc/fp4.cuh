@@ -97,14 +97,16 @@ __device__ inline uint2 fp4_quantize_group(uint4 lo, uint4 hi, uint32_t* scale) 
   return make_uint2(fp4_pack8(a, s, rcp), fp4_pack8(b, s, rcp));
 }
 
-// Four E2M1 nibbles (the low 16 bits of w, nibble k = channel k) as four
-// E4M3 bytes worth 2^-6 times their values: the nibble's three magnitude bits
-// m go to bits 2..4 of the byte and its sign to bit 7.  (m = 0..3 land on the
-// E4M3 subnormal / first binade as 0, 2^-7, 2^-6, 1.5 * 2^-6, and m = 4..7 on
-// 2^-5, 1.5 * 2^-5, 2^-4, 1.5 * 2^-4: exactly 2^-6 * {0, .5, 1, 1.5, 2, 3, 4, 6}.)
-__device__ inline uint32_t e2m1x4_to_e4m3x4_scaled(uint32_t w) {
-  const uint32_t t = __byte_perm(w, 0u, 0x1100u);   // bytes: w0 w0 w1 w1
-  return ((t & 0x00070007u) << 2) | ((t & 0x70007000u) >> 2) | ((t & 0x00080008u) << 4) | (t & 0x80008000u);
+// Eight E2M1 nibbles (nibble k of w = channel k) as eight E4M3 bytes worth
+// 2^-6 times their values, in the channel order 0, 2, 4, 6 (ev) and 1, 3, 5, 7
+// (od): a nibble's three magnitude bits m go to bits 2..4 of its byte and its
+// sign to bit 7.  (m = 0..3 land on the E4M3 subnormals / first binade as 0,
+// 2^-7, 2^-6, 1.5 * 2^-6 and m = 4..7 on 2^-5, 1.5 * 2^-5, 2^-4, 1.5 * 2^-4:
+// exactly 2^-6 * {0, .5, 1, 1.5, 2, 3, 4, 6}.)  A dot product is the same in
+// any channel order, so keys and query widened alike multiply correctly.
+__device__ inline void e2m1x8_to_e4m3x8_scaled(uint32_t w, uint32_t& ev, uint32_t& od) {
+  ev = ((w & 0x07070707u) << 2) | ((w & 0x08080808u) << 4);
+  od = ((w >> 2) & 0x1C1C1C1Cu) | (w & 0x80808080u);
 }
 
 // Four E2M1 nibbles (low 16 bits of w) as signed bytes of twice their values

@@ -11,7 +11,8 @@
 // Exact group dots on the tensor cores.  Every E2M1 level times 2 is an
 // integer, so D is a multiple of 1/4 with |D| <= 16 * 36 = 576.  The keys and
 // the query are widened to E4M3 bytes worth 2^-6 times their E2M1 values (a
-// bit shuffle, exact) and multiplied with kind::f8f6f4: every product is a
+// bit shuffle, exact; within every 8 channels the even ones first, the same in
+// keys and query) and multiplied with kind::f8f6f4: every product is a
 // multiple of 2^-14 below 2^-6 * 36 and every partial sum a multiple of 2^-14
 // below 2^-3, so the tensor core forms D * 2^-12 without any rounding (the
 // accumulation keeps far more than the 12 bits involved).  One MMA per 32
@@ -20,7 +21,8 @@
 // of the k-step's accumulator is D_{t,h,2ks+p}: 128 columns per tile, one per
 // (group, head).
 //
-// Scales and the bound in fp32.  y = (sk * 4096) * D2 (D2 = the accumulator)
+// Scales and the bound in fp32 (pairs of heads per f32x2 instruction, each
+// lane rounded as a scalar one).  y = (sk * 4096) * D2 (D2 = the accumulator)
 // is exact (<= 16 significant bits); d_h = sum_g sq_{h,g} y_g is a chain of 8
 // FMAs (7 roundings) and v = sum_h w_h max(d_h, 0) a chain of 16 FMAs, so
 //   |v - s| <= (gamma_7 + gamma_16 (1 + gamma_7)) sum_h |w_h| sum_c |q_hc k_tc|
@@ -40,8 +42,8 @@
 //   * warp 1 (one thread): 4 MMAs per tile (M = 128, N = 32, K = 32) into one
 //     of three tensor-memory accumulators;
 //   * warps 6-9 / 10-13 (epilogue, alternate tiles): the row's 8 key scales
-//     (read from global memory while the MMAs run), scores, bound, block
-//     maxima, writes.
+//     (read from global memory two tiles ahead), scores, bound, block maxima,
+//     writes.
 #include <cmath>
 
 #include "common.cuh"
@@ -55,7 +57,11 @@ namespace csa2 {
 
 namespace {
 
-constexpr int kFThreads = 448;            // warp 0 TMA, 1 MMA, 2-5 converter, 6-9 / 10-13 epilogue
+constexpr int kConvWarps = 4;             // converter warps 2-5, four code rows per thread
+constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kEpiWarp0 = 2 + kConvWarps;  // epilogue groups: warps 6-9 (even tiles), 10-13 (odd)
+constexpr int kEpiThreads = 128;          // threads of an epilogue group: one per row
+constexpr int kFThreads = 32 * (kEpiWarp0 + 8);
 constexpr int kCStages = 8;               // code ring depth
 constexpr int kCodeBytes = kTile * 64;    // 8 KB of FP4 codes per tile
 constexpr int kAStages = 4;               // operand stages
@@ -96,29 +102,46 @@ __device__ inline uint2 query_group(const IdxArgs& a, int b, int h, int g, uint3
   return fp4_quantize_group(lo, hi4, sc);
 }
 
+__device__ inline void conv_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConvThreads) : "memory");
+}
+
 // Converter group (gt = 0..127 owns head gt/8, group gt%8): B of sequence b
-// into sm.qb.  Row (p, h) = 16 p + h holds the widened query of head h in the
-// groups of parity p; the chunks of the other parity are zero.
+// into sm.qb.  Row 16 p + h holds the widened query of head h in the groups of
+// parity p; the chunks of the other parity are zero.  So column 32 ks + 16 p
+// + h of a tile's accumulator is head h's dot over group 2 ks + p: column
+// 16 g + h for group g.
 __device__ void build_b(const IdxArgs& a, FScanSmem& sm, int b, int gt) {
-  const int h = gt >> 3, g = gt & 7;
-  uint32_t sc;
-  const uint2 c = query_group(a, b, h, g, &sc);
-  const uint4 v = make_uint4(e2m1x4_to_e4m3x4_scaled(c.x), e2m1x4_to_e4m3x4_scaled(c.x >> 16),
-                             e2m1x4_to_e4m3x4_scaled(c.y), e2m1x4_to_e4m3x4_scaled(c.y >> 16));
-  group_sync(1);                                   // the previous B has been copied out
-  const int p = g & 1;
-  *reinterpret_cast<uint4*>(sm.qb + tc::sw128_offset(16 * p + h, g)) = v;
-  *reinterpret_cast<uint4*>(sm.qb + tc::sw128_offset(16 * (1 - p) + h, g)) = make_uint4(0, 0, 0, 0);
-  group_sync(1);
+  const int h = (gt >> 3) & 15, g = gt & 7;
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (gt < 128) {
+    uint32_t sc;
+    const uint2 c = query_group(a, b, h, g, &sc);
+    e2m1x8_to_e4m3x8_scaled(c.x, v.x, v.y);
+    e2m1x8_to_e4m3x8_scaled(c.y, v.z, v.w);
+  }
+  conv_sync();                                     // the previous B has been copied out
+  if (gt < 128) {
+    const int p = g & 1;
+    *reinterpret_cast<uint4*>(sm.qb + tc::sw128_offset(16 * p + h, g)) = v;
+    *reinterpret_cast<uint4*>(sm.qb + tc::sw128_offset(16 * (1 - p) + h, g)) = make_uint4(0, 0, 0, 0);
+  }
+  conv_sync();
+}
+
+__device__ inline void epi_sync(int eg) {
+  asm volatile("bar.sync %0, %1;" ::"r"(2 + eg), "n"(kEpiThreads) : "memory");
 }
 
 // Epilogue group eg (gt = 0..127 owns head gt/8, group gt%8): the scales,
 // weights and bound factors of sequence b.
 __device__ void epi_query(const IdxArgs& a, FScanSmem& sm, int b, int gt, int eg) {
-  const int h = gt >> 3, g = gt & 7, hi = a.d.idx_heads;
-  uint32_t sc;
-  const uint2 c = query_group(a, b, h, g, &sc);
-  const float wh = h < hi ? __ldg(a.w + int64_t(b) * hi + h) : 0.0f;
+  const int h = (gt >> 3) & 15, g = gt & 7, hi = a.d.idx_heads;
+  const bool own = gt < 128;
+  uint32_t sc = 0;
+  uint2 c = make_uint2(0, 0);
+  if (own) c = query_group(a, b, h, g, &sc);
+  const float wh = own && h < hi ? __ldg(a.w + int64_t(b) * hi + h) : 0.0f;
   const float wg = gt < hi ? __ldg(a.w + int64_t(b) * hi + gt) : 0.0f;
   // 2 * sum |qhat| over the group: twice each level is an integer
   const uint32_t twice[4] = {e2m1x4_to_i8x4_twice(c.x & 0x7777u), e2m1x4_to_i8x4_twice((c.x >> 16) & 0x7777u),
@@ -126,37 +149,61 @@ __device__ void epi_query(const IdxArgs& a, FScanSmem& sm, int b, int gt, int eg
   int s2 = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) s2 = __dp4a(int(twice[i]), int(0x01010101), s2);
-  const float sqv = h < hi ? e4m3_to_f32(sc) : 0.0f;
-  group_sync(2 + eg);                              // the previous sequence's values are no longer read
-  sm.sq[eg][g][h] = sqv;
-  sm.ucon[eg][g][h] = __fmul_ru(fabsf(wh), sqv * float(s2) * 0.5f);   // sqv * s2 / 2 is exact
+  const float sqv = own && h < hi ? e4m3_to_f32(sc) : 0.0f;
+  epi_sync(eg);                                    // the previous sequence's values are no longer read
+  if (own) {
+    sm.sq[eg][g][h] = sqv;
+    sm.ucon[eg][g][h] = __fmul_ru(fabsf(wh), sqv * float(s2) * 0.5f);   // sqv * s2 / 2 is exact
+  }
   if (gt < kMaxIdxHeads) sm.wv[eg][gt] = wg;
-  group_sync(2 + eg);
+  epi_sync(eg);
   if (gt < 8) {
     float u = 0.0f;
 #pragma unroll
     for (int i = 0; i < kMaxIdxHeads; ++i) u = __fadd_ru(u, sm.ucon[eg][gt][i]);
     sm.ub[eg][gt] = __fmul_ru(__fmul_ru(a.err_coef, 6.0f), u);
   }
-  group_sync(2 + eg);
+  epi_sync(eg);
 }
 
-// d_h += sum over the 2 groups g0, g0+1 of sq_{h,g} * (sk'_g * D2[16 (g - g0) + h]).
+// Packed pairs of fp32 values (two heads) for the f32x2 instructions: each
+// lane of a pair is rounded exactly as the scalar instruction would round it.
+__device__ inline uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ inline void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ inline uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ inline uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// d_h += sq_{h,g} * (sk'_g * D2[16 (g - g0) + h]) over the 2 groups g0, g0+1,
+// two heads per instruction (acc2[j] holds heads 2j, 2j+1).
 __device__ inline void group_terms(const FScanSmem& sm, int eg, int g0, const float (&dv)[32], const float (&skp)[8],
-                                   float (&acc)[kMaxIdxHeads]) {
+                                   uint64_t (&acc2)[kMaxIdxHeads / 2]) {
 #pragma unroll
   for (int gg = 0; gg < 2; ++gg) {
     const int g = g0 + gg;
-    const float4* sq4 = reinterpret_cast<const float4*>(sm.sq[eg][g]);
+    const uint64_t sk2 = f2_pack(skp[g], skp[g]);
+    const ulonglong2* sq2 = reinterpret_cast<const ulonglong2*>(sm.sq[eg][g]);
 #pragma unroll
-    for (int h4 = 0; h4 < 4; ++h4) {
-      const float4 s = sq4[h4];
-      const float sv[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int h = 4 * h4 + j;
-        acc[h] = __fmaf_rn(sv[j], skp[g] * dv[16 * gg + h], acc[h]);   // skp * dv is exact
-      }
+    for (int j4 = 0; j4 < 4; ++j4) {
+      const ulonglong2 s = sq2[j4];                       // heads 4 j4 .. 4 j4 + 3
+      const int c = 16 * gg + 4 * j4;
+      const uint64_t y0 = f2_mul(sk2, f2_pack(dv[c], dv[c + 1]));        // exact
+      const uint64_t y1 = f2_mul(sk2, f2_pack(dv[c + 2], dv[c + 3]));
+      acc2[2 * j4] = f2_fma(s.x, y0, acc2[2 * j4]);
+      acc2[2 * j4 + 1] = f2_fma(s.y, y1, acc2[2 * j4 + 1]);
     }
   }
 }
@@ -165,7 +212,6 @@ __device__ inline void group_terms(const FScanSmem& sm, int eg, int g0, const fl
 // quarter r / 32) of epilogue group eg.
 __device__ inline void fp4_epilogue(const IdxArgs& a, bool reindex, const FScanSmem& sm, int eg, const TileRef& pt,
                                     uint32_t tmem_d, int64_t row, uint2 kscale, int r, int lane) {
-  const bool valid = row >= 0;
   float skp[8], sk[8];
   const uint32_t kw[2] = {kscale.x, kscale.y};
 #pragma unroll
@@ -176,21 +222,27 @@ __device__ inline void fp4_epilogue(const IdxArgs& a, bool reindex, const FScanS
   }
 #pragma unroll
   for (int g = 0; g < 8; ++g) skp[g] = sk[g] * 4096.0f;    // undoes the 2^-6 * 2^-6 of the widening
-  float acc[kMaxIdxHeads];
+  uint64_t acc2[kMaxIdxHeads / 2];
 #pragma unroll
-  for (int h = 0; h < kMaxIdxHeads; ++h) acc[h] = 0.0f;
+  for (int j = 0; j < kMaxIdxHeads / 2; ++j) acc2[j] = 0;
 #pragma unroll
   for (int ks = 0; ks < 4; ++ks) {                          // groups 2ks, 2ks+1
     float dv[32];
     tc::tmem_ld32(tmem_d + 32 * ks, dv);
-    group_terms(sm, eg, 2 * ks, dv, skp, acc);
+    group_terms(sm, eg, 2 * ks, dv, skp, acc2);
   }
   float v = 0.0f;
 #pragma unroll
-  for (int h = 0; h < kMaxIdxHeads; ++h) v = __fmaf_rn(sm.wv[eg][h], fmaxf(acc[h], 0.0f), v);
+  for (int j = 0; j < kMaxIdxHeads / 2; ++j) {
+    float d0, d1;
+    f2_unpack(acc2[j], d0, d1);
+    v = __fmaf_rn(sm.wv[eg][2 * j], fmaxf(d0, 0.0f), v);
+    v = __fmaf_rn(sm.wv[eg][2 * j + 1], fmaxf(d1, 0.0f), v);
+  }
   float delta = 0x1p-140f;
 #pragma unroll
   for (int g = 0; g < 8; ++g) delta = __fmaf_ru(sk[g], sm.ub[eg][g], delta);
+  const bool valid = row >= 0;
   if (!valid) { v = -INFINITY; delta = 0.0f; }
   float bmax = v, bd = delta;
 #pragma unroll
@@ -237,15 +289,15 @@ __global__ void __launch_bounds__(kFThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kCStages; ++s) {
       tc::mbar_init(&sm.cfull[s], 1);             // the producer's arrival (with its TMA bytes)
-      tc::mbar_init(&sm.cempty[s], 4);            // the converter warps
+      tc::mbar_init(&sm.cempty[s], kConvWarps);   // the converter warps
     }
     for (int s = 0; s < kAStages; ++s) {
-      tc::mbar_init(&sm.afull[s], 4);             // the converter warps
+      tc::mbar_init(&sm.afull[s], kConvWarps);    // the converter warps
       tc::mbar_init(&sm.aempty[s], 1);            // the MMAs' commit
     }
     for (int i = 0; i < kDBufs; ++i) {
       tc::mbar_init(&sm.d_full[i], 1);
-      tc::mbar_init(&sm.d_empty[i], 4);
+      tc::mbar_init(&sm.d_empty[i], 4);           // the 4 warps of an epilogue group
     }
     tc::fence_mbar_init();
     sm.abort_flag = 0;
@@ -288,7 +340,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         tc::mbar_wait_bounded(&sm.d_full[(issued - 1) % kDBufs], uint32_t(((issued - 1) / kDBufs) & 1),
                               20ull * 1000 * 1000);
     }
-  } else if (wid < 6) {
+  } else if (wid < kEpiWarp0) {
     // ================= converter (warps 2-5) =================
     const int gt = tid - 64;
     const int j = gt & 3;                              // 16-byte piece of a code row: channels 32j .. 32j+31
@@ -317,38 +369,52 @@ __global__ void __launch_bounds__(kFThreads, 1)
         const uint32_t w[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
         uint32_t e[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          e[2 * u] = e2m1x4_to_e4m3x4_scaled(w[u]);
-          e[2 * u + 1] = e2m1x4_to_e4m3x4_scaled(w[u] >> 16);
-        }
+        for (int u = 0; u < 4; ++u) e2m1x8_to_e4m3x8_scaled(w[u], e[2 * u], e[2 * u + 1]);
         *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * j)) = make_uint4(e[0], e[1], e[2], e[3]);
         *reinterpret_cast<uint4*>(dst + tc::sw128_offset(r, 2 * j + 1)) = make_uint4(e[4], e[5], e[6], e[7]);
       }
-      const uint4* qsrc = reinterpret_cast<const uint4*>(sm.qb);
-      uint4* qdst = reinterpret_cast<uint4*>(dst + kAKeyBytes);
 #pragma unroll
-      for (int i = 0; i < kBBytes / 16 / kGroupThreads; ++i) qdst[gt + i * kGroupThreads] = qsrc[gt + i * kGroupThreads];
+      for (int i = 0; i < kBBytes / 16 / kConvThreads; ++i)
+        reinterpret_cast<uint4*>(dst + kAKeyBytes)[gt + i * kConvThreads] =
+            reinterpret_cast<const uint4*>(sm.qb)[gt + i * kConvThreads];
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) arrive(&sm.afull[aring.stage]);
     }
   } else {
     // ================= epilogue groups (warps 6-9: even tiles, 10-13: odd) ==========
-    const int eg = (wid - 6) >> 2;
-    const int gt = tid - 192 - eg * kGroupThreads;
+    const int eg = (wid - kEpiWarp0) >> 2;
+    const int gt = tid - 32 * kEpiWarp0 - eg * kEpiThreads;
     const int quarter = wid & 3;                       // TMEM lanes 32*quarter ..
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = uint32_t(quarter * 32) << 16;
-    int cb = 0, cur_b = -1;
-    int64_t cbase = 0;
+    // the row's cache row and key scales are loaded two of the group's tiles
+    // ahead, so that their memory latency overlaps the tiles in between
+    int pb = 0, cur_b = -1;
+    int64_t pbase = 0;
+    TileRef tA = {0, 0, 0}, tB = {0, 0, 0};
+    int64_t rA = -1, rB = -1;
+    uint2 kA = make_uint2(0, 0), kB = make_uint2(0, 0);
+    auto fetch = [&](int kk, TileRef& t, int64_t& row, uint2& ks) {
+      if (kk >= ntiles) return;
+      t = tile_of(a, sm, reindex, g0 + kk, pb, pbase);
+      row = row_of(a, reindex, t, r);
+      ks = row >= 0 ? __ldg(reinterpret_cast<const uint2*>(a.idx_scales + row * 8)) : make_uint2(0, 0);
+    };
+    fetch(eg, tA, rA, kA);
+    fetch(eg + 2, tB, rB, kB);
     for (int k = eg; k < ntiles; k += 2) {
-      const TileRef tr = tile_of(a, sm, reindex, g0 + k, cb, cbase);
+      const TileRef tr = tA;
+      const int64_t row = rA;
+      const uint2 ks = kA;
+      tA = tB;
+      rA = rB;
+      kA = kB;
+      fetch(k + 4, tB, rB, kB);
       if (tr.b != cur_b) {
         epi_query(a, sm, tr.b, gt, eg);
         cur_b = tr.b;
       }
-      const int64_t row = row_of(a, reindex, tr, r);
-      const uint2 ks = row >= 0 ? __ldg(reinterpret_cast<const uint2*>(a.idx_scales + row * 8)) : make_uint2(0, 0);
       const int buf = k % kDBufs;
       if (!wait_or_abort(sm, &sm.d_full[buf], uint32_t((k / kDBufs) & 1))) break;
       tc::tc_fence_after_sync();

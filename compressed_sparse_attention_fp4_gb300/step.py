@@ -30,7 +30,7 @@ class StepBuffers:
     kv_codes: torch.Tensor          # uint8 [rows, 256]
     kv_scales: torch.Tensor         # uint8 [rows, 32]
     kv_rope: torch.Tensor           # bf16  [rows, 64]
-    idx_k: torch.Tensor             # uint8 [rows, 128] (E4M3) or fp32 [rows, 64]
+    idx_k: torch.Tensor             # uint8 [rows, 128] (E4M3), fp32 [rows, 64] or uint8 [rows * 72] (FP4)
     page_table: torch.Tensor | None
     ctx_len: torch.Tensor           # int32 [B]
     # per-layer inputs
@@ -43,6 +43,8 @@ class StepBuffers:
     # optional decode-time append of the newest token at every Full layer
     new_latent: torch.Tensor | None = None   # bf16 [B, 512]
     new_rows: torch.Tensor | None = None     # int64 [B] cache rows of position N-1
+    new_idx_k: torch.Tensor | None = None    # bf16 [B, 128]: its indexer key (FP4 indexer keys)
+    idx_rows: int = 0                        # cache rows of the FP4 indexer-K buffer
     # outputs
     out: torch.Tensor = None        # fp32 [L, B, H, 512]
     lse: torch.Tensor = None        # fp32 [L, B, H]
@@ -67,7 +69,8 @@ class StepBuffers:
 def step_calls(sb: StepBuffers, stream=None) -> list:
     """The library calls of one decode step, in order, as (label, thunk) pairs.
 
-    Labels: ``append`` (FP4 write of the newest token), ``F`` / ``Ri`` (the
+    Labels: ``append`` (FP4 write of the newest token's latent and, for FP4
+    indexer keys, ``append_idx`` of its indexer key), ``F`` / ``Ri`` (the
     indexer of a Full / Reindex layer) and ``attn:<mode>`` (a layer's core
     attention), each with its layer number."""
     d, B = sb.dims, sb.batch
@@ -80,6 +83,9 @@ def step_calls(sb: StepBuffers, stream=None) -> list:
             if sb.new_latent is not None:
                 calls.append((f"append@{l}", lambda: csa2.fp4_kv_quantize_scatter(
                     sb.new_latent, sb.new_rows, sb.kv_codes, sb.kv_scales, stream=stream)))
+                if sb.new_idx_k is not None:
+                    calls.append((f"append_idx@{l}", lambda: csa2.fp4_idx_k_quantize_scatter(
+                        sb.new_idx_k, sb.idx_k, sb.idx_rows, sb.new_rows, stream=stream)))
             calls.append((f"F@{l}", lambda l=l: csa2.indexer_full_topk(
                 d, B, sb.idx_k, sb.page_table, sb.ctx_len, sb.idx_q[l], sb.idx_w[l], sb.pool,
                 sb.pool_len, sb.topk[l], sb.ws, stream=stream)))

@@ -21,6 +21,9 @@ library targets):
 ``1m``     B=1, N=1,048,576, as ``128k`` plus 32 planted positions drawn
            uniformly in [0, N/2) whose indexer-K row and latent are scaled by
            4 before rounding to the storage formats.
+``1m-fp4`` / ``128k-fp4``  as ``1m`` / ``128k`` with FP4 indexer keys: the
+           keys are drawn as bf16 rows and written to the cache by the
+           library's FP4 indexer-key write (the query stays bf16).
 ``codec``  bf16 slab [1,048,576, 512], N(0,1), 5 outlier channels (1% of
            512, rounded) scaled by 20.
 ``mix``    B=64, N_b uniform in [8192, 262144], KV in 64-position pages with
@@ -61,7 +64,7 @@ class Workload:
     ctx_lens: list
     idx_heads: int = 16
     idx_dim: int = 128
-    idx_k_dtype: str = "fp8"            # "fp8" (E4M3) or "fp32"
+    idx_k_dtype: str = "fp8"            # "fp8" (E4M3), "fp32" or "fp4" (bf16 keys the library writes as FP4)
     heads: int = 64
     pool_blocks: int = 2048
     topk: int = 512
@@ -97,6 +100,10 @@ def workload(name: str, **over) -> Workload:
         wl = Workload("128k", [131072] * 8, schedule=sched_128k)
     elif name == "1m":
         wl = Workload("1m", [1048576], schedule=sched_128k, planted=32)
+    elif name == "1m-fp4":
+        wl = Workload("1m-fp4", [1048576], idx_k_dtype="fp4", schedule=sched_128k, planted=32)
+    elif name == "128k-fp4":
+        wl = Workload("128k-fp4", [131072] * 8, idx_k_dtype="fp4", schedule=sched_128k)
     elif name == "mix":
         rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(0, spawn_key=(_T_MISC, 1))))
         lens = rng.integers(8192, 262144, size=64, endpoint=True).tolist()
@@ -170,7 +177,8 @@ def sequence_kv(wl: Workload, b: int, lo: int = 0, hi: int | None = None):
     """Main-KV latent (bf16 bits), rope (bf16 bits) and indexer K rows [lo, hi).
 
     Returns dict ``latent`` uint16 [n, 512], ``rope`` uint16 [n, 64] and
-    ``idx_k`` uint8 [n, Di] (E4M3) or float32 [n, Di].
+    ``idx_k`` uint8 [n, Di] (E4M3), float32 [n, Di], or uint16 [n, Di]
+    (bf16 bits, for the library's FP4 indexer-key write).
     """
     hi = wl.ctx_lens[b] if hi is None else hi
     lat = _normal_rows(wl, _T_LAT, b, lo, hi, LATENT) * _chan_scale(wl, 0, LATENT)
@@ -182,7 +190,12 @@ def sequence_kv(wl: Workload, b: int, lo: int = 0, hi: int | None = None):
         lat[pl] *= wl.planted_factor
         ik[pl] *= wl.planted_factor
     out = {"latent": to_bf16_bits(lat), "rope": to_bf16_bits(rope)}
-    out["idx_k"] = to_e4m3_bytes(ik) if wl.idx_k_dtype == "fp8" else ik.astype(np.float32)
+    if wl.idx_k_dtype == "fp8":
+        out["idx_k"] = to_e4m3_bytes(ik)
+    elif wl.idx_k_dtype == "fp4":
+        out["idx_k"] = to_bf16_bits(ik)
+    else:
+        out["idx_k"] = ik.astype(np.float32)
     return out
 
 
@@ -201,7 +214,8 @@ def layer_inputs(wl: Workload, b: int, layer: int):
 
     ``q`` uint16 [H, 576] (bf16), ``swa`` uint16 [W, 576] (bf16),
     ``swa_len`` int, and for every layer (used only by Full / Reindex layers)
-    ``idx_q`` [Hi, Di] (bf16 bits for the E4M3 indexer, float32 otherwise)
+    ``idx_q`` [Hi, Di] (bf16 bits for the E4M3 and FP4 indexers, float32
+    otherwise)
     and ``idx_w`` float32 [Hi].
     """
     r = _rng(wl, _T_Q, b, layer)
@@ -217,7 +231,7 @@ def layer_inputs(wl: Workload, b: int, layer: int):
         "q": to_bf16_bits(q),
         "swa": to_bf16_bits(swa),
         "swa_len": min(wl.swa, wl.ctx_lens[b]),
-        "idx_q": to_bf16_bits(iq) if wl.idx_k_dtype == "fp8" else iq,
+        "idx_q": to_bf16_bits(iq) if wl.idx_k_dtype in ("fp8", "fp4") else iq,
         "idx_w": iw,
     }
 
