@@ -29,6 +29,17 @@ Readings (each also in the design notes):
   lse_h = m + ln(sum_e exp(logit_e - m)) with m the max logit.  An empty E
   gives o = 0 and lse = -inf.
 
+Multi-query decode (speculative verification: [P2] DSpark paragraph, draft
+blocks over the SWA-128 window; [P3] section 3 component table, DSpark row).
+Readings:
+
+* The q_len query tokens of a sequence are its newest tokens, oldest first;
+  they are the last q_len rows of the valid SWA window and share the layer's
+  Top-K set (the indexer context is the committed prefix).
+* Query i sees every valid Top-K entry and the window rows
+  r < swa_len - (q_len - 1 - i): its own row and the older ones (causal
+  within the draft block).  q_len = 1 is the single-query decode above.
+
 Arithmetic is float64 (numpy / BLAS matrix products as library steps).
 """
 from __future__ import annotations
@@ -70,6 +81,46 @@ def sparse_attn_decode(q, latent, rope, topk, swa, swa_len, scale):
     z = p.sum(axis=1, keepdims=True)
     out = (p @ vals) / z
     lse = (m + np.log(z))[:, 0]
+    return out, lse
+
+
+def sparse_attn_decode_mq(q, latent, rope, topk, swa, swa_len, scale):
+    """Attention of q_len consecutive decode queries of one sequence.
+
+    q: [q_len, H, 576] (oldest query first); the other arguments as in
+    ``sparse_attn_decode`` (one Top-K set, one window of ``swa_len`` valid
+    rows).  One key set E = {valid Top-K entries} + {window rows} with a
+    visibility mask: query i sees all main entries and window rows
+    r < swa_len - (q_len - 1 - i).  Returns (out [q_len, H, 512], lse
+    [q_len, H]) in float64.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    ql, H = q.shape[0], q.shape[1]
+    topk = np.asarray(topk, dtype=np.int64)
+    idx = topk[topk >= 0]
+    lat_sel = np.asarray(latent[idx], dtype=np.float64).reshape(idx.shape[0], LATENT)
+    rope_sel = np.asarray(rope[idx], dtype=np.float64).reshape(idx.shape[0], ROPE)
+    nm = idx.shape[0]
+    swa = np.asarray(swa, dtype=np.float64)[:swa_len]
+    keys = np.concatenate([np.concatenate([lat_sel, rope_sel], axis=1), swa], axis=0)   # [E, 576]
+    vals = np.concatenate([lat_sel, swa[:, :LATENT]], axis=0)                           # [E, 512]
+    E = keys.shape[0]
+    # visible[i, e]: main entries always, window row r = e - nm while r < limit_i
+    limit = np.maximum(0, swa_len - (ql - 1 - np.arange(ql)))
+    r = np.arange(E) - nm
+    visible = (r[None, :] < 0) | (r[None, :] < limit[:, None])                         # [q_len, E]
+    out = np.zeros((ql, H, LATENT))
+    lse = np.full((ql, H), -np.inf)
+    if E == 0:
+        return out, lse
+    logits = scale * np.einsum("qhc,ec->qhe", q, keys)                                  # [q_len, H, E]
+    logits = np.where(visible[:, None, :], logits, -np.inf)
+    m = logits.max(axis=2, keepdims=True)                                               # [q_len, H, 1]
+    has = np.isfinite(m)
+    p = np.where(visible[:, None, :], np.exp(logits - np.where(has, m, 0.0)), 0.0)
+    z = p.sum(axis=2, keepdims=True)
+    out = np.where(has, np.einsum("qhe,ed->qhd", p, vals) / np.where(has, z, 1.0), 0.0)
+    lse = np.where(has, m + np.log(np.where(has, z, 1.0)), -np.inf)[:, :, 0]
     return out, lse
 
 
