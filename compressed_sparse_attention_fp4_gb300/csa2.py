@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "libcsa2.so")
 LATENT, ROPE, DQK, PAGE, BLOCK = 512, 64, 576, 64, 8
 IDXK_E4M3, IDXK_F32, IDXK_FP4 = 0, 1, 2
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
+MAX_QLEN = 4
 
 STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED_SHAPE",
           3: "CSA2_ERR_WORKSPACE_TOO_SMALL", 4: "CSA2_ERR_CUDA",
@@ -55,6 +56,8 @@ SIGNATURES = {
                                     _P, _P, _SZ, _P]),
     "csa2_sparse_attn_decode": (_I32, [ctypes.POINTER(CDims), _I32, _I32, _P, _P, _P, _P, _P,
                                        _P, _P, _P, _P, _F, _P, _P, _P, _SZ, _P]),
+    "csa2_sparse_attn_decode_mq": (_I32, [ctypes.POINTER(CDims), _I32, _I32, _I32, _P, _P, _P, _P, _P,
+                                          _P, _P, _P, _P, _F, _P, _P, _P, _SZ, _P]),
     "csa2_sparse_attn_decode_noalloc": (_I32, [ctypes.POINTER(CDims), _I32, _I32, _P, _P, _P, _P,
                                                _P, _P, _P, _P, _P, _F, _P, _P, _P, _P]),
     "csa2_get_device_status": (_I32, [_P, _P, ctypes.POINTER(_I32)]),
@@ -203,6 +206,17 @@ def csa2_sparse_attn_decode(dims: Dims, batch: int, mode: int, q, kv_codes, kv_s
                             ws, stream=None):
     _check("csa2_sparse_attn_decode", _lib.csa2_sparse_attn_decode(
         ctypes.byref(dims.c()), batch, mode, _ptr(q), _ptr(kv_codes), _ptr(kv_scales),
+        _ptr(kv_rope), _ptr(page_table), _ptr(ctx_len), _ptr(topk), _ptr(swa_kv), _ptr(swa_len),
+        float(scale), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def csa2_sparse_attn_decode_mq(dims: Dims, batch: int, q_len: int, mode: int, q, kv_codes, kv_scales,
+                               kv_rope, page_table, ctx_len, topk, swa_kv, swa_len, scale: float, out, lse,
+                               ws, stream=None):
+    """Multi-query decode attention: q bf16 [B, q_len, H, 576] (the newest
+    q_len tokens, oldest first), out fp32 [B, q_len, H, 512], lse [B, q_len, H]."""
+    _check("csa2_sparse_attn_decode_mq", _lib.csa2_sparse_attn_decode_mq(
+        ctypes.byref(dims.c()), batch, int(q_len), mode, _ptr(q), _ptr(kv_codes), _ptr(kv_scales),
         _ptr(kv_rope), _ptr(page_table), _ptr(ctx_len), _ptr(topk), _ptr(swa_kv), _ptr(swa_len),
         float(scale), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
 

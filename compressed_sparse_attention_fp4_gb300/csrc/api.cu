@@ -44,6 +44,46 @@ csa2_status check_ws(const csa2_dims* d, int32_t batch, const void* ws, size_t w
   return CSA2_OK;
 }
 
+// Attention call with q_len queries per sequence (1: the single-query call).
+csa2_status attn_call(const csa2_dims* d, int32_t batch, int32_t q_len, int32_t mode, const uint16_t* q,
+                      const uint8_t* kv_codes, const uint8_t* kv_scales, const uint16_t* kv_rope,
+                      const int32_t* page_table, const int32_t* ctx_len, const int32_t* topk,
+                      const uint16_t* swa_kv, const int32_t* swa_len, float scale, float* out, float* lse, void* ws,
+                      size_t ws_bytes, void* stream) {
+  csa2_status st = check_dims(d, batch);
+  if (st != CSA2_OK) return st;
+  if (mode < CSA2_MODE_FULL || mode > CSA2_MODE_REUSE) return CSA2_ERR_INVALID_ARG;
+  if (q_len < 1 || q_len > CSA2_MAX_QLEN) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (q_len > 1 && attn_uses_partials(*d)) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if ((st = check_paging(d, page_table)) != CSA2_OK) return st;
+  WsLayout L;
+  if ((st = check_ws(d, batch, ws, ws_bytes, &L)) != CSA2_OK) return st;
+  if (batch == 0) return CSA2_OK;
+  if ((st = check_attn_ptrs(d, mode, q, kv_codes, kv_scales, kv_rope, ctx_len, topk, swa_kv, swa_len, scale, out,
+                            lse)) != CSA2_OK)
+    return st;
+  AttnArgs a = {};
+  a.d = *d;
+  a.batch = batch;
+  a.q = q;
+  a.codes = kv_codes;
+  a.scales = kv_scales;
+  a.rope = kv_rope;
+  a.page_table = page_table;
+  a.ctx_len = ctx_len;
+  a.topk = topk;
+  a.swa = swa_kv;
+  a.swa_len = swa_len;
+  a.scale = scale;
+  a.out = out;
+  a.lse = lse;
+  a.ws = static_cast<uint8_t*>(ws);
+  a.L = L;
+  a.early = mode == CSA2_MODE_REUSE;
+  a.q_len = q_len;
+  return from_cuda(launch_attention(a, as_stream(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -177,35 +217,19 @@ csa2_status csa2_sparse_attn_decode(const csa2_dims* d, int32_t batch, int32_t m
                                     const int32_t* topk, const uint16_t* swa_kv,
                                     const int32_t* swa_len, float scale, float* out, float* lse,
                                     void* ws, size_t ws_bytes, void* stream) {
-  csa2_status st = check_dims(d, batch);
-  if (st != CSA2_OK) return st;
-  if (mode < CSA2_MODE_FULL || mode > CSA2_MODE_REUSE) return CSA2_ERR_INVALID_ARG;
-  if ((st = check_paging(d, page_table)) != CSA2_OK) return st;
-  WsLayout L;
-  if ((st = check_ws(d, batch, ws, ws_bytes, &L)) != CSA2_OK) return st;
-  if (batch == 0) return CSA2_OK;
-  if ((st = check_attn_ptrs(d, mode, q, kv_codes, kv_scales, kv_rope, ctx_len, topk, swa_kv, swa_len, scale, out,
-                            lse)) != CSA2_OK)
-    return st;
-  AttnArgs a = {};
-  a.d = *d;
-  a.batch = batch;
-  a.q = q;
-  a.codes = kv_codes;
-  a.scales = kv_scales;
-  a.rope = kv_rope;
-  a.page_table = page_table;
-  a.ctx_len = ctx_len;
-  a.topk = topk;
-  a.swa = swa_kv;
-  a.swa_len = swa_len;
-  a.scale = scale;
-  a.out = out;
-  a.lse = lse;
-  a.ws = static_cast<uint8_t*>(ws);
-  a.L = L;
-  a.early = mode == CSA2_MODE_REUSE;
-  return from_cuda(launch_attention(a, as_stream(stream)));
+  return attn_call(d, batch, 1, mode, q, kv_codes, kv_scales, kv_rope, page_table, ctx_len, topk, swa_kv, swa_len,
+                   scale, out, lse, ws, ws_bytes, stream);
+}
+
+csa2_status csa2_sparse_attn_decode_mq(const csa2_dims* d, int32_t batch, int32_t q_len, int32_t mode,
+                                       const uint16_t* q, const uint8_t* kv_codes,
+                                       const uint8_t* kv_scales, const uint16_t* kv_rope,
+                                       const int32_t* page_table, const int32_t* ctx_len,
+                                       const int32_t* topk, const uint16_t* swa_kv,
+                                       const int32_t* swa_len, float scale, float* out, float* lse,
+                                       void* ws, size_t ws_bytes, void* stream) {
+  return attn_call(d, batch, q_len, mode, q, kv_codes, kv_scales, kv_rope, page_table, ctx_len, topk, swa_kv,
+                   swa_len, scale, out, lse, ws, ws_bytes, stream);
 }
 
 csa2_status csa2_get_device_status(const void* ws, void* stream, int32_t* word) {

@@ -585,7 +585,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_cluster_kernel(AttnArgs 
   cg::cluster_group cl = cg::this_cluster();
   const int chunk = int(cl.block_rank()), S = int(cl.num_blocks());
   const int nhg = (a.d.heads + kCHeads - 1) / kCHeads;
-  const int b = blockIdx.y / nhg, hg = blockIdx.y % nhg;
+  // blockIdx.y: (sequence, query of the sequence, head group); query qi of a
+  // multi-query call sees the window rows below swa_len - (q_len - 1 - qi)
+  const int qrow = blockIdx.y / nhg, hg = blockIdx.y % nhg;
+  const int b = qrow / a.q_len, qi = qrow % a.q_len;
   const int H = a.d.heads, K = a.d.topk, W = a.d.swa;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const bool paged = a.page_table != nullptr;
@@ -614,7 +617,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_cluster_kernel(AttnArgs 
     // L2 prefetch (a hint: nothing is read into the SM) of what is read right
     // after the wait: the window length, this head group's query rows (36 KB)
     // and this chunk's window rows; the reads themselves follow the wait
-    const char* qb = reinterpret_cast<const char*>(a.q + (int64_t(b) * H + h0) * kDqk);
+    const char* qb = reinterpret_cast<const char*>(a.q + (int64_t(qrow) * H + h0) * kDqk);
     const char* wb = reinterpret_cast<const char*>(a.swa + (int64_t(b) * W + w0) * kDqk);
     const int qlines = (nh * kDqk * 2 + 127) / 128, wlines = (nw * kDqk * 2 + 127) / 128;
     for (int i = tid; i < qlines + wlines; i += kAttnThreads) {
@@ -632,7 +635,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_cluster_kernel(AttnArgs 
   int swl = __ldg(a.swa_len + b);
   constexpr int kQVec = kCHeads * (kDqk / 8);        // 16-byte pieces of the query rows
   constexpr int kQPer = (kQVec + kAttnThreads - 1) / kAttnThreads;
-  const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + (int64_t(b) * H + h0) * kDqk);
+  const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + (int64_t(qrow) * H + h0) * kDqk);
   uint4 qv[kQPer];
 #pragma unroll
   for (int k = 0; k < kQPer; ++k) {
@@ -652,13 +655,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_cluster_kernel(AttnArgs 
   {
     // this chunk's share of the head group's output rows: zeros
     const int z0 = nh * chunk / S, z1 = nh * (chunk + 1) / S;
-    float4* orow = reinterpret_cast<float4*>(a.out + (int64_t(b) * H + h0 + z0) * kLatent);
+    float4* orow = reinterpret_cast<float4*>(a.out + (int64_t(qrow) * H + h0 + z0) * kLatent);
     for (int i = tid; i < (z1 - z0) * 128; i += kAttnThreads) orow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   if (swl < 0 || swl > W) {
-    if (tid == 0 && chunk == 0 && hg == 0) raise_err(a.ws, CSA2_DEV_SWA_LEN);
+    if (tid == 0 && chunk == 0 && hg == 0 && qi == 0) raise_err(a.ws, CSA2_DEV_SWA_LEN);
     swl = swl < 0 ? 0 : W;
   }
+  swl = max(0, swl - (a.q_len - 1 - qi));            // the later queries' rows are not visible
   // query pieces into the swizzled K-major tile [region][head row]
 #pragma unroll
   for (int k = 0; k < kQPer; ++k) {
@@ -830,7 +834,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_cluster_kernel(AttnArgs 
     const float ms = sm.ml_all[chunk][0][tid];
     sm.fac[tid] = (ms == -INFINITY || !(L > 0.0f)) ? 0.0f : exp2f(ms - M) / L;
     if (lse_cta && tid < nh)
-      a.lse[int64_t(b) * H + h0 + tid] = L > 0.0f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
+      a.lse[int64_t(qrow) * H + h0 + tid] = L > 0.0f ? M * 0.6931471805599453f + logf(L) : -INFINITY;
   }
   ok = tc::mbar_wait_bounded(&sm.bar_o, 0) && ok;
   tc::tc_fence_after_sync();
@@ -838,7 +842,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_cluster_kernel(AttnArgs 
   if (!ok && tid == 0) raise_err(a.ws, CSA2_DEV_TIMEOUT);
   // scaled O (hi + lo parts) added into the output straight from tensor
   // memory: for one head a warp's 32 lanes hold 32 consecutive dims
-  float* dst0 = a.out + (int64_t(b) * H + h0) * kLatent + quarter * 32 + lane;
+  float* dst0 = a.out + (int64_t(qrow) * H + h0) * kLatent + quarter * 32 + lane;
 #pragma unroll 1
   for (int mt = 0; mt < 4; ++mt) {
     float hi[8], lo[8];
@@ -923,7 +927,7 @@ cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
     cudaError_t e = prepare_kernel(attn_cluster_kernel, smem, false, done);
     if (e != cudaSuccess) return e;
     CSA2_PROFILED(st, "attn_cluster_tc",
-                  (e = launch_pdl(attn_cluster_kernel, dim3(unsigned(chunks), unsigned(nhg * a.batch), 1),
+                  (e = launch_pdl(attn_cluster_kernel, dim3(unsigned(chunks), unsigned(nhg * a.batch * a.q_len), 1),
                                   dim3(kAttnThreads), smem, st, unsigned(chunks), a, a.early)));
     return e;
   }

@@ -117,6 +117,7 @@ struct AttnArgs {
   uint8_t* ws;
   WsLayout L;
   int early;                   // Reuse mode: indices and main KV may be read before the wait
+  int q_len;                   // queries per sequence (1; 2..4 for a multi-query call, cluster path only)
 };
 
 cudaError_t launch_quantize(const uint16_t* x, int64_t n, const int64_t* dst_rows, uint8_t* codes,

@@ -112,6 +112,7 @@ extern "C" csa2_status csa2_sparse_attn_decode_noalloc(
   a.ws = static_cast<uint8_t*>(scratch);
   a.L = L;
   a.early = mode == CSA2_MODE_REUSE;
+  a.q_len = 1;
   if (launch_attention(a, cs) != cudaSuccess) return CSA2_ERR_CUDA;
   if (err_word) {
     publish_error_word<<<1, 1, 0, cs>>>(err_word);

@@ -222,6 +222,9 @@ csa2_status indexer_reindex_topk(const csa2_dims* d, int32_t batch,
  *   entries, the SWA row (576) / its first 512 channels for SWA entries;
  *   logit = scale * q[b][h] . key(e);  out = softmax-weighted sum of values;
  *   lse = max logit + ln(sum exp(logit - max)); empty E: out 0, lse -inf.
+ *   out is the sum of the parts of up to 8 chunks of 128 entries, added in
+ *   the order the chunks finish: repeated calls can differ in the last bits
+ *   of out (lse does not).
  *   mode: csa2_mode.  Indices are always supplied.  CSA2_MODE_REUSE (the
  *     layer keeps the KV and indices an earlier layer used) lets the call
  *     start reading topk, ctx_len, page_table and the main-KV planes
@@ -246,6 +249,34 @@ csa2_status csa2_sparse_attn_decode(const csa2_dims* d, int32_t batch, int32_t m
                                     const int32_t* topk, const uint16_t* swa_kv,
                                     const int32_t* swa_len, float scale, float* out,
                                     float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Multi-query decode attention: q_len (1 .. CSA2_MAX_QLEN) consecutive new
+ * tokens per sequence, e.g. the draft tokens a speculative step verifies
+ * (stamatios.com "DeepSeek-V4.1 Flash comprime cache KV para 890 bytes por
+ * token", DSpark paragraph: draft blocks over the SWA-128 window; foosynaptic
+ * atlas, section 3 component table, DSpark row).  The q_len tokens are the
+ * newest rows of each sequence's SWA window and share the layer's Top-K set:
+ * query i (0-based, oldest first) of sequence b attends to the valid topk
+ * entries and to SWA rows 0 .. swa_len[b] - (q_len - 1 - i) - 1 (its own row
+ * and the older ones), with the rules of csa2_sparse_attn_decode otherwise.
+ * q_len == 1 is exactly csa2_sparse_attn_decode.
+ *   q:   device bf16 [B][q_len][H][576], 16-byte aligned
+ *   out: device fp32 [B][q_len][H][512];  lse: device fp32 [B][q_len][H]
+ *   other arguments as for csa2_sparse_attn_decode (one Top-K set, one SWA
+ *   window and one swa_len per sequence).
+ * Limit: for q_len > 1, topk + swa <= 1024 (at most 8 chunks of 128
+ * entries, merged inside one thread-block cluster); larger shapes return
+ * CSA2_ERR_UNSUPPORTED_SHAPE.
+ * Errors: as csa2_sparse_attn_decode; q_len outside 1 .. CSA2_MAX_QLEN is
+ *         CSA2_ERR_UNSUPPORTED_SHAPE. */
+#define CSA2_MAX_QLEN 4
+csa2_status csa2_sparse_attn_decode_mq(const csa2_dims* d, int32_t batch, int32_t q_len, int32_t mode,
+                                       const uint16_t* q, const uint8_t* kv_codes,
+                                       const uint8_t* kv_scales, const uint16_t* kv_rope,
+                                       const int32_t* page_table, const int32_t* ctx_len,
+                                       const int32_t* topk, const uint16_t* swa_kv,
+                                       const int32_t* swa_len, float scale, float* out, float* lse,
+                                       void* ws, size_t ws_bytes, void* stream);
 
 /* Allocation-free variant of csa2_sparse_attn_decode.  The pages describe
  * no counterpart of this call; it exists for callers that must not allocate
