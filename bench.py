@@ -52,8 +52,10 @@ def peaks():
 # algorithmic bytes (per sequence; see the design notes for the derivation)
 # ---------------------------------------------------------------------------
 def attn_layer_bytes(wl):
-    H, K, W = wl.heads, wl.topk, wl.swa
-    return (K * ENTRY_B + W * 576 * 2 + H * 576 * 2 + H * 513 * 4 + K * 4)
+    """One sequence's attention layer: its Top-K entries, window, indices, and
+    the queries and outputs of its q_len query tokens."""
+    H, K, W, Q = wl.heads, wl.topk, wl.swa, wl.q_len
+    return (K * ENTRY_B + W * 576 * 2 + Q * H * 576 * 2 + Q * H * 513 * 4 + K * 4)
 
 
 def idx_row_bytes(wl):
@@ -212,7 +214,7 @@ def oracle_query(wl, b, kv, layers):
 
 def arm_config(wl, world):
     """The workload description both arms print."""
-    return {"workload": f"decode-{wl.name}", "batch": wl.batch,
+    return {"workload": f"decode-{wl.name}", "batch": wl.batch, "q_len": wl.q_len,
             "ctx": wl.ctx_lens[0] if len(set(wl.ctx_lens)) == 1 else "mixed",
             "schedule": "".join(m[0] if m != "Ri" else "I" for m in wl.schedule),
             "l2": "flushed before every timed step (2x L2 write)",
@@ -341,8 +343,14 @@ def roofline_table(wl, kern, steps_launches, peak, peak_kind):
 # null once the kernel's source changes.  Units: indexed positions for the
 # scans, sequence-layers for the attention.
 TRAFFIC_UNITS = {
-    # decode-128k capture (1,048,576 positions): 134,321,664 B read + 3,892,224 B written
-    ("indexer_scan_tc", "035146e3c735"): (134321664 + 3892224) / 1048576,
+    # decode-128k capture (8 x 131,072 = 1,048,576 positions): 134,319,616 B read + 3,536,128 B written
+    ("indexer_scan_tc", "9b77308c25b9"): (134319616 + 3536128) / 1048576,
+    # decode-128k Reindex capture (8 x 16,384 pool positions): 16,942,848 B read, 0 written
+    ("reindex_score_tc", "9b77308c25b9"): 16942848 / 131072,
+    # decode-1m-fp4 capture (1,048,576 positions): 75,581,696 B read + 1,408,512 B written
+    ("indexer_scan_fp4", "226069cc75b6"): (75581696 + 1408512) / 1048576,
+    # decode-128k capture (8 sequence-layers): 3,930,368 B read, 0 written (outputs stay in L2)
+    ("attn_cluster_tc", "2e496407fa56"): 3930368 / 8,
 }
 
 
@@ -396,7 +404,7 @@ def measure_workload(wl, args, dev, world, flush, with_e2e):
     barrier()
     times = np.array([a.elapsed_time(b) for a, b in ev])          # ms
     t_step = max_over_ranks(float(times.mean()), world, dev)
-    qps = job_queries_per_s(world, wl.batch, t_step)
+    qps = job_queries_per_s(world, wl.batch * wl.q_len, t_step)
     status = csa2.get_device_status(sb.ws)
 
     # ---- kernels of one step and their durations (eager, the library's own
@@ -518,7 +526,7 @@ def e2e_legs(sb, args, dev, world, flush, wl):
         run_pipelined(args.steps, graphed)
         torch.cuda.synchronize()
         elapsed = max_over_ranks(time.perf_counter() - t0, world, dev)   # the slowest rank
-        return world * wl.batch * args.steps / elapsed
+        return world * wl.batch * wl.q_len * args.steps / elapsed
 
     e2e_qps = e2e_rate(True)
     e2e_eager_qps = e2e_rate(False)
@@ -686,8 +694,17 @@ def main():
         s4["clocks"] = r4["clocks"]
         del r4
         torch.cuda.empty_cache()
-        line["workloads"] = {"decode-1m": s1, "decode-1m-fp4": s4, "codec-1m-rows": codec_rates(dev)}
-    if rank == 0 and not args.no_cpu_baseline:
+        wlq = synth.workload("128k-q4")
+        rq = measure_workload(wlq, args, dev, world, flush, with_e2e=False)
+        sq = summarise(rq, peak, peak_kind)
+        sq["config"] = arm_config(wlq, world)
+        sq["clocks"] = rq["clocks"]
+        sq["unit"] = "query tokens/s (4 per sequence and step)"
+        del rq
+        torch.cuda.empty_cache()
+        line["workloads"] = {"decode-1m": s1, "decode-1m-fp4": s4, "decode-128k-q4": sq,
+                             "codec-1m-rows": codec_rates(dev)}
+    if rank == 0 and not args.no_cpu_baseline and wl.q_len == 1:
         line["cpu_baseline"] = cpu_baseline(wl)
     if world > 1:
         dist.destroy_process_group()
