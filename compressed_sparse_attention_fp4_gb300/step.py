@@ -34,7 +34,7 @@ class StepBuffers:
     page_table: torch.Tensor | None
     ctx_len: torch.Tensor           # int32 [B]
     # per-layer inputs
-    q: torch.Tensor                 # bf16 [L, B, H, 576]
+    q: torch.Tensor                 # bf16 [L, B, H, 576] ([L, B, q_len, H, 576] for q_len > 1)
     swa: torch.Tensor               # bf16 [L, B, W, 576]
     swa_len: torch.Tensor           # int32 [L, B]
     idx_q: torch.Tensor             # bf16 / fp32 [L, B, Hi, Di]
@@ -45,9 +45,10 @@ class StepBuffers:
     new_rows: torch.Tensor | None = None     # int64 [B] cache rows of position N-1
     new_idx_k: torch.Tensor | None = None    # bf16 [B, 128]: its indexer key (FP4 indexer keys)
     idx_rows: int = 0                        # cache rows of the FP4 indexer-K buffer
+    q_len: int = 1                           # query tokens per sequence (multi-query decode)
     # outputs
-    out: torch.Tensor = None        # fp32 [L, B, H, 512]
-    lse: torch.Tensor = None        # fp32 [L, B, H]
+    out: torch.Tensor = None        # fp32 [L, B, (q_len,) H, 512]
+    lse: torch.Tensor = None        # fp32 [L, B, (q_len,) H]
     topk: torch.Tensor = None       # int32 [L, B, K]  (indices each layer used)
     pool: torch.Tensor = None       # int32 [B, P]
     pool_len: torch.Tensor = None   # int32 [B]
@@ -57,8 +58,9 @@ class StepBuffers:
     def allocate_outputs(self):
         L, B, d = len(self.schedule), self.batch, self.dims
         dev = self.q.device
-        self.out = torch.empty((L, B, d.heads, csa2.LATENT), dtype=torch.float32, device=dev)
-        self.lse = torch.empty((L, B, d.heads), dtype=torch.float32, device=dev)
+        qd = () if self.q_len == 1 else (self.q_len,)
+        self.out = torch.empty((L, B) + qd + (d.heads, csa2.LATENT), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((L, B) + qd + (d.heads,), dtype=torch.float32, device=dev)
         self.topk = torch.full((L, B, d.topk), -1, dtype=torch.int32, device=dev)
         self.pool = torch.full((B, d.pool_blocks), -1, dtype=torch.int32, device=dev)
         self.pool_len = torch.zeros((B,), dtype=torch.int32, device=dev)
@@ -103,10 +105,16 @@ def step_calls(sb: StepBuffers, stream=None) -> list:
             m = csa2.MODE_REUSE
         else:
             raise ValueError(f"unknown layer mode {mode!r}")
-        calls.append((f"attn:{mode}@{l}", lambda l=l, m=m, cur=cur: csa2.csa2_sparse_attn_decode(
-            d, B, m, sb.q[l], sb.kv_codes, sb.kv_scales, sb.kv_rope, sb.page_table, sb.ctx_len,
-            sb.topk[cur], sb.swa[l], sb.swa_len[l], sb.scale, sb.out[l], sb.lse[l], sb.ws,
-            stream=stream)))
+        if sb.q_len == 1:
+            calls.append((f"attn:{mode}@{l}", lambda l=l, m=m, cur=cur: csa2.csa2_sparse_attn_decode(
+                d, B, m, sb.q[l], sb.kv_codes, sb.kv_scales, sb.kv_rope, sb.page_table, sb.ctx_len,
+                sb.topk[cur], sb.swa[l], sb.swa_len[l], sb.scale, sb.out[l], sb.lse[l], sb.ws,
+                stream=stream)))
+        else:
+            calls.append((f"attn:{mode}@{l}", lambda l=l, m=m, cur=cur: csa2.csa2_sparse_attn_decode_mq(
+                d, B, sb.q_len, m, sb.q[l], sb.kv_codes, sb.kv_scales, sb.kv_rope, sb.page_table,
+                sb.ctx_len, sb.topk[cur], sb.swa[l], sb.swa_len[l], sb.scale, sb.out[l], sb.lse[l], sb.ws,
+                stream=stream)))
     return calls
 
 

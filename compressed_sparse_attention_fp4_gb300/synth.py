@@ -26,6 +26,9 @@ library targets):
            library's FP4 indexer-key write (the query stays bf16).
 ``codec``  bf16 slab [1,048,576, 512], N(0,1), 5 outlier channels (1% of
            512, rounded) scaled by 20.
+``128k-q4`` as ``128k`` with 4 query tokens per sequence and layer (the
+           newest tokens, e.g. drafts a speculative step verifies): the
+           attention query is [4, H, 576], the window and Top-K are shared.
 ``mix``    B=64, N_b uniform in [8192, 262144], KV in 64-position pages with
            a seeded random physical page order, schedule blocks of
            (F, Ru, Ru, Ri, Ru, Ru), as ``128k`` otherwise.
@@ -73,6 +76,7 @@ class Workload:
     paged: bool = False
     schedule: list = field(default_factory=lambda: ["F"] + ["Ru"] * 5 + ["Ri"] + ["Ru"] * 5)
     q_sigma: float = 1.0 / math.sqrt(576.0)
+    q_len: int = 1                      # query tokens per sequence and layer (multi-query decode)
     planted: int = 0
     planted_factor: float = 4.0
     seed: int = 0
@@ -102,6 +106,8 @@ def workload(name: str, **over) -> Workload:
         wl = Workload("1m", [1048576], schedule=sched_128k, planted=32)
     elif name == "1m-fp4":
         wl = Workload("1m-fp4", [1048576], idx_k_dtype="fp4", schedule=sched_128k, planted=32)
+    elif name == "128k-q4":
+        wl = Workload("128k-q4", [131072] * 8, schedule=sched_128k, q_len=4)
     elif name == "128k-fp4":
         wl = Workload("128k-fp4", [131072] * 8, idx_k_dtype="fp4", schedule=sched_128k)
     elif name == "mix":
@@ -219,7 +225,8 @@ def layer_inputs(wl: Workload, b: int, layer: int):
     and ``idx_w`` float32 [Hi].
     """
     r = _rng(wl, _T_Q, b, layer)
-    q = r.standard_normal((wl.heads, D_QK), dtype=np.float32) * np.float32(wl.q_sigma)
+    q = r.standard_normal((wl.q_len * wl.heads, D_QK), dtype=np.float32) * np.float32(wl.q_sigma)
+    q = q.reshape((wl.heads, D_QK) if wl.q_len == 1 else (wl.q_len, wl.heads, D_QK))
     r = _rng(wl, _T_SWA, b, layer)
     swa = r.standard_normal((wl.swa, D_QK), dtype=np.float32)
     swa[:, :LATENT] *= _chan_scale(wl, 0, LATENT)

@@ -85,7 +85,8 @@ def build(wl: synth.Workload, device="cuda", threads=None, keep_new_token=True) 
         del lat
     L = len(wl.schedule)
     H, W, Hi, Di = wl.heads, wl.swa, wl.idx_heads, wl.idx_dim
-    q = np.empty((L, B, H, synth.D_QK), dtype=np.uint16)
+    qshape = (L, B, H, synth.D_QK) if wl.q_len == 1 else (L, B, wl.q_len, H, synth.D_QK)
+    q = np.empty(qshape, dtype=np.uint16)
     swa = np.empty((L, B, W, synth.D_QK), dtype=np.uint16)
     swa_len = np.empty((L, B), dtype=np.int32)
     bf16_q = wl.idx_k_dtype in ("fp8", "fp4")
@@ -107,5 +108,5 @@ def build(wl: synth.Workload, device="cuda", threads=None, keep_new_token=True) 
         idx_w=torch.from_numpy(iw).to(dev), scale=wl.scale,
         new_latent=new_latent if keep_new_token else None,
         new_rows=new_rows if keep_new_token else None,
-        new_idx_k=new_idx_k if (fp4k and keep_new_token) else None, idx_rows=rows)
+        new_idx_k=new_idx_k if (fp4k and keep_new_token) else None, idx_rows=rows, q_len=wl.q_len)
     return sb.allocate_outputs()
