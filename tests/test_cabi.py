@@ -118,3 +118,47 @@ def test_workspace_layout_mirror(mod):
     off = ws_offsets(d, 3)
     assert off["blk_delta"] > off["blk_scores"] > off["pos_scores"] >= 256
     assert mod.workspace_size(d, 3) > off["ri_delta"]
+
+
+def test_host_argument_errors_fp4_and_multi_query(mod):
+    """The FP4 indexer-key write, the FP4 indexer dtype and the multi-query
+    attention call validate on the host, before any CUDA call."""
+    lib = mod._lib
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    # FP4 indexer-key write: null / negative / misaligned / too many rows without destinations
+    assert lib.fp4_idx_k_quantize_scatter(None, 4, None, fake, 16, None) == 1
+    assert lib.fp4_idx_k_quantize_scatter(fake, -1, None, fake, 16, None) == 1
+    assert lib.fp4_idx_k_quantize_scatter(fake, 4, None, fake, -1, None) == 1
+    assert lib.fp4_idx_k_quantize_scatter(P(0x10008), 4, None, fake, 16, None) == 1
+    assert lib.fp4_idx_k_quantize_scatter(fake, 4, None, P(0x10008), 16, None) == 1
+    assert lib.fp4_idx_k_quantize_scatter(fake, 4, P(0x10004), fake, 16, None) == 1
+    assert lib.fp4_idx_k_quantize_scatter(fake, 17, None, fake, 16, None) == 1
+    assert lib.fp4_idx_k_quantize_scatter(None, 0, None, None, 0, None) == 0      # empty: no-op
+    # FP4 indexer dims: idx_dim must be 128; the FP4 query must be 16-byte aligned
+    d4 = mod.Dims(idx_k_dtype=mod.IDXK_FP4, max_ctx=1024, pool_blocks=64, topk=128)
+    assert mod.workspace_size(d4, 2) > 0
+    with pytest.raises(mod.Csa2Error) as e:
+        mod.workspace_size(mod.Dims(idx_k_dtype=mod.IDXK_FP4, idx_dim=64), 1)
+    assert e.value.code == 2
+    ws = mod.workspace_size(d4, 2)
+    wsp = P(0x20000)
+    args = [fake, None, fake, P(0x10004)] + [fake] * 4      # idx_q only 4-byte aligned
+    assert lib.indexer_full_topk(ctypes.byref(d4.c()), 2, *args, wsp, ws, None) == 1
+    # multi-query attention: q_len outside 1..4, more than 8 chunks with q_len > 1, bad mode
+    d = mod.Dims(max_ctx=1024, pool_blocks=64, topk=512)
+    dc = ctypes.byref(d.c())
+    wsa = mod.workspace_size(d, 2)
+    a = [fake] * 4 + [None] + [fake] * 4
+    for ql in (0, 5, -1):
+        assert lib.csa2_sparse_attn_decode_mq(dc, 2, ql, 0, *a, 0.1, fake, fake, wsp, wsa, None) == 2
+    dbig = mod.Dims(max_ctx=4096, pool_blocks=64, topk=1024)
+    wsb = mod.workspace_size(dbig, 2)
+    assert lib.csa2_sparse_attn_decode_mq(ctypes.byref(dbig.c()), 2, 2, 0, *a, 0.1, fake, fake, wsp, wsb,
+                                          None) == 2
+    assert lib.csa2_sparse_attn_decode_mq(dc, 2, 2, 3, *a, 0.1, fake, fake, wsp, wsa, None) == 1
+    assert lib.csa2_sparse_attn_decode_mq(dc, 2, 2, 0, *a, float("nan"), fake, fake, wsp, wsa, None) == 1
+    # q_len 1 with more than 8 chunks stays allowed (the split-KV path): it gets past the
+    # shape checks and stops at the misaligned workspace
+    assert lib.csa2_sparse_attn_decode_mq(ctypes.byref(dbig.c()), 2, 1, 0, *a, 0.1, fake, fake, P(0x20010),
+                                          wsb, None) == 1
