@@ -21,6 +21,7 @@ LATENT, ROPE, DQK, PAGE, BLOCK = 512, 64, 576, 64, 8
 IDXK_E4M3, IDXK_F32, IDXK_FP4 = 0, 1, 2
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
 MAX_QLEN = 4
+IDX_EARLY_INPUTS = 1
 
 STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED_SHAPE",
           3: "CSA2_ERR_WORKSPACE_TOO_SMALL", 4: "CSA2_ERR_CUDA",
@@ -54,6 +55,10 @@ SIGNATURES = {
                                  _P, _SZ, _P]),
     "indexer_reindex_topk": (_I32, [ctypes.POINTER(CDims), _I32, _P, _P, _P, _P, _P, _P, _P,
                                     _P, _P, _SZ, _P]),
+    "indexer_full_topk_ex": (_I32, [ctypes.POINTER(CDims), _I32, _I32, _P, _P, _P, _P, _P, _P, _P,
+                                    _P, _P, _SZ, _P]),
+    "indexer_reindex_topk_ex": (_I32, [ctypes.POINTER(CDims), _I32, _I32, _P, _P, _P, _P, _P, _P,
+                                       _P, _P, _P, _SZ, _P]),
     "csa2_sparse_attn_decode": (_I32, [ctypes.POINTER(CDims), _I32, _I32, _P, _P, _P, _P, _P,
                                        _P, _P, _P, _P, _F, _P, _P, _P, _SZ, _P]),
     "csa2_sparse_attn_decode_mq": (_I32, [ctypes.POINTER(CDims), _I32, _I32, _I32, _P, _P, _P, _P, _P,
@@ -186,7 +191,14 @@ def fp4_kv_dequantize(codes: torch.Tensor, scales: torch.Tensor, y: torch.Tensor
 
 
 def indexer_full_topk(dims: Dims, batch: int, idx_k, page_table, ctx_len, idx_q, w,
-                      pool_out, pool_len_out, topk_out, ws, stream=None):
+                      pool_out, pool_len_out, topk_out, ws, stream=None, flags: int = 0):
+    """flags: IDX_EARLY_INPUTS (see indexer_full_topk_ex in include/csa2.h) or 0."""
+    if flags:
+        _check("indexer_full_topk_ex", _lib.indexer_full_topk_ex(
+            ctypes.byref(dims.c()), batch, int(flags), _ptr(idx_k), _ptr(page_table), _ptr(ctx_len),
+            _ptr(idx_q), _ptr(w), _ptr(pool_out), _ptr(pool_len_out), _ptr(topk_out), _ptr(ws), ws.numel(),
+            _stream(stream)))
+        return
     _check("indexer_full_topk", _lib.indexer_full_topk(
         ctypes.byref(dims.c()), batch, _ptr(idx_k), _ptr(page_table), _ptr(ctx_len), _ptr(idx_q),
         _ptr(w), _ptr(pool_out), _ptr(pool_len_out), _ptr(topk_out), _ptr(ws), ws.numel(),
@@ -194,7 +206,14 @@ def indexer_full_topk(dims: Dims, batch: int, idx_k, page_table, ctx_len, idx_q,
 
 
 def indexer_reindex_topk(dims: Dims, batch: int, idx_k, page_table, ctx_len, idx_q, w,
-                         pool_blocks, pool_len, topk_out, ws, stream=None):
+                         pool_blocks, pool_len, topk_out, ws, stream=None, flags: int = 0):
+    """flags: IDX_EARLY_INPUTS (see indexer_reindex_topk_ex in include/csa2.h) or 0."""
+    if flags:
+        _check("indexer_reindex_topk_ex", _lib.indexer_reindex_topk_ex(
+            ctypes.byref(dims.c()), batch, int(flags), _ptr(idx_k), _ptr(page_table), _ptr(ctx_len),
+            _ptr(idx_q), _ptr(w), _ptr(pool_blocks), _ptr(pool_len), _ptr(topk_out), _ptr(ws), ws.numel(),
+            _stream(stream)))
+        return
     _check("indexer_reindex_topk", _lib.indexer_reindex_topk(
         ctypes.byref(dims.c()), batch, _ptr(idx_k), _ptr(page_table), _ptr(ctx_len), _ptr(idx_q),
         _ptr(w), _ptr(pool_blocks), _ptr(pool_len), _ptr(topk_out), _ptr(ws), ws.numel(),

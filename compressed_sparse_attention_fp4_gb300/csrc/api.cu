@@ -151,6 +151,15 @@ csa2_status indexer_full_topk(const csa2_dims* d, int32_t batch, const void* idx
                               const int32_t* page_table, const int32_t* ctx_len, const void* idx_q,
                               const float* w, int32_t* pool_blocks_out, int32_t* pool_len_out,
                               int32_t* topk_out, void* ws, size_t ws_bytes, void* stream) {
+  return indexer_full_topk_ex(d, batch, 0, idx_k, page_table, ctx_len, idx_q, w, pool_blocks_out, pool_len_out,
+                              topk_out, ws, ws_bytes, stream);
+}
+
+csa2_status indexer_full_topk_ex(const csa2_dims* d, int32_t batch, int32_t flags, const void* idx_k,
+                                 const int32_t* page_table, const int32_t* ctx_len, const void* idx_q,
+                                 const float* w, int32_t* pool_blocks_out, int32_t* pool_len_out,
+                                 int32_t* topk_out, void* ws, size_t ws_bytes, void* stream) {
+  if (flags & ~int32_t(CSA2_IDX_EARLY_INPUTS)) return CSA2_ERR_INVALID_ARG;
   csa2_status st = check_dims(d, batch);
   if (st != CSA2_OK) return st;
   if ((st = check_paging(d, page_table)) != CSA2_OK) return st;
@@ -175,6 +184,7 @@ csa2_status indexer_full_topk(const csa2_dims* d, int32_t batch, const void* idx
   a.topk_out = topk_out;
   a.ws = static_cast<uint8_t*>(ws);
   a.L = L;
+  a.early = (flags & CSA2_IDX_EARLY_INPUTS) ? 1 : 0;
   return from_cuda(launch_full(a, as_stream(stream)));
 }
 
@@ -183,6 +193,15 @@ csa2_status indexer_reindex_topk(const csa2_dims* d, int32_t batch, const void* 
                                  const void* idx_q, const float* w, const int32_t* pool_blocks,
                                  const int32_t* pool_len, int32_t* topk_out, void* ws,
                                  size_t ws_bytes, void* stream) {
+  return indexer_reindex_topk_ex(d, batch, 0, idx_k, page_table, ctx_len, idx_q, w, pool_blocks, pool_len, topk_out,
+                                 ws, ws_bytes, stream);
+}
+
+csa2_status indexer_reindex_topk_ex(const csa2_dims* d, int32_t batch, int32_t flags, const void* idx_k,
+                                    const int32_t* page_table, const int32_t* ctx_len, const void* idx_q,
+                                    const float* w, const int32_t* pool_blocks, const int32_t* pool_len,
+                                    int32_t* topk_out, void* ws, size_t ws_bytes, void* stream) {
+  if (flags & ~int32_t(CSA2_IDX_EARLY_INPUTS)) return CSA2_ERR_INVALID_ARG;
   csa2_status st = check_dims(d, batch);
   if (st != CSA2_OK) return st;
   if ((st = check_paging(d, page_table)) != CSA2_OK) return st;
@@ -207,6 +226,7 @@ csa2_status indexer_reindex_topk(const csa2_dims* d, int32_t batch, const void* 
   a.topk_out = topk_out;
   a.ws = static_cast<uint8_t*>(ws);
   a.L = L;
+  a.early = (flags & CSA2_IDX_EARLY_INPUTS) ? 1 : 0;
   return from_cuda(launch_reindex(a, as_stream(stream)));
 }
 

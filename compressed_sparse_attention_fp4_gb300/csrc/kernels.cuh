@@ -97,6 +97,7 @@ struct IdxArgs {
   uint8_t* ws;
   WsLayout L;
   float err_coef;              // delta = err_coef * sum_h|w_h|*||q_h||_1 * max|k|
+  int early;                   // CSA2_IDX_EARLY_INPUTS: keys, lengths, pages (and the pool) may be read before the wait
 };
 
 struct AttnArgs {

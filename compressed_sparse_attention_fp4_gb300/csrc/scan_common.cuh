@@ -192,10 +192,12 @@ __device__ inline void gather_pool_tile(const CUtensorMap* map, uint8_t* dst, ui
 // window of up to kStages tiles (pool ids and lengths, then page table: the
 // loads of all its blocks in flight together), then gathers each tile with
 // one 8-row TMA box per block into stage `base + stage * stride`.
+// wait_first: the producer has not waited for the previous kernel yet (the
+// call's inputs allowed it); it does so once the first ring of loads is out.
 template <int kRowBytes, int kStages, class Sm>
 __device__ inline void produce_reindex(const IdxArgs& a, const CUtensorMap* map, Sm& sm, uint8_t* base,
                                        uint32_t stride, uint64_t* full, uint64_t* empty, int64_t g0, int ntiles,
-                                       int lane) {
+                                       int lane, bool wait_first) {
   constexpr int kResolvePer = kStages * 16 / 32;   // blocks a producer lane resolves per window
   static_assert(kResolvePer * 32 == kStages * 16, "whole windows of tiles");
   const uint64_t policy = tc::l2_policy_evict_first();
@@ -264,7 +266,12 @@ __device__ inline void produce_reindex(const IdxArgs& a, const CUtensorMap* map,
       gather_pool_tile<kRowBytes>(map, base + size_t(ring.stage) * stride, &full[ring.stage], lane < 16 ? rb : -1,
                                   lane, policy);
     }
+    if (wait_first) {
+      pdl_wait();
+      wait_first = false;
+    }
   }
+  if (wait_first) pdl_wait();
   // after an abort, let the copies still in flight land before the CTA exits
   if (sm.abort_flag && lane == 0)
     for (int j = max(0, k - kStages); j < k; ++j)
@@ -274,17 +281,22 @@ __device__ inline void produce_reindex(const IdxArgs& a, const CUtensorMap* map,
 // Producer thread for Full tiles: one TMA tile (or two page boxes) per stage.
 template <int kRowBytes, int kStages, class Sm>
 __device__ inline void produce_full(const IdxArgs& a, const CUtensorMap* map, Sm& sm, uint8_t* base, uint32_t stride,
-                                    uint64_t* full, uint64_t* empty, int64_t g0, int ntiles) {
+                                    uint64_t* full, uint64_t* empty, int64_t g0, int ntiles, bool wait_first) {
   const uint64_t policy = tc::l2_policy_evict_first();
   int pb = 0;
   int64_t pbase = 0;
   int k = 0;
   RingPos<kStages> ring;
   for (; k < ntiles; ++k, ring.next()) {
+    if (wait_first && k == kStages) {
+      pdl_wait();
+      wait_first = false;
+    }
     if (k >= kStages && !wait_or_abort(sm, &empty[ring.stage], ring.phase ^ 1u)) break;
     issue_tile_load<kRowBytes>(a, map, base + size_t(ring.stage) * stride, &full[ring.stage],
                                tile_of(a, sm, false, g0 + k, pb, pbase), policy);
   }
+  if (wait_first) pdl_wait();
   // after an abort, let the copies still in flight land before the CTA exits
   if (sm.abort_flag)
     for (int j = max(0, k - kStages); j < k; ++j)

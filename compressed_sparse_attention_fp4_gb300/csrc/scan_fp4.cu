@@ -273,8 +273,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
   FScanSmem& sm = *reinterpret_cast<FScanSmem*>(smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u));
   __shared__ int64_t total_tiles_s;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  pdl_wait();
-  pdl_launch_dependents();
+  // early inputs: the lengths and the keys may be read before the previous
+  // kernel finishes; everything else waits for it (below)
+  if (!a.early) {
+    pdl_wait();
+    pdl_launch_dependents();
+  }
   if (wid == 0) {
     const int64_t tsum = count_tiles(a, sm, reindex, lane);
     if (lane == 0) total_tiles_s = tsum;
@@ -307,13 +311,20 @@ __global__ void __launch_bounds__(kFThreads, 1)
   tc::tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_slot;
   const int ntiles = int(g1 - g0);
+  if (a.early && wid != 0) {
+    // the producer (warp 0) waits once its first ring of codes is in flight
+    pdl_wait();
+    pdl_launch_dependents();
+  }
 
   if (wid == 0) {
     // ================= producer: FP4 codes =================
     if (reindex)
-      produce_reindex<64, kCStages>(a, &kmap, sm, sm.craw[0], kCodeBytes, sm.cfull, sm.cempty, g0, ntiles, lane);
+      produce_reindex<64, kCStages>(a, &kmap, sm, sm.craw[0], kCodeBytes, sm.cfull, sm.cempty, g0, ntiles, lane,
+                                    a.early != 0);
     else if (lane == 0)
-      produce_full<64, kCStages>(a, &kmap, sm, sm.craw[0], kCodeBytes, sm.cfull, sm.cempty, g0, ntiles);
+      produce_full<64, kCStages>(a, &kmap, sm, sm.craw[0], kCodeBytes, sm.cfull, sm.cempty, g0, ntiles,
+                                 a.early != 0);
   } else if (wid == 1) {
     // ================= MMA issuer =================
     if (lane == 0) {

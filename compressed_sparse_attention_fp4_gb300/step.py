@@ -88,15 +88,19 @@ def step_calls(sb: StepBuffers, stream=None) -> list:
                 if sb.new_idx_k is not None:
                     calls.append((f"append_idx@{l}", lambda: csa2.fp4_idx_k_quantize_scatter(
                         sb.new_idx_k, sb.idx_k, sb.idx_rows, sb.new_rows, stream=stream)))
-            calls.append((f"F@{l}", lambda l=l: csa2.indexer_full_topk(
+            # the keys are not written by the call before (the latent append or an
+            # attention call) unless the newest token's FP4 key write precedes it
+            fl = csa2.IDX_EARLY_INPUTS if sb.new_idx_k is None else 0
+            calls.append((f"F@{l}", lambda l=l, fl=fl: csa2.indexer_full_topk(
                 d, B, sb.idx_k, sb.page_table, sb.ctx_len, sb.idx_q[l], sb.idx_w[l], sb.pool,
-                sb.pool_len, sb.topk[l], sb.ws, stream=stream)))
+                sb.pool_len, sb.topk[l], sb.ws, stream=stream, flags=fl)))
             cur = l
             m = csa2.MODE_FULL
         elif mode == "Ri":
+            # follows an attention call, which writes none of the keys, lengths or pool
             calls.append((f"Ri@{l}", lambda l=l: csa2.indexer_reindex_topk(
                 d, B, sb.idx_k, sb.page_table, sb.ctx_len, sb.idx_q[l], sb.idx_w[l], sb.pool,
-                sb.pool_len, sb.topk[l], sb.ws, stream=stream)))
+                sb.pool_len, sb.topk[l], sb.ws, stream=stream, flags=csa2.IDX_EARLY_INPUTS)))
             cur = l
             m = csa2.MODE_REINDEX
         elif mode == "Ru":

@@ -213,6 +213,28 @@ csa2_status indexer_reindex_topk(const csa2_dims* d, int32_t batch,
                                  const int32_t* pool_len, int32_t* topk_out,
                                  void* ws, size_t ws_bytes, void* stream);
 
+/* indexer_full_topk / indexer_reindex_topk with flags (0: the plain calls).
+ * CSA2_IDX_EARLY_INPUTS: idx_k, page_table and ctx_len (and, for Reindex,
+ * pool_blocks and pool_len) are not written by the operation enqueued just
+ * before this call on the stream (they were written by earlier work, before
+ * that operation began), so the call may start reading them -- the scan
+ * streams its first key tiles -- while that operation is still running.
+ * idx_q, w, the outputs and the workspace are accessed only after it has
+ * finished.  In a decode step this holds for a Full layer that follows the
+ * latent append (not the indexer-key write) and for a Reindex layer that
+ * follows an attention call.  Other bits: CSA2_ERR_INVALID_ARG. */
+#define CSA2_IDX_EARLY_INPUTS 1
+csa2_status indexer_full_topk_ex(const csa2_dims* d, int32_t batch, int32_t flags,
+                                 const void* idx_k, const int32_t* page_table,
+                                 const int32_t* ctx_len, const void* idx_q, const float* w,
+                                 int32_t* pool_blocks_out, int32_t* pool_len_out,
+                                 int32_t* topk_out, void* ws, size_t ws_bytes, void* stream);
+csa2_status indexer_reindex_topk_ex(const csa2_dims* d, int32_t batch, int32_t flags,
+                                    const void* idx_k, const int32_t* page_table,
+                                    const int32_t* ctx_len, const void* idx_q, const float* w,
+                                    const int32_t* pool_blocks, const int32_t* pool_len,
+                                    int32_t* topk_out, void* ws, size_t ws_bytes, void* stream);
+
 /* Sparse MLA-style decode attention, all layer modes (atlas 3.2 mode table
  * and figure "异构 KV": main Q reads the Top-K main-KV entries and the
  * exact SWA KV, merged; Reuse keeps KV and indices and changes only Q).

@@ -162,3 +162,15 @@ def test_host_argument_errors_fp4_and_multi_query(mod):
     # shape checks and stops at the misaligned workspace
     assert lib.csa2_sparse_attn_decode_mq(ctypes.byref(dbig.c()), 2, 1, 0, *a, 0.1, fake, fake, P(0x20010),
                                           wsb, None) == 1
+
+
+def test_indexer_ex_flags(mod):
+    lib = mod._lib
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    d = mod.Dims(max_ctx=1024, pool_blocks=64, topk=128)
+    ws = mod.workspace_size(d, 2)
+    args = [fake, None] + [fake] * 6
+    assert lib.indexer_full_topk_ex(ctypes.byref(d.c()), 2, 2, *args, fake, ws, None) == 1      # unknown flag
+    assert lib.indexer_full_topk_ex(ctypes.byref(d.c()), 2, 1, *args, fake, ws - 1, None) == 3   # checks as usual
+    assert lib.indexer_reindex_topk_ex(ctypes.byref(d.c()), 2, -1, fake, None, *([fake] * 6), fake, ws, None) == 1

@@ -168,3 +168,32 @@ def test_eight_heads_odd_band():
     w2 = rng.random(p.w_raw.shape).astype(np.float32)
     tk = run_reindex(p, pool, plen, qd, torch.from_numpy(w2).cuda())
     check_reindex(p, pool, tk, bf16_f64(raw), w2)
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_early_inputs_flag_same_ids(paged):
+    """With IDX_EARLY_INPUTS the scans stream their first key tiles before the
+    wait on the previous kernel; the ids are those of the plain calls (and of
+    the oracle), right after a kernel that writes other memory."""
+    from compressed_sparse_attention_fp4_gb300 import csa2
+    p = make_problem([70001, 9000, 17], paged=paged, seed=23, with_kv=False)
+    pool, plen, topk = run_full(p)
+    check_full(p, pool, plen, topk)
+    scratch = torch.zeros(1 << 24, dtype=torch.uint8, device="cuda")
+    pool2 = torch.full_like(pool, -7)
+    plen2 = torch.zeros_like(plen)
+    tk2 = torch.full_like(topk, -7)
+    scratch.fill_(1)                                    # the kernel just before: writes other memory
+    csa2.indexer_full_topk(p.dims, p.B, p.idx_k, p.page_table, p.ctx, p.idx_q, p.w, pool2, plen2, tk2, p.ws,
+                           flags=csa2.IDX_EARLY_INPUTS)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(pool2.cpu().numpy(), pool.cpu().numpy())
+    np.testing.assert_array_equal(plen2.cpu().numpy(), plen.cpu().numpy())
+    np.testing.assert_array_equal(tk2.cpu().numpy(), topk.cpu().numpy())
+    tk_ri = run_reindex(p, pool, plen)
+    tk_ri2 = torch.full_like(topk, -7)
+    scratch.fill_(2)
+    csa2.indexer_reindex_topk(p.dims, p.B, p.idx_k, p.page_table, p.ctx, p.idx_q, p.w, pool, plen, tk_ri2, p.ws,
+                              flags=csa2.IDX_EARLY_INPUTS)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(tk_ri2.cpu().numpy(), tk_ri.cpu().numpy())

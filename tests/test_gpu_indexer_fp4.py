@@ -165,3 +165,21 @@ def test_fp4_flat_topk_equals_pool_topk():
     s = ofp4.scores(qc, qs, p.w_raw[0].astype(np.float64), kc, ks)
     flat = np.sort(oix.top_order(s, p.K))
     np.testing.assert_array_equal(topk.cpu().numpy()[0], flat)
+
+
+def test_fp4_early_inputs_flag_same_ids():
+    p = make_fp4_problem([70001, 1000], seed=24)
+    pool, plen, topk = run_full(p)
+    check_full(p, pool, plen, topk)
+    pool2, plen2, tk2 = torch.full_like(pool, -7), torch.zeros_like(plen), torch.full_like(topk, -7)
+    csa2.indexer_full_topk(p.dims, p.B, p.idx_k, p.page_table, p.ctx, p.idx_q, p.w, pool2, plen2, tk2, p.ws,
+                           flags=csa2.IDX_EARLY_INPUTS)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(tk2.cpu().numpy(), topk.cpu().numpy())
+    np.testing.assert_array_equal(pool2.cpu().numpy(), pool.cpu().numpy())
+    tk_ri = run_reindex(p, pool, plen)
+    tk_ri2 = torch.full_like(topk, -7)
+    csa2.indexer_reindex_topk(p.dims, p.B, p.idx_k, p.page_table, p.ctx, p.idx_q, p.w, pool, plen, tk_ri2, p.ws,
+                              flags=csa2.IDX_EARLY_INPUTS)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(tk_ri2.cpu().numpy(), tk_ri.cpu().numpy())
