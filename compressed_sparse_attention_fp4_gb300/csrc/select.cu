@@ -1189,7 +1189,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
   const int b = blockIdx.y;
-  pdl_wait();
+  // This kernel starts only once the scan before it (same call) has passed its
+  // own wait: the work before the call is complete.  The query, the weights,
+  // the lengths and the pool, which the scan does not write, are read before
+  // waiting for the scan; its scores and everything else after.
   pdl_launch_dependents();
   SelCtx c;
   c.b = b;
@@ -1214,6 +1217,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
     load_query_fp4(a, sm, b);
   else
     load_query_factors(a, sm, b);
+  pdl_wait();
   c.n_ctx = check_ctx(n_raw, a.d, a.page_table != nullptr, a.ws);
   const int64_t scap = a.L.sel_cap;
   double* g_exact = reinterpret_cast<double*>(a.ws + a.L.sel_exact) + int64_t(b) * scap;
