@@ -1047,7 +1047,11 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
       bits &= bits - 1;
       int64_t gi = base + wv * 32 + bp;
       int64_t id = (kind == kBlocks) ? gi : int64_t(sm.pool_ids[gi >> 3]) * kBlock + (gi & 7);
-      if (off + o < k) out[off + o] = int32_t(id);
+      if (off + o < k) {
+        out[off + o] = int32_t(id);
+        // one CTA: the pool also goes straight to shared memory for the Top-K
+        if (kind == kBlocks && c.cs == 1) sm.pool_ids[off + o] = int32_t(id);
+      }
       ++o;
     }
   }
@@ -1236,7 +1240,12 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
       if (threadIdx.x == 0) a.pool_len_out[b] = int32_t(p_sel);
     }
     cl_sync(c);                    // every rank's pool ids are written (read through L2)
-    for (int i = threadIdx.x; i < kMaxPool; i += blockDim.x) sm.pool_ids[i] = i < p_sel ? __ldcg(pool + i) : -1;
+    if (c.cs > 1) {
+      for (int i = threadIdx.x; i < kMaxPool; i += blockDim.x) sm.pool_ids[i] = i < p_sel ? __ldcg(pool + i) : -1;
+    } else {
+      for (int i = threadIdx.x; i < kMaxPool; i += blockDim.x)
+        if (i >= p_sel) sm.pool_ids[i] = -1;       // ids below p_sel: written by the selection
+    }
     __syncthreads();
     // valid pool positions (the context's last block may be partial)
     int has_last = __syncthreads_or(threadIdx.x < kMaxPool && threadIdx.x < p_sel &&
