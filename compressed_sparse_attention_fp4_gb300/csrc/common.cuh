@@ -39,9 +39,10 @@ struct WsLayout {
   int64_t ri_delta;     // f32 [B][P]             Reindex: bound per pool block
   int64_t attn_o;       // f32 [B][S][H][512]     split-KV partial outputs
   int64_t attn_ml;      // f32 [B][S][H][2]       partial (max, sum)
-  int64_t sel_exact;    // f64 [B][sel_cap]       exact scores of band items
-  int64_t sel_list;     // i32 [B][sel_cap]       band item lists
-  int64_t sel_pick;     // u8  [B][sel_cap]       band items picked
+  int64_t sel_exact;    // f64 [B][2][sel_cap]    exact scores of band items (per selection side)
+  int64_t sel_list;     // i32 [B][2][sel_cap]    band item lists
+  int64_t sel_pick;     // u8  [B][2][sel_cap]    band items picked
+  int64_t sel_blocks;   // i32 [B][P]             Full, Top-K side: the blocks its positions come from
   int64_t total;
   int64_t nb_max;       // ceil(max_ctx / 8)
   int64_t sel_cap;      // max(NBmax, P*8): items of one selection
@@ -95,9 +96,10 @@ __host__ __device__ inline WsLayout make_layout(const csa2_dims& d, int batch) {
   L.attn_o = off;  off = align256(off + int64_t(batch) * L.splits * d.heads * kLatent * 4);
   L.attn_ml = off; off = align256(off + int64_t(batch) * L.splits * d.heads * 2 * 4);
   L.sel_cap = L.nb_max > pool * kBlock ? L.nb_max : pool * kBlock;
-  L.sel_exact = off; off = align256(off + int64_t(batch) * L.sel_cap * 8);
-  L.sel_list = off;  off = align256(off + int64_t(batch) * L.sel_cap * 4);
-  L.sel_pick = off;  off = align256(off + int64_t(batch) * L.sel_cap);
+  L.sel_exact = off; off = align256(off + int64_t(batch) * 2 * L.sel_cap * 8);
+  L.sel_list = off;  off = align256(off + int64_t(batch) * 2 * L.sel_cap * 4);
+  L.sel_pick = off;  off = align256(off + int64_t(batch) * 2 * L.sel_cap);
+  L.sel_blocks = off; off = align256(off + int64_t(batch) * pool * 4);
   L.total = off;
   return L;
 }

@@ -81,15 +81,28 @@ constexpr int kExRowWords = 132;          // 128 words + 4: 16-byte aligned rows
 constexpr int kExSumThreads = 64;         // threads that form the ordered head sums
 constexpr int kStageWords = 2;            // row words a staging thread loads per batch
 
+constexpr int kFastRows = 64;             // positions of one pass of the E4M3 / FP4 re-scoring
+constexpr int kExTailWords = 832;         // extends the work area for the E4M3 pass
+
 struct ExScratch {
-  double dd[2][kExRows * kMaxIdxHeads];     // w_h * ReLU(d_h) of a round, double-buffered
   double cand_score[kSelThreads];
   int64_t cand_pos[kSelThreads];            // candidate positions of a chunk
   unsigned long long item_best[128];
   int32_t cand_item[kSelThreads];
+  // work area of the re-scoring (dd, krows and tail are contiguous; the E4M3
+  // pass lays its own [kFastRows][kMaxIdxHeads] doubles and
+  // [kFastRows][128] staged integers over all three)
+  double dd[2][kExRows * kMaxIdxHeads];     // w_h * ReLU(d_h) of a round, double-buffered
   __align__(16) int32_t krows[kExRows * kExRowWords];   // staged keys: E4M3 as k*2^9 integers, or fp32 bits
+  int32_t tail[kExTailWords];
 };
 static_assert(sizeof(ExScratch) <= sizeof(uint32_t) * kSelCapPerCta, "exact scratch must fit keyU");
+static_assert(offsetof(ExScratch, krows) == offsetof(ExScratch, dd) + sizeof(ExScratch::dd) &&
+              offsetof(ExScratch, tail) == offsetof(ExScratch, krows) + sizeof(ExScratch::krows),
+              "contiguous work area");
+static_assert(offsetof(ExScratch, dd) % 16 == 0, "16-byte aligned work area");
+static_assert(sizeof(double) * kFastRows * kMaxIdxHeads + sizeof(int32_t) * kFastRows * 128 <=
+              sizeof(ExScratch::dd) + sizeof(ExScratch::krows) + sizeof(ExScratch::tail), "E4M3 pass fits");
 
 __device__ inline ExScratch& ex_scratch(SelSmem& sm) { return *reinterpret_cast<ExScratch*>(sm.keyU); }
 
@@ -97,6 +110,7 @@ struct SelCtx {
   int rank, cs;
   int64_t n_ctx;
   int b;
+  int side;                                 // selection side: its band scratch in the workspace
 };
 
 __device__ inline void cl_sync(const SelCtx& c) {
@@ -496,14 +510,7 @@ __device__ void exact_scores(const IdxArgs& a, SelSmem& sm, const SelCtx& c, con
   }
 }
 
-// Exact scores of up to kFastRows positions in one pass (E4M3 keys, every
-// head's query on the int64 path): the positions' key rows are staged once
-// (all loads in flight together), two threads per (position, head) each sum
-// 64 exact products k*2^9 x qi in int64 and combine their halves, the head
-// dot is rounded once to fp64 and w_h * ReLU(d_h) formed; then one thread
-// per position adds the heads in order in fp64.  -inf for invalid positions.
-constexpr int kFastRows = 64;
-static_assert(kFastRows * 128 <= int(sizeof(int32_t)) * kExRows * kExRowWords, "staged rows fit");
+static_assert(kFastRows * 128 <= int(sizeof(int32_t)) * kExRows * kExRowWords, "staged FP4 rows fit");
 static_assert(kFastRows * kMaxIdxHeads <= 2 * kExRows * kMaxIdxHeads, "head products fit");
 
 // FP4 query and keys: d_h = sum_g sk_g sq_hg I_hg / 4 with I_hg = sum over the
@@ -581,54 +588,74 @@ __device__ void exact_scores_fp4(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
   __syncthreads();
 }
 
+// Exact scores of up to kFastRows positions in one pass (E4M3 keys, every
+// head's query on the int64 path).  The positions' key rows are staged once
+// as the integers k*2^9 (all loads in flight together).  A lane then holds 16
+// channels of one head's integer query in registers -- lane = (head of 4,
+// eighth e), the eighth being the channels 32j + 4e + {0..3}, j < 4, so that
+// the 8 lanes of a head read a staged row as 128 consecutive bytes -- and
+// walks the positions: 16 exact products k*2^9 x qi summed in int64, the 8
+// lanes' sums combined by shuffles (exact in any order), the head dot rounded
+// once to fp64 and w_h * ReLU(d_h) formed; then one thread per position adds
+// the heads in order in fp64.  -inf for invalid positions.
 __device__ void exact_scores_fast(const IdxArgs& a, SelSmem& sm, const SelCtx& c, const int64_t* pos, int np,
                                   double* out) {
   ExScratch& ex = ex_scratch(sm);
-  const int tid = threadIdx.x, hi = a.d.idx_heads;
-  uint4* rows = reinterpret_cast<uint4*>(ex.krows);           // [kFastRows][8] x 16 bytes
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, hi = a.d.idx_heads;
   double* dd = &ex.dd[0][0];                                   // [kFastRows][kMaxIdxHeads]
-  // ---- stage the rows: 8 threads per position, one 16-byte piece each ----------
+  int32_t* kdec = reinterpret_cast<int32_t*>(dd + kFastRows * kMaxIdxHeads);   // [kFastRows][128]
+  // ---- stage the rows: 8 threads per position, the words 8j + e of the row ----
   if (tid < np * 8) {
-    const int p = tid >> 3, part = tid & 7;
+    const int p = tid >> 3, e = tid & 7;
     const int64_t t = pos[p];
-    uint4 v = make_uint4(0, 0, 0, 0);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
     if (t >= 0 && t < c.n_ctx) {
       const int64_t r = kv_row(a.page_table, a.d, c.b, t, a.ws);
-      if (r >= 0) v = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(a.idx_k) + r * 128) + part);
-    }
-    rows[p * 8 + part] = v;
-  }
-  __syncthreads();
-  // ---- products: task = (position, head, half of the 128 channels) ------------
-  // warp-uniform trip count: both halves of a task sit in one warp and every
-  // lane takes part in the combining shuffle
-  const int lane = tid & 31, ntask = np * hi * 2;
-  for (int base = tid - lane; base < ntask; base += kSelThreads) {
-    const int task = base + lane;
-    const bool act = task < ntask;
-    const int half = task & 1, ph = task >> 1, p = act ? ph / hi : 0, h = act ? ph % hi : 0;
-    const uint4* kr = rows + p * 8 + half * 4;                 // 64 key bytes
-    const int4* q4 = reinterpret_cast<const int4*>(sm.qi + h * kQiStride + half * 64);
-    long long acc = 0;
+      if (r >= 0) {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(a.idx_k) + r * 128) + e;
 #pragma unroll
-    for (int w = 0; w < (act ? 4 : 0); ++w) {
-      const uint4 kw = kr[w];
-      const uint32_t kb[4] = {kw.x, kw.y, kw.z, kw.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int4 qv = q4[w * 4 + u];
-        acc += (long long)qv.x * sm.k_lut[kb[u] & 0xFF];
-        acc += (long long)qv.y * sm.k_lut[(kb[u] >> 8) & 0xFF];
-        acc += (long long)qv.z * sm.k_lut[(kb[u] >> 16) & 0xFF];
-        acc += (long long)qv.w * sm.k_lut[kb[u] >> 24];
+        for (int j = 0; j < 4; ++j) w[j] = __ldg(src + 8 * j);
       }
     }
-    acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);               // the other half (exact)
-    if (act && half == 0) {
-      const double d = int_to_f64_rn(acc, sm.q_elo[h] - 9);
-      const unsigned long long db = (unsigned long long)__double_as_longlong(d);
-      const bool positive = (db >> 63) == 0 && db != 0;
-      dd[p * kMaxIdxHeads + h] = __dmul_rn(f32_to_f64_exact(sm.w[h]), positive ? d : 0.0);
+    int4* dst = reinterpret_cast<int4*>(kdec + p * 128) + e;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      dst[8 * j] = make_int4(sm.k_lut[w[j] & 0xFF], sm.k_lut[(w[j] >> 8) & 0xFF], sm.k_lut[(w[j] >> 16) & 0xFF],
+                             sm.k_lut[w[j] >> 24]);
+  }
+  // ---- this lane's query channels (registers) ----------------------------------
+  const int wpp = (hi + 3) >> 2;                               // warps per position
+  const int ngroups = kSelWarps / wpp;                         // positions walked at once
+  const int g = wid / wpp, h = (wid % wpp) * 4 + (lane >> 3), e = lane & 7;
+  const bool hv = g < ngroups && h < hi;
+  int4 q[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    q[j] = hv ? reinterpret_cast<const int4*>(sm.qi + h * kQiStride)[8 * j + e] : make_int4(0, 0, 0, 0);
+  __syncthreads();
+  // ---- products: a warp walks positions g, g + ngroups, ... (warp-uniform) -------
+  if (g < ngroups) {
+#pragma unroll 1
+    for (int p = g; p < np; p += ngroups) {
+      const int4* kr = reinterpret_cast<const int4*>(kdec + p * 128) + e;
+      long long acc = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int4 k = kr[8 * j];
+        acc += (long long)q[j].x * k.x;
+        acc += (long long)q[j].y * k.y;
+        acc += (long long)q[j].z * k.z;
+        acc += (long long)q[j].w * k.w;
+      }
+      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
+      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 2);
+      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 4);
+      if (hv && e == 0) {
+        const double d = int_to_f64_rn(acc, sm.q_elo[h] - 9);
+        const unsigned long long db = (unsigned long long)__double_as_longlong(d);
+        const bool positive = (db >> 63) == 0 && db != 0;
+        dd[p * kMaxIdxHeads + h] = __dmul_rn(f32_to_f64_exact(sm.w[h]), positive ? d : 0.0);
+      }
     }
   }
   __syncthreads();
@@ -638,7 +665,7 @@ __device__ void exact_scores_fast(const IdxArgs& a, SelSmem& sm, const SelCtx& c
     double sum = -INFINITY;
     if (t >= 0 && t < c.n_ctx) {
       sum = 0.0;
-      for (int h = 0; h < hi; ++h) sum = __dadd_rn(sum, dd[tid * kMaxIdxHeads + h]);
+      for (int h2 = 0; h2 < hi; ++h2) sum = __dadd_rn(sum, dd[tid * kMaxIdxHeads + h2]);
     }
     out[tid] = sum;
   }
@@ -653,10 +680,13 @@ __device__ inline uint64_t f64_key(double x) {
 
 // Selects the k best of n items of `kind`; writes their ids ascending to
 // out[0 .. k).  All CTAs of the cluster take part (items split by rank).
+// With `superset` (block items) no exact re-scoring takes place: the ids of
+// every item whose bounds let it be among the k best (the certain ones and the
+// band) are written ascending, at most pool_blocks of them.  Returns the
+// number of items selected (superset: all of them, also those not written).
 template <bool kFp4>
-__device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c, ItemKind kind,
-                                 int64_t n_items, int64_t k, int32_t* out, double* g_exact,
-                                 int32_t* g_list, uint8_t* g_pick) {
+__device__ int64_t certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c, ItemKind kind,
+                                    int64_t n_items, int64_t k, int32_t* out, bool superset = false) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   // the items are split evenly over the cluster's CTAs (whole 32-item words)
   const int64_t per = min64(kSelCapPerCta, ((n_items + c.cs - 1) / c.cs + 31) & ~int64_t(31));
@@ -793,253 +823,269 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
       atomicAdd(&sm.cnt_in, my_in);
       atomicAdd(&sm.cnt_band, my_band);
     }
-    // ordered list of this CTA's band items (keyL area is free now)
-    uint32_t nband = scan_words(sm, sm.band_bits, nwords);
-    int32_t* blist = reinterpret_cast<int32_t*>(sm.keyL);
-    for (int wv = tid; wv < nwords; wv += blockDim.x) {
-      uint32_t bits = sm.band_bits[wv], o = sm.word_off[wv];
-      while (bits) {
-        int bp = __ffs(bits) - 1;
-        bits &= bits - 1;
-        blist[o++] = wv * 32 + bp;
-      }
-    }
-    __syncthreads();
-    // A selection held by one CTA with a band of at most kSelThreads items
-    // keeps the band's exact-score keys in shared memory (in the histogram
-    // space, free after the radix step) and marks its picks directly; the
-    // workspace lists serve the cluster case and larger bands.
-    const bool local_pick = c.cs == 1 && nband <= uint32_t(kSelThreads);
-    uint64_t* band_key = reinterpret_cast<uint64_t*>(&sm.hist[0][0]);
-    static_assert(sizeof(sm.hist) >= kSelThreads * sizeof(uint64_t), "band keys fit the histograms");
-    // exact scores of the band, a chunk of items at a time.  For a block,
-    // only the positions whose upper bound reaches the block's best lower
-    // bound can hold its exact maximum; the others are not re-scored.
-    const float* ws_f = reinterpret_cast<const float*>(a.ws);
-    ExScratch& ex = ex_scratch(sm);
-    for (uint32_t j0 = 0; j0 < nband; j0 += kExItems) {
-      const int nit = int(min64(kExItems, int64_t(nband) - j0));
-      if (tid == 0) sm.n_cand = 0;
+    if (superset) {
+      // every item that may be among the k best: certain or in the band
       __syncthreads();
-      // a few band blocks: every valid position of each is a candidate (no
-      // filter by the position scores, one round trip less)
-      const bool all_pos = sm.fast_exact && kind == kBlocks && nit * kBlock <= kFastRows;
-      if (all_pos) {
-        if (tid < nit * kBlock) {
-          const int j = tid >> 3;
-          const int64_t t = (base + blist[j0 + j]) * kBlock + (tid & 7);
-          ex.cand_pos[tid] = t < c.n_ctx ? t : -1;
-          ex.cand_item[tid] = j;
-          if ((tid & 7) == 0) ex.item_best[j] = 0;
+      for (int wv = tid; wv < nwords; wv += blockDim.x) sm.sel_bits[wv] |= sm.band_bits[wv];
+    } else {
+      // this side's band scratch in the workspace (cluster case, large bands)
+      const int64_t wso = (int64_t(c.b) * 2 + c.side) * a.L.sel_cap;
+      double* g_exact = reinterpret_cast<double*>(a.ws + a.L.sel_exact) + wso;
+      int32_t* g_list = reinterpret_cast<int32_t*>(a.ws + a.L.sel_list) + wso;
+      uint8_t* g_pick = a.ws + a.L.sel_pick + wso;
+      // ordered list of this CTA's band items (keyL area is free now)
+      uint32_t nband = scan_words(sm, sm.band_bits, nwords);
+      int32_t* blist = reinterpret_cast<int32_t*>(sm.keyL);
+      for (int wv = tid; wv < nwords; wv += blockDim.x) {
+        uint32_t bits = sm.band_bits[wv], o = sm.word_off[wv];
+        while (bits) {
+          int bp = __ffs(bits) - 1;
+          bits &= bits - 1;
+          blist[o++] = wv * 32 + bp;
         }
-        if (tid == 0) sm.n_cand = uint32_t(nit * kBlock);
       }
-      for (int j = all_pos ? nit : wid; j < nit; j += kSelWarps) {
-        int64_t gi = base + blist[j0 + j];
-        if (kind == kBlocks) {
-          int64_t t = gi * kBlock + (lane & 7);
-          bool ok = lane < kBlock && t < c.n_ctx;
-          float dl = ws_f[(a.L.blk_delta >> 2) + int64_t(c.b) * a.L.nb_max + gi];
-          float v = ok ? ws_f[(a.L.pos_scores >> 2) + int64_t(c.b) * a.d.max_ctx + t] : -INFINITY;
-          float lo = ok ? __fadd_rd(v, -dl) : -INFINITY;
-          float hv = ok ? __fadd_ru(v, dl) : -INFINITY;
-          float lmax = lo;
-#pragma unroll
-          for (int o = 16; o; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
-          bool cand = ok && hv >= lmax;
-          uint32_t m = __ballot_sync(0xFFFFFFFFu, cand);
-          uint32_t slot0 = 0;
-          if (lane == 0) slot0 = atomicAdd(&sm.n_cand, uint32_t(__popc(m)));
-          slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
-          if (cand) {
-            uint32_t sl = slot0 + __popc(m & ((1u << lane) - 1));
-            ex.cand_pos[sl] = t;
+      __syncthreads();
+      // A selection held by one CTA with a band of at most kSelThreads items
+      // keeps the band's exact-score keys in shared memory (in the histogram
+      // space, free after the radix step) and marks its picks directly; the
+      // workspace lists serve the cluster case and larger bands.
+      const bool local_pick = c.cs == 1 && nband <= uint32_t(kSelThreads);
+      uint64_t* band_key = reinterpret_cast<uint64_t*>(&sm.hist[0][0]);
+      static_assert(sizeof(sm.hist) >= kSelThreads * sizeof(uint64_t), "band keys fit the histograms");
+      // exact scores of the band, a chunk of items at a time.  For a block,
+      // only the positions whose upper bound reaches the block's best lower
+      // bound can hold its exact maximum; the others are not re-scored.
+      const float* ws_f = reinterpret_cast<const float*>(a.ws);
+      ExScratch& ex = ex_scratch(sm);
+      for (uint32_t j0 = 0; j0 < nband; j0 += kExItems) {
+        const int nit = int(min64(kExItems, int64_t(nband) - j0));
+        if (tid == 0) sm.n_cand = 0;
+        __syncthreads();
+        // a few band blocks: every valid position of each is a candidate (no
+        // filter by the position scores, one round trip less)
+        const bool all_pos = sm.fast_exact && kind == kBlocks && nit * kBlock <= kFastRows;
+        if (all_pos) {
+          if (tid < nit * kBlock) {
+            const int j = tid >> 3;
+            const int64_t t = (base + blist[j0 + j]) * kBlock + (tid & 7);
+            ex.cand_pos[tid] = t < c.n_ctx ? t : -1;
+            ex.cand_item[tid] = j;
+            if ((tid & 7) == 0) ex.item_best[j] = 0;
+          }
+          if (tid == 0) sm.n_cand = uint32_t(nit * kBlock);
+        }
+        for (int j = all_pos ? nit : wid; j < nit; j += kSelWarps) {
+          int64_t gi = base + blist[j0 + j];
+          if (kind == kBlocks) {
+            int64_t t = gi * kBlock + (lane & 7);
+            bool ok = lane < kBlock && t < c.n_ctx;
+            float dl = ws_f[(a.L.blk_delta >> 2) + int64_t(c.b) * a.L.nb_max + gi];
+            float v = ok ? ws_f[(a.L.pos_scores >> 2) + int64_t(c.b) * a.d.max_ctx + t] : -INFINITY;
+            float lo = ok ? __fadd_rd(v, -dl) : -INFINITY;
+            float hv = ok ? __fadd_ru(v, dl) : -INFINITY;
+            float lmax = lo;
+  #pragma unroll
+            for (int o = 16; o; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xFFFFFFFFu, lmax, o));
+            bool cand = ok && hv >= lmax;
+            uint32_t m = __ballot_sync(0xFFFFFFFFu, cand);
+            uint32_t slot0 = 0;
+            if (lane == 0) slot0 = atomicAdd(&sm.n_cand, uint32_t(__popc(m)));
+            slot0 = __shfl_sync(0xFFFFFFFFu, slot0, 0);
+            if (cand) {
+              uint32_t sl = slot0 + __popc(m & ((1u << lane) - 1));
+              ex.cand_pos[sl] = t;
+              ex.cand_item[sl] = j;
+            }
+          } else if (lane == 0) {
+            int32_t blk = sm.pool_ids[gi >> 3];
+            uint32_t sl = atomicAdd(&sm.n_cand, 1u);
+            ex.cand_pos[sl] = blk < 0 ? -1 : int64_t(blk) * kBlock + (gi & 7);
             ex.cand_item[sl] = j;
           }
-        } else if (lane == 0) {
-          int32_t blk = sm.pool_ids[gi >> 3];
-          uint32_t sl = atomicAdd(&sm.n_cand, 1u);
-          ex.cand_pos[sl] = blk < 0 ? -1 : int64_t(blk) * kBlock + (gi & 7);
-          ex.cand_item[sl] = j;
-        }
-        if (lane == 0) ex.item_best[j] = 0;       // key of -inf is above 0
-      }
-      __syncthreads();
-      const int ncand = int(sm.n_cand);
-      if constexpr (kFp4) {
-        for (int c0 = 0; c0 < ncand; c0 += kFastRows)
-          exact_scores_fp4(a, sm, c, ex.cand_pos + c0, min(kFastRows, ncand - c0), ex.cand_score + c0);
-      } else if (sm.fast_exact) {
-        for (int c0 = 0; c0 < ncand; c0 += kFastRows)
-          exact_scores_fast(a, sm, c, ex.cand_pos + c0, min(kFastRows, ncand - c0), ex.cand_score + c0);
-      } else {
-        exact_scores(a, sm, c, ex.cand_pos, ncand, ex.cand_score);
-      }
-      for (int i = tid; i < ncand; i += blockDim.x)
-        atomicMax(&ex.item_best[ex.cand_item[i]], f64_key(ex.cand_score[i]));
-      __syncthreads();
-      for (int j = tid; j < nit; j += blockDim.x) {
-        int64_t gi = base + blist[j0 + j];
-        uint64_t kk = ex.item_best[j];
-        if (local_pick) {
-          band_key[j0 + j] = kk ? kk : f64_key(-INFINITY);   // the key of the decoded score
-          continue;
-        }
-        uint64_t u = (kk >> 63) ? (kk & ~(uint64_t(1) << 63)) : ~kk;   // inverse of f64_key
-        g_exact[gi] = kk ? __longlong_as_double((long long)u) : -INFINITY;
-        g_pick[gi] = 0;
-      }
-      __syncthreads();
-    }
-    cl_sync(c);
-    uint32_t tot_in = sm.cnt_in, tot_band = sm.cnt_band, band_off = 0;
-    if (c.cs > 1) {
-      // the ranks' counters, one rank per lane of warp 0 (not one remote read
-      // per rank by every thread)
-      if (wid == 0) {
-        uint32_t ci = 0, cb = 0;
-        if (lane < c.cs) {
-          ci = *remote(c, &sm.cnt_in, lane);
-          cb = *remote(c, &sm.cnt_band, lane);
-        }
-        const uint32_t ti = __reduce_add_sync(0xFFFFFFFFu, ci), tb = __reduce_add_sync(0xFFFFFFFFu, cb);
-        const uint32_t bo = __reduce_add_sync(0xFFFFFFFFu, lane < c.rank ? cb : 0u);
-        if (lane == 0) { sm.tot3[0] = ti; sm.tot3[1] = tb; sm.tot3[2] = bo; }
-      }
-      __syncthreads();
-      tot_in = sm.tot3[0];
-      tot_band = sm.tot3[1];
-      band_off = sm.tot3[2];
-    }
-    if (!local_pick)
-      for (uint32_t j = tid; j < nband; j += blockDim.x) g_list[band_off + j] = int32_t(base + blist[j]);
-    cl_sync(c);
-    // ---- rank 0 picks the best (k - tot_in) band items by exact score -----
-    int64_t need = k - int64_t(tot_in);
-    if (c.rank == 0 && need > 0) {
-      if (need >= int64_t(tot_band)) {
-        for (uint32_t i = tid; i < tot_band; i += blockDim.x) {
-          if (local_pick) atomicOr(&sm.sel_bits[blist[i] >> 5], 1u << (blist[i] & 31));
-          else g_pick[g_list[i]] = 1;
-        }
-      } else if (tot_band <= kSelThreads) {
-        // small band: each item's rank = the number of band items ahead of it
-        uint64_t* skey = reinterpret_cast<uint64_t*>(sm.keyU);
-        int32_t* sidx = reinterpret_cast<int32_t*>(sm.keyL);
-        for (uint32_t i = tid; i < tot_band; i += blockDim.x) {
-          if (local_pick) {                    // sidx is the band list itself (base 0)
-            skey[i] = band_key[i];
-          } else {
-            int32_t it = g_list[i];
-            skey[i] = f64_key(g_exact[it]);
-            sidx[i] = it;
-          }
+          if (lane == 0) ex.item_best[j] = 0;       // key of -inf is above 0
         }
         __syncthreads();
-        // one warp per item: the lanes count the band items ahead of it
-        for (uint32_t i = wid; i < tot_band; i += kSelWarps) {
-          const uint64_t mk = skey[i];
-          const int32_t mi = sidx[i];
-          uint32_t rank = 0;
-          for (uint32_t j = lane; j < tot_band; j += 32) {
-            const uint64_t kj = skey[j];
-            rank += (kj > mk || (kj == mk && sidx[j] < mi)) ? 1u : 0u;
-          }
-          rank = __reduce_add_sync(0xFFFFFFFFu, rank);
-          if (lane == 0 && rank < uint32_t(need)) {
-            if (local_pick) atomicOr(&sm.sel_bits[mi >> 5], 1u << (mi & 31));
-            else g_pick[mi] = 1;
-          }
+        const int ncand = int(sm.n_cand);
+        if constexpr (kFp4) {
+          for (int c0 = 0; c0 < ncand; c0 += kFastRows)
+            exact_scores_fp4(a, sm, c, ex.cand_pos + c0, min(kFastRows, ncand - c0), ex.cand_score + c0);
+        } else if (sm.fast_exact) {
+          for (int c0 = 0; c0 < ncand; c0 += kFastRows)
+            exact_scores_fast(a, sm, c, ex.cand_pos + c0, min(kFastRows, ncand - c0), ex.cand_score + c0);
+        } else {
+          exact_scores(a, sm, c, ex.cand_pos, ncand, ex.cand_score);
         }
-      } else if (tot_band <= kSortCap) {
-        uint64_t* skey = reinterpret_cast<uint64_t*>(sm.keyU);
-        int32_t* sidx = reinterpret_cast<int32_t*>(sm.keyL);
-        int nsort = 1;
-        while (nsort < int(tot_band)) nsort <<= 1;
-        for (int i = tid; i < nsort; i += blockDim.x) {
-          if (i < int(tot_band)) { int32_t it = g_list[i]; skey[i] = f64_key(g_exact[it]); sidx[i] = it; }
-          else { skey[i] = 0; sidx[i] = INT_MAX; }
+        for (int i = tid; i < ncand; i += blockDim.x)
+          atomicMax(&ex.item_best[ex.cand_item[i]], f64_key(ex.cand_score[i]));
+        __syncthreads();
+        for (int j = tid; j < nit; j += blockDim.x) {
+          int64_t gi = base + blist[j0 + j];
+          uint64_t kk = ex.item_best[j];
+          if (local_pick) {
+            band_key[j0 + j] = kk ? kk : f64_key(-INFINITY);   // the key of the decoded score
+            continue;
+          }
+          uint64_t u = (kk >> 63) ? (kk & ~(uint64_t(1) << 63)) : ~kk;   // inverse of f64_key
+          g_exact[gi] = kk ? __longlong_as_double((long long)u) : -INFINITY;
+          g_pick[gi] = 0;
         }
         __syncthreads();
-        for (int size = 2; size <= nsort; size <<= 1) {
-          for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = tid; i < nsort; i += blockDim.x) {
-              int j = i ^ stride;
-              if (j > i) {
-                bool desc = (i & size) == 0;
-                bool i_first = skey[i] > skey[j] || (skey[i] == skey[j] && sidx[i] < sidx[j]);
-                if (desc != i_first) {
-                  uint64_t tk = skey[i]; skey[i] = skey[j]; skey[j] = tk;
-                  int32_t ti = sidx[i]; sidx[i] = sidx[j]; sidx[j] = ti;
+      }
+      cl_sync(c);
+      uint32_t tot_in = sm.cnt_in, tot_band = sm.cnt_band, band_off = 0;
+      if (c.cs > 1) {
+        // the ranks' counters, one rank per lane of warp 0 (not one remote read
+        // per rank by every thread)
+        if (wid == 0) {
+          uint32_t ci = 0, cb = 0;
+          if (lane < c.cs) {
+            ci = *remote(c, &sm.cnt_in, lane);
+            cb = *remote(c, &sm.cnt_band, lane);
+          }
+          const uint32_t ti = __reduce_add_sync(0xFFFFFFFFu, ci), tb = __reduce_add_sync(0xFFFFFFFFu, cb);
+          const uint32_t bo = __reduce_add_sync(0xFFFFFFFFu, lane < c.rank ? cb : 0u);
+          if (lane == 0) { sm.tot3[0] = ti; sm.tot3[1] = tb; sm.tot3[2] = bo; }
+        }
+        __syncthreads();
+        tot_in = sm.tot3[0];
+        tot_band = sm.tot3[1];
+        band_off = sm.tot3[2];
+      }
+      if (!local_pick)
+        for (uint32_t j = tid; j < nband; j += blockDim.x) g_list[band_off + j] = int32_t(base + blist[j]);
+      cl_sync(c);
+      // ---- rank 0 picks the best (k - tot_in) band items by exact score -----
+      int64_t need = k - int64_t(tot_in);
+      if (c.rank == 0 && need > 0) {
+        if (need >= int64_t(tot_band)) {
+          for (uint32_t i = tid; i < tot_band; i += blockDim.x) {
+            if (local_pick) atomicOr(&sm.sel_bits[blist[i] >> 5], 1u << (blist[i] & 31));
+            else g_pick[g_list[i]] = 1;
+          }
+        } else if (tot_band <= kSelThreads) {
+          // small band: each item's rank = the number of band items ahead of it
+          uint64_t* skey = reinterpret_cast<uint64_t*>(sm.keyU);
+          int32_t* sidx = reinterpret_cast<int32_t*>(sm.keyL);
+          for (uint32_t i = tid; i < tot_band; i += blockDim.x) {
+            if (local_pick) {                    // sidx is the band list itself (base 0)
+              skey[i] = band_key[i];
+            } else {
+              int32_t it = g_list[i];
+              skey[i] = f64_key(g_exact[it]);
+              sidx[i] = it;
+            }
+          }
+          __syncthreads();
+          // one warp per item: the lanes count the band items ahead of it
+          for (uint32_t i = wid; i < tot_band; i += kSelWarps) {
+            const uint64_t mk = skey[i];
+            const int32_t mi = sidx[i];
+            uint32_t rank = 0;
+            for (uint32_t j = lane; j < tot_band; j += 32) {
+              const uint64_t kj = skey[j];
+              rank += (kj > mk || (kj == mk && sidx[j] < mi)) ? 1u : 0u;
+            }
+            rank = __reduce_add_sync(0xFFFFFFFFu, rank);
+            if (lane == 0 && rank < uint32_t(need)) {
+              if (local_pick) atomicOr(&sm.sel_bits[mi >> 5], 1u << (mi & 31));
+              else g_pick[mi] = 1;
+            }
+          }
+        } else if (tot_band <= kSortCap) {
+          uint64_t* skey = reinterpret_cast<uint64_t*>(sm.keyU);
+          int32_t* sidx = reinterpret_cast<int32_t*>(sm.keyL);
+          int nsort = 1;
+          while (nsort < int(tot_band)) nsort <<= 1;
+          for (int i = tid; i < nsort; i += blockDim.x) {
+            if (i < int(tot_band)) { int32_t it = g_list[i]; skey[i] = f64_key(g_exact[it]); sidx[i] = it; }
+            else { skey[i] = 0; sidx[i] = INT_MAX; }
+          }
+          __syncthreads();
+          for (int size = 2; size <= nsort; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+              for (int i = tid; i < nsort; i += blockDim.x) {
+                int j = i ^ stride;
+                if (j > i) {
+                  bool desc = (i & size) == 0;
+                  bool i_first = skey[i] > skey[j] || (skey[i] == skey[j] && sidx[i] < sidx[j]);
+                  if (desc != i_first) {
+                    uint64_t tk = skey[i]; skey[i] = skey[j]; skey[j] = tk;
+                    int32_t ti = sidx[i]; sidx[i] = sidx[j]; sidx[j] = ti;
+                  }
                 }
+              }
+              __syncthreads();
+            }
+          }
+          for (int i = tid; i < need; i += blockDim.x) g_pick[sidx[i]] = 1;
+        } else {
+          // large band (massive exact ties): 64-bit radix select streamed over
+          // the global band list by this CTA alone
+          uint32_t* h64 = &sm.hist[0][0];
+          __shared__ unsigned long long pref64;
+          __shared__ uint32_t rem64;
+          if (tid == 0) { pref64 = 0; rem64 = uint32_t(need); }
+          __syncthreads();
+          for (int pass = 0; pass < 8; ++pass) {
+            int shift = 56 - 8 * pass;
+            uint64_t maskHi = pass ? (~uint64_t(0) << (64 - 8 * pass)) : 0;
+            if (tid < 256) h64[tid] = 0;
+            __syncthreads();
+            for (uint32_t i = tid; i < tot_band; i += blockDim.x) {
+              uint64_t key = f64_key(g_exact[g_list[i]]);
+              if ((key & maskHi) == pref64) atomicAdd(&h64[(key >> shift) & 0xFF], 1u);
+            }
+            __syncthreads();
+            if (tid == 0) {
+              uint32_t acc = 0;
+              for (int bkt = 255; bkt >= 0; --bkt) {
+                if (acc + h64[bkt] >= rem64) { pref64 |= uint64_t(bkt) << shift; rem64 -= acc; break; }
+                acc += h64[bkt];
               }
             }
             __syncthreads();
           }
-        }
-        for (int i = tid; i < need; i += blockDim.x) g_pick[sidx[i]] = 1;
-      } else {
-        // large band (massive exact ties): 64-bit radix select streamed over
-        // the global band list by this CTA alone
-        uint32_t* h64 = &sm.hist[0][0];
-        __shared__ unsigned long long pref64;
-        __shared__ uint32_t rem64;
-        if (tid == 0) { pref64 = 0; rem64 = uint32_t(need); }
-        __syncthreads();
-        for (int pass = 0; pass < 8; ++pass) {
-          int shift = 56 - 8 * pass;
-          uint64_t maskHi = pass ? (~uint64_t(0) << (64 - 8 * pass)) : 0;
-          if (tid < 256) h64[tid] = 0;
-          __syncthreads();
-          for (uint32_t i = tid; i < tot_band; i += blockDim.x) {
-            uint64_t key = f64_key(g_exact[g_list[i]]);
-            if ((key & maskHi) == pref64) atomicAdd(&h64[(key >> shift) & 0xFF], 1u);
-          }
-          __syncthreads();
           if (tid == 0) {
-            uint32_t acc = 0;
-            for (int bkt = 255; bkt >= 0; --bkt) {
-              if (acc + h64[bkt] >= rem64) { pref64 |= uint64_t(bkt) << shift; rem64 -= acc; break; }
-              acc += h64[bkt];
+            uint64_t kappa = pref64;
+            uint32_t taken = 0;
+            for (uint32_t i = 0; i < tot_band; ++i) {
+              uint64_t key = f64_key(g_exact[g_list[i]]);
+              if (key > kappa) g_pick[g_list[i]] = 1;
+              else if (key == kappa && taken < rem64) { g_pick[g_list[i]] = 1; ++taken; }
             }
           }
-          __syncthreads();
         }
-        if (tid == 0) {
-          uint64_t kappa = pref64;
-          uint32_t taken = 0;
-          for (uint32_t i = 0; i < tot_band; ++i) {
-            uint64_t key = f64_key(g_exact[g_list[i]]);
-            if (key > kappa) g_pick[g_list[i]] = 1;
-            else if (key == kappa && taken < rem64) { g_pick[g_list[i]] = 1; ++taken; }
+      }
+      cl_sync(c);
+      if (!local_pick)
+        for (int wv = tid; wv < nwords; wv += blockDim.x) {
+          uint32_t bits = sm.band_bits[wv];
+          while (bits) {
+            int bp = __ffs(bits) - 1;
+            bits &= bits - 1;
+            if (g_pick[base + wv * 32 + bp]) atomicOr(&sm.sel_bits[wv], 1u << bp);
           }
         }
-      }
     }
-    cl_sync(c);
-    if (!local_pick)
-      for (int wv = tid; wv < nwords; wv += blockDim.x) {
-        uint32_t bits = sm.band_bits[wv];
-        while (bits) {
-          int bp = __ffs(bits) - 1;
-          bits &= bits - 1;
-          if (g_pick[base + wv * 32 + bp]) atomicOr(&sm.sel_bits[wv], 1u << bp);
-        }
-      }
   }
   // ---- ordered output ------------------------------------------------------
   uint32_t nsel = scan_words(sm, sm.sel_bits, nwords);
   if (tid == 0) sm.cnt_sel = nsel;
   cl_sync(c);
   uint32_t off = 0;
+  int64_t total = nsel;
   if (c.cs > 1) {
     if (wid == 0) {
-      const uint32_t v = __reduce_add_sync(0xFFFFFFFFu, lane < c.rank ? *remote(c, &sm.cnt_sel, lane) : 0u);
-      if (lane == 0) sm.tot3[0] = v;
+      const uint32_t mine = lane < c.cs ? *remote(c, &sm.cnt_sel, lane) : 0u;
+      const uint32_t v = __reduce_add_sync(0xFFFFFFFFu, lane < c.rank ? mine : 0u);
+      const uint32_t all = __reduce_add_sync(0xFFFFFFFFu, mine);
+      if (lane == 0) { sm.tot3[0] = v; sm.tot3[1] = all; }
     }
     __syncthreads();
     off = sm.tot3[0];
+    total = sm.tot3[1];
   }
+  const int64_t cap = superset ? int64_t(a.d.pool_blocks) : k;
   for (int wv = tid; wv < nwords; wv += blockDim.x) {
     uint32_t bits = sm.sel_bits[wv], o = sm.word_off[wv];
     while (bits) {
@@ -1047,7 +1093,7 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
       bits &= bits - 1;
       int64_t gi = base + wv * 32 + bp;
       int64_t id = (kind == kBlocks) ? gi : int64_t(sm.pool_ids[gi >> 3]) * kBlock + (gi & 7);
-      if (off + o < k) {
+      if (off + o < cap) {
         out[off + o] = int32_t(id);
         // one CTA: the pool also goes straight to shared memory for the Top-K
         if (kind == kBlocks && c.cs == 1) sm.pool_ids[off + o] = int32_t(id);
@@ -1056,6 +1102,7 @@ __device__ void certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
     }
   }
   cl_sync(c);     // no rank leaves while another still reads its counters
+  return total;
 }
 
 // Sum of one int per thread over the CTA (uses sm.red[1]).
@@ -1223,38 +1270,55 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
     load_query_factors(a, sm, b);
   pdl_wait();
   c.n_ctx = check_ctx(n_raw, a.d, a.page_table != nullptr, a.ws);
-  const int64_t scap = a.L.sel_cap;
-  double* g_exact = reinterpret_cast<double*>(a.ws + a.L.sel_exact) + int64_t(b) * scap;
-  int32_t* g_list = reinterpret_cast<int32_t*>(a.ws + a.L.sel_list) + int64_t(b) * scap;
-  uint8_t* g_pick = a.ws + a.L.sel_pick + int64_t(b) * scap;
+  const int side = int(blockIdx.z);
+  c.side = side;
   const int P = a.d.pool_blocks, K = a.d.topk;
   __syncthreads();
   int64_t nb = (c.n_ctx + kBlock - 1) / kBlock;
   if (!reindex) {
-    int64_t p_sel = min64(P, nb);
-    int32_t* pool = a.pool_out + int64_t(b) * P;
-    certified_select<kFp4>(a, sm, c, kBlocks, nb, p_sel, pool, g_exact, g_list, g_pick);
-    if (c.rank == 0) {
-      for (int i = threadIdx.x; i < P; i += blockDim.x)
-        if (i >= p_sel) pool[i] = -1;
-      if (threadIdx.x == 0) a.pool_len_out[b] = int32_t(p_sel);
+    // The Top-K positions lie in the K best blocks (a block ahead of the
+    // block of a Top-K position p holds a position ahead of p), which the
+    // pool holds when K <= P or the pool is every block.  Then side 1 takes
+    // the Top-K from the blocks whose bounds let them be among the K best
+    // (a superset of them), at the same time as side 0 selects the pool; else
+    // side 0 does both in turn and side 1 has nothing to do.
+    const bool split = K <= P || nb <= P;
+    if (side == 1 && !split) return;
+    const int64_t p_sel = min64(P, nb);
+    int64_t n_blk = p_sel;                       // blocks the Top-K positions are taken from
+    int32_t* blocks = side == 0 ? a.pool_out + int64_t(b) * P       // their ids (ascending)
+                                : reinterpret_cast<int32_t*>(a.ws + a.L.sel_blocks) + int64_t(b) * P;
+    // side 1: the superset first; a band too wide for it (ties) takes the
+    // pool itself, as side 0 finds it
+    for (int pass = side; pass >= 0; --pass) {
+      const bool sup = pass == 1;
+      n_blk = certified_select<kFp4>(a, sm, c, kBlocks, nb, sup ? min64(K, nb) : p_sel, blocks, sup);
+      if (n_blk <= P) break;
     }
-    cl_sync(c);                    // every rank's pool ids are written (read through L2)
+    if (side == 0) {
+      if (c.rank == 0) {
+        for (int i = threadIdx.x; i < P; i += blockDim.x)
+          if (i >= p_sel) blocks[i] = -1;
+        if (threadIdx.x == 0) a.pool_len_out[b] = int32_t(p_sel);
+      }
+      if (split) return;
+    }
+    cl_sync(c);                    // every rank's block ids are written (read through L2)
     if (c.cs > 1) {
-      for (int i = threadIdx.x; i < kMaxPool; i += blockDim.x) sm.pool_ids[i] = i < p_sel ? __ldcg(pool + i) : -1;
+      for (int i = threadIdx.x; i < kMaxPool; i += blockDim.x) sm.pool_ids[i] = i < n_blk ? __ldcg(blocks + i) : -1;
     } else {
       for (int i = threadIdx.x; i < kMaxPool; i += blockDim.x)
-        if (i >= p_sel) sm.pool_ids[i] = -1;       // ids below p_sel: written by the selection
+        if (i >= n_blk) sm.pool_ids[i] = -1;       // ids below n_blk: written by the selection
     }
     __syncthreads();
-    // valid pool positions (the context's last block may be partial)
-    int has_last = __syncthreads_or(threadIdx.x < kMaxPool && threadIdx.x < p_sel &&
+    // valid positions of the blocks (the context's last block may be partial)
+    int has_last = __syncthreads_or(threadIdx.x < kMaxPool && threadIdx.x < n_blk &&
                                     (sm.pool_ids[threadIdx.x] == nb - 1 ||
-                                     (threadIdx.x + 1024 < p_sel && sm.pool_ids[threadIdx.x + 1024] == nb - 1)));
-    int64_t npos = p_sel * kBlock - (has_last ? (nb * kBlock - c.n_ctx) : 0);
+                                     (threadIdx.x + 1024 < n_blk && sm.pool_ids[threadIdx.x + 1024] == nb - 1)));
+    int64_t npos = n_blk * kBlock - (has_last ? (nb * kBlock - c.n_ctx) : 0);
     int64_t k_sel = min64(K, npos);
     int32_t* tk = a.topk_out + int64_t(b) * K;
-    certified_select<kFp4>(a, sm, c, kPoolPos, p_sel * kBlock, k_sel, tk, g_exact, g_list, g_pick);
+    certified_select<kFp4>(a, sm, c, kPoolPos, n_blk * kBlock, k_sel, tk);
     if (c.rank == 0)
       for (int i = threadIdx.x; i < K; i += blockDim.x)
         if (i >= k_sel) tk[i] = -1;
@@ -1277,7 +1341,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
     int64_t npos = block_sum(sm, my);
     int64_t k_sel = min64(K, npos);
     int32_t* tk = a.topk_out + int64_t(b) * K;
-    certified_select<kFp4>(a, sm, c, kReindexPos, int64_t(plen) * kBlock, k_sel, tk, g_exact, g_list, g_pick);
+    certified_select<kFp4>(a, sm, c, kReindexPos, int64_t(plen) * kBlock, k_sel, tk);
     for (int i = threadIdx.x; i < K; i += blockDim.x)
       if (i >= k_sel) tk[i] = -1;
   }
@@ -1295,7 +1359,7 @@ cudaError_t launch_select(IdxArgs a, bool reindex, cudaStream_t st) {
   cudaError_t e = prepare_kernel(kern, smem, false, done[fp4 ? 1 : 0]);
   if (e != cudaSuccess) return e;
   CSA2_PROFILED(st, reindex ? "select_reindex" : "select_full",
-                (e = launch_pdl(kern, dim3(unsigned(cs), unsigned(a.batch), 1), dim3(kSelThreads), smem, st,
+                (e = launch_pdl(kern, dim3(unsigned(cs), unsigned(a.batch), reindex ? 1u : 2u), dim3(kSelThreads), smem, st,
                                 unsigned(cs), a, cs, reindex)));
   return e;
 }
