@@ -590,14 +590,15 @@ __device__ void exact_scores_fp4(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
 
 // Exact scores of up to kFastRows positions in one pass (E4M3 keys, every
 // head's query on the int64 path).  The positions' key rows are staged once
-// as the integers k*2^9 (all loads in flight together).  A lane then holds 16
-// channels of one head's integer query in registers -- lane = (head of 4,
-// eighth e), the eighth being the channels 32j + 4e + {0..3}, j < 4, so that
-// the 8 lanes of a head read a staged row as 128 consecutive bytes -- and
-// walks the positions: 16 exact products k*2^9 x qi summed in int64, the 8
-// lanes' sums combined by shuffles (exact in any order), the head dot rounded
-// once to fp64 and w_h * ReLU(d_h) formed; then one thread per position adds
-// the heads in order in fp64.  -inf for invalid positions.
+// as the integers k*2^9 (all loads in flight together).  A lane then holds 8
+// channels of one head's integer query in registers -- lane = (head of 2,
+// sixteenth e), the sixteenth being the channels 64j + 4e + {0..3}, j < 2, so
+// that the 16 lanes of a head read a staged row as 256 consecutive bytes -- and
+// walks the positions: 8 exact products k*2^9 x qi summed in int64 and the 16
+// lanes' sums combined by shuffles (exact in any order).  Then one thread per
+// (position, head) rounds the dot once to fp64 and forms w_h * ReLU(d_h), and
+// one thread per position adds the heads in order in fp64.  -inf for invalid
+// positions.
 __device__ void exact_scores_fast(const IdxArgs& a, SelSmem& sm, const SelCtx& c, const int64_t* pos, int np,
                                   double* out) {
   ExScratch& ex = ex_scratch(sm);
@@ -624,14 +625,14 @@ __device__ void exact_scores_fast(const IdxArgs& a, SelSmem& sm, const SelCtx& c
                              sm.k_lut[w[j] >> 24]);
   }
   // ---- this lane's query channels (registers) ----------------------------------
-  const int wpp = (hi + 3) >> 2;                               // warps per position
+  const int wpp = (hi + 1) >> 1;                               // warps per position
   const int ngroups = kSelWarps / wpp;                         // positions walked at once
-  const int g = wid / wpp, h = (wid % wpp) * 4 + (lane >> 3), e = lane & 7;
+  const int g = wid / wpp, h = (wid % wpp) * 2 + (lane >> 4), e = lane & 15;
   const bool hv = g < ngroups && h < hi;
-  int4 q[4];
+  int4 q[2];
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    q[j] = hv ? reinterpret_cast<const int4*>(sm.qi + h * kQiStride)[8 * j + e] : make_int4(0, 0, 0, 0);
+  for (int j = 0; j < 2; ++j)
+    q[j] = hv ? reinterpret_cast<const int4*>(sm.qi + h * kQiStride)[16 * j + e] : make_int4(0, 0, 0, 0);
   __syncthreads();
   // ---- products: a warp walks positions g, g + ngroups, ... (warp-uniform) -------
   if (g < ngroups) {
@@ -640,8 +641,8 @@ __device__ void exact_scores_fast(const IdxArgs& a, SelSmem& sm, const SelCtx& c
       const int4* kr = reinterpret_cast<const int4*>(kdec + p * 128) + e;
       long long acc = 0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int4 k = kr[8 * j];
+      for (int j = 0; j < 2; ++j) {
+        const int4 k = kr[16 * j];
         acc += (long long)q[j].x * k.x;
         acc += (long long)q[j].y * k.y;
         acc += (long long)q[j].z * k.z;
@@ -650,13 +651,20 @@ __device__ void exact_scores_fast(const IdxArgs& a, SelSmem& sm, const SelCtx& c
       acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
       acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 2);
       acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 4);
-      if (hv && e == 0) {
-        const double d = int_to_f64_rn(acc, sm.q_elo[h] - 9);
-        const unsigned long long db = (unsigned long long)__double_as_longlong(d);
-        const bool positive = (db >> 63) == 0 && db != 0;
-        dd[p * kMaxIdxHeads + h] = __dmul_rn(f32_to_f64_exact(sm.w[h]), positive ? d : 0.0);
-      }
+      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 8);
+      if (hv && e == 0) reinterpret_cast<long long*>(dd)[p * kMaxIdxHeads + h] = acc;
     }
+  }
+  __syncthreads();
+  // ---- the head dots in fp64, one (position, head) per thread (full warps on
+  // the fp64 path) -------------------------------------------------------------------
+  for (int i = tid; i < np * hi; i += kSelThreads) {
+    const int p = i / hi, hh = i - p * hi;
+    const long long acc = reinterpret_cast<const long long*>(dd)[p * kMaxIdxHeads + hh];
+    const double d = int_to_f64_rn(acc, sm.q_elo[hh] - 9);
+    const unsigned long long db = (unsigned long long)__double_as_longlong(d);
+    const bool positive = (db >> 63) == 0 && db != 0;
+    dd[p * kMaxIdxHeads + hh] = __dmul_rn(f32_to_f64_exact(sm.w[hh]), positive ? d : 0.0);
   }
   __syncthreads();
   // ---- ordered head sums ----------------------------------------------------------

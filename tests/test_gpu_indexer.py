@@ -92,6 +92,22 @@ def test_full_ties_large_band():
     check_full(p, *run_full(p))
 
 
+def test_full_cluster_ties_topk_side_falls_back():
+    """A context above one selection CTA (a cluster of 2) with massive ties:
+    the Top-K side's superset of the K best blocks is wider than the pool
+    buffer, so that side selects the pool itself first; a short context in the
+    same call takes every block."""
+    p = make_problem([200000, 3000], kind="ties", P=1024, K=256, seed=30, with_kv=False)
+    check_full(p, *run_full(p))
+
+
+def test_full_cluster_pool_smaller_than_topk():
+    """K > P on a cluster of 2: the Top-K must come from the pool's positions
+    (no superset of the K best blocks), selected after the pool."""
+    p = make_problem([140000, 900], P=64, K=128, seed=31, with_kv=False)
+    check_full(p, *run_full(p))
+
+
 def test_error_bound_holds():
     """|approximate score - exact score| <= delta for every position."""
     p = make_problem([60000, 12345], seed=7, with_kv=False)

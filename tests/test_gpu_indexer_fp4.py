@@ -110,6 +110,12 @@ def test_fp4_reindex_paged_ragged(paged):
     np.testing.assert_array_equal(run_reindex(p, pool, plen).cpu().numpy(), tk_full.cpu().numpy())
 
 
+def test_fp4_cluster_selection():
+    """A context above one selection CTA (a cluster of 2), with a short one."""
+    p = make_fp4_problem([200000, 5000], seed=32, P=512, K=256)
+    check_full(p, *run_full(p))
+
+
 def test_fp4_exact_ties():
     """Keys drawn from 3 distinct rows: huge groups of exactly equal scores."""
     p = make_fp4_problem([30000, 5000], kind="ties", P=256, K=512, seed=5)
