@@ -23,6 +23,15 @@
 // a thread-block cluster of up to 8 CTAs that merge their radix histograms
 // through distributed shared memory.  Cluster barriers are hardware barriers
 // (no software spin).
+//
+// Full mode runs two selection sides at once (grid z).  Side 0 selects the
+// pool.  Side 1 selects the Top-K positions from the blocks whose bounds let
+// them be among the K best blocks (the certain ones and the band of a block
+// selection with k = K, without exact re-scoring): a Top-K position's block
+// is among the K best blocks, and these are in the pool when K <= P or the
+// pool is every block.  Otherwise side 0 selects the pool and then the Top-K
+// of its positions.  The positions of at most P blocks are selected by one
+// CTA (rank 0 of a cluster).
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -42,6 +51,8 @@ constexpr int kSelWarps = kSelThreads / 32;
 static_assert(kMaxPool % kSelThreads == 0, "pool ids per selection thread");
 constexpr int kSortCap = 4096;
 constexpr int kBins = 2048;                 // 11-bit radix digits
+constexpr int kMaxSelCluster = 8;           // CTAs of a selection cluster
+static_assert(kMaxCtx / kBlock <= int64_t(kMaxSelCluster) * kSelCapPerCta, "block items fit the cluster");
 constexpr int kExItems = 128;               // band items re-scored per chunk (<= 8 positions each)
 constexpr int kQiStride = 132;              // words per head row of the integer query (16-byte
                                             // loads of 16 heads spread over all banks)
@@ -63,7 +74,7 @@ struct SelSmem {
   float w[kMaxIdxHeads];
   int32_t pool_ids[kMaxPool];
   uint32_t red[2][kSelWarps];
-  uint32_t bucket[2], rem[2];
+  uint32_t bucket, bucket_cnt, rem;
   uint32_t kmin, kmax, base_key;
   float dmax, dmax_all, dred[kSelWarps];
   uint32_t kmax_all;
@@ -153,50 +164,42 @@ __device__ uint32_t scan_words(SelSmem& sm, const uint32_t* bits, int nwords) {
   return total;
 }
 
-// For both key kinds j in {0: U, 1: L}: the bin (scanning from the top) that
-// holds the sm.rem[j]-th largest key of sm.ghist[j]; updates bucket / rem.
-// Thread t owns bins 2047-2t and 2046-2t.
-__device__ void find_buckets(SelSmem& sm) {
+// The bin (scanning from the top) of histogram h that holds the sm.rem-th
+// largest key; sets sm.bucket and sm.bucket_cnt (its count) and updates
+// sm.rem.  Thread t owns bins 2047-2t and 2046-2t.
+static_assert(kBins == 2 * kSelThreads, "two bins per thread");
+__device__ void find_bucket(SelSmem& sm, const uint32_t* h) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  uint32_t c0[2], c1[2], tot[2], incl[2];
+  const uint32_t rem = sm.rem;               // rewritten only after the barriers below
+  const uint32_t c0 = h[kBins - 1 - 2 * tid], c1 = h[kBins - 2 - 2 * tid], tot = c0 + c1;
+  uint32_t x = tot;
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    c0[j] = sm.ghist[j][kBins - 1 - 2 * tid];
-    c1[j] = sm.ghist[j][kBins - 2 - 2 * tid];
-    tot[j] = c0[j] + c1[j];
-    uint32_t x = tot[j];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-      if (lane >= o) x += y;
-    }
-    incl[j] = x;
-    if (lane == 31) sm.red[j][wid] = x;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
   }
+  if (lane == 31) sm.red[0][wid] = x;
   __syncthreads();
-  if (wid < 2) {
-    uint32_t s = sm.red[wid][lane];
+  if (wid == 0) {
+    uint32_t s = sm.red[0][lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      uint32_t y = __shfl_up_sync(0xFFFFFFFFu, s, o);
+      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, s, o);
       if (lane >= o) s += y;
     }
-    sm.red[wid][lane] = s;
+    sm.red[0][lane] = s;
   }
   __syncthreads();
-  uint32_t rem[2] = {sm.rem[0], sm.rem[1]};
-  __syncthreads();
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    uint32_t before = (wid ? sm.red[j][wid - 1] : 0) + incl[j] - tot[j];
-    if (before < rem[j] && rem[j] <= before + tot[j]) {
-      if (before + c0[j] >= rem[j]) {
-        sm.bucket[j] = kBins - 1 - 2 * tid;
-        sm.rem[j] = rem[j] - before;
-      } else {
-        sm.bucket[j] = kBins - 2 - 2 * tid;
-        sm.rem[j] = rem[j] - before - c0[j];
-      }
+  const uint32_t before = (wid ? sm.red[0][wid - 1] : 0) + x - tot;
+  if (before < rem && rem <= before + tot) {
+    if (before + c0 >= rem) {
+      sm.bucket = kBins - 1 - 2 * tid;
+      sm.bucket_cnt = c0;
+      sm.rem = rem - before;
+    } else {
+      sm.bucket = kBins - 2 - 2 * tid;
+      sm.bucket_cnt = c1;
+      sm.rem = rem - before - c0;
     }
   }
   __syncthreads();
@@ -234,6 +237,17 @@ __device__ void radix_edges(SelSmem& sm, const SelCtx& c, int n_local, uint32_t 
   if (lane == 0) { sm.red[0][wid] = kmin_l; sm.red[1][wid] = kmax_l; sm.dred[wid] = dmax_l; }
   __syncthreads();
   static_assert(kSelWarps == 32, "one lane per warp partial");
+  // the key range and the largest bound, set by lane 0 of warp 0 (of rank 0's
+  // view for a cluster: every rank computes the same values)
+  auto set_range = [&](uint32_t lo, uint32_t hi, float dm) {
+    sm.rem = k;
+    sm.base_key = lo;
+    sm.kmax_all = hi;
+    sm.dmax_all = dm;
+    const uint32_t range = hi - lo;
+    const int bits = range ? 32 - __clz(range) : 0;
+    sm.shift0 = bits > 11 ? bits - 11 : 0;
+  };
   if (wid == 0) {                      // the warps' partials, one per lane
     uint32_t a0 = sm.red[0][lane], a1 = sm.red[1][lane];
     float dm = sm.dred[lane];
@@ -244,35 +258,32 @@ __device__ void radix_edges(SelSmem& sm, const SelCtx& c, int n_local, uint32_t 
       dm = fmaxf(dm, __shfl_xor_sync(0xFFFFFFFFu, dm, o));
     }
     if (lane == 0) {
-      sm.kmin = a0;
-      sm.kmax = a1;
-      sm.dmax = dm;
+      if (c.cs > 1) {
+        sm.kmin = a0;
+        sm.kmax = a1;
+        sm.dmax = dm;
+      } else {
+        set_range(a0, a1, dm);
+      }
     }
   }
-  cl_sync(c);
-  if (wid == 0) {                      // the ranks' values, one rank per lane
-    uint32_t a0 = 0xFFFFFFFFu, a1 = 0;
-    float dm = 0.0f;
-    if (lane < c.cs) {
-      a0 = *remote(c, &sm.kmin, lane);
-      a1 = *remote(c, &sm.kmax, lane);
-      dm = *remote(c, &sm.dmax, lane);
-    }
+  if (c.cs > 1) {
+    cl_sync(c);
+    if (wid == 0) {                    // the ranks' values, one rank per lane
+      uint32_t a0 = 0xFFFFFFFFu, a1 = 0;
+      float dm = 0.0f;
+      if (lane < c.cs) {
+        a0 = *remote(c, &sm.kmin, lane);
+        a1 = *remote(c, &sm.kmax, lane);
+        dm = *remote(c, &sm.dmax, lane);
+      }
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      a0 = min(a0, __shfl_xor_sync(0xFFFFFFFFu, a0, o));
-      a1 = max(a1, __shfl_xor_sync(0xFFFFFFFFu, a1, o));
-      dm = fmaxf(dm, __shfl_xor_sync(0xFFFFFFFFu, dm, o));
-    }
-    if (lane == 0) {
-      sm.rem[0] = k;
-      sm.rem[1] = k;
-      sm.base_key = a0;
-      sm.kmax_all = a1;
-      sm.dmax_all = dm;
-      uint32_t range = a1 - a0;
-      int bits = range ? 32 - __clz(range) : 0;
-      sm.shift0 = bits > 11 ? bits - 11 : 0;
+      for (int o = 16; o; o >>= 1) {
+        a0 = min(a0, __shfl_xor_sync(0xFFFFFFFFu, a0, o));
+        a1 = max(a1, __shfl_xor_sync(0xFFFFFFFFu, a1, o));
+        dm = fmaxf(dm, __shfl_xor_sync(0xFFFFFFFFu, dm, o));
+      }
+      if (lane == 0) set_range(a0, a1, dm);
     }
   }
   cl_sync(c);       // the range is read before any rank overwrites kmin / kmax
@@ -281,7 +292,7 @@ __device__ void radix_edges(SelSmem& sm, const SelCtx& c, int n_local, uint32_t 
   uint32_t b0 = 0;
   int width_shift = sh0;
   for (int pass = 0; pass < 2; ++pass) {
-    for (int i = tid; i < 2 * kBins; i += blockDim.x) (&sm.hist[0][0])[i] = 0;
+    for (int i = tid; i < kBins; i += blockDim.x) sm.hist[0][i] = 0;
     __syncthreads();
     const int sh = pass ? sh1 : sh0;
     for (int i = tid; i < n_local; i += blockDim.x) {
@@ -292,26 +303,32 @@ __device__ void radix_edges(SelSmem& sm, const SelCtx& c, int n_local, uint32_t 
       else if ((du >> sh0) == b0) atomicAdd(&sm.hist[0][(du - (b0 << sh0)) >> sh], 1u);
     }
     cl_sync(c);
-    for (int i = tid; i < kBins; i += blockDim.x) {
-      uint32_t t = 0;
-      for (int r = 0; r < c.cs; ++r) t += remote(c, &sm.hist[0][0], r)[i];
-      sm.ghist[0][i] = t;
-      sm.ghist[1][i] = 0;
+    const uint32_t* h = &sm.hist[0][0];
+    if (c.cs > 1) {
+      // the ranks' histograms summed (every rank's loads in flight together)
+      for (int i = tid; i < kBins; i += blockDim.x) {
+        uint32_t t = 0;
+#pragma unroll 4
+        for (int r = 0; r < kMaxSelCluster; ++r)
+          if (r < c.cs) t += remote(c, &sm.hist[0][0], r)[i];
+        sm.ghist[0][i] = t;
+      }
+      cl_sync(c);     // every rank has read every histogram before they are reset
+      h = &sm.ghist[0][0];
     }
-    cl_sync(c);     // every rank has read every histogram before they are reset
-    find_buckets(sm);
+    find_bucket(sm, h);
     if (pass == 0) {
-      b0 = sm.bucket[0];
+      b0 = sm.bucket;
       // narrow enough: few items, or a value width below the largest bound
       // (refining could not shrink the band by more than that)
       const uint64_t top = min64(int64_t(kb) + (int64_t(b0) << sh0) + ((int64_t(1) << sh0) - 1), int64_t(sm.kmax_all));
       const float wv = key_f32(uint32_t(top)) - key_f32(kb + (b0 << sh0));
-      if (sh0 == 0 || sm.ghist[0][b0] <= kRefine || wv <= sm.dmax_all) break;
+      if (sh0 == 0 || sm.bucket_cnt <= kRefine || wv <= sm.dmax_all) break;
     } else {
       width_shift = sh1;
     }
   }
-  const uint32_t lo = pass_lo(b0, sh0, sm.bucket[0], width_shift, sh1);
+  const uint32_t lo = pass_lo(b0, sh0, sm.bucket, width_shift, sh1);
   // the bucket's top, clamped to the largest key (the k-th largest is below it)
   const uint64_t hi64 = uint64_t(kb) + lo + ((uint64_t(1) << width_shift) - 1);
   const uint32_t hi_key = hi64 > sm.kmax_all ? sm.kmax_all : uint32_t(hi64);
@@ -809,15 +826,16 @@ __device__ int64_t certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx&
     uint32_t muE, lamE;
     radix_edges(sm, c, n_local, uint32_t(k), kmin_l, kmax_l, dmax_l, muE, lamE);
     uint32_t my_in = 0, my_band = 0;                  // lane 0's warp totals
+    // key order is float order (-0 and +0 one key): compare the bounds as floats
+    const float muF = key_f32(muE), lamF = key_f32(lamE);
     for (int i0 = tid - lane; i0 < n_local; i0 += blockDim.x) {
       const int i = i0 + lane;
       const uint32_t kv = i < n_local ? sm.keyU[i] : 0u;
       bool in = false, band = false;
       if (kv != 0) {
         const float v = key_f32(kv), dl = __uint_as_float(sm.keyL[i]);
-        const uint32_t u = f32_key(__fadd_ru(v, dl)), l = f32_key(__fadd_rd(v, -dl));
-        in = l > muE;
-        band = !in && u >= lamE;
+        in = __fadd_rd(v, -dl) > muF;
+        band = !in && __fadd_ru(v, dl) >= lamF;
       }
       const uint32_t mi = __ballot_sync(0xFFFFFFFFu, in), mb = __ballot_sync(0xFFFFFFFFu, band);
       if (lane == 0) {
@@ -1241,8 +1259,10 @@ __device__ void load_query_factors(const IdxArgs& a, SelSmem& sm, int b) {
   }
 }
 
-// Full mode: pool over the cluster, then Top-K of the pool positions on rank
-// 0.  Reindex mode (cluster of 1): Top-K of the pool positions.
+// Full mode: side 0 selects the pool over the cluster, side 1 the Top-K from a
+// superset of the K best blocks (or side 0 the Top-K of the pool positions
+// after the pool), the positions on rank 0 alone.  Reindex mode (cluster of
+// 1): Top-K of the pool positions.
 template <bool kFp4>
 __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int cs, bool reindex) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -1313,6 +1333,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
     }
     cl_sync(c);                    // every rank's block ids are written (read through L2)
     if (c.cs > 1) {
+      // the positions of at most P blocks fit one CTA: rank 0 takes them alone
+      // (no cluster exchange); the other ranks' shared memory is not read again
+      if (c.rank != 0) return;
+      c.cs = 1;
       for (int i = threadIdx.x; i < kMaxPool; i += blockDim.x) sm.pool_ids[i] = i < n_blk ? __ldcg(blocks + i) : -1;
     } else {
       for (int i = threadIdx.x; i < kMaxPool; i += blockDim.x)
