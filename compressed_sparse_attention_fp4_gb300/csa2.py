@@ -22,6 +22,7 @@ IDXK_E4M3, IDXK_F32, IDXK_FP4 = 0, 1, 2
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
 MAX_QLEN = 4
 IDX_EARLY_INPUTS = 1
+KV_EARLY_INPUTS = 1
 
 STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED_SHAPE",
           3: "CSA2_ERR_WORKSPACE_TOO_SMALL", 4: "CSA2_ERR_CUDA",
@@ -49,6 +50,7 @@ SIGNATURES = {
     "csa2_workspace_size": (_I32, [ctypes.POINTER(CDims), _I32, ctypes.POINTER(_SZ)]),
     "fp4_kv_quantize": (_I32, [_P, _I64, _P, _P, _P]),
     "fp4_kv_quantize_scatter": (_I32, [_P, _I64, _P, _P, _P, _P]),
+    "fp4_kv_quantize_scatter_ex": (_I32, [_P, _I64, _P, _P, _P, _I32, _P]),
     "fp4_idx_k_quantize_scatter": (_I32, [_P, _I64, _P, _P, _I64, _P]),
     "fp4_kv_dequantize": (_I32, [_P, _P, _I64, _P, _P]),
     "indexer_full_topk": (_I32, [ctypes.POINTER(CDims), _I32, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -156,8 +158,14 @@ def fp4_kv_quantize(x: torch.Tensor, codes: torch.Tensor | None = None,
 
 
 def fp4_kv_quantize_scatter(x: torch.Tensor, dst_rows: torch.Tensor, codes: torch.Tensor,
-                            scales: torch.Tensor, stream=None):
-    """Quantize row i of x into cache row dst_rows[i] (int64)."""
+                            scales: torch.Tensor, stream=None, flags: int = 0):
+    """Quantize row i of x into cache row dst_rows[i] (int64).  flags:
+    KV_EARLY_INPUTS (see fp4_kv_quantize_scatter_ex in include/csa2.h) or 0."""
+    if flags:
+        _check("fp4_kv_quantize_scatter_ex",
+               _lib.fp4_kv_quantize_scatter_ex(_ptr(x), x.shape[0], _ptr(dst_rows), _ptr(codes),
+                                               _ptr(scales), int(flags), _stream(stream)))
+        return
     _check("fp4_kv_quantize_scatter",
            _lib.fp4_kv_quantize_scatter(_ptr(x), x.shape[0], _ptr(dst_rows), _ptr(codes),
                                         _ptr(scales), _stream(stream)))

@@ -116,17 +116,23 @@ csa2_status fp4_kv_quantize(const uint16_t* x, int64_t n, uint8_t* codes, uint8_
   if (n < 0) return CSA2_ERR_INVALID_ARG;
   if (n == 0) return CSA2_OK;
   if (!x || !codes || !scales || !aligned(x, 16) || !aligned(codes, 4)) return CSA2_ERR_INVALID_ARG;
-  return from_cuda(launch_quantize(x, n, nullptr, codes, scales, as_stream(stream)));
+  return from_cuda(launch_quantize(x, n, nullptr, codes, scales, false, as_stream(stream)));
 }
 
-csa2_status fp4_kv_quantize_scatter(const uint16_t* x, int64_t n, const int64_t* dst_rows,
-                                    uint8_t* codes, uint8_t* scales, void* stream) {
-  if (n < 0) return CSA2_ERR_INVALID_ARG;
+csa2_status fp4_kv_quantize_scatter_ex(const uint16_t* x, int64_t n, const int64_t* dst_rows,
+                                       uint8_t* codes, uint8_t* scales, int32_t flags, void* stream) {
+  if (n < 0 || (flags & ~int32_t(CSA2_KV_EARLY_INPUTS)) != 0) return CSA2_ERR_INVALID_ARG;
   if (n == 0) return CSA2_OK;
   if (!x || !dst_rows || !codes || !scales || !aligned(x, 16) || !aligned(codes, 4) ||
       !aligned(dst_rows, 8))
     return CSA2_ERR_INVALID_ARG;
-  return from_cuda(launch_quantize(x, n, dst_rows, codes, scales, as_stream(stream)));
+  return from_cuda(launch_quantize(x, n, dst_rows, codes, scales, (flags & CSA2_KV_EARLY_INPUTS) != 0,
+                                   as_stream(stream)));
+}
+
+csa2_status fp4_kv_quantize_scatter(const uint16_t* x, int64_t n, const int64_t* dst_rows,
+                                    uint8_t* codes, uint8_t* scales, void* stream) {
+  return fp4_kv_quantize_scatter_ex(x, n, dst_rows, codes, scales, 0, stream);
 }
 
 csa2_status fp4_idx_k_quantize_scatter(const uint16_t* x, int64_t n, const int64_t* dst_rows,

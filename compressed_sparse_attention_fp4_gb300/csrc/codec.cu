@@ -22,11 +22,15 @@ namespace csa2 {
 __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__ x, int64_t n,
                                                        const int64_t* __restrict__ dst_rows,
                                                        uint32_t* __restrict__ codes,
-                                                       uint8_t* __restrict__ scales) {
+                                                       uint8_t* __restrict__ scales, int early) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-  pdl_wait();
+  // early inputs: the kernel before writes none of x / dst_rows and touches
+  // none of the destination rows; the rows are written while it runs, and
+  // this grid completes only after it (the wait at the end), so whatever
+  // waits on this grid also sees that kernel's results
+  if (!early) pdl_wait();
   pdl_launch_dependents();
   for (int64_t row = warp; row < n; row += nwarps) {
     int64_t dst = dst_rows ? dst_rows[row] : row;
@@ -42,6 +46,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint4* __restrict__
       if ((lane & 1) == 0) scales[dst * 32 + r * 16 + (lane >> 1)] = uint8_t(sc);
     }
   }
+  if (early) pdl_wait();
 }
 
 // Two E2M1 nibbles (low nibble = first) -> f16x2 (low half = first), exact.
@@ -123,13 +128,13 @@ static int codec_grid(int64_t n) {
 }
 
 cudaError_t launch_quantize(const uint16_t* x, int64_t n, const int64_t* dst_rows, uint8_t* codes,
-                            uint8_t* scales, cudaStream_t st) {
+                            uint8_t* scales, bool early, cudaStream_t st) {
   if (n == 0) return cudaSuccess;
   cudaError_t e;
   CSA2_PROFILED(st, "fp4_quantize",
                 (e = launch_pdl(quantize_kernel, dim3(codec_grid(n)), dim3(256), 0, st, 1,
                                 reinterpret_cast<const uint4*>(x), n, dst_rows,
-                                reinterpret_cast<uint32_t*>(codes), scales)));
+                                reinterpret_cast<uint32_t*>(codes), scales, early ? 1 : 0)));
   return e;
 }
 

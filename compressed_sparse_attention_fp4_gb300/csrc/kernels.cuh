@@ -122,7 +122,7 @@ struct AttnArgs {
 };
 
 cudaError_t launch_quantize(const uint16_t* x, int64_t n, const int64_t* dst_rows, uint8_t* codes,
-                            uint8_t* scales, cudaStream_t st);
+                            uint8_t* scales, bool early, cudaStream_t st);
 cudaError_t launch_quantize_idx(const uint16_t* x, int64_t n, const int64_t* dst_rows, uint8_t* idx_k,
                                 int64_t cache_rows, cudaStream_t st);
 cudaError_t launch_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t n, uint16_t* y,

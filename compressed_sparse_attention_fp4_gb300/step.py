@@ -82,18 +82,21 @@ def step_calls(sb: StepBuffers, stream=None) -> list:
     cur = None
     for l, mode in enumerate(sb.schedule):
         if mode == "F":
-            if sb.new_latent is not None:
-                calls.append((f"append@{l}", lambda: csa2.fp4_kv_quantize_scatter(
-                    sb.new_latent, sb.new_rows, sb.kv_codes, sb.kv_scales, stream=stream)))
-                if sb.new_idx_k is not None:
-                    calls.append((f"append_idx@{l}", lambda: csa2.fp4_idx_k_quantize_scatter(
-                        sb.new_idx_k, sb.idx_k, sb.idx_rows, sb.new_rows, stream=stream)))
-            # the keys are not written by the call before (the latent append or an
-            # attention call) unless the newest token's FP4 key write precedes it
-            fl = csa2.IDX_EARLY_INPUTS if sb.new_idx_k is None else 0
+            if sb.new_latent is not None and sb.new_idx_k is not None:
+                calls.append((f"append_idx@{l}", lambda: csa2.fp4_idx_k_quantize_scatter(
+                    sb.new_idx_k, sb.idx_k, sb.idx_rows, sb.new_rows, stream=stream)))
+            # the keys are not written by the call before (an attention call, or
+            # nothing) unless the newest token's FP4 key write precedes it
+            fl = csa2.IDX_EARLY_INPUTS if sb.new_idx_k is None or sb.new_latent is None else 0
             calls.append((f"F@{l}", lambda l=l, fl=fl: csa2.indexer_full_topk(
                 d, B, sb.idx_k, sb.page_table, sb.ctx_len, sb.idx_q[l], sb.idx_w[l], sb.pool,
                 sb.pool_len, sb.topk[l], sb.ws, stream=stream, flags=fl)))
+            if sb.new_latent is not None:
+                # the newest token's latent goes into the main KV while the indexer
+                # runs (the indexer reads no main-KV rows); attention comes after both
+                calls.append((f"append@{l}", lambda: csa2.fp4_kv_quantize_scatter(
+                    sb.new_latent, sb.new_rows, sb.kv_codes, sb.kv_scales, stream=stream,
+                    flags=csa2.KV_EARLY_INPUTS)))
             cur = l
             m = csa2.MODE_FULL
         elif mode == "Ri":

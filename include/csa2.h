@@ -145,6 +145,20 @@ csa2_status fp4_kv_quantize_scatter(const uint16_t* x, int64_t n,
                                     const int64_t* dst_rows, uint8_t* codes,
                                     uint8_t* scales, void* stream);
 
+/* fp4_kv_quantize_scatter with flags (0: the plain call).
+ * CSA2_KV_EARLY_INPUTS: the operation enqueued just before this call on the
+ * stream writes neither x nor dst_rows and reads or writes none of the
+ * destination rows, so the rows may be written while it is still running;
+ * the call still completes only after that operation has completed, so
+ * later work on the stream sees the results of both.  In a decode step this
+ * holds for the newest token's append enqueued after the Full layer's
+ * indexer call (which reads no main-KV rows).  Other bits:
+ * CSA2_ERR_INVALID_ARG. */
+#define CSA2_KV_EARLY_INPUTS 1
+csa2_status fp4_kv_quantize_scatter_ex(const uint16_t* x, int64_t n,
+                                       const int64_t* dst_rows, uint8_t* codes,
+                                       uint8_t* scales, int32_t flags, void* stream);
+
 /* FP4 indexer-key write (the main-KV format of fp4_kv_quantize applied to
  * the indexer keys: foosynaptic atlas 3.2 "FP4 main KV" and the FP4-trained
  * indexer of newsaint.id section 4).  Row i of x (bf16 [n][128], device,
@@ -220,9 +234,10 @@ csa2_status indexer_reindex_topk(const csa2_dims* d, int32_t batch,
  * that operation began), so the call may start reading them -- the scan
  * streams its first key tiles -- while that operation is still running.
  * idx_q, w, the outputs and the workspace are accessed only after it has
- * finished.  In a decode step this holds for a Full layer that follows the
- * latent append (not the indexer-key write) and for a Reindex layer that
- * follows an attention call.  Other bits: CSA2_ERR_INVALID_ARG. */
+ * finished.  In a decode step this holds for a Full layer that follows an
+ * attention call or the latent append (not the indexer-key write) and for a
+ * Reindex layer that follows an attention call.  Other bits:
+ * CSA2_ERR_INVALID_ARG. */
 #define CSA2_IDX_EARLY_INPUTS 1
 csa2_status indexer_full_topk_ex(const csa2_dims* d, int32_t batch, int32_t flags,
                                  const void* idx_k, const int32_t* page_table,

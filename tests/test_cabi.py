@@ -174,3 +174,16 @@ def test_indexer_ex_flags(mod):
     assert lib.indexer_full_topk_ex(ctypes.byref(d.c()), 2, 2, *args, fake, ws, None) == 1      # unknown flag
     assert lib.indexer_full_topk_ex(ctypes.byref(d.c()), 2, 1, *args, fake, ws - 1, None) == 3   # checks as usual
     assert lib.indexer_reindex_topk_ex(ctypes.byref(d.c()), 2, -1, fake, None, *([fake] * 6), fake, ws, None) == 1
+
+
+def test_kv_append_ex_flags(mod):
+    lib = mod._lib
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    f = lib.fp4_kv_quantize_scatter_ex
+    assert f(fake, 4, fake, fake, fake, 2, None) == 1          # unknown flag
+    assert f(fake, 4, fake, fake, fake, -1, None) == 1
+    assert f(fake, 0, fake, fake, fake, 1, None) == 0          # nothing to write
+    assert f(None, 4, fake, fake, fake, 1, None) == 1          # checks as usual
+    assert f(P(0x10008), 4, fake, fake, fake, 1, None) == 1    # x not 16-byte aligned
+    assert mod.KV_EARLY_INPUTS == 1

@@ -104,6 +104,15 @@ def test_ragged_row_counts_and_scatter(lib):
     codes.zero_()
     lib.fp4_kv_quantize_scatter(_to_dev(x), dst2, codes, scales)
     assert not codes.cpu().numpy()[perm[::2]].any()
+    # early inputs (written while the kernel before runs, completed after it): the same bytes
+    codes.zero_()
+    scales.zero_()
+    busy = torch.empty(1 << 26, dtype=torch.uint8, device="cuda")
+    busy.fill_(3)                                   # some kernel just before
+    lib.fp4_kv_quantize_scatter(_to_dev(x), dst, codes, scales, flags=lib.KV_EARLY_INPUTS)
+    np.testing.assert_array_equal(codes.cpu().numpy()[perm], oc)
+    np.testing.assert_array_equal(scales.cpu().numpy()[perm], os_)
+    assert not codes.cpu().numpy()[rest].any()
 
 
 def test_codec_workload_full_size(lib):
