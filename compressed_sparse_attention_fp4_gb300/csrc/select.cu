@@ -24,14 +24,15 @@
 // through distributed shared memory.  Cluster barriers are hardware barriers
 // (no software spin).
 //
-// Full mode runs two selection sides at once (grid z).  Side 0 selects the
-// pool.  Side 1 selects the Top-K positions from the blocks whose bounds let
-// them be among the K best blocks (the certain ones and the band of a block
-// selection with k = K, without exact re-scoring): a Top-K position's block
-// is among the K best blocks, and these are in the pool when K <= P or the
-// pool is every block.  Otherwise side 0 selects the pool and then the Top-K
-// of its positions.  The positions of at most P blocks are selected by one
-// CTA (rank 0 of a cluster).
+// Full mode runs two selection sides at once (grid z) while both fit one
+// wave of one CTA per SM.  Side 0 selects the pool.  Side 1 selects the
+// Top-K positions from the blocks whose bounds let them be among the K best
+// blocks (the certain ones and the band of a block selection with k = K,
+// without exact re-scoring): a Top-K position's block is among the K best
+// blocks, and these are in the pool when K <= P or the pool is every block.
+// Otherwise (or for a larger batch) side 0 selects the pool and then the
+// Top-K of its positions.  The positions of at most P blocks are selected by
+// one CTA (rank 0 of a cluster).
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -1264,7 +1265,7 @@ __device__ void load_query_factors(const IdxArgs& a, SelSmem& sm, int b) {
 // after the pool), the positions on rank 0 alone.  Reindex mode (cluster of
 // 1): Top-K of the pool positions.
 template <bool kFp4>
-__global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int cs, bool reindex) {
+__global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int cs, bool reindex, bool two_sides) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
   const int b = blockIdx.y;
@@ -1310,7 +1311,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
     // the Top-K from the blocks whose bounds let them be among the K best
     // (a superset of them), at the same time as side 0 selects the pool; else
     // side 0 does both in turn and side 1 has nothing to do.
-    const bool split = K <= P || nb <= P;
+    const bool split = two_sides && (K <= P || nb <= P);
     if (side == 1 && !split) return;
     const int64_t p_sel = min64(P, nb);
     int64_t n_blk = p_sel;                       // blocks the Top-K positions are taken from
@@ -1386,13 +1387,16 @@ cudaError_t launch_select(IdxArgs a, bool reindex, cudaStream_t st) {
   const int cs = reindex ? 1 : int((a.L.nb_max + kSelCapPerCta - 1) / kSelCapPerCta);
   const size_t smem = sizeof(SelSmem);
   const bool fp4 = a.d.idx_k_dtype == CSA2_IDXK_FP4;
+  // Full: the two sides side by side while both fit one wave (one CTA per
+  // SM); a larger batch selects the pool and then its Top-K in one CTA set
+  const bool two_sides = !reindex && int64_t(cs) * a.batch * 2 <= device_sms();
   auto kern = fp4 ? select_kernel<true> : select_kernel<false>;
   static KernelAttrs done[2];
   cudaError_t e = prepare_kernel(kern, smem, false, done[fp4 ? 1 : 0]);
   if (e != cudaSuccess) return e;
   CSA2_PROFILED(st, reindex ? "select_reindex" : "select_full",
-                (e = launch_pdl(kern, dim3(unsigned(cs), unsigned(a.batch), reindex ? 1u : 2u), dim3(kSelThreads), smem, st,
-                                unsigned(cs), a, cs, reindex)));
+                (e = launch_pdl(kern, dim3(unsigned(cs), unsigned(a.batch), two_sides ? 2u : 1u), dim3(kSelThreads),
+                                smem, st, unsigned(cs), a, cs, reindex, two_sides)));
   return e;
 }
 
