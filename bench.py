@@ -349,12 +349,12 @@ def roofline_table(wl, kern, steps_launches, peak, peak_kind):
 # null once the kernel's source changes.  Units: indexed positions for the
 # scans, sequence-layers for the attention.
 TRAFFIC_UNITS = {
-    # decode-128k capture (8 x 131,072 = 1,048,576 positions): 134,319,616 B read + 3,536,128 B written
-    ("indexer_scan_tc", "9b77308c25b9"): (134319616 + 3536128) / 1048576,
-    # decode-128k Reindex capture (8 x 16,384 pool positions): 16,942,848 B read, 0 written
-    ("reindex_score_tc", "9b77308c25b9"): 16942848 / 131072,
-    # decode-1m-fp4 capture (1,048,576 positions): 75,581,696 B read + 1,408,512 B written
-    ("indexer_scan_fp4", "226069cc75b6"): (75581696 + 1408512) / 1048576,
+    # decode-128k capture (8 x 131,072 = 1,048,576 positions): 134,323,456 B read + 3,971,328 B written
+    ("indexer_scan_tc", "34b2a05f427c"): (134323456 + 3971328) / 1048576,
+    # decode-128k Reindex capture (8 x 16,384 pool positions): 16,943,104 B read, 0 written
+    ("reindex_score_tc", "34b2a05f427c"): 16943104 / 131072,
+    # decode-1m-fp4 capture (1,048,576 positions): 75,580,160 B read + 1,634,560 B written
+    ("indexer_scan_fp4", "982de1fdde57"): (75580160 + 1634560) / 1048576,
     # decode-128k capture (8 sequence-layers): 3,930,368 B read, 0 written (outputs stay in L2)
     ("attn_cluster_tc", "2e496407fa56"): 3930368 / 8,
 }
