@@ -51,23 +51,29 @@ def oracle_sequence(wl_name: str, b: int, want_scores: bool = False):
     wl = synth.workload(wl_name)
     kv = synth.sequence_kv(wl, b)
     n = wl.ctx_lens[b]
-    keys = idxk_f64(kv["idx_k"], wl.idx_k_dtype)
+    if wl.idx_k_dtype == "fp4":
+        # FP4 indexer: the oracle quantizes the bf16 query and keys itself
+        from oracle import indexer_fp4 as ix
+        keys = bf16_f64(kv["idx_k"])
+    else:
+        ix = oix
+        keys = idxk_f64(kv["idx_k"], wl.idx_k_dtype)
     layers = [synth.layer_inputs(wl, b, l) for l in range(len(wl.schedule))]
-    conv_q = (lambda x: bf16_f64(x)) if wl.idx_k_dtype == "fp8" else (lambda x: x.astype(np.float64))
+    conv_q = (lambda x: bf16_f64(x)) if wl.idx_k_dtype in ("fp8", "fp4") else (lambda x: x.astype(np.float64))
     res, pool, cur = [], None, None
     for l, mode in enumerate(wl.schedule):
         li = layers[l]
         rec = {"mode": mode}
         if mode == "F":
-            r = oix.full_topk(conv_q(li["idx_q"]), li["idx_w"].astype(np.float64), keys,
-                              wl.pool_blocks, wl.topk)
+            r = ix.full_topk(conv_q(li["idx_q"]), li["idx_w"].astype(np.float64), keys,
+                             wl.pool_blocks, wl.topk)
             pool, cur = r["pool"], r["topk"]
             rec.update(pool=pool, margin_pool=r["margin_pool"], margin_topk=r["margin_topk"])
             if want_scores:
                 rec["scores"] = r["scores"]
         elif mode == "Ri":
-            r = oix.reindex_topk(conv_q(li["idx_q"]), li["idx_w"].astype(np.float64), keys, pool,
-                                 wl.topk)
+            r = ix.reindex_topk(conv_q(li["idx_q"]), li["idx_w"].astype(np.float64), keys, pool,
+                                wl.topk)
             cur = r["topk"]
             rec.update(margin_topk=r["margin_topk"])
         rec["topk"] = cur
@@ -77,10 +83,11 @@ def oracle_sequence(wl_name: str, b: int, want_scores: bool = False):
     lat = np.zeros((n, 512))
     lat[need] = oracle_latent(kv["latent"][need])
     rope = bf16_f64(kv["rope"])
+    attend = oatt.sparse_attn_decode if wl.q_len == 1 else oatt.sparse_attn_decode_mq
     for l, r in enumerate(res):
         li = layers[l]
-        r["out"], r["lse"] = oatt.sparse_attn_decode(bf16_f64(li["q"]), lat, rope, r["topk"],
-                                                     bf16_f64(li["swa"]), li["swa_len"], wl.scale)
+        r["out"], r["lse"] = attend(bf16_f64(li["q"]), lat, rope, r["topk"], bf16_f64(li["swa"]),
+                                    li["swa_len"], wl.scale)
     return res
 
 

@@ -98,6 +98,29 @@ def test_128k_workload():
     check_step(wl, sb, range(wl.batch), bound=True)
 
 
+def test_128k_fp4_keys_workload():
+    """FP4 indexer keys (the library writes every key, the newest token's in
+    the step, before the Full layer's scan): all 8 sequences, every layer; the
+    FP4 scan's bound at every position."""
+    wl = synth.workload("128k-fp4")
+    sb = workload.build(wl)
+    g = GraphedStep(sb)
+    g.replay()
+    torch.cuda.synchronize()
+    check_step(wl, sb, range(wl.batch), bound=True)
+
+
+def test_128k_four_query_tokens_workload():
+    """Four query tokens per sequence and layer (one Top-K set, each query's
+    own window limit): all 8 sequences, every layer and query."""
+    wl = synth.workload("128k-q4")
+    sb = workload.build(wl)
+    g = GraphedStep(sb)
+    g.replay()
+    torch.cuda.synchronize()
+    check_step(wl, sb, range(wl.batch))
+
+
 def test_1m_workload():
     """The 1,048,576-position sequence, every layer; the bound at every position."""
     wl = synth.workload("1m")
