@@ -306,15 +306,24 @@ __device__ void radix_edges(SelSmem& sm, const SelCtx& c, int n_local, uint32_t 
     cl_sync(c);
     const uint32_t* h = &sm.hist[0][0];
     if (c.cs > 1) {
-      // the ranks' histograms summed (every rank's loads in flight together)
-      for (int i = tid; i < kBins; i += blockDim.x) {
+      // the ranks' histograms summed: each rank sums its own slice of the bins
+      // over the ranks (every rank's loads in flight together), then gathers
+      // the other slices from their owners
+      const int per = (kBins + c.cs - 1) / c.cs;
+      const int lo = c.rank * per, hi = min(kBins, lo + per);
+      for (int i = lo + tid; i < hi; i += blockDim.x) {
         uint32_t t = 0;
 #pragma unroll 4
         for (int r = 0; r < kMaxSelCluster; ++r)
           if (r < c.cs) t += remote(c, &sm.hist[0][0], r)[i];
         sm.ghist[0][i] = t;
       }
-      cl_sync(c);     // every rank has read every histogram before they are reset
+      cl_sync(c);     // every slice summed; every rank has read every histogram before they are reset
+      for (int i = tid; i < kBins; i += blockDim.x) {
+        const int owner = i / per;
+        if (owner != c.rank) sm.ghist[0][i] = remote(c, &sm.ghist[0][0], owner)[i];
+      }
+      __syncthreads();
       h = &sm.ghist[0][0];
     }
     find_bucket(sm, h);

@@ -108,6 +108,14 @@ def test_full_cluster_pool_smaller_than_topk():
     check_full(p, *run_full(p))
 
 
+def test_full_large_batch_selects_in_turn():
+    """80 sequences: two selection sides per sequence would not fit one wave of
+    one CTA per SM, so each sequence's CTA selects the pool and then its Top-K."""
+    lens = [int(x) for x in np.random.default_rng(33).integers(1, 6000, size=80)]
+    p = make_problem(lens, P=256, K=128, seed=33, with_kv=False)
+    check_full(p, *run_full(p))
+
+
 def test_error_bound_holds():
     """|approximate score - exact score| <= delta for every position."""
     p = make_problem([60000, 12345], seed=7, with_kv=False)
