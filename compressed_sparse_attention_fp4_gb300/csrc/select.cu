@@ -838,32 +838,37 @@ __device__ int64_t certified_select(const IdxArgs& a, SelSmem& sm, const SelCtx&
     uint32_t my_in = 0, my_band = 0;                  // lane 0's warp totals
     // key order is float order (-0 and +0 one key): compare the bounds as floats
     const float muF = key_f32(muE), lamF = key_f32(lamE);
-    for (int i0 = tid - lane; i0 < n_local; i0 += blockDim.x) {
-      const int i = i0 + lane;
-      const uint32_t kv = i < n_local ? sm.keyU[i] : 0u;
-      bool in = false, band = false;
-      if (kv != 0) {
-        const float v = key_f32(kv), dl = __uint_as_float(sm.keyL[i]);
-        in = __fadd_rd(v, -dl) > muF;
-        band = !in && __fadd_ru(v, dl) >= lamF;
-      }
-      const uint32_t mi = __ballot_sync(0xFFFFFFFFu, in), mb = __ballot_sync(0xFFFFFFFFu, band);
-      if (lane == 0) {
-        sm.sel_bits[i0 >> 5] = mi;
-        sm.band_bits[i0 >> 5] = mb;
-        my_in += __popc(mi);
-        my_band += __popc(mb);
-      }
-    }
-    if (lane == 0) {
-      atomicAdd(&sm.cnt_in, my_in);
-      atomicAdd(&sm.cnt_band, my_band);
-    }
     if (superset) {
-      // every item that may be among the k best: certain or in the band
-      __syncthreads();
-      for (int wv = tid; wv < nwords; wv += blockDim.x) sm.sel_bits[wv] |= sm.band_bits[wv];
+      // every item that may be among the k best (certain or in the band): U >= lambda'
+      for (int i0 = tid - lane; i0 < n_local; i0 += blockDim.x) {
+        const int i = i0 + lane;
+        const uint32_t kv = i < n_local ? sm.keyU[i] : 0u;
+        const bool may = kv != 0 && __fadd_ru(key_f32(kv), __uint_as_float(sm.keyL[i])) >= lamF;
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, may);
+        if (lane == 0) sm.sel_bits[i0 >> 5] = m;
+      }
     } else {
+      for (int i0 = tid - lane; i0 < n_local; i0 += blockDim.x) {
+        const int i = i0 + lane;
+        const uint32_t kv = i < n_local ? sm.keyU[i] : 0u;
+        bool in = false, band = false;
+        if (kv != 0) {
+          const float v = key_f32(kv), dl = __uint_as_float(sm.keyL[i]);
+          in = __fadd_rd(v, -dl) > muF;
+          band = !in && __fadd_ru(v, dl) >= lamF;
+        }
+        const uint32_t mi = __ballot_sync(0xFFFFFFFFu, in), mb = __ballot_sync(0xFFFFFFFFu, band);
+        if (lane == 0) {
+          sm.sel_bits[i0 >> 5] = mi;
+          sm.band_bits[i0 >> 5] = mb;
+          my_in += __popc(mi);
+          my_band += __popc(mb);
+        }
+      }
+      if (lane == 0) {
+        atomicAdd(&sm.cnt_in, my_in);
+        atomicAdd(&sm.cnt_band, my_band);
+      }
       // this side's band scratch in the workspace (cluster case, large bands)
       const int64_t wso = (int64_t(c.b) * 2 + c.side) * a.L.sel_cap;
       double* g_exact = reinterpret_cast<double*>(a.ws + a.L.sel_exact) + wso;
