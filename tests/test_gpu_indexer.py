@@ -101,6 +101,14 @@ def test_full_cluster_ties_topk_side_falls_back():
     check_full(p, *run_full(p))
 
 
+@pytest.mark.parametrize("paged", [False, True])
+def test_full_cluster_two_sides(paged):
+    """A cluster of 2 per sequence and both selection sides (K <= P), on a
+    contiguous and a paged cache."""
+    p = make_problem([200000, 3000, 140001], paged=paged, P=1024, K=256, seed=34, with_kv=False)
+    check_full(p, *run_full(p))
+
+
 def test_full_cluster_pool_smaller_than_topk():
     """K > P on a cluster of 2: the Top-K must come from the pool's positions
     (no superset of the K best blocks), selected after the pool."""
