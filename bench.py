@@ -348,6 +348,8 @@ def roofline_table(wl, kern, steps_launches, peak, peak_kind):
 # per unit of work, keyed by (kernel, hash of its source file when captured);
 # null once the kernel's source changes.  Units: indexed positions for the
 # scans, sequence-layers for the attention.
+NOMINAL_HBM_GBS = 8000.0      # nominal HBM bandwidth (~8 TB/s; the measured copy peak is the roofline)
+
 TRAFFIC_UNITS = {
     # decode-128k capture (8 x 131,072 = 1,048,576 positions): 134,323,456 B read + 3,971,328 B written
     ("indexer_scan_tc", "34b2a05f427c"): (134323456 + 3971328) / 1048576,
@@ -570,7 +572,8 @@ def summarise(res, peak, peak_kind):
     dom = max((n for n in tab if "bytes_per_launch" in tab[n]), key=lambda n: tab[n]["us_per_step"])
     d = tab[dom]
     roof = {"bound": "hbm", "kernel": dom, "achieved": d["achieved_gbs"], "peak": peak, "unit": "GB/s",
-            "frac": d["frac"], "peak_source": peak_kind, "bytes_per_launch": d["bytes_per_launch"],
+            "frac": d["frac"], "frac_of_nominal": d["achieved_gbs"] / NOMINAL_HBM_GBS,
+            "peak_source": peak_kind, "bytes_per_launch": d["bytes_per_launch"],
             "avg_launch_us": d["avg_us"], "traffic": d.get("traffic")}
     return {
         "value": res["qps"], "ms_per_step": t,
@@ -578,6 +581,7 @@ def summarise(res, peak, peak_kind):
         "algorithmic_bytes_per_step": sbytes,
         "step_gbs": sbytes / (t * 1e-3) / 1e9,
         "step_frac_of_peak": sbytes / (t * 1e-3) / 1e9 / peak,
+        "step_frac_of_nominal_hbm": sbytes / (t * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
         "kernel_us": res["kern_us"],
         "roofline": roof,
         "roofline_kernels": tab,
@@ -693,6 +697,7 @@ def main():
         "e2e_eager": res["e2e_eager"],
     }
     for k in ("ms_per_step_p5_p50_p95", "algorithmic_bytes_per_step", "step_gbs", "step_frac_of_peak",
+              "step_frac_of_nominal_hbm",
               "kernel_us", "roofline_kernels", "graph_attribution", "device_status"):
         line[k] = summ[k]
     if not args.no_extra and world == 1 and wl.name == "128k":
