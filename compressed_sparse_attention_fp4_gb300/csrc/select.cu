@@ -1318,26 +1318,57 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
   const int P = a.d.pool_blocks, K = a.d.topk;
   __syncthreads();
   int64_t nb = (c.n_ctx + kBlock - 1) / kBlock;
-  if (!reindex) {
-    // The Top-K positions lie in the K best blocks (a block ahead of the
-    // block of a Top-K position p holds a position ahead of p), which the
-    // pool holds when K <= P or the pool is every block.  Then side 1 takes
-    // the Top-K from the blocks whose bounds let them be among the K best
-    // (a superset of them), at the same time as side 0 selects the pool; else
-    // side 0 does both in turn and side 1 has nothing to do.
-    const bool split = two_sides && (K <= P || nb <= P);
-    if (side == 1 && !split) return;
-    const int64_t p_sel = min64(P, nb);
-    int64_t n_blk = p_sel;                       // blocks the Top-K positions are taken from
-    int32_t* blocks = side == 0 ? a.pool_out + int64_t(b) * P       // their ids (ascending)
-                                : reinterpret_cast<int32_t*>(a.ws + a.L.sel_blocks) + int64_t(b) * P;
-    // side 1: the superset first; a band too wide for it (ties) takes the
-    // pool itself, as side 0 finds it
-    for (int pass = side; pass >= 0; --pass) {
-      const bool sup = pass == 1;
-      n_blk = certified_select<kFp4>(a, sm, c, kBlocks, nb, sup ? min64(K, nb) : p_sel, blocks, sup);
-      if (n_blk <= P) break;
+  // Full: the Top-K positions lie in the K best blocks (a block ahead of the
+  // block of a Top-K position p holds a position ahead of p), which the pool
+  // holds when K <= P or the pool is every block.  Then side 1 takes the
+  // Top-K from the blocks whose bounds let them be among the K best (a
+  // superset of them), at the same time as side 0 selects the pool; else
+  // side 0 does both in turn and side 1 has nothing to do.
+  const bool split = !reindex && two_sides && (K <= P || nb <= P);
+  if (!reindex && side == 1 && !split) return;
+  const int64_t p_sel = min64(P, nb);
+  int32_t* blocks = side == 0 ? a.pool_out + int64_t(b) * P       // the blocks' ids (ascending)
+                              : reinterpret_cast<int32_t*>(a.ws + a.L.sel_blocks) + int64_t(b) * P;
+  int32_t* tk = a.topk_out + int64_t(b) * K;
+  ItemKind kind = reindex ? kReindexPos : kBlocks;
+  bool sup = !reindex && side == 1;
+  int64_t n_items = nb, k_sel = sup ? min64(K, nb) : p_sel;
+  if (reindex) {
+    int32_t plen = plen_raw;
+    if (plen < 0 || plen > P) { if (threadIdx.x == 0) raise_err(a.ws, CSA2_DEV_POOL); plen = 0; }
+#pragma unroll
+    for (int j = 0; j < kPoolPer; ++j) {
+      const int i = threadIdx.x + j * kSelThreads;
+      int32_t blk = i < plen ? pin_raw[j] : -1;
+      if (blk >= nb) { raise_err(a.ws, CSA2_DEV_POOL); blk = -1; }
+      sm.pool_ids[i] = blk;
     }
+    __syncthreads();
+    int my = 0;
+    for (int i = threadIdx.x; i < plen; i += blockDim.x) {
+      int32_t blk = sm.pool_ids[i];
+      if (blk >= 0) my += int(min64(kBlock, c.n_ctx - int64_t(blk) * kBlock));
+    }
+    n_items = int64_t(plen) * kBlock;
+    k_sel = min64(K, block_sum(sm, my));
+  }
+  // One call site of the selection for every phase a CTA runs (the blocks,
+  // then the positions), so that a later phase finds its code in the
+  // instruction cache.
+  for (;;) {
+    const int64_t got = certified_select<kFp4>(a, sm, c, kind, n_items, k_sel, kind == kBlocks ? blocks : tk, sup);
+    if (kind != kBlocks) {
+      if (c.rank == 0)
+        for (int i = threadIdx.x; i < K; i += blockDim.x)
+          if (i >= k_sel) tk[i] = -1;
+      return;
+    }
+    if (sup && got > P) {          // a band too wide for the superset (ties): the pool itself, as side 0 finds it
+      sup = false;
+      k_sel = p_sel;
+      continue;
+    }
+    const int64_t n_blk = sup ? got : p_sel;      // blocks the Top-K positions are taken from
     if (side == 0) {
       if (c.rank == 0) {
         for (int i = threadIdx.x; i < P; i += blockDim.x)
@@ -1362,35 +1393,11 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(IdxArgs a, int c
     int has_last = __syncthreads_or(threadIdx.x < kMaxPool && threadIdx.x < n_blk &&
                                     (sm.pool_ids[threadIdx.x] == nb - 1 ||
                                      (threadIdx.x + 1024 < n_blk && sm.pool_ids[threadIdx.x + 1024] == nb - 1)));
-    int64_t npos = n_blk * kBlock - (has_last ? (nb * kBlock - c.n_ctx) : 0);
-    int64_t k_sel = min64(K, npos);
-    int32_t* tk = a.topk_out + int64_t(b) * K;
-    certified_select<kFp4>(a, sm, c, kPoolPos, n_blk * kBlock, k_sel, tk);
-    if (c.rank == 0)
-      for (int i = threadIdx.x; i < K; i += blockDim.x)
-        if (i >= k_sel) tk[i] = -1;
-  } else {
-    int32_t plen = plen_raw;
-    if (plen < 0 || plen > P) { if (threadIdx.x == 0) raise_err(a.ws, CSA2_DEV_POOL); plen = 0; }
-#pragma unroll
-    for (int j = 0; j < kPoolPer; ++j) {
-      const int i = threadIdx.x + j * kSelThreads;
-      int32_t blk = i < plen ? pin_raw[j] : -1;
-      if (blk >= nb) { raise_err(a.ws, CSA2_DEV_POOL); blk = -1; }
-      sm.pool_ids[i] = blk;
-    }
-    __syncthreads();
-    int my = 0;
-    for (int i = threadIdx.x; i < plen; i += blockDim.x) {
-      int32_t blk = sm.pool_ids[i];
-      if (blk >= 0) my += int(min64(kBlock, c.n_ctx - int64_t(blk) * kBlock));
-    }
-    int64_t npos = block_sum(sm, my);
-    int64_t k_sel = min64(K, npos);
-    int32_t* tk = a.topk_out + int64_t(b) * K;
-    certified_select<kFp4>(a, sm, c, kReindexPos, int64_t(plen) * kBlock, k_sel, tk);
-    for (int i = threadIdx.x; i < K; i += blockDim.x)
-      if (i >= k_sel) tk[i] = -1;
+    const int64_t npos = n_blk * kBlock - (has_last ? (nb * kBlock - c.n_ctx) : 0);
+    kind = kPoolPos;
+    sup = false;
+    n_items = n_blk * kBlock;
+    k_sel = min64(K, npos);
   }
 }
 
