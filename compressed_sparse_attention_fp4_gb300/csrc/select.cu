@@ -1190,88 +1190,81 @@ __device__ void load_query_fp4(const IdxArgs& a, SelSmem& sm, int b) {
 // per-head minima, sums and flags are reduced in the warp first and reach
 // shared memory with one atomic per warp.
 __device__ void load_query_factors(const IdxArgs& a, SelSmem& sm, int b) {
-  const int hi = a.d.idx_heads, di = a.d.idx_dim, n = hi * di;
-  const int lane = threadIdx.x & 31;
-
+  const int hi = a.d.idx_heads, di = a.d.idx_dim;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const bool fp8 = a.d.idx_k_dtype == CSA2_IDXK_E4M3;
-  // every global load of this thread is issued before the first use
-  constexpr int kPer = kMaxIdxHeads * 128 / kSelThreads;
-  static_assert(kPer * kSelThreads == kMaxIdxHeads * 128, "query elements per thread");
-  float qv[kPer];
+  // one warp per head (its di <= 128 channels, 4 per lane: channel lane + 32 j);
+  // every global load of the warp is issued before the first use, and a head's
+  // reductions stay inside its warp (no block barrier between the steps)
+  static_assert(kMaxIdxHeads <= kSelWarps, "a warp per indexer head");
+  constexpr int kPerLane = 128 / 32;
+  const int h = wid;
+  const bool head = h < hi;
+  float qv[kPerLane];
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int i = threadIdx.x + j * kSelThreads;
-    const int64_t qidx = int64_t(b) * n + i;
-    qv[j] = i >= n ? 0.0f
-                   : fp8 ? bf16_to_f32(reinterpret_cast<const uint16_t*>(a.idx_q)[qidx])
-                         : reinterpret_cast<const float*>(a.idx_q)[qidx];
+  for (int j = 0; j < kPerLane; ++j) {
+    const int ch = lane + 32 * j;
+    const int64_t qidx = (int64_t(b) * hi + h) * di + ch;
+    qv[j] = !head || ch >= di ? 0.0f
+          : fp8 ? bf16_to_f32(reinterpret_cast<const uint16_t*>(a.idx_q)[qidx])
+                : reinterpret_cast<const float*>(a.idx_q)[qidx];
   }
   const float wv = threadIdx.x < hi ? a.w[int64_t(b) * hi + threadIdx.x] : 0.0f;
-  if (threadIdx.x < kMaxIdxHeads) {
-    sm.q_elo[threadIdx.x] = INT_MAX;
-    sm.q_fast[threadIdx.x] = 1;
-    sm.q_l1[threadIdx.x] = 0;
+  if (threadIdx.x >= 512 && threadIdx.x < 512 + 256) {
+    const Factor f = factor_e4m3(threadIdx.x - 512);
+    sm.k_lut[threadIdx.x - 512] = f.sig * (1 << (f.exp + 9));
   }
-  __syncthreads();
-  // a warp's 32 elements lie in one head (n is a multiple of 32)
+  bool fast = true;                                   // this thread's share of the AND below
+  if (h < kMaxIdxHeads) {
+    Factor f[kPerLane];
+    int lsb = INT_MAX;                                // lowest set bit of the head's values
 #pragma unroll
-  for (int j = 0; j < kPer; ++j) {
-    const int i = threadIdx.x + j * kSelThreads;
-    if (i >= n) break;
-    const int h = i / di, ch = i % di;
-    const Factor f = factor_f32(qv[j]);
-    sm.qf[ch * kMaxIdxHeads + h] = f;
-    int lsb = f.sig ? f.exp + __ffs(abs(f.sig)) - 1 : INT_MAX;      // lowest set bit
-    lsb = __reduce_min_sync(0xFFFFFFFFu, lsb);
-    if (lane == 0 && lsb != INT_MAX) atomicMin(&sm.q_elo[h], lsb);
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const int h = i / di, ch = i % di;
-    const Factor f = sm.qf[ch * kMaxIdxHeads + h];
-    int32_t qv = 0;
-    bool wide = false;
-    unsigned long long mag64 = 0;
-    if (f.sig) {
-      // q = sig * 2^exp = qv * 2^q_elo; sh < 0 only drops trailing zero bits
-      const int sh = f.exp - sm.q_elo[h];
-      int mag = abs(f.sig);
-      const int bits = 32 - __clz(mag) + sh;
-      if (bits > 30) {
-        wide = true;
-      } else {
-        mag = sh >= 0 ? (mag << sh) : (mag >> -sh);
-        qv = f.sig < 0 ? -mag : mag;
-        mag64 = (unsigned long long)mag;
+    for (int j = 0; j < kPerLane; ++j) {
+      const int ch = lane + 32 * j;
+      f[j] = factor_f32(qv[j]);
+      if (head && ch < di) {
+        sm.qf[ch * kMaxIdxHeads + h] = f[j];
+        if (f[j].sig) lsb = min(lsb, f[j].exp + __ffs(abs(f[j].sig)) - 1);
       }
     }
-    sm.qi[h * kQiStride + ch] = qv;
-    // mag < 2^30: the warp sums of its 16-bit halves fit 32 bits
-    const uint32_t s_lo = __reduce_add_sync(0xFFFFFFFFu, uint32_t(mag64 & 0xFFFF));
-    const uint32_t s_hi = __reduce_add_sync(0xFFFFFFFFu, uint32_t(mag64 >> 16));
-    const bool any_wide = __any_sync(0xFFFFFFFFu, wide);
-    if (lane == 0) {
-      if (any_wide) atomicAnd(&sm.q_fast[h], 0);
-      atomicAdd(&sm.q_l1[h], (unsigned long long)s_hi * 65536ull + s_lo);
+    const int q_elo = __reduce_min_sync(0xFFFFFFFFu, lsb);
+    bool wide = false;
+    unsigned long long l1 = 0;                        // sum of |qi| (each below 2^30)
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) {
+      const int ch = lane + 32 * j;
+      if (!head || ch >= di) continue;
+      int32_t q = 0;
+      if (f[j].sig) {
+        // q = sig * 2^exp = q * 2^q_elo; sh < 0 only drops trailing zero bits
+        const int sh = f[j].exp - q_elo;
+        int mag = abs(f[j].sig);
+        const int bits = 32 - __clz(mag) + sh;
+        if (bits > 30) {
+          wide = true;
+        } else {
+          mag = sh >= 0 ? (mag << sh) : (mag >> -sh);
+          q = f[j].sig < 0 ? -mag : mag;
+          l1 += (unsigned long long)mag;
+        }
+      }
+      sm.qi[h * kQiStride + ch] = q;
     }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
+    const bool any_wide = __any_sync(0xFFFFFFFFu, wide);
+    // int64 room: sum_c |qi| * max|k*2^9| (448 * 512) must stay below 2^62
+    const bool qf_h = head && !any_wide && fp8 && di == 128 && l1 < (1ull << 62) / 229376ull;
+    if (lane == 0) {
+      sm.q_elo[h] = q_elo;
+      sm.q_fast[h] = qf_h ? 1 : 0;
+      sm.q_l1[h] = l1;
+    }
+    fast = !head || qf_h;
   }
   if (threadIdx.x < hi) sm.w[threadIdx.x] = wv;
-  __syncthreads();
-  if (threadIdx.x < kMaxIdxHeads) {
-    // int64 room: sum_c |qi| * max|k*2^9| (448 * 512) must stay below 2^62
-    if (threadIdx.x >= hi || !fp8 || di != 128 || sm.q_l1[threadIdx.x] >= (1ull << 62) / 229376ull)
-      sm.q_fast[threadIdx.x] = 0;
-  }
-  if (threadIdx.x < 256) {
-    const Factor f = factor_e4m3(threadIdx.x);
-    sm.k_lut[threadIdx.x] = f.sig * (1 << (f.exp + 9));
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int fast = fp8 && di == 128;
-    for (int h = 0; h < hi; ++h) fast = fast && sm.q_fast[h];
-    sm.fast_exact = fast;
-  }
+  const int all_fast = __syncthreads_and(fast ? 1 : 0);
+  if (threadIdx.x == 0) sm.fast_exact = fp8 && di == 128 && all_fast;
 }
 
 // Full mode: side 0 selects the pool over the cluster, side 1 the Top-K from a
