@@ -1185,10 +1185,9 @@ __device__ void load_query_fp4(const IdxArgs& a, SelSmem& sm, int b) {
   __syncthreads();
 }
 
-// Query factors of sequence b.  Elements h*di + ch are spread over the
-// threads so that a warp's 32 elements share one head (di is 64 or 128):
-// per-head minima, sums and flags are reduced in the warp first and reach
-// shared memory with one atomic per warp.
+// Query factors of sequence b: for every head its values as factors, as
+// integers qi over the head's lowest set bit q_elo, the flag of the exact
+// int64 path and the weights; the E4M3 value table.  One warp per head.
 __device__ void load_query_factors(const IdxArgs& a, SelSmem& sm, int b) {
   const int hi = a.d.idx_heads, di = a.d.idx_dim;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
