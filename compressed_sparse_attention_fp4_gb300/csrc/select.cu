@@ -617,19 +617,16 @@ __device__ void exact_scores_fp4(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
 
 // Exact scores of up to kFastRows positions in one pass (E4M3 keys, every
 // head's query on the int64 path).  The positions' key rows are staged once
-// as the integers k*2^9 (all loads in flight together).  A lane then holds 8
-// channels of one head's integer query in registers -- lane = (head of 2,
-// sixteenth e), the sixteenth being the channels 64j + 4e + {0..3}, j < 2, so
-// that the 16 lanes of a head read a staged row as 256 consecutive bytes -- and
-// walks the positions: 8 exact products k*2^9 x qi summed in int64 and the 16
-// lanes' sums combined by shuffles (exact in any order).  Then one thread per
-// (position, head) rounds the dot once to fp64 and forms w_h * ReLU(d_h), and
-// one thread per position adds the heads in order in fp64.  -inf for invalid
-// positions.
+// as the integers k*2^9 (all loads in flight together).  Then one thread per
+// (position, head) sums its 128 exact products k*2^9 x qi in int64 (a warp's
+// 32 pairs read one or two staged rows and the rows of up to 16 heads of the
+// integer query: broadcasts, no cross-lane reduction), rounds the dot once to
+// fp64 and forms w_h * ReLU(d_h); one thread per position adds the heads in
+// order in fp64.  -inf for invalid positions.
 __device__ void exact_scores_fast(const IdxArgs& a, SelSmem& sm, const SelCtx& c, const int64_t* pos, int np,
                                   double* out) {
   ExScratch& ex = ex_scratch(sm);
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, hi = a.d.idx_heads;
+  const int tid = threadIdx.x, hi = a.d.idx_heads;
   double* dd = &ex.dd[0][0];                                   // [kFastRows][kMaxIdxHeads]
   int32_t* kdec = reinterpret_cast<int32_t*>(dd + kFastRows * kMaxIdxHeads);   // [kFastRows][128]
   // ---- stage the rows: 8 threads per position, the words 8j + e of the row ----
@@ -651,47 +648,29 @@ __device__ void exact_scores_fast(const IdxArgs& a, SelSmem& sm, const SelCtx& c
       dst[8 * j] = make_int4(sm.k_lut[w[j] & 0xFF], sm.k_lut[(w[j] >> 8) & 0xFF], sm.k_lut[(w[j] >> 16) & 0xFF],
                              sm.k_lut[w[j] >> 24]);
   }
-  // ---- this lane's query channels (registers) ----------------------------------
-  const int wpp = (hi + 1) >> 1;                               // warps per position
-  const int ngroups = kSelWarps / wpp;                         // positions walked at once
-  const int g = wid / wpp, h = (wid % wpp) * 2 + (lane >> 4), e = lane & 15;
-  const bool hv = g < ngroups && h < hi;
-  int4 q[2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j)
-    q[j] = hv ? reinterpret_cast<const int4*>(sm.qi + h * kQiStride)[16 * j + e] : make_int4(0, 0, 0, 0);
   __syncthreads();
-  // ---- products: a warp walks positions g, g + ngroups, ... (warp-uniform) -------
-  if (g < ngroups) {
-#pragma unroll 1
-    for (int p = g; p < np; p += ngroups) {
-      const int4* kr = reinterpret_cast<const int4*>(kdec + p * 128) + e;
-      long long acc = 0;
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int4 k = kr[16 * j];
-        acc += (long long)q[j].x * k.x;
-        acc += (long long)q[j].y * k.y;
-        acc += (long long)q[j].z * k.z;
-        acc += (long long)q[j].w * k.w;
-      }
-      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
-      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 2);
-      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 4);
-      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 8);
-      if (hv && e == 0) reinterpret_cast<long long*>(dd)[p * kMaxIdxHeads + h] = acc;
-    }
-  }
-  __syncthreads();
-  // ---- the head dots in fp64, one (position, head) per thread (full warps on
-  // the fp64 path) -------------------------------------------------------------------
+  // ---- one (position, head) per thread: the exact dot, then w_h * ReLU(d_h) -------
   for (int i = tid; i < np * hi; i += kSelThreads) {
-    const int p = i / hi, hh = i - p * hi;
-    const long long acc = reinterpret_cast<const long long*>(dd)[p * kMaxIdxHeads + hh];
-    const double d = int_to_f64_rn(acc, sm.q_elo[hh] - 9);
+    const int p = i / hi, h = i - p * hi;
+    const int4* kr = reinterpret_cast<const int4*>(kdec + p * 128);
+    const int4* qr = reinterpret_cast<const int4*>(sm.qi + h * kQiStride);
+    long long acc0 = 0, acc1 = 0;                              // two chains, summed exactly
+#pragma unroll 2
+    for (int c4 = 0; c4 < 32; c4 += 2) {
+      const int4 k0 = kr[c4], q0 = qr[c4], k1 = kr[c4 + 1], q1 = qr[c4 + 1];
+      acc0 += (long long)q0.x * k0.x;
+      acc1 += (long long)q1.x * k1.x;
+      acc0 += (long long)q0.y * k0.y;
+      acc1 += (long long)q1.y * k1.y;
+      acc0 += (long long)q0.z * k0.z;
+      acc1 += (long long)q1.z * k1.z;
+      acc0 += (long long)q0.w * k0.w;
+      acc1 += (long long)q1.w * k1.w;
+    }
+    const double d = int_to_f64_rn(acc0 + acc1, sm.q_elo[h] - 9);
     const unsigned long long db = (unsigned long long)__double_as_longlong(d);
     const bool positive = (db >> 63) == 0 && db != 0;
-    dd[p * kMaxIdxHeads + hh] = __dmul_rn(f32_to_f64_exact(sm.w[hh]), positive ? d : 0.0);
+    dd[p * kMaxIdxHeads + h] = __dmul_rn(f32_to_f64_exact(sm.w[h]), positive ? d : 0.0);
   }
   __syncthreads();
   // ---- ordered head sums ----------------------------------------------------------
