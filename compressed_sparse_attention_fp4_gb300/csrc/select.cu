@@ -546,8 +546,8 @@ static_assert(kFastRows * kMaxIdxHeads <= 2 * kExRows * kMaxIdxHeads, "head prod
 // M_k M_q I << (E_k + E_q + 18) (shift 0..28, below 2^47); the 8 terms sum
 // exactly in int64 (below 2^50) and d_h = sum * 2^-20 is exact in fp64.
 // Staging: 8 threads per position, one group each (8 code bytes widened to
-// 16 signed bytes, and the scale's M, E); products: two threads per
-// (position, head), 4 groups each (dp4a), halves combined.
+// 16 signed bytes, and the scale's M, E); products: one thread per
+// (position, head), its 8 groups (dp4a).
 __device__ void exact_scores_fp4(const IdxArgs& a, SelSmem& sm, const SelCtx& c, const int64_t* pos, int np,
                                  double* out) {
   ExScratch& ex = ex_scratch(sm);
@@ -573,18 +573,14 @@ __device__ void exact_scores_fp4(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
     ksc[p * 8 + g] = make_int2(f.sig, f.exp);
   }
   __syncthreads();
-  // warp-uniform trip count: both halves of a task sit in one warp and every
-  // lane takes part in the combining shuffle
-  const int lane = tid & 31, ntask = np * hi * 2;
-  for (int base = tid - lane; base < ntask; base += kSelThreads) {
-    const int task = base + lane;
-    const bool act = task < ntask;
-    const int half = task & 1, ph = task >> 1, p = act ? ph / hi : 0, h = act ? ph % hi : 0;
+  // one thread per (position, head): its 8 group terms, the dot rounded once
+  // to fp64 and w_h * ReLU(d_h) (the fp64 steps in full warps)
+  for (int i = tid; i < np * hi; i += kSelThreads) {
+    const int p = i / hi, h = i - p * hi;
     const uint4* q4 = reinterpret_cast<const uint4*>(sm.qi + h * kQiStride);
     long long acc = 0;
-#pragma unroll 1
-    for (int gg = 0; gg < (act ? 4 : 0); ++gg) {
-      const int g = 4 * half + gg;
+#pragma unroll 2
+    for (int g = 0; g < 8; ++g) {
       const uint4 kv = rows[p * 8 + g], qv = q4[g];
       int dot = __dp4a(int(kv.x), int(qv.x), 0);
       dot = __dp4a(int(kv.y), int(qv.y), dot);
@@ -594,13 +590,10 @@ __device__ void exact_scores_fp4(const IdxArgs& a, SelSmem& sm, const SelCtx& c,
       const Factor qf = sm.qf[h * 8 + g];
       acc += (long long)(kf.x * qf.sig * dot) * (1ll << (kf.y + qf.exp + 18));   // shift 0..28
     }
-    acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);               // the other half (exact)
-    if (act && half == 0) {
-      const double d = int_to_f64_rn(acc, -20);
-      const unsigned long long db = (unsigned long long)__double_as_longlong(d);
-      const bool positive = (db >> 63) == 0 && db != 0;
-      dd[p * kMaxIdxHeads + h] = __dmul_rn(f32_to_f64_exact(sm.w[h]), positive ? d : 0.0);
-    }
+    const double d = int_to_f64_rn(acc, -20);
+    const unsigned long long db = (unsigned long long)__double_as_longlong(d);
+    const bool positive = (db >> 63) == 0 && db != 0;
+    dd[p * kMaxIdxHeads + h] = __dmul_rn(f32_to_f64_exact(sm.w[h]), positive ? d : 0.0);
   }
   __syncthreads();
   if (tid < np) {
