@@ -124,6 +124,17 @@ def test_full_large_batch_selects_in_turn():
     check_full(p, *run_full(p))
 
 
+@pytest.mark.parametrize("Hi,P,K", [(1, 64, 8), (3, 4, 5), (5, 16, 16), (16, 2048, 2048)])
+def test_full_and_reindex_odd_shapes(Hi, P, K):
+    """Head counts that are not a multiple of the per-warp layouts, a pool
+    smaller than K (the Top-K after the pool), K = P (the superset rarely
+    fits: the pool itself) and K = P = 2048, on ragged contexts."""
+    p = make_problem([1, 9, 300, 5000, 20001], Hi=Hi, P=P, K=K, seed=40 + Hi, with_kv=False)
+    pool, plen, topk = run_full(p)
+    check_full(p, pool, plen, topk)
+    np.testing.assert_array_equal(run_reindex(p, pool, plen).cpu().numpy(), topk.cpu().numpy())
+
+
 def test_error_bound_holds():
     """|approximate score - exact score| <= delta for every position."""
     p = make_problem([60000, 12345], seed=7, with_kv=False)
