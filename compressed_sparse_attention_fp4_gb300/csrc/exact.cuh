@@ -10,7 +10,9 @@
 // Fixed point: every factor is sig * 2^exp with an integer significand (<=
 // 24 bits), so every product is an integer P (< 2^48) times 2^E.  Pass 1
 // finds the span of the products; if the sum fits in 62 bits it is
-// accumulated in one int64, else in an 11-limb (704-bit) two's-complement
+// accumulated in one int64, if it fits in 126 bits in one 128-bit integer
+// (kept in registers: the usual case of fp32 keys, whose smallest products
+// sit far below the largest), else in an 11-limb (704-bit) two's-complement
 // integer, which covers the whole fp32 x fp32 range.
 #pragma once
 
@@ -118,13 +120,33 @@ __device__ inline double limbs_to_double(uint64_t* L, int e0) {
   return neg ? -r : r;
 }
 
-// Correctly rounded fp64 value of sum_c q[c] * k[c] (q, k as Factors).
-// `kf(c)` returns the Factor of the key's channel c.
-template <class KF>
-__device__ double exact_head_dot(const Factor* __restrict__ q, int n, KF kf) {
+// Round the signed 128-bit integer v times 2^e0 to the nearest fp64 (ties
+// to even): the top 64 significant bits with a sticky bit for the rest go
+// through one correctly rounded 64-bit conversion (the sticky bit sits below
+// the rounding position, so it only breaks ties).
+__device__ inline double i128_to_double(__int128 v, int e0) {
+  const bool neg = v < 0;
+  const unsigned __int128 m = neg ? (unsigned __int128)0 - (unsigned __int128)v : (unsigned __int128)v;
+  const uint64_t hi = uint64_t(m >> 64), lo = uint64_t(m);
+  double r;
+  if (hi == 0) {
+    r = scalbn(__ull2double_rn(lo), e0);
+  } else {
+    const int s = 64 - __clzll((long long)hi);             // bits of hi, 1..64
+    const uint64_t mask = s == 64 ? ~uint64_t(0) : ((uint64_t(1) << s) - 1);
+    const uint64_t top64 = uint64_t(m >> s) | uint64_t((lo & mask) != 0);
+    r = scalbn(__ull2double_rn(top64), e0 + s);
+  }
+  return neg ? -r : r;
+}
+
+// Correctly rounded fp64 value of sum_c q(c) * k(c), the factors given as
+// Factors by `qf(c)` and `kf(c)`.
+template <class QF, class KF>
+__device__ double exact_head_dot(QF qf, int n, KF kf) {
   int elo = INT_MAX, ehi = INT_MIN;
   for (int c = 0; c < n; ++c) {
-    Factor a = q[c], b = kf(c);
+    Factor a = qf(c), b = kf(c);
     if (a.sig == 0 || b.sig == 0) continue;
     uint64_t P = uint64_t(llabs((long long)a.sig)) * uint64_t(llabs((long long)b.sig));
     int E = a.exp + b.exp;
@@ -136,7 +158,7 @@ __device__ double exact_head_dot(const Factor* __restrict__ q, int n, KF kf) {
   if (width <= 62) {
     long long acc = 0;
     for (int c = 0; c < n; ++c) {
-      Factor a = q[c], b = kf(c);
+      Factor a = qf(c), b = kf(c);
       if (a.sig == 0 || b.sig == 0) continue;
       unsigned long long P = uint64_t(llabs((long long)a.sig)) * uint64_t(llabs((long long)b.sig));
       long long term = (long long)(P << (a.exp + b.exp - elo));
@@ -144,10 +166,22 @@ __device__ double exact_head_dot(const Factor* __restrict__ q, int n, KF kf) {
     }
     return scalbn(__ll2double_rn(acc), elo);
   }
+  if (width <= 126) {
+    // every term is below 2^(width - 8) and the sum of <= 128 terms below 2^(width - 1)
+    __int128 acc = 0;
+    for (int c = 0; c < n; ++c) {
+      Factor a = qf(c), b = kf(c);
+      if (a.sig == 0 || b.sig == 0) continue;
+      const uint64_t P = uint64_t(llabs((long long)a.sig)) * uint64_t(llabs((long long)b.sig));
+      const __int128 term = (__int128)((unsigned __int128)P << (a.exp + b.exp - elo));
+      acc += ((a.sig < 0) != (b.sig < 0)) ? -term : term;
+    }
+    return i128_to_double(acc, elo);
+  }
   uint64_t L[kLimbs];
   for (int k = 0; k < kLimbs; ++k) L[k] = 0;
   for (int c = 0; c < n; ++c) {
-    Factor a = q[c], b = kf(c);
+    Factor a = qf(c), b = kf(c);
     if (a.sig == 0 || b.sig == 0) continue;
     uint64_t P = uint64_t(llabs((long long)a.sig)) * uint64_t(llabs((long long)b.sig));
     bool neg = (a.sig < 0) != (b.sig < 0);

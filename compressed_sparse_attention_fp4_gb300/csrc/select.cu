@@ -523,9 +523,7 @@ __device__ void exact_scores(const IdxArgs& a, SelSmem& sm, const SelCtx& c, con
           auto kf = [&](int ch) {
             return fp8 ? Factor{kr[ch], -9} : factor_f32(__int_as_float(kr[ch]));
           };
-          Factor qrow[128];
-          for (int ch = 0; ch < di; ++ch) qrow[ch] = sm.qf[ch * kMaxIdxHeads + h];
-          d = exact_head_dot(qrow, di, kf);
+          d = exact_head_dot([&](int ch) { return sm.qf[ch * kMaxIdxHeads + h]; }, di, kf);
         }
         // w_h * ReLU(d_h)
         const unsigned long long db = (unsigned long long)__double_as_longlong(d);

@@ -72,8 +72,13 @@ def make_problem(ctx_lens, Hi=16, Di=128, dtype="fp8", P=2048, K=512, H=64, W=12
             p.idx_k_raw.append(raw)
             dev_k[p.rows_of[b]] = raw
             continue
-        if kind == "ties":
+        if kind in ("ties", "wide"):
             base = rng.standard_normal((3, Di)).astype(np.float32) * scale_ch
+            if kind == "wide":
+                # (fp32 keys) products spanning more than 126 bits: channel 0
+                # large, channels 1-3 near the bottom of the fp32 normal range
+                base[:, 0] *= np.float32(2.0 ** 12)
+                base[:, 1:4] *= np.float32(2.0 ** -100)
             k = base[rng.integers(0, 3, n)]
         else:
             k = rng.standard_normal((n, Di)).astype(np.float32) * scale_ch

@@ -55,6 +55,23 @@ def test_full_fp32_keys():
     check_full(p, *run_full(p))
 
 
+@pytest.mark.parametrize("kind", ["ties", "wide"])
+def test_fp32_keys_exact_ties(kind):
+    """fp32 keys drawn from 3 rows, so that the bands hold whole tie groups and
+    most positions are re-scored exactly: random rows (head dots whose products
+    span 63-126 bits, the 128-bit accumulator) and rows whose products span more
+    than 126 bits (the multi-limb accumulator); Full, then Reindex on the pool."""
+    p = make_problem([3000, 517, 9], Hi=4, Di=64, dtype="fp32", P=64, K=128, H=16, seed=21,
+                     kind=kind, with_kv=False)
+    pool, plen, tk_full = run_full(p)
+    check_full(p, pool, plen, tk_full)
+    rng = np.random.default_rng(22)
+    q2 = rng.standard_normal(p.idx_q_f64.shape).astype(np.float32)
+    w2 = rng.random(p.w_raw.shape).astype(np.float32)
+    topk = run_reindex(p, pool, plen, torch.from_numpy(q2).cuda(), torch.from_numpy(w2).cuda())
+    check_reindex(p, pool, topk, q2.astype(np.float64), w2)
+
+
 @pytest.mark.parametrize("dtype", ["fp8", "fp32"])
 def test_reindex(dtype):
     kw = dict(Hi=4, Di=64, P=64, K=128) if dtype == "fp32" else {}
