@@ -131,6 +131,18 @@ def test_1m_workload():
     check_step(wl, sb, range(wl.batch), bound=True)
 
 
+def test_1m_fp4_keys_workload():
+    """The 1,048,576-position sequence with FP4 indexer keys (the library's FP4
+    key write, scan and selection), every layer; the FP4 scan's bound at every
+    position."""
+    wl = synth.workload("1m-fp4")
+    sb = workload.build(wl)
+    g = GraphedStep(sb)
+    g.replay()
+    torch.cuda.synchronize()
+    check_step(wl, sb, range(wl.batch), bound=True)
+
+
 def test_mix_workload_every_sequence():
     """All 64 serving-mix sequences (paged, N in [8K, 256K]), every layer."""
     wl = synth.workload("mix")
