@@ -40,10 +40,11 @@
 //     out as B; each tile's codes become 128-byte swizzled K-major E4M3 rows
 //     in one of 4 operand stages, followed by a copy of B;
 //   * warp 1 (one thread): 4 MMAs per tile (M = 128, N = 32, K = 32) into one
-//     of three tensor-memory accumulators;
-//   * warps 6-9 / 10-13 (epilogue, alternate tiles): the row's 8 key scales
-//     (read from global memory two tiles ahead), scores, bound, block maxima,
-//     writes.
+//     of four tensor-memory accumulators;
+//   * warps 6-9, 10-13, 14-17 (three epilogue groups, tiles in turn): the
+//     row's 8 key scales (read from global memory two of the group's tiles
+//     ahead), scores, bound, block maxima, writes.  The epilogue is the
+//     slowest role, so three groups work on three tiles at once.
 #include <cmath>
 
 #include "common.cuh"
@@ -59,27 +60,29 @@ namespace {
 
 constexpr int kConvWarps = 4;             // converter warps 2-5, four code rows per thread
 constexpr int kConvThreads = 32 * kConvWarps;
-constexpr int kEpiWarp0 = 2 + kConvWarps;  // epilogue groups: warps 6-9 (even tiles), 10-13 (odd)
+constexpr int kEpiWarp0 = 2 + kConvWarps;  // epilogue groups from warp 6, four warps each
+constexpr int kEpiGroups = 3;             // tile k goes to group k % 3
 constexpr int kEpiThreads = 128;          // threads of an epilogue group: one per row
-constexpr int kFThreads = 32 * (kEpiWarp0 + 8);
+constexpr int kFThreads = 32 * (kEpiWarp0 + 4 * kEpiGroups);
 constexpr int kCStages = 8;               // code ring depth
 constexpr int kCodeBytes = kTile * 64;    // 8 KB of FP4 codes per tile
 constexpr int kAStages = 4;               // operand stages
 constexpr int kAKeyBytes = kTile * 128;   // 16 KB of widened keys
 constexpr int kBBytes = 32 * 128;         // B: 32 rows of 128 channels
 constexpr int kAStride = kAKeyBytes + kBBytes;
-constexpr int kDBufs = 3;
+constexpr int kDBufs = kEpiGroups + 1;
 constexpr int kDCols = 128;               // accumulator columns per tile
+static_assert(kDBufs * kDCols <= 512, "accumulators fit in tensor memory");
 constexpr uint32_t kTmemCols = 512;
 
 struct FScanSmem {
   uint8_t astage[kAStages][kAStride];     // widened keys, then B; 1024-aligned
   uint8_t craw[kCStages][kCodeBytes];     // FP4 codes as loaded
   uint8_t qb[kBBytes];                    // the converter's current B
-  float sq[2][8][kMaxIdxHeads];           // [epilogue group][group g][head h]: query scale
-  float wv[2][kMaxIdxHeads];              // [epilogue group]: w_h (0 past the heads)
-  float ub[2][8];                         // [epilogue group]: bound factor per key group
-  float ucon[2][8][kMaxIdxHeads];         // [epilogue group]: |w_h| sq_hg sum|qhat|, rounded up
+  float sq[kEpiGroups][8][kMaxIdxHeads];  // [epilogue group][group g][head h]: query scale
+  float wv[kEpiGroups][kMaxIdxHeads];     // [epilogue group]: w_h (0 past the heads)
+  float ub[kEpiGroups][8];                // [epilogue group]: bound factor per key group
+  float ucon[kEpiGroups][8][kMaxIdxHeads];  // [epilogue group]: |w_h| sq_hg sum|qhat|, rounded up
   int64_t seq_items[kSeqCache];
   int32_t n_seq_cached;
   uint64_t cfull[kCStages], cempty[kCStages];
@@ -393,7 +396,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       if (lane == 0) arrive(&sm.afull[aring.stage]);
     }
   } else {
-    // ================= epilogue groups (warps 6-9: even tiles, 10-13: odd) ==========
+    // ================= epilogue groups (four warps each, tiles in turn) ==========
     const int eg = (wid - kEpiWarp0) >> 2;
     const int gt = tid - 32 * kEpiWarp0 - eg * kEpiThreads;
     const int quarter = wid & 3;                       // TMEM lanes 32*quarter ..
@@ -413,15 +416,15 @@ __global__ void __launch_bounds__(kFThreads, 1)
       ks = row >= 0 ? __ldg(reinterpret_cast<const uint2*>(a.idx_scales + row * 8)) : make_uint2(0, 0);
     };
     fetch(eg, tA, rA, kA);
-    fetch(eg + 2, tB, rB, kB);
-    for (int k = eg; k < ntiles; k += 2) {
+    fetch(eg + kEpiGroups, tB, rB, kB);
+    for (int k = eg; k < ntiles; k += kEpiGroups) {
       const TileRef tr = tA;
       const int64_t row = rA;
       const uint2 ks = kA;
       tA = tB;
       rA = rB;
       kA = kB;
-      fetch(k + 4, tB, rB, kB);
+      fetch(k + 2 * kEpiGroups, tB, rB, kB);
       if (tr.b != cur_b) {
         epi_query(a, sm, tr.b, gt, eg);
         cur_b = tr.b;
