@@ -355,8 +355,8 @@ TRAFFIC_UNITS = {
     ("indexer_scan_tc", "34b2a05f427c"): (134323456 + 3971328) / 1048576,
     # decode-128k Reindex capture (8 x 16,384 pool positions): 16,943,104 B read, 0 written
     ("reindex_score_tc", "34b2a05f427c"): 16943104 / 131072,
-    # decode-1m-fp4 capture (1,048,576 positions): 75,580,160 B read + 1,634,560 B written
-    ("indexer_scan_fp4", "982de1fdde57"): (75580160 + 1634560) / 1048576,
+    # decode-1m-fp4 capture (1,048,576 positions): 75,582,720 B read + 2,287,360 B written
+    ("indexer_scan_fp4", "07bb9e54dbfe"): (75582720 + 2287360) / 1048576,
     # decode-128k capture (8 sequence-layers): 3,930,368 B read, 0 written (outputs stay in L2)
     ("attn_cluster_tc", "2e496407fa56"): 3930368 / 8,
 }
