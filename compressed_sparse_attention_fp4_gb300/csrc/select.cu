@@ -431,8 +431,9 @@ __device__ inline ItemVal load_item(const IdxArgs& a, ItemKind kind, const SelCt
 // chain of dependent fp64 additions, one thread per position) while the
 // other threads stage round r's indexer-K rows in shared memory and compute
 // its products w_h * ReLU(d_h): one thread per (position, head) sums the Di
-// exact products serially in int64 (or, for a span too wide, in the
-// multi-limb accumulator) and rounds once.
+// exact products serially in int64, in a 128-bit integer when their span is
+// wider (the usual case for fp32 keys), or in the multi-limb accumulator
+// beyond 126 bits, and rounds once.
 __device__ void exact_scores(const IdxArgs& a, SelSmem& sm, const SelCtx& c, const int64_t* pos,
                              int np, double* out) {
   ExScratch& ex = ex_scratch(sm);
