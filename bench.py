@@ -277,7 +277,7 @@ def kernel_bytes(wl, name):
         return sum(idx_row * n for n in wl.ctx_lens)
     if name in ("reindex_score_tc", "reindex_score_fp4", "reindex_score_cuda_core"):
         return sum(idx_row * min(wl.pool_blocks * 8, n) + wl.pool_blocks * 4 for n in wl.ctx_lens)
-    if name in ("attn_cluster_tc", "attn_partial_tc"):
+    if name in ("attn_cluster_tc", "attn_seq_tc", "attn_partial_tc"):
         return wl.batch * attn_layer_bytes(wl)
     if name == "fp4_quantize":
         return wl.batch * (1024 + 288)
@@ -364,7 +364,8 @@ TRAFFIC_UNITS = {
 
 def traffic_of(wl, name):
     files = {"indexer_scan_tc": "scan.cu", "reindex_score_tc": "scan.cu", "indexer_scan_fp4": "scan_fp4.cu",
-             "reindex_score_fp4": "scan_fp4.cu", "attn_cluster_tc": "attention.cu", "attn_partial_tc": "attention.cu"}
+             "reindex_score_fp4": "scan_fp4.cu", "attn_cluster_tc": "attention.cu", "attn_seq_tc": "attention.cu",
+             "attn_partial_tc": "attention.cu"}
     if name not in files:
         return None
     per_unit = TRAFFIC_UNITS.get((name, src_hash(files[name])))

@@ -446,6 +446,7 @@ struct ClusterSmall {
   float fac[kCHeads];                                // 2^(m_chunk - M) / L per head
   __align__(16) float ml_mine[2][kCHeads];           // this chunk's (m, l), base-2 m
   __align__(16) float ml_all[kMaxClusterSplits][2][kCHeads];   // every chunk's (m, l)
+  int64_t rows[kCEntries];                           // cache row of each entry slot (cluster_gather)
 };
 
 size_t cluster_smem_bytes() { return 1024 + size_t(kKvBytes) + size_t(kCQBytes) + sizeof(ClusterSmall); }
@@ -513,67 +514,90 @@ __device__ inline float butterfly8(const float (&v)[8], int lane) {
   return op(u, __shfl_xor_sync(0xFFFFFFFFu, u, 1));
 }
 
-// Gathers this thread's share of the chunk's FP4 main-KV entries and writes
-// them, dequantized exactly to bf16, into the 128-byte swizzled KV tile:
-// entry e = tid % 128, channel regions 2 sub and 2 sub + 1 (sub = tid / 128:
-// latent channels 128 sub .. 128 sub + 127) and rope chunks 2 sub, 2 sub + 1.
-// Entry e of chunk c is Top-K slot m0 + e for e < nm, window row w0 + e - nm
-// for nm <= e < nm + nw, else empty.  Returns the entry's cache row (-1: no
-// main entry, its tile row zeroed; -2 - r: window row r, written later).
-__device__ inline int64_t cluster_gather(const AttnArgs& a, uint8_t* kv_s, int b, int m0, int nm, int w0, int nw,
-                                         int64_t n_ctx, int tid) {
-  const int e = tid & (kCEntries - 1), sub = tid >> 7;
-  const int K = a.d.topk;
-  int64_t row = -1;
-  if (e < nm) {
-    const int32_t t = __ldg(a.topk + int64_t(b) * K + m0 + e);
-    if (t >= 0 && t < n_ctx) {
-      row = kv_row(a.page_table, a.d, b, t, a.ws);
-      if (row < 0) row = -1;
-    } else if (sub == 0 && (t >= n_ctx || t < -1)) {
-      raise_err(a.ws, CSA2_DEV_TOPK_IDX);
+// Coalesced gather: a half-warp reads one entry's 256 code bytes (16 lanes x
+// 16 bytes), its 32 scale bytes (2 a lane) and its 128 rope bytes (lanes 0-7),
+// so that a warp instruction touches the lines of two entries rather than of
+// 32.  Thread piece k (0..3) is entry 2 (warp + 16 k) + lane / 16, codes
+// piece lane % 16 (latent channels 32 p .. 32 p + 31).
+struct GatherCo {
+  uint4 cd[4], rp[4];
+  uint32_t sc[4];
+  uint32_t skip;                                     // bit k: piece k is a window row (written with the window)
+};
+
+__device__ inline void gather_load_co(const AttnArgs& a, GatherCo& g, const int64_t* rows, int nm, int nw,
+                                          int wid, int lane) {
+  const int p = lane & 15;
+  g.skip = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e = 2 * (wid + 16 * k) + (lane >> 4);
+    const int64_t row = e < nm ? rows[e] : -1;
+    if (e >= nm && e < nm + nw) g.skip |= 1u << k;
+    g.cd[k] = make_uint4(0, 0, 0, 0);
+    g.rp[k] = make_uint4(0, 0, 0, 0);
+    g.sc[k] = 0;
+    if (row >= 0) {
+      g.cd[k] = __ldg(reinterpret_cast<const uint4*>(a.codes + row * kCodesPerRow) + p);
+      g.sc[k] = __ldg(reinterpret_cast<const uint16_t*>(a.scales + row * kScalesPerRow) + p);
+      if (p < 8) g.rp[k] = __ldg(reinterpret_cast<const uint4*>(a.rope + row * kRope) + p);
     }
-  } else if (e < nm + nw) {
-    return -2 - int64_t(w0 + e - nm);                // window row: written after the wait
   }
-  uint4 cd[4], rp[2];
-  uint32_t sc[2] = {0, 0};
+}
+
+__device__ inline void gather_store_co(uint8_t* kv_s, const GatherCo& g, int wid, int lane) {
+  const int p = lane & 15;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) cd[i] = make_uint4(0, 0, 0, 0);
-  rp[0] = rp[1] = make_uint4(0, 0, 0, 0);
-  if (row >= 0) {
-    // codes: 64 bytes (channels 128 sub ..); scales: 8 bytes; rope: 32 bytes
-    const uint4* cp = reinterpret_cast<const uint4*>(a.codes + row * kCodesPerRow) + 4 * sub;
+  for (int k = 0; k < 4; ++k) {
+    if ((g.skip >> k) & 1) continue;
+    const int e = 2 * (wid + 16 * k) + (lane >> 4);
+    const uint32_t cw[4] = {g.cd[k].x, g.cd[k].y, g.cd[k].z, g.cd[k].w};
+    uint8_t* region = kv_s + (p >> 1) * kRegion;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) cd[i] = __ldg(cp + i);
-    const uint16_t* sp = reinterpret_cast<const uint16_t*>(a.scales + row * kScalesPerRow) + 4 * sub;
-    sc[0] = uint32_t(__ldg(sp)) | (uint32_t(__ldg(sp + 1)) << 16);
-    sc[1] = uint32_t(__ldg(sp + 2)) | (uint32_t(__ldg(sp + 3)) << 16);
-    const uint4* rq = reinterpret_cast<const uint4*>(a.rope + row * kRope) + 2 * sub;
-    rp[0] = __ldg(rq);
-    rp[1] = __ldg(rq + 1);
-  }
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {                      // region 2 sub + r: channels 64 (2 sub + r) ..
-    const uint32_t cw[8] = {cd[2 * r].x, cd[2 * r].y, cd[2 * r].z, cd[2 * r].w,
-                            cd[2 * r + 1].x, cd[2 * r + 1].y, cd[2 * r + 1].z, cd[2 * r + 1].w};
-    uint8_t* region = kv_s + (2 * sub + r) * kRegion;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {                    // 16-byte chunk c: channels 8c .. 8c + 7
-      const float s = e4m3_to_f32((sc[r] >> (8 * (c >> 1))) & 0xFF);
+    for (int q = 0; q < 4; ++q) {                    // 16-byte chunk (p & 1) * 4 + q: 8 channels
+      const float sc = e4m3_to_f32((g.sc[k] >> (8 * (q >> 1))) & 0xFF);
       uint32_t w[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint32_t h2 = e2m1x2_to_f16x2_a((cw[c] >> (8 * i)) & 0xFF);
-        w[i] = pack_bf16x2(__half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF))) * s,
-                           __half2float(__ushort_as_half(uint16_t(h2 >> 16))) * s);
+        const uint32_t h2 = e2m1x2_to_f16x2_a((cw[q] >> (8 * i)) & 0xFF);
+        w[i] = pack_bf16x2(__half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF))) * sc,
+                           __half2float(__ushort_as_half(uint16_t(h2 >> 16))) * sc);
       }
-      st_shared_v4(region, tc::sw128_offset(e, c), make_uint4(w[0], w[1], w[2], w[3]));
+      st_shared_v4(region, tc::sw128_offset(e, (p & 1) * 4 + q), make_uint4(w[0], w[1], w[2], w[3]));
     }
+    if (p < 8) st_shared_v4(kv_s + 8 * kRegion, tc::sw128_offset(e, p), g.rp[k]);
   }
-  st_shared_v4(kv_s + 8 * kRegion, tc::sw128_offset(e, 2 * sub), rp[0]);
-  st_shared_v4(kv_s + 8 * kRegion, tc::sw128_offset(e, 2 * sub + 1), rp[1]);
-  return row;
+}
+
+// The chunk's FP4 main-KV entries, dequantized exactly to bf16 into the
+// 128-byte swizzled KV tile: threads 0..127 resolve entry tid's cache row into
+// rows_s (Top-K slot m0 + e for e < nm; -2 - r for window row r = w0 + e - nm,
+// written later; -1: no entry, its tile row zeroed), then every thread loads
+// and writes its four coalesced pieces.  Returns the row of entry tid % 128.
+__device__ inline int64_t cluster_gather(const AttnArgs& a, uint8_t* kv_s, int64_t* rows_s, int b, int m0, int nm,
+                                         int w0, int nw, int64_t n_ctx, int tid) {
+  const int K = a.d.topk;
+  if (tid < kCEntries) {
+    const int e = tid;
+    int64_t row = -1;
+    if (e < nm) {
+      const int32_t t = __ldg(a.topk + int64_t(b) * K + m0 + e);
+      if (t >= 0 && t < n_ctx) {
+        row = kv_row(a.page_table, a.d, b, t, a.ws);
+        if (row < 0) row = -1;
+      } else if (t >= n_ctx || t < -1) {
+        raise_err(a.ws, CSA2_DEV_TOPK_IDX);
+      }
+    } else if (e < nm + nw) {
+      row = -2 - int64_t(w0 + e - nm);
+    }
+    rows_s[e] = row;
+  }
+  __syncthreads();
+  GatherCo g;
+  gather_load_co(a, g, rows_s, nm, nw, tid >> 5, tid & 31);
+  gather_store_co(kv_s, g, tid >> 5, tid & 31);
+  return rows_s[tid & (kCEntries - 1)];
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_cluster_kernel(AttnArgs a, int early) {
@@ -626,7 +650,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_cluster_kernel(AttnArgs 
     }
     if (tid == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.swa_len + b));
   }
-  if (early) row = cluster_gather(a, kv_s, b, m0, nm, w0, nw, checked_ctx(a.ctx_len, a.d, b, paged, a.ws), tid);
+  if (early) row = cluster_gather(a, kv_s, sm.rows, b, m0, nm, w0, nw, checked_ctx(a.ctx_len, a.d, b, paged, a.ws), tid);
   pdl_wait();
   pdl_launch_dependents();
   // ---- after the wait: the window length, this head group's query (32 rows
@@ -651,7 +675,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_cluster_kernel(AttnArgs 
     const int i = tid + k * kAttnThreads;
     wv[k] = i < nwv ? __ldg(wsrc + i) : make_uint4(0, 0, 0, 0);
   }
-  if (!early) row = cluster_gather(a, kv_s, b, m0, nm, w0, nw, checked_ctx(a.ctx_len, a.d, b, paged, a.ws), tid);
+  if (!early) row = cluster_gather(a, kv_s, sm.rows, b, m0, nm, w0, nw, checked_ctx(a.ctx_len, a.d, b, paged, a.ws), tid);
   {
     // this chunk's share of the head group's output rows: zeros
     const int z0 = nh * chunk / S, z1 = nh * (chunk + 1) / S;
@@ -866,6 +890,373 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_cluster_kernel(AttnArgs 
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// ===========================================================================
+// One CTA per (sequence, query, 32-head group) walking all the chunks: for
+// large batches.  A cluster per head group puts S CTAs on S SMs for one
+// head group, so a batch of 64 sequences x 2 head groups x 5 chunks needs
+// about five rounds of the 28 clusters of 5 that fit at once; walking the
+// chunks inside one CTA runs the 128 head groups side by side in one round.
+// Per chunk: gather and dequantize the entries, S^T = KV . Q^T, softmax
+// against a per-head reference maximum, O^T += V^T . P^T in tensor memory.
+// The reference moves only when a chunk's maximum exceeds it by more than
+// 2^8 (P stays below 256, which bf16 hi + lo and fp32 carry exactly enough);
+// then the head's accumulated O and its sum are scaled by 2^(old - new)
+// through tensor-memory loads and stores.  The output rows are written once,
+// plainly (no zeroing, no reduce-adds).
+// ===========================================================================
+constexpr float kRescaleLog2 = 8.0f;
+
+struct SeqSmall {
+  uint64_t bar_s, bar_o;
+  uint32_t valid[kCEntries / 32];                    // bit e: entry slot e holds an entry
+  uint32_t tmem_slot;
+  __align__(16) float red_m[4][4][8];                // [head octet][lane quarter][head]
+  float red_l[4][4][8];
+  float mref[kCHeads];                               // reference maximum (base 2), -inf: none yet
+  float lsum[kCHeads];                               // sum of 2^(x - mref) over the entries so far
+  int64_t rows[kMaxClusterSplits * kCEntries];       // cache row of every chunk's Top-K slot (-1: none)
+};
+
+size_t seq_smem_bytes() {
+  return 1024 + size_t(kKvBytes) + size_t(kCQBytes) + size_t(2 * kCPRegion) + sizeof(SeqSmall);
+}
+
+// Cache rows of every chunk's Top-K slots (the checks of cluster_gather).
+__device__ inline void seq_resolve_rows(const AttnArgs& a, int64_t* rows, int b, int S, int64_t n_ctx, int tid) {
+  const int K = a.d.topk;
+  for (int i = tid; i < S * kCEntries; i += kAttnThreads) {
+    const int c = i / kCEntries, e = i % kCEntries;
+    const int m0 = attn_chunk_main_lo(K, c, S), nm = attn_chunk_main_lo(K, c + 1, S) - m0;
+    int64_t row = -1;
+    if (e < nm) {
+      const int32_t t = __ldg(a.topk + int64_t(b) * K + m0 + e);
+      if (t >= 0 && t < n_ctx) {
+        row = kv_row(a.page_table, a.d, b, t, a.ws);
+        if (row < 0) row = -1;
+      } else if (t >= n_ctx || t < -1) {
+        raise_err(a.ws, CSA2_DEV_TOPK_IDX);
+      }
+    }
+    rows[i] = row;
+  }
+}
+
+// The reference maximum after a chunk whose maximum is mc, and the factor
+// that rescales what was accumulated against the old one.
+__device__ inline void seq_reference(float mo, float mc, float& mn, float& alpha) {
+  mn = mo;
+  if (mc != -INFINITY && (mo == -INFINITY || mc > mo + kRescaleLog2)) mn = mc;
+  alpha = (mo == -INFINITY || mn == mo) ? 1.0f : exp2f(mo - mn);
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_seq_kernel(AttnArgs a, int early) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* kv_s = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);   // 9 x 16 KB
+  uint8_t* q_s = kv_s + kKvBytes;                    // 9 x 4 KB: the query, kept for every chunk
+  uint8_t* p_s = q_s + kCQBytes;                     // P^T hi / lo: two regions of 64 entries
+  SeqSmall& sm = *reinterpret_cast<SeqSmall*>(p_s + 2 * kCPRegion);
+
+  const int S = a.L.splits;
+  const int nhg = (a.d.heads + kCHeads - 1) / kCHeads;
+  const int qrow = blockIdx.x / nhg, hg = blockIdx.x % nhg;
+  const int b = qrow / a.q_len, qi = qrow % a.q_len;
+  const int H = a.d.heads, K = a.d.topk, W = a.d.swa;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const bool paged = a.page_table != nullptr;
+  const int h0 = hg * kCHeads, nh = min(kCHeads, H - h0);
+  if (wid == 0) tc::tmem_alloc(&sm.tmem_slot, kCTmemCols);
+  if (tid == 0) {
+    tc::mbar_init(&sm.bar_s, kSAcc);                 // one commit per S-issuing thread
+    tc::mbar_init(&sm.bar_o, 4);                     // one commit per O-issuing thread
+    tc::fence_mbar_init();
+  }
+  if (tid < kCHeads) {
+    sm.mref[tid] = -INFINITY;
+    sm.lsum[tid] = 0.0f;
+  }
+  {
+    // L2 prefetch (hints: nothing is read into the SM) of what is read after
+    // the wait: the query rows, the first chunk's window rows, the window length
+    const char* qb = reinterpret_cast<const char*>(a.q + (int64_t(qrow) * H + h0) * kDqk);
+    int w00, nw0;
+    attn_chunk_window(K, W, 0, S, w00, nw0);
+    const char* wb = reinterpret_cast<const char*>(a.swa + (int64_t(b) * W + w00) * kDqk);
+    const int qlines = (nh * kDqk * 2 + 127) / 128, wlines = (nw0 * kDqk * 2 + 127) / 128;
+    for (int i = tid; i < qlines + wlines; i += kAttnThreads) {
+      const char* pf = i < qlines ? qb + 128 * i : wb + 128 * (i - qlines);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(pf));
+    }
+    if (tid == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.swa_len + b));
+  }
+  const int64_t n_ctx = checked_ctx(a.ctx_len, a.d, b, paged, a.ws);
+  int m0 = attn_chunk_main_lo(K, 0, S), nm = attn_chunk_main_lo(K, 1, S) - m0, w0, nw;
+  attn_chunk_window(K, W, 0, S, w0, nw);
+  GatherCo g;
+  if (early) {                                       // Reuse: the indices and the first chunk before the wait
+    seq_resolve_rows(a, sm.rows, b, S, n_ctx, tid);
+    __syncthreads();
+    gather_load_co(a, g, sm.rows, nm, nw, wid, lane);
+    gather_store_co(kv_s, g, wid, lane);
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  int swl = __ldg(a.swa_len + b);
+  {
+    constexpr int kQVec = kCHeads * (kDqk / 8);
+    constexpr int kQPer = (kQVec + kAttnThreads - 1) / kAttnThreads;
+    const uint4* qsrc = reinterpret_cast<const uint4*>(a.q + (int64_t(qrow) * H + h0) * kDqk);
+    uint4 qv[kQPer];
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = tid + k * kAttnThreads;
+      qv[k] = (i < kQVec && i / (kDqk / 8) < nh) ? __ldg(qsrc + i) : make_uint4(0, 0, 0, 0);
+    }
+    if (!early) {
+      seq_resolve_rows(a, sm.rows, b, S, n_ctx, tid);
+      __syncthreads();
+      gather_load_co(a, g, sm.rows, nm, nw, wid, lane);
+      gather_store_co(kv_s, g, wid, lane);
+    }
+#pragma unroll
+    for (int k = 0; k < kQPer; ++k) {
+      const int i = tid + k * kAttnThreads;
+      if (i < kQVec) {
+        const int h = i / (kDqk / 8), j = i % (kDqk / 8);
+        st_shared_v4(q_s, (j >> 3) * kCQRegion + tc::sw128_offset(h, j & 7), qv[k]);
+      }
+    }
+  }
+  if (swl < 0 || swl > W) {
+    if (tid == 0 && hg == 0 && qi == 0) raise_err(a.ws, CSA2_DEV_SWA_LEN);
+    swl = swl < 0 ? 0 : W;
+  }
+  swl = max(0, swl - (a.q_len - 1 - qi));            // the later queries' rows are not visible
+  tc::tc_fence_before_sync();
+  __syncthreads();
+  tc::tc_fence_after_sync();
+  const uint32_t tmem = sm.tmem_slot;
+  const uint32_t kv_addr = tc::smem_u32(kv_s), q_addr = tc::smem_u32(q_s);
+  const int quarter = wid & 3, oct = wid >> 2;       // lanes 32 quarter.., heads 8 oct..
+  const int e = quarter * 32 + lane;
+  const float c2 = a.scale * 1.4426950408889634f;    // logits in base 2
+  bool ok = true;
+
+  // the chunk's window rows are entries nm .. nm + nw - 1 (zeros at or past
+  // swa_len); the first kWFirst 16-byte pieces a thread are loaded together
+  // with the chunk's entries, at the end of the previous chunk's softmax
+  constexpr int kWFirst = 4;
+  uint4 wv[kWFirst];
+  auto load_window_first = [&](int w0_, int nw_) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.swa + (int64_t(b) * W + w0_) * kDqk);
+#pragma unroll
+    for (int k = 0; k < kWFirst; ++k) {
+      const int i = tid + k * kAttnThreads;
+      wv[k] = (i < nw_ * (kDqk / 8) && w0_ + i / (kDqk / 8) < swl) ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  load_window_first(w0, nw);
+  for (int c = 0; c < S; ++c) {
+    const int nwv = nw * (kDqk / 8);
+    const uint4* wsrc = reinterpret_cast<const uint4*>(a.swa + (int64_t(b) * W + w0) * kDqk);
+    if (c > 0) {
+      // the previous chunk's O MMAs have read the tile and P^T
+      ok = tc::mbar_wait_bounded(&sm.bar_o, uint32_t((c - 1) & 1)) && ok;
+      tc::tc_fence_after_sync();
+      gather_store_co(kv_s, g, wid, lane);
+    }
+#pragma unroll
+    for (int k = 0; k < kWFirst; ++k) {
+      const int i = tid + k * kAttnThreads;
+      if (i < nwv) {
+        const int r = i / (kDqk / 8), j = i % (kDqk / 8);
+        st_shared_v4(kv_s, (j >> 3) * kRegion + tc::sw128_offset(nm + r, j & 7), wv[k]);
+      }
+    }
+    for (int base = kWFirst * kAttnThreads; base < nwv; base += kWFirst * kAttnThreads) {
+#pragma unroll
+      for (int k = 0; k < kWFirst; ++k) {
+        const int i = base + tid + k * kAttnThreads;
+        wv[k] = (i < nwv && w0 + i / (kDqk / 8) < swl) ? __ldg(wsrc + i) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < kWFirst; ++k) {
+        const int i = base + tid + k * kAttnThreads;
+        if (i < nwv) {
+          const int r = i / (kDqk / 8), j = i % (kDqk / 8);
+          st_shared_v4(kv_s, (j >> 3) * kRegion + tc::sw128_offset(nm + r, j & 7), wv[k]);
+        }
+      }
+    }
+    {
+      const int64_t* rows_c = sm.rows + c * kCEntries;
+      const int ee = tid & (kCEntries - 1);
+      const bool has = ee < nm ? rows_c[ee] >= 0 : (ee < nm + nw && w0 + ee - nm < swl);
+      const uint32_t m = __ballot_sync(0xFFFFFFFFu, has);
+      if (tid < kCEntries && lane == 0) sm.valid[tid >> 5] = m;
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before_sync();
+    __syncthreads();
+    tc::tc_fence_after_sync();
+
+    // ---- S^T = KV . Q^T: 4 accumulators, 9 K steps spread over them ----------------------
+    if (wid < kSAcc && lane == 0) {
+      constexpr uint32_t idS = tc::idesc_bf16(kCEntries, kCHeads, 0, 0);
+      const uint64_t ad0 = tc::smem_desc(kv_addr, 16, 1024, 2), bd0 = tc::smem_desc(q_addr, 16, 1024, 2);
+      const int k4 = wid;
+#pragma unroll
+      for (int kb = 0; kb < 9; ++kb) {
+        const uint32_t off = uint32_t(kb * kRegion + k4 * 32), qoff = uint32_t(kb * kCQRegion + k4 * 32);
+        tc::mma_bf16(tmem + uint32_t(k4 * kCHeads), ad0 + (off >> 4), bd0 + (qoff >> 4), idS, kb > 0);
+      }
+      tc::mma_commit(&sm.bar_s);
+    }
+    __syncwarp();
+    ok = tc::mbar_wait_bounded(&sm.bar_s, uint32_t(c & 1)) && ok;
+    tc::tc_fence_after_sync();
+
+    // ---- softmax against the reference maximum: 16 warps, 8 heads each -----------------
+    float alpha[8];
+    {
+      float x[8];
+      {
+        const uint32_t ta = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(oct * 8);
+        float x1[8], x2[8], x3[8];
+        tc::tmem_ld8(ta, x);
+        tc::tmem_ld8(ta + kCHeads, x1);
+        tc::tmem_ld8(ta + 2 * kCHeads, x2);
+        tc::tmem_ld8(ta + 3 * kCHeads, x3);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = (x[j] + x1[j]) + (x2[j] + x3[j]);
+      }
+      const bool v_e = (sm.valid[e >> 5] >> (e & 31)) & 1;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = v_e ? x[j] * c2 : -INFINITY;
+      {
+        float mx[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(mx[j]) : "f"(x[j]));
+        if (lane == 0) {
+          float4* dst = reinterpret_cast<float4*>(&sm.red_m[oct][quarter][0]);
+          dst[0] = make_float4(mx[0], mx[1], mx[2], mx[3]);
+          dst[1] = make_float4(mx[4], mx[5], mx[6], mx[7]);
+        }
+      }
+      __syncthreads();
+      float p[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float mc = fmaxf(fmaxf(sm.red_m[oct][0][j], sm.red_m[oct][1][j]),
+                               fmaxf(sm.red_m[oct][2][j], sm.red_m[oct][3][j]));
+        float mn;
+        seq_reference(sm.mref[oct * 8 + j], mc, mn, alpha[j]);
+        p[j] = (mn == -INFINITY || x[j] == -INFINITY) ? 0.0f : exp2f(x[j] - mn);
+      }
+      const float l = butterfly8<false>(p, lane);
+      if ((lane & 3) == 0) sm.red_l[oct][quarter][octet_index(lane)] = l;
+      uint8_t* reg = p_s + (e >> 6) * kCPRegion;
+      const uint32_t ch = uint32_t((e >> 3) & 7), el = uint32_t(e & 7) * 2;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int h = oct * 8 + j;
+        const uint32_t hb = pack_bf16x2(p[j], 0.0f);
+        const float hv = __uint_as_float(hb << 16);
+        *reinterpret_cast<uint16_t*>(reg + tc::sw128_offset(uint32_t(h), ch) + el) = uint16_t(hb & 0xFFFF);
+        *reinterpret_cast<uint16_t*>(reg + tc::sw128_offset(uint32_t(kCHeads + h), ch) + el) =
+            uint16_t(pack_bf16x2(p[j] - hv, 0.0f) & 0xFFFF);
+      }
+    }
+    // ---- the heads whose reference moved: scale their accumulated O (the
+    //      factors are the same in every lane of the warp) -----------------------------
+    bool moved = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) moved = moved || alpha[j] != 1.0f;
+    if (c > 0 && moved) {
+#pragma unroll 1
+      for (int mt = 0; mt < 4; ++mt) {
+        const uint32_t ta = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(kCOCol + 64 * mt + oct * 8);
+        float hi[8], lo[8];
+        tc::tmem_ld8(ta, hi);
+        tc::tmem_ld8(ta + kCHeads, lo);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          hi[j] *= alpha[j];
+          lo[j] *= alpha[j];
+        }
+        tc::tmem_st8(ta, hi);
+        tc::tmem_st8(ta + kCHeads, lo);
+      }
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before_sync();
+    __syncthreads();
+    tc::tc_fence_after_sync();
+    // the heads' running state (every thread has read the old reference), by
+    // warp 1, while warps 0 and 2-4 issue the O MMAs
+    if (wid == 1) {
+      const int o8 = lane >> 3, j = lane & 7;
+      const float mc = fmaxf(fmaxf(sm.red_m[o8][0][j], sm.red_m[o8][1][j]),
+                             fmaxf(sm.red_m[o8][2][j], sm.red_m[o8][3][j]));
+      float mn, al;
+      seq_reference(sm.mref[lane], mc, mn, al);
+      const float lc = (sm.red_l[o8][0][j] + sm.red_l[o8][1][j]) + (sm.red_l[o8][2][j] + sm.red_l[o8][3][j]);
+      sm.lsum[lane] = sm.lsum[lane] * al + lc;
+      sm.mref[lane] = mn;
+    }
+    // ---- O^T += V^T . [P_hi | P_lo]^T (4 M-tiles of 128 dims, N = 64, K = 128) ------------
+    if ((wid == 0 || (wid >= 2 && wid <= 4)) && lane == 0) {
+      constexpr uint32_t idO = tc::idesc_bf16(kCEntries, 2 * kCHeads, 1, 0);
+      const uint64_t bp0 = tc::smem_desc(tc::smem_u32(p_s), 16, 1024, 2);
+      const uint64_t av0 = tc::smem_desc(kv_addr, kRegion, 1024, 2);
+      const int mt = wid == 0 ? 0 : wid - 1;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        tc::mma_bf16(tmem + kCOCol + 64 * mt, av0 + (((2 * mt) * kRegion + ks * 2048) >> 4),
+                     bp0 + (((ks >> 2) * kCPRegion + (ks & 3) * 32) >> 4), idO, c > 0 || ks > 0);
+      tc::mma_commit(&sm.bar_o);
+    }
+    __syncwarp();
+    if (c + 1 < S) {                                 // the next chunk's entries and window: loads in flight
+      m0 = attn_chunk_main_lo(K, c + 1, S);
+      nm = attn_chunk_main_lo(K, c + 2, S) - m0;
+      attn_chunk_window(K, W, c + 1, S, w0, nw);
+      load_window_first(w0, nw);
+      gather_load_co(a, g, sm.rows + (c + 1) * kCEntries, nm, nw, wid, lane);
+    }
+  }
+  ok = tc::mbar_wait_bounded(&sm.bar_o, uint32_t((S - 1) & 1)) && ok;
+  tc::tc_fence_after_sync();
+  __syncthreads();
+  if (!ok && tid == 0) raise_err(a.ws, CSA2_DEV_TIMEOUT);
+  // ---- out = O / sum, lse = ref ln 2 + ln(sum): a warp's 32 lanes write 32
+  //      consecutive dims of one head ----------------------------------------------------
+  float* dst0 = a.out + (int64_t(qrow) * H + h0) * kLatent + quarter * 32 + lane;
+#pragma unroll 1
+  for (int mt = 0; mt < 4; ++mt) {
+    float hi[8], lo[8];
+    const uint32_t ta = tmem + (uint32_t(quarter * 32) << 16) + uint32_t(kCOCol + 64 * mt + oct * 8);
+    tc::tmem_ld8(ta, hi);
+    tc::tmem_ld8(ta + kCHeads, lo);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int hh = oct * 8 + j;
+      if (hh < nh) {
+        const float L = sm.lsum[hh];
+        dst0[int64_t(hh) * kLatent + mt * 128] = L > 0.0f ? (hi[j] + lo[j]) / L : 0.0f;
+      }
+    }
+  }
+  if (tid < nh) {
+    const float L = sm.lsum[tid];
+    a.lse[int64_t(qrow) * H + h0 + tid] = L > 0.0f ? sm.mref[tid] * 0.6931471805599453f + logf(L) : -INFINITY;
+  }
+  tc::tc_fence_before_sync();
+  __syncthreads();
+  tc::tc_fence_after_sync();
+  if (wid == 0) tc::tmem_dealloc(tmem, kCTmemCols);
+}
+
+
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
   const int h = blockIdx.x, b = blockIdx.y, H = a.d.heads, S = a.L.splits;
   pdl_wait();
@@ -916,16 +1307,67 @@ static bool encode_rows_map(CUtensorMap* map, const void* base, uint64_t rows, u
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
+// Clusters of `chunks` attention CTAs that fit on the device at once (read
+// once per device and cluster size).
+static int cluster_capacity(int chunks, size_t smem) {
+  static std::atomic<int> cap[kMaxDevices][kMaxClusterSplits + 1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  int n = cap[dev][chunks].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = unsigned(chunks);
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.gridDim = dim3(unsigned(chunks), 1, 1);
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (cudaOccupancyMaxActiveClusters(&n, attn_cluster_kernel, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = max(1, device_sms() / chunks);               // no answer: as if every SM took a CTA
+  }
+  cap[dev][chunks].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// Whether the chunk-walking kernel finishes before the clusters: rounds of
+// clusters (about 13 us each: gather, S, softmax, merge) against rounds of
+// one CTA per head group that sets up in about 6 us and walks `chunks`
+// chunks at about 7.5 us each -- figures measured on this GPU (128K,
+// 4-query and serving-mix workloads; tenths of a microsecond below).
+static bool attention_walks_chunks(int items, int chunks, size_t cluster_smem) {
+  const int cap = cluster_capacity(chunks, cluster_smem);
+  const int64_t cluster_rounds = (items + cap - 1) / cap;
+  const int64_t seq_rounds = (items + device_sms() - 1) / device_sms();
+  return seq_rounds * (60 + 75 * int64_t(chunks)) < cluster_rounds * 130;
+}
+
 cudaError_t launch_attention(AttnArgs a, cudaStream_t st) {
   const int H = a.d.heads, K = a.d.topk, W = a.d.swa;
   if (!attn_uses_partials(a.d)) {
-    // one cluster of 128-entry chunks per (sequence, group of 32 heads)
+    // one cluster of 128-entry chunks per (sequence, group of 32 heads), or,
+    // for many head groups, one CTA per head group walking the chunks
     const int chunks = a.L.splits;
     const int nhg = (H + kCHeads - 1) / kCHeads;
     const size_t smem = cluster_smem_bytes();
     static KernelAttrs done;
     cudaError_t e = prepare_kernel(attn_cluster_kernel, smem, false, done);
     if (e != cudaSuccess) return e;
+    const int items = nhg * a.batch * a.q_len;
+    if (attention_walks_chunks(items, chunks, smem)) {
+      const size_t sm2 = seq_smem_bytes();
+      static KernelAttrs done_seq;
+      e = prepare_kernel(attn_seq_kernel, sm2, false, done_seq);
+      if (e != cudaSuccess) return e;
+      CSA2_PROFILED(st, "attn_seq_tc",
+                    (e = launch_pdl(attn_seq_kernel, dim3(unsigned(items)), dim3(kAttnThreads), sm2, st, 1, a,
+                                    a.early)));
+      return e;
+    }
     CSA2_PROFILED(st, "attn_cluster_tc",
                   (e = launch_pdl(attn_cluster_kernel, dim3(unsigned(chunks), unsigned(nhg * a.batch * a.q_len), 1),
                                   dim3(kAttnThreads), smem, st, unsigned(chunks), a, a.early)));
