@@ -259,9 +259,11 @@ csa2_status indexer_reindex_topk_ex(const csa2_dims* d, int32_t batch, int32_t f
  *   entries, the SWA row (576) / its first 512 channels for SWA entries;
  *   logit = scale * q[b][h] . key(e);  out = softmax-weighted sum of values;
  *   lse = max logit + ln(sum exp(logit - max)); empty E: out 0, lse -inf.
- *   out is the sum of the parts of up to 8 chunks of 128 entries, added in
- *   the order the chunks finish: repeated calls can differ in the last bits
- *   of out (lse does not).
+ *   out is the sum of the parts of up to 8 chunks of 128 entries: for few
+ *   (sequence, 32-head group) pairs each chunk runs on its own SM and the
+ *   parts are added in the order the chunks finish, so repeated calls can
+ *   differ in the last bits of out (lse does not); for many pairs one CTA
+ *   accumulates the chunks in order and out is reproducible.
  *   mode: csa2_mode.  Indices are always supplied.  CSA2_MODE_REUSE (the
  *     layer keeps the KV and indices an earlier layer used) lets the call
  *     start reading topk, ctx_len, page_table and the main-KV planes
@@ -324,8 +326,8 @@ csa2_status csa2_sparse_attn_decode_mq(const csa2_dims* d, int32_t batch, int32_
  * CSA2_NOALLOC_SCRATCH_BYTES inside the library, held on every GPU that
  * loads the library until the process exits.
  *   Limit: with S = ceil((topk + swa) / 128) chunks of entries, up to 8
- *   chunks are merged inside one thread-block cluster and need only the
- *   256-byte error word (any batch).  Above 8 chunks the per-chunk partial
+ *   chunks are merged inside one thread-block cluster (or accumulated by one
+ *   CTA) and need only the 256-byte error word (any batch).  Above 8 chunks the per-chunk partial
  *   outputs live in the array: 256 + B*S*H*2048 + B*S*H*8 bytes (each part
  *   rounded up to 256) must fit it -- up to batch 5 at Top-2048, SWA-128,
  *   64 heads; larger shapes return CSA2_ERR_WORKSPACE_TOO_SMALL and launch
