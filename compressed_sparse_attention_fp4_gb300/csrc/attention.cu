@@ -514,56 +514,65 @@ __device__ inline float butterfly8(const float (&v)[8], int lane) {
   return op(u, __shfl_xor_sync(0xFFFFFFFFu, u, 1));
 }
 
-// Coalesced gather: a half-warp reads one entry's 256 code bytes (16 lanes x
-// 16 bytes), its 32 scale bytes (2 a lane) and its 128 rope bytes (lanes 0-7),
-// so that a warp instruction touches the lines of two entries rather than of
-// 32.  Thread piece k (0..3) is entry 2 (warp + 16 k) + lane / 16, codes
-// piece lane % 16 (latent channels 32 p .. 32 p + 31).
+// Coalesced gather: a half-warp reads one entry (its 256 code bytes, 32 scale
+// bytes and 128 rope bytes), so that a warp instruction touches the lines of
+// two entries rather than of 32.  Lane p (0..15) of the half-warp owns the
+// 16-byte chunk c = p % 8 (8 channels) of the latent regions p / 8 + 2 j
+// (j = 0..3): each of its four stores is then one of 8 chunk positions of
+// the swizzled rows across the half-warp (no bank conflicts), and each load
+// instruction reads 64 contiguous code bytes of the entry.  Thread piece k
+// (0..3) is entry 2 (warp + 16 k) + lane / 16.
 struct GatherCo {
-  uint4 cd[4], rp[4];
-  uint32_t sc[4];
+  uint32_t cw[4][4];                                 // [entry piece][region j]: 8 FP4 codes
+  uint32_t sb[4];                                    // [entry piece]: byte j = the scale of region j's chunk
+  uint4 rp[4];                                       // rope chunk p (lanes p < 8)
   uint32_t skip;                                     // bit k: piece k is a window row (written with the window)
 };
 
 __device__ inline void gather_load_co(const AttnArgs& a, GatherCo& g, const int64_t* rows, int nm, int nw,
-                                          int wid, int lane) {
-  const int p = lane & 15;
+                                      int wid, int lane) {
+  const int p = lane & 15, c = p & 7, r0 = p >> 3;
   g.skip = 0;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int e = 2 * (wid + 16 * k) + (lane >> 4);
     const int64_t row = e < nm ? rows[e] : -1;
     if (e >= nm && e < nm + nw) g.skip |= 1u << k;
-    g.cd[k] = make_uint4(0, 0, 0, 0);
+    g.sb[k] = 0;
     g.rp[k] = make_uint4(0, 0, 0, 0);
-    g.sc[k] = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) g.cw[k][j] = 0;
     if (row >= 0) {
-      g.cd[k] = __ldg(reinterpret_cast<const uint4*>(a.codes + row * kCodesPerRow) + p);
-      g.sc[k] = __ldg(reinterpret_cast<const uint16_t*>(a.scales + row * kScalesPerRow) + p);
+      const uint8_t* cp = a.codes + row * kCodesPerRow;
+      const uint8_t* sp = a.scales + row * kScalesPerRow;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = r0 + 2 * j;                    // region: latent channels 64 r .. 64 r + 63
+        g.cw[k][j] = __ldg(reinterpret_cast<const uint32_t*>(cp + 32 * r + 4 * c));
+        g.sb[k] |= uint32_t(__ldg(sp + 4 * r + (c >> 1))) << (8 * j);
+      }
       if (p < 8) g.rp[k] = __ldg(reinterpret_cast<const uint4*>(a.rope + row * kRope) + p);
     }
   }
 }
 
 __device__ inline void gather_store_co(uint8_t* kv_s, const GatherCo& g, int wid, int lane) {
-  const int p = lane & 15;
+  const int p = lane & 15, c = p & 7, r0 = p >> 3;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     if ((g.skip >> k) & 1) continue;
     const int e = 2 * (wid + 16 * k) + (lane >> 4);
-    const uint32_t cw[4] = {g.cd[k].x, g.cd[k].y, g.cd[k].z, g.cd[k].w};
-    uint8_t* region = kv_s + (p >> 1) * kRegion;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {                    // 16-byte chunk (p & 1) * 4 + q: 8 channels
-      const float sc = e4m3_to_f32((g.sc[k] >> (8 * (q >> 1))) & 0xFF);
+    for (int j = 0; j < 4; ++j) {
+      const float sc = e4m3_to_f32((g.sb[k] >> (8 * j)) & 0xFF);
       uint32_t w[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint32_t h2 = e2m1x2_to_f16x2_a((cw[q] >> (8 * i)) & 0xFF);
+        const uint32_t h2 = e2m1x2_to_f16x2_a((g.cw[k][j] >> (8 * i)) & 0xFF);
         w[i] = pack_bf16x2(__half2float(__ushort_as_half(uint16_t(h2 & 0xFFFF))) * sc,
                            __half2float(__ushort_as_half(uint16_t(h2 >> 16))) * sc);
       }
-      st_shared_v4(region, tc::sw128_offset(e, (p & 1) * 4 + q), make_uint4(w[0], w[1], w[2], w[3]));
+      st_shared_v4(kv_s + (r0 + 2 * j) * kRegion, tc::sw128_offset(e, c), make_uint4(w[0], w[1], w[2], w[3]));
     }
     if (p < 8) st_shared_v4(kv_s + 8 * kRegion, tc::sw128_offset(e, p), g.rp[k]);
   }
