@@ -357,8 +357,8 @@ TRAFFIC_UNITS = {
     ("reindex_score_tc", "34b2a05f427c"): 16943104 / 131072,
     # decode-1m-fp4 capture (1,048,576 positions): 75,582,720 B read + 2,287,360 B written
     ("indexer_scan_fp4", "07bb9e54dbfe"): (75582720 + 2287360) / 1048576,
-    # decode-128k capture (8 sequence-layers): 3,955,712 B read, 0 written (outputs stay in L2)
-    ("attn_cluster_tc", "4029153bc9b2"): 3955712 / 8,
+    # decode-128k capture (8 sequence-layers): 3,957,504 B read, 0 written (outputs stay in L2)
+    ("attn_cluster_tc", "764442a6e89c"): 3957504 / 8,
 }
 
 
