@@ -111,3 +111,25 @@ def test_multi_query_limits():
         csa2.csa2_sparse_attn_decode_mq(big.dims, 1, 2, csa2.MODE_FULL, q, big.codes, big.scales, big.rope, None,
                                         big.ctx, tkb, big.swa, big.swa_len, SCALE, out, lse, big.ws)
     assert e.value.code == 2
+
+
+@pytest.mark.parametrize("mode", [csa2.MODE_REUSE, csa2.MODE_FULL])
+def test_multi_query_large_batch_walks_chunks(mode):
+    """32 sequences x 4 queries x 2 head groups (256 head groups): the library
+    takes the chunk-walking kernel, each query with its own window limit."""
+    rng = np.random.default_rng(41)
+    lens = rng.integers(300, 3000, 32).tolist()
+    lens[0] = 40                         # fewer positions than Top-K
+    p = make_problem(lens, seed=41)
+    tk = random_topk(p, rng)
+    sl = rng.integers(0, 129, p.B).astype(np.int32)
+    sl[:3] = [0, 2, 128]                 # no window; shorter than the draft block; full
+    q_raw, q_dev = mq_queries(p, 4, 141)
+    csa2.profile_enable(True)
+    try:
+        out, lse = run_mq(p, 4, q_dev, tk, sl, mode)
+        rec = csa2.profile_read()
+    finally:
+        csa2.profile_enable(False)
+    assert rec.get("attn_seq_tc", (0, 0.0))[0] == 1, rec
+    check_mq(p, 4, q_raw, tk, out, lse, sl)
