@@ -105,6 +105,38 @@ def test_no_alloc_matches_workspace_call_and_oracle_twice(K, paged):
     assert int(err.item()) == 0
 
 
+def test_no_alloc_large_batch_walks_chunks():
+    """64 sequences x 2 head groups: the allocation-free call takes the
+    chunk-walking kernel (no scratch but the error word) and allocates
+    nothing; results as the workspace call's and the oracle's."""
+    rng = np.random.default_rng(37)
+    p = make_problem(rng.integers(200, 2500, 64).tolist(), seed=37)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tk = _topk(p, rng)
+    tk_dev = torch.from_numpy(tk).cuda()
+    out = torch.full((p.B, p.H, 512), float("nan"), device="cuda")
+    lse = torch.full((p.B, p.H), float("nan"), device="cuda")
+    csa2.profile_enable(True)
+    try:
+        _no_alloc(p, tk_dev, p.q, err, out, lse)
+        rec = csa2.profile_read()
+    finally:
+        csa2.profile_enable(False)
+    assert rec.get("attn_seq_tc", (0, 0.0))[0] == 1, rec
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    reserved0 = torch.cuda.memory_reserved()
+    out.fill_(float("nan"))
+    _no_alloc(p, tk_dev, p.q, err, out, lse)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0 and torch.cuda.memory_reserved() == reserved0
+    got = (out.cpu().numpy(), lse.cpu().numpy())
+    _close(got, tuple(t.cpu().numpy() for t in _with_workspace(p, tk, p.q)))
+    _close(got, _oracle(p, tk, p.q_raw))
+    assert int(err.item()) == 0
+
+
 def test_no_alloc_reports_device_errors_and_limit():
     p = make_problem([100], seed=32)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
